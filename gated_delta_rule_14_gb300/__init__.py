@@ -1,0 +1,157 @@
+"""KLA gated delta-rule recurrence on NVIDIA GB300 (sm_103a): thin Python binding.
+
+The recurrence (Gist.science, "Riepilogo Tecnico: Attenzione Lineare Kaczmarz (KLA)"):
+for each sequence and head, a d_k x d_v state S is carried over tokens with
+``S~ = alpha (.) S``, ``e = v - S~^T k``, ``beta = eta / (||k||^2 + eps)``,
+``S = S~ + beta k e^T`` and the read ``o = S^T q`` after the write. ``alpha`` is a
+scalar per token and head, or one value per key channel.
+
+``chunk_fwd`` runs the chunkwise prefill and ``decode_step`` one fused
+single-token step. Both call the C ABI of ``include/kla.h`` through ctypes; torch
+only supplies device memory and the current CUDA stream. Every step of the
+computation runs in this package's CUDA kernels; if the library is missing the
+calls raise.
+"""
+from __future__ import annotations
+
+from typing import Optional, Tuple
+
+import torch
+
+from . import _native
+from ._native import KlaError  # noqa: F401
+
+__all__ = ["chunk_fwd", "decode_step", "workspace_size", "device_status", "KlaError"]
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return _native.KLA_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return _native.KLA_DTYPE_F32
+    raise TypeError(f"q/k/v must be bfloat16 or float32, got {t.dtype}")
+
+
+def _check_dev(name: str, t: torch.Tensor, dtype=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream_ptr(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def workspace_size(B: int, T: int, H: int, d_k: int, d_v: int, chunk: int = 64,
+                   dtype: torch.dtype = torch.bfloat16, per_channel_gate: bool = False) -> int:
+    """Device scratch bytes ``chunk_fwd`` needs for these sizes (0 when none)."""
+    code = _native.KLA_DTYPE_BF16 if dtype == torch.bfloat16 else _native.KLA_DTYPE_F32
+    gate = _native.KLA_GATE_CHANNEL if per_channel_gate else _native.KLA_GATE_SCALAR
+    return int(_native.lib().kla_chunk_fwd_workspace_size(B, T, H, d_k, d_v, chunk, code, gate))
+
+
+def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, alpha: torch.Tensor, eta: torch.Tensor,
+              eps: float = 1e-6, S0: Optional[torch.Tensor] = None, *, chunk: int = 64,
+              out: Optional[torch.Tensor] = None, final_state: bool = True,
+              S_T: Optional[torch.Tensor] = None,
+              workspace: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Chunkwise KLA prefill.
+
+    q, k: [B,T,H,d_k]; v: [B,T,H,d_v] (bf16 or fp32, same dtype); alpha: fp32 [B,T,H]
+    (scalar gate) or [B,T,H,d_k] (per-key-channel gate); eta: fp32 [B,T,H];
+    S0: fp32 [B,H,d_k,d_v] or None (zeros). Returns (o [B,T,H,d_v] in q's dtype,
+    S_T fp32 [B,H,d_k,d_v] or None). ``S_T`` may be passed (it may be ``S0`` itself).
+    """
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _check_dev(n, t)
+    dcode = _dtype_code(q)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    if q.dim() != 4:
+        raise ValueError("q must be [B, T, H, d_k]")
+    B, T, H, d_k = q.shape
+    d_v = v.shape[-1]
+    if k.shape != q.shape or v.shape[:3] != q.shape[:3]:
+        raise ValueError("q, k, v shapes disagree")
+    _check_dev("alpha", alpha, torch.float32)
+    _check_dev("eta", eta, torch.float32)
+    if tuple(alpha.shape) == (B, T, H):
+        gate = _native.KLA_GATE_SCALAR
+    elif tuple(alpha.shape) == (B, T, H, d_k):
+        gate = _native.KLA_GATE_CHANNEL
+    else:
+        raise ValueError(f"alpha must be [B,T,H] or [B,T,H,d_k], got {tuple(alpha.shape)}")
+    if tuple(eta.shape) != (B, T, H):
+        raise ValueError("eta must be [B, T, H]")
+    if S0 is not None:
+        _check_dev("S0", S0, torch.float32)
+        if tuple(S0.shape) != (B, H, d_k, d_v):
+            raise ValueError("S0 must be [B, H, d_k, d_v]")
+    if out is None:
+        out = torch.empty((B, T, H, d_v), dtype=q.dtype, device=q.device)
+    else:
+        _check_dev("out", out, q.dtype)
+    if S_T is None and final_state:
+        S_T = torch.empty((B, H, d_k, d_v), dtype=torch.float32, device=q.device)
+    elif S_T is not None:
+        _check_dev("S_T", S_T, torch.float32)
+    ws_need = _native.lib().kla_chunk_fwd_workspace_size(B, T, H, d_k, d_v, chunk, dcode, gate)
+    if ws_need and workspace is None:
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = _native.lib().kla_chunk_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(eta), float(eps), _ptr(S0), _ptr(out), _ptr(S_T),
+        B, T, H, d_k, d_v, int(chunk), dcode, gate, _ptr(workspace), ws_bytes, _stream_ptr(q.device))
+    _native.check(st, "kla_chunk_fwd")
+    return out, S_T
+
+
+def decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, alpha: torch.Tensor, eta: torch.Tensor,
+                S: torch.Tensor, eps: float = 1e-6, *, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """One fused KLA token step for B sequences; ``S`` (fp32 [B,H,d_k,d_v]) is updated in place.
+
+    q, k: [B,H,d_k]; v: [B,H,d_v]; alpha: fp32 [B,H] or [B,H,d_k]; eta: fp32 [B,H].
+    Returns o [B,H,d_v] in q's dtype.
+    """
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _check_dev(n, t)
+    dcode = _dtype_code(q)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    B, H, d_k = q.shape
+    d_v = v.shape[-1]
+    _check_dev("alpha", alpha, torch.float32)
+    _check_dev("eta", eta, torch.float32)
+    _check_dev("S", S, torch.float32)
+    if tuple(alpha.shape) == (B, H):
+        gate = _native.KLA_GATE_SCALAR
+    elif tuple(alpha.shape) == (B, H, d_k):
+        gate = _native.KLA_GATE_CHANNEL
+    else:
+        raise ValueError("alpha must be [B,H] or [B,H,d_k]")
+    if tuple(S.shape) != (B, H, d_k, d_v) or tuple(eta.shape) != (B, H) or tuple(k.shape) != (B, H, d_k):
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty((B, H, d_v), dtype=q.dtype, device=q.device)
+    else:
+        _check_dev("out", out, q.dtype)
+    st = _native.lib().kla_decode_step(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(eta), float(eps), _ptr(S), _ptr(out),
+        B, H, d_k, d_v, dcode, gate, _stream_ptr(q.device))
+    _native.check(st, "kla_decode_step")
+    return out
+
+
+def device_status(device=None) -> None:
+    """Synchronise the current stream and raise if a bounded device wait or range check fired."""
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    _native.check(_native.lib().kla_device_status(_stream_ptr(dev)), "kla_device_status")

@@ -1,0 +1,168 @@
+// kla_api.cu -- the C ABI declared in include/kla.h: host-side validation, dispatch to
+// the CUDA kernels, and the device error word.
+#include <mutex>
+
+#include "kla_internal.cuh"
+
+namespace {
+
+// One error word per device; bounded device waits and range checks OR bits into it.
+__device__ unsigned g_err_word;
+
+constexpr int kMaxDevices = 64;
+unsigned *g_err_ptr[kMaxDevices] = {};
+std::mutex g_err_mutex;
+
+// Device address of g_err_word on the current device (looked up once per device).
+cudaError_t err_word(unsigned **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_err_mutex);
+    if (!g_err_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_err_word);
+        if (e != cudaSuccess) return e;
+        g_err_ptr[dev] = static_cast<unsigned *>(p);
+    }
+    *out = g_err_ptr[dev];
+    return cudaSuccess;
+}
+
+bool aligned(const void *p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; }
+bool aligned16(const void *p) { return aligned(p, 16); }
+bool supported_d(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+bool supported_chunk(int c) { return c == 16 || c == 32 || c == 64; }
+
+// `vec_align`: required alignment of q, k, v and o (16 for the chunk path, whose tiles may be
+// moved by TMA; the element size for decode). alpha and eta are read as scalars.
+// `ntok` = 0 (no tokens) allows the token tensors to be NULL.
+kla_status check_common(const void *q, const void *k, const void *v, const float *alpha,
+                        const float *eta, const void *o, int B, int H, int d_k, int d_v,
+                        kla_dtype dtype, kla_gate gate, uintptr_t vec_align, size_t ntok) {
+    if (ntok > 0 && (!q || !k || !v || !alpha || !eta || !o)) return KLA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || d_k < 1 || d_v < 1) return KLA_ERR_INVALID_ARG;
+    if (dtype != KLA_DTYPE_F32 && dtype != KLA_DTYPE_BF16) return KLA_ERR_INVALID_ARG;
+    if (gate != KLA_GATE_SCALAR && gate != KLA_GATE_CHANNEL) return KLA_ERR_INVALID_ARG;
+    if (vec_align == 0) vec_align = dtype == KLA_DTYPE_BF16 ? 2 : 4;
+    if (!aligned(q, vec_align) || !aligned(k, vec_align) || !aligned(v, vec_align) || !aligned(o, vec_align) ||
+        !aligned(alpha, 4) || !aligned(eta, 4))
+        return KLA_ERR_INVALID_ARG;
+    if (!supported_d(d_k) || !supported_d(d_v)) return KLA_ERR_UNSUPPORTED;
+    return KLA_OK;
+}
+
+// [lo, hi) byte range of a buffer, for overlap checks.
+struct Span {
+    uintptr_t lo, hi;
+};
+Span span(const void *p, size_t bytes) {
+    uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return {a, a + bytes};
+}
+bool overlaps(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi; }
+
+}  // namespace
+
+extern "C" {
+
+int kla_abi_version(void) { return 100; }
+
+const char *kla_status_string(kla_status s) {
+    switch (s) {
+        case KLA_OK: return "KLA_OK";
+        case KLA_ERR_INVALID_ARG: return "KLA_ERR_INVALID_ARG: bad pointer, size, alignment or workspace";
+        case KLA_ERR_UNSUPPORTED: return "KLA_ERR_UNSUPPORTED: size or chunk not implemented";
+        case KLA_ERR_CUDA: return "KLA_ERR_CUDA: a CUDA call or kernel launch failed";
+        case KLA_ERR_TIMEOUT: return "KLA_ERR_TIMEOUT: a bounded device wait gave up";
+    }
+    return "KLA_ERR_UNKNOWN";
+}
+
+size_t kla_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v, int chunk, kla_dtype dtype,
+                                    kla_gate gate) {
+    (void)B; (void)T; (void)H; (void)d_k; (void)d_v; (void)chunk; (void)dtype; (void)gate;
+    return 0;
+}
+
+kla_status kla_chunk_fwd(const void *q, const void *k, const void *v, const float *alpha, const float *eta,
+                         float eps, const float *S0, void *o, float *S_T, int B, int T, int H, int d_k, int d_v,
+                         int chunk, kla_dtype dtype, kla_gate gate, void *workspace, size_t workspace_bytes,
+                         void *stream) {
+    if (T < 0) return KLA_ERR_INVALID_ARG;
+    kla_status st = check_common(q, k, v, alpha, eta, o, B, H, d_k, d_v, dtype, gate, 16,
+                                 static_cast<size_t>(B) * T * H);
+    if (st != KLA_OK) return st;
+    if (!supported_chunk(chunk)) return KLA_ERR_UNSUPPORTED;
+    if ((S0 && !aligned16(S0)) || (S_T && !aligned16(S_T))) return KLA_ERR_INVALID_ARG;
+    const size_t need = kla_chunk_fwd_workspace_size(B, T, H, d_k, d_v, chunk, dtype, gate);
+    if (workspace_bytes < need || (need > 0 && !workspace)) return KLA_ERR_INVALID_ARG;
+    if (!(eps == eps)) return KLA_ERR_INVALID_ARG;   // NaN stabiliser
+
+    // The final state may alias S0 exactly but must not overlap anything else.
+    const size_t esz = dtype == KLA_DTYPE_BF16 ? 2 : 4;
+    const size_t ntok = static_cast<size_t>(B) * T * H;
+    const size_t sbytes = static_cast<size_t>(B) * H * d_k * d_v * 4;
+    if (S_T) {
+        Span s = span(S_T, sbytes);
+        const Span others[] = {span(q, ntok * d_k * esz), span(k, ntok * d_k * esz), span(v, ntok * d_v * esz),
+                               span(o, ntok * d_v * esz),
+                               span(alpha, ntok * (gate == KLA_GATE_CHANNEL ? d_k : 1) * 4),
+                               span(eta, ntok * 4)};
+        for (const Span &x : others)
+            if (x.hi > x.lo && overlaps(s, x)) return KLA_ERR_INVALID_ARG;
+        if (S0 && S0 != S_T && overlaps(s, span(S0, sbytes))) return KLA_ERR_INVALID_ARG;
+    }
+
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (T == 0) {   // no tokens: the final state is the initial state
+        if (!S_T) return KLA_OK;
+        cudaError_t e = S0 ? (S0 == S_T ? cudaSuccess : cudaMemcpyAsync(S_T, S0, sbytes, cudaMemcpyDeviceToDevice, cs))
+                           : cudaMemsetAsync(S_T, 0, sbytes, cs);
+        return e == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
+    }
+
+    kla::ChunkArgs a{q, k, v, alpha, eta, eps, S0, o, S_T, B, T, H, d_k, d_v, chunk, dtype, gate,
+                     workspace, workspace_bytes, nullptr, cs};
+    if (err_word(&a.err) != cudaSuccess) return KLA_ERR_CUDA;
+    cudaError_t e = kla::chunk_tc_supports(a) ? kla::launch_chunk_tc(a) : kla::launch_chunk_simt(a);
+    return e == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
+}
+
+kla_status kla_decode_step(const void *q, const void *k, const void *v, const float *alpha, const float *eta,
+                           float eps, float *S, void *o, int B, int H, int d_k, int d_v, kla_dtype dtype,
+                           kla_gate gate, void *stream) {
+    kla_status st = check_common(q, k, v, alpha, eta, o, B, H, d_k, d_v, dtype, gate, 0, 1);
+    if (st != KLA_OK) return st;
+    if (!S || !aligned16(S)) return KLA_ERR_INVALID_ARG;
+    if (!(eps == eps)) return KLA_ERR_INVALID_ARG;
+    const size_t esz = dtype == KLA_DTYPE_BF16 ? 2 : 4;
+    const size_t nh = static_cast<size_t>(B) * H;
+    Span s = span(S, nh * d_k * d_v * 4);
+    const Span others[] = {span(q, nh * d_k * esz), span(k, nh * d_k * esz), span(v, nh * d_v * esz),
+                           span(o, nh * d_v * esz), span(alpha, nh * (gate == KLA_GATE_CHANNEL ? d_k : 1) * 4),
+                           span(eta, nh * 4)};
+    for (const Span &x : others)
+        if (overlaps(s, x)) return KLA_ERR_INVALID_ARG;
+    kla::DecodeArgs a{q, k, v, alpha, eta, eps, S, o, B, H, d_k, d_v, dtype, gate, static_cast<cudaStream_t>(stream)};
+    return kla::launch_decode(a) == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
+}
+
+kla_status kla_device_status(void *stream) {
+    unsigned *p = nullptr;
+    if (err_word(&p) != cudaSuccess) return KLA_ERR_CUDA;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    unsigned h = 0;
+    if (cudaStreamSynchronize(cs) != cudaSuccess) return KLA_ERR_CUDA;
+    if (cudaMemcpy(&h, p, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return KLA_ERR_CUDA;
+    if (h) {
+        const unsigned zero = 0;
+        if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return KLA_ERR_CUDA;
+    }
+    if (h & kla::kErrTimeout) return KLA_ERR_TIMEOUT;
+    if (h & kla::kErrGateRange) return KLA_ERR_INVALID_ARG;
+    return KLA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,165 @@
+// kla_decode.cu -- fused single-token KLA step (decode).
+//
+// Per (sequence b, head h) and token (GeekNews, "Revisando las variantes de atencion lineal
+// de la familia DeltaNet", section "Kernel Triton recurrente fusionado para decodificacion";
+// step size from the KLA page, section "La Regola di Aggiornamento KLA"):
+//   S~ = alpha (.) S ;  e = v - S~^T k ;  beta = eta / (||k||^2 + eps) ;  S = S~ + beta k e^T ;
+//   o = S^T q.
+// Expanding the read after the write gives o = S~^T q + beta e (k . q), so both reductions
+// over the key rows (S~^T k and S~^T q) come from ONE pass over the old state, and the new
+// state is written in the same pass: every state element is read once and written once.
+// The step is HBM-bound (8 d_k d_v bytes of state traffic against 7 d_k d_v flops), so it
+// runs on the CUDA cores with 128-bit coalesced loads and stores.
+//
+// Grid: one CTA of 128 threads per (32-column value tile, head, sequence). A CTA keeps its
+// d_k x 32 tile of S in registers (8 float4 per thread at d_k = 128) between the reduction
+// and the write.
+#include <algorithm>
+
+#include "kla_internal.cuh"
+
+namespace kla {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kMaxRowsPerThread = 8;
+
+struct DecodeParams {
+    const void *q, *k, *v;
+    const float *alpha, *eta;
+    float eps;
+    float *S;
+    void *o;
+    int B, H, DK, DV, BV;
+};
+
+template <typename TIn, bool kChannel, int NCG>   // NCG = float4 column groups per tile (BV / 4)
+__global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) {
+    constexpr int RG = kThreads / NCG;            // row groups
+    __shared__ float sk[128], sq[128], sa[128];
+    __shared__ float sred[2][kThreads / 32][NCG * 4];
+    __shared__ float snorm[2][kThreads / 32];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cg = tid % NCG, rg = tid / NCG;
+    const int v0 = blockIdx.x * (NCG * 4);
+    const int h = blockIdx.y, b = blockIdx.z;
+    const size_t bh = static_cast<size_t>(b) * p.H + h;
+    const int DK = p.DK;
+    float *Sbh = p.S + bh * DK * p.DV;
+
+    // Issue the state loads first: they are the long pole.
+    float4 s[kMaxRowsPerThread];
+#pragma unroll
+    for (int r = 0; r < kMaxRowsPerThread; ++r) {
+        const int i = rg + r * RG;
+        if (i < DK) s[r] = *reinterpret_cast<const float4 *>(Sbh + static_cast<size_t>(i) * p.DV + v0 + cg * 4);
+    }
+
+    const TIn *q = static_cast<const TIn *>(p.q) + bh * DK;
+    const TIn *k = static_cast<const TIn *>(p.k) + bh * DK;
+    float kk = 0.f, kq = 0.f;
+    if (tid < DK) {
+        const float kt = to_f32(k[tid]), qt = to_f32(q[tid]);
+        sk[tid] = kt;
+        sq[tid] = qt;
+        sa[tid] = kChannel ? p.alpha[bh * DK + tid] : 0.f;
+        kk = kt * kt;
+        kq = kt * qt;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        kk += __shfl_xor_sync(0xffffffffu, kk, off);
+        kq += __shfl_xor_sync(0xffffffffu, kq, off);
+    }
+    if (lane == 0) { snorm[0][warp] = kk; snorm[1][warp] = kq; }
+    __syncthreads();
+    float knorm2 = 0.f, kdotq = 0.f;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) { knorm2 += snorm[0][w]; kdotq += snorm[1][w]; }
+    const float beta = kla_beta(p.eta[bh], knorm2, p.eps);
+    const float a_scalar = kChannel ? 1.f : p.alpha[bh];
+
+    // Partial reductions over this thread's rows of the decayed state.
+    float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
+#pragma unroll
+    for (int r = 0; r < kMaxRowsPerThread; ++r) {
+        const int i = rg + r * RG;
+        if (i < DK) {
+            const float a = kChannel ? sa[i] : a_scalar;
+            const float ak = a * sk[i], aq = a * sq[i];
+            pk.x = fmaf(ak, s[r].x, pk.x); pk.y = fmaf(ak, s[r].y, pk.y);
+            pk.z = fmaf(ak, s[r].z, pk.z); pk.w = fmaf(ak, s[r].w, pk.w);
+            pq.x = fmaf(aq, s[r].x, pq.x); pq.y = fmaf(aq, s[r].y, pq.y);
+            pq.z = fmaf(aq, s[r].z, pq.z); pq.w = fmaf(aq, s[r].w, pq.w);
+        }
+    }
+    // Reduce over the row groups of the warp (lanes sharing a column group).
+#pragma unroll
+    for (int off = NCG; off < 32; off <<= 1) {
+        pk.x += __shfl_xor_sync(0xffffffffu, pk.x, off); pk.y += __shfl_xor_sync(0xffffffffu, pk.y, off);
+        pk.z += __shfl_xor_sync(0xffffffffu, pk.z, off); pk.w += __shfl_xor_sync(0xffffffffu, pk.w, off);
+        pq.x += __shfl_xor_sync(0xffffffffu, pq.x, off); pq.y += __shfl_xor_sync(0xffffffffu, pq.y, off);
+        pq.z += __shfl_xor_sync(0xffffffffu, pq.z, off); pq.w += __shfl_xor_sync(0xffffffffu, pq.w, off);
+    }
+    if (lane < NCG) {
+        *reinterpret_cast<float4 *>(&sred[0][warp][lane * 4]) = pk;
+        *reinterpret_cast<float4 *>(&sred[1][warp][lane * 4]) = pq;
+    }
+    __syncthreads();
+    float4 pred = make_float4(0.f, 0.f, 0.f, 0.f), rd = pred;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) {
+        const float4 x = *reinterpret_cast<const float4 *>(&sred[0][w][cg * 4]);
+        const float4 y = *reinterpret_cast<const float4 *>(&sred[1][w][cg * 4]);
+        pred.x += x.x; pred.y += x.y; pred.z += x.z; pred.w += x.w;
+        rd.x += y.x; rd.y += y.y; rd.z += y.z; rd.w += y.w;
+    }
+    const TIn *vv = static_cast<const TIn *>(p.v) + bh * p.DV + v0 + cg * 4;
+    float4 e;
+    e.x = to_f32(vv[0]) - pred.x; e.y = to_f32(vv[1]) - pred.y;
+    e.z = to_f32(vv[2]) - pred.z; e.w = to_f32(vv[3]) - pred.w;
+
+    if (rg == 0) {   // o = S~^T q + beta e (k . q)
+        TIn *o = static_cast<TIn *>(p.o) + bh * p.DV + v0 + cg * 4;
+        const float bkq = beta * kdotq;
+        o[0] = from_f32<TIn>(fmaf(bkq, e.x, rd.x));
+        o[1] = from_f32<TIn>(fmaf(bkq, e.y, rd.y));
+        o[2] = from_f32<TIn>(fmaf(bkq, e.z, rd.z));
+        o[3] = from_f32<TIn>(fmaf(bkq, e.w, rd.w));
+    }
+    // S = S~ + beta k e^T
+#pragma unroll
+    for (int r = 0; r < kMaxRowsPerThread; ++r) {
+        const int i = rg + r * RG;
+        if (i < DK) {
+            const float a = kChannel ? sa[i] : a_scalar;
+            const float bk = beta * sk[i];
+            float4 x;
+            x.x = fmaf(a, s[r].x, bk * e.x); x.y = fmaf(a, s[r].y, bk * e.y);
+            x.z = fmaf(a, s[r].z, bk * e.z); x.w = fmaf(a, s[r].w, bk * e.w);
+            *reinterpret_cast<float4 *>(Sbh + static_cast<size_t>(i) * p.DV + v0 + cg * 4) = x;
+        }
+    }
+}
+
+template <typename TIn, bool kChannel>
+cudaError_t launch_t(const DecodeArgs &a) {
+    const int BV = std::min(a.d_v, 32);
+    DecodeParams p{a.q, a.k, a.v, a.alpha, a.eta, a.eps, a.S, a.o, a.B, a.H, a.d_k, a.d_v, BV};
+    dim3 grid(a.d_v / BV, a.H, a.B);
+    if (BV == 32) decode_kernel<TIn, kChannel, 8><<<grid, kThreads, 0, a.stream>>>(p);
+    else decode_kernel<TIn, kChannel, 4><<<grid, kThreads, 0, a.stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs &a) {
+    const bool ch = a.gate == KLA_GATE_CHANNEL;
+    if (a.dtype == KLA_DTYPE_BF16)
+        return ch ? launch_t<__nv_bfloat16, true>(a) : launch_t<__nv_bfloat16, false>(a);
+    return ch ? launch_t<float, true>(a) : launch_t<float, false>(a);
+}
+
+}  // namespace kla

@@ -1,0 +1,70 @@
+// kla_internal.cuh -- shared declarations of the KLA CUDA library (not part of the ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kla.h"
+
+namespace kla {
+
+// Device-side error bits, OR-ed into one word per device (see kla_device_status).
+enum : unsigned {
+    kErrTimeout = 1u,      // a bounded wait gave up
+    kErrGateRange = 2u,    // per-channel log-decay outside the exact range of a factorised product
+};
+
+// Everything a chunk-forward launcher needs; pointers are device pointers.
+struct ChunkArgs {
+    const void *q, *k, *v;
+    const float *alpha, *eta;
+    float eps;
+    const float *S0;
+    void *o;
+    float *S_T;
+    int B, T, H, d_k, d_v, chunk;
+    kla_dtype dtype;
+    kla_gate gate;
+    void *workspace;
+    size_t workspace_bytes;
+    unsigned *err;         // device error word
+    cudaStream_t stream;
+};
+
+struct DecodeArgs {
+    const void *q, *k, *v;
+    const float *alpha, *eta;
+    float eps;
+    float *S;
+    void *o;
+    int B, H, d_k, d_v;
+    kla_dtype dtype;
+    kla_gate gate;
+    cudaStream_t stream;
+};
+
+// fp32 CUDA-core chunk path: any supported size, fp32 or bf16 storage.
+cudaError_t launch_chunk_simt(const ChunkArgs &a);
+// tcgen05 tensor-core chunk path: bf16, d_k = d_v = 128, chunk = 64.
+bool chunk_tc_supports(const ChunkArgs &a);
+cudaError_t launch_chunk_tc(const ChunkArgs &a);
+// fused single-token decode step.
+cudaError_t launch_decode(const DecodeArgs &a);
+
+// ------------------------------------------------------------------ device helpers
+template <typename T> __device__ __forceinline__ float to_f32(T x);
+template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// beta = eta / (||k||^2 + eps), 0 when the denominator is exactly zero.
+__device__ __forceinline__ float kla_beta(float eta, float knorm2, float eps) {
+    const float den = knorm2 + eps;
+    return den == 0.0f ? 0.0f : eta / den;
+}
+
+}  // namespace kla

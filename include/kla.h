@@ -1,0 +1,138 @@
+/*
+ * kla.h -- C ABI of the KLA gated delta-rule recurrence on NVIDIA GB300 (sm_103a).
+ *
+ * The operation (Gist.science, "Riepilogo Tecnico: Attenzione Lineare Kaczmarz
+ * (KLA)", sections "Derivazione Teorica" and "La Regola di Aggiornamento KLA"):
+ * for every sequence b and head h, a state S (d_k x d_v; rows are key channels,
+ * columns value channels) is carried over tokens t = 0..T-1:
+ *
+ *     S~_t  = alpha_t (.) S_{t-1}                 forget (gate on the key rows)
+ *     e_t   = v_t - S~_t^T k_t                     residual against the decayed state
+ *     beta_t= eta_t / (||k_t||^2 + eps)            Kaczmarz step (0 if the denominator is 0)
+ *     S_t   = S~_t + beta_t k_t e_t^T              write
+ *     o_t   = S_t^T q_t                            read, after the write
+ *
+ * alpha_t is one scalar per (b, t, h) (Gated DeltaNet / KLA gate) or one value per
+ * key channel (Kimi Delta Attention gate: GeekNews, "Revisando las variantes de
+ * atencion lineal de la familia DeltaNet", section "Kimi Delta Attention"), in
+ * which case row i of S is scaled by alpha_t[i].
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers to row-major, contiguous tensors.
+ *    Alignment: the state (S0, S_T, S) 16 bytes; q, k, v, o 16 bytes for
+ *    kla_chunk_fwd and their element size for kla_decode_step; alpha, eta 4 bytes.
+ *    The caller allocates and owns every buffer; the library allocates no device
+ *    memory and keeps no per-call state.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL is
+ *    the legacy default stream). A returned KLA_OK means the work was enqueued.
+ *  - Argument errors are detected on the host before anything is launched and
+ *    return KLA_ERR_INVALID_ARG or KLA_ERR_UNSUPPORTED; nothing is written then.
+ *  - Device-side waits are bounded; a wait that gives up records a flag that
+ *    kla_device_status() reports as KLA_ERR_TIMEOUT.
+ *  - Supported sizes: d_k, d_v in {16, 32, 64, 128}; chunk in {16, 32, 64}.
+ *    bf16 inputs with d_k = d_v = 128 and chunk = 64 run on the tensor-core
+ *    (tcgen05) path; every other supported case runs on the fp32 CUDA-core path.
+ */
+#ifndef KLA_H
+#define KLA_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kla_status {
+    KLA_OK = 0,
+    KLA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer, workspace too small */
+    KLA_ERR_UNSUPPORTED = 2,   /* valid but not implemented size / chunk combination */
+    KLA_ERR_CUDA = 3,          /* a CUDA runtime call or a launch failed */
+    KLA_ERR_TIMEOUT = 4        /* a bounded device wait gave up (see kla_device_status) */
+} kla_status;
+
+typedef enum kla_dtype {
+    KLA_DTYPE_F32 = 0,         /* q, k, v, o stored as IEEE fp32 */
+    KLA_DTYPE_BF16 = 1         /* q, k, v, o stored as bfloat16 */
+} kla_dtype;
+
+typedef enum kla_gate {
+    KLA_GATE_SCALAR = 0,       /* alpha [B, T, H]: one gate per token and head */
+    KLA_GATE_CHANNEL = 1       /* alpha [B, T, H, d_k]: one gate per key channel */
+} kla_gate;
+
+/*
+ * Chunkwise prefill (GeekNews page above, section "KDA por chunks: reordenar la
+ * recurrencia como multiplicaciones de matrices"; the KLA page, section
+ * "Implementazione", for beta entering the chunk solver as a diagonal).
+ * The result equals the token-by-token recurrence up to floating-point rounding.
+ *
+ *   q, k     [B, T, H, d_k]  dtype            read only
+ *   v        [B, T, H, d_v]  dtype            read only
+ *   alpha    fp32, [B, T, H] (KLA_GATE_SCALAR) or [B, T, H, d_k] (KLA_GATE_CHANNEL),
+ *            values in (0, 1]; the log-decay is taken on the device
+ *   eta      fp32 [B, T, H], any finite value (eta = 1 with eps = 0 is the exact projection)
+ *   eps      stabiliser added to ||k||^2
+ *   S0       fp32 [B, H, d_k, d_v] initial state, or NULL for zeros
+ *   o        [B, T, H, d_v] dtype, written (rounded to nearest even for bf16)
+ *   S_T      fp32 [B, H, d_k, d_v] final state, or NULL if not wanted; may be the same
+ *            pointer as S0 (in-place continuation); must not overlap any other argument
+ *   T        >= 0; T = 0 writes S_T = S0 (or zeros) and no outputs, and then q, k, v,
+ *            alpha, eta and o may be NULL. T need not be a multiple of chunk; the last
+ *            chunk is masked.
+ *   chunk    tokens per chunk
+ *   workspace, workspace_bytes: device scratch of at least
+ *            kla_chunk_fwd_workspace_size(...) bytes (may be NULL when that size is 0)
+ *
+ * Per-key-channel gates on the tensor-core path: the in-chunk products use the
+ * chunk start as reference point, which is exact as long as the log-decay of every
+ * key channel summed over one chunk stays above -80 (alpha averaged over 64 tokens
+ * above about 0.29). A chunk outside that range raises a device flag that
+ * kla_device_status() reports as KLA_ERR_INVALID_ARG.
+ */
+kla_status kla_chunk_fwd(const void *q, const void *k, const void *v,
+                         const float *alpha, const float *eta, float eps,
+                         const float *S0, void *o, float *S_T,
+                         int B, int T, int H, int d_k, int d_v, int chunk,
+                         kla_dtype dtype, kla_gate gate,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of device scratch kla_chunk_fwd needs for these sizes (0 if none). */
+size_t kla_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v, int chunk,
+                                    kla_dtype dtype, kla_gate gate);
+
+/*
+ * One fused single-token step for B sequences (GeekNews page above, section
+ * "Kernel Triton recurrente fusionado para decodificacion": forget, predict,
+ * residual, outer-product write, read; the KLA step of the KLA page).
+ * Each head's state is read once and written once.
+ *
+ *   q, k     [B, H, d_k] dtype;  v [B, H, d_v] dtype
+ *   alpha    fp32 [B, H] or [B, H, d_k];  eta fp32 [B, H]
+ *   S        fp32 [B, H, d_k, d_v], updated in place
+ *   o        [B, H, d_v] dtype, written
+ */
+kla_status kla_decode_step(const void *q, const void *k, const void *v,
+                           const float *alpha, const float *eta, float eps,
+                           float *S, void *o,
+                           int B, int H, int d_k, int d_v,
+                           kla_dtype dtype, kla_gate gate, void *stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device-side error flags that
+ * bounded waits and range checks of earlier calls on this device may have set.
+ * Returns KLA_OK, KLA_ERR_TIMEOUT, KLA_ERR_INVALID_ARG (a per-channel gate outside
+ * the exact range of the tensor-core path) or KLA_ERR_CUDA.
+ */
+kla_status kla_device_status(void *stream);
+
+/* Static, human-readable name of a status code. */
+const char *kla_status_string(kla_status status);
+
+/* ABI version of this header (major * 100 + minor). */
+int kla_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KLA_H */

@@ -1,0 +1,95 @@
+"""The C-ABI library loads, exports every symbol include/kla.h declares, and rejects bad
+arguments on the host before launching anything (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gated_delta_rule_14_gb300 import _native, build
+    build.build()
+    return _native.lib()
+
+
+def declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", h)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(kla_[a-z_0-9]+)\s*\(", txt, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for required in ("kla_chunk_fwd", "kla_decode_step", "kla_chunk_fwd_workspace_size", "kla_status_string",
+                     "kla_device_status", "kla_abi_version"):
+        assert required in names, names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    for code, token in [(0, "KLA_OK"), (1, "INVALID_ARG"), (2, "UNSUPPORTED"), (3, "CUDA"), (4, "TIMEOUT")]:
+        assert token in lib.kla_status_string(code).decode()
+    assert "UNKNOWN" in lib.kla_status_string(99).decode()
+    assert lib.kla_abi_version() == 100
+
+
+# Fake, never dereferenced device addresses: every case below must be rejected on the host.
+A = 0x7f0000000000
+
+
+def chunk(lib, **kw):
+    args = dict(q=A, k=A + 0x10000000, v=A + 0x20000000, alpha=A + 0x30000000, eta=A + 0x38000000, eps=1e-6,
+                S0=None, o=A + 0x40000000, S_T=None, B=1, T=64, H=1, d_k=16, d_v=16, chunk=16, dtype=0, gate=0,
+                ws=None, ws_bytes=0, stream=None)
+    args.update(kw)
+    return lib.kla_chunk_fwd(args["q"], args["k"], args["v"], args["alpha"], args["eta"], args["eps"],
+                             args["S0"], args["o"], args["S_T"], args["B"], args["T"], args["H"], args["d_k"],
+                             args["d_v"], args["chunk"], args["dtype"], args["gate"], args["ws"], args["ws_bytes"],
+                             args["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(o=None), 1), (dict(q=None, T=0), 0), (dict(alpha=None), 1), (dict(eta=None), 1),
+    (dict(T=-1), 1), (dict(B=0), 1), (dict(H=0), 1), (dict(dtype=7), 1), (dict(gate=3), 1),
+    (dict(q=A + 8), 1), (dict(o=A + 0x40000004), 1), (dict(S0=A + 0x50000002), 1),
+    (dict(d_k=48), 2), (dict(d_v=256), 2), (dict(chunk=128), 2), (dict(chunk=8), 2),
+    (dict(eps=float("nan")), 1),
+    (dict(S_T=A + 0x10000000), 1),                     # final state overlapping k
+    (dict(S0=A + 0x50000000, S_T=A + 0x50000200), 1),  # partial overlap of S0 and S_T
+])
+def test_chunk_fwd_rejects_on_host(lib, kw, code):
+    assert chunk(lib, **kw) == code
+
+
+def test_decode_rejects_on_host(lib):
+    f = lib.kla_decode_step
+    ok = dict(q=A, k=A + 0x1000000, v=A + 0x2000000, alpha=A + 0x3000000, eta=A + 0x3800000, S=A + 0x4000000,
+              o=A + 0x5000000)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return f(a["q"], a["k"], a["v"], a["alpha"], a["eta"], 1e-6, a["S"], a["o"], 2, 2, 16, 16, 1, 0, None)
+    assert call(S=None) == 1
+    assert call(S=A + 0x4000004) == 1
+    assert call(q=A + 1) == 1                # bf16 vector not aligned to its element
+    assert call(v=None) == 1
+    assert call(S=A) == 1                    # state overlaps q
+    assert f(A, A + 0x1000000, A + 0x2000000, A + 0x3000000, A + 0x3800000, 1e-6, A + 0x4000000, A + 0x5000000,
+             2, 2, 24, 16, 1, 0, None) == 2
+
+
+def test_workspace_size_is_a_host_call(lib):
+    assert lib.kla_chunk_fwd_workspace_size(8, 4096, 16, 128, 128, 64, 1, 0) >= 0

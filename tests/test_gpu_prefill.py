@@ -1,0 +1,121 @@
+"""Chunkwise prefill on the GPU against the fp64 oracle (relative L2 over the whole tensor:
+<= 1e-5 for fp32 inputs, <= 1e-2 for bf16 inputs with the fp32 state)."""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import gather_chains, oracle_chains, run_prefill, sample_chains, to_dev, DEV
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-5, "bf16": 1e-2}
+
+
+def check(inp, o, S, chains=None):
+    o_ref, s_ref = oracle_chains(inp, chains)
+    if chains is None:
+        chains = [(b, h) for b in range(inp.wl.B) for h in range(inp.wl.H)]
+    o_g, s_g = gather_chains(o, S, chains)
+    tol = TOL[inp.wl.dtype]
+    eo, es = oracle.rel_l2(o_g, o_ref), oracle.rel_l2(s_g, s_ref)
+    assert np.isfinite(o).all() and np.isfinite(S).all()
+    assert eo <= tol and es <= tol, f"rel-L2 o={eo:.3e} S={es:.3e} tol={tol}"
+    return eo, es
+
+
+def test_tiny_config():
+    inp = synth.make_prefill("tiny", seed=0)
+    o, S = run_prefill(inp)
+    check(inp, o, S)
+
+
+CASES = [
+    # (dtype, d_k, d_v, chunk, T, gate, s0)
+    ("f32", 16, 16, 16, 1, "scalar", 0.0),
+    ("f32", 16, 16, 16, 17, "channel", 0.1),
+    ("f32", 32, 64, 32, 100, "scalar", 0.1),
+    ("f32", 64, 32, 64, 130, "channel", 0.0),
+    ("f32", 128, 128, 64, 75, "scalar", 0.05),
+    ("f32", 128, 128, 16, 40, "channel", 0.05),
+    ("bf16", 16, 16, 16, 33, "scalar", 0.1),
+    ("bf16", 64, 64, 32, 97, "channel", 0.1),
+    ("bf16", 128, 128, 64, 1, "scalar", 0.05),
+    ("bf16", 128, 128, 64, 63, "scalar", 0.0),
+    ("bf16", 128, 128, 64, 64, "scalar", 0.05),
+    ("bf16", 128, 128, 64, 65, "scalar", 0.05),
+    ("bf16", 128, 128, 64, 300, "scalar", 0.05),
+    ("bf16", 128, 128, 64, 257, "channel", 0.05),
+    ("bf16", 128, 128, 16, 50, "scalar", 0.0),
+]
+
+
+@pytest.mark.parametrize("dtype,dk,dv,C,T,gate,s0", CASES, ids=lambda x: str(x))
+def test_small_shapes(dtype, dk, dv, C, T, gate, s0):
+    base = "kda8k" if gate == "channel" else "gdn4k"
+    inp = synth.make_prefill(base, seed=T * 7 + dk, B=2, T=T, H=3, d_k=dk, d_v=dv, chunk=C, dtype=dtype,
+                             s0_sigma=s0)
+    o, S = run_prefill(inp)
+    check(inp, o, S)
+
+
+def test_eta_one_eps_zero_exact_projection_and_extreme_gates():
+    # unrelaxed KLA (eta = 1, eps = 0) and gates near 0 and 1
+    inp = synth.make_prefill("gdn4k", seed=5, B=1, T=130, H=2, s0_sigma=0.05)
+    inp.eta[...] = 1.0
+    inp.alpha[0, :40] = 1.0
+    inp.alpha[0, 40:50] = 1e-30
+    inp = synth.PrefillInputs(dataclasses.replace(inp.wl, eps=0.0), inp.q, inp.k, inp.v, inp.alpha, inp.eta, inp.S0)
+    o, S = run_prefill(inp)
+    check(inp, o, S)
+
+
+def test_continuation_two_calls_equal_one():
+    import gated_delta_rule_14_gb300 as kla
+    inp = synth.make_prefill("gdn4k", seed=9, B=2, T=200, H=2, s0_sigma=0.05)
+    q, k, v, a, e, S0 = (to_dev(x) for x in (inp.q, inp.k, inp.v, inp.alpha, inp.eta, inp.S0))
+    o_full, S_full = kla.chunk_fwd(q, k, v, a, e, inp.wl.eps, S0)
+    T1 = 77
+    o1, S1 = kla.chunk_fwd(q[:, :T1].contiguous(), k[:, :T1].contiguous(), v[:, :T1].contiguous(),
+                           a[:, :T1].contiguous(), e[:, :T1].contiguous(), inp.wl.eps, S0)
+    o2, S2 = kla.chunk_fwd(q[:, T1:].contiguous(), k[:, T1:].contiguous(), v[:, T1:].contiguous(),
+                           a[:, T1:].contiguous(), e[:, T1:].contiguous(), inp.wl.eps, S1)
+    kla.device_status(DEV)
+    o_ref, s_ref = oracle_chains(inp)
+    o_cat = np.concatenate([o1.float().cpu().numpy(), o2.float().cpu().numpy()], axis=1)
+    o_g, s_g = gather_chains(o_cat, S2.cpu().numpy(), [(b, h) for b in range(2) for h in range(2)])
+    assert oracle.rel_l2(o_g, o_ref) <= 1e-2 and oracle.rel_l2(s_g, s_ref) <= 1e-2
+    assert oracle.rel_l2(S2.cpu().numpy(), S_full.cpu().numpy()) <= 1e-2
+
+
+def test_state_in_place_and_empty_sequence():
+    import torch
+
+    import gated_delta_rule_14_gb300 as kla
+    inp = synth.make_prefill("gdn4k", seed=10, B=1, T=70, H=2, s0_sigma=0.05)
+    S = to_dev(inp.S0).clone()
+    o, S_out = kla.chunk_fwd(to_dev(inp.q), to_dev(inp.k), to_dev(inp.v), to_dev(inp.alpha), to_dev(inp.eta),
+                             inp.wl.eps, S, S_T=S)
+    kla.device_status(DEV)
+    assert S_out.data_ptr() == S.data_ptr()
+    o_ref, s_ref = oracle_chains(inp)
+    assert oracle.rel_l2(S.cpu().numpy()[0], s_ref) <= 1e-2
+    # T = 0: the final state is the initial state, no output
+    z = torch.empty((1, 0, 2, 128), dtype=torch.bfloat16, device=DEV)
+    za = torch.empty((1, 0, 2), dtype=torch.float32, device=DEV)
+    S0 = to_dev(inp.S0)
+    o, ST = kla.chunk_fwd(z, z, z, za, za, 1e-6, S0)
+    kla.device_status(DEV)
+    assert o.shape == (1, 0, 2, 128) and torch.equal(ST, S0)
+    o, ST = kla.chunk_fwd(z, z, z, za, za, 1e-6, None)
+    assert torch.count_nonzero(ST).item() == 0
+
+
+@pytest.mark.parametrize("name,nchains", [("gdn4k", 8), ("kda8k", 6), ("long131k", 2)])
+def test_full_config_sampled(name, nchains):
+    inp = synth.make_prefill(name, seed=0)
+    o, S = run_prefill(inp)
+    chains = sample_chains(inp.wl.B, inp.wl.H, nchains, seed=1)
+    check(inp, o, S, chains)
