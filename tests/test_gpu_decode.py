@@ -47,6 +47,8 @@ def test_decode_full_config_sampled():
 
 
 def test_decode_equals_one_token_prefill():
+    """A decode step is a one-token prefill: both match the oracle (the decode state in fp32
+    arithmetic to 1e-5; the prefill, which may use bf16 tensor-core operands, to 1e-2)."""
     import gated_delta_rule_14_gb300 as kla
     dd = synth.make_decode(seed=4, B=2, H=3, steps=1)
     S = to_dev(dd.S)
@@ -55,5 +57,12 @@ def test_decode_equals_one_token_prefill():
     S_d = S.clone()
     o_d = kla.decode_step(q, k, v, a, e, S_d, dd.wl.eps)
     kla.device_status(DEV)
-    assert oracle.rel_l2(o_d.float().cpu().numpy(), o_p[:, 0].float().cpu().numpy()) <= 1e-2
-    assert oracle.rel_l2(S_d.cpu().numpy(), S_p.cpu().numpy()) <= 1e-5
+    heads = [(b, h) for b in range(2) for h in range(3)]
+    o_ref, s_ref = decode_oracle(dd, heads)
+    o_d_g = np.stack([o_d.float().cpu().numpy()[b, h] for b, h in heads])[:, None]
+    o_p_g = np.stack([o_p[:, 0].float().cpu().numpy()[b, h] for b, h in heads])[:, None]
+    s_d_g = np.stack([S_d.cpu().numpy()[b, h] for b, h in heads])
+    s_p_g = np.stack([S_p.cpu().numpy()[b, h] for b, h in heads])
+    assert oracle.rel_l2(s_d_g, s_ref) <= 1e-5
+    assert oracle.rel_l2(s_p_g, s_ref) <= 1e-2
+    assert oracle.rel_l2(o_d_g, o_ref) <= 1e-2 and oracle.rel_l2(o_p_g, o_ref) <= 1e-2
