@@ -12,20 +12,26 @@
 //   O   = diag(e^{G}) Q S + A E,  A = lower(e^{G_i-G_j} q_i.k_j)
 //   S' <- e^{G_end} S + (diag(e^{G_end - G}) K)^T E
 //
-// One CTA per (sequence, head) walks its chunks in order; it is one SM's worth of work and the
-// grid is B*H CTAs. Every product runs on the 5th-generation tensor cores in the transposed
-// orientation that puts 128 rows (d_k or d_v) on the TMEM lanes:
+// One CTA per (sequence, head) walks its chunks in order. Every large product runs on the
+// 5th-generation tensor cores in the transposed orientation that puts 128 rows (d_k or d_v)
+// on the TMEM lanes:
 //   [K;Q] K^T            -> TMEM  (KK^T | QK^T)           M=128 N=64  K=128
 //   K^T (T diag(beta e^G))^T, V^T (T diag(beta))^T -> W^T, U^T        M=128 N=64  K=64
 //   S^T W^T, S^T Q^T     -> (W S)^T, (Q S)^T              M=128 N=64  K=128
 //   E^T_s K              -> (K_end^T E)^T                  M=128 N=128 K=64
 //   E^T A^T              -> (A E)^T                        M=128 N=64  K=64
 // Operands are bf16 in 128-byte-swizzled shared memory (q/k/v tiles arrive by TMA, derived
-// tiles are written by the threads), accumulators are fp32 in tensor memory. The 64 x 64
-// unit-triangular inverse is computed in fp32 on the CUDA cores (16 x 16 diagonal blocks by
-// substitution, then block forward substitution). The state S^T lives in registers in fp32
-// (thread = one value channel, 64 key channels), and is re-rounded to bf16 only as an MMA
-// operand, never as the carried state.
+// tiles are written by the threads), accumulators are fp32 in tensor memory. The state S^T
+// lives in registers in fp32 (thread = one value channel, 64 key channels) and is rounded to
+// bf16 only as an MMA operand, never as the carried state.
+//
+// The 64 x 64 unit-lower inverse T is built in fp32: the four 16 x 16 diagonal blocks by
+// substitution, then two levels of block merging (16 -> 32 -> 64) whose 16x8 products run as
+// warp-level tf32 MMAs.
+//
+// Schedule: the work of chunk c that depends on the carried state (S^T W^T, E, E^T K, the state
+// update and the output) is interleaved with the state-independent work of chunk c+1 (norms,
+// [K;Q]K^T, R, A, the solve, W^T, U^T), so the tensor cores and the CUDA cores overlap.
 #include <cuda.h>
 
 #include <algorithm>
@@ -42,21 +48,24 @@ constexpr int kC = 64;          // chunk
 constexpr int kD = 128;         // d_k = d_v
 constexpr int kThreads = 256;
 constexpr float kMinLogGate = -80.0f;
+constexpr float kSafeDecay = -80.0f;   // chunk decay above which e^{-G_j} is representable
 constexpr uint32_t kWaitLimit = 1u << 24;
 
 // ---- shared memory map (offsets from a 1024-byte aligned base)
-constexpr uint32_t OFF_QK = 0;                       // 2 stages x 32 KB: [blk0: K rows 0-63 | Q rows 0-63][blk1 ...]
+constexpr uint32_t OFF_QK = 0;                        // 2 stages x 32 KB: [blk0: K rows | Q rows][blk1 ...]
 constexpr uint32_t QK_STAGE = 32768;
-constexpr uint32_t OFF_V = OFF_QK + 2 * QK_STAGE;    // 2 stages x 16 KB: [blk0: 64 rows][blk1: 64 rows]
+constexpr uint32_t OFF_V = OFF_QK + 2 * QK_STAGE;     // 2 stages x 16 KB: [blk0: 64 rows][blk1: 64 rows]
 constexpr uint32_t V_STAGE = 16384;
-constexpr uint32_t OFF_AQK = OFF_V + 2 * V_STAGE;    // 8 KB: A (query rows) bf16, K-major
-constexpr uint32_t OFF_X = OFF_AQK + 8192;           // 17 KB: R fp32 [64][65], then T_K | T_V bf16 tiles
-constexpr uint32_t OFF_Y = OFF_X + 17408;            // 17 KB: T fp32 [64][65], then W^T bf16 tile
-constexpr uint32_t OFF_ST = OFF_Y + 17408;           // 32 KB: S^T bf16, K-major, 2 blocks of 128 rows
-constexpr uint32_t OFF_ET = OFF_ST + 32768;          // 16 KB: E^T bf16 (also fp32 scratch of the solve)
-constexpr uint32_t OFF_ETS = OFF_ET + 16384;         // 16 KB: E^T diag(e^{G_end-G}) bf16, then O staging
-constexpr uint32_t OFF_SMALL = OFF_ETS + 16384;      // small vectors + barriers
-constexpr uint32_t SMEM_BYTES = OFF_SMALL + 2048 + 1024;   // + alignment slack
+constexpr uint32_t OFF_AQK = OFF_V + 2 * V_STAGE;     // 2 x 8 KB: A (query rows) bf16, K-major
+constexpr uint32_t OFF_WT = OFF_AQK + 2 * 8192;       // 16 KB: T fp32 during the solve, then W^T bf16
+constexpr uint32_t OFF_ST = OFF_WT + 16384;           // 32 KB: S^T bf16, K-major, 2 blocks of 128 rows
+constexpr uint32_t OFF_ET = OFF_ST + 32768;           // 16 KB: E^T bf16
+constexpr uint32_t OFF_ETS = OFF_ET + 16384;          // 16 KB: E^T diag(e^{G_end-G}) bf16, then O staging
+constexpr uint32_t OFF_R = OFF_ETS + 16384;           // 16 KB: R fp32, then T_K | T_V bf16 tiles
+constexpr uint32_t OFF_XS = OFF_R + 16384;            // 7 KB: solve scratch
+constexpr uint32_t OFF_SMALL = OFF_XS + 7168;         // per-chunk vectors + barriers
+constexpr uint32_t SMEM_BYTES = OFF_SMALL + 4096 + 1024;   // + alignment slack
+static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 // ---- tensor memory columns (512 allocated)
 constexpr uint32_t TM_A = 0;      // [KK^T ; QK^T]     64 cols
@@ -69,18 +78,24 @@ constexpr uint32_t TM_2 = 384;    // (K_end^T E)^T     128
 
 constexpr uint32_t kTileBytes = 4 * 8192 + 2 * 8192;   // q, k, v chunk tiles per stage
 
-struct Small {
-    float G[kC];
+struct ChunkVec {          // per-chunk vectors (double-buffered by chunk parity)
+    float G[kC];           // inclusive prefix of log-gates
     float beta[kC];
-    float expG[kC];
-    float expEnd[kC];
+    float eG[kC];          // e^{G_i}
+    float enG[kC];         // e^{-G_i} (valid when `safe`)
+    float eEnd[kC];        // e^{G_end - G_i}
     float eta[kC];
+    int safe;              // G_end >= kSafeDecay: e^{G_i - G_j} = e^{G_i} e^{-G_j} without overflow
+    int pad[3];
+};
+struct Small {
+    ChunkVec v[2];
     uint64_t full[2];
     uint64_t mA, mW, m1, m2;
     uint32_t tmem_base;
     volatile int abort;
 };
-static_assert(sizeof(Small) <= 2048, "small area");
+static_assert(sizeof(Small) <= 4096, "small area");
 
 struct TcParams {
     const float *alpha, *eta;
@@ -93,6 +108,16 @@ struct TcParams {
 
 __device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
+// fp32 64 x 64 matrices in shared memory, rows of 64 with the float4 groups of each 32-column
+// half permuted by the row (keeps row-vector stores and the mma fragment loads conflict-free).
+__device__ __forceinline__ int fidx(int r, int c) { return r * 64 + (c ^ ((r & 7) << 2)); }
+
+__device__ __forceinline__ void st_v4_f32(float *p, float a, float b, float c, float d) {
+    *reinterpret_cast<float4 *>(p) = make_float4(a, b, c, d);
+}
+__device__ __forceinline__ void st_bf16x8(uint32_t addr, const float *x) {
+    st_shared_v4(addr, pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -102,13 +127,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     Small &sm = *reinterpret_cast<Small *>(smem + OFF_SMALL);
-    float *Rm = reinterpret_cast<float *>(smem + OFF_X);    // [64][65]
-    float *Tm = reinterpret_cast<float *>(smem + OFF_Y);    // [64][65]
-    float *Xs = reinterpret_cast<float *>(smem + OFF_ET);   // solve scratch [3][16][16]
+    float *Rm = reinterpret_cast<float *>(smem + OFF_R);    // R, swizzled fp32 [64][64]
+    float *Tm = reinterpret_cast<float *>(smem + OFF_WT);   // T, swizzled fp32 [64][64]
+    float *Xs = reinterpret_cast<float *>(smem + OFF_XS);   // solve scratch
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, half = warp >> 2;
     const int row = quarter * 32 + lane;        // TMEM lane of this thread
+    const int g8 = lane >> 2, t4 = lane & 3;     // mma.sync fragment coordinates
     const int bh = blockIdx.x;
     const int b = bh / p.H, h = bh % p.H;
     const int nchunks = (p.T + kC - 1) / kC;
@@ -141,11 +167,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t tbase = sm.tmem_base;
     const uint32_t tlane = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
 
+    const uint32_t id_qk = idesc_bf16(128, 64, 0, 0);     // K-major x K-major, N=64
+    const uint32_t id_w = idesc_bf16(128, 64, 1, 0);      // MN-major A, K-major B
+    const uint32_t id_1a = idesc_bf16(128, 64, 0, 1);     // K-major A, MN-major B
+    const uint32_t id_2 = idesc_bf16(128, 128, 0, 1);     // N=128, MN-major B
+
+    auto qk_of = [&](int c) { return sbase + OFF_QK + (c & 1) * QK_STAGE; };
+    auto v_of = [&](int c) { return sbase + OFF_V + (c & 1) * V_STAGE; };
+    auto aqk_of = [&](int c) { return sbase + OFF_AQK + (c & 1) * 8192; };
+
     auto issue_loads = [&](int c) {   // thread 0 only
-        const int st = c & 1;
-        const uint32_t bar = bar_full0 + 8 * st;
-        const uint32_t qk = sbase + OFF_QK + st * QK_STAGE;
-        const uint32_t vv = sbase + OFF_V + st * V_STAGE;
+        const uint32_t bar = bar_full0 + 8 * (c & 1);
+        const uint32_t qk = qk_of(c), vv = v_of(c);
         mbar_arrive_expect_tx(bar, kTileBytes);
         const int t0 = c * kC;
         tma_load_4d(qk + 0, &tm_k, bar, 0, h, t0, b);
@@ -155,6 +188,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tma_load_4d(vv + 0, &tm_v, bar, 0, h, t0, b);
         tma_load_4d(vv + 8192, &tm_v, bar, 64, h, t0, b);
     };
+    auto wait = [&](uint32_t bar, uint32_t parity) {
+        if (!mbar_wait_bounded(bar, parity, kWaitLimit)) sm.abort = 1;
+    };
+
     if (tid == 0) {
         issue_loads(0);
         if (nchunks > 1) issue_loads(1);
@@ -163,13 +200,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // State S^T: this thread owns value channel m = row, key channels [64*half, 64*half + 64).
     float s_reg[64];
     {
-        const int m = row;
         const float *S0 = p.S0 ? p.S0 + static_cast<size_t>(bh) * kD * kD : nullptr;
 #pragma unroll
-        for (int kk = 0; kk < 64; ++kk) s_reg[kk] = S0 ? S0[(64 * half + kk) * kD + m] : 0.f;
+        for (int kk = 0; kk < 64; ++kk) s_reg[kk] = S0 ? S0[(64 * half + kk) * kD + row] : 0.f;
     }
 
-    // Gates of the next chunk, prefetched by warp 0 (two tokens per lane).
+    // Gates of the next chunk to be prepared, prefetched by warp 0 (two tokens per lane).
     float a_nx[2] = {1.f, 1.f}, e_nx[2] = {0.f, 0.f};
     auto load_gates = [&](int c) {
         if (warp == 0 && c < nchunks) {
@@ -185,51 +221,36 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     };
     load_gates(0);
 
-    const uint32_t id_qk = idesc_bf16(128, 64, 0, 0);     // K-major x K-major, N=64
-    const uint32_t id_w = idesc_bf16(128, 64, 1, 0);      // MN-major A, K-major B
-    const uint32_t id_1a = idesc_bf16(128, 64, 0, 1);     // K-major A, MN-major B
-    const uint32_t id_2 = idesc_bf16(128, 128, 0, 1);     // N=128, MN-major B
-
-    for (int c = 0; c < nchunks; ++c) {
-        const int st = c & 1;
-        const uint32_t ph = c & 1;
-        const uint32_t qk = sbase + OFF_QK + st * QK_STAGE;
-        const uint32_t vv = sbase + OFF_V + st * V_STAGE;
-
-        // ---- (1) gates: log-decay prefix, eta; prefetch the next chunk's gates
+    // =========================================================== state-independent work
+    // (a) gates, norms, beta and the decay tables; issue [K;Q] K^T.
+    auto intra_front = [&](int c) {
+        ChunkVec &cv = sm.v[c & 1];
+        const uint32_t qk = qk_of(c);
         if (warp == 0) {
             const float g0 = fmaxf(__logf(a_nx[0]), kMinLogGate), g1 = fmaxf(__logf(a_nx[1]), kMinLogGate);
-            const float e0 = e_nx[0], e1 = e_nx[1];
             float s = g0 + g1;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
                 const float y = __shfl_up_sync(0xffffffffu, s, off);
                 if (lane >= off) s += y;
             }
-            sm.G[2 * lane + 1] = s;
-            sm.G[2 * lane] = s - g1;
-            sm.eta[2 * lane] = e0;
-            sm.eta[2 * lane + 1] = e1;
+            const float gend = __shfl_sync(0xffffffffu, s, 31);
+            const float G0 = s - g1, G1 = s;
+            cv.G[2 * lane] = G0;
+            cv.G[2 * lane + 1] = G1;
+            cv.eG[2 * lane] = __expf(G0);
+            cv.eG[2 * lane + 1] = __expf(G1);
+            cv.enG[2 * lane] = __expf(-G0);
+            cv.enG[2 * lane + 1] = __expf(-G1);
+            cv.eEnd[2 * lane] = __expf(gend - G0);
+            cv.eEnd[2 * lane + 1] = __expf(gend - G1);
+            cv.eta[2 * lane] = e_nx[0];
+            cv.eta[2 * lane + 1] = e_nx[1];
+            if (lane == 0) cv.safe = gend >= kSafeDecay;
         }
         load_gates(c + 1);
-        if (tid == 0) tma_store_wait_read_all();   // previous chunk's O staging is free again
-
-        // ---- (2) S^T as a bf16 K-major operand (block = half, row = m)
-        {
-            const uint32_t base = sbase + OFF_ST + half * 16384;
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                st_shared_v4(base + sw128_off(row, ch * 16), pack_bf16(s_reg[8 * ch + 0], s_reg[8 * ch + 1]),
-                             pack_bf16(s_reg[8 * ch + 2], s_reg[8 * ch + 3]),
-                             pack_bf16(s_reg[8 * ch + 4], s_reg[8 * ch + 5]),
-                             pack_bf16(s_reg[8 * ch + 6], s_reg[8 * ch + 7]));
-            }
-        }
-
-        // ---- wait for this chunk's q/k/v tiles
-        if (!mbar_wait_bounded(bar_full0 + 8 * st, (c >> 1) & 1, kWaitLimit)) sm.abort = 1;
-
-        // ---- (3) ||k_i||^2: 4 threads per key row, 32 channels each
+        wait(bar_full0 + 8 * (c & 1), (c >> 1) & 1);
+        // ||k_i||^2: 4 threads per key row, 32 channels each
         float n2 = 0.f;
         {
             const int i = tid >> 2, part = tid & 3;
@@ -248,19 +269,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             n2 += __shfl_xor_sync(0xffffffffu, n2, 1);
             n2 += __shfl_xor_sync(0xffffffffu, n2, 2);
         }
-        __syncthreads();   // #1: G, eta visible
-        if (sm.abort) break;
-        if ((tid & 3) == 0) {
-            const int i = tid >> 2;
-            const float G = sm.G[i];
-            sm.beta[i] = kla_beta(sm.eta[i], n2, p.eps);
-            sm.expG[i] = __expf(G);
-            sm.expEnd[i] = __expf(sm.G[kC - 1] - G);
-        }
-        fence_proxy_async_smem();   // S^T tile -> tensor core
-        __syncthreads();            // #2
-
-        // ---- (4) [K;Q] K^T and S^T Q^T
+        __syncthreads();   // eta of this chunk visible
+        if ((tid & 3) == 0) cv.beta[tid >> 2] = kla_beta(cv.eta[tid >> 2], n2, p.eps);
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
@@ -268,173 +278,237 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
                 mma_bf16(tbase + TM_A, sw128_desc(qk + off, 16, 1024), sw128_desc(qk + off, 16, 1024), id_qk, s);
             }
+            mma_commit(bar_A);
+        }
+    };
+
+    // (b) R and A from [KK^T; QK^T]; T = (I + R)^{-1}; T_K, T_V; issue W^T, U^T.
+    auto intra_mid = [&](int c) {
+        ChunkVec &cv = sm.v[c & 1];
+        wait(bar_A, c & 1);
+        tc_fence_after();
+        {
+            uint32_t v[32];
+            tmem_ld32(tlane + TM_A + 32 * half, v);
+            tmem_ld_wait();
+            const int i = row & (kC - 1);
+            const bool key_row = row < kC;
+            const float Gi = cv.G[i], ei = cv.eG[i];
+            const float scale = key_row ? cv.beta[i] : 1.f;
+            const bool safe = cv.safe != 0;
+            float x[32];
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+                const int j = 32 * half + jj;
+                const float dcy = safe ? ei * cv.enG[j] : __expf(Gi - cv.G[j]);
+                const bool keep = key_row ? (j < i) : (j <= i);
+                x[jj] = keep ? scale * dcy * __uint_as_float(v[jj]) : 0.f;
+            }
+            if (key_row) {
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4)
+                    st_v4_f32(Rm + fidx(i, 32 * half + 4 * q4), x[4 * q4], x[4 * q4 + 1], x[4 * q4 + 2],
+                              x[4 * q4 + 3]);
+            } else {
+                const uint32_t base = aqk_of(c);
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) st_bf16x8(base + sw128_off(i, half * 64 + ch * 16), x + 8 * ch);
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        // ---- diagonal 16x16 blocks: right-looking substitution, lane = column (warps 0-1)
+        if (warp < 2) {
+            const int o = 16 * (2 * warp + (lane >> 4));
+            const int l = lane & 15;
+            float acc[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i] = (i == l) ? 1.f : 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float xj = acc[j];
+#pragma unroll
+                for (int i = j + 1; i < 16; ++i) acc[i] = fmaf(-Rm[fidx(o + i, o + j)], xj, acc[i]);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) Tm[fidx(o + i, o + l)] = acc[i];
+        }
+        __syncthreads();
+        // ---- merge 16 -> 32: T_{2p+1,2p} = -T_{2p+1,2p+1} (R_{2p+1,2p} T_{2p,2p}) (warps 0-3, tf32 mma)
+        if (warp < 4) {
+            const int pp = warp >> 1, nt = warp & 1;
+            const int r0 = 16 * (2 * pp + 1), c0 = 16 * (2 * pp);
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                const uint32_t a[4] = {to_tf32(Rm[fidx(r0 + g8, c0 + 8 * ks + t4)]),
+                                       to_tf32(Rm[fidx(r0 + g8 + 8, c0 + 8 * ks + t4)]),
+                                       to_tf32(Rm[fidx(r0 + g8, c0 + 8 * ks + t4 + 4)]),
+                                       to_tf32(Rm[fidx(r0 + g8 + 8, c0 + 8 * ks + t4 + 4)])};
+                const uint32_t bb[2] = {to_tf32(Tm[fidx(c0 + 8 * ks + t4, c0 + 8 * nt + g8)]),
+                                        to_tf32(Tm[fidx(c0 + 8 * ks + t4 + 4, c0 + 8 * nt + g8)])};
+                mma_tf32_16x8x8(d, a, bb);
+            }
+            float *X = Xs + warp * 128;   // 16 x 8, row stride 8
+            X[g8 * 8 + 2 * t4] = d[0];
+            X[g8 * 8 + 2 * t4 + 1] = d[1];
+            X[(g8 + 8) * 8 + 2 * t4] = d[2];
+            X[(g8 + 8) * 8 + 2 * t4 + 1] = d[3];
+            __syncwarp();
+            float e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                const uint32_t a[4] = {to_tf32(Tm[fidx(r0 + g8, r0 + 8 * ks + t4)]),
+                                       to_tf32(Tm[fidx(r0 + g8 + 8, r0 + 8 * ks + t4)]),
+                                       to_tf32(Tm[fidx(r0 + g8, r0 + 8 * ks + t4 + 4)]),
+                                       to_tf32(Tm[fidx(r0 + g8 + 8, r0 + 8 * ks + t4 + 4)])};
+                const uint32_t bb[2] = {to_tf32(X[(8 * ks + t4) * 8 + g8]), to_tf32(X[(8 * ks + t4 + 4) * 8 + g8])};
+                mma_tf32_16x8x8(e, a, bb);
+            }
+            const int cc = c0 + 8 * nt + 2 * t4;
+            Tm[fidx(r0 + g8, cc)] = -e[0];
+            Tm[fidx(r0 + g8, cc + 1)] = -e[1];
+            Tm[fidx(r0 + g8 + 8, cc)] = -e[2];
+            Tm[fidx(r0 + g8 + 8, cc + 1)] = -e[3];
+        }
+        __syncthreads();
+        // ---- merge 32 -> 64: T_{32:,0:32} = -T_{32:,32:} (R_{32:,0:32} T_{0:32,0:32}) (8 warps)
+        {
+            const int mt = warp >> 2, nt = warp & 3;
+            float *X2 = Xs + 512;   // 32 x 32, row stride 40
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                if (ks < nt) continue;   // T_{0:32,0:32} is lower triangular
+                const int ra = 32 + 16 * mt;
+                const uint32_t a[4] = {to_tf32(Rm[fidx(ra + g8, 8 * ks + t4)]),
+                                       to_tf32(Rm[fidx(ra + g8 + 8, 8 * ks + t4)]),
+                                       to_tf32(Rm[fidx(ra + g8, 8 * ks + t4 + 4)]),
+                                       to_tf32(Rm[fidx(ra + g8 + 8, 8 * ks + t4 + 4)])};
+                const uint32_t bb[2] = {to_tf32(Tm[fidx(8 * ks + t4, 8 * nt + g8)]),
+                                        to_tf32(Tm[fidx(8 * ks + t4 + 4, 8 * nt + g8)])};
+                mma_tf32_16x8x8(d, a, bb);
+            }
+            const int rr = 16 * mt + g8, cc = 8 * nt + 2 * t4;
+            X2[rr * 40 + cc] = d[0];
+            X2[rr * 40 + cc + 1] = d[1];
+            X2[(rr + 8) * 40 + cc] = d[2];
+            X2[(rr + 8) * 40 + cc + 1] = d[3];
+            __syncthreads();
+            float e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                if (ks > 2 * mt + 1) continue;   // T_{32:,32:} is lower triangular
+                const int ra = 32 + 16 * mt;
+                const uint32_t a[4] = {to_tf32(Tm[fidx(ra + g8, 32 + 8 * ks + t4)]),
+                                       to_tf32(Tm[fidx(ra + g8 + 8, 32 + 8 * ks + t4)]),
+                                       to_tf32(Tm[fidx(ra + g8, 32 + 8 * ks + t4 + 4)]),
+                                       to_tf32(Tm[fidx(ra + g8 + 8, 32 + 8 * ks + t4 + 4)])};
+                const uint32_t bb[2] = {to_tf32(X2[(8 * ks + t4) * 40 + 8 * nt + g8]),
+                                        to_tf32(X2[(8 * ks + t4 + 4) * 40 + 8 * nt + g8])};
+                mma_tf32_16x8x8(e, a, bb);
+            }
+            const int ro = 32 + rr;
+            Tm[fidx(ro, cc)] = -e[0];
+            Tm[fidx(ro, cc + 1)] = -e[1];
+            Tm[fidx(ro + 8, cc)] = -e[2];
+            Tm[fidx(ro + 8, cc + 1)] = -e[3];
+        }
+        __syncthreads();
+        // ---- T_K = T diag(beta e^G), T_V = T diag(beta): bf16 K-major (rows n, k contiguous)
+        {
+            const int n = tid >> 2, kq = tid & 3;
+            float tk[16], tv[16];
+#pragma unroll
+            for (int u4 = 0; u4 < 4; ++u4) {
+                const float4 t = *reinterpret_cast<const float4 *>(Tm + fidx(n, 16 * kq + 4 * u4));
+                const float tt[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int k = 16 * kq + 4 * u4 + u;
+                    const float val = (k <= n) ? tt[u] : 0.f;
+                    tv[4 * u4 + u] = val * cv.beta[k];
+                    tk[4 * u4 + u] = tv[4 * u4 + u] * cv.eG[k];
+                }
+            }
+            const uint32_t bk = sbase + OFF_R, bv = sbase + OFF_R + 8192;
+            __syncthreads();   // every R read done before T_K/T_V overwrite it
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const uint32_t off = sw128_off(n, 32 * kq + 16 * hh);
+                st_bf16x8(bk + off, tk + 8 * hh);
+                st_bf16x8(bv + off, tv + 8 * hh);
+            }
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t qk = qk_of(c), vv = v_of(c);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(tbase + TM_W, sw128_desc(qk + s * 2048, 16384, 1024),
+                         sw128_desc(sbase + OFF_R + s * 32, 16, 1024), id_w, s);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(tbase + TM_U, sw128_desc(vv + s * 2048, 8192, 1024),
+                         sw128_desc(sbase + OFF_R + 8192 + s * 32, 16, 1024), id_w, s);
+            mma_commit(bar_W);
+        }
+    };
+
+    // (c) W^T -> bf16 MN-major B operand (rows k, 64 tokens per row), into the T area.
+    auto intra_back = [&](int c) {
+        wait(bar_W, c & 1);
+        tc_fence_after();
+        uint32_t v[32];
+        tmem_ld32(tlane + TM_W + 32 * half, v);
+        tmem_ld_wait();
+        const uint32_t base = sbase + OFF_WT;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch)
+            st_shared_v4(base + sw128_off(row, half * 64 + ch * 16),
+                         pack_bf16(__uint_as_float(v[8 * ch]), __uint_as_float(v[8 * ch + 1])),
+                         pack_bf16(__uint_as_float(v[8 * ch + 2]), __uint_as_float(v[8 * ch + 3])),
+                         pack_bf16(__uint_as_float(v[8 * ch + 4]), __uint_as_float(v[8 * ch + 5])),
+                         pack_bf16(__uint_as_float(v[8 * ch + 6]), __uint_as_float(v[8 * ch + 7])));
+        fence_proxy_async_smem();
+        tc_fence_before();
+    };
+
+    // ============================================================ state-dependent work
+    // (d) S^T -> bf16 operand; issue S^T W^T and S^T Q^T.
+    auto inter_issue1 = [&](int c) {
+        if (tid == 0) tma_store_wait_read_all();   // the previous output staging is free again
+        const uint32_t base = sbase + OFF_ST + half * 16384;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) st_bf16x8(base + sw128_off(row, ch * 16), s_reg + 8 * ch);
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t qk = qk_of(c);
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const uint32_t aoff = (s >> 2) * 16384 + (s & 3) * 32;
+                mma_bf16(tbase + TM_1A, sw128_desc(sbase + OFF_ST + aoff, 16, 1024),
+                         sw128_desc(sbase + OFF_WT + s * 2048, 16384, 1024), id_1a, s);
+            }
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
                 const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
                 mma_bf16(tbase + TM_1B, sw128_desc(sbase + OFF_ST + off, 16, 1024),
                          sw128_desc(qk + 8192 + off, 16, 1024), id_qk, s);
             }
-            mma_commit(bar_A);
-        }
-        if (!mbar_wait_bounded(bar_A, ph, kWaitLimit)) sm.abort = 1;
-        tc_fence_after();
-
-        // ---- (5) R (key rows) and A (query rows)
-        {
-            uint32_t v[32];
-            tmem_ld32(tlane + TM_A + 32 * half, v);
-            tmem_ld_wait();
-            if (row < kC) {
-                const int i = row;
-                const float Gi = sm.G[i], bi = sm.beta[i];
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int j = 32 * half + jj;
-                    const float r = (j < i) ? bi * __expf(Gi - sm.G[j]) * __uint_as_float(v[jj]) : 0.f;
-                    Rm[i * 65 + j] = r;
-                }
-            } else {
-                const int i = row - kC;
-                const float Gi = sm.G[i];
-                float a[32];
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int j = 32 * half + jj;
-                    a[jj] = (j <= i) ? __expf(Gi - sm.G[j]) * __uint_as_float(v[jj]) : 0.f;
-                }
-                const uint32_t base = sbase + OFF_AQK;
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch)
-                    st_shared_v4(base + sw128_off(i, half * 64 + ch * 16), pack_bf16(a[8 * ch], a[8 * ch + 1]),
-                                 pack_bf16(a[8 * ch + 2], a[8 * ch + 3]), pack_bf16(a[8 * ch + 4], a[8 * ch + 5]),
-                                 pack_bf16(a[8 * ch + 6], a[8 * ch + 7]));
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();   // #3
-        if (sm.abort) break;
-
-        // ---- (6) T = (I + R)^{-1}, fp32. Diagonal 16x16 blocks by substitution (warps 0-3).
-        if (warp < 4 && lane < 16) {
-            const int o = 16 * warp;
-            float x[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float acc = (i == lane) ? 1.f : 0.f;
-#pragma unroll
-                for (int j = 0; j < i; ++j) acc = fmaf(-Rm[(o + i) * 65 + o + j], x[j], acc);
-                x[i] = acc;
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) Tm[(o + i) * 65 + o + lane] = x[i];
-        }
-        __syncthreads();
-        // Off-diagonal blocks, by distance d from the diagonal:
-        //   X_ba = sum_{x=a}^{b-1} R_bx T_xa ;  T_ba = -T_bb X_ba
-#pragma unroll 1
-        for (int d = 1; d < 4; ++d) {
-            const int nblk = 4 - d;
-            for (int idx = tid; idx < nblk * 256; idx += kThreads) {
-                const int blk = idx >> 8, i = (idx >> 4) & 15, j = idx & 15;
-                const int bb = blk + d, aa = blk;
-                float acc = 0.f;
-                for (int x = aa; x < bb; ++x)
-#pragma unroll
-                    for (int u = 0; u < 16; ++u)
-                        acc = fmaf(Rm[(16 * bb + i) * 65 + 16 * x + u], Tm[(16 * x + u) * 65 + 16 * aa + j], acc);
-                Xs[idx] = acc;
-            }
-            __syncthreads();
-            for (int idx = tid; idx < nblk * 256; idx += kThreads) {
-                const int blk = idx >> 8, i = (idx >> 4) & 15, j = idx & 15;
-                const int bb = blk + d, aa = blk;
-                float acc = 0.f;
-#pragma unroll
-                for (int u = 0; u < 16; ++u)
-                    if (u <= i) acc = fmaf(Tm[(16 * bb + i) * 65 + 16 * bb + u], Xs[(blk << 8) + (u << 4) + j], acc);
-                Tm[(16 * bb + i) * 65 + 16 * aa + j] = -acc;
-            }
-            __syncthreads();
-        }
-
-        // ---- (7) T_K = T diag(beta e^G), T_V = T diag(beta): bf16 K-major (rows n, k contiguous)
-        {
-            const int n = tid >> 2, kq = tid & 3;
-            float tk[16], tv[16];
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int k = 16 * kq + u;
-                const float t = (k <= n) ? Tm[n * 65 + k] : 0.f;
-                tv[u] = t * sm.beta[k];
-                tk[u] = tv[u] * sm.expG[k];
-            }
-            const uint32_t bk = sbase + OFF_X, bv = sbase + OFF_X + 8192;
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const uint32_t off = sw128_off(n, 32 * kq + 16 * hh);
-                const float *a = tk + 8 * hh, *e = tv + 8 * hh;
-                st_shared_v4(bk + off, pack_bf16(a[0], a[1]), pack_bf16(a[2], a[3]), pack_bf16(a[4], a[5]),
-                             pack_bf16(a[6], a[7]));
-                st_shared_v4(bv + off, pack_bf16(e[0], e[1]), pack_bf16(e[2], e[3]), pack_bf16(e[4], e[5]),
-                             pack_bf16(e[6], e[7]));
-            }
-        }
-        fence_proxy_async_smem();
-        __syncthreads();
-
-        // ---- (8) W^T = K^T T_K^T, U^T = V^T T_V^T
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                mma_bf16(tbase + TM_W, sw128_desc(qk + s * 2048, 16384, 1024),
-                         sw128_desc(sbase + OFF_X + s * 32, 16, 1024), id_w, s);
-            }
-#pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                mma_bf16(tbase + TM_U, sw128_desc(vv + s * 2048, 8192, 1024),
-                         sw128_desc(sbase + OFF_X + 8192 + s * 32, 16, 1024), id_w, s);
-            }
-            mma_commit(bar_W);
-        }
-        if (!mbar_wait_bounded(bar_W, ph, kWaitLimit)) sm.abort = 1;
-        tc_fence_after();
-
-        // ---- (9) W^T -> bf16, MN-major B operand (rows k, 64 tokens per row)
-        {
-            uint32_t v[32];
-            tmem_ld32(tlane + TM_W + 32 * half, v);
-            tmem_ld_wait();
-            const uint32_t base = sbase + OFF_Y;
-#pragma unroll
-            for (int ch = 0; ch < 4; ++ch)
-                st_shared_v4(base + sw128_off(row, half * 64 + ch * 16),
-                             pack_bf16(__uint_as_float(v[8 * ch]), __uint_as_float(v[8 * ch + 1])),
-                             pack_bf16(__uint_as_float(v[8 * ch + 2]), __uint_as_float(v[8 * ch + 3])),
-                             pack_bf16(__uint_as_float(v[8 * ch + 4]), __uint_as_float(v[8 * ch + 5])),
-                             pack_bf16(__uint_as_float(v[8 * ch + 6]), __uint_as_float(v[8 * ch + 7])));
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (sm.abort) break;
-
-        // ---- (10) (W S)^T = S^T W^T
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint32_t aoff = (s >> 2) * 16384 + (s & 3) * 32;
-                mma_bf16(tbase + TM_1A, sw128_desc(sbase + OFF_ST + aoff, 16, 1024),
-                         sw128_desc(sbase + OFF_Y + s * 2048, 16384, 1024), id_1a, s);
-            }
             mma_commit(bar_1);
         }
-        if (!mbar_wait_bounded(bar_1, ph, kWaitLimit)) sm.abort = 1;
-        tc_fence_after();
+    };
 
-        // ---- (11) E^T = U^T - (W S)^T, and E^T diag(e^{G_end - G})
+    // (e) E^T = U^T - (W S)^T and E^T diag(e^{G_end-G}); issue E^T_s K and E^T A^T.
+    auto inter_issue2 = [&](int c) {
+        const ChunkVec &cv = sm.v[c & 1];
+        wait(bar_1, c & 1);
+        tc_fence_after();
         {
             uint32_t u[32], w[32];
             tmem_ld32(tlane + TM_U + 32 * half, u);
@@ -444,27 +518,21 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) {
                 e[jj] = __uint_as_float(u[jj]) - __uint_as_float(w[jj]);
-                es[jj] = e[jj] * sm.expEnd[32 * half + jj];
+                es[jj] = e[jj] * cv.eEnd[32 * half + jj];
             }
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {
                 const uint32_t off = sw128_off(row, half * 64 + ch * 16);
-                st_shared_v4(sbase + OFF_ET + off, pack_bf16(e[8 * ch], e[8 * ch + 1]),
-                             pack_bf16(e[8 * ch + 2], e[8 * ch + 3]), pack_bf16(e[8 * ch + 4], e[8 * ch + 5]),
-                             pack_bf16(e[8 * ch + 6], e[8 * ch + 7]));
-                st_shared_v4(sbase + OFF_ETS + off, pack_bf16(es[8 * ch], es[8 * ch + 1]),
-                             pack_bf16(es[8 * ch + 2], es[8 * ch + 3]), pack_bf16(es[8 * ch + 4], es[8 * ch + 5]),
-                             pack_bf16(es[8 * ch + 6], es[8 * ch + 7]));
+                st_bf16x8(sbase + OFF_ET + off, e + 8 * ch);
+                st_bf16x8(sbase + OFF_ETS + off, es + 8 * ch);
             }
         }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
-        if (sm.abort) break;
-
-        // ---- (12) (K_end^T E)^T = E^T_s K  and  (A E)^T = E^T A^T
         if (tid == 0) {
             tc_fence_after();
+            const uint32_t qk = qk_of(c);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
                 mma_bf16(tbase + TM_2, sw128_desc(sbase + OFF_ETS + s * 32, 16, 1024),
@@ -472,15 +540,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
             for (int s = 0; s < 4; ++s)
                 mma_bf16(tbase + TM_3, sw128_desc(sbase + OFF_ET + s * 32, 16, 1024),
-                         sw128_desc(sbase + OFF_AQK + s * 32, 16, 1024), id_qk, s);
+                         sw128_desc(aqk_of(c) + s * 32, 16, 1024), id_qk, s);
             mma_commit(bar_2);
         }
-        if (!mbar_wait_bounded(bar_2, ph, kWaitLimit)) sm.abort = 1;
-        tc_fence_after();
+    };
 
-        // ---- (13) S^T <- e^{G_end} S^T + (K_end^T E)^T   (fp32, registers)
+    // (f) S^T <- e^{G_end} S^T + (K_end^T E)^T; O^T = e^{G} (Q S)^T + (A E)^T -> TMA store.
+    auto inter_finish = [&](int c) {
+        const ChunkVec &cv = sm.v[c & 1];
+        wait(bar_2, c & 1);
+        tc_fence_after();
         {
-            const float gam = sm.expG[kC - 1];
+            const float gam = cv.eG[kC - 1];
             uint32_t v[32];
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
@@ -491,19 +562,28 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     s_reg[32 * hh + kk] = fmaf(gam, s_reg[32 * hh + kk], __uint_as_float(v[kk]));
             }
         }
-        // ---- (14) O^T = diag-scaled (Q S)^T + (A E)^T -> staging [blk][token][64 ch] for TMA store
         {
             uint32_t qs[32], ae[32];
             tmem_ld32(tlane + TM_1B + 32 * half, qs);
             tmem_ld32(tlane + TM_3 + 32 * half, ae);
             tmem_ld_wait();
-            const int m = row;
-            uint8_t *stg = smem + OFF_ETS + (m >> 6) * 8192 + (m & 63) * 2;
+            float o[32];
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int n = 32 * half + jj;
-                const float o = fmaf(sm.expG[n], __uint_as_float(qs[jj]), __uint_as_float(ae[jj]));
-                *reinterpret_cast<__nv_bfloat16 *>(stg + n * 128) = __float2bfloat16_rn(o);
+            for (int jj = 0; jj < 32; ++jj)
+                o[jj] = fmaf(cv.eG[32 * half + jj], __uint_as_float(qs[jj]), __uint_as_float(ae[jj]));
+            // Pair value channels (m, m^1) so each lane stores 2 channels of 16 tokens as bf16x2:
+            // even lanes keep tokens 0-15 of their half, odd lanes tokens 16-31.
+            const bool odd = lane & 1;
+            const int m0 = row & ~1;
+            uint8_t *stg = smem + OFF_ETS + (m0 >> 6) * 8192 + (m0 & 63) * 2;
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+                const float mine = odd ? o[jj + 16] : o[jj];
+                const float send = odd ? o[jj] : o[jj + 16];
+                const float other = __shfl_xor_sync(0xffffffffu, send, 1);
+                const int n = 32 * half + jj + (odd ? 16 : 0);
+                const uint32_t pr = odd ? pack_bf16(other, mine) : pack_bf16(mine, other);
+                *reinterpret_cast<uint32_t *>(stg + n * 128) = pr;
             }
         }
         fence_proxy_async_smem();
@@ -516,6 +596,22 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tma_store_commit();
             if (c + 2 < nchunks) issue_loads(c + 2);
         }
+    };
+
+    // ================================================================== schedule
+    intra_front(0);
+    intra_mid(0);
+    intra_back(0);
+    __syncthreads();
+    for (int c = 0; c < nchunks && !sm.abort; ++c) {
+        const bool next = c + 1 < nchunks;
+        inter_issue1(c);
+        if (next) intra_front(c + 1);
+        inter_issue2(c);
+        if (next) intra_mid(c + 1);
+        inter_finish(c);
+        if (next) intra_back(c + 1);
+        __syncthreads();
     }
 
     if (sm.abort && tid == 0) atomicOr(p.err, kErrTimeout);
