@@ -21,17 +21,20 @@
 //   E^T_s K              -> (K_end^T E)^T                  M=128 N=128 K=64
 //   E^T A^T              -> (A E)^T                        M=128 N=64  K=64
 // Operands are bf16 in 128-byte-swizzled shared memory (q/k/v tiles arrive by TMA, derived
-// tiles are written by the threads), accumulators are fp32 in tensor memory. The state S^T
-// lives in registers in fp32 (thread = one value channel, 64 key channels) and is rounded to
-// bf16 only as an MMA operand, never as the carried state.
+// tiles are written by the threads), accumulators are fp32 in tensor memory.
 //
-// The 64 x 64 unit-lower inverse T is built in fp32: the four 16 x 16 diagonal blocks by
-// substitution, then two levels of block merging (16 -> 32 -> 64) whose 16x8 products run as
-// warp-level tf32 MMAs.
-//
-// Schedule: the work of chunk c that depends on the carried state (S^T W^T, E, E^T K, the state
-// update and the output) is interleaved with the state-independent work of chunk c+1 (norms,
-// [K;Q]K^T, R, A, the solve, W^T, U^T), so the tensor cores and the CUDA cores overlap.
+// Two warp groups share the SM:
+//  * state group (warps 0-7): owns S^T in fp32 registers (thread = one value channel, 64 key
+//    channels) and runs the chain of chunk c: S^T W^T and S^T Q^T, E, E^T K and E^T A^T, the
+//    state update, the output tile and its TMA store;
+//  * operand group (warps 8-15): meanwhile builds the state-independent operands of chunk
+//    c+1: gates, norms, [K;Q] K^T, R and A, T = (I + R)^{-1}, W^T and U^T.
+// The 64 x 64 unit-lower inverse T is computed in fp32: 16 x 16 diagonal blocks by
+// substitution, then two levels of block merging (16 -> 32 -> 64) on warp-level tf32 MMAs.
+// The groups hand over through mbarriers that alternate strictly (no wait can alias a phase
+// two steps back): `ready` (operands of chunk c are complete), `freed` (the state group has
+// consumed the single-buffered W^T tile and U^T of chunk c), `done[c&1]` (chunk c is fully
+// retired: its A tile, gate vectors and q/k/v stage may be reused).
 #include <cuda.h>
 
 #include <algorithm>
@@ -46,7 +49,9 @@ using namespace ptx;
 
 constexpr int kC = 64;          // chunk
 constexpr int kD = 128;         // d_k = d_v
-constexpr int kThreads = 256;
+constexpr int kGroup = 256;     // threads per warp group
+constexpr int kThreads = 2 * kGroup;
+constexpr uint32_t kBarState = 1, kBarOperand = 2;   // named barriers of the two groups
 constexpr float kMinLogGate = -80.0f;
 constexpr float kSafeDecay = -80.0f;   // chunk decay above which e^{-G_j} is representable
 constexpr uint32_t kWaitLimit = 1u << 24;
@@ -90,8 +95,10 @@ struct ChunkVec {          // per-chunk vectors (double-buffered by chunk parity
 };
 struct Small {
     ChunkVec v[2];
-    uint64_t full[2];
-    uint64_t mA, mW, m1, m2;
+    uint64_t full[2];              // q/k/v stage landed (TMA)
+    uint64_t mA, mW, m1, m2;       // tcgen05.commit of the four MMA groups
+    uint64_t ready, freed;         // operand group -> state group, state group -> operand group
+    uint64_t done[2];              // chunk retired, by parity
     uint32_t tmem_base;
     volatile int abort;
 };
@@ -118,6 +125,12 @@ __device__ __forceinline__ void st_v4_f32(float *p, float a, float b, float c, f
 __device__ __forceinline__ void st_bf16x8(uint32_t addr, const float *x) {
     st_shared_v4(addr, pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
 }
+__device__ __forceinline__ void st_bf16x8u(uint32_t addr, const uint32_t *x) {
+    st_shared_v4(addr, pack_bf16(__uint_as_float(x[0]), __uint_as_float(x[1])),
+                 pack_bf16(__uint_as_float(x[2]), __uint_as_float(x[3])),
+                 pack_bf16(__uint_as_float(x[4]), __uint_as_float(x[5])),
+                 pack_bf16(__uint_as_float(x[6]), __uint_as_float(x[7])));
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -130,11 +143,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     float *Rm = reinterpret_cast<float *>(smem + OFF_R);    // R, swizzled fp32 [64][64]
     float *Tm = reinterpret_cast<float *>(smem + OFF_WT);   // T, swizzled fp32 [64][64]
     float *Xs = reinterpret_cast<float *>(smem + OFF_XS);   // solve scratch
+    __shared__ int abort_snap[2];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, half = warp >> 2;
-    const int row = quarter * 32 + lane;        // TMEM lane of this thread
-    const int g8 = lane >> 2, t4 = lane & 3;     // mma.sync fragment coordinates
+    const int grp = warp >> 3;                  // 0: state group, 1: operand group
+    const int gw = warp & 7, gtid = tid & (kGroup - 1);
+    const int half = gw >> 2;
+    const int row = (warp & 3) * 32 + lane;     // TMEM lane of this thread
+    const int g8 = lane >> 2, t4 = lane & 3;    // mma.sync fragment coordinates
     const int bh = blockIdx.x;
     const int b = bh / p.H, h = bh % p.H;
     const int nchunks = (p.T + kC - 1) / kC;
@@ -142,6 +158,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t bar_full0 = smem_u32(&sm.full[0]);
     const uint32_t bar_A = smem_u32(&sm.mA), bar_W = smem_u32(&sm.mW);
     const uint32_t bar_1 = smem_u32(&sm.m1), bar_2 = smem_u32(&sm.m2);
+    const uint32_t bar_ready = smem_u32(&sm.ready), bar_freed = smem_u32(&sm.freed);
+    const uint32_t bar_done0 = smem_u32(&sm.done[0]);
 
     if (tid == 0) {
         mbar_init(bar_full0, 1);
@@ -150,7 +168,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_init(bar_W, 1);
         mbar_init(bar_1, 1);
         mbar_init(bar_2, 1);
+        mbar_init(bar_ready, 1);
+        mbar_init(bar_freed, 1);
+        mbar_init(bar_done0, 1);
+        mbar_init(bar_done0 + 8, 1);
         sm.abort = 0;
+        abort_snap[0] = abort_snap[1] = 0;
         fence_mbar_init();
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
@@ -165,7 +188,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = sm.tmem_base;
-    const uint32_t tlane = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t tlane = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);
 
     const uint32_t id_qk = idesc_bf16(128, 64, 0, 0);     // K-major x K-major, N=64
     const uint32_t id_w = idesc_bf16(128, 64, 1, 0);      // MN-major A, K-major B
@@ -176,7 +199,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     auto v_of = [&](int c) { return sbase + OFF_V + (c & 1) * V_STAGE; };
     auto aqk_of = [&](int c) { return sbase + OFF_AQK + (c & 1) * 8192; };
 
-    auto issue_loads = [&](int c) {   // thread 0 only
+    auto issue_loads = [&](int c) {   // one thread
         const uint32_t bar = bar_full0 + 8 * (c & 1);
         const uint32_t qk = qk_of(c), vv = v_of(c);
         mbar_arrive_expect_tx(bar, kTileBytes);
@@ -191,24 +214,25 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     auto wait = [&](uint32_t bar, uint32_t parity) {
         if (!mbar_wait_bounded(bar, parity, kWaitLimit)) sm.abort = 1;
     };
+    const uint32_t gbar = grp == 0 ? kBarState : kBarOperand;
+    auto gsync = [&]() { named_sync(gbar, kGroup); };
+    // Uniform per-group abort decision: one thread snapshots the flag before a group barrier.
+    auto group_aborted = [&]() {
+        if (gtid == 0) abort_snap[grp] = sm.abort;
+        gsync();
+        return abort_snap[grp] != 0;
+    };
 
     if (tid == 0) {
         issue_loads(0);
         if (nchunks > 1) issue_loads(1);
     }
 
-    // State S^T: this thread owns value channel m = row, key channels [64*half, 64*half + 64).
-    float s_reg[64];
-    {
-        const float *S0 = p.S0 ? p.S0 + static_cast<size_t>(bh) * kD * kD : nullptr;
-#pragma unroll
-        for (int kk = 0; kk < 64; ++kk) s_reg[kk] = S0 ? S0[(64 * half + kk) * kD + row] : 0.f;
-    }
-
-    // Gates of the next chunk to be prepared, prefetched by warp 0 (two tokens per lane).
+    // ===================================================================== operand group
+    // Gates of the next chunk to be prepared, prefetched by the group's first warp.
     float a_nx[2] = {1.f, 1.f}, e_nx[2] = {0.f, 0.f};
     auto load_gates = [&](int c) {
-        if (warp == 0 && c < nchunks) {
+        if (grp == 1 && gw == 0 && c < nchunks) {
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int t = c * kC + 2 * lane + u;
@@ -219,14 +243,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
         }
     };
-    load_gates(0);
 
-    // =========================================================== state-independent work
     // (a) gates, norms, beta and the decay tables; issue [K;Q] K^T.
-    auto intra_front = [&](int c) {
+    auto op_front = [&](int c) {
         ChunkVec &cv = sm.v[c & 1];
         const uint32_t qk = qk_of(c);
-        if (warp == 0) {
+        if (c >= 2) wait(bar_done0 + 8 * (c & 1), ((c - 2) >> 1) & 1);   // chunk c-2 retired
+        if (gw == 0) {
             const float g0 = fmaxf(__logf(a_nx[0]), kMinLogGate), g1 = fmaxf(__logf(a_nx[1]), kMinLogGate);
             float s = g0 + g1;
 #pragma unroll
@@ -253,7 +276,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // ||k_i||^2: 4 threads per key row, 32 channels each
         float n2 = 0.f;
         {
-            const int i = tid >> 2, part = tid & 3;
+            const int i = gtid >> 2, part = gtid & 3;
             const uint32_t base = qk + (part >> 1) * 16384;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -269,9 +292,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             n2 += __shfl_xor_sync(0xffffffffu, n2, 1);
             n2 += __shfl_xor_sync(0xffffffffu, n2, 2);
         }
-        __syncthreads();   // eta of this chunk visible
-        if ((tid & 3) == 0) cv.beta[tid >> 2] = kla_beta(cv.eta[tid >> 2], n2, p.eps);
-        if (tid == 0) {
+        gsync();   // eta of this chunk visible
+        if ((gtid & 3) == 0) cv.beta[gtid >> 2] = kla_beta(cv.eta[gtid >> 2], n2, p.eps);
+        if (gtid == 0) {
             tc_fence_after();
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
@@ -283,8 +306,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     };
 
     // (b) R and A from [KK^T; QK^T]; T = (I + R)^{-1}; T_K, T_V; issue W^T, U^T.
-    auto intra_mid = [&](int c) {
+    auto op_mid = [&](int c) {
         ChunkVec &cv = sm.v[c & 1];
+        gsync();   // beta of this chunk visible
         wait(bar_A, c & 1);
         tc_fence_after();
         {
@@ -293,16 +317,29 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tmem_ld_wait();
             const int i = row & (kC - 1);
             const bool key_row = row < kC;
-            const float Gi = cv.G[i], ei = cv.eG[i];
             const float scale = key_row ? cv.beta[i] : 1.f;
-            const bool safe = cv.safe != 0;
             float x[32];
+            if (cv.safe) {
+                const float ei = cv.eG[i] * scale;
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int j = 32 * half + jj;
-                const float dcy = safe ? ei * cv.enG[j] : __expf(Gi - cv.G[j]);
-                const bool keep = key_row ? (j < i) : (j <= i);
-                x[jj] = keep ? scale * dcy * __uint_as_float(v[jj]) : 0.f;
+                for (int q4 = 0; q4 < 8; ++q4) {
+                    const float4 en = *reinterpret_cast<const float4 *>(&cv.enG[32 * half + 4 * q4]);
+                    const float e4[4] = {en.x, en.y, en.z, en.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int jj = 4 * q4 + u, j = 32 * half + jj;
+                        const bool keep = key_row ? (j < i) : (j <= i);
+                        x[jj] = keep ? ei * e4[u] * __uint_as_float(v[jj]) : 0.f;
+                    }
+                }
+            } else {
+                const float Gi = cv.G[i];
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int j = 32 * half + jj;
+                    const bool keep = key_row ? (j < i) : (j <= i);
+                    x[jj] = keep ? scale * __expf(Gi - cv.G[j]) * __uint_as_float(v[jj]) : 0.f;
+                }
             }
             if (key_row) {
 #pragma unroll
@@ -315,28 +352,53 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 for (int ch = 0; ch < 4; ++ch) st_bf16x8(base + sw128_off(i, half * 64 + ch * 16), x + 8 * ch);
             }
         }
+        fence_proxy_async_smem();
         tc_fence_before();
-        __syncthreads();
-        // ---- diagonal 16x16 blocks: right-looking substitution, lane = column (warps 0-1)
-        if (warp < 2) {
-            const int o = 16 * (2 * warp + (lane >> 4));
-            const int l = lane & 15;
-            float acc[16];
+        // The W^T tile area (T lives there during the solve) and U^T are single-buffered: wait
+        // until the state group has consumed those of chunk c-1.
+        if (c >= 1) wait(bar_freed, (c - 1) & 1);
+        gsync();
+        // ---- diagonal 16x16 blocks (one per warp pair): right-looking substitution in steps of
+        // 4 rows. Lane = (row group r4 = lane / 8, column l = 8 (warp & 1) + lane % 8); the lanes of
+        // row group jb finalise their 4 rows, broadcast them by shuffle, and the lanes below update.
+        {
+            const int o = 16 * (gw >> 1);
+            const int l = 8 * (gw & 1) + (lane & 7), r4 = lane >> 3;
+            float acc[4];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) acc[i] = (i == l) ? 1.f : 0.f;
+            for (int u = 0; u < 4; ++u) acc[u] = (4 * r4 + u == l) ? 1.f : 0.f;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float xj = acc[j];
+            for (int jb = 0; jb < 4; ++jb) {
+                if (r4 == jb) {   // 4 x 4 substitution on the diagonal sub-block
 #pragma unroll
-                for (int i = j + 1; i < 16; ++i) acc[i] = fmaf(-Rm[fidx(o + i, o + j)], xj, acc[i]);
+                    for (int u = 1; u < 4; ++u) {
+                        const float4 rr = *reinterpret_cast<const float4 *>(Rm + fidx(o + 4 * jb + u, o + 4 * jb));
+                        const float rv[4] = {rr.x, rr.y, rr.z, rr.w};
+#pragma unroll
+                        for (int v2 = 0; v2 < u; ++v2) acc[u] = fmaf(-rv[v2], acc[v2], acc[u]);
+                    }
+                }
+                float xb[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) xb[u] = __shfl_sync(0xffffffffu, acc[u], jb * 8 + (lane & 7));
+                if (r4 > jb) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float4 rr = *reinterpret_cast<const float4 *>(Rm + fidx(o + 4 * r4 + u, o + 4 * jb));
+                        acc[u] = fmaf(-rr.x, xb[0], acc[u]);
+                        acc[u] = fmaf(-rr.y, xb[1], acc[u]);
+                        acc[u] = fmaf(-rr.z, xb[2], acc[u]);
+                        acc[u] = fmaf(-rr.w, xb[3], acc[u]);
+                    }
+                }
             }
 #pragma unroll
-            for (int i = 0; i < 16; ++i) Tm[fidx(o + i, o + l)] = acc[i];
+            for (int u = 0; u < 4; ++u) Tm[fidx(o + 4 * r4 + u, o + l)] = acc[u];
         }
-        __syncthreads();
+        gsync();
         // ---- merge 16 -> 32: T_{2p+1,2p} = -T_{2p+1,2p+1} (R_{2p+1,2p} T_{2p,2p}) (warps 0-3, tf32 mma)
-        if (warp < 4) {
-            const int pp = warp >> 1, nt = warp & 1;
+        if (gw < 4) {
+            const int pp = gw >> 1, nt = gw & 1;
             const int r0 = 16 * (2 * pp + 1), c0 = 16 * (2 * pp);
             float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -349,7 +411,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                         to_tf32(Tm[fidx(c0 + 8 * ks + t4 + 4, c0 + 8 * nt + g8)])};
                 mma_tf32_16x8x8(d, a, bb);
             }
-            float *X = Xs + warp * 128;   // 16 x 8, row stride 8
+            float *X = Xs + gw * 128;   // 16 x 8, row stride 8
             X[g8 * 8 + 2 * t4] = d[0];
             X[g8 * 8 + 2 * t4 + 1] = d[1];
             X[(g8 + 8) * 8 + 2 * t4] = d[2];
@@ -371,10 +433,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             Tm[fidx(r0 + g8 + 8, cc)] = -e[2];
             Tm[fidx(r0 + g8 + 8, cc + 1)] = -e[3];
         }
-        __syncthreads();
+        gsync();
         // ---- merge 32 -> 64: T_{32:,0:32} = -T_{32:,32:} (R_{32:,0:32} T_{0:32,0:32}) (8 warps)
         {
-            const int mt = warp >> 2, nt = warp & 3;
+            const int mt = gw >> 2, nt = gw & 3;
             float *X2 = Xs + 512;   // 32 x 32, row stride 40
             float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -394,7 +456,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             X2[rr * 40 + cc + 1] = d[1];
             X2[(rr + 8) * 40 + cc] = d[2];
             X2[(rr + 8) * 40 + cc + 1] = d[3];
-            __syncthreads();
+            gsync();
             float e[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
@@ -414,25 +476,28 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             Tm[fidx(ro + 8, cc)] = -e[2];
             Tm[fidx(ro + 8, cc + 1)] = -e[3];
         }
-        __syncthreads();
+        gsync();
         // ---- T_K = T diag(beta e^G), T_V = T diag(beta): bf16 K-major (rows n, k contiguous)
         {
-            const int n = tid >> 2, kq = tid & 3;
+            const int n = gtid >> 2, kq = gtid & 3;
             float tk[16], tv[16];
 #pragma unroll
             for (int u4 = 0; u4 < 4; ++u4) {
-                const float4 t = *reinterpret_cast<const float4 *>(Tm + fidx(n, 16 * kq + 4 * u4));
-                const float tt[4] = {t.x, t.y, t.z, t.w};
+                const int k0 = 16 * kq + 4 * u4;
+                const float4 t = *reinterpret_cast<const float4 *>(Tm + fidx(n, k0));
+                const float4 bt = *reinterpret_cast<const float4 *>(&cv.beta[k0]);
+                const float4 eg = *reinterpret_cast<const float4 *>(&cv.eG[k0]);
+                const float tt[4] = {t.x, t.y, t.z, t.w}, b4[4] = {bt.x, bt.y, bt.z, bt.w};
+                const float g4[4] = {eg.x, eg.y, eg.z, eg.w};
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const int k = 16 * kq + 4 * u4 + u;
-                    const float val = (k <= n) ? tt[u] : 0.f;
-                    tv[4 * u4 + u] = val * cv.beta[k];
-                    tk[4 * u4 + u] = tv[4 * u4 + u] * cv.eG[k];
+                    const float val = (k0 + u <= n) ? tt[u] : 0.f;
+                    tv[4 * u4 + u] = val * b4[u];
+                    tk[4 * u4 + u] = tv[4 * u4 + u] * g4[u];
                 }
             }
             const uint32_t bk = sbase + OFF_R, bv = sbase + OFF_R + 8192;
-            __syncthreads();   // every R read done before T_K/T_V overwrite it
+            gsync();   // every R read done before T_K/T_V overwrite it
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const uint32_t off = sw128_off(n, 32 * kq + 16 * hh);
@@ -441,8 +506,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
         }
         fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0) {
+        gsync();
+        if (gtid == 0) {
             tc_fence_after();
             const uint32_t qk = qk_of(c), vv = v_of(c);
 #pragma unroll
@@ -457,8 +522,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
     };
 
-    // (c) W^T -> bf16 MN-major B operand (rows k, 64 tokens per row), into the T area.
-    auto intra_back = [&](int c) {
+    // (c) W^T -> bf16 MN-major B operand (rows k, 64 tokens per row) over the T area; then
+    // hand chunk c to the state group.
+    auto op_back = [&](int c) {
         wait(bar_W, c & 1);
         tc_fence_after();
         uint32_t v[32];
@@ -466,26 +532,31 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tmem_ld_wait();
         const uint32_t base = sbase + OFF_WT;
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch)
-            st_shared_v4(base + sw128_off(row, half * 64 + ch * 16),
-                         pack_bf16(__uint_as_float(v[8 * ch]), __uint_as_float(v[8 * ch + 1])),
-                         pack_bf16(__uint_as_float(v[8 * ch + 2]), __uint_as_float(v[8 * ch + 3])),
-                         pack_bf16(__uint_as_float(v[8 * ch + 4]), __uint_as_float(v[8 * ch + 5])),
-                         pack_bf16(__uint_as_float(v[8 * ch + 6]), __uint_as_float(v[8 * ch + 7])));
+        for (int ch = 0; ch < 4; ++ch) st_bf16x8u(base + sw128_off(row, half * 64 + ch * 16), v + 8 * ch);
         fence_proxy_async_smem();
         tc_fence_before();
+        gsync();
+        if (gtid == 0) mbar_arrive(bar_ready);
     };
 
-    // ============================================================ state-dependent work
+    // ======================================================================= state group
+    // S^T: this thread owns value channel m = row, key channels [64*half, 64*half + 64).
+    float s_reg[64];
+    if (grp == 0) {
+        const float *S0 = p.S0 ? p.S0 + static_cast<size_t>(bh) * kD * kD : nullptr;
+#pragma unroll
+        for (int kk = 0; kk < 64; ++kk) s_reg[kk] = S0 ? S0[(64 * half + kk) * kD + row] : 0.f;
+    }
+
     // (d) S^T -> bf16 operand; issue S^T W^T and S^T Q^T.
-    auto inter_issue1 = [&](int c) {
-        if (tid == 0) tma_store_wait_read_all();   // the previous output staging is free again
+    auto st_issue1 = [&](int c) {
         const uint32_t base = sbase + OFF_ST + half * 16384;
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) st_bf16x8(base + sw128_off(row, ch * 16), s_reg + 8 * ch);
         fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0) {
+        if (gtid == 0) tma_store_wait_read_all();   // the previous output staging is free again
+        gsync();
+        if (gtid == 0) {
             tc_fence_after();
             const uint32_t qk = qk_of(c);
 #pragma unroll
@@ -504,33 +575,36 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
     };
 
-    // (e) E^T = U^T - (W S)^T and E^T diag(e^{G_end-G}); issue E^T_s K and E^T A^T.
-    auto inter_issue2 = [&](int c) {
+    // (e) E^T = U^T - (W S)^T and E^T diag(e^{G_end-G}); release W^T and U^T; issue E^T_s K
+    // and E^T A^T.
+    auto st_issue2 = [&](int c) {
         const ChunkVec &cv = sm.v[c & 1];
         wait(bar_1, c & 1);
         tc_fence_after();
-        {
-            uint32_t u[32], w[32];
-            tmem_ld32(tlane + TM_U + 32 * half, u);
-            tmem_ld32(tlane + TM_1A + 32 * half, w);
-            tmem_ld_wait();
-            float e[32], es[32];
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
+        for (int pc = 0; pc < 2; ++pc) {
+            uint32_t u[16], w[16];
+            tmem_ld16(tlane + TM_U + 32 * half + 16 * pc, u);
+            tmem_ld16(tlane + TM_1A + 32 * half + 16 * pc, w);
+            tmem_ld_wait();
+            float e[16], es[16];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
                 e[jj] = __uint_as_float(u[jj]) - __uint_as_float(w[jj]);
-                es[jj] = e[jj] * cv.eEnd[32 * half + jj];
+                es[jj] = e[jj] * cv.eEnd[32 * half + 16 * pc + jj];
             }
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                const uint32_t off = sw128_off(row, half * 64 + ch * 16);
+            for (int ch = 0; ch < 2; ++ch) {
+                const uint32_t off = sw128_off(row, half * 64 + pc * 32 + ch * 16);
                 st_bf16x8(sbase + OFF_ET + off, e + 8 * ch);
                 st_bf16x8(sbase + OFF_ETS + off, es + 8 * ch);
             }
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
+        gsync();
+        if (gtid == 0) {
+            mbar_arrive(bar_freed);   // W^T read by the finished S^T W^T, U^T loaded by every thread
             tc_fence_after();
             const uint32_t qk = qk_of(c);
 #pragma unroll
@@ -545,16 +619,17 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
     };
 
-    // (f) S^T <- e^{G_end} S^T + (K_end^T E)^T; O^T = e^{G} (Q S)^T + (A E)^T -> TMA store.
-    auto inter_finish = [&](int c) {
+    // (f) S^T <- e^{G_end} S^T + (K_end^T E)^T; O^T = e^{G} (Q S)^T + (A E)^T -> TMA store;
+    // retire chunk c and prefetch chunk c+2 into its stage.
+    auto st_finish = [&](int c) {
         const ChunkVec &cv = sm.v[c & 1];
         wait(bar_2, c & 1);
         tc_fence_after();
         {
             const float gam = cv.eG[kC - 1];
-            uint32_t v[32];
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
+                uint32_t v[32];
                 tmem_ld32(tlane + TM_2 + 64 * half + 32 * hh, v);
                 tmem_ld_wait();
 #pragma unroll
@@ -563,60 +638,69 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
         }
         {
-            uint32_t qs[32], ae[32];
-            tmem_ld32(tlane + TM_1B + 32 * half, qs);
-            tmem_ld32(tlane + TM_3 + 32 * half, ae);
-            tmem_ld_wait();
-            float o[32];
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj)
-                o[jj] = fmaf(cv.eG[32 * half + jj], __uint_as_float(qs[jj]), __uint_as_float(ae[jj]));
-            // Pair value channels (m, m^1) so each lane stores 2 channels of 16 tokens as bf16x2:
-            // even lanes keep tokens 0-15 of their half, odd lanes tokens 16-31.
+            // Pair value channels (m, m^1) so each lane stores two channels as one bf16x2:
+            // within each group of 16 tokens, even lanes keep tokens 0-7, odd lanes 8-15.
             const bool odd = lane & 1;
             const int m0 = row & ~1;
             uint8_t *stg = smem + OFF_ETS + (m0 >> 6) * 8192 + (m0 & 63) * 2;
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-                const float mine = odd ? o[jj + 16] : o[jj];
-                const float send = odd ? o[jj] : o[jj + 16];
-                const float other = __shfl_xor_sync(0xffffffffu, send, 1);
-                const int n = 32 * half + jj + (odd ? 16 : 0);
-                const uint32_t pr = odd ? pack_bf16(other, mine) : pack_bf16(mine, other);
-                *reinterpret_cast<uint32_t *>(stg + n * 128) = pr;
+            for (int pc = 0; pc < 2; ++pc) {
+                uint32_t qs[16], ae[16];
+                tmem_ld16(tlane + TM_1B + 32 * half + 16 * pc, qs);
+                tmem_ld16(tlane + TM_3 + 32 * half + 16 * pc, ae);
+                tmem_ld_wait();
+                float o[16];
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj)
+                    o[jj] = fmaf(cv.eG[32 * half + 16 * pc + jj], __uint_as_float(qs[jj]), __uint_as_float(ae[jj]));
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    const float mine = odd ? o[jj + 8] : o[jj];
+                    const float send = odd ? o[jj] : o[jj + 8];
+                    const float other = __shfl_xor_sync(0xffffffffu, send, 1);
+                    const int n = 32 * half + 16 * pc + jj + (odd ? 8 : 0);
+                    const uint32_t pr = odd ? pack_bf16(other, mine) : pack_bf16(mine, other);
+                    *reinterpret_cast<uint32_t *>(stg + n * 128) = pr;
+                }
             }
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
+        gsync();
+        if (gtid == 0) {
             const int t0 = c * kC;
             tma_store_4d(&tm_o, sbase + OFF_ETS, 0, h, t0, b);
             tma_store_4d(&tm_o, sbase + OFF_ETS + 8192, 64, h, t0, b);
             tma_store_commit();
             if (c + 2 < nchunks) issue_loads(c + 2);
+            mbar_arrive(bar_done0 + 8 * (c & 1));
         }
     };
 
     // ================================================================== schedule
-    intra_front(0);
-    intra_mid(0);
-    intra_back(0);
-    __syncthreads();
-    for (int c = 0; c < nchunks && !sm.abort; ++c) {
-        const bool next = c + 1 < nchunks;
-        inter_issue1(c);
-        if (next) intra_front(c + 1);
-        inter_issue2(c);
-        if (next) intra_mid(c + 1);
-        inter_finish(c);
-        if (next) intra_back(c + 1);
-        __syncthreads();
+    if (grp == 1) {
+        load_gates(0);
+        for (int c = 0; c < nchunks; ++c) {
+            if (group_aborted()) break;
+            op_front(c);
+            op_mid(c);
+            op_back(c);
+        }
+    } else {
+        for (int c = 0; c < nchunks; ++c) {
+            wait(bar_ready, c & 1);
+            if (group_aborted()) break;
+            tc_fence_after();
+            st_issue1(c);
+            st_issue2(c);
+            st_finish(c);
+        }
     }
+    __syncthreads();
 
     if (sm.abort && tid == 0) atomicOr(p.err, kErrTimeout);
     if (tid == 0) tma_store_wait_all();
-    if (p.S_T && !sm.abort) {
+    if (grp == 0 && p.S_T && !sm.abort) {
         float *ST = p.S_T + static_cast<size_t>(bh) * kD * kD;
 #pragma unroll
         for (int kk = 0; kk < 64; ++kk) ST[(64 * half + kk) * kD + row] = s_reg[kk];
