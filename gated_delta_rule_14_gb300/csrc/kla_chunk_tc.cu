@@ -1,6 +1,7 @@
 // kla_chunk_tc.cu -- tensor-core (tcgen05) chunkwise KLA prefill for sm_103a.
 //
-// Scope: bf16 q/k/v/o, d_k = d_v = 128, chunk C = 64, scalar gate, fp32 state.
+// Scope: bf16 q/k/v/o, d_k = d_v = 128, chunk C = 64, fp32 state; scalar gate (one alpha per
+// token and head) or per-key-channel gate (one alpha per token, head and key channel).
 //
 // Algebra (GeekNews, "Revisando las variantes de atencion lineal de la familia DeltaNet",
 // section "KDA por chunks"; KLA page, section "Implementazione": beta enters only as the
@@ -69,7 +70,8 @@ constexpr uint32_t OFF_ETS = OFF_ET + 16384;          // 16 KB: E^T diag(e^{G_en
 constexpr uint32_t OFF_R = OFF_ETS + 16384;           // 16 KB: R fp32, then T_K | T_V bf16 tiles
 constexpr uint32_t OFF_XS = OFF_R + 16384;            // 7 KB: solve scratch
 constexpr uint32_t OFF_SMALL = OFF_XS + 7168;         // per-chunk vectors + barriers
-constexpr uint32_t SMEM_BYTES = OFF_SMALL + 4096 + 1024;   // + alignment slack
+constexpr uint32_t SMALL_BYTES = 8192;
+constexpr uint32_t SMEM_BYTES = OFF_SMALL + SMALL_BYTES + 1024;   // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 // ---- tensor memory columns (512 allocated)
@@ -93,8 +95,20 @@ struct ChunkVec {          // per-chunk vectors (double-buffered by chunk parity
     int safe;              // G_end >= kSafeDecay: e^{G_i - G_j} = e^{G_i} e^{-G_j} without overflow
     int pad[3];
 };
+// Per-key-channel vectors of one chunk (per-channel gate only), double-buffered by parity.
+// r = kRef is the in-chunk reference token: every factor e^{G_i - G_r} or e^{G_r - G_i} spans
+// at most 32 tokens of decay.
+constexpr int kRef = 31;
+static_assert(kRef == kC / 2 - 1, "the per-channel products split the chunk into two halves of 32 tokens");
+struct ChanVec {
+    float eGr[kD];         // e^{G_r}: scales the state operand
+    float gam[kD];         // e^{G_end}: decay of the state over the chunk
+    float F[kD];           // e^{G_end - G_r}
+    float pad[kD];
+};
 struct Small {
     ChunkVec v[2];
+    ChanVec ch[2];
     uint64_t full[2];              // q/k/v stage landed (TMA)
     uint64_t mA, mW, m1, m2;       // tcgen05.commit of the four MMA groups
     uint64_t ready, freed;         // operand group -> state group, state group -> operand group
@@ -102,10 +116,10 @@ struct Small {
     uint32_t tmem_base;
     volatile int abort;
 };
-static_assert(sizeof(Small) <= 4096, "small area");
+static_assert(sizeof(Small) <= SMALL_BYTES, "small area");
 
 struct TcParams {
-    const float *alpha, *eta;
+    const float *alpha, *eta;   // alpha: [B,T,H] (scalar gate) or [B,T,H,d_k] (per-channel gate)
     float eps;
     const float *S0;
     float *S_T;
@@ -132,6 +146,7 @@ __device__ __forceinline__ void st_bf16x8u(uint32_t addr, const uint32_t *x) {
                  pack_bf16(__uint_as_float(x[6]), __uint_as_float(x[7])));
 }
 
+template <bool kCh>   // per-key-channel gate
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -244,12 +259,29 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
     };
 
+    // Per-channel gates (per-channel gate only): thread = (key channel ch, token half th) holds
+    // the 32 gates of its half of the next chunk, clamped to e^-80 like the log-gates.
+    const int gch = gtid & (kD - 1), gth = gtid >> 7;
+    float ga[kCh ? 32 : 1];
+    auto load_chgates = [&](int c) {
+        if constexpr (kCh) {
+            if (grp == 1 && c < nchunks) {
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    const int t = c * kC + 32 * gth + u;
+                    ga[u] = t < p.T ? fmaxf(p.alpha[((static_cast<size_t>(b) * p.T + t) * p.H + h) * kD + gch], 1.8e-35f)
+                                    : 1.f;
+                }
+            }
+        }
+    };
+
     // (a) gates, norms, beta and the decay tables; issue [K;Q] K^T.
     auto op_front = [&](int c) {
         ChunkVec &cv = sm.v[c & 1];
         const uint32_t qk = qk_of(c);
         if (c >= 2) wait(bar_done0 + 8 * (c & 1), ((c - 2) >> 1) & 1);   // chunk c-2 retired
-        if (gw == 0) {
+        if (!kCh && gw == 0) {
             const float g0 = fmaxf(__logf(a_nx[0]), kMinLogGate), g1 = fmaxf(__logf(a_nx[1]), kMinLogGate);
             float s = g0 + g1;
 #pragma unroll
@@ -270,6 +302,21 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             cv.eta[2 * lane] = e_nx[0];
             cv.eta[2 * lane + 1] = e_nx[1];
             if (lane == 0) cv.safe = gend >= kSafeDecay;
+        }
+        if (kCh && gw == 0) {
+            cv.eta[2 * lane] = e_nx[0];
+            cv.eta[2 * lane + 1] = e_nx[1];
+            if (lane == 0) cv.safe = 1;
+        }
+        // per-channel: products of the gates over each half of the chunk
+        float zprod = 1.f;
+        if constexpr (kCh) {
+#pragma unroll
+            for (int u = 0; u < 32; ++u) zprod *= ga[u];
+            ChanVec &chv = sm.ch[c & 1];
+            if (gth == 0) chv.eGr[gch] = zprod;   // e^{G_r}
+            else chv.F[gch] = zprod;              // e^{G_end - G_r}
+            if (zprod < 1.8e-35f) atomicOr(p.err, kErrGateRange);
         }
         load_gates(c + 1);
         wait(bar_full0 + 8 * (c & 1), (c >> 1) & 1);
@@ -294,12 +341,57 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         gsync();   // eta of this chunk visible
         if ((gtid & 3) == 0) cv.beta[gtid >> 2] = kla_beta(cv.eta[gtid >> 2], n2, p.eps);
+        uint32_t kb_stride = 16384, kb_base = qk;   // B operand of [K;Q] K^T: raw K rows
+        if constexpr (kCh) {
+            // Scaled tiles with reference token r: K_r = K e^{G-G_r}, Q_r = Q e^{G-G_r} (in place),
+            // K_m = K e^{G_r-G} (B of [K_r;Q_r] K_m^T, over the R area) and K_end = K e^{G_end-G}
+            // (B of E^T K_end, over the E^T_s area, free once chunk c-1 is retired).
+            ChanVec &chv = sm.ch[c & 1];
+            const float F = chv.F[gch];
+            if (gth == 0) chv.gam[gch] = zprod * F;
+            if (c >= 1) wait(bar_done0 + 8 * ((c - 1) & 1), ((c - 1) >> 1) & 1);
+            const uint32_t col = (gch & 63) * 2, blk = gch >> 6;
+            __nv_bfloat16 *Kt = reinterpret_cast<__nv_bfloat16 *>(smem + (qk - sbase) + blk * 16384);
+            __nv_bfloat16 *Qt = reinterpret_cast<__nv_bfloat16 *>(smem + (qk - sbase) + blk * 16384 + 8192);
+            uint8_t *Km = smem + OFF_R + blk * 8192, *Ke = smem + OFF_ETS + blk * 8192;
+            float run = 1.f;
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+                // th 1: tokens 32..63 ascending, run = e^{G_i - G_r};  th 0: tokens 31..0, run = e^{G_r - G_i}
+                const int uu = gth ? u : 31 - u;
+                const int i = 32 * gth + uu;
+                float fr, fm;
+                if (gth) {
+                    run *= ga[uu];
+                    fr = run;
+                    fm = __frcp_rn(run);
+                } else {
+                    fm = run;
+                    fr = __frcp_rn(run);
+                    run *= ga[uu];
+                }
+                const uint32_t off = sw128_off(i, col);
+                const float kv = __bfloat162float(*reinterpret_cast<__nv_bfloat16 *>(reinterpret_cast<uint8_t *>(Kt) + off));
+                const float qv = __bfloat162float(*reinterpret_cast<__nv_bfloat16 *>(reinterpret_cast<uint8_t *>(Qt) + off));
+                *reinterpret_cast<__nv_bfloat16 *>(reinterpret_cast<uint8_t *>(Kt) + off) = __float2bfloat16_rn(kv * fr);
+                *reinterpret_cast<__nv_bfloat16 *>(reinterpret_cast<uint8_t *>(Qt) + off) = __float2bfloat16_rn(qv * fr);
+                *reinterpret_cast<__nv_bfloat16 *>(Km + off) = __float2bfloat16_rn(kv * fm);
+                *reinterpret_cast<__nv_bfloat16 *>(Ke + off) = __float2bfloat16_rn(kv * (F * fm));
+            }
+            load_chgates(c + 1);
+            fence_proxy_async_smem();
+            gsync();
+            kb_stride = 8192;
+            kb_base = sbase + OFF_R;
+        }
         if (gtid == 0) {
             tc_fence_after();
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
                 const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
-                mma_bf16(tbase + TM_A, sw128_desc(qk + off, 16, 1024), sw128_desc(qk + off, 16, 1024), id_qk, s);
+                const uint32_t boff = (s >> 2) * kb_stride + (s & 3) * 32;
+                mma_bf16(tbase + TM_A, sw128_desc(qk + off, 16, 1024), sw128_desc(kb_base + boff, 16, 1024), id_qk,
+                         s);
             }
             mma_commit(bar_A);
         }
@@ -319,7 +411,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const bool key_row = row < kC;
             const float scale = key_row ? cv.beta[i] : 1.f;
             float x[32];
-            if (cv.safe) {
+            if (kCh) {   // the decay is inside the scaled operands
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int j = 32 * half + jj;
+                    const bool keep = key_row ? (j < i) : (j <= i);
+                    x[jj] = keep ? scale * __uint_as_float(v[jj]) : 0.f;
+                }
+            } else if (cv.safe) {
                 const float ei = cv.eG[i] * scale;
 #pragma unroll
                 for (int q4 = 0; q4 < 8; ++q4) {
@@ -510,10 +609,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (gtid == 0) {
             tc_fence_after();
             const uint32_t qk = qk_of(c), vv = v_of(c);
+            // scalar gate: W^T = K^T T_K^T; per-channel gate: W_r^T = K_r^T T_V^T (the factor
+            // e^{G_r} of W is carried by the state operand instead)
+            const uint32_t tw = sbase + OFF_R + (kCh ? 8192 : 0);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_bf16(tbase + TM_W, sw128_desc(qk + s * 2048, 16384, 1024),
-                         sw128_desc(sbase + OFF_R + s * 32, 16, 1024), id_w, s);
+                mma_bf16(tbase + TM_W, sw128_desc(qk + s * 2048, 16384, 1024), sw128_desc(tw + s * 32, 16, 1024),
+                         id_w, s);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
                 mma_bf16(tbase + TM_U, sw128_desc(vv + s * 2048, 8192, 1024),
@@ -551,8 +653,21 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // (d) S^T -> bf16 operand; issue S^T W^T and S^T Q^T.
     auto st_issue1 = [&](int c) {
         const uint32_t base = sbase + OFF_ST + half * 16384;
+        if constexpr (kCh) {   // state operand S^T diag(e^{G_r}) (per key channel)
+            const float *eGr = sm.ch[c & 1].eGr + 64 * half;
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) st_bf16x8(base + sw128_off(row, ch * 16), s_reg + 8 * ch);
+            for (int ch = 0; ch < 8; ++ch) {
+                const float4 a = *reinterpret_cast<const float4 *>(eGr + 8 * ch);
+                const float4 bq = *reinterpret_cast<const float4 *>(eGr + 8 * ch + 4);
+                const float x[8] = {s_reg[8 * ch] * a.x,     s_reg[8 * ch + 1] * a.y, s_reg[8 * ch + 2] * a.z,
+                                    s_reg[8 * ch + 3] * a.w, s_reg[8 * ch + 4] * bq.x, s_reg[8 * ch + 5] * bq.y,
+                                    s_reg[8 * ch + 6] * bq.z, s_reg[8 * ch + 7] * bq.w};
+                st_bf16x8(base + sw128_off(row, ch * 16), x);
+            }
+        } else {
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) st_bf16x8(base + sw128_off(row, ch * 16), s_reg + 8 * ch);
+        }
         fence_proxy_async_smem();
         if (gtid == 0) tma_store_wait_read_all();   // the previous output staging is free again
         gsync();
@@ -597,7 +712,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int ch = 0; ch < 2; ++ch) {
                 const uint32_t off = sw128_off(row, half * 64 + pc * 32 + ch * 16);
                 st_bf16x8(sbase + OFF_ET + off, e + 8 * ch);
-                st_bf16x8(sbase + OFF_ETS + off, es + 8 * ch);
+                if (!kCh) st_bf16x8(sbase + OFF_ETS + off, es + 8 * ch);
             }
         }
         fence_proxy_async_smem();
@@ -607,10 +722,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mbar_arrive(bar_freed);   // W^T read by the finished S^T W^T, U^T loaded by every thread
             tc_fence_after();
             const uint32_t qk = qk_of(c);
+            // scalar gate: (E^T diag(e^{G_end-G})) K; per-channel gate: E^T K_end (K_end over the
+            // E^T_s area, 64-row blocks)
+            const uint32_t a2 = sbase + (kCh ? OFF_ET : OFF_ETS);
+            const uint32_t b2 = kCh ? sbase + OFF_ETS : qk, lbo2 = kCh ? 8192 : 16384;
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_bf16(tbase + TM_2, sw128_desc(sbase + OFF_ETS + s * 32, 16, 1024),
-                         sw128_desc(qk + s * 2048, 16384, 1024), id_2, s);
+                mma_bf16(tbase + TM_2, sw128_desc(a2 + s * 32, 16, 1024), sw128_desc(b2 + s * 2048, lbo2, 1024), id_2,
+                         s);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
                 mma_bf16(tbase + TM_3, sw128_desc(sbase + OFF_ET + s * 32, 16, 1024),
@@ -627,14 +746,17 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tc_fence_after();
         {
             const float gam = cv.eG[kC - 1];
+            const float *gch = sm.ch[c & 1].gam + 64 * half;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 uint32_t v[32];
                 tmem_ld32(tlane + TM_2 + 64 * half + 32 * hh, v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int kk = 0; kk < 32; ++kk)
-                    s_reg[32 * hh + kk] = fmaf(gam, s_reg[32 * hh + kk], __uint_as_float(v[kk]));
+                for (int kk = 0; kk < 32; ++kk) {
+                    const float gk = kCh ? gch[32 * hh + kk] : gam;
+                    s_reg[32 * hh + kk] = fmaf(gk, s_reg[32 * hh + kk], __uint_as_float(v[kk]));
+                }
             }
         }
         {
@@ -642,7 +764,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // within each group of 16 tokens, even lanes keep tokens 0-7, odd lanes 8-15.
             const bool odd = lane & 1;
             const int m0 = row & ~1;
-            uint8_t *stg = smem + OFF_ETS + (m0 >> 6) * 8192 + (m0 & 63) * 2;
+            uint8_t *stg = smem + (kCh ? OFF_ET : OFF_ETS) + (m0 >> 6) * 8192 + (m0 & 63) * 2;
 #pragma unroll
             for (int pc = 0; pc < 2; ++pc) {
                 uint32_t qs[16], ae[16];
@@ -652,7 +774,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 float o[16];
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj)
-                    o[jj] = fmaf(cv.eG[32 * half + 16 * pc + jj], __uint_as_float(qs[jj]), __uint_as_float(ae[jj]));
+                    o[jj] = fmaf(kCh ? 1.f : cv.eG[32 * half + 16 * pc + jj], __uint_as_float(qs[jj]),
+                                 __uint_as_float(ae[jj]));
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj) {
                     const float mine = odd ? o[jj + 8] : o[jj];
@@ -669,8 +792,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         gsync();
         if (gtid == 0) {
             const int t0 = c * kC;
-            tma_store_4d(&tm_o, sbase + OFF_ETS, 0, h, t0, b);
-            tma_store_4d(&tm_o, sbase + OFF_ETS + 8192, 64, h, t0, b);
+            const uint32_t stg0 = sbase + (kCh ? OFF_ET : OFF_ETS);
+            tma_store_4d(&tm_o, stg0, 0, h, t0, b);
+            tma_store_4d(&tm_o, stg0 + 8192, 64, h, t0, b);
             tma_store_commit();
             if (c + 2 < nchunks) issue_loads(c + 2);
             mbar_arrive(bar_done0 + 8 * (c & 1));
@@ -680,6 +804,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // ================================================================== schedule
     if (grp == 1) {
         load_gates(0);
+        load_chgates(0);
         for (int c = 0; c < nchunks; ++c) {
             if (group_aborted()) break;
             op_front(c);
@@ -750,8 +875,7 @@ bool make_map(CUtensorMap *m, const void *base, int B, int T, int H, bool swizzl
 }  // namespace
 
 bool chunk_tc_supports(const ChunkArgs &a) {
-    return a.dtype == KLA_DTYPE_BF16 && a.d_k == kD && a.d_v == kD && a.chunk == kC && a.gate == KLA_GATE_SCALAR &&
-           a.T > 0;
+    return a.dtype == KLA_DTYPE_BF16 && a.d_k == kD && a.d_v == kD && a.chunk == kC && a.T > 0;
 }
 
 cudaError_t launch_chunk_tc(const ChunkArgs &a) {
@@ -760,10 +884,11 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a) {
         !make_map(&mv, a.v, a.B, a.T, a.H, true) || !make_map(&mo, a.o, a.B, a.T, a.H, false))
         return cudaErrorInvalidValue;
     TcParams p{a.alpha, a.eta, a.eps, a.S0, a.S_T, a.B, a.T, a.H, a.err};
-    cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto kern = a.gate == KLA_GATE_CHANNEL ? chunk_tc_kernel<true> : chunk_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(SMEM_BYTES));
     if (e != cudaSuccess) return e;
-    chunk_tc_kernel<<<a.B * a.H, kThreads, SMEM_BYTES, a.stream>>>(mq, mk, mv, mo, p);
+    kern<<<a.B * a.H, kThreads, SMEM_BYTES, a.stream>>>(mq, mk, mv, mo, p);
     return cudaGetLastError();
 }
 

@@ -83,11 +83,12 @@ typedef enum kla_gate {
  *   workspace, workspace_bytes: device scratch of at least
  *            kla_chunk_fwd_workspace_size(...) bytes (may be NULL when that size is 0)
  *
- * Per-key-channel gates on the tensor-core path: the in-chunk products use the
- * chunk start as reference point, which is exact as long as the log-decay of every
- * key channel summed over one chunk stays above -80 (alpha averaged over 64 tokens
- * above about 0.29). A chunk outside that range raises a device flag that
- * kla_device_status() reports as KLA_ERR_INVALID_ARG.
+ * Per-key-channel gates on the tensor-core path: the in-chunk products are factorised
+ * around the 32nd token of each chunk, which is exact as long as, for every key channel, the
+ * product of the gates over tokens 0-31 and over tokens 32-63 of a chunk each stays above
+ * e^-80 (the gates averaged over 32 tokens above about 0.082). A chunk outside that range
+ * raises a device flag that kla_device_status() reports as KLA_ERR_INVALID_ARG (its results
+ * are then not valid); chunk = 16 or 32 runs the fp32 path, which has no such limit.
  */
 kla_status kla_chunk_fwd(const void *q, const void *k, const void *v,
                          const float *alpha, const float *eta, float eps,

@@ -119,3 +119,21 @@ def test_full_config_sampled(name, nchains):
     o, S = run_prefill(inp)
     chains = sample_chains(inp.wl.B, inp.wl.H, nchains, seed=1)
     check(inp, o, S, chains)
+
+
+def test_channel_gate_out_of_range_is_reported():
+    """Per-channel gates whose product over half a chunk falls below e^-80 are outside the exact
+    range of the tensor-core path: the call reports it through kla_device_status."""
+    import gated_delta_rule_14_gb300 as kla
+    inp = synth.make_prefill("kda8k", seed=3, B=1, T=64, H=1)
+    inp.alpha[0, :32, 0, 5] = 1e-3       # 32 tokens at 1e-3: product 1e-96
+    with pytest.raises(kla.KlaError) as ei:
+        run_prefill(inp)
+    assert ei.value.status == 1
+    # the same gates run exactly on the fp32 path (chunk 32)
+    o, S = run_prefill(inp, chunk=32)
+    check(inp, o, S)
+    # and the device flag was cleared by the first status read
+    inp2 = synth.make_prefill("kda8k", seed=4, B=1, T=64, H=1)
+    o, S = run_prefill(inp2)
+    check(inp2, o, S)
