@@ -55,7 +55,7 @@ constexpr int kThreads = 2 * kGroup;
 constexpr uint32_t kBarState = 1, kBarOperand = 2;   // named barriers of the two groups
 constexpr float kMinLogGate = -80.0f;
 constexpr float kSafeDecay = -80.0f;   // chunk decay above which e^{-G_j} is representable
-constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr uint32_t kWaitLimit = 100000;   // x 20 us: a stuck wait gives up after ~2 s
 
 // ---- shared memory map (offsets from a 1024-byte aligned base)
 constexpr uint32_t OFF_QK = 0;                        // 2 stages x 32 KB: [blk0: K rows | Q rows][blk1 ...]
@@ -152,7 +152,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                 const TcParams p) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base, derived from the shared array itself so that every access below
+    // stays a shared-memory access (no generic addressing)
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
     Small &sm = *reinterpret_cast<Small *>(smem + OFF_SMALL);
     float *Rm = reinterpret_cast<float *>(smem + OFF_R);    // R, swizzled fp32 [64][64]
@@ -243,22 +245,56 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (nchunks > 1) issue_loads(1);
     }
 
-    // ===================================================================== operand group
-    // Gates of the next chunk to be prepared, prefetched by the group's first warp.
+    // Per-token gate vectors (G, e^{G}, e^{-G}, e^{G_end - G}, eta) of a chunk are computed by
+    // warp 0 of the state group two chunks ahead, from gates it prefetched into registers (two
+    // tokens per lane), and handed to the operand group through `done`.
     float a_nx[2] = {1.f, 1.f}, e_nx[2] = {0.f, 0.f};
     auto load_gates = [&](int c) {
-        if (grp == 1 && gw == 0 && c < nchunks) {
+        if (warp == 0 && c < nchunks) {
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int t = c * kC + 2 * lane + u;
                 const bool ok = t < p.T;
                 const size_t tok = (static_cast<size_t>(b) * p.T + t) * p.H + h;
-                a_nx[u] = ok ? p.alpha[tok] : 1.f;
+                a_nx[u] = (ok && !kCh) ? p.alpha[tok] : 1.f;
                 e_nx[u] = ok ? p.eta[tok] : 0.f;
             }
         }
     };
+    auto gate_vec = [&](int c) {   // warp 0 only
+        if (c >= nchunks) return;
+        ChunkVec &cv = sm.v[c & 1];
+        const float g0 = fmaxf(__logf(a_nx[0]), kMinLogGate), g1 = fmaxf(__logf(a_nx[1]), kMinLogGate);
+        float s = g0 + g1;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, s, off);
+            if (lane >= off) s += y;
+        }
+        const float gend = __shfl_sync(0xffffffffu, s, 31);
+        const float G0 = s - g1, G1 = s;
+        cv.G[2 * lane] = G0;
+        cv.G[2 * lane + 1] = G1;
+        cv.eG[2 * lane] = __expf(G0);
+        cv.eG[2 * lane + 1] = __expf(G1);
+        cv.enG[2 * lane] = __expf(-G0);
+        cv.enG[2 * lane + 1] = __expf(-G1);
+        cv.eEnd[2 * lane] = __expf(gend - G0);
+        cv.eEnd[2 * lane + 1] = __expf(gend - G1);
+        cv.eta[2 * lane] = e_nx[0];
+        cv.eta[2 * lane + 1] = e_nx[1];
+        if (lane == 0) cv.safe = kCh ? 1 : (gend >= kSafeDecay);
+    };
+    if (warp == 0) {   // chunks 0 and 1 before the groups split; chunk 2 prefetched
+        load_gates(0);
+        gate_vec(0);
+        load_gates(1);
+        gate_vec(1);
+        load_gates(2);
+    }
+    __syncthreads();
 
+    // ===================================================================== operand group
     // Per-channel gates (per-channel gate only): thread = (key channel ch, token half th) holds
     // the 32 gates of its half of the next chunk, clamped to e^-80 like the log-gates.
     const int gch = gtid & (kD - 1), gth = gtid >> 7;
@@ -281,33 +317,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         ChunkVec &cv = sm.v[c & 1];
         const uint32_t qk = qk_of(c);
         if (c >= 2) wait(bar_done0 + 8 * (c & 1), ((c - 2) >> 1) & 1);   // chunk c-2 retired
-        if (!kCh && gw == 0) {
-            const float g0 = fmaxf(__logf(a_nx[0]), kMinLogGate), g1 = fmaxf(__logf(a_nx[1]), kMinLogGate);
-            float s = g0 + g1;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, s, off);
-                if (lane >= off) s += y;
-            }
-            const float gend = __shfl_sync(0xffffffffu, s, 31);
-            const float G0 = s - g1, G1 = s;
-            cv.G[2 * lane] = G0;
-            cv.G[2 * lane + 1] = G1;
-            cv.eG[2 * lane] = __expf(G0);
-            cv.eG[2 * lane + 1] = __expf(G1);
-            cv.enG[2 * lane] = __expf(-G0);
-            cv.enG[2 * lane + 1] = __expf(-G1);
-            cv.eEnd[2 * lane] = __expf(gend - G0);
-            cv.eEnd[2 * lane + 1] = __expf(gend - G1);
-            cv.eta[2 * lane] = e_nx[0];
-            cv.eta[2 * lane + 1] = e_nx[1];
-            if (lane == 0) cv.safe = gend >= kSafeDecay;
-        }
-        if (kCh && gw == 0) {
-            cv.eta[2 * lane] = e_nx[0];
-            cv.eta[2 * lane + 1] = e_nx[1];
-            if (lane == 0) cv.safe = 1;
-        }
+        // T_K/T_V (R area) and TM_W/TM_U of chunk c-1 are read by its W^T/U^T MMAs
+        if (c >= 1) wait(bar_W, (c - 1) & 1);
         // per-channel: products of the gates over each half of the chunk
         float zprod = 1.f;
         if constexpr (kCh) {
@@ -318,8 +329,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             else chv.F[gch] = zprod;              // e^{G_end - G_r}
             if (zprod < 1.8e-35f) atomicOr(p.err, kErrGateRange);
         }
-        load_gates(c + 1);
         wait(bar_full0 + 8 * (c & 1), (c >> 1) & 1);
+        if (!kCh && gtid == 0) {   // scalar gate: [K;Q] K^T needs only the tiles; issue it first
+            tc_fence_after();
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
+                mma_bf16(tbase + TM_A, sw128_desc(qk + off, 16, 1024), sw128_desc(qk + off, 16, 1024), id_qk, s);
+            }
+            mma_commit(bar_A);
+        }
         // ||k_i||^2: 4 threads per key row, 32 channels each
         float n2 = 0.f;
         {
@@ -384,7 +403,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             kb_stride = 8192;
             kb_base = sbase + OFF_R;
         }
-        if (gtid == 0) {
+        if (kCh && gtid == 0) {
             tc_fence_after();
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
@@ -404,51 +423,56 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         wait(bar_A, c & 1);
         tc_fence_after();
         {
-            uint32_t v[32];
-            tmem_ld32(tlane + TM_A + 32 * half, v);
-            tmem_ld_wait();
+            // two passes of 16 columns keep the live registers low
             const int i = row & (kC - 1);
             const bool key_row = row < kC;
             const float scale = key_row ? cv.beta[i] : 1.f;
-            float x[32];
-            if (kCh) {   // the decay is inside the scaled operands
+            const bool safe = cv.safe != 0;
+            const float ei = cv.eG[i] * scale, Gi = cv.G[i];
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int j = 32 * half + jj;
-                    const bool keep = key_row ? (j < i) : (j <= i);
-                    x[jj] = keep ? scale * __uint_as_float(v[jj]) : 0.f;
-                }
-            } else if (cv.safe) {
-                const float ei = cv.eG[i] * scale;
+            for (int pc = 0; pc < 2; ++pc) {
+                uint32_t v[16];
+                tmem_ld16(tlane + TM_A + 32 * half + 16 * pc, v);
+                tmem_ld_wait();
+                const int j0 = 32 * half + 16 * pc;
+                float x[16];
+                if (kCh) {   // the decay is inside the scaled operands
 #pragma unroll
-                for (int q4 = 0; q4 < 8; ++q4) {
-                    const float4 en = *reinterpret_cast<const float4 *>(&cv.enG[32 * half + 4 * q4]);
-                    const float e4[4] = {en.x, en.y, en.z, en.w};
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int jj = 4 * q4 + u, j = 32 * half + jj;
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int j = j0 + jj;
                         const bool keep = key_row ? (j < i) : (j <= i);
-                        x[jj] = keep ? ei * e4[u] * __uint_as_float(v[jj]) : 0.f;
+                        x[jj] = keep ? scale * __uint_as_float(v[jj]) : 0.f;
+                    }
+                } else if (safe) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const float4 en = *reinterpret_cast<const float4 *>(&cv.enG[j0 + 4 * q4]);
+                        const float e4[4] = {en.x, en.y, en.z, en.w};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int jj = 4 * q4 + u, j = j0 + jj;
+                            const bool keep = key_row ? (j < i) : (j <= i);
+                            x[jj] = keep ? ei * e4[u] * __uint_as_float(v[jj]) : 0.f;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int j = j0 + jj;
+                        const bool keep = key_row ? (j < i) : (j <= i);
+                        x[jj] = keep ? scale * __expf(Gi - cv.G[j]) * __uint_as_float(v[jj]) : 0.f;
                     }
                 }
-            } else {
-                const float Gi = cv.G[i];
+                if (key_row) {
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int j = 32 * half + jj;
-                    const bool keep = key_row ? (j < i) : (j <= i);
-                    x[jj] = keep ? scale * __expf(Gi - cv.G[j]) * __uint_as_float(v[jj]) : 0.f;
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        st_v4_f32(Rm + fidx(i, j0 + 4 * q4), x[4 * q4], x[4 * q4 + 1], x[4 * q4 + 2], x[4 * q4 + 3]);
+                } else {
+                    const uint32_t base = aqk_of(c);
+#pragma unroll
+                    for (int ch = 0; ch < 2; ++ch)
+                        st_bf16x8(base + sw128_off(i, half * 64 + pc * 32 + ch * 16), x + 8 * ch);
                 }
-            }
-            if (key_row) {
-#pragma unroll
-                for (int q4 = 0; q4 < 8; ++q4)
-                    st_v4_f32(Rm + fidx(i, 32 * half + 4 * q4), x[4 * q4], x[4 * q4 + 1], x[4 * q4 + 2],
-                              x[4 * q4 + 3]);
-            } else {
-                const uint32_t base = aqk_of(c);
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) st_bf16x8(base + sw128_off(i, half * 64 + ch * 16), x + 8 * ch);
             }
         }
         fence_proxy_async_smem();
@@ -621,25 +645,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 mma_bf16(tbase + TM_U, sw128_desc(vv + s * 2048, 8192, 1024),
                          sw128_desc(sbase + OFF_R + 8192 + s * 32, 16, 1024), id_w, s);
             mma_commit(bar_W);
+            mbar_arrive(bar_ready);   // A, gate vectors and tiles of chunk c written; W^T/U^T in flight
         }
     };
 
-    // (c) W^T -> bf16 MN-major B operand (rows k, 64 tokens per row) over the T area; then
-    // hand chunk c to the state group.
-    auto op_back = [&](int c) {
-        wait(bar_W, c & 1);
-        tc_fence_after();
-        uint32_t v[32];
-        tmem_ld32(tlane + TM_W + 32 * half, v);
-        tmem_ld_wait();
-        const uint32_t base = sbase + OFF_WT;
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) st_bf16x8u(base + sw128_off(row, half * 64 + ch * 16), v + 8 * ch);
-        fence_proxy_async_smem();
-        tc_fence_before();
-        gsync();
-        if (gtid == 0) mbar_arrive(bar_ready);
-    };
 
     // ======================================================================= state group
     // S^T: this thread owns value channel m = row, key channels [64*half, 64*half + 64).
@@ -652,6 +661,19 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     // (d) S^T -> bf16 operand; issue S^T W^T and S^T Q^T.
     auto st_issue1 = [&](int c) {
+        load_gates(c + 2);   // warp 0: gates of chunk c+2, turned into vectors at the end of chunk c
+        // W^T of chunk c -> bf16 MN-major B operand (rows k, 64 tokens per row), over the T area
+        wait(bar_W, c & 1);
+        tc_fence_after();
+#pragma unroll
+        for (int pc = 0; pc < 2; ++pc) {
+            uint32_t v[16];
+            tmem_ld16(tlane + TM_W + 32 * half + 16 * pc, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch)
+                st_bf16x8u(sbase + OFF_WT + sw128_off(row, half * 64 + pc * 32 + ch * 16), v + 8 * ch);
+        }
         const uint32_t base = sbase + OFF_ST + half * 16384;
         if constexpr (kCh) {   // state operand S^T diag(e^{G_r}) (per key channel)
             const float *eGr = sm.ch[c & 1].eGr + 64 * half;
@@ -748,14 +770,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const float gam = cv.eG[kC - 1];
             const float *gch = sm.ch[c & 1].gam + 64 * half;
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                uint32_t v[32];
-                tmem_ld32(tlane + TM_2 + 64 * half + 32 * hh, v);
+            for (int hh = 0; hh < 4; ++hh) {
+                uint32_t v[16];
+                tmem_ld16(tlane + TM_2 + 64 * half + 16 * hh, v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int kk = 0; kk < 32; ++kk) {
-                    const float gk = kCh ? gch[32 * hh + kk] : gam;
-                    s_reg[32 * hh + kk] = fmaf(gk, s_reg[32 * hh + kk], __uint_as_float(v[kk]));
+                for (int kk = 0; kk < 16; ++kk) {
+                    const float gk = kCh ? gch[16 * hh + kk] : gam;
+                    s_reg[16 * hh + kk] = fmaf(gk, s_reg[16 * hh + kk], __uint_as_float(v[kk]));
                 }
             }
         }
@@ -797,19 +819,22 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tma_store_4d(&tm_o, stg0 + 8192, 64, h, t0, b);
             tma_store_commit();
             if (c + 2 < nchunks) issue_loads(c + 2);
-            mbar_arrive(bar_done0 + 8 * (c & 1));
+        }
+        if (warp == 0) {   // gate vectors of chunk c+2 into the buffer chunk c just released
+            gate_vec(c + 2);
+            __threadfence_block();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_done0 + 8 * (c & 1));
         }
     };
 
     // ================================================================== schedule
     if (grp == 1) {
-        load_gates(0);
         load_chgates(0);
         for (int c = 0; c < nchunks; ++c) {
             if (group_aborted()) break;
             op_front(c);
             op_mid(c);
-            op_back(c);
         }
     } else {
         for (int c = 0; c < nchunks; ++c) {

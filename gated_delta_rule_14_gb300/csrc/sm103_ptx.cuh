@@ -35,11 +35,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Waits for phase `parity` of the barrier; gives up after `limit` polls (each poll may itself
-// block for a hardware-defined interval). Returns false on time-out.
+// Same test, but a thread whose phase is not complete may be suspended for up to `ns`
+// nanoseconds (it resumes when the phase completes), so waiting warps leave the issue slots
+// to the warps that have work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        "selp.b32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+// Waits for phase `parity` of the barrier; gives up after `limit` polls of at most 20 us each
+// (so a wait never lasts more than limit x 20 us). Returns false on time-out.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t limit) {
     for (uint32_t i = 0; i < limit; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     return false;
 }
 
