@@ -145,7 +145,9 @@ kla_status kla_decode_step(const void *q, const void *k, const void *v, const fl
                            span(eta, nh * 4)};
     for (const Span &x : others)
         if (overlaps(s, x)) return KLA_ERR_INVALID_ARG;
-    kla::DecodeArgs a{q, k, v, alpha, eta, eps, S, o, B, H, d_k, d_v, dtype, gate, static_cast<cudaStream_t>(stream)};
+    kla::DecodeArgs a{q, k, v, alpha, eta, eps, S, o, B, H, d_k, d_v, dtype, gate, nullptr,
+                      static_cast<cudaStream_t>(stream)};
+    if (err_word(&a.err) != cudaSuccess) return KLA_ERR_CUDA;
     return kla::launch_decode(a) == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
 }
 

@@ -41,6 +41,7 @@ struct DecodeArgs {
     int B, H, d_k, d_v;
     kla_dtype dtype;
     kla_gate gate;
+    unsigned *err;         // device error word
     cudaStream_t stream;
 };
 
