@@ -53,6 +53,23 @@ PREFILL_FLOP_PER_TOKEN_HEAD = 6 * 128 * 128 + 5 * 64 * 128 + 64 * 64 / 3
 DECODE_BYTES_PER_HEAD_STEP = 8 * 128 * 128 + 4 * 2 * 128 + 8
 
 
+# DRAM bytes (read + write) per launch of the tensor-core prefill kernel on the gdn4k
+# workload, from the ncu capture summarised in profiles/chunk_tc_gdn4k_full.md, keyed by the
+# fingerprint of the kernel sources it was taken on. Any other source state reports null.
+TC_SOURCES = ("gated_delta_rule_14_gb300/csrc/kla_chunk_tc.cu", "gated_delta_rule_14_gb300/csrc/sm103_ptx.cuh",
+              "gated_delta_rule_14_gb300/csrc/kla_internal.cuh")
+TC_TRAFFIC_GDN4K = {"87fce72d7b4c5312": 520.870912e6}
+
+
+def tc_fingerprint() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in TC_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -405,7 +422,7 @@ def main():
     tokens_all = reduce_sum(res["tokens"], world, dev)
     value = tokens_all / (ms_max * 1e-3)
     kern_ms = res["ms"]
-    roof = roofline(res["alg_bytes"], kern_ms, pk)
+    roof = roofline(res["alg_bytes"], kern_ms, pk, traffic=TC_TRAFFIC_GDN4K.get(tc_fingerprint()))
     tensor = {"achieved_tflops": round(res["alg_flop"] / (kern_ms * 1e-3) / 1e12, 2),
               "peak_tflops": pk["bf16_tflops"],
               "frac": round(res["alg_flop"] / (kern_ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4)}
