@@ -82,8 +82,10 @@ const char *kla_status_string(kla_status s) {
 
 size_t kla_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v, int chunk, kla_dtype dtype,
                                     kla_gate gate) {
-    (void)B; (void)T; (void)H; (void)d_k; (void)d_v; (void)chunk; (void)dtype; (void)gate;
-    return 0;
+    if (B < 1 || H < 1 || T < 1) return 0;
+    kla::ChunkArgs a{};
+    a.B = B; a.T = T; a.H = H; a.d_k = d_k; a.d_v = d_v; a.chunk = chunk; a.dtype = dtype; a.gate = gate;
+    return kla::chunk_tc_supports(a) ? kla::chunk_tc_workspace_bytes(B, T, H) : 0;
 }
 
 kla_status kla_chunk_fwd(const void *q, const void *k, const void *v, const float *alpha, const float *eta,

@@ -118,12 +118,26 @@ struct Small {
 };
 static_assert(sizeof(Small) <= SMALL_BYTES, "small area");
 
+// Initial state and final state addressing. A launch covers `seg_count` segments of every
+// (sequence, head) chain, starting at segment `seg_begin`; segment s spans tokens
+// [s * seg_len, min(T, (s + 1) * seg_len)). A whole-sequence call is one segment.
+enum : int {
+    kS0Chain = 0,      // S0 + bh * d^2 for the chain's first segment, zeros for later segments (NULL: zeros)
+    kS0Segment = 1,    // S0 + (bh * nseg + s) * d^2
+    kS0Identity = 2,   // the identity (the transition of a segment is its final state from S0 = I, v = 0)
+    kSTLast = 0,       // S_T + bh * d^2, written by the chain's last segment only (NULL: not written)
+    kSTSegment = 1,    // S_T + (bh * nseg + s) * d^2
+};
 struct TcParams {
     const float *alpha, *eta;   // alpha: [B,T,H] (scalar gate) or [B,T,H,d_k] (per-channel gate)
     float eps;
     const float *S0;
     float *S_T;
     int B, T, H;
+    int seg_len, seg_begin, seg_count, nseg;   // segments (seg_len a multiple of the chunk)
+    int s0_mode, st_mode;
+    int zero_v;    // treat v as zero (U = 0): the transition run of a segment
+    int no_out;    // 0: write o; 1: no output; 2: only the chain's first segment writes o
     unsigned *err;
 };
 
@@ -168,9 +182,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int half = gw >> 2;
     const int row = (warp & 3) * 32 + lane;     // TMEM lane of this thread
     const int g8 = lane >> 2, t4 = lane & 3;    // mma.sync fragment coordinates
-    const int bh = blockIdx.x;
+    const int bh = blockIdx.x / p.seg_count;
+    const int seg = p.seg_begin + static_cast<int>(blockIdx.x) % p.seg_count;
     const int b = bh / p.H, h = bh % p.H;
-    const int nchunks = (p.T + kC - 1) / kC;
+    const int t_begin = seg * p.seg_len, t_end = min(p.T, t_begin + p.seg_len);
+    const int nchunks = (t_end - t_begin + kC - 1) / kC;
+    const bool write_out = p.no_out == 0 || (p.no_out == 2 && seg == 0);
 
     const uint32_t bar_full0 = smem_u32(&sm.full[0]);
     const uint32_t bar_A = smem_u32(&sm.mA), bar_W = smem_u32(&sm.mW);
@@ -219,14 +236,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     auto issue_loads = [&](int c) {   // one thread
         const uint32_t bar = bar_full0 + 8 * (c & 1);
         const uint32_t qk = qk_of(c), vv = v_of(c);
-        mbar_arrive_expect_tx(bar, kTileBytes);
-        const int t0 = c * kC;
+        mbar_arrive_expect_tx(bar, p.zero_v ? 4 * 8192 : kTileBytes);
+        const int t0 = t_begin + c * kC;
         tma_load_4d(qk + 0, &tm_k, bar, 0, h, t0, b);
         tma_load_4d(qk + 8192, &tm_q, bar, 0, h, t0, b);
         tma_load_4d(qk + 16384, &tm_k, bar, 64, h, t0, b);
         tma_load_4d(qk + 24576, &tm_q, bar, 64, h, t0, b);
-        tma_load_4d(vv + 0, &tm_v, bar, 0, h, t0, b);
-        tma_load_4d(vv + 8192, &tm_v, bar, 64, h, t0, b);
+        if (!p.zero_v) {
+            tma_load_4d(vv + 0, &tm_v, bar, 0, h, t0, b);
+            tma_load_4d(vv + 8192, &tm_v, bar, 64, h, t0, b);
+        }
     };
     auto wait = [&](uint32_t bar, uint32_t parity) {
         if (!mbar_wait_bounded(bar, parity, kWaitLimit)) sm.abort = 1;
@@ -253,8 +272,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (warp == 0 && c < nchunks) {
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-                const int t = c * kC + 2 * lane + u;
-                const bool ok = t < p.T;
+                const int t = t_begin + c * kC + 2 * lane + u;
+                const bool ok = t < t_end;
                 const size_t tok = (static_cast<size_t>(b) * p.T + t) * p.H + h;
                 a_nx[u] = (ok && !kCh) ? p.alpha[tok] : 1.f;
                 e_nx[u] = ok ? p.eta[tok] : 0.f;
@@ -304,8 +323,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (grp == 1 && c < nchunks) {
 #pragma unroll
                 for (int u = 0; u < 32; ++u) {
-                    const int t = c * kC + 32 * gth + u;
-                    ga[u] = t < p.T ? fmaxf(p.alpha[((static_cast<size_t>(b) * p.T + t) * p.H + h) * kD + gch], 1.8e-35f)
+                    const int t = t_begin + c * kC + 32 * gth + u;
+                    ga[u] = t < t_end ? fmaxf(p.alpha[((static_cast<size_t>(b) * p.T + t) * p.H + h) * kD + gch], 1.8e-35f)
                                     : 1.f;
                 }
             }
@@ -640,10 +659,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int s = 0; s < 4; ++s)
                 mma_bf16(tbase + TM_W, sw128_desc(qk + s * 2048, 16384, 1024), sw128_desc(tw + s * 32, 16, 1024),
                          id_w, s);
+            if (!p.zero_v) {
 #pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_bf16(tbase + TM_U, sw128_desc(vv + s * 2048, 8192, 1024),
-                         sw128_desc(sbase + OFF_R + 8192 + s * 32, 16, 1024), id_w, s);
+                for (int s = 0; s < 4; ++s)
+                    mma_bf16(tbase + TM_U, sw128_desc(vv + s * 2048, 8192, 1024),
+                             sw128_desc(sbase + OFF_R + 8192 + s * 32, 16, 1024), id_w, s);
+            }
             mma_commit(bar_W);
             mbar_arrive(bar_ready);   // A, gate vectors and tiles of chunk c written; W^T/U^T in flight
         }
@@ -654,9 +675,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // S^T: this thread owns value channel m = row, key channels [64*half, 64*half + 64).
     float s_reg[64];
     if (grp == 0) {
-        const float *S0 = p.S0 ? p.S0 + static_cast<size_t>(bh) * kD * kD : nullptr;
+        const float *S0 = nullptr;
+        if (p.s0_mode == kS0Segment) S0 = p.S0 + (static_cast<size_t>(bh) * p.nseg + seg) * kD * kD;
+        else if (p.s0_mode == kS0Chain && p.S0 && seg == 0) S0 = p.S0 + static_cast<size_t>(bh) * kD * kD;
+        const bool ident = p.s0_mode == kS0Identity;
 #pragma unroll
-        for (int kk = 0; kk < 64; ++kk) s_reg[kk] = S0 ? S0[(64 * half + kk) * kD + row] : 0.f;
+        for (int kk = 0; kk < 64; ++kk)
+            s_reg[kk] = S0 ? S0[(64 * half + kk) * kD + row] : ((ident && 64 * half + kk == row) ? 1.f : 0.f);
     }
 
     // (d) S^T -> bf16 operand; issue S^T W^T and S^T Q^T.
@@ -702,11 +727,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 mma_bf16(tbase + TM_1A, sw128_desc(sbase + OFF_ST + aoff, 16, 1024),
                          sw128_desc(sbase + OFF_WT + s * 2048, 16384, 1024), id_1a, s);
             }
+            if (write_out) {
 #pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
-                mma_bf16(tbase + TM_1B, sw128_desc(sbase + OFF_ST + off, 16, 1024),
-                         sw128_desc(qk + 8192 + off, 16, 1024), id_qk, s);
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
+                    mma_bf16(tbase + TM_1B, sw128_desc(sbase + OFF_ST + off, 16, 1024),
+                             sw128_desc(qk + 8192 + off, 16, 1024), id_qk, s);
+                }
             }
             mma_commit(bar_1);
         }
@@ -727,7 +754,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             float e[16], es[16];
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
-                e[jj] = __uint_as_float(u[jj]) - __uint_as_float(w[jj]);
+                e[jj] = (p.zero_v ? 0.f : __uint_as_float(u[jj])) - __uint_as_float(w[jj]);
                 es[jj] = e[jj] * cv.eEnd[32 * half + 16 * pc + jj];
             }
 #pragma unroll
@@ -752,10 +779,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int s = 0; s < 4; ++s)
                 mma_bf16(tbase + TM_2, sw128_desc(a2 + s * 32, 16, 1024), sw128_desc(b2 + s * 2048, lbo2, 1024), id_2,
                          s);
+            if (write_out) {
 #pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_bf16(tbase + TM_3, sw128_desc(sbase + OFF_ET + s * 32, 16, 1024),
-                         sw128_desc(aqk_of(c) + s * 32, 16, 1024), id_qk, s);
+                for (int s = 0; s < 4; ++s)
+                    mma_bf16(tbase + TM_3, sw128_desc(sbase + OFF_ET + s * 32, 16, 1024),
+                             sw128_desc(aqk_of(c) + s * 32, 16, 1024), id_qk, s);
+            }
             mma_commit(bar_2);
         }
     };
@@ -781,7 +810,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
             }
         }
-        {
+        if (write_out) {
             // Pair value channels (m, m^1) so each lane stores two channels as one bf16x2:
             // within each group of 16 tokens, even lanes keep tokens 0-7, odd lanes 8-15.
             const bool odd = lane & 1;
@@ -813,11 +842,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tc_fence_before();
         gsync();
         if (gtid == 0) {
-            const int t0 = c * kC;
+            const int t0 = t_begin + c * kC;
             const uint32_t stg0 = sbase + (kCh ? OFF_ET : OFF_ETS);
-            tma_store_4d(&tm_o, stg0, 0, h, t0, b);
-            tma_store_4d(&tm_o, stg0 + 8192, 64, h, t0, b);
-            tma_store_commit();
+            if (write_out) {
+                tma_store_4d(&tm_o, stg0, 0, h, t0, b);
+                tma_store_4d(&tm_o, stg0 + 8192, 64, h, t0, b);
+                tma_store_commit();
+            }
             if (c + 2 < nchunks) issue_loads(c + 2);
         }
         if (warp == 0) {   // gate vectors of chunk c+2 into the buffer chunk c just released
@@ -850,8 +881,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     if (sm.abort && tid == 0) atomicOr(p.err, kErrTimeout);
     if (tid == 0) tma_store_wait_all();
-    if (grp == 0 && p.S_T && !sm.abort) {
-        float *ST = p.S_T + static_cast<size_t>(bh) * kD * kD;
+    float *ST = nullptr;
+    if (p.S_T && p.st_mode == kSTSegment) ST = p.S_T + (static_cast<size_t>(bh) * p.nseg + seg) * kD * kD;
+    else if (p.S_T && seg == p.nseg - 1) ST = p.S_T + static_cast<size_t>(bh) * kD * kD;
+    if (grp == 0 && ST && !sm.abort) {
 #pragma unroll
         for (int kk = 0; kk < 64; ++kk) ST[(64 * half + kk) * kD + row] = s_reg[kk];
     }
@@ -897,7 +930,51 @@ bool make_map(CUtensorMap *m, const void *base, int B, int T, int H, bool swizzl
     return r == CUDA_SUCCESS;
 }
 
+// Number of segments a chain of `nchunks` chunks is split into, chosen to minimise the
+// wall time in chunk-steps when each CTA occupies one SM: pass 1 runs the value run of
+// segments 0..n-2 and the transition run of segments 1..n-2, pass 3 reruns segments 1..n-1.
+int plan_segments(int B, int T, int H) {
+    const int chains = B * H, nchunks = (T + kC - 1) / kC;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess || sms <= 0)
+        return 1;
+    auto waves = [&](long ctas) { return (ctas + sms - 1) / sms; };
+    const double base = static_cast<double>(waves(chains)) * nchunks;
+    double best = 0.8 * base;   // only split when it saves a fifth or more
+    int best_n = 1;
+    for (int n = 2; n <= 64; ++n) {
+        const int L = (nchunks + n - 1) / n;   // chunks per segment
+        if (L < 8) break;
+        const int nn = (nchunks + L - 1) / L;
+        if (nn < 2) continue;
+        const double cost = static_cast<double>(waves(static_cast<long>(chains) * ((nn - 1) + (nn - 2))) +
+                                                waves(static_cast<long>(chains) * (nn - 1))) * L;
+        if (cost < best) {
+            best = cost;
+            best_n = n;
+        }
+    }
+    return best_n;
+}
+
+struct SegPlan {
+    int nseg, seg_len;   // seg_len in tokens, a multiple of the chunk
+};
+SegPlan make_plan(int B, int T, int H) {
+    const int n = plan_segments(B, T, H);
+    if (n <= 1) return {1, ((T + kC - 1) / kC) * kC};
+    const int nchunks = (T + kC - 1) / kC, L = (nchunks + n - 1) / n;
+    return {(nchunks + L - 1) / L, L * kC};
+}
+
 }  // namespace
+
+size_t chunk_tc_workspace_bytes(int B, int T, int H) {
+    const SegPlan pl = make_plan(B, T, H);
+    if (pl.nseg <= 1) return 0;
+    return 3ull * B * H * pl.nseg * kD * kD * sizeof(float);   // Z, M and the start states
+}
 
 bool chunk_tc_supports(const ChunkArgs &a) {
     return a.dtype == KLA_DTYPE_BF16 && a.d_k == kD && a.d_v == kD && a.chunk == kC && a.T > 0;
@@ -908,12 +985,55 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a) {
     if (!make_map(&mq, a.q, a.B, a.T, a.H, true) || !make_map(&mk, a.k, a.B, a.T, a.H, true) ||
         !make_map(&mv, a.v, a.B, a.T, a.H, true) || !make_map(&mo, a.o, a.B, a.T, a.H, false))
         return cudaErrorInvalidValue;
-    TcParams p{a.alpha, a.eta, a.eps, a.S0, a.S_T, a.B, a.T, a.H, a.err};
     auto kern = a.gate == KLA_GATE_CHANNEL ? chunk_tc_kernel<true> : chunk_tc_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(SMEM_BYTES));
     if (e != cudaSuccess) return e;
-    kern<<<a.B * a.H, kThreads, SMEM_BYTES, a.stream>>>(mq, mk, mv, mo, p);
+    const int chains = a.B * a.H;
+    const SegPlan pl = make_plan(a.B, a.T, a.H);
+    TcParams p{a.alpha, a.eta, a.eps, a.S0, a.S_T, a.B, a.T, a.H, pl.seg_len, 0, 1, pl.nseg,
+               kS0Chain, kSTLast, 0, 0, a.err};
+    if (pl.nseg <= 1) {
+        kern<<<chains, kThreads, SMEM_BYTES, a.stream>>>(mq, mk, mv, mo, p);
+        return cudaGetLastError();
+    }
+    // Sequence-parallel scan over segments (workspace: Z | M | start states, each
+    // [chains][nseg][d][d] fp32).
+    if (!a.workspace || a.workspace_bytes < chunk_tc_workspace_bytes(a.B, a.T, a.H)) return cudaErrorInvalidValue;
+    const size_t part = static_cast<size_t>(chains) * pl.nseg * kD * kD;
+    float *Z = static_cast<float *>(a.workspace), *M = Z + part, *Sst = M + part;
+    // pass 1a: segments 0..n-2 from the true start (segment 0) or zero; segment 0 writes its outputs
+    TcParams p1 = p;
+    p1.seg_begin = 0;
+    p1.seg_count = pl.nseg - 1;
+    p1.S_T = Z;
+    p1.st_mode = kSTSegment;
+    p1.no_out = 2;
+    kern<<<chains * p1.seg_count, kThreads, SMEM_BYTES, a.stream>>>(mq, mk, mv, mo, p1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // pass 1b: transitions of segments 1..n-2 (start from I, v = 0, no outputs)
+    if (pl.nseg > 2) {
+        TcParams p2 = p;
+        p2.seg_begin = 1;
+        p2.seg_count = pl.nseg - 2;
+        p2.S0 = nullptr;
+        p2.s0_mode = kS0Identity;
+        p2.S_T = M;
+        p2.st_mode = kSTSegment;
+        p2.zero_v = 1;
+        p2.no_out = 1;
+        kern<<<chains * p2.seg_count, kThreads, SMEM_BYTES, a.stream>>>(mq, mk, mv, mo, p2);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    // pass 2: start states of segments 1..n-1
+    if ((e = launch_seg_combine(Z, M, Sst, chains, pl.nseg, a.stream)) != cudaSuccess) return e;
+    // pass 3: segments 1..n-1 from their true start states; the last one writes S_T
+    TcParams p3 = p;
+    p3.seg_begin = 1;
+    p3.seg_count = pl.nseg - 1;
+    p3.S0 = Sst;
+    p3.s0_mode = kS0Segment;
+    kern<<<chains * p3.seg_count, kThreads, SMEM_BYTES, a.stream>>>(mq, mk, mv, mo, p3);
     return cudaGetLastError();
 }
 

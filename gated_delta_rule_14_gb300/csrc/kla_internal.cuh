@@ -50,6 +50,12 @@ cudaError_t launch_chunk_simt(const ChunkArgs &a);
 // tcgen05 tensor-core chunk path: bf16, d_k = d_v = 128, chunk = 64.
 bool chunk_tc_supports(const ChunkArgs &a);
 cudaError_t launch_chunk_tc(const ChunkArgs &a);
+// Device scratch the tensor-core path needs for these sizes (non-zero when it splits long
+// sequences into segments that run in parallel).
+size_t chunk_tc_workspace_bytes(int B, int T, int H);
+// Start states of the segments of every chain: S_start[s+1] = M_s S_start[s] + Z_s.
+cudaError_t launch_seg_combine(const float *Z, const float *M, float *Sst, int chains, int nseg,
+                               cudaStream_t stream);
 // fused single-token decode step.
 cudaError_t launch_decode(const DecodeArgs &a);
 
