@@ -102,6 +102,31 @@ size_t kla_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v, int c
                                     kla_dtype dtype, kla_gate gate);
 
 /*
+ * Chunkwise prefill that allocates nothing, for callers that cannot allocate device memory
+ * (for example a runtime whose memory manager owns all device memory, or code that must not
+ * allocate while work is in flight on its stream). The pages have no counterpart: it is a
+ * deployment variant of kla_chunk_fwd with the same arguments, results and errors, minus the
+ * workspace. The scratch that kla_chunk_fwd would take from the caller (non-zero only when a
+ * long sequence with few (sequence, head) chains is split into segments) comes instead from a
+ * fixed array of KLA_NOALLOC_SCRATCH_BYTES inside the library's device image; every GPU that
+ * loads the library holds that array until the process exits.
+ *  - Sizes whose scratch (kla_chunk_fwd_workspace_size) exceeds KLA_NOALLOC_SCRATCH_BYTES are
+ *    rejected with KLA_ERR_UNSUPPORTED before anything is launched.
+ *  - The first call on a device that needs scratch looks up the array's device address with
+ *    that device current (a host-side runtime query, no allocation); make that first call
+ *    before any stream capture.
+ *  - All calls on a device share the array, and it keeps the last call's contents (each call
+ *    writes every element it reads, so nothing needs clearing). Calls whose kernels may run at
+ *    the same time on the GPU race on it: order them (one stream, or events).
+ */
+#define KLA_NOALLOC_SCRATCH_BYTES (24u << 20)
+kla_status kla_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
+                                 const float *alpha, const float *eta, float eps,
+                                 const float *S0, void *o, float *S_T,
+                                 int B, int T, int H, int d_k, int d_v, int chunk,
+                                 kla_dtype dtype, kla_gate gate, void *stream);
+
+/*
  * One fused single-token step for B sequences (GeekNews page above, section
  * "Kernel Triton recurrente fusionado para decodificacion": forget, predict,
  * residual, outer-product write, read; the KLA step of the KLA page).
