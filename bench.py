@@ -12,8 +12,9 @@ kernel neither finds its inputs in L2 nor pays for writing back the flush's dirt
 the kernels are launched on.
 
 Extras in the same JSON line: long131k prefill (B=1 H=16 T=131072), kda8k prefill
-(per-key-channel gate, B=4 H=16 T=8192) and decode (batch 64, H16, 1024 single-token
-steps, L2 flushed before every step), each with its own roofline.
+(per-key-channel gate, B=4 H=16 T=8192), decode (batch 64, H16, 1024 single-token
+steps, L2 flushed before every step) and verify4 (the decode batch advanced 4 tokens per
+call, as in speculative verification), each with its own roofline.
 
 --impl reference times the fp64 CPU oracle on the host cores on a bounded sample of the
 same workload (whole sequences of some (b, h) chains) and reports the same metric.
@@ -270,6 +271,29 @@ def bench_decode(steps_tok, seed, dev, flush, stream, pk, passes=1, warm_tokens=
             "launches": passes * steps_tok}
 
 
+def bench_verify(ntok, calls, seed, dev, flush, stream, pk):
+    """Multi-token decode (speculative verification): every call advances the decode batch's
+    states in place by `ntok` tokens; L2 flushed before every call."""
+    import torch
+
+    import gated_delta_rule_14_gb300 as kla
+    inp, d = prefill_inputs("decode", seed, dev, T=ntok, chunk=64, s0_sigma=0.02)
+    wl = inp.wl
+    S = to_dev(inp.S0, dev)
+    o = torch.empty((wl.B, wl.T, wl.H, wl.d_v), dtype=torch.bfloat16, device=dev)
+
+    def step():
+        kla.chunk_fwd(d["q"], d["k"], d["v"], d["alpha"], d["eta"], wl.eps, S, chunk=64, out=o, S_T=S)
+
+    ms = statistics.fmean(time_steps(step, calls, 3, flush, stream))
+    kla.device_status(dev)
+    heads = wl.B * wl.H
+    alg_bytes = heads * (8 * wl.d_k * wl.d_v + ntok * (PREFILL_BYTES_PER_TOKEN_HEAD))
+    return {"value": wl.B * ntok / (ms * 1e-3), "unit": "tokens/s", "ms_per_call": ms, "calls": calls,
+            "tokens_per_call": ntok, "batch": wl.B, "roofline": roofline(alg_bytes, ms, pk),
+            "l2": "flushed before every call (256 MiB write, then 256 MiB read)"}
+
+
 def e2e_prefill(res, steps, warmup, dev, stream):
     """Same workload through the public API with pinned host buffers: H2D of the inputs, the
     prefill, and D2H of the outputs and final state, all inside the timed region."""
@@ -451,6 +475,10 @@ def main():
                             "batch": 64, "l2": "flushed before every token step (256 MiB write, then 256 MiB read)",
                             "roofline": roofline(dr["alg_bytes_per_step"], dr["ms_per_token_step"], pk)}
         launches += dr["launches"]
+        t0 = time.time()
+        extras["verify4"] = bench_verify(4, 256, seed=rank, dev=dev, flush=flush, stream=stream, pk=pk)
+        clocks.mark(t0, time.time())
+        launches += 256
     clk = clocks.stop()
 
     cpu = None

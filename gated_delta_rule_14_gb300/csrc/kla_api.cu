@@ -85,6 +85,7 @@ size_t kla_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v, int c
     if (B < 1 || H < 1 || T < 1) return 0;
     kla::ChunkArgs a{};
     a.B = B; a.T = T; a.H = H; a.d_k = d_k; a.d_v = d_v; a.chunk = chunk; a.dtype = dtype; a.gate = gate;
+    if (kla::short_seq_supports(a)) return 0;
     return kla::chunk_tc_supports(a) ? kla::chunk_tc_workspace_bytes(B, T, H) : 0;
 }
 
@@ -128,7 +129,9 @@ kla_status kla_chunk_fwd(const void *q, const void *k, const void *v, const floa
     kla::ChunkArgs a{q, k, v, alpha, eta, eps, S0, o, S_T, B, T, H, d_k, d_v, chunk, dtype, gate,
                      workspace, workspace_bytes, nullptr, cs};
     if (err_word(&a.err) != cudaSuccess) return KLA_ERR_CUDA;
-    cudaError_t e = kla::chunk_tc_supports(a) ? kla::launch_chunk_tc(a) : kla::launch_chunk_simt(a);
+    cudaError_t e = kla::short_seq_supports(a) ? kla::launch_short_seq(a)
+                    : kla::chunk_tc_supports(a) ? kla::launch_chunk_tc(a)
+                                                : kla::launch_chunk_simt(a);
     return e == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
 }
 

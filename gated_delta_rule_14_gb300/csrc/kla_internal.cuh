@@ -58,6 +58,11 @@ cudaError_t launch_seg_combine(const float *Z, const float *M, float *Sst, int c
                                cudaStream_t stream);
 // fused single-token decode step.
 cudaError_t launch_decode(const DecodeArgs &a);
+// Short sequences (multi-token decode, speculative verification): the state tile stays in
+// registers while the tokens are walked one by one; any supported size and dtype.
+constexpr int kShortSeqMaxT = 16;
+bool short_seq_supports(const ChunkArgs &a);
+cudaError_t launch_short_seq(const ChunkArgs &a);
 
 // ------------------------------------------------------------------ device helpers
 template <typename T> __device__ __forceinline__ float to_f32(T x);
