@@ -30,11 +30,15 @@ struct ShortParams {
     int B, T, H, DK, DV;
 };
 
-// CGW = float4 column groups per warp (2 for a 32-column tile, 1 for 16 columns). A warp owns
-// CGW * 4 columns over ALL d_k rows, so the reductions over the rows stay inside the warp and
-// the token loop runs without block barriers; lanes split as CGW column groups x (32 / CGW)
-// row groups, each lane holding kRows consecutive rows (kRows = d_k / row groups, at least 1;
-// lanes past d_k hold nothing when d_k is below the row-group count).
+// Lane layout. A warp owns CGW float4 column groups (CGW * 4 value columns) over ALL d_k rows,
+// so the reductions over the rows stay inside the warp and the token loop runs without block
+// barriers. Lane = cg + CGW * rg: CGW column groups x (32 / CGW) row groups, each row group
+// holding kRows consecutive rows (kRows = d_k / row groups, at least 1; row groups past d_k
+// hold nothing). CGW = 2 (32-column tiles) or 1 (16-column tiles, d_v = 16).
+//
+// The state tile passes through shared memory on its way in and out, so HBM sees whole 128-byte
+// rows per warp access; its 16-byte units are XOR-swizzled by row group, which keeps the
+// per-lane row reads free of bank conflicts.
 template <int kRows>
 __device__ __forceinline__ void rows_from_smem(const float *src, float (&dst)[kRows]) {
     if constexpr (kRows % 4 == 0) {
@@ -49,32 +53,73 @@ __device__ __forceinline__ void rows_from_smem(const float *src, float (&dst)[kR
     }
 }
 
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Reduce 8 partial sums over the row-group lanes of one column group. The first three levels
+// halve the values each lane carries (reduce-scatter), so 8 + the remaining levels shuffles
+// replace 8 per level; afterwards the lane with (lane >> 2) & 7 == m holds the full sum m.
+template <int CGW>
+__device__ __forceinline__ float reduce_scatter8(const float (&x)[8], int lane) {
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+    float y[4], z[2];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {   // off 16: keep the half selected by lane bit 4
+        const float send = b4 ? x[j] : x[j + 4];
+        const float keep = b4 ? x[j + 4] : x[j];
+        y[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {   // off 8
+        const float send = b3 ? y[j] : y[j + 2];
+        const float keep = b3 ? y[j + 2] : y[j];
+        z[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    float w;
+    {                               // off 4
+        const float send = b2 ? z[0] : z[1];
+        const float keep = b2 ? z[1] : z[0];
+        w = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+#pragma unroll
+    for (int off = 2; off >= CGW; off >>= 1) w += __shfl_xor_sync(0xffffffffu, w, off);
+    return w;
+}
+
 template <typename TIn, bool kChannel, int CGW, int kRows>
 __global__ void __launch_bounds__(kThreads) short_seq_kernel(const ShortParams p) {
     constexpr int kWarps = kThreads / 32;
     constexpr int BV = kWarps * CGW * 4;          // columns per CTA
+    constexpr int U = BV / 4;                     // 16-byte units per tile row
     __shared__ __align__(16) float sk[kShortSeqMaxT][128];
     __shared__ __align__(16) float sq[kShortSeqMaxT][128];
     __shared__ __align__(16) float sa[kChannel ? kShortSeqMaxT : 1][128];
     __shared__ __align__(16) float sv[kShortSeqMaxT][BV];
+    __shared__ __align__(16) float stile[128 * BV];
     __shared__ float sbeta[kShortSeqMaxT], skq[kShortSeqMaxT], sas[kShortSeqMaxT];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cg = lane % CGW, rg = lane / CGW;
     const int h = blockIdx.y, b = blockIdx.z;
     const int vt0 = blockIdx.x * BV;              // first column of the CTA's tile
-    const int col = vt0 + warp * CGW * 4 + cg * 4;   // first of this lane's four columns
+    const int ucol = warp * CGW + cg;             // this lane's 16-byte unit within a tile row
     const size_t bh = static_cast<size_t>(b) * p.H + h;
     const int DK = p.DK, T = p.T;
     const int r0 = rg * kRows;
     const bool live = r0 < DK;
+    // swizzled float offset of unit u of tile row i
+    auto tile_at = [&](int i, int u) { return i * BV + ((u ^ (((i / kRows) & 3) << 1)) & (U - 1)) * 4; };
 
-    // 1. state rows of this lane (the long pole: issued first)
-    float4 s[kRows];
-#pragma unroll
-    for (int r = 0; r < kRows; ++r) {
-        s[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (live && p.S0) s[r] = *reinterpret_cast<const float4 *>(p.S0 + (bh * DK + r0 + r) * p.DV + col);
+    // 1. state tile -> shared memory, coalesced, asynchronous
+    if (p.S0) {
+        const float *src = p.S0 + bh * DK * p.DV + vt0;
+        for (int idx = tid; idx < DK * U; idx += kThreads) {
+            const int i = idx / U, u = idx - i * U;
+            cp_async16(&stile[tile_at(i, u)], src + static_cast<size_t>(i) * p.DV + u * 4);
+        }
     }
 
     // 2. every token's vectors into shared memory
@@ -114,61 +159,88 @@ __global__ void __launch_bounds__(kThreads) short_seq_kernel(const ShortParams p
             skq[t] = kq;
         }
     }
+    cp_async_wait_all();
     __syncthreads();
 
-    // 4. the tokens, in order; no block barrier from here on
+    // 4. this lane's rows of the state, as float2 pairs (x, y) and (z, w) of its four columns
+    float2 s[kRows][2];
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (live && p.S0) x = *reinterpret_cast<const float4 *>(&stile[tile_at(r0 + r, ucol)]);
+        s[r][0] = make_float2(x.x, x.y);
+        s[r][1] = make_float2(x.z, x.w);
+    }
+    const int rr = live ? r0 : 0;   // lanes past d_k read row 0 and discard it
+
+    // 5. the tokens, in order; no block barrier from here on
     for (int t = 0; t < T; ++t) {
         const float beta = sbeta[t], kdotq = skq[t];
         const float as = kChannel ? 1.f : sas[t];
-        float kr[kRows], qr[kRows], ar[kRows];
-        const int rr = live ? r0 : 0;   // lanes past d_k read row 0 and discard it
+        float kr[kRows], qr[kRows], ar[kRows], kg[kRows];
         rows_from_smem<kRows>(&sk[t][rr], kr);
         rows_from_smem<kRows>(&sq[t][rr], qr);
-        if constexpr (kChannel) rows_from_smem<kRows>(&sa[t][rr], ar);
-        float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) kg[r] = kr[r];
+        if constexpr (kChannel) {
+            rows_from_smem<kRows>(&sa[t][rr], ar);
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) { kg[r] *= ar[r]; qr[r] *= ar[r]; }   // rows of alpha (.) k, q
+        }
+        // partial S~^T k and S~^T q over this lane's rows (for a scalar gate alpha is applied
+        // after the reduction); packed fp32 FMAs over column pairs
+        float2 pk0 = make_float2(0.f, 0.f), pk1 = pk0, pq0 = pk0, pq1 = pk0;
+        if (live) {
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) {
+                const float2 kk2 = make_float2(kg[r], kg[r]), qq2 = make_float2(qr[r], qr[r]);
+                pk0 = __ffma2_rn(kk2, s[r][0], pk0); pk1 = __ffma2_rn(kk2, s[r][1], pk1);
+                pq0 = __ffma2_rn(qq2, s[r][0], pq0); pq1 = __ffma2_rn(qq2, s[r][1], pq1);
+            }
+        }
+        const float part[8] = {pk0.x, pk0.y, pk1.x, pk1.y, pq0.x, pq0.y, pq1.x, pq1.y};
+        const float red = reduce_scatter8<CGW>(part, lane) * as;   // full sum number (lane >> 2) & 7
+        // every lane needs the four prediction sums of its column group
+        const int src = lane & 3;
+        float pred[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) pred[j] = __shfl_sync(0xffffffffu, red, (j << 2) | src);
+        const float4 vt = *reinterpret_cast<const float4 *>(&sv[t][ucol * 4]);
+        const float e[4] = {vt.x - pred[0], vt.y - pred[1], vt.z - pred[2], vt.w - pred[3]};
+        const int m = (lane >> 2) & 7;
+        if (m >= 4 && (lane & (3 & ~(CGW - 1))) == 0) {   // o = S~^T q + beta e (k . q)
+            const int j = m - 4;
+            const float ej = j == 0 ? e[0] : j == 1 ? e[1] : j == 2 ? e[2] : e[3];
+            static_cast<TIn *>(p.o)[tok(t) * p.DV + vt0 + ucol * 4 + j] = from_f32<TIn>(fmaf(beta * kdotq, ej, red));
+        }
+        // S = S~ + beta k e^T (lanes past d_k update rows they never store)
+        const float2 e01 = make_float2(e[0], e[1]), e23 = make_float2(e[2], e[3]);
 #pragma unroll
         for (int r = 0; r < kRows; ++r) {
-            if (live) {
-                const float a = kChannel ? ar[r] : as;
-                const float ak = a * kr[r], aq = a * qr[r];
-                pk.x = fmaf(ak, s[r].x, pk.x); pk.y = fmaf(ak, s[r].y, pk.y);
-                pk.z = fmaf(ak, s[r].z, pk.z); pk.w = fmaf(ak, s[r].w, pk.w);
-                pq.x = fmaf(aq, s[r].x, pq.x); pq.y = fmaf(aq, s[r].y, pq.y);
-                pq.z = fmaf(aq, s[r].z, pq.z); pq.w = fmaf(aq, s[r].w, pq.w);
-            }
-        }
-#pragma unroll
-        for (int off = CGW; off < 32; off <<= 1) {
-            pk.x += __shfl_xor_sync(0xffffffffu, pk.x, off); pk.y += __shfl_xor_sync(0xffffffffu, pk.y, off);
-            pk.z += __shfl_xor_sync(0xffffffffu, pk.z, off); pk.w += __shfl_xor_sync(0xffffffffu, pk.w, off);
-            pq.x += __shfl_xor_sync(0xffffffffu, pq.x, off); pq.y += __shfl_xor_sync(0xffffffffu, pq.y, off);
-            pq.z += __shfl_xor_sync(0xffffffffu, pq.z, off); pq.w += __shfl_xor_sync(0xffffffffu, pq.w, off);
-        }
-        const float4 vt = *reinterpret_cast<const float4 *>(&sv[t][col - vt0]);
-        float4 e;
-        e.x = vt.x - pk.x; e.y = vt.y - pk.y; e.z = vt.z - pk.z; e.w = vt.w - pk.w;
-        if (rg == 0) {   // o = S~^T q + beta e (k . q)
-            TIn *o = static_cast<TIn *>(p.o) + tok(t) * p.DV + col;
-            const float bkq = beta * kdotq;
-            o[0] = from_f32<TIn>(fmaf(bkq, e.x, pq.x));
-            o[1] = from_f32<TIn>(fmaf(bkq, e.y, pq.y));
-            o[2] = from_f32<TIn>(fmaf(bkq, e.z, pq.z));
-            o[3] = from_f32<TIn>(fmaf(bkq, e.w, pq.w));
-        }
-#pragma unroll
-        for (int r = 0; r < kRows; ++r) {   // S = S~ + beta k e^T
-            if (live) {
-                const float a = kChannel ? ar[r] : as;
-                const float bk = beta * kr[r];
-                s[r].x = fmaf(a, s[r].x, bk * e.x); s[r].y = fmaf(a, s[r].y, bk * e.y);
-                s[r].z = fmaf(a, s[r].z, bk * e.z); s[r].w = fmaf(a, s[r].w, bk * e.w);
-            }
+            const float a = kChannel ? ar[r] : as;
+            const float bk = beta * kr[r];
+            const float2 a2 = make_float2(a, a), bk2 = make_float2(bk, bk);
+            s[r][0] = __ffma2_rn(a2, s[r][0], __fmul2_rn(bk2, e01));
+            s[r][1] = __ffma2_rn(a2, s[r][1], __fmul2_rn(bk2, e23));
         }
     }
+
+    // 6. final state -> shared memory -> HBM, coalesced
     if (p.S_T) {
+        __syncthreads();   // every lane's reads of the incoming tile are done
+        if (live) {
 #pragma unroll
-        for (int r = 0; r < kRows; ++r)
-            if (live) *reinterpret_cast<float4 *>(p.S_T + (bh * DK + r0 + r) * p.DV + col) = s[r];
+            for (int r = 0; r < kRows; ++r)
+                *reinterpret_cast<float4 *>(&stile[tile_at(r0 + r, ucol)]) =
+                    make_float4(s[r][0].x, s[r][0].y, s[r][1].x, s[r][1].y);
+        }
+        __syncthreads();
+        float *dst = p.S_T + bh * DK * p.DV + vt0;
+        for (int idx = tid; idx < DK * U; idx += kThreads) {
+            const int i = idx / U, u = idx - i * U;
+            *reinterpret_cast<float4 *>(dst + static_cast<size_t>(i) * p.DV + u * 4) =
+                *reinterpret_cast<const float4 *>(&stile[tile_at(i, u)]);
+        }
     }
 }
 
