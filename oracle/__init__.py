@@ -7,7 +7,9 @@ calls it, and it imports nothing from the CUDA library.
 Two independent restatements of what the recurrence computes:
 
 * ``recurrent`` -- the plain sequential fp64 recurrence (C, ``kla_oracle.c``),
-  token by token: forget, predict, residual, KLA step size, write, read.
+  token by token: forget, predict, residual, step size (the KLA step, or the raw
+  write strength of DeltaNet / Gated DeltaNet), write, read (with an optional
+  query scale).
   This is the definition the GPU results are compared against.
 * ``chunkwise`` -- an fp64 NumPy restatement of the chunk algebra (cumulative
   log-decay, provisional error, unit-triangular correction, end-of-chunk state
@@ -58,21 +60,27 @@ class Oracle:
     def __init__(self, path: str):
         self.path = path
         self.lib = ctypes.CDLL(path)
-        f = self.lib.kla_oracle_recurrent
+        f = self.lib.kla_oracle_recurrent_ex
         dp = ctypes.POINTER(ctypes.c_double)
         f.argtypes = [dp, dp, dp, dp, ctypes.c_int, dp, ctypes.c_double, dp, dp, dp,
                       ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_long,
-                      ctypes.c_int]
+                      ctypes.c_int, ctypes.c_double, ctypes.c_int]
         f.restype = ctypes.c_int
         self._f = f
 
-    def recurrent(self, q, k, v, alpha, eta, eps, S0=None, nthreads: int = 1):
+    def recurrent(self, q, k, v, alpha, eta, eps, S0=None, nthreads: int = 1, beta_mode: str = "kla",
+                  q_scale: float = 1.0):
         """Run the fp64 recurrence.
 
         q, k: [B,T,H,d_k]; v: [B,T,H,d_v]; alpha: [B,T,H] (scalar gate) or
         [B,T,H,d_k] (per-key-channel gate); eta: [B,T,H]; S0: [B,H,d_k,d_v] or None.
+        beta_mode "kla": beta = eta / (||k||^2 + eps); "raw": beta = eta (DeltaNet /
+        Gated DeltaNet write strength). The read is o_t = S_t^T (q_scale * q_t).
         Returns (o [B,T,H,d_v], S_T [B,H,d_k,d_v]) as float64.
         """
+        modes = {"kla": 0, "raw": 1}
+        if beta_mode not in modes:
+            raise ValueError(f"beta_mode {beta_mode!r}")
         q = np.ascontiguousarray(q, dtype=np.float64)
         k = np.ascontiguousarray(k, dtype=np.float64)
         v = np.ascontiguousarray(v, dtype=np.float64)
@@ -99,7 +107,7 @@ class Oracle:
             return None if a is None else a.ctypes.data_as(dp)
 
         rc = self._f(P(q), P(k), P(v), P(alpha), per_channel, P(eta), float(eps), P(S0), P(o), P(ST),
-                     B, T, H, dk, dv, int(nthreads))
+                     B, T, H, dk, dv, modes[beta_mode], float(q_scale), int(nthreads))
         if rc != 0:
             raise RuntimeError(f"kla_oracle_recurrent failed with {rc}")
         return o, ST

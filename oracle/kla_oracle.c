@@ -14,9 +14,12 @@
  *   2. predict:  p = S~^T k_t
  *   3. residual: e = v_t - p
  *   4. step:     beta = eta_t / (||k_t||^2 + eps)     (beta := 0 if the
- *                denominator is exactly 0)
+ *                denominator is exactly 0)  -- the KLA step (beta_mode 0), or
+ *                beta = eta_t                         -- the raw write strength of
+ *                DeltaNet / Gated DeltaNet (beta_mode 1)
  *   5. write:    S = S~ + beta k_t e^T
- *   6. read:     o_t = S^T q_t               (after the write)
+ *   6. read:     o_t = S^T (s q_t)           (after the write; s = q_scale, 1 by
+ *                default, d_k^{-1/2} in Kimi Delta Attention)
  *
  * Sources (page titles and sections):
  *  - Gist.science "Riepilogo Tecnico: Attenzione Lineare Kaczmarz (KLA)",
@@ -27,7 +30,10 @@
  *  - GeekNews "Revisando las variantes de atencion lineal de la familia DeltaNet",
  *    section "Gated DeltaNet: primero olvidar todo el estado": the mandated order
  *    forget -> predict -> correct -> write; section "Kimi Delta Attention":
- *    the per-key-channel gate and the read after the write.
+ *    the per-key-channel gate and the read after the write, which reads with the
+ *    scaled query d_k^{-1/2} q (and the in-chunk coefficients carry the same s,
+ *    section "KDA por chunks"); section "Gated DeltaNet": beta_t in (0,1) is the
+ *    write strength itself, the plain delta-rule step without the KLA normaliser.
  *  - Paithon "Scrivere meglio nella memoria: gate e delta rule": the key-channel
  *    side of the diagonal gate.
  *
@@ -58,6 +64,8 @@ typedef struct {
     long B, T, H, dk, dv;
     int alpha_per_channel;
     double eps;
+    int beta_mode;        /* 0: beta = eta / (||k||^2 + eps);  1: beta = eta */
+    double q_scale;       /* read with s * q */
     long chain_begin, chain_end;
     int status;
 } job_t;
@@ -118,6 +126,9 @@ static int run_chain(const job_t *J, long b, long h, double *S, double *St, doub
 #else
         double beta = (den == 0.0) ? 0.0 : eta / den;
 #endif
+#if KLA_ORACLE_MUTANT != 8   /* mutant 8: the raw mode still takes the KLA step */
+        if (J->beta_mode == 1) beta = eta;
+#endif
 
         /* 5. write: S = S~ + beta k e^T */
         for (long i = 0; i < dk; ++i) {
@@ -125,8 +136,13 @@ static int run_chain(const job_t *J, long b, long h, double *S, double *St, doub
             for (long j = 0; j < dv; ++j) S[i * dv + j] = St[i * dv + j] + bk * p[j];
         }
 
-        /* 6. read after the write: o = S^T q */
+        /* 6. read after the write: o = S^T (s q) */
         double *ot = J->o + tok * dv;
+#if KLA_ORACLE_MUTANT == 9
+        const double s = 1.0;           /* mutant: the query scale is dropped */
+#else
+        const double s = J->q_scale;
+#endif
         for (long j = 0; j < dv; ++j) ot[j] = 0.0;
 #if KLA_ORACLE_MUTANT == 5
         /* mutant: read before the write */
@@ -138,7 +154,7 @@ static int run_chain(const job_t *J, long b, long h, double *S, double *St, doub
             for (long j = 0; j < dv; ++j) ot[i % dv] += S[i * dv + j] * qt[j % dk];
 #else
         for (long i = 0; i < dk; ++i)
-            for (long j = 0; j < dv; ++j) ot[j] += S[i * dv + j] * qt[i];
+            for (long j = 0; j < dv; ++j) ot[j] += S[i * dv + j] * (s * qt[i]);
 #endif
     }
     if (J->S_T) memcpy(J->S_T + ((b * H + h) * dk) * dv, S, sizeof(double) * dk * dv);
@@ -161,20 +177,25 @@ static void *worker(void *arg)
 /*
  * Runs the recurrence for all B*H chains; chains are split over `nthreads`
  * POSIX threads (each chain is independent, so the split changes no result).
- * Returns 0 on success, -1 on bad arguments, -2 on allocation failure.
+ * beta_mode 0 takes the KLA step, 1 the raw write strength beta = eta; the read
+ * uses q_scale * q. Returns 0 on success, -1 on bad arguments, -2 on allocation
+ * failure.
  */
-int kla_oracle_recurrent(const double *q, const double *k, const double *v,
-                         const double *alpha, int alpha_per_channel,
-                         const double *eta, double eps, const double *S0,
-                         double *o, double *S_T,
-                         long B, long T, long H, long dk, long dv, int nthreads)
+int kla_oracle_recurrent_ex(const double *q, const double *k, const double *v,
+                            const double *alpha, int alpha_per_channel,
+                            const double *eta, double eps, const double *S0,
+                            double *o, double *S_T,
+                            long B, long T, long H, long dk, long dv,
+                            int beta_mode, double q_scale, int nthreads)
 {
-    if (!q || !k || !v || !alpha || !eta || !o || B < 0 || T < 0 || H < 0 || dk < 1 || dv < 1)
+    if (!q || !k || !v || !alpha || !eta || !o || B < 0 || T < 0 || H < 0 || dk < 1 || dv < 1 ||
+        (beta_mode != 0 && beta_mode != 1))
         return -1;
     long chains = B * H;
     if (nthreads < 1) nthreads = 1;
     if (nthreads > chains) nthreads = (int)(chains > 0 ? chains : 1);
-    job_t base = {q, k, v, alpha, eta, S0, o, S_T, B, T, H, dk, dv, alpha_per_channel, eps, 0, 0, 0};
+    job_t base = {q, k, v, alpha, eta, S0, o, S_T, B, T, H, dk, dv, alpha_per_channel, eps,
+                  beta_mode, q_scale, 0, 0, 0};
     job_t *jobs = (job_t *)calloc((size_t)nthreads, sizeof(job_t));
     pthread_t *tid = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
     if (!jobs || !tid) { free(jobs); free(tid); return -2; }
@@ -199,3 +220,14 @@ int kla_oracle_recurrent(const double *q, const double *k, const double *v,
 }
 
 int kla_oracle_mutant_id(void) { return KLA_ORACLE_MUTANT; }
+
+/* The KLA recurrence with the default read (beta_mode 0, q_scale 1). */
+int kla_oracle_recurrent(const double *q, const double *k, const double *v,
+                         const double *alpha, int alpha_per_channel,
+                         const double *eta, double eps, const double *S0,
+                         double *o, double *S_T,
+                         long B, long T, long H, long dk, long dv, int nthreads)
+{
+    return kla_oracle_recurrent_ex(q, k, v, alpha, alpha_per_channel, eta, eps, S0, o, S_T,
+                                   B, T, H, dk, dv, 0, 1.0, nthreads);
+}

@@ -31,10 +31,11 @@ def _one(x):
     return x.reshape((1, x.shape[0], 1) + x.shape[1:])
 
 
-def _run(orc, q, k, v, alpha, eta, eps, S0=None):
-    """Single chain helper: q,k [T,dk], v [T,dv], alpha [T] or [T,dk], eta [T], S0 [dk,dv]."""
+def _run(orc, q, k, v, alpha, eta, eps, S0=None, **mode):
+    """Single chain helper: q,k [T,dk], v [T,dv], alpha [T] or [T,dk], eta [T], S0 [dk,dv].
+    ``mode``: beta_mode / q_scale of the oracle (KLA step and unscaled read by default)."""
     s0 = None if S0 is None else np.asarray(S0, dtype=np.float64)[None, None]
-    o, ST = orc.recurrent(_one(q), _one(k), _one(v), _one(alpha), _one(eta), eps, s0)
+    o, ST = orc.recurrent(_one(q), _one(k), _one(v), _one(alpha), _one(eta), eps, s0, **mode)
     return o[0, :, 0], ST[0, 0]
 
 
@@ -293,9 +294,101 @@ def pin_zero_key(orc):
     _close(o[0], (0.6 * S0).T @ q[0], 1e-14, "zero key read")
 
 
+def pin_raw_beta_worked(orc):
+    """[PB] 'Correggere: la delta rule' read in the raw-beta mode (beta = eta, the write
+    strength of DeltaNet and Gated DeltaNet): the phone-book numbers with a unit label
+    (7 -> 8.5 at half knob, 10 at full, 7 at zero), and the marker label of squared norm 2
+    at full knob overshooting 7 -> 13 -> 7 -> 13, where the KLA step lands on 10."""
+    gd = _golden()
+    for key in ("phone_book_half", "phone_book_full", "phone_book_zero"):
+        g = gd[key]
+        kk = np.array([[g["key"]]])
+        o, ST = _run(orc, kk, kk, np.array([[g["value"]]]), np.ones(1), np.array([g["knob"]]), 0.3,
+                     np.array([[g["state"]]]), beta_mode="raw")
+        assert abs(o[0, 0] - g["printed"]) <= 1e-12, (key, o[0, 0])
+        assert abs(ST[0, 0] - g["printed"]) <= 1e-12, (key, ST[0, 0])
+    g = gd["marker_overshoot"]
+    n = len(g["printed_sequence"])
+    kk = np.full((n, 1), np.sqrt(g["key_norm_sq"]))
+    S0 = np.array([[g["state_read"] / np.sqrt(g["key_norm_sq"])]])
+    v = np.full((n, 1), g["value"])
+    o, _ = _run(orc, kk, kk, v, np.ones(n), np.full(n, g["raw_beta"]), 0.0, S0, beta_mode="raw")
+    _close(o[:, 0], g["printed_sequence"], 1e-13, "raw-beta overshoot sequence")
+    o, _ = _run(orc, kk, kk, v, np.ones(n), np.full(n, g["raw_beta"]), 0.0, S0, beta_mode="kla")
+    _close(o[:, 0], np.full(n, g["value"]), 1e-13, "KLA step on the same tokens")
+
+
+def pin_raw_beta_first_write_and_limits(orc):
+    """[PB] 'Tutto e regressione online': from an empty memory with the knob at half, the first
+    write is half of what blind summing writes (S_1 = beta v k^T); [PB] 'Unire oblio e
+    correzione': with beta -> 0 the write switches off with the correction and the memory only
+    fades (S_t = alpha_t S_{t-1}), and with alpha = 1 the pure delta rule remains, whose
+    re-read along a unit key is (1 - beta) S^T k + beta v."""
+    rng = np.random.default_rng(31)
+    dk, dv = 6, 4
+    k = rng.normal(size=(1, dk))
+    k /= np.linalg.norm(k)
+    v = rng.normal(size=(1, dv))
+    q = rng.normal(size=(1, dk))
+    o, ST = _run(orc, q, k, v, np.ones(1), np.array([0.5]), 1e-3, None, beta_mode="raw")
+    _close(ST, 0.5 * np.outer(k[0], v[0]), 1e-15, "first write at half knob")
+    _close(o[0], 0.5 * (k[0] @ q[0]) * v[0], 1e-14, "first read at half knob")
+    T = 5
+    S0 = rng.normal(size=(dk, dv))
+    a = rng.uniform(0.5, 1.0, size=T)
+    qs = rng.normal(size=(T, dk))
+    ks = rng.normal(size=(T, dk))
+    o, ST = _run(orc, qs, ks, rng.normal(size=(T, dv)), a, np.zeros(T), 0.0, S0, beta_mode="raw")
+    _close(ST, np.prod(a) * S0, 1e-13, "beta = 0 leaves only the fade")
+    for t in range(T):
+        _close(o[t], np.prod(a[: t + 1]) * (S0.T @ qs[t]), 1e-12, f"faded read t={t}")
+    o, _ = _run(orc, k, k, v, np.ones(1), np.array([0.3]), 5.0, S0, beta_mode="raw")
+    _close(o[0], 0.7 * (S0.T @ k[0]) + 0.3 * v[0], 1e-12, "pure delta rule re-read")
+
+
+def pin_raw_beta_is_kla_with_rescaled_eta(orc):
+    """Both step sizes write beta k e^T with the same residual, so the raw mode fed
+    eta_t / (||k_t||^2 + eps) reproduces the KLA step fed eta_t, for any gate."""
+    rng = np.random.default_rng(32)
+    T, dk, dv = 9, 5, 4
+    for per_channel in (False, True):
+        q, k = rng.normal(size=(T, dk)), rng.normal(size=(T, dk)) * rng.uniform(0.3, 3.0, size=(T, 1))
+        v = rng.normal(size=(T, dv))
+        a = rng.uniform(0.4, 1.0, size=(T, dk) if per_channel else (T,))
+        eta, eps = rng.uniform(0.1, 1.0, size=T), 0.25
+        S0 = rng.normal(size=(dk, dv))
+        o1, s1 = _run(orc, q, k, v, a, eta, eps, S0)
+        o2, s2 = _run(orc, q, k, v, a, eta / (np.sum(k * k, axis=1) + eps), 123.0, S0, beta_mode="raw")
+        _close(o2, o1, 1e-12, "raw vs KLA outputs")
+        _close(s2, s1, 1e-12, "raw vs KLA states")
+
+
+def pin_query_scale(orc):
+    """[GN] 'Kimi Delta Attention': the read is o_t = S_t (d_k^{-1/2} q_t), and 'KDA por
+    chunks' carries the same s in every read coefficient. From an empty state one token
+    writes beta v k^T, so o_1 = s beta (k . q) v; the scale touches the read only."""
+    rng = np.random.default_rng(33)
+    dk, dv = 16, 3
+    s = dk ** -0.5
+    q, k, v = rng.normal(size=(1, dk)), rng.normal(size=(1, dk)), rng.normal(size=(1, dv))
+    beta = 0.8 / (k[0] @ k[0] + 1e-2)
+    o, ST = _run(orc, q, k, v, np.array([0.9]), np.array([0.8]), 1e-2, None, q_scale=s)
+    _close(ST, beta * np.outer(k[0], v[0]), 1e-14, "one write from zero")
+    _close(o[0], s * beta * (k[0] @ q[0]) * v[0], 1e-13, "scaled read of one write")
+    T = 7
+    q, k, v = rng.normal(size=(T, dk)), rng.normal(size=(T, dk)), rng.normal(size=(T, dv))
+    a, eta = rng.uniform(0.5, 1.0, size=(T, dk)), rng.uniform(0.1, 1.0, size=T)
+    S0 = rng.normal(size=(dk, dv))
+    o1, s1 = _run(orc, q, k, v, a, eta, 1e-3, S0)
+    o2, s2 = _run(orc, q, k, v, a, eta, 1e-3, S0, q_scale=s)
+    _close(o2, s * o1, 1e-13, "outputs scale with s")
+    _close(s2, s1, 0.0, "state does not see s")
+
+
 PINS = [
     pin_unrelaxed_constraint, pin_deltanet_reread, pin_pure_decay, pin_orthogonal_locality,
     pin_worked_scalar, pin_marker_overshoot, pin_transition_eigen, pin_gradient_step,
     pin_linear_attention_split, pin_dplr_transition, pin_chunkwise_equals_recurrent,
-    pin_continuation, pin_zero_key,
+    pin_continuation, pin_zero_key, pin_raw_beta_worked, pin_raw_beta_first_write_and_limits,
+    pin_raw_beta_is_kla_with_rescaled_eta, pin_query_scale,
 ]
