@@ -4,7 +4,11 @@ The recurrence (Gist.science, "Riepilogo Tecnico: Attenzione Lineare Kaczmarz (K
 for each sequence and head, a d_k x d_v state S is carried over tokens with
 ``S~ = alpha (.) S``, ``e = v - S~^T k``, ``beta = eta / (||k||^2 + eps)``,
 ``S = S~ + beta k e^T`` and the read ``o = S^T q`` after the write. ``alpha`` is a
-scalar per token and head, or one value per key channel.
+scalar per token and head, or one value per key channel. ``beta_mode="raw"`` takes
+``beta = eta`` instead (the write strength of DeltaNet / Gated DeltaNet), and
+``q_scale`` reads with a scaled query, ``o = S^T (s q)`` (GeekNews, "Revisando las
+variantes de atencion lineal de la familia DeltaNet", sections "Gated DeltaNet" and
+"Kimi Delta Attention").
 
 ``chunk_fwd`` runs the chunkwise prefill and ``decode_step`` one fused
 single-token step. Both call the C ABI of ``include/kla.h`` through ctypes; torch
@@ -51,6 +55,15 @@ def _stream_ptr(device) -> int:
     return torch.cuda.current_stream(device).cuda_stream
 
 
+_BETA_MODES = {"kla": _native.KLA_BETA_KACZMARZ, "raw": _native.KLA_BETA_RAW}
+
+
+def _beta_code(beta_mode: str) -> int:
+    if beta_mode not in _BETA_MODES:
+        raise ValueError(f"beta_mode must be 'kla' or 'raw', got {beta_mode!r}")
+    return _BETA_MODES[beta_mode]
+
+
 def workspace_size(B: int, T: int, H: int, d_k: int, d_v: int, chunk: int = 64,
                    dtype: torch.dtype = torch.bfloat16, per_channel_gate: bool = False) -> int:
     """Device scratch bytes ``chunk_fwd`` needs for these sizes (0 when none)."""
@@ -63,14 +76,18 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, alpha: torch.Te
               eps: float = 1e-6, S0: Optional[torch.Tensor] = None, *, chunk: int = 64,
               out: Optional[torch.Tensor] = None, final_state: bool = True,
               S_T: Optional[torch.Tensor] = None,
-              workspace: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+              workspace: Optional[torch.Tensor] = None, beta_mode: str = "kla",
+              q_scale: float = 1.0) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """Chunkwise KLA prefill.
 
     q, k: [B,T,H,d_k]; v: [B,T,H,d_v] (bf16 or fp32, same dtype); alpha: fp32 [B,T,H]
     (scalar gate) or [B,T,H,d_k] (per-key-channel gate); eta: fp32 [B,T,H];
     S0: fp32 [B,H,d_k,d_v] or None (zeros). Returns (o [B,T,H,d_v] in q's dtype,
     S_T fp32 [B,H,d_k,d_v] or None). ``S_T`` may be passed (it may be ``S0`` itself).
+    ``beta_mode``: "kla" (beta = eta / (||k||^2 + eps)) or "raw" (beta = eta);
+    ``q_scale``: o = S^T (q_scale q).
     """
+    bcode = _beta_code(beta_mode)
     for n, t in (("q", q), ("k", k), ("v", v)):
         _check_dev(n, t)
     dcode = _dtype_code(q)
@@ -108,20 +125,23 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, alpha: torch.Te
     if ws_need and workspace is None:
         workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = _native.lib().kla_chunk_fwd(
+    st = _native.lib().kla_chunk_fwd_ex(
         _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(eta), float(eps), _ptr(S0), _ptr(out), _ptr(S_T),
-        B, T, H, d_k, d_v, int(chunk), dcode, gate, _ptr(workspace), ws_bytes, _stream_ptr(q.device))
-    _native.check(st, "kla_chunk_fwd")
+        B, T, H, d_k, d_v, int(chunk), dcode, gate, bcode, float(q_scale), _ptr(workspace), ws_bytes,
+        _stream_ptr(q.device))
+    _native.check(st, "kla_chunk_fwd_ex")
     return out, S_T
 
 
 def decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, alpha: torch.Tensor, eta: torch.Tensor,
-                S: torch.Tensor, eps: float = 1e-6, *, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+                S: torch.Tensor, eps: float = 1e-6, *, out: Optional[torch.Tensor] = None,
+                beta_mode: str = "kla", q_scale: float = 1.0) -> torch.Tensor:
     """One fused KLA token step for B sequences; ``S`` (fp32 [B,H,d_k,d_v]) is updated in place.
 
     q, k: [B,H,d_k]; v: [B,H,d_v]; alpha: fp32 [B,H] or [B,H,d_k]; eta: fp32 [B,H].
-    Returns o [B,H,d_v] in q's dtype.
+    Returns o [B,H,d_v] in q's dtype. ``beta_mode`` and ``q_scale`` as in ``chunk_fwd``.
     """
+    bcode = _beta_code(beta_mode)
     for n, t in (("q", q), ("k", k), ("v", v)):
         _check_dev(n, t)
     dcode = _dtype_code(q)
@@ -144,10 +164,10 @@ def decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, alpha: torch.
         out = torch.empty((B, H, d_v), dtype=q.dtype, device=q.device)
     else:
         _check_dev("out", out, q.dtype)
-    st = _native.lib().kla_decode_step(
+    st = _native.lib().kla_decode_step_ex(
         _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(eta), float(eps), _ptr(S), _ptr(out),
-        B, H, d_k, d_v, dcode, gate, _stream_ptr(q.device))
-    _native.check(st, "kla_decode_step")
+        B, H, d_k, d_v, dcode, gate, bcode, float(q_scale), _stream_ptr(q.device))
+    _native.check(st, "kla_decode_step_ex")
     return out
 
 

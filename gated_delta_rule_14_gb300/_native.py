@@ -21,6 +21,8 @@ KLA_DTYPE_F32 = 0
 KLA_DTYPE_BF16 = 1
 KLA_GATE_SCALAR = 0
 KLA_GATE_CHANNEL = 1
+KLA_BETA_KACZMARZ = 0
+KLA_BETA_RAW = 1
 
 _lock = threading.Lock()
 _lib = None
@@ -43,10 +45,16 @@ def _declare(lib):
     lib.kla_chunk_fwd.argtypes = [vp, vp, vp, fp, fp, ctypes.c_float, fp, vp, fp,
                                   i, i, i, i, i, i, i, i, vp, sz, vp]
     lib.kla_chunk_fwd.restype = ctypes.c_int
+    lib.kla_chunk_fwd_ex.argtypes = [vp, vp, vp, fp, fp, ctypes.c_float, fp, vp, fp,
+                                     i, i, i, i, i, i, i, i, i, ctypes.c_float, vp, sz, vp]
+    lib.kla_chunk_fwd_ex.restype = ctypes.c_int
     lib.kla_chunk_fwd_workspace_size.argtypes = [i, i, i, i, i, i, i, i]
     lib.kla_chunk_fwd_workspace_size.restype = sz
     lib.kla_decode_step.argtypes = [vp, vp, vp, fp, fp, ctypes.c_float, fp, vp, i, i, i, i, i, i, vp]
     lib.kla_decode_step.restype = ctypes.c_int
+    lib.kla_decode_step_ex.argtypes = [vp, vp, vp, fp, fp, ctypes.c_float, fp, vp, i, i, i, i, i, i, i,
+                                       ctypes.c_float, vp]
+    lib.kla_decode_step_ex.restype = ctypes.c_int
     lib.kla_device_status.argtypes = [vp]
     lib.kla_device_status.restype = ctypes.c_int
     lib.kla_status_string.argtypes = [ctypes.c_int]

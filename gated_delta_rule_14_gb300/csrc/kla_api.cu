@@ -53,6 +53,11 @@ kla_status check_common(const void *q, const void *k, const void *v, const float
     return KLA_OK;
 }
 
+// Step-size mode known and query scale finite.
+bool valid_mode(kla_beta_mode m, float q_scale) {
+    return (m == KLA_BETA_KACZMARZ || m == KLA_BETA_RAW) && q_scale == q_scale && q_scale - q_scale == 0.0f;
+}
+
 // [lo, hi) byte range of a buffer, for overlap checks.
 struct Span {
     uintptr_t lo, hi;
@@ -67,7 +72,7 @@ bool overlaps(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi; }
 
 extern "C" {
 
-int kla_abi_version(void) { return 100; }
+int kla_abi_version(void) { return 101; }
 
 const char *kla_status_string(kla_status s) {
     switch (s) {
@@ -89,11 +94,12 @@ size_t kla_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v, int c
     return kla::chunk_tc_supports(a) ? kla::chunk_tc_workspace_bytes(B, T, H) : 0;
 }
 
-kla_status kla_chunk_fwd(const void *q, const void *k, const void *v, const float *alpha, const float *eta,
-                         float eps, const float *S0, void *o, float *S_T, int B, int T, int H, int d_k, int d_v,
-                         int chunk, kla_dtype dtype, kla_gate gate, void *workspace, size_t workspace_bytes,
-                         void *stream) {
+kla_status kla_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *alpha, const float *eta,
+                            float eps, const float *S0, void *o, float *S_T, int B, int T, int H, int d_k, int d_v,
+                            int chunk, kla_dtype dtype, kla_gate gate, kla_beta_mode beta_mode, float q_scale,
+                            void *workspace, size_t workspace_bytes, void *stream) {
     if (T < 0) return KLA_ERR_INVALID_ARG;
+    if (!valid_mode(beta_mode, q_scale)) return KLA_ERR_INVALID_ARG;
     kla_status st = check_common(q, k, v, alpha, eta, o, B, H, d_k, d_v, dtype, gate, 16,
                                  static_cast<size_t>(B) * T * H);
     if (st != KLA_OK) return st;
@@ -128,6 +134,8 @@ kla_status kla_chunk_fwd(const void *q, const void *k, const void *v, const floa
 
     kla::ChunkArgs a{q, k, v, alpha, eta, eps, S0, o, S_T, B, T, H, d_k, d_v, chunk, dtype, gate,
                      workspace, workspace_bytes, nullptr, cs};
+    a.beta_raw = beta_mode == KLA_BETA_RAW;
+    a.q_scale = q_scale;
     if (err_word(&a.err) != cudaSuccess) return KLA_ERR_CUDA;
     cudaError_t e = kla::short_seq_supports(a) ? kla::launch_short_seq(a)
                     : kla::chunk_tc_supports(a) ? kla::launch_chunk_tc(a)
@@ -135,9 +143,18 @@ kla_status kla_chunk_fwd(const void *q, const void *k, const void *v, const floa
     return e == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
 }
 
-kla_status kla_decode_step(const void *q, const void *k, const void *v, const float *alpha, const float *eta,
-                           float eps, float *S, void *o, int B, int H, int d_k, int d_v, kla_dtype dtype,
-                           kla_gate gate, void *stream) {
+kla_status kla_chunk_fwd(const void *q, const void *k, const void *v, const float *alpha, const float *eta,
+                         float eps, const float *S0, void *o, float *S_T, int B, int T, int H, int d_k, int d_v,
+                         int chunk, kla_dtype dtype, kla_gate gate, void *workspace, size_t workspace_bytes,
+                         void *stream) {
+    return kla_chunk_fwd_ex(q, k, v, alpha, eta, eps, S0, o, S_T, B, T, H, d_k, d_v, chunk, dtype, gate,
+                            KLA_BETA_KACZMARZ, 1.0f, workspace, workspace_bytes, stream);
+}
+
+kla_status kla_decode_step_ex(const void *q, const void *k, const void *v, const float *alpha, const float *eta,
+                              float eps, float *S, void *o, int B, int H, int d_k, int d_v, kla_dtype dtype,
+                              kla_gate gate, kla_beta_mode beta_mode, float q_scale, void *stream) {
+    if (!valid_mode(beta_mode, q_scale)) return KLA_ERR_INVALID_ARG;
     kla_status st = check_common(q, k, v, alpha, eta, o, B, H, d_k, d_v, dtype, gate, 0, 1);
     if (st != KLA_OK) return st;
     if (!S || !aligned16(S)) return KLA_ERR_INVALID_ARG;
@@ -152,8 +169,17 @@ kla_status kla_decode_step(const void *q, const void *k, const void *v, const fl
         if (overlaps(s, x)) return KLA_ERR_INVALID_ARG;
     kla::DecodeArgs a{q, k, v, alpha, eta, eps, S, o, B, H, d_k, d_v, dtype, gate, nullptr,
                       static_cast<cudaStream_t>(stream)};
+    a.beta_raw = beta_mode == KLA_BETA_RAW;
+    a.q_scale = q_scale;
     if (err_word(&a.err) != cudaSuccess) return KLA_ERR_CUDA;
     return kla::launch_decode(a) == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
+}
+
+kla_status kla_decode_step(const void *q, const void *k, const void *v, const float *alpha, const float *eta,
+                           float eps, float *S, void *o, int B, int H, int d_k, int d_v, kla_dtype dtype,
+                           kla_gate gate, void *stream) {
+    return kla_decode_step_ex(q, k, v, alpha, eta, eps, S, o, B, H, d_k, d_v, dtype, gate, KLA_BETA_KACZMARZ,
+                              1.0f, stream);
 }
 
 kla_status kla_device_status(void *stream) {

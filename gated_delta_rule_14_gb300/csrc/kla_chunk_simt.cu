@@ -38,6 +38,8 @@ struct SimtParams {
     void *o;
     float *S_T;
     int B, T, H, DK, DV, C, BV;
+    int beta_raw;
+    float q_scale;
 };
 
 template <typename TIn, bool kChannel>
@@ -118,7 +120,7 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(const SimtParams p
             const int i = tid - 32;
             float n2 = 0.f;
             for (int ch = 0; ch < DK; ++ch) n2 = fmaf(sK[i * DK + ch], sK[i * DK + ch], n2);
-            sBeta[i] = kla_beta(sEta[i], n2, p.eps);
+            sBeta[i] = kla_beta(sEta[i], n2, p.eps, p.beta_raw);
         }
         __syncthreads();
         // ---- R, A and the right-hand sides
@@ -173,7 +175,7 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(const SimtParams p
             sU[idx] = acc;
         }
         __syncthreads();
-        // ---- O = (exp(G) . Q) S + A E
+        // ---- O = s ((exp(G) . Q) S + A E)
         for (int idx = tid; idx < C * BV; idx += kThreads) {
             const int i = idx / BV, m = idx % BV;
             if (i >= L) continue;
@@ -183,7 +185,7 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(const SimtParams p
                 acc = fmaf(expf(G) * sQ[i * DK + ch], sS[ch * BV + m], acc);
             }
             for (int j = 0; j <= i; ++j) acc = fmaf(sA[i * C + j], sU[j * BV + m], acc);
-            o[((static_cast<size_t>(b) * p.T + t0 + i) * p.H + h) * p.DV + v0 + m] = from_f32<TIn>(acc);
+            o[((static_cast<size_t>(b) * p.T + t0 + i) * p.H + h) * p.DV + v0 + m] = from_f32<TIn>(p.q_scale * acc);
         }
         __syncthreads();
         // ---- S' = exp(G_end) . S + K_end^T E
@@ -214,7 +216,7 @@ size_t simt_smem_bytes(int DK, int C, int BV, bool channel) {
 template <typename TIn, bool kChannel>
 cudaError_t launch_t(const ChunkArgs &a) {
     SimtParams p{a.q, a.k, a.v, a.alpha, a.eta, a.eps, a.S0, a.o, a.S_T,
-                 a.B, a.T, a.H, a.d_k, a.d_v, a.chunk, std::min(a.d_v, 32)};
+                 a.B, a.T, a.H, a.d_k, a.d_v, a.chunk, std::min(a.d_v, 32), a.beta_raw, a.q_scale};
     const size_t smem = simt_smem_bytes(p.DK, p.C, p.BV, kChannel);
     cudaError_t e = cudaFuncSetAttribute(chunk_simt_kernel<TIn, kChannel>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));

@@ -139,6 +139,8 @@ struct TcParams {
     int zero_v;    // treat v as zero (U = 0): the transition run of a segment
     int no_out;    // 0: write o; 1: no output; 2: only the chain's first segment writes o
     unsigned *err;
+    int beta_raw;  // 1: beta = eta
+    float q_scale; // o = S^T (q_scale q)
 };
 
 __device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x << 16); }
@@ -378,7 +380,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             n2 += __shfl_xor_sync(0xffffffffu, n2, 2);
         }
         gsync();   // eta of this chunk visible
-        if ((gtid & 3) == 0) cv.beta[gtid >> 2] = kla_beta(cv.eta[gtid >> 2], n2, p.eps);
+        if ((gtid & 3) == 0) cv.beta[gtid >> 2] = kla_beta(cv.eta[gtid >> 2], n2, p.eps, p.beta_raw);
         uint32_t kb_stride = 16384, kb_base = qk;   // B operand of [K;Q] K^T: raw K rows
         if constexpr (kCh) {
             // Scaled tiles with reference token r: K_r = K e^{G-G_r}, Q_r = Q e^{G-G_r} (in place),
@@ -822,11 +824,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tmem_ld16(tlane + TM_1B + 32 * half + 16 * pc, qs);
                 tmem_ld16(tlane + TM_3 + 32 * half + 16 * pc, ae);
                 tmem_ld_wait();
-                float o[16];
+                float o[16];   // s (e^G Q S + A E)
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj)
-                    o[jj] = fmaf(kCh ? 1.f : cv.eG[32 * half + 16 * pc + jj], __uint_as_float(qs[jj]),
-                                 __uint_as_float(ae[jj]));
+                    o[jj] = p.q_scale * fmaf(kCh ? 1.f : cv.eG[32 * half + 16 * pc + jj], __uint_as_float(qs[jj]),
+                                             __uint_as_float(ae[jj]));
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj) {
                     const float mine = odd ? o[jj + 8] : o[jj];
@@ -992,7 +994,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a) {
     const int chains = a.B * a.H;
     const SegPlan pl = make_plan(a.B, a.T, a.H);
     TcParams p{a.alpha, a.eta, a.eps, a.S0, a.S_T, a.B, a.T, a.H, pl.seg_len, 0, 1, pl.nseg,
-               kS0Chain, kSTLast, 0, 0, a.err};
+               kS0Chain, kSTLast, 0, 0, a.err, a.beta_raw, a.q_scale};
     if (pl.nseg <= 1) {
         kern<<<chains, kThreads, SMEM_BYTES, a.stream>>>(mq, mk, mv, mo, p);
         return cudaGetLastError();

@@ -31,6 +31,8 @@ struct DecodeParams {
     float *S;
     void *o;
     int B, H, DK, DV, BV;
+    int beta_raw;
+    float q_scale;
 };
 
 template <typename TIn, bool kChannel, int NCG>   // NCG = float4 column groups per tile (BV / 4)
@@ -77,7 +79,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
     float knorm2 = 0.f, kdotq = 0.f;
 #pragma unroll
     for (int w = 0; w < kThreads / 32; ++w) { knorm2 += snorm[0][w]; kdotq += snorm[1][w]; }
-    const float beta = kla_beta(p.eta[bh], knorm2, p.eps);
+    const float beta = kla_beta(p.eta[bh], knorm2, p.eps, p.beta_raw);
     const float a_scalar = kChannel ? 1.f : p.alpha[bh];
 
     // Partial reductions over this thread's rows of the decayed state.
@@ -120,13 +122,13 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
     e.x = to_f32(vv[0]) - pred.x; e.y = to_f32(vv[1]) - pred.y;
     e.z = to_f32(vv[2]) - pred.z; e.w = to_f32(vv[3]) - pred.w;
 
-    if (rg == 0) {   // o = S~^T q + beta e (k . q)
+    if (rg == 0) {   // o = s (S~^T q + beta e (k . q))
         TIn *o = static_cast<TIn *>(p.o) + bh * p.DV + v0 + cg * 4;
-        const float bkq = beta * kdotq;
-        o[0] = from_f32<TIn>(fmaf(bkq, e.x, rd.x));
-        o[1] = from_f32<TIn>(fmaf(bkq, e.y, rd.y));
-        o[2] = from_f32<TIn>(fmaf(bkq, e.z, rd.z));
-        o[3] = from_f32<TIn>(fmaf(bkq, e.w, rd.w));
+        const float bkq = beta * kdotq, sc = p.q_scale;
+        o[0] = from_f32<TIn>(sc * fmaf(bkq, e.x, rd.x));
+        o[1] = from_f32<TIn>(sc * fmaf(bkq, e.y, rd.y));
+        o[2] = from_f32<TIn>(sc * fmaf(bkq, e.z, rd.z));
+        o[3] = from_f32<TIn>(sc * fmaf(bkq, e.w, rd.w));
     }
     // S = S~ + beta k e^T
 #pragma unroll
@@ -146,7 +148,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
 template <typename TIn, bool kChannel>
 cudaError_t launch_t(const DecodeArgs &a) {
     const int BV = std::min(a.d_v, 32);
-    DecodeParams p{a.q, a.k, a.v, a.alpha, a.eta, a.eps, a.S, a.o, a.B, a.H, a.d_k, a.d_v, BV};
+    DecodeParams p{a.q, a.k, a.v, a.alpha, a.eta, a.eps, a.S, a.o, a.B, a.H, a.d_k, a.d_v, BV, a.beta_raw, a.q_scale};
     dim3 grid(a.d_v / BV, a.H, a.B);
     if (BV == 32) decode_kernel<TIn, kChannel, 8><<<grid, kThreads, 0, a.stream>>>(p);
     else decode_kernel<TIn, kChannel, 4><<<grid, kThreads, 0, a.stream>>>(p);

@@ -30,6 +30,8 @@ struct ChunkArgs {
     size_t workspace_bytes;
     unsigned *err;         // device error word
     cudaStream_t stream;
+    int beta_raw;          // 1: beta = eta (KLA_BETA_RAW)
+    float q_scale;         // o = S^T (q_scale q)
 };
 
 struct DecodeArgs {
@@ -43,6 +45,8 @@ struct DecodeArgs {
     kla_gate gate;
     unsigned *err;         // device error word
     cudaStream_t stream;
+    int beta_raw;          // 1: beta = eta (KLA_BETA_RAW)
+    float q_scale;         // o = S^T (q_scale q)
 };
 
 // fp32 CUDA-core chunk path: any supported size, fp32 or bf16 storage.
@@ -73,8 +77,10 @@ template <typename T> __device__ __forceinline__ T from_f32(float x);
 template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
-// beta = eta / (||k||^2 + eps), 0 when the denominator is exactly zero.
-__device__ __forceinline__ float kla_beta(float eta, float knorm2, float eps) {
+// beta = eta / (||k||^2 + eps), 0 when the denominator is exactly zero; beta = eta in the
+// raw mode (DeltaNet / Gated DeltaNet write strength).
+__device__ __forceinline__ float kla_beta(float eta, float knorm2, float eps, int raw) {
+    if (raw) return eta;
     const float den = knorm2 + eps;
     return den == 0.0f ? 0.0f : eta / den;
 }

@@ -28,6 +28,8 @@ struct ShortParams {
     void *o;
     float *S_T;
     int B, T, H, DK, DV;
+    int beta_raw;
+    float q_scale;
 };
 
 // Lane layout. A warp owns CGW float4 column groups (CGW * 4 value columns) over ALL d_k rows,
@@ -155,7 +157,7 @@ __global__ void __launch_bounds__(kThreads) short_seq_kernel(const ShortParams p
             kq += __shfl_xor_sync(0xffffffffu, kq, off);
         }
         if (lane == 0) {
-            sbeta[t] = kla_beta(sbeta[t], kk, p.eps);
+            sbeta[t] = kla_beta(sbeta[t], kk, p.eps, p.beta_raw);
             skq[t] = kq;
         }
     }
@@ -208,10 +210,11 @@ __global__ void __launch_bounds__(kThreads) short_seq_kernel(const ShortParams p
         const float4 vt = *reinterpret_cast<const float4 *>(&sv[t][ucol * 4]);
         const float e[4] = {vt.x - pred[0], vt.y - pred[1], vt.z - pred[2], vt.w - pred[3]};
         const int m = (lane >> 2) & 7;
-        if (m >= 4 && (lane & (3 & ~(CGW - 1))) == 0) {   // o = S~^T q + beta e (k . q)
+        if (m >= 4 && (lane & (3 & ~(CGW - 1))) == 0) {   // o = s (S~^T q + beta e (k . q))
             const int j = m - 4;
             const float ej = j == 0 ? e[0] : j == 1 ? e[1] : j == 2 ? e[2] : e[3];
-            static_cast<TIn *>(p.o)[tok(t) * p.DV + vt0 + ucol * 4 + j] = from_f32<TIn>(fmaf(beta * kdotq, ej, red));
+            static_cast<TIn *>(p.o)[tok(t) * p.DV + vt0 + ucol * 4 + j] =
+                from_f32<TIn>(p.q_scale * fmaf(beta * kdotq, ej, red));
         }
         // S = S~ + beta k e^T (lanes past d_k update rows they never store)
         const float2 e01 = make_float2(e[0], e[1]), e23 = make_float2(e[2], e[3]);
@@ -259,7 +262,8 @@ cudaError_t launch_rows(const ChunkArgs &a, const ShortParams &p, dim3 grid) {
 template <typename TIn, bool kChannel>
 cudaError_t launch_t(const ChunkArgs &a) {
     const int BV = std::min(a.d_v, 32);   // d_v is 16, 32, 64 or 128
-    ShortParams p{a.q, a.k, a.v, a.alpha, a.eta, a.eps, a.S0, a.o, a.S_T, a.B, a.T, a.H, a.d_k, a.d_v};
+    ShortParams p{a.q, a.k, a.v, a.alpha, a.eta, a.eps, a.S0, a.o, a.S_T, a.B, a.T, a.H, a.d_k, a.d_v, a.beta_raw,
+                  a.q_scale};
     dim3 grid(a.d_v / BV, a.H, a.B);
     return BV == 32 ? launch_rows<TIn, kChannel, 2>(a, p, grid) : launch_rows<TIn, kChannel, 1>(a, p, grid);
 }

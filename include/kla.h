@@ -12,6 +12,13 @@
  *     S_t   = S~_t + beta_t k_t e_t^T              write
  *     o_t   = S_t^T q_t                            read, after the write
  *
+ * The _ex entry points add two options (GeekNews, "Revisando las variantes de
+ * atencion lineal de la familia DeltaNet", sections "Gated DeltaNet: primero
+ * olvidar todo el estado" and "Kimi Delta Attention"):
+ * beta_t = eta_t itself, the write strength of DeltaNet and Gated DeltaNet
+ * (KLA_BETA_RAW), and a query scale s on the read, o_t = S_t^T (s q_t)
+ * (s = d_k^{-1/2} in Kimi Delta Attention).
+ *
  * alpha_t is one scalar per (b, t, h) (Gated DeltaNet / KLA gate) or one value per
  * key channel (Kimi Delta Attention gate: GeekNews, "Revisando las variantes de
  * atencion lineal de la familia DeltaNet", section "Kimi Delta Attention"), in
@@ -60,6 +67,11 @@ typedef enum kla_gate {
     KLA_GATE_CHANNEL = 1       /* alpha [B, T, H, d_k]: one gate per key channel */
 } kla_gate;
 
+typedef enum kla_beta_mode {
+    KLA_BETA_KACZMARZ = 0,     /* beta = eta / (||k||^2 + eps): the KLA step */
+    KLA_BETA_RAW = 1           /* beta = eta: DeltaNet / Gated DeltaNet write strength; eps unused */
+} kla_beta_mode;
+
 /*
  * Chunkwise prefill (GeekNews page above, section "KDA por chunks: reordenar la
  * recurrencia como multiplicaciones de matrices"; the KLA page, section
@@ -97,7 +109,23 @@ kla_status kla_chunk_fwd(const void *q, const void *k, const void *v,
                          kla_dtype dtype, kla_gate gate,
                          void *workspace, size_t workspace_bytes, void *stream);
 
-/* Bytes of device scratch kla_chunk_fwd needs for these sizes (0 if none). */
+/*
+ * kla_chunk_fwd with the step-size mode and the query scale chosen by the caller (see the top of
+ * this file). kla_chunk_fwd(...) is kla_chunk_fwd_ex(..., KLA_BETA_KACZMARZ, 1.0f, ...).
+ *   beta_mode  KLA_BETA_KACZMARZ or KLA_BETA_RAW; anything else is KLA_ERR_INVALID_ARG
+ *   q_scale    finite scale s of the read o_t = S_t^T (s q_t); the state does not depend on it;
+ *              a NaN or infinite value is KLA_ERR_INVALID_ARG
+ * Arguments, layouts, workspace and errors are otherwise those of kla_chunk_fwd.
+ */
+kla_status kla_chunk_fwd_ex(const void *q, const void *k, const void *v,
+                            const float *alpha, const float *eta, float eps,
+                            const float *S0, void *o, float *S_T,
+                            int B, int T, int H, int d_k, int d_v, int chunk,
+                            kla_dtype dtype, kla_gate gate, kla_beta_mode beta_mode, float q_scale,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of device scratch kla_chunk_fwd / kla_chunk_fwd_ex need for these sizes (0 if none);
+ * the step-size mode and the query scale do not change it. */
 size_t kla_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v, int chunk,
                                     kla_dtype dtype, kla_gate gate);
 
@@ -142,6 +170,14 @@ kla_status kla_decode_step(const void *q, const void *k, const void *v,
                            float *S, void *o,
                            int B, int H, int d_k, int d_v,
                            kla_dtype dtype, kla_gate gate, void *stream);
+
+/* kla_decode_step with the step-size mode and the query scale of kla_chunk_fwd_ex. */
+kla_status kla_decode_step_ex(const void *q, const void *k, const void *v,
+                              const float *alpha, const float *eta, float eps,
+                              float *S, void *o,
+                              int B, int H, int d_k, int d_v,
+                              kla_dtype dtype, kla_gate gate, kla_beta_mode beta_mode, float q_scale,
+                              void *stream);
 
 /*
  * Synchronises `stream`, then reads and clears the device-side error flags that

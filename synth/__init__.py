@@ -26,6 +26,10 @@ decode     batch 64, H16, d128, 1024 single-token steps, bf16 q/k/v ~ N(0,1),
            scalar alpha = sigmoid(N(3,1)), eta = sigmoid(N(0,1)),
            S drawn i.i.d. N(0, 0.02^2) in fp32 (stand-in for a 32K-token state)
 =========  =====================================================================
+
+Any workload can be redrawn with ``key_norm="l2"``: keys scaled to unit L2 norm
+(in float64, before the storage rounding), as DeltaNet normalises them; the raw
+write strength beta = eta is only stable with such keys.
 """
 from __future__ import annotations
 
@@ -72,6 +76,7 @@ class Workload:
     eps: float = 1e-6
     s0_sigma: float = 0.0   # 0 => S0 = 0
     steps: int = 0          # decode workloads: number of single-token steps
+    key_norm: str = "none"  # "l2": every key scaled to unit L2 norm before storage (DeltaNet keys)
 
 
 WORKLOADS = {
@@ -143,6 +148,16 @@ def _gate(rng, shape, wl: Workload) -> np.ndarray:
     return a.astype(np.float32)
 
 
+def _keys(rng, shape, wl: Workload) -> np.ndarray:
+    k = _normal(rng, shape)
+    if wl.key_norm == "l2":
+        k = k.astype(np.float64)
+        k = k / np.sqrt(np.sum(k * k, axis=-1, keepdims=True))
+    elif wl.key_norm != "none":
+        raise ValueError(wl.key_norm)
+    return k
+
+
 def _sigmoid01(rng, shape) -> np.ndarray:
     x = rng.standard_normal(shape, dtype=np.float32).astype(np.float64)
     return (1.0 / (1.0 + np.exp(-x))).astype(np.float32)
@@ -159,7 +174,7 @@ def custom_prefill(wl: Workload, seed: int = 0) -> PrefillInputs:
     rq, rk, rv, ra, re, rs = _streams(seed, 6)
     B, T, H, dk, dv = wl.B, wl.T, wl.H, wl.d_k, wl.d_v
     q = _store(_normal(rq, (B, T, H, dk)), wl.dtype)
-    k = _store(_normal(rk, (B, T, H, dk)), wl.dtype)
+    k = _store(_keys(rk, (B, T, H, dk), wl), wl.dtype)
     v = _store(_normal(rv, (B, T, H, dv)), wl.dtype)
     ashape = (B, T, H) if wl.gate == "scalar" else (B, T, H, dk)
     alpha = _gate(ra, ashape, wl)
@@ -182,7 +197,7 @@ def make_decode(seed: int = 0, **override) -> DecodeInputs:
     rq, rk, rv, ra, re, rs = _streams(seed, 6)
     n, B, H, dk, dv = wl.steps, wl.B, wl.H, wl.d_k, wl.d_v
     q = _store(_normal(rq, (n, B, H, dk)), wl.dtype)
-    k = _store(_normal(rk, (n, B, H, dk)), wl.dtype)
+    k = _store(_keys(rk, (n, B, H, dk), wl), wl.dtype)
     v = _store(_normal(rv, (n, B, H, dv)), wl.dtype)
     ashape = (n, B, H) if wl.gate == "scalar" else (n, B, H, dk)
     alpha = _gate(ra, ashape, wl)

@@ -29,8 +29,9 @@ def run_prefill(inp, chunk=None, **kw):
     return o.float().cpu().numpy().astype(np.float64), ST.cpu().numpy().astype(np.float64)
 
 
-def oracle_chains(inp, chains=None):
-    """fp64 oracle on the listed (b, h) chains (all when None); returns o [n,T,dv], S [n,dk,dv]."""
+def oracle_chains(inp, chains=None, **mode):
+    """fp64 oracle on the listed (b, h) chains (all when None); returns o [n,T,dv], S [n,dk,dv].
+    ``mode``: beta_mode / q_scale passed to the oracle."""
     B, T, H = inp.wl.B, inp.wl.T, inp.wl.H
     if chains is None:
         chains = [(b, h) for b in range(B) for h in range(H)]
@@ -43,7 +44,7 @@ def oracle_chains(inp, chains=None):
             return np.stack([a[b, h] for b, h in chains])[:, None]
         return np.stack([a[b, :, h] for b, h in chains])[:, :, None]
     o, S = oracle.recurrent(pick("q"), pick("k"), pick("v"), pick("alpha"), pick("eta"), inp.wl.eps, pick("S0"),
-                            nthreads=os.cpu_count() or 1)
+                            nthreads=os.cpu_count() or 1, **mode)
     return o[:, :, 0], S[:, 0]
 
 
@@ -57,7 +58,7 @@ def sample_chains(B, H, n, seed=0):
     return [(int(i) // H, int(i) % H) for i in sorted(idx)]
 
 
-def decode_oracle(d, heads=None):
+def decode_oracle(d, heads=None, **mode):
     """Oracle over all decode steps: the steps of one head are the tokens of one chain."""
     n, B, H = d.alpha.shape[:3]
     heads = heads or [(b, h) for b in range(B) for h in range(H)]
@@ -70,5 +71,5 @@ def decode_oracle(d, heads=None):
     Al = np.stack([al[:, b, h] for b, h in heads])[:, :, None]
     Et = np.stack([et[:, b, h] for b, h in heads])[:, :, None]
     S0 = np.stack([d.S[b, h] for b, h in heads]).astype(np.float64)[:, None]
-    o, S = oracle.recurrent(Q, K, V, Al, Et, d.wl.eps, S0, nthreads=os.cpu_count() or 1)
+    o, S = oracle.recurrent(Q, K, V, Al, Et, d.wl.eps, S0, nthreads=os.cpu_count() or 1, **mode)
     return o[:, :, 0], S[:, 0]

@@ -29,7 +29,7 @@ def declared_functions():
 def test_header_declares_entry_points():
     names = declared_functions()
     for required in ("kla_chunk_fwd", "kla_decode_step", "kla_chunk_fwd_workspace_size", "kla_status_string",
-                     "kla_device_status", "kla_abi_version"):
+                     "kla_device_status", "kla_abi_version", "kla_chunk_fwd_ex", "kla_decode_step_ex"):
         assert required in names, names
 
 
@@ -42,7 +42,7 @@ def test_status_strings_and_version(lib):
     for code, token in [(0, "KLA_OK"), (1, "INVALID_ARG"), (2, "UNSUPPORTED"), (3, "CUDA"), (4, "TIMEOUT")]:
         assert token in lib.kla_status_string(code).decode()
     assert "UNKNOWN" in lib.kla_status_string(99).decode()
-    assert lib.kla_abi_version() == 100
+    assert lib.kla_abi_version() == 101
 
 
 # Fake, never dereferenced device addresses: every case below must be rejected on the host.
@@ -93,3 +93,23 @@ def test_decode_rejects_on_host(lib):
 
 def test_workspace_size_is_a_host_call(lib):
     assert lib.kla_chunk_fwd_workspace_size(8, 4096, 16, 128, 128, 64, 1, 0) >= 0
+
+
+@pytest.mark.parametrize("mode,scale,code", [
+    (2, 1.0, 1), (-1, 1.0, 1), (0, float("nan"), 1), (1, float("inf"), 1), (0, float("-inf"), 1),
+])
+def test_ex_entry_points_reject_bad_options_on_host(lib, mode, scale, code):
+    f = lib.kla_chunk_fwd_ex
+    assert f(A, A + 0x10000000, A + 0x20000000, A + 0x30000000, A + 0x38000000, 1e-6, None, A + 0x40000000,
+             None, 1, 64, 1, 16, 16, 16, 0, 0, mode, scale, None, 0, None) == code
+    g = lib.kla_decode_step_ex
+    assert g(A, A + 0x1000000, A + 0x2000000, A + 0x3000000, A + 0x3800000, 1e-6, A + 0x4000000, A + 0x5000000,
+             2, 2, 16, 16, 1, 0, mode, scale, None) == code
+
+
+def test_ex_entry_points_accept_the_options_before_checking_pointers(lib):
+    # valid options do not mask an argument error that comes after them
+    f = lib.kla_chunk_fwd_ex
+    assert f(None, A, A, A, A, 1e-6, None, A, None, 1, 64, 1, 16, 16, 16, 0, 0, 1, 0.25, None, 0, None) == 1
+    assert f(A, A + 0x10000000, A + 0x20000000, A + 0x30000000, A + 0x38000000, 1e-6, None, A + 0x40000000,
+             None, 1, 64, 1, 48, 16, 16, 0, 0, 1, 0.0, None, 0, None) == 2
