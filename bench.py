@@ -404,6 +404,7 @@ def main():
     ap.add_argument("--ref-chains", type=int, default=16)
     ap.add_argument("--cpu-chains", type=int, default=64)
     ap.add_argument("--decode-steps", type=int, default=1024)
+    ap.add_argument("--verify-calls", type=int, default=256)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -476,9 +477,9 @@ def main():
                             "roofline": roofline(dr["alg_bytes_per_step"], dr["ms_per_token_step"], pk)}
         launches += dr["launches"]
         t0 = time.time()
-        extras["verify4"] = bench_verify(4, 256, seed=rank, dev=dev, flush=flush, stream=stream, pk=pk)
+        extras["verify4"] = bench_verify(4, args.verify_calls, seed=rank, dev=dev, flush=flush, stream=stream, pk=pk)
         clocks.mark(t0, time.time())
-        launches += 256
+        launches += args.verify_calls
     clk = clocks.stop()
 
     cpu = None

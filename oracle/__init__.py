@@ -11,6 +11,9 @@ Two independent restatements of what the recurrence computes:
   write strength of DeltaNet / Gated DeltaNet), write, read (with an optional
   query scale).
   This is the definition the GPU results are compared against.
+* ``Oracle.backward`` -- the reverse-mode derivative of ``recurrent`` (C), the chain
+  rule through the same six steps in reverse order (the pages give no backward
+  algebra), pinned by finite differences of ``recurrent``.
 * ``chunkwise`` -- an fp64 NumPy restatement of the chunk algebra (cumulative
   log-decay, provisional error, unit-triangular correction, end-of-chunk state
   and in-chunk outputs) from GeekNews "Revisando las variantes de atencion
@@ -111,6 +114,41 @@ class Oracle:
         if rc != 0:
             raise RuntimeError(f"kla_oracle_recurrent failed with {rc}")
         return o, ST
+
+
+    def backward(self, q, k, v, alpha, eta, eps, S0, dO, dS_T=None, nthreads: int = 1, beta_mode: str = "kla",
+                 q_scale: float = 1.0):
+        """Reverse-mode derivative of ``recurrent`` for a loss with dL/do = dO [B,T,H,d_v] and
+        dL/dS_T = dS_T [B,H,d_k,d_v] (None: 0). Returns a dict of float64 arrays: dq, dk, dv,
+        dalpha (shaped like alpha), deta, dS0. Keeps every chain's states: small cases only."""
+        modes = {"kla": 0, "raw": 1}
+        if beta_mode not in modes:
+            raise ValueError(f"beta_mode {beta_mode!r}")
+        c = lambda a: None if a is None else np.ascontiguousarray(a, dtype=np.float64)  # noqa: E731
+        q, k, v, alpha, eta, S0, dO, dS_T = (c(x) for x in (q, k, v, alpha, eta, S0, dO, dS_T))
+        B, T, H, dk = q.shape
+        dv = v.shape[-1]
+        per_channel = 1 if alpha.shape == (B, T, H, dk) else 0
+        if not per_channel and alpha.shape != (B, T, H):
+            raise ValueError(f"alpha shape {alpha.shape}")
+        assert dO.shape == (B, T, H, dv)
+        out = {"dq": np.zeros_like(q), "dk": np.zeros_like(k), "dv": np.zeros_like(v),
+               "dalpha": np.zeros_like(alpha), "deta": np.zeros_like(eta), "dS0": np.zeros((B, H, dk, dv))}
+        dp = ctypes.POINTER(ctypes.c_double)
+
+        def P(a):
+            return None if a is None else a.ctypes.data_as(dp)
+        f = self.lib.kla_oracle_backward
+        f.argtypes = [dp, dp, dp, dp, ctypes.c_int, dp, ctypes.c_double, dp, dp, dp, dp, dp, dp, dp, dp, dp,
+                      ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_long,
+                      ctypes.c_int, ctypes.c_double, ctypes.c_int]
+        f.restype = ctypes.c_int
+        rc = f(P(q), P(k), P(v), P(alpha), per_channel, P(eta), float(eps), P(S0), P(dO), P(dS_T),
+               P(out["dq"]), P(out["dk"]), P(out["dv"]), P(out["dalpha"]), P(out["deta"]), P(out["dS0"]),
+               B, T, H, dk, dv, modes[beta_mode], float(q_scale), int(nthreads))
+        if rc != 0:
+            raise RuntimeError(f"kla_oracle_backward failed with {rc}")
+        return out
 
 
 def load(mutant: int = 0) -> Oracle:

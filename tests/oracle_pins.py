@@ -385,10 +385,45 @@ def pin_query_scale(orc):
     _close(s2, s1, 0.0, "state does not see s")
 
 
+def pin_backward_finite_differences(orc):
+    """The backward pass is the derivative of the forward: for L = sum(W_o * o) + sum(W_s * S_T)
+    with random weights, every gradient the backward returns (q, k, v, alpha, eta, S0) matches
+    central differences of the forward oracle, for both gates, both step sizes, a query scale,
+    with and without a final-state gradient."""
+    rng = np.random.default_rng(41)
+    B, T, H, dk, dv = 1, 6, 1, 3, 2
+    names = {"q": "dq", "k": "dk", "v": "dv", "alpha": "dalpha", "eta": "deta", "S0": "dS0"}
+    for per_channel, mode, with_ds in ((False, "kla", True), (True, "kla", False), (False, "raw", False),
+                                       (True, "raw", True)):
+        x = {"q": rng.normal(size=(B, T, H, dk)), "k": rng.normal(size=(B, T, H, dk)) * 0.7,
+             "v": rng.normal(size=(B, T, H, dv)),
+             "alpha": rng.uniform(0.5, 1.0, size=(B, T, H, dk) if per_channel else (B, T, H)),
+             "eta": rng.uniform(0.1, 0.9, size=(B, T, H)), "S0": rng.normal(size=(B, H, dk, dv))}
+        Wo, Ws = rng.normal(size=(B, T, H, dv)), (rng.normal(size=(B, H, dk, dv)) if with_ds else None)
+        eps, s = 0.3, 0.7
+
+        def loss(a):
+            o, ST = orc.recurrent(a["q"], a["k"], a["v"], a["alpha"], a["eta"], eps, a["S0"], beta_mode=mode,
+                                  q_scale=s)
+            return float(np.sum(o * Wo) + (np.sum(ST * Ws) if Ws is not None else 0.0))
+        g = orc.backward(x["q"], x["k"], x["v"], x["alpha"], x["eta"], eps, x["S0"], Wo, Ws, beta_mode=mode,
+                         q_scale=s)
+        for n, arr in x.items():
+            fd = np.zeros_like(arr)
+            for idx in np.ndindex(arr.shape):
+                xp, xm = dict(x), dict(x)
+                xp[n] = arr.copy()
+                xm[n] = arr.copy()
+                xp[n][idx] += 1e-6
+                xm[n][idx] -= 1e-6
+                fd[idx] = (loss(xp) - loss(xm)) / 2e-6
+            _close(g[names[n]], fd, 1e-7, f"d{n} ({mode}, per_channel={per_channel})")
+
+
 PINS = [
     pin_unrelaxed_constraint, pin_deltanet_reread, pin_pure_decay, pin_orthogonal_locality,
     pin_worked_scalar, pin_marker_overshoot, pin_transition_eigen, pin_gradient_step,
     pin_linear_attention_split, pin_dplr_transition, pin_chunkwise_equals_recurrent,
     pin_continuation, pin_zero_key, pin_raw_beta_worked, pin_raw_beta_first_write_and_limits,
-    pin_raw_beta_is_kla_with_rescaled_eta, pin_query_scale,
+    pin_raw_beta_is_kla_with_rescaled_eta, pin_query_scale, pin_backward_finite_differences,
 ]
