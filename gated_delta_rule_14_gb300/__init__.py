@@ -10,8 +10,9 @@ scalar per token and head, or one value per key channel. ``beta_mode="raw"`` tak
 variantes de atencion lineal de la familia DeltaNet", sections "Gated DeltaNet" and
 "Kimi Delta Attention").
 
-``chunk_fwd`` runs the chunkwise prefill and ``decode_step`` one fused
-single-token step. Both call the C ABI of ``include/kla.h`` through ctypes; torch
+``chunk_fwd`` runs the chunkwise prefill, ``decode_step`` one fused single-token
+step and ``chunk_bwd`` the backward pass (gradients of a loss given dL/do and
+dL/dS_T). Both call the C ABI of ``include/kla.h`` through ctypes; torch
 only supplies device memory and the current CUDA stream. Every step of the
 computation runs in this package's CUDA kernels; if the library is missing the
 calls raise.
@@ -25,7 +26,8 @@ import torch
 from . import _native
 from ._native import KlaError  # noqa: F401
 
-__all__ = ["chunk_fwd", "decode_step", "workspace_size", "device_status", "KlaError"]
+__all__ = ["chunk_fwd", "chunk_bwd", "decode_step", "workspace_size", "bwd_workspace_size", "device_status",
+           "KlaError"]
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -131,6 +133,63 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, alpha: torch.Te
         _stream_ptr(q.device))
     _native.check(st, "kla_chunk_fwd_ex")
     return out, S_T
+
+
+def bwd_workspace_size(B: int, T: int, H: int, d_k: int, d_v: int) -> int:
+    """Device scratch bytes ``chunk_bwd`` needs for these sizes."""
+    return int(_native.lib().kla_chunk_bwd_workspace_size(B, T, H, d_k, d_v))
+
+
+def chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, alpha: torch.Tensor, eta: torch.Tensor,
+              dO: torch.Tensor, eps: float = 1e-6, S0: Optional[torch.Tensor] = None,
+              dS_T: Optional[torch.Tensor] = None, *, beta_mode: str = "kla", q_scale: float = 1.0,
+              want_dS0: bool = True, workspace: Optional[torch.Tensor] = None):
+    """Backward pass of ``chunk_fwd`` run with the same inputs and options.
+
+    dO: [B,T,H,d_v] in q's dtype (dL/do); dS_T: fp32 [B,H,d_k,d_v] or None (dL/dS_T = 0).
+    Returns a dict of fp32 gradients: dq, dk [B,T,H,d_k]; dv [B,T,H,d_v]; dalpha (alpha's shape);
+    deta [B,T,H]; dS0 [B,H,d_k,d_v] (None unless ``want_dS0``).
+    """
+    bcode = _beta_code(beta_mode)
+    for n, t in (("q", q), ("k", k), ("v", v), ("dO", dO)):
+        _check_dev(n, t)
+    dcode = _dtype_code(q)
+    if k.dtype != q.dtype or v.dtype != q.dtype or dO.dtype != q.dtype:
+        raise TypeError("q, k, v and dO must share one dtype")
+    B, T, H, d_k = q.shape
+    d_v = v.shape[-1]
+    if k.shape != q.shape or v.shape[:3] != q.shape[:3] or dO.shape != v.shape:
+        raise ValueError("q, k, v, dO shapes disagree")
+    _check_dev("alpha", alpha, torch.float32)
+    _check_dev("eta", eta, torch.float32)
+    if tuple(alpha.shape) == (B, T, H):
+        gate = _native.KLA_GATE_SCALAR
+    elif tuple(alpha.shape) == (B, T, H, d_k):
+        gate = _native.KLA_GATE_CHANNEL
+    else:
+        raise ValueError(f"alpha must be [B,T,H] or [B,T,H,d_k], got {tuple(alpha.shape)}")
+    if tuple(eta.shape) != (B, T, H):
+        raise ValueError("eta must be [B, T, H]")
+    for n, t in (("S0", S0), ("dS_T", dS_T)):
+        if t is not None:
+            _check_dev(n, t, torch.float32)
+            if tuple(t.shape) != (B, H, d_k, d_v):
+                raise ValueError(f"{n} must be [B, H, d_k, d_v]")
+    f32 = dict(dtype=torch.float32, device=q.device)
+    g = {"dq": torch.empty((B, T, H, d_k), **f32), "dk": torch.empty((B, T, H, d_k), **f32),
+         "dv": torch.empty((B, T, H, d_v), **f32), "dalpha": torch.empty(alpha.shape, **f32),
+         "deta": torch.empty((B, T, H), **f32),
+         "dS0": torch.empty((B, H, d_k, d_v), **f32) if want_dS0 else None}
+    need = bwd_workspace_size(B, T, H, d_k, d_v)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = _native.lib().kla_chunk_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(eta), float(eps), _ptr(S0), _ptr(dO), _ptr(dS_T),
+        _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["dalpha"]), _ptr(g["deta"]), _ptr(g["dS0"]),
+        B, T, H, d_k, d_v, dcode, gate, bcode, float(q_scale), _ptr(workspace), ws_bytes, _stream_ptr(q.device))
+    _native.check(st, "kla_chunk_bwd")
+    return g
 
 
 def decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, alpha: torch.Tensor, eta: torch.Tensor,

@@ -55,6 +55,11 @@ def _declare(lib):
     lib.kla_decode_step_ex.argtypes = [vp, vp, vp, fp, fp, ctypes.c_float, fp, vp, i, i, i, i, i, i, i,
                                        ctypes.c_float, vp]
     lib.kla_decode_step_ex.restype = ctypes.c_int
+    lib.kla_chunk_bwd.argtypes = [vp, vp, vp, fp, fp, ctypes.c_float, fp, vp, fp, fp, fp, fp, fp, fp, fp,
+                                  i, i, i, i, i, i, i, i, ctypes.c_float, vp, sz, vp]
+    lib.kla_chunk_bwd.restype = ctypes.c_int
+    lib.kla_chunk_bwd_workspace_size.argtypes = [i, i, i, i, i]
+    lib.kla_chunk_bwd_workspace_size.restype = sz
     lib.kla_device_status.argtypes = [vp]
     lib.kla_device_status.restype = ctypes.c_int
     lib.kla_status_string.argtypes = [ctypes.c_int]

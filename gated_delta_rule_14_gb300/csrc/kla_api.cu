@@ -182,6 +182,57 @@ kla_status kla_decode_step(const void *q, const void *k, const void *v, const fl
                               1.0f, stream);
 }
 
+size_t kla_chunk_bwd_workspace_size(int B, int T, int H, int d_k, int d_v) {
+    return kla::bwd_workspace_bytes(B, T, H, d_k, d_v);
+}
+
+kla_status kla_chunk_bwd(const void *q, const void *k, const void *v, const float *alpha, const float *eta,
+                         float eps, const float *S0, const void *dO, const float *dS_T, float *dq, float *dk,
+                         float *dv, float *dalpha, float *deta, float *dS0, int B, int T, int H, int d_k, int d_v,
+                         kla_dtype dtype, kla_gate gate, kla_beta_mode beta_mode, float q_scale, void *workspace,
+                         size_t workspace_bytes, void *stream) {
+    if (T < 0) return KLA_ERR_INVALID_ARG;
+    if (!valid_mode(beta_mode, q_scale)) return KLA_ERR_INVALID_ARG;
+    const size_t ntok = static_cast<size_t>(B) * T * H;
+    kla_status st = check_common(q, k, v, alpha, eta, dO, B, H, d_k, d_v, dtype, gate, 0, ntok);
+    if (st != KLA_OK) return st;
+    if (ntok > 0 && (!dq || !dk || !dv || !dalpha || !deta)) return KLA_ERR_INVALID_ARG;
+    if (!aligned(dq, 4) || !aligned(dk, 4) || !aligned(dalpha, 4) || !aligned(deta, 4) || !aligned16(dv))
+        return KLA_ERR_INVALID_ARG;
+    if ((S0 && !aligned16(S0)) || (dS_T && !aligned16(dS_T)) || (dS0 && !aligned16(dS0))) return KLA_ERR_INVALID_ARG;
+    if (!(eps == eps)) return KLA_ERR_INVALID_ARG;
+    const size_t need = kla::bwd_workspace_bytes(B, T, H, d_k, d_v);
+    if (workspace_bytes < need || (need > 0 && (!workspace || !aligned16(workspace)))) return KLA_ERR_INVALID_ARG;
+
+    const size_t esz = dtype == KLA_DTYPE_BF16 ? 2 : 4;
+    const size_t sbytes = static_cast<size_t>(B) * H * d_k * d_v * 4;
+    const size_t abytes = ntok * (gate == KLA_GATE_CHANNEL ? d_k : 1) * 4;
+    const Span outs[] = {span(dq, ntok * d_k * 4), span(dk, ntok * d_k * 4), span(dv, ntok * d_v * 4),
+                         span(dalpha, abytes), span(deta, ntok * 4), span(dS0, dS0 ? sbytes : 0),
+                         span(workspace, need)};
+    const Span ins[] = {span(q, ntok * d_k * esz), span(k, ntok * d_k * esz), span(v, ntok * d_v * esz),
+                        span(dO, ntok * d_v * esz), span(alpha, abytes), span(eta, ntok * 4),
+                        span(S0, S0 ? sbytes : 0), span(dS_T, dS_T ? sbytes : 0)};
+    for (size_t i = 0; i < sizeof(outs) / sizeof(outs[0]); ++i) {
+        if (outs[i].hi <= outs[i].lo) continue;
+        for (const Span &x : ins)
+            if (x.hi > x.lo && overlaps(outs[i], x)) return KLA_ERR_INVALID_ARG;
+        for (size_t j = i + 1; j < sizeof(outs) / sizeof(outs[0]); ++j)
+            if (outs[j].hi > outs[j].lo && overlaps(outs[i], outs[j])) return KLA_ERR_INVALID_ARG;
+    }
+
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (T == 0) {   // no tokens: dL/dS0 = dL/dS_T
+        if (!dS0) return KLA_OK;
+        cudaError_t e = dS_T ? cudaMemcpyAsync(dS0, dS_T, sbytes, cudaMemcpyDeviceToDevice, cs)
+                             : cudaMemsetAsync(dS0, 0, sbytes, cs);
+        return e == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
+    }
+    kla::BwdArgs a{q, k, v, dO, alpha, eta, eps, S0, dS_T, dq, dk, dv, dalpha, deta, dS0, B, T, H, d_k, d_v,
+                   dtype, gate, beta_mode == KLA_BETA_RAW, q_scale, workspace, workspace_bytes, cs};
+    return kla::launch_bwd(a) == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
+}
+
 kla_status kla_device_status(void *stream) {
     unsigned *p = nullptr;
     if (err_word(&p) != cudaSuccess) return KLA_ERR_CUDA;

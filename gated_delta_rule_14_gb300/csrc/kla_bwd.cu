@@ -1,0 +1,401 @@
+// kla_bwd.cu -- backward pass of the KLA recurrence (reverse-mode derivative), fp32.
+//
+// The pages give no backward algebra (GeekNews, "Revisando las variantes de atencion lineal de la
+// familia DeltaNet", section "KDA por chunks", names training as the use of the chunk mode); this
+// is the chain rule through the forward steps in reverse order. With G = dL/dS_t carried from the
+// last token down to the first, per token t (state S_{t-1} entering it, S~ = alpha (.) S_{t-1},
+// residual e = v - S~^T k, step beta, read o = S_t^T (s q)):
+//   read:     dq = s S_t do = s (S~ do + beta k (e . do));      G += s q do^T
+//   write:    gk = G^T k;  de = beta gk;  dbeta = gk . e;       dk = beta G e
+//   residual: dv = de;  dS~ = G - k de^T;                       dk -= S~ de
+//   step:     KLA: deta = dbeta / (n + eps), dk -= 2 beta dbeta / (n + eps) k  (n = ||k||^2;
+//             nothing flows when n + eps == 0);  raw: deta = dbeta
+//   forget:   dalpha_i = sum_j S_{t-1}[i,j] dS~[i,j] (summed over i for a scalar gate);
+//             G = alpha (.) dS~
+// and dS0 = G at the end.
+//
+// One CTA of 4 d_v threads per (sequence, head) chain. A warp owns 8 value columns over all d_k
+// rows (lanes: 2 column groups x 16 row groups of kRows = d_k / 16 consecutive rows), so every
+// column reduction (S~^T k, G^T k) stays inside the warp; row reductions (dq, dk, per-channel
+// dalpha) and the scalars (e . do, dbeta, scalar dalpha) go through shared memory with one
+// block barrier per token.
+//   phase F: the forward recurrence, saving the state at every kBlk-token boundary and every
+//            residual e_t (the only forward quantities the reverse needs besides the inputs);
+//   phase R: blocks of kBlk tokens in reverse order: the block's checkpoint goes to shared
+//            memory, and before each reverse token the state entering it is rebuilt from the
+//            checkpoint with the stored residuals (S <- alpha S + beta k e^T: no reductions).
+#include <algorithm>
+
+#include "kla_internal.cuh"
+
+namespace kla {
+namespace {
+
+constexpr int kBlk = 8;   // tokens per checkpoint block
+
+struct BwdParams {
+    const void *q, *k, *v, *dO;
+    const float *alpha, *eta;
+    float eps;
+    const float *S0, *dST;
+    float *dq, *dk, *dv, *dalpha, *deta, *dS0;
+    float *ckpt;   // [B*H][nblk][DK][DV]
+    float *e;      // [B, T, H, DV]
+    int B, T, H, DK, DV, nblk;
+    int beta_raw;
+    float q_scale;
+};
+
+// Reduce 4 partial column sums over the 16 row-group lanes (lane bits 1-4) and hand every lane
+// the 4 totals of its column group: a two-level reduce-scatter, two plain levels, then 4
+// shuffles back.
+__device__ __forceinline__ void colsum4(float (&x)[4], int lane) {
+    const bool b4 = lane & 16, b3 = lane & 8;
+    float y[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const float send = b4 ? x[j] : x[j + 2];
+        const float keep = b4 ? x[j + 2] : x[j];
+        y[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+    const float send = b3 ? y[0] : y[1];
+    const float keep = b3 ? y[1] : y[0];
+    float w = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    w += __shfl_xor_sync(0xffffffffu, w, 4);
+    w += __shfl_xor_sync(0xffffffffu, w, 2);
+    // lane with bits (4, 3) = (hi, lo) holds column 2 hi + lo of its group
+    const int cg = lane & 1;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) x[j] = __shfl_sync(0xffffffffu, w, ((j >> 1) << 4) | ((j & 1) << 3) | cg);
+}
+
+template <typename TIn, bool kChannel, int kRows>
+__global__ void __launch_bounds__(512, 1) bwd_kernel(const BwdParams p) {
+    extern __shared__ __align__(16) float bsm[];
+    const int DK = p.DK, DV = p.DV, T = p.T;
+    const int nwarps = DV / 8;
+    // shared memory carve-up (floats)
+    float *sS = bsm;                                  // checkpoint [DK][DV]
+    float *sk = sS + DK * DV;                         // [kBlk][DK]
+    float *sq = sk + kBlk * DK;                       // [kBlk][DK]
+    float *sa = sq + kBlk * DK;                       // [kBlk][DK] (per-channel gate) or [kBlk]
+    float *sv = sa + kBlk * DK;                       // [kBlk][DV]: v (phase F) or e (phase R)
+    float *sdo = sv + kBlk * DV;                      // [kBlk][DV]
+    float *sbeta = sdo + kBlk * DV;                   // [kBlk]
+    float *sden = sbeta + kBlk;                       // [kBlk]: ||k||^2 + eps
+    float *sas = sden + kBlk;                         // [kBlk]: scalar gate
+    float *red = sas + kBlk;                          // [2][16 warps][3][DK] row partials
+    float *reds = red + 2 * 16 * 3 * DK;              // [2][16 warps][4] scalar partials
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cg = lane & 1, rg = lane >> 1;
+    const int h = blockIdx.x, b = blockIdx.y;
+    const size_t bh = static_cast<size_t>(b) * p.H + h;
+    const int col = warp * 8 + cg * 4;                // this lane's first value column
+    const int r0 = rg * kRows;
+    const bool live = r0 < DK;
+    const int rr = live ? r0 : 0;
+    auto tok = [&](int t) { return (static_cast<size_t>(b) * T + t) * p.H + h; };
+    const float s = p.q_scale;
+    float *ck = p.ckpt + bh * static_cast<size_t>(p.nblk) * DK * DV;
+
+    // stage tokens [t0, t0 + n) of the block: k, q, gates, beta; v (phase F) or e (phase R), do
+    auto stage = [&](int t0, int n, bool reverse) {
+        const TIn *gk = static_cast<const TIn *>(p.k), *gq = static_cast<const TIn *>(p.q);
+        for (int idx = tid; idx < n * DK; idx += blockDim.x) {
+            const int u = idx / DK, c = idx - u * DK;
+            const size_t g = tok(t0 + u) * DK + c;
+            sk[u * DK + c] = to_f32(gk[g]);
+            if (reverse) sq[u * DK + c] = to_f32(gq[g]);
+            if (kChannel) sa[u * DK + c] = p.alpha[g];
+        }
+        for (int idx = tid; idx < n * DV; idx += blockDim.x) {
+            const int u = idx / DV, c = idx - u * DV;
+            const size_t g = tok(t0 + u) * DV + c;
+            if (reverse) {
+                sv[u * DV + c] = p.e[g];
+                sdo[u * DV + c] = to_f32(static_cast<const TIn *>(p.dO)[g]);
+            } else {
+                sv[u * DV + c] = to_f32(static_cast<const TIn *>(p.v)[g]);
+            }
+        }
+        if (!kChannel && tid < n) sas[tid] = p.alpha[tok(t0 + tid)];
+        __syncthreads();
+        for (int u = warp; u < n; u += nwarps) {   // ||k||^2 and beta, one warp per token
+            float kk = 0.f;
+            for (int c = lane; c < DK; c += 32) kk = fmaf(sk[u * DK + c], sk[u * DK + c], kk);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) kk += __shfl_xor_sync(0xffffffffu, kk, off);
+            if (lane == 0) {
+                const float eta = p.eta[tok(t0 + u)];
+                sden[u] = kk + p.eps;
+                sbeta[u] = kla_beta(eta, kk, p.eps, p.beta_raw);
+            }
+        }
+        __syncthreads();
+    };
+    auto rows_of = [&](const float *v, float (&out)[kRows]) {
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) out[r] = v[rr + r];
+    };
+    auto gate_rows = [&](int u, float (&a)[kRows]) {
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) a[r] = kChannel ? sa[u * DK + rr + r] : sas[u];
+    };
+
+    // ------------------------------------------------------------------ phase F: forward
+    float S[kRows][4];
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (live && p.S0) x = *reinterpret_cast<const float4 *>(p.S0 + (bh * DK + r0 + r) * DV + col);
+        S[r][0] = x.x; S[r][1] = x.y; S[r][2] = x.z; S[r][3] = x.w;
+    }
+    for (int blk = 0; blk < p.nblk; ++blk) {
+        const int t0 = blk * kBlk, n = min(kBlk, T - t0);
+        if (live) {   // checkpoint: the state entering token t0
+#pragma unroll
+            for (int r = 0; r < kRows; ++r)
+                *reinterpret_cast<float4 *>(ck + (static_cast<size_t>(blk) * DK + r0 + r) * DV + col) =
+                    make_float4(S[r][0], S[r][1], S[r][2], S[r][3]);
+        }
+        stage(t0, n, false);
+        for (int u = 0; u < n; ++u) {
+            float kr[kRows], a[kRows];
+            rows_of(sk + u * DK, kr);
+            gate_rows(u, a);
+            float pk[4] = {0.f, 0.f, 0.f, 0.f};
+            if (live) {
+#pragma unroll
+                for (int r = 0; r < kRows; ++r) {
+                    const float ak = a[r] * kr[r];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) pk[c] = fmaf(ak, S[r][c], pk[c]);
+                }
+            }
+            colsum4(pk, lane);
+            const float beta = sbeta[u];
+            float e[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) e[c] = sv[u * DV + col + c] - pk[c];
+            if (rg == 0)
+                *reinterpret_cast<float4 *>(p.e + tok(t0 + u) * DV + col) = make_float4(e[0], e[1], e[2], e[3]);
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) {
+                const float bk = beta * kr[r];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) S[r][c] = fmaf(a[r], S[r][c], bk * e[c]);
+            }
+        }
+        __syncthreads();   // the staging area is rewritten by the next block
+    }
+
+    // ------------------------------------------------------------------ phase R: reverse
+    float G[kRows][4];
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (live && p.dST) x = *reinterpret_cast<const float4 *>(p.dST + (bh * DK + r0 + r) * DV + col);
+        G[r][0] = x.x; G[r][1] = x.y; G[r][2] = x.z; G[r][3] = x.w;
+    }
+    int par = 0;
+    for (int blk = p.nblk - 1; blk >= 0; --blk) {
+        const int t0 = blk * kBlk, n = min(kBlk, T - t0);
+        for (int idx = tid; idx < DK * DV / 4; idx += blockDim.x)
+            reinterpret_cast<float4 *>(sS)[idx] =
+                reinterpret_cast<const float4 *>(ck + static_cast<size_t>(blk) * DK * DV)[idx];
+        stage(t0, n, true);   // ends with a barrier: sS is visible too
+        for (int u = n - 1; u >= 0; --u) {
+            // the state entering token t0 + u: checkpoint, then u stored updates
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) {
+                const float4 x = *reinterpret_cast<const float4 *>(sS + (rr + r) * DV + col);
+                S[r][0] = x.x; S[r][1] = x.y; S[r][2] = x.z; S[r][3] = x.w;
+            }
+            for (int w = 0; w < u; ++w) {
+                float kr[kRows], a[kRows];
+                rows_of(sk + w * DK, kr);
+                gate_rows(w, a);
+                const float beta = sbeta[w];
+                const float4 ew = *reinterpret_cast<const float4 *>(sv + w * DV + col);
+                const float e[4] = {ew.x, ew.y, ew.z, ew.w};
+#pragma unroll
+                for (int r = 0; r < kRows; ++r) {
+                    const float bk = beta * kr[r];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) S[r][c] = fmaf(a[r], S[r][c], bk * e[c]);
+                }
+            }
+            // the reverse step of token t = t0 + u
+            float kr[kRows], qr[kRows], a[kRows];
+            rows_of(sk + u * DK, kr);
+            rows_of(sq + u * DK, qr);
+            gate_rows(u, a);
+            const float beta = sbeta[u];
+            const float4 e4 = *reinterpret_cast<const float4 *>(sv + u * DV + col);
+            const float4 d4 = *reinterpret_cast<const float4 *>(sdo + u * DV + col);
+            const float e[4] = {e4.x, e4.y, e4.z, e4.w}, dov[4] = {d4.x, d4.y, d4.z, d4.w};
+            float rowA[kRows], rowB[kRows], rowC[kRows];
+            float gk[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) {
+                float sdo_ = 0.f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float st = a[r] * S[r][c];              // S~
+                    sdo_ = fmaf(st, dov[c], sdo_);
+                    G[r][c] = fmaf(s * qr[r], dov[c], G[r][c]);   // read
+                    gk[c] = fmaf(G[r][c], kr[r], gk[c]);
+                }
+                rowA[r] = sdo_;
+            }
+            if (!live) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) gk[c] = 0.f;
+            }
+            colsum4(gk, lane);
+            float de[4], sc_edo = 0.f, sc_db = 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                de[c] = beta * gk[c];
+                sc_edo = fmaf(e[c], dov[c], sc_edo);
+                sc_db = fmaf(gk[c], e[c], sc_db);
+            }
+            if (rg == 0)
+                *reinterpret_cast<float4 *>(p.dv + tok(t0 + u) * DV + col) = make_float4(de[0], de[1], de[2], de[3]);
+            float sc_da = 0.f;
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) {
+                float ge = 0.f, sde = 0.f, da = 0.f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float st = a[r] * S[r][c];
+                    ge = fmaf(G[r][c], e[c], ge);
+                    sde = fmaf(st, de[c], sde);
+                    const float dst = fmaf(-kr[r], de[c], G[r][c]);   // dS~
+                    da = fmaf(S[r][c], dst, da);
+                    G[r][c] = a[r] * dst;                               // forget
+                }
+                rowB[r] = fmaf(beta, ge, -sde);
+                rowC[r] = da;
+                sc_da += da;
+            }
+            // row partials: combine the two column groups, then one row set per warp
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) {
+                rowA[r] += __shfl_xor_sync(0xffffffffu, rowA[r], 1);
+                rowB[r] += __shfl_xor_sync(0xffffffffu, rowB[r], 1);
+                rowC[r] += __shfl_xor_sync(0xffffffffu, rowC[r], 1);
+            }
+            float *rd = red + (par * 16 + warp) * 3 * DK;
+            if (cg == 0 && live) {
+#pragma unroll
+                for (int r = 0; r < kRows; ++r) {
+                    rd[r0 + r] = rowA[r];
+                    rd[DK + r0 + r] = rowB[r];
+                    rd[2 * DK + r0 + r] = rowC[r];
+                }
+            }
+            // scalars: e . do and dbeta over the columns (row group 0 holds them), the scalar
+            // dalpha over everything
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) sc_da += __shfl_xor_sync(0xffffffffu, sc_da, off);
+            sc_edo += __shfl_xor_sync(0xffffffffu, sc_edo, 1);
+            sc_db += __shfl_xor_sync(0xffffffffu, sc_db, 1);
+            if (lane == 0) {
+                float *rs = reds + (par * 16 + warp) * 4;
+                rs[0] = sc_edo;
+                rs[1] = sc_db;
+                rs[2] = sc_da;
+            }
+            __syncthreads();
+            {
+                float edo = 0.f, db = 0.f, dat = 0.f;
+                for (int w = 0; w < nwarps; ++w) {
+                    const float *rs = reds + (par * 16 + w) * 4;
+                    edo += rs[0];
+                    db += rs[1];
+                    dat += rs[2];
+                }
+                const size_t tk = tok(t0 + u);
+                const float den = sden[u];
+                const bool flows = p.beta_raw || den != 0.f;
+                for (int idx = tid; idx < (kChannel ? 2 : 1) * DK; idx += blockDim.x) {
+                    if (idx < DK) {   // dq and dk of row idx
+                        const int i = idx;
+                        float A = 0.f, Bk = 0.f;
+                        for (int w = 0; w < nwarps; ++w) {
+                            A += red[(par * 16 + w) * 3 * DK + i];
+                            Bk += red[(par * 16 + w) * 3 * DK + DK + i];
+                        }
+                        const float ki = sk[u * DK + i];
+                        p.dq[tk * DK + i] = s * fmaf(beta * ki, edo, A);
+                        float dki = Bk;
+                        if (!p.beta_raw && flows) dki = fmaf(-2.f * beta * db / den, ki, dki);
+                        p.dk[tk * DK + i] = dki;
+                    } else {          // per-channel dalpha of row idx - DK
+                        const int i = idx - DK;
+                        float C = 0.f;
+                        for (int w = 0; w < nwarps; ++w) C += red[(par * 16 + w) * 3 * DK + 2 * DK + i];
+                        p.dalpha[tk * DK + i] = C;
+                    }
+                }
+                if (tid == 0) {
+                    p.deta[tk] = p.beta_raw ? db : (flows ? db / den : 0.f);
+                    if (!kChannel) p.dalpha[tk] = dat;
+                }
+            }
+            par ^= 1;   // the other buffer is rewritten only after the next barrier
+        }
+        __syncthreads();   // checkpoint and staging areas are rewritten by the next block
+    }
+    if (p.dS0 && live) {
+#pragma unroll
+        for (int r = 0; r < kRows; ++r)
+            *reinterpret_cast<float4 *>(p.dS0 + (bh * DK + r0 + r) * DV + col) =
+                make_float4(G[r][0], G[r][1], G[r][2], G[r][3]);
+    }
+}
+
+size_t bwd_smem_bytes(int DK, int DV) {
+    const size_t floats = static_cast<size_t>(DK) * DV + 3ull * kBlk * DK + 2ull * kBlk * DV + 3 * kBlk +
+                          2ull * 16 * 3 * DK + 2 * 16 * 4;
+    return floats * sizeof(float);
+}
+
+template <typename TIn, bool kChannel>
+cudaError_t launch_t(const BwdArgs &a) {
+    const int nblk = (a.T + kBlk - 1) / kBlk;
+    float *ck = static_cast<float *>(a.workspace);
+    float *ew = ck + static_cast<size_t>(a.B) * a.H * nblk * a.d_k * a.d_v;
+    BwdParams p{a.q, a.k, a.v, a.dO, a.alpha, a.eta, a.eps, a.S0, a.dS_T, a.dq, a.dk, a.dv, a.dalpha, a.deta,
+                a.dS0, ck, ew, a.B, a.T, a.H, a.d_k, a.d_v, nblk, a.beta_raw, a.q_scale};
+    const size_t smem = bwd_smem_bytes(a.d_k, a.d_v);
+    const int rows = std::max(1, a.d_k / 16);
+    auto kern = rows == 1 ? bwd_kernel<TIn, kChannel, 1>
+              : rows == 2 ? bwd_kernel<TIn, kChannel, 2>
+              : rows == 4 ? bwd_kernel<TIn, kChannel, 4>
+                          : bwd_kernel<TIn, kChannel, 8>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.H, a.B);
+    kern<<<grid, 4 * a.d_v, smem, a.stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t bwd_workspace_bytes(int B, int T, int H, int d_k, int d_v) {
+    if (B < 1 || H < 1 || T < 1) return 0;
+    const size_t nblk = (static_cast<size_t>(T) + kBlk - 1) / kBlk;
+    return (static_cast<size_t>(B) * H * nblk * d_k * d_v + static_cast<size_t>(B) * T * H * d_v) * sizeof(float);
+}
+
+cudaError_t launch_bwd(const BwdArgs &a) {
+    const bool ch = a.gate == KLA_GATE_CHANNEL;
+    if (a.dtype == KLA_DTYPE_BF16)
+        return ch ? launch_t<__nv_bfloat16, true>(a) : launch_t<__nv_bfloat16, false>(a);
+    return ch ? launch_t<float, true>(a) : launch_t<float, false>(a);
+}
+
+}  // namespace kla

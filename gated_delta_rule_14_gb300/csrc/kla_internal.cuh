@@ -49,6 +49,23 @@ struct DecodeArgs {
     float q_scale;         // o = S^T (q_scale q)
 };
 
+// Backward pass: gradients of a loss given dL/do and dL/dS_T; every gradient is fp32.
+struct BwdArgs {
+    const void *q, *k, *v, *dO;
+    const float *alpha, *eta;
+    float eps;
+    const float *S0, *dS_T;
+    float *dq, *dk, *dv, *dalpha, *deta, *dS0;
+    int B, T, H, d_k, d_v;
+    kla_dtype dtype;
+    kla_gate gate;
+    int beta_raw;
+    float q_scale;
+    void *workspace;
+    size_t workspace_bytes;
+    cudaStream_t stream;
+};
+
 // fp32 CUDA-core chunk path: any supported size, fp32 or bf16 storage.
 cudaError_t launch_chunk_simt(const ChunkArgs &a);
 // tcgen05 tensor-core chunk path: bf16, d_k = d_v = 128, chunk = 64.
@@ -60,6 +77,9 @@ size_t chunk_tc_workspace_bytes(int B, int T, int H);
 // Start states of the segments of every chain: S_start[s+1] = M_s S_start[s] + Z_s.
 cudaError_t launch_seg_combine(const float *Z, const float *M, float *Sst, int chains, int nseg,
                                cudaStream_t stream);
+// backward pass (checkpoints every 8 tokens plus the residuals in the workspace).
+size_t bwd_workspace_bytes(int B, int T, int H, int d_k, int d_v);
+cudaError_t launch_bwd(const BwdArgs &a);
 // fused single-token decode step.
 cudaError_t launch_decode(const DecodeArgs &a);
 // Short sequences (multi-token decode, speculative verification): the state tile stays in

@@ -180,6 +180,40 @@ kla_status kla_decode_step_ex(const void *q, const void *k, const void *v,
                               void *stream);
 
 /*
+ * Backward pass of kla_chunk_fwd_ex (training): the gradients of a scalar loss L with respect to
+ * every input, given dO = dL/do and dS_T = dL/dS_T. The pages give no backward algebra; this is
+ * the chain rule through forget, predict, residual, step size, write and read in reverse token
+ * order (the fp64 oracle of the tests is checked against finite differences of the forward).
+ * All arithmetic is fp32; every gradient is written in fp32.
+ *
+ *   q, k, v, alpha, eta, eps, S0, dtype, gate, beta_mode, q_scale: as for kla_chunk_fwd_ex (the
+ *            same values the forward ran with); q, k, v need only their element alignment here
+ *   dO       [B, T, H, d_v] dtype                 dL/do (read only)
+ *   dS_T     fp32 [B, H, d_k, d_v] or NULL (zero)  dL/dS_T (read only)
+ *   dq, dk   fp32 [B, T, H, d_k]                   written
+ *   dv       fp32 [B, T, H, d_v], 16-byte aligned  written
+ *   dalpha   fp32, shaped like alpha               written (dL/dalpha, not dL/dlog alpha)
+ *   deta     fp32 [B, T, H]                        written
+ *   dS0      fp32 [B, H, d_k, d_v] or NULL         written when given (dL/dS0)
+ *   workspace, workspace_bytes: device scratch of at least kla_chunk_bwd_workspace_size(...) bytes,
+ *            16-byte aligned: the state every 8 tokens and every residual of the forward,
+ *            (ceil(T / 8) d_k d_v + T d_v) floats per (sequence, head)
+ * Outputs must not overlap each other or any input. T = 0 writes dS0 = dS_T (or zeros) only.
+ * Supported sizes: d_k, d_v in {16, 32, 64, 128}. One CTA per (sequence, head) walks its tokens
+ * forward, then backward: the time grows with T, not with B * H.
+ */
+kla_status kla_chunk_bwd(const void *q, const void *k, const void *v,
+                         const float *alpha, const float *eta, float eps, const float *S0,
+                         const void *dO, const float *dS_T,
+                         float *dq, float *dk, float *dv, float *dalpha, float *deta, float *dS0,
+                         int B, int T, int H, int d_k, int d_v,
+                         kla_dtype dtype, kla_gate gate, kla_beta_mode beta_mode, float q_scale,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of device scratch kla_chunk_bwd needs for these sizes (0 when T = 0). */
+size_t kla_chunk_bwd_workspace_size(int B, int T, int H, int d_k, int d_v);
+
+/*
  * Synchronises `stream`, then reads and clears the device-side error flags that
  * bounded waits and range checks of earlier calls on this device may have set.
  * Returns KLA_OK, KLA_ERR_TIMEOUT, KLA_ERR_INVALID_ARG (a per-channel gate outside

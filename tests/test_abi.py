@@ -29,7 +29,8 @@ def declared_functions():
 def test_header_declares_entry_points():
     names = declared_functions()
     for required in ("kla_chunk_fwd", "kla_decode_step", "kla_chunk_fwd_workspace_size", "kla_status_string",
-                     "kla_device_status", "kla_abi_version", "kla_chunk_fwd_ex", "kla_decode_step_ex"):
+                     "kla_device_status", "kla_abi_version", "kla_chunk_fwd_ex", "kla_decode_step_ex",
+                     "kla_chunk_bwd", "kla_chunk_bwd_workspace_size"):
         assert required in names, names
 
 
@@ -113,3 +114,33 @@ def test_ex_entry_points_accept_the_options_before_checking_pointers(lib):
     assert f(None, A, A, A, A, 1e-6, None, A, None, 1, 64, 1, 16, 16, 16, 0, 0, 1, 0.25, None, 0, None) == 1
     assert f(A, A + 0x10000000, A + 0x20000000, A + 0x30000000, A + 0x38000000, 1e-6, None, A + 0x40000000,
              None, 1, 64, 1, 48, 16, 16, 0, 0, 1, 0.0, None, 0, None) == 2
+
+
+def bwd(lib, **kw):
+    args = dict(q=A, k=A + 0x10000000, v=A + 0x20000000, alpha=A + 0x30000000, eta=A + 0x38000000, S0=None,
+                dO=A + 0x40000000, dST=None, dq=A + 0x50000000, dk=A + 0x58000000, dv=A + 0x60000000,
+                dalpha=A + 0x68000000, deta=A + 0x6c000000, dS0=None, B=1, T=64, H=1, d_k=16, d_v=16, dtype=0,
+                gate=0, mode=0, scale=1.0, ws=A + 0x70000000, ws_bytes=1 << 26, stream=None)
+    args.update(kw)
+    a = args
+    return lib.kla_chunk_bwd(a["q"], a["k"], a["v"], a["alpha"], a["eta"], 1e-6, a["S0"], a["dO"], a["dST"], a["dq"],
+                             a["dk"], a["dv"], a["dalpha"], a["deta"], a["dS0"], a["B"], a["T"], a["H"], a["d_k"],
+                             a["d_v"], a["dtype"], a["gate"], a["mode"], a["scale"], a["ws"], a["ws_bytes"],
+                             a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dq=None), 1), (dict(dO=None), 1), (dict(ws=None), 1), (dict(ws_bytes=16), 1), (dict(ws=A + 0x70000008), 1),
+    (dict(dv=A + 0x60000004), 1), (dict(dq=A + 0x20000000), 1),      # dq overlaps v
+    (dict(dk=A + 0x50000100), 1),                                   # dk overlaps dq
+    (dict(dS0=A + 0x70000000), 1),                                  # dS0 overlaps the workspace
+    (dict(mode=3), 1), (dict(scale=float("nan")), 1), (dict(d_k=24), 2), (dict(T=-1), 1),
+])
+def test_bwd_rejects_on_host(lib, kw, code):
+    assert bwd(lib, **kw) == code
+
+
+def test_bwd_workspace_size(lib):
+    # state every 8 tokens plus every residual, fp32
+    assert lib.kla_chunk_bwd_workspace_size(2, 20, 3, 16, 32) == (2 * 3 * 3 * 16 * 32 + 2 * 20 * 3 * 32) * 4
+    assert lib.kla_chunk_bwd_workspace_size(2, 0, 3, 16, 32) == 0

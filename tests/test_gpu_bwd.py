@@ -1,0 +1,127 @@
+"""Backward pass (kla_chunk_bwd) against the fp64 oracle's backward, which is itself pinned to
+finite differences of the forward. Every gradient (q, k, v, alpha, eta, S0) is compared by
+relative L2 over the whole tensor. The GPU computes in fp32 throughout and the oracle receives
+the same stored (fp32 or bf16-rounded) inputs, so both input types are held to fp32-level bounds:
+1e-5 for fp32 inputs, 1e-4 for bf16 inputs (longer sums of larger terms)."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import DEV, sample_chains, to_dev
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-5, "bf16": 1e-4}
+NAMES = ("dq", "dk", "dv", "dalpha", "deta", "dS0")
+
+
+def _grad_inputs(inp, seed, with_dst):
+    rng = np.random.default_rng(seed)
+    wl = inp.wl
+    dO = rng.standard_normal((wl.B, wl.T, wl.H, wl.d_v)).astype(np.float32)
+    if wl.dtype == "bf16":
+        dO = synth.f32_to_bf16_bits(dO)
+    dST = rng.standard_normal((wl.B, wl.H, wl.d_k, wl.d_v)).astype(np.float32) if with_dst else None
+    return dO, dST
+
+
+def _as64(a):
+    if a is None:
+        return None
+    return synth.bf16_bits_to_f32(a).astype(np.float64) if a.dtype == np.uint16 else a.astype(np.float64)
+
+
+def run_gpu(inp, dO, dST, **mode):
+    import gated_delta_rule_14_gb300 as kla
+    g = kla.chunk_bwd(to_dev(inp.q), to_dev(inp.k), to_dev(inp.v), to_dev(inp.alpha), to_dev(inp.eta), to_dev(dO),
+                      inp.wl.eps, to_dev(inp.S0), to_dev(dST), **mode)
+    kla.device_status(DEV)
+    return {n: (None if g[n] is None else g[n].cpu().numpy().astype(np.float64)) for n in NAMES}
+
+
+def run_oracle(inp, dO, dST, chains=None, **mode):
+    """Oracle gradients on the listed (b, h) chains, each as its own B=1, H=1 problem."""
+    wl = inp.wl
+    chains = chains or [(b, h) for b in range(wl.B) for h in range(wl.H)]
+    out = {n: [] for n in NAMES}
+    for b, h in chains:
+        f = lambda a: None if a is None else _as64(a)[b:b + 1, :, h:h + 1]  # noqa: E731
+        s0 = None if inp.S0 is None else inp.S0[b:b + 1, h:h + 1].astype(np.float64)
+        dst = None if dST is None else dST[b:b + 1, h:h + 1].astype(np.float64)
+        g = oracle.load().backward(f(inp.q), f(inp.k), f(inp.v), f(inp.alpha), f(inp.eta), wl.eps, s0, f(dO), dst,
+                                   **mode)
+        for n in NAMES:
+            out[n].append(g[n][0, :, 0] if n != "dS0" else g[n][0, 0])
+    return {n: np.stack(v) for n, v in out.items()}
+
+
+def pick(g, chains):
+    return {n: (None if g[n] is None else
+                np.stack([g[n][b, :, h] if n != "dS0" else g[n][b, h] for b, h in chains])) for n in NAMES}
+
+
+def compare(got, ref, tol, skip=()):
+    for n in NAMES:
+        if n in skip:
+            continue
+        assert np.isfinite(got[n]).all(), n
+        err = oracle.rel_l2(got[n], ref[n])
+        assert err <= tol, f"{n}: rel-L2 {err:.3e} > {tol}"
+
+
+CASES = [
+    # (base, overrides, mode, with dL/dS_T)
+    ("tiny", dict(B=2, T=1, H=2, s0_sigma=0.1), {}, True),
+    ("tiny", dict(B=1, T=37, H=3, d_k=32, d_v=64, s0_sigma=0.1), {}, False),
+    ("kda8k", dict(B=2, T=21, H=2, d_k=64, d_v=16, dtype="f32", s0_sigma=0.1), {}, True),
+    ("gdn4k", dict(B=1, T=100, H=2, dtype="f32", s0_sigma=0.05, key_norm="l2"), dict(beta_mode="raw"), True),
+    ("gdn4k", dict(B=2, T=130, H=2, s0_sigma=0.05), {}, True),
+    ("kda8k", dict(B=1, T=64, H=2, s0_sigma=0.05), dict(q_scale=128 ** -0.5), False),
+    ("gdn4k", dict(B=1, T=203, H=1, d_k=16, d_v=128, dtype="f32"), dict(q_scale=0.5), True),
+]
+
+
+@pytest.mark.parametrize("base,over,mode,with_dst", CASES, ids=lambda x: str(x)[:36])
+def test_backward_against_oracle(base, over, mode, with_dst):
+    inp = synth.make_prefill(base, seed=over["T"] + 5, **over)
+    dO, dST = _grad_inputs(inp, seed=over["T"], with_dst=with_dst)
+    got = run_gpu(inp, dO, dST, **mode)
+    ref = run_oracle(inp, dO, dST, **mode)
+    chains = [(b, h) for b in range(inp.wl.B) for h in range(inp.wl.H)]
+    compare(pick(got, chains), ref, TOL[inp.wl.dtype])
+
+
+def test_backward_without_ds0_and_empty_sequence():
+    import torch
+
+    import gated_delta_rule_14_gb300 as kla
+    inp = synth.make_prefill("gdn4k", seed=3, B=1, T=19, H=2, s0_sigma=0.05)
+    dO, dST = _grad_inputs(inp, seed=4, with_dst=True)
+    full = run_gpu(inp, dO, dST)
+    g = kla.chunk_bwd(to_dev(inp.q), to_dev(inp.k), to_dev(inp.v), to_dev(inp.alpha), to_dev(inp.eta), to_dev(dO),
+                      inp.wl.eps, to_dev(inp.S0), to_dev(dST), want_dS0=False)
+    kla.device_status(DEV)
+    assert g["dS0"] is None
+    for n in ("dq", "dk", "dv", "dalpha", "deta"):
+        assert np.array_equal(g[n].cpu().numpy().astype(np.float64), full[n]), n
+    # T = 0: dL/dS0 = dL/dS_T
+    z = torch.empty((1, 0, 2, 128), dtype=torch.bfloat16, device=DEV)
+    za = torch.empty((1, 0, 2), dtype=torch.float32, device=DEV)
+    dst = to_dev(dST)
+    g = kla.chunk_bwd(z, z, z, za, za, z, 1e-6, to_dev(inp.S0), dst)
+    kla.device_status(DEV)
+    assert torch.equal(g["dS0"], dst)
+
+
+@pytest.mark.parametrize("name,nchains", [("gdn4k", 2), ("kda8k", 1)])
+def test_full_config_sampled(name, nchains):
+    """The bench configuration (all chains on the GPU), checked on sampled chains."""
+    inp = synth.make_prefill(name, seed=1)
+    if name == "kda8k":
+        inp = synth.make_prefill(name, seed=1, T=2048)   # keeps the oracle's stored states small
+    dO, dST = _grad_inputs(inp, seed=2, with_dst=True)
+    got = run_gpu(inp, dO, dST)
+    chains = sample_chains(inp.wl.B, inp.wl.H, nchains, seed=5)
+    ref = run_oracle(inp, dO, dST, chains)
+    compare(pick(got, chains), ref, TOL[inp.wl.dtype])
