@@ -14,7 +14,8 @@ the kernels are launched on.
 Extras in the same JSON line: long131k prefill (B=1 H=16 T=131072), kda8k prefill
 (per-key-channel gate, B=4 H=16 T=8192), decode (batch 64, H16, 1024 single-token
 steps, L2 flushed before every step) and verify4 (the decode batch advanced 4 tokens per
-call, as in speculative verification), each with its own roofline.
+call, as in speculative verification) and bwd_gdn4k (the backward pass of the headline
+workload), each with its own roofline.
 
 --impl reference times the fp64 CPU oracle on the host cores on a bounded sample of the
 same workload (whole sequences of some (b, h) chains) and reports the same metric.
@@ -294,6 +295,32 @@ def bench_verify(ntok, calls, seed, dev, flush, stream, pk):
             "l2": "flushed before every call (256 MiB write, then 256 MiB read)"}
 
 
+BWD_BYTES_PER_TOKEN_HEAD = 4 * 2 * 128 + 8 + 3 * 4 * 128 + 8   # q, k, v, dO in; dq, dk, dv, dalpha, deta out
+
+
+def bench_bwd(name, steps, seed, dev, flush, stream, pk):
+    """Backward pass of the named prefill workload (dL/do random bf16, dL/dS_T = 0)."""
+    import torch
+
+    import gated_delta_rule_14_gb300 as kla
+    inp, d = prefill_inputs(name, seed, dev)
+    wl = inp.wl
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    dO = torch.randn((wl.B, wl.T, wl.H, wl.d_v), device=dev, generator=g).to(torch.bfloat16)
+    ws = torch.empty(kla.bwd_workspace_size(wl.B, wl.T, wl.H, wl.d_k, wl.d_v), dtype=torch.uint8, device=dev)
+
+    def step():
+        kla.chunk_bwd(d["q"], d["k"], d["v"], d["alpha"], d["eta"], dO, wl.eps, workspace=ws, want_dS0=False)
+
+    ms = statistics.fmean(time_steps(step, steps, 1, flush, stream))
+    kla.device_status(dev)
+    alg = wl.B * wl.T * wl.H * BWD_BYTES_PER_TOKEN_HEAD
+    return {"value": wl.B * wl.T / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
+            "workspace_bytes": ws.numel(), "roofline": roofline(alg, ms, pk),
+            "note": "token-sequential fp32 backward, one CTA per (sequence, head): latency-bound"}
+
+
 def e2e_prefill(res, steps, warmup, dev, stream):
     """Same workload through the public API with pinned host buffers: H2D of the inputs, the
     prefill, and D2H of the outputs and final state, all inside the timed region."""
@@ -405,6 +432,7 @@ def main():
     ap.add_argument("--cpu-chains", type=int, default=64)
     ap.add_argument("--decode-steps", type=int, default=1024)
     ap.add_argument("--verify-calls", type=int, default=256)
+    ap.add_argument("--no-bwd", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -480,6 +508,12 @@ def main():
         extras["verify4"] = bench_verify(4, args.verify_calls, seed=rank, dev=dev, flush=flush, stream=stream, pk=pk)
         clocks.mark(t0, time.time())
         launches += args.verify_calls
+        if not args.no_bwd:
+            t0 = time.time()
+            extras["bwd_gdn4k"] = bench_bwd("gdn4k", 3, seed=rank, dev=dev, flush=flush, stream=stream, pk=pk)
+            clocks.mark(t0, time.time())
+            launches += 3
+            torch.cuda.empty_cache()
     clk = clocks.stop()
 
     cpu = None

@@ -21,9 +21,10 @@
 // block barrier per token.
 //   phase F: the forward recurrence, saving the state at every kBlk-token boundary and every
 //            residual e_t (the only forward quantities the reverse needs besides the inputs);
-//   phase R: blocks of kBlk tokens in reverse order: the block's checkpoint goes to shared
-//            memory, and before each reverse token the state entering it is rebuilt from the
-//            checkpoint with the stored residuals (S <- alpha S + beta k e^T: no reductions).
+//   phase R: blocks of kBlk tokens in reverse order: the block's checkpoint and the state
+//            half-way through the block are kept in shared memory, and before each reverse token
+//            the state entering it is rebuilt from the nearer of the two with the stored
+//            residuals (S <- alpha S + beta k e^T: no reductions).
 #include <algorithm>
 
 #include "kla_internal.cuh"
@@ -75,8 +76,11 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const BwdParams p) {
     const int DK = p.DK, DV = p.DV, T = p.T;
     const int nwarps = DV / 8;
     // shared memory carve-up (floats)
-    float *sS = bsm;                                  // checkpoint [DK][DV]
-    float *sk = sS + DK * DV;                         // [kBlk][DK]
+    // thread-private state copies, interleaved by thread so a warp's float4 accesses are
+    // contiguous: element (r, 4 columns) of thread t at float4 index r * blockDim + t
+    float4 *sS = reinterpret_cast<float4 *>(bsm);     // state entering the block
+    float4 *sMid = sS + kRows * blockDim.x;           // state entering the block's token kBlk / 2
+    float *sk = bsm + 8 * kRows * blockDim.x;         // [kBlk][DK]
     float *sq = sk + kBlk * DK;                       // [kBlk][DK]
     float *sa = sq + kBlk * DK;                       // [kBlk][DK] (per-channel gate) or [kBlk]
     float *sv = sa + kBlk * DK;                       // [kBlk][DV]: v (phase F) or e (phase R)
@@ -84,8 +88,8 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const BwdParams p) {
     float *sbeta = sdo + kBlk * DV;                   // [kBlk]
     float *sden = sbeta + kBlk;                       // [kBlk]: ||k||^2 + eps
     float *sas = sden + kBlk;                         // [kBlk]: scalar gate
-    float *red = sas + kBlk;                          // [2][16 warps][3][DK] row partials
-    float *reds = red + 2 * 16 * 3 * DK;              // [2][16 warps][4] scalar partials
+    float *red = sas + kBlk;                          // [2][3][16 warps][DK] row partials
+    float *reds = red + 2 * 3 * 16 * DK;              // [2][16 warps][4] scalar partials
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cg = lane & 1, rg = lane >> 1;
@@ -198,34 +202,59 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const BwdParams p) {
         if (live && p.dST) x = *reinterpret_cast<const float4 *>(p.dST + (bh * DK + r0 + r) * DV + col);
         G[r][0] = x.x; G[r][1] = x.y; G[r][2] = x.z; G[r][3] = x.w;
     }
+    // partial slots of warps that do not exist (d_v < 128) stay zero, so the sums below run over
+    // all 16 slots without a bound
+    for (int idx = tid; idx < 2 * 3 * 16 * DK + 2 * 16 * 4; idx += blockDim.x) red[idx] = 0.f;
+    __syncthreads();
+    const int nthr = blockDim.x;
+    auto load_state = [&](const float4 *src) {
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+            const float4 x = src[r * nthr + tid];
+            S[r][0] = x.x; S[r][1] = x.y; S[r][2] = x.z; S[r][3] = x.w;
+        }
+    };
+    auto store_state = [&](float4 *dst) {
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) dst[r * nthr + tid] = make_float4(S[r][0], S[r][1], S[r][2], S[r][3]);
+    };
+    // S <- alpha_w (.) S + beta_w k_w e_w^T with the stored residual of token w of the block
+    auto replay = [&](int w) {
+        float kr[kRows], a[kRows];
+        rows_of(sk + w * DK, kr);
+        gate_rows(w, a);
+        const float beta = sbeta[w];
+        const float4 ew = *reinterpret_cast<const float4 *>(sv + w * DV + col);
+        const float e[4] = {ew.x, ew.y, ew.z, ew.w};
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+            const float bk = beta * kr[r];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) S[r][c] = fmaf(a[r], S[r][c], bk * e[c]);
+        }
+    };
+    constexpr int kHalf = kBlk / 2;
     int par = 0;
     for (int blk = p.nblk - 1; blk >= 0; --blk) {
         const int t0 = blk * kBlk, n = min(kBlk, T - t0);
-        for (int idx = tid; idx < DK * DV / 4; idx += blockDim.x)
-            reinterpret_cast<float4 *>(sS)[idx] =
-                reinterpret_cast<const float4 *>(ck + static_cast<size_t>(blk) * DK * DV)[idx];
-        stage(t0, n, true);   // ends with a barrier: sS is visible too
+        // this lane's part of the block checkpoint (its own rows and columns: no barrier needed)
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (live) x = *reinterpret_cast<const float4 *>(ck + (static_cast<size_t>(blk) * DK + r0 + r) * DV + col);
+            sS[r * nthr + tid] = x;
+        }
+        stage(t0, n, true);
+        if (n > kHalf) {   // the state entering token kHalf of the block
+            load_state(sS);
+            for (int w = 0; w < kHalf; ++w) replay(w);
+            store_state(sMid);
+        }
         for (int u = n - 1; u >= 0; --u) {
-            // the state entering token t0 + u: checkpoint, then u stored updates
-#pragma unroll
-            for (int r = 0; r < kRows; ++r) {
-                const float4 x = *reinterpret_cast<const float4 *>(sS + (rr + r) * DV + col);
-                S[r][0] = x.x; S[r][1] = x.y; S[r][2] = x.z; S[r][3] = x.w;
-            }
-            for (int w = 0; w < u; ++w) {
-                float kr[kRows], a[kRows];
-                rows_of(sk + w * DK, kr);
-                gate_rows(w, a);
-                const float beta = sbeta[w];
-                const float4 ew = *reinterpret_cast<const float4 *>(sv + w * DV + col);
-                const float e[4] = {ew.x, ew.y, ew.z, ew.w};
-#pragma unroll
-                for (int r = 0; r < kRows; ++r) {
-                    const float bk = beta * kr[r];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) S[r][c] = fmaf(a[r], S[r][c], bk * e[c]);
-                }
-            }
+            // the state entering token t0 + u: the nearest saved state, then the stored updates
+            const int from = u >= kHalf ? kHalf : 0;
+            load_state(u >= kHalf ? sMid : sS);
+            for (int w = from; w < u; ++w) replay(w);
             // the reverse step of token t = t0 + u
             float kr[kRows], qr[kRows], a[kRows];
             rows_of(sk + u * DK, kr);
@@ -287,13 +316,13 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const BwdParams p) {
                 rowB[r] += __shfl_xor_sync(0xffffffffu, rowB[r], 1);
                 rowC[r] += __shfl_xor_sync(0xffffffffu, rowC[r], 1);
             }
-            float *rd = red + (par * 16 + warp) * 3 * DK;
+            float *rd = red + (par * 3 * 16 + warp) * DK;   // quantity q at rd + q * 16 * DK
             if (cg == 0 && live) {
 #pragma unroll
                 for (int r = 0; r < kRows; ++r) {
                     rd[r0 + r] = rowA[r];
-                    rd[DK + r0 + r] = rowB[r];
-                    rd[2 * DK + r0 + r] = rowC[r];
+                    rd[16 * DK + r0 + r] = rowB[r];
+                    rd[32 * DK + r0 + r] = rowC[r];
                 }
             }
             // scalars: e . do and dbeta over the columns (row group 0 holds them), the scalar
@@ -302,52 +331,53 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const BwdParams p) {
             for (int off = 16; off > 0; off >>= 1) sc_da += __shfl_xor_sync(0xffffffffu, sc_da, off);
             sc_edo += __shfl_xor_sync(0xffffffffu, sc_edo, 1);
             sc_db += __shfl_xor_sync(0xffffffffu, sc_db, 1);
-            if (lane == 0) {
-                float *rs = reds + (par * 16 + warp) * 4;
-                rs[0] = sc_edo;
-                rs[1] = sc_db;
-                rs[2] = sc_da;
-            }
+            if (lane == 0)
+                reinterpret_cast<float4 *>(reds)[par * 16 + warp] = make_float4(sc_edo, sc_db, sc_da, 0.f);
             __syncthreads();
             {
-                float edo = 0.f, db = 0.f, dat = 0.f;
-                for (int w = 0; w < nwarps; ++w) {
-                    const float *rs = reds + (par * 16 + w) * 4;
-                    edo += rs[0];
-                    db += rs[1];
-                    dat += rs[2];
-                }
                 const size_t tk = tok(t0 + u);
                 const float den = sden[u];
                 const bool flows = p.beta_raw || den != 0.f;
-                for (int idx = tid; idx < (kChannel ? 2 : 1) * DK; idx += blockDim.x) {
-                    if (idx < DK) {   // dq and dk of row idx
-                        const int i = idx;
-                        float A = 0.f, Bk = 0.f;
-                        for (int w = 0; w < nwarps; ++w) {
-                            A += red[(par * 16 + w) * 3 * DK + i];
-                            Bk += red[(par * 16 + w) * 3 * DK + DK + i];
+                for (int idx = tid; idx < 3 * DK; idx += nthr) {
+                    const int qn = idx / DK, i = idx - qn * DK;   // quantity: 0 dq, 1 dk, 2 dalpha
+                    if (qn == 2 && !kChannel) {
+                        if (i == 0) {
+                            float dat = 0.f;
+#pragma unroll
+                            for (int w = 0; w < 16; ++w) dat += reinterpret_cast<const float4 *>(reds)[par * 16 + w].z;
+                            p.dalpha[tk] = dat;
                         }
-                        const float ki = sk[u * DK + i];
-                        p.dq[tk * DK + i] = s * fmaf(beta * ki, edo, A);
-                        float dki = Bk;
+                        continue;
+                    }
+                    const float *src = red + ((par * 3 + qn) * 16) * DK + i;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int w = 0; w < 16; ++w) acc += src[w * DK];
+                    if (qn == 2) {
+                        p.dalpha[tk * DK + i] = acc;
+                        continue;
+                    }
+                    float edo = 0.f, db = 0.f;
+#pragma unroll
+                    for (int w = 0; w < 16; ++w) {
+                        const float4 x = reinterpret_cast<const float4 *>(reds)[par * 16 + w];
+                        edo += x.x;
+                        db += x.y;
+                    }
+                    const float ki = sk[u * DK + i];
+                    if (qn == 0) {
+                        p.dq[tk * DK + i] = s * fmaf(beta * ki, edo, acc);
+                    } else {
+                        float dki = acc;
                         if (!p.beta_raw && flows) dki = fmaf(-2.f * beta * db / den, ki, dki);
                         p.dk[tk * DK + i] = dki;
-                    } else {          // per-channel dalpha of row idx - DK
-                        const int i = idx - DK;
-                        float C = 0.f;
-                        for (int w = 0; w < nwarps; ++w) C += red[(par * 16 + w) * 3 * DK + 2 * DK + i];
-                        p.dalpha[tk * DK + i] = C;
+                        if (i == 0) p.deta[tk] = p.beta_raw ? db : (flows ? db / den : 0.f);
                     }
-                }
-                if (tid == 0) {
-                    p.deta[tk] = p.beta_raw ? db : (flows ? db / den : 0.f);
-                    if (!kChannel) p.dalpha[tk] = dat;
                 }
             }
             par ^= 1;   // the other buffer is rewritten only after the next barrier
         }
-        __syncthreads();   // checkpoint and staging areas are rewritten by the next block
+        __syncthreads();   // the staging area is rewritten by the next block
     }
     if (p.dS0 && live) {
 #pragma unroll
@@ -357,9 +387,10 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const BwdParams p) {
     }
 }
 
-size_t bwd_smem_bytes(int DK, int DV) {
-    const size_t floats = static_cast<size_t>(DK) * DV + 3ull * kBlk * DK + 2ull * kBlk * DV + 3 * kBlk +
-                          2ull * 16 * 3 * DK + 2 * 16 * 4;
+size_t bwd_smem_bytes(int DK, int DV, int rows) {
+    const size_t threads = 4ull * DV;
+    const size_t floats = 8ull * rows * threads + 3ull * kBlk * DK + 2ull * kBlk * DV + 3 * kBlk +
+                          2ull * 3 * 16 * DK + 2 * 16 * 4;
     return floats * sizeof(float);
 }
 
@@ -370,8 +401,8 @@ cudaError_t launch_t(const BwdArgs &a) {
     float *ew = ck + static_cast<size_t>(a.B) * a.H * nblk * a.d_k * a.d_v;
     BwdParams p{a.q, a.k, a.v, a.dO, a.alpha, a.eta, a.eps, a.S0, a.dS_T, a.dq, a.dk, a.dv, a.dalpha, a.deta,
                 a.dS0, ck, ew, a.B, a.T, a.H, a.d_k, a.d_v, nblk, a.beta_raw, a.q_scale};
-    const size_t smem = bwd_smem_bytes(a.d_k, a.d_v);
     const int rows = std::max(1, a.d_k / 16);
+    const size_t smem = bwd_smem_bytes(a.d_k, a.d_v, rows);
     auto kern = rows == 1 ? bwd_kernel<TIn, kChannel, 1>
               : rows == 2 ? bwd_kernel<TIn, kChannel, 2>
               : rows == 4 ? bwd_kernel<TIn, kChannel, 4>
