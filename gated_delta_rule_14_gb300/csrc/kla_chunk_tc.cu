@@ -110,7 +110,7 @@ struct Small {
     ChunkVec v[2];
     ChanVec ch[2];
     uint64_t full[2];              // q/k/v stage landed (TMA)
-    uint64_t mA, mW, m1, m2;       // tcgen05.commit of the four MMA groups
+    uint64_t mA, mW, m1, m2, mO;   // tcgen05.commit of the five MMA groups
     uint64_t ready, freed;         // operand group -> state group, state group -> operand group
     uint64_t done[2];              // chunk retired, by parity
     uint32_t tmem_base;
@@ -193,7 +193,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     const uint32_t bar_full0 = smem_u32(&sm.full[0]);
     const uint32_t bar_A = smem_u32(&sm.mA), bar_W = smem_u32(&sm.mW);
-    const uint32_t bar_1 = smem_u32(&sm.m1), bar_2 = smem_u32(&sm.m2);
+    const uint32_t bar_1 = smem_u32(&sm.m1), bar_2 = smem_u32(&sm.m2), bar_o = smem_u32(&sm.mO);
     const uint32_t bar_ready = smem_u32(&sm.ready), bar_freed = smem_u32(&sm.freed);
     const uint32_t bar_done0 = smem_u32(&sm.done[0]);
 
@@ -204,6 +204,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_init(bar_W, 1);
         mbar_init(bar_1, 1);
         mbar_init(bar_2, 1);
+        mbar_init(bar_o, 1);
         mbar_init(bar_ready, 1);
         mbar_init(bar_freed, 1);
         mbar_init(bar_done0, 1);
@@ -437,6 +438,23 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
     };
 
+    // W^T = K^T T_K^T and U^T = V^T T_V^T of chunk c (scalar gate); per-channel gate: W_r^T =
+    // K_r^T T_V^T (the factor e^{G_r} of W is carried by the state operand instead).
+    auto issue_wu = [&](int c) {   // one thread
+        tc_fence_after();
+        const uint32_t qk = qk_of(c), vv = v_of(c);
+        const uint32_t tw = sbase + OFF_R + (kCh ? 8192 : 0);
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+            mma_bf16(tbase + TM_W, sw128_desc(qk + s * 2048, 16384, 1024), sw128_desc(tw + s * 32, 16, 1024), id_w, s);
+        if (!p.zero_v) {
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(tbase + TM_U, sw128_desc(vv + s * 2048, 8192, 1024),
+                         sw128_desc(sbase + OFF_R + 8192 + s * 32, 16, 1024), id_w, s);
+        }
+        mma_commit(bar_W);
+    };
     // (b) R and A from [KK^T; QK^T]; T = (I + R)^{-1}; T_K, T_V; issue W^T, U^T.
     auto op_mid = [&](int c) {
         ChunkVec &cv = sm.v[c & 1];
@@ -652,22 +670,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         fence_proxy_async_smem();
         gsync();
         if (gtid == 0) {
-            tc_fence_after();
-            const uint32_t qk = qk_of(c), vv = v_of(c);
-            // scalar gate: W^T = K^T T_K^T; per-channel gate: W_r^T = K_r^T T_V^T (the factor
-            // e^{G_r} of W is carried by the state operand instead)
-            const uint32_t tw = sbase + OFF_R + (kCh ? 8192 : 0);
-#pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_bf16(tbase + TM_W, sw128_desc(qk + s * 2048, 16384, 1024), sw128_desc(tw + s * 32, 16, 1024),
-                         id_w, s);
-            if (!p.zero_v) {
-#pragma unroll
-                for (int s = 0; s < 4; ++s)
-                    mma_bf16(tbase + TM_U, sw128_desc(vv + s * 2048, 8192, 1024),
-                             sw128_desc(sbase + OFF_R + 8192 + s * 32, 16, 1024), id_w, s);
-            }
-            mma_commit(bar_W);
+            issue_wu(c);
             mbar_arrive(bar_ready);   // A, gate vectors and tiles of chunk c written; W^T/U^T in flight
         }
     };
@@ -686,7 +689,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             s_reg[kk] = S0 ? S0[(64 * half + kk) * kD + row] : ((ident && 64 * half + kk == row) ? 1.f : 0.f);
     }
 
-    // (d) S^T -> bf16 operand; issue S^T W^T and S^T Q^T.
+    // (c') W^T = K^T T_K^T and U^T = V^T T_V^T of chunk c, issued by the state group (which
+    // waits for them next) so that the operand group moves on to chunk c+1 at once. Per-channel
+    // gate: W_r^T = K_r^T T_V^T (the factor e^{G_r} of W is carried by the state operand).
+    // (d) S^T -> bf16 operand; issue S^T W^T.
     auto st_issue1 = [&](int c) {
         load_gates(c + 2);   // warp 0: gates of chunk c+2, turned into vectors at the end of chunk c
         // W^T of chunk c -> bf16 MN-major B operand (rows k, 64 tokens per row), over the T area
@@ -722,20 +728,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         gsync();
         if (gtid == 0) {
             tc_fence_after();
-            const uint32_t qk = qk_of(c);
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
                 const uint32_t aoff = (s >> 2) * 16384 + (s & 3) * 32;
                 mma_bf16(tbase + TM_1A, sw128_desc(sbase + OFF_ST + aoff, 16, 1024),
                          sw128_desc(sbase + OFF_WT + s * 2048, 16384, 1024), id_1a, s);
-            }
-            if (write_out) {
-#pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
-                    mma_bf16(tbase + TM_1B, sw128_desc(sbase + OFF_ST + off, 16, 1024),
-                             sw128_desc(qk + 8192 + off, 16, 1024), id_qk, s);
-                }
             }
             mma_commit(bar_1);
         }
@@ -781,13 +778,20 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int s = 0; s < 4; ++s)
                 mma_bf16(tbase + TM_2, sw128_desc(a2 + s * 32, 16, 1024), sw128_desc(b2 + s * 2048, lbo2, 1024), id_2,
                          s);
-            if (write_out) {
+            mma_commit(bar_2);   // the state update waits only for this one
+            if (write_out) {     // the output products: S^T Q^T and E^T A^T
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
+                    mma_bf16(tbase + TM_1B, sw128_desc(sbase + OFF_ST + off, 16, 1024),
+                             sw128_desc(qk + 8192 + off, 16, 1024), id_qk, s);
+                }
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
                     mma_bf16(tbase + TM_3, sw128_desc(sbase + OFF_ET + s * 32, 16, 1024),
                              sw128_desc(aqk_of(c) + s * 32, 16, 1024), id_qk, s);
             }
-            mma_commit(bar_2);
+            mma_commit(bar_o);
         }
     };
 
@@ -812,6 +816,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
             }
         }
+        wait(bar_o, c & 1);
+        tc_fence_after();
         if (write_out) {
             // Pair value channels (m, m^1) so each lane stores two channels as one bf16x2:
             // within each group of 16 tokens, even lanes keep tokens 0-7, odd lanes 8-15.
