@@ -354,10 +354,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         wait(bar_full0 + 8 * (c & 1), (c >> 1) & 1);
         if (!kCh && gtid == 0) {   // scalar gate: [K;Q] K^T needs only the tiles; issue it first
             tc_fence_after();
+            const uint64_t dq = sw128_desc(qk, 16, 1024);
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
                 const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
-                mma_bf16(tbase + TM_A, sw128_desc(qk + off, 16, 1024), sw128_desc(qk + off, 16, 1024), id_qk, s);
+                mma_bf16(tbase + TM_A, desc_add(dq, off), desc_add(dq, off), id_qk, s);
             }
             mma_commit(bar_A);
         }
@@ -427,12 +428,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         if (kCh && gtid == 0) {
             tc_fence_after();
+            const uint64_t dq = sw128_desc(qk, 16, 1024), dkb = sw128_desc(kb_base, 16, 1024);
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
                 const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
                 const uint32_t boff = (s >> 2) * kb_stride + (s & 3) * 32;
-                mma_bf16(tbase + TM_A, sw128_desc(qk + off, 16, 1024), sw128_desc(kb_base + boff, 16, 1024), id_qk,
-                         s);
+                mma_bf16(tbase + TM_A, desc_add(dq, off), desc_add(dkb, boff), id_qk, s);
             }
             mma_commit(bar_A);
         }
@@ -444,14 +445,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tc_fence_after();
         const uint32_t qk = qk_of(c), vv = v_of(c);
         const uint32_t tw = sbase + OFF_R + (kCh ? 8192 : 0);
+        const uint64_t dk = sw128_desc(qk, 16384, 1024), dtw = sw128_desc(tw, 16, 1024);
 #pragma unroll
-        for (int s = 0; s < 4; ++s)
-            mma_bf16(tbase + TM_W, sw128_desc(qk + s * 2048, 16384, 1024), sw128_desc(tw + s * 32, 16, 1024), id_w, s);
+        for (int s = 0; s < 4; ++s) mma_bf16(tbase + TM_W, desc_add(dk, s * 2048), desc_add(dtw, s * 32), id_w, s);
         if (!p.zero_v) {
+            const uint64_t dv = sw128_desc(vv, 8192, 1024), dtv = sw128_desc(sbase + OFF_R + 8192, 16, 1024);
 #pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_bf16(tbase + TM_U, sw128_desc(vv + s * 2048, 8192, 1024),
-                         sw128_desc(sbase + OFF_R + 8192 + s * 32, 16, 1024), id_w, s);
+            for (int s = 0; s < 4; ++s) mma_bf16(tbase + TM_U, desc_add(dv, s * 2048), desc_add(dtv, s * 32), id_w, s);
         }
         mma_commit(bar_W);
     };
@@ -728,11 +728,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         gsync();
         if (gtid == 0) {
             tc_fence_after();
+            const uint64_t dst = sw128_desc(sbase + OFF_ST, 16, 1024), dwt = sw128_desc(sbase + OFF_WT, 16384, 1024);
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
                 const uint32_t aoff = (s >> 2) * 16384 + (s & 3) * 32;
-                mma_bf16(tbase + TM_1A, sw128_desc(sbase + OFF_ST + aoff, 16, 1024),
-                         sw128_desc(sbase + OFF_WT + s * 2048, 16384, 1024), id_1a, s);
+                mma_bf16(tbase + TM_1A, desc_add(dst, aoff), desc_add(dwt, s * 2048), id_1a, s);
             }
             mma_commit(bar_1);
         }
@@ -774,22 +774,20 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // E^T_s area, 64-row blocks)
             const uint32_t a2 = sbase + (kCh ? OFF_ET : OFF_ETS);
             const uint32_t b2 = kCh ? sbase + OFF_ETS : qk, lbo2 = kCh ? 8192 : 16384;
+            const uint64_t da2 = sw128_desc(a2, 16, 1024), db2 = sw128_desc(b2, lbo2, 1024);
 #pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_bf16(tbase + TM_2, sw128_desc(a2 + s * 32, 16, 1024), sw128_desc(b2 + s * 2048, lbo2, 1024), id_2,
-                         s);
+            for (int s = 0; s < 4; ++s) mma_bf16(tbase + TM_2, desc_add(da2, s * 32), desc_add(db2, s * 2048), id_2, s);
             mma_commit(bar_2);   // the state update waits only for this one
             if (write_out) {     // the output products: S^T Q^T and E^T A^T
+                const uint64_t dst = sw128_desc(sbase + OFF_ST, 16, 1024), dqq = sw128_desc(qk + 8192, 16, 1024);
 #pragma unroll
                 for (int s = 0; s < 8; ++s) {
                     const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
-                    mma_bf16(tbase + TM_1B, sw128_desc(sbase + OFF_ST + off, 16, 1024),
-                             sw128_desc(qk + 8192 + off, 16, 1024), id_qk, s);
+                    mma_bf16(tbase + TM_1B, desc_add(dst, off), desc_add(dqq, off), id_qk, s);
                 }
+                const uint64_t det = sw128_desc(sbase + OFF_ET, 16, 1024), daq = sw128_desc(aqk_of(c), 16, 1024);
 #pragma unroll
-                for (int s = 0; s < 4; ++s)
-                    mma_bf16(tbase + TM_3, sw128_desc(sbase + OFF_ET + s * 32, 16, 1024),
-                             sw128_desc(aqk_of(c) + s * 32, 16, 1024), id_qk, s);
+                for (int s = 0; s < 4; ++s) mma_bf16(tbase + TM_3, desc_add(det, s * 32), desc_add(daq, s * 32), id_qk, s);
             }
             mma_commit(bar_o);
         }

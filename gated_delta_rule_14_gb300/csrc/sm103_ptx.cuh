@@ -172,6 +172,14 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
     return d;
 }
 
+// Descriptor of the same tile `byte_off` bytes further on: the start-address field holds
+// address / 16 in 14 bits and shared-memory addresses stay below 256 KB, so the offset adds
+// without carrying into the neighbouring fields (one 64-bit add per MMA instead of rebuilding
+// the descriptor).
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t byte_off) {
+    return desc + static_cast<uint64_t>(byte_off >> 4);
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 D.
 // a_mn / b_mn: 1 if the operand is MN-major (transposed), 0 if K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
