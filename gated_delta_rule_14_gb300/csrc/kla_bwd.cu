@@ -47,6 +47,10 @@ struct BwdParams {
     float q_scale;
 };
 
+__device__ __forceinline__ void prefetch_l2(const void *ptr) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
 // Reduce 4 partial column sums over the 16 row-group lanes (lane bits 1-4) and hand every lane
 // the 4 totals of its column group: a two-level reduce-scatter, two plain levels, then 4
 // shuffles back.
@@ -138,6 +142,38 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const BwdParams p) {
         }
         __syncthreads();
     };
+    // Pull the inputs of tokens [t0, t0 + n) (and, in reverse, the block checkpoint) into L2 while
+    // the current block runs, so the next block's staging waits on L2 rather than HBM.
+    auto prefetch_block = [&](int t0, int n, bool reverse, int blk) {
+        const int esz = sizeof(TIn);
+        const int lk = (DK * esz + 127) / 128, lv = (DV * esz + 127) / 128, le = (DV * 4 + 127) / 128;
+        const int la = kChannel ? (DK * 4 + 127) / 128 : 0;
+        const int per = lk * (reverse ? 2 : 1) + (reverse ? le + lv : lv) + la + 1;
+        for (int idx = tid; idx < n * per; idx += blockDim.x) {
+            const int u = idx / per;
+            int l = idx - u * per;
+            const size_t tk = tok(t0 + u);
+            const char *ptr;
+            if (l < lk) ptr = static_cast<const char *>(p.k) + tk * DK * esz + l * 128;
+            else if ((l -= lk) < (reverse ? lk : 0)) ptr = static_cast<const char *>(p.q) + tk * DK * esz + l * 128;
+            else {
+                if (reverse) l -= lk;
+                if (!reverse && l < lv) ptr = static_cast<const char *>(p.v) + tk * DV * esz + l * 128;
+                else if (reverse && l < le) ptr = reinterpret_cast<const char *>(p.e + tk * DV) + l * 128;
+                else if (reverse && (l -= le) < lv) ptr = static_cast<const char *>(p.dO) + tk * DV * esz + l * 128;
+                else {
+                    l -= lv;
+                    if (l < la) ptr = reinterpret_cast<const char *>(p.alpha + tk * DK) + l * 128;
+                    else ptr = reinterpret_cast<const char *>(p.eta + tk);
+                }
+            }
+            prefetch_l2(ptr);
+        }
+        if (reverse && live) {
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) prefetch_l2(ck + (static_cast<size_t>(blk) * DK + r0 + r) * DV + col);
+        }
+    };
     auto rows_of = [&](const float *v, float (&out)[kRows]) {
 #pragma unroll
         for (int r = 0; r < kRows; ++r) out[r] = v[rr + r];
@@ -164,6 +200,7 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const BwdParams p) {
                     make_float4(S[r][0], S[r][1], S[r][2], S[r][3]);
         }
         stage(t0, n, false);
+        if (blk + 1 < p.nblk) prefetch_block(t0 + kBlk, min(kBlk, T - t0 - kBlk), false, blk + 1);
         for (int u = 0; u < n; ++u) {
             float kr[kRows], a[kRows];
             rows_of(sk + u * DK, kr);
@@ -245,6 +282,7 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const BwdParams p) {
             sS[r * nthr + tid] = x;
         }
         stage(t0, n, true);
+        if (blk > 0) prefetch_block(t0 - kBlk, kBlk, true, blk - 1);
         if (n > kHalf) {   // the state entering token kHalf of the block
             load_state(sS);
             for (int w = 0; w < kHalf; ++w) replay(w);
