@@ -13,7 +13,8 @@ the kernels are launched on.
 
 Extras in the same JSON line: long131k prefill (B=1 H=16 T=131072), kda8k prefill
 (per-key-channel gate, B=4 H=16 T=8192), decode (batch 64, H16, 1024 single-token
-steps, L2 flushed before every step) and verify4 (the decode batch advanced 4 tokens per
+steps, L2 flushed before every step), decode_graph (the same steps as one CUDA graph, L2 not
+flushed), verify4 (the decode batch advanced 4 tokens per
 call, as in speculative verification) and bwd_gdn4k (the backward pass of the headline
 workload), each with its own roofline.
 
@@ -272,6 +273,47 @@ def bench_decode(steps_tok, seed, dev, flush, stream, pk, passes=1, warm_tokens=
             "launches": passes * steps_tok}
 
 
+def bench_decode_graph(steps_tok, seed, dev, pk, replays=3):
+    """The decode steps captured once in a CUDA graph and replayed back to back (no L2 flush:
+    the 64 MB of state stays resident in the 129 MB L2 between steps, as it would for one layer
+    decoding alone)."""
+    import torch
+
+    import gated_delta_rule_14_gb300 as kla
+    dd = synth.make_decode(seed=seed, steps=steps_tok)
+    q, k, v, a, e = (to_dev(x, dev) for x in (dd.q, dd.k, dd.v, dd.alpha, dd.eta))
+    S = to_dev(dd.S, dev)
+    o = torch.empty(q.shape[:3] + (dd.wl.d_v,), dtype=torch.bfloat16, device=dev)
+    kla.decode_step(q[0], k[0], v[0], a[0], e[0], S, dd.wl.eps, out=o[0])   # first call outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            for i in range(steps_tok):
+                kla.decode_step(q[i], k[i], v[i], a[i], e[i], S, dd.wl.eps, out=o[i])
+    torch.cuda.synchronize()
+    g.replay()   # warm-up
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cur = torch.cuda.current_stream(dev)
+    e0.record(cur)
+    for _ in range(replays):
+        g.replay()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    kla.device_status(dev)
+    ms = e0.elapsed_time(e1) / replays
+    heads = dd.wl.B * dd.wl.H
+    gbs = heads * DECODE_BYTES_PER_HEAD_STEP * steps_tok / (ms * 1e-3) / 1e9
+    return {"value": dd.wl.B * steps_tok / (ms * 1e-3), "unit": "tokens/s", "ms_per_token_step": ms / steps_tok,
+            "token_steps": steps_tok, "batch": dd.wl.B, "launches": steps_tok * replays,
+            "l2": "not flushed: the 64 MB state stays L2-resident between steps",
+            "effective_gbs": round(gbs, 1),
+            "note": "one CUDA graph of all steps; effective GB/s above the HBM peak means L2 hits"}
+
+
 def bench_verify(ntok, calls, seed, dev, flush, stream, pk):
     """Multi-token decode (speculative verification): every call advances the decode batch's
     states in place by `ntok` tokens; L2 flushed before every call."""
@@ -504,6 +546,11 @@ def main():
                             "batch": 64, "l2": "flushed before every token step (256 MiB write, then 256 MiB read)",
                             "roofline": roofline(dr["alg_bytes_per_step"], dr["ms_per_token_step"], pk)}
         launches += dr["launches"]
+        t0 = time.time()
+        dg = bench_decode_graph(args.decode_steps, seed=rank, dev=dev, pk=pk)
+        clocks.mark(t0, time.time())
+        extras["decode_graph"] = dg
+        launches += dg["launches"]
         t0 = time.time()
         extras["verify4"] = bench_verify(4, args.verify_calls, seed=rank, dev=dev, flush=flush, stream=stream, pk=pk)
         clocks.mark(t0, time.time())
