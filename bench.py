@@ -57,11 +57,12 @@ DECODE_BYTES_PER_HEAD_STEP = 8 * 128 * 128 + 4 * 2 * 128 + 8
 
 
 # DRAM bytes (read + write) per launch of the tensor-core prefill kernel on the gdn4k
-# workload, from the ncu capture summarised in profiles/chunk_tc_gdn4k_full.md, keyed by the
-# fingerprint of the kernel sources it was taken on. Any other source state reports null.
+# workload, from an ncu capture of that kernel (dram__bytes_read.sum + dram__bytes_write.sum),
+# keyed by the fingerprint of the kernel sources it was taken on. Any other source state
+# reports null.
 TC_SOURCES = ("gated_delta_rule_14_gb300/csrc/kla_chunk_tc.cu", "gated_delta_rule_14_gb300/csrc/sm103_ptx.cuh",
               "gated_delta_rule_14_gb300/csrc/kla_internal.cuh")
-TC_TRAFFIC_GDN4K = {"87fce72d7b4c5312": 520.870912e6}
+TC_TRAFFIC_GDN4K = {"52fa364b4aaa08ff": 520.920832e6}
 
 
 def tc_fingerprint() -> str:
