@@ -145,10 +145,199 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
     }
 }
 
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// Persistent, software-pipelined variant for 32-column tiles with 16-byte aligned vectors: each
+// CTA walks tiles (32 value columns of one head) with a grid stride and copies the next tile's
+// state, k, q, v and gates into the other half of a double buffer (cp.async) while it reduces,
+// updates and writes the current one, so an SM always has loads in flight. Same arithmetic, in
+// the same order, as decode_kernel.
+template <typename TIn, bool kChannel>
+__global__ void __launch_bounds__(kThreads, 5) decode_pipe_kernel(const DecodeParams p, int ntiles) {
+    constexpr int NCG = 8, RG = kThreads / NCG, BV = 32;
+    __shared__ __align__(16) float sS[2][128 * BV];
+    __shared__ __align__(16) TIn skq[2][2][128];
+    __shared__ __align__(16) TIn sv[2][BV];
+    __shared__ __align__(16) float sal[2][kChannel ? 128 : 4];
+    __shared__ __align__(16) float seta[2][4];
+    __shared__ float sa[128];
+    __shared__ float sred[2][kThreads / 32][NCG * 4];
+    __shared__ float snorm[2][kThreads / 32];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cg = tid % NCG, rg = tid / NCG;
+    const int DK = p.DK, DV = p.DV, ctiles = DV / BV;
+    auto tile_bh = [&](int t, int &v0) {
+        v0 = (t % ctiles) * BV;
+        return static_cast<size_t>(t / ctiles);   // = b * H + h
+    };
+    auto prefetch = [&](int t, int slot) {
+        int v0;
+        const size_t bh = tile_bh(t, v0);
+        const float *Sg = p.S + bh * DK * DV + v0;
+        for (int c = tid; c < DK * (BV / 4); c += kThreads) {
+            const int row = c >> 3, ch = c & 7;
+            cp_async16(&sS[slot][row * BV + ch * 4], Sg + static_cast<size_t>(row) * DV + ch * 4);
+        }
+        constexpr int per16 = 16 / sizeof(TIn);
+        const int nkq = DK / per16;                       // 16-byte chunks of k (and of q)
+        const TIn *gk = static_cast<const TIn *>(p.k) + bh * DK, *gq = static_cast<const TIn *>(p.q) + bh * DK;
+        if (tid < nkq) cp_async16(&skq[slot][0][tid * per16], gk + tid * per16);
+        else if (tid < 2 * nkq) cp_async16(&skq[slot][1][(tid - nkq) * per16], gq + (tid - nkq) * per16);
+        const int nv = BV / per16;
+        if (tid >= 64 && tid < 64 + nv)
+            cp_async16(&sv[slot][(tid - 64) * per16], static_cast<const TIn *>(p.v) + bh * DV + v0 + (tid - 64) * per16);
+        if (kChannel) {
+            if (tid >= 96 && tid < 96 + DK / 4) cp_async16(&sal[slot][(tid - 96) * 4], p.alpha + bh * DK + (tid - 96) * 4);
+        } else if (tid == 96) {
+            cp_async4(&sal[slot][0], p.alpha + bh);
+        }
+        if (tid == 127) cp_async4(&seta[slot][0], p.eta + bh);
+    };
+
+    int it = 0;
+    if (blockIdx.x < ntiles) prefetch(blockIdx.x, 0);
+    cp_async_commit();
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+        const int slot = it & 1;
+        if (t + static_cast<int>(gridDim.x) < ntiles) prefetch(t + gridDim.x, slot ^ 1);
+        cp_async_commit();
+        cp_async_wait_1();   // this thread's copies of tile t have landed
+        __syncthreads();     // and everyone else's
+        int v0;
+        const size_t bh = tile_bh(t, v0);
+
+        float4 s[kMaxRowsPerThread];
+#pragma unroll
+        for (int r = 0; r < kMaxRowsPerThread; ++r) {
+            const int i = rg + r * RG;
+            if (i < DK) s[r] = *reinterpret_cast<const float4 *>(&sS[slot][i * BV + cg * 4]);
+        }
+        float kk = 0.f, kq = 0.f;
+        if (tid < DK) {
+            const float kt = to_f32(skq[slot][0][tid]), qt = to_f32(skq[slot][1][tid]);
+            sa[tid] = kChannel ? sal[slot][tid] : 0.f;
+            kk = kt * kt;
+            kq = kt * qt;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            kk += __shfl_xor_sync(0xffffffffu, kk, off);
+            kq += __shfl_xor_sync(0xffffffffu, kq, off);
+        }
+        if (lane == 0) { snorm[0][warp] = kk; snorm[1][warp] = kq; }
+        __syncthreads();
+        float knorm2 = 0.f, kdotq = 0.f;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) { knorm2 += snorm[0][w]; kdotq += snorm[1][w]; }
+        const float beta = kla_beta(seta[slot][0], knorm2, p.eps, p.beta_raw);
+        const float a_scalar = kChannel ? 1.f : sal[slot][0];
+
+        float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
+#pragma unroll
+        for (int r = 0; r < kMaxRowsPerThread; ++r) {
+            const int i = rg + r * RG;
+            if (i < DK) {
+                const float a = kChannel ? sa[i] : a_scalar;
+                const float ak = a * to_f32(skq[slot][0][i]), aq = a * to_f32(skq[slot][1][i]);
+                pk.x = fmaf(ak, s[r].x, pk.x); pk.y = fmaf(ak, s[r].y, pk.y);
+                pk.z = fmaf(ak, s[r].z, pk.z); pk.w = fmaf(ak, s[r].w, pk.w);
+                pq.x = fmaf(aq, s[r].x, pq.x); pq.y = fmaf(aq, s[r].y, pq.y);
+                pq.z = fmaf(aq, s[r].z, pq.z); pq.w = fmaf(aq, s[r].w, pq.w);
+            }
+        }
+#pragma unroll
+        for (int off = NCG; off < 32; off <<= 1) {
+            pk.x += __shfl_xor_sync(0xffffffffu, pk.x, off); pk.y += __shfl_xor_sync(0xffffffffu, pk.y, off);
+            pk.z += __shfl_xor_sync(0xffffffffu, pk.z, off); pk.w += __shfl_xor_sync(0xffffffffu, pk.w, off);
+            pq.x += __shfl_xor_sync(0xffffffffu, pq.x, off); pq.y += __shfl_xor_sync(0xffffffffu, pq.y, off);
+            pq.z += __shfl_xor_sync(0xffffffffu, pq.z, off); pq.w += __shfl_xor_sync(0xffffffffu, pq.w, off);
+        }
+        if (lane < NCG) {
+            *reinterpret_cast<float4 *>(&sred[0][warp][lane * 4]) = pk;
+            *reinterpret_cast<float4 *>(&sred[1][warp][lane * 4]) = pq;
+        }
+        __syncthreads();
+        float4 pred = make_float4(0.f, 0.f, 0.f, 0.f), rd = pred;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) {
+            const float4 x = *reinterpret_cast<const float4 *>(&sred[0][w][cg * 4]);
+            const float4 y = *reinterpret_cast<const float4 *>(&sred[1][w][cg * 4]);
+            pred.x += x.x; pred.y += x.y; pred.z += x.z; pred.w += x.w;
+            rd.x += y.x; rd.y += y.y; rd.z += y.z; rd.w += y.w;
+        }
+        const TIn *vv = &sv[slot][cg * 4];
+        float4 e;
+        e.x = to_f32(vv[0]) - pred.x; e.y = to_f32(vv[1]) - pred.y;
+        e.z = to_f32(vv[2]) - pred.z; e.w = to_f32(vv[3]) - pred.w;
+        if (rg == 0) {   // o = s (S~^T q + beta e (k . q))
+            TIn *o = static_cast<TIn *>(p.o) + bh * DV + v0 + cg * 4;
+            const float bkq = beta * kdotq, sc = p.q_scale;
+            o[0] = from_f32<TIn>(sc * fmaf(bkq, e.x, rd.x));
+            o[1] = from_f32<TIn>(sc * fmaf(bkq, e.y, rd.y));
+            o[2] = from_f32<TIn>(sc * fmaf(bkq, e.z, rd.z));
+            o[3] = from_f32<TIn>(sc * fmaf(bkq, e.w, rd.w));
+        }
+        float *Sbh = p.S + bh * DK * DV;
+#pragma unroll
+        for (int r = 0; r < kMaxRowsPerThread; ++r) {   // S = S~ + beta k e^T
+            const int i = rg + r * RG;
+            if (i < DK) {
+                const float a = kChannel ? sa[i] : a_scalar;
+                const float bk = beta * to_f32(skq[slot][0][i]);
+                float4 x;
+                x.x = fmaf(a, s[r].x, bk * e.x); x.y = fmaf(a, s[r].y, bk * e.y);
+                x.z = fmaf(a, s[r].z, bk * e.z); x.w = fmaf(a, s[r].w, bk * e.w);
+                *reinterpret_cast<float4 *>(Sbh + static_cast<size_t>(i) * DV + v0 + cg * 4) = x;
+            }
+        }
+        __syncthreads();   // slot, sa, sred and snorm are rewritten by the next tile
+    }
+}
+
+template <typename TIn, bool kChannel>
+int pipe_grid(int ntiles) {
+    static int per_sm[64] = {};   // resident CTAs per SM, per device (looked up once)
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return 0;
+    if (per_sm[dev] == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_pipe_kernel<TIn, kChannel>, kThreads, 0) !=
+                cudaSuccess || n <= 0)
+            return 0;
+        per_sm[dev] = n;
+    }
+    return std::min(ntiles, per_sm[dev] * sms);
+}
+
+bool pipe_ok(const DecodeArgs &a) {
+    auto al = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; };
+    return a.d_v % 32 == 0 && a.d_k % 8 == 0 && al(a.q) && al(a.k) && al(a.v) && al(a.S) &&
+           (a.gate == KLA_GATE_SCALAR || al(a.alpha));
+}
+
 template <typename TIn, bool kChannel>
 cudaError_t launch_t(const DecodeArgs &a) {
     const int BV = std::min(a.d_v, 32);
     DecodeParams p{a.q, a.k, a.v, a.alpha, a.eta, a.eps, a.S, a.o, a.B, a.H, a.d_k, a.d_v, BV, a.beta_raw, a.q_scale};
+    if (pipe_ok(a)) {
+        const int ntiles = (a.d_v / 32) * a.H * a.B;
+        const int g = pipe_grid<TIn, kChannel>(ntiles);
+        if (g > 0) {
+            decode_pipe_kernel<TIn, kChannel><<<g, kThreads, 0, a.stream>>>(p, ntiles);
+            return cudaGetLastError();
+        }
+    }
     dim3 grid(a.d_v / BV, a.H, a.B);
     if (BV == 32) decode_kernel<TIn, kChannel, 8><<<grid, kThreads, 0, a.stream>>>(p);
     else decode_kernel<TIn, kChannel, 4><<<grid, kThreads, 0, a.stream>>>(p);
