@@ -387,38 +387,39 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if constexpr (kCh) {
             // Scaled tiles with reference token r: K_r = K e^{G-G_r}, Q_r = Q e^{G-G_r} (in place),
             // K_m = K e^{G_r-G} (B of [K_r;Q_r] K_m^T, over the R area) and K_end = K e^{G_end-G}
-            // (B of E^T K_end, over the E^T_s area, free once chunk c-1 is retired).
+            // (B of E^T K_end, over the E^T_s area, free once E^T K_end of chunk c-1 has run).
             ChanVec &chv = sm.ch[c & 1];
             const float F = chv.F[gch];
             if (gth == 0) chv.gam[gch] = zprod * F;
-            if (c >= 1) wait(bar_done0 + 8 * ((c - 1) & 1), ((c - 1) >> 1) & 1);
+            if (c >= 1) wait(bar_2, (c - 1) & 1);
             const uint32_t col = (gch & 63) * 2, blk = gch >> 6;
-            __nv_bfloat16 *Kt = reinterpret_cast<__nv_bfloat16 *>(smem + (qk - sbase) + blk * 16384);
-            __nv_bfloat16 *Qt = reinterpret_cast<__nv_bfloat16 *>(smem + (qk - sbase) + blk * 16384 + 8192);
-            uint8_t *Km = smem + OFF_R + blk * 8192, *Ke = smem + OFF_ETS + blk * 8192;
+            const uint32_t Kt = qk + blk * 16384, Qt = Kt + 8192;
+            const uint32_t Km = sbase + OFF_R + blk * 8192, Ke = sbase + OFF_ETS + blk * 8192;
+            auto bits = [](float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); };
             float run = 1.f;
 #pragma unroll
             for (int u = 0; u < 32; ++u) {
                 // th 1: tokens 32..63 ascending, run = e^{G_i - G_r};  th 0: tokens 31..0, run = e^{G_r - G_i}
+                // (the factors scale bf16 operands: the fast reciprocal's 2 ulp are far below bf16's)
                 const int uu = gth ? u : 31 - u;
                 const int i = 32 * gth + uu;
                 float fr, fm;
                 if (gth) {
                     run *= ga[uu];
                     fr = run;
-                    fm = __frcp_rn(run);
+                    fm = __fdividef(1.f, run);
                 } else {
                     fm = run;
-                    fr = __frcp_rn(run);
+                    fr = __fdividef(1.f, run);
                     run *= ga[uu];
                 }
                 const uint32_t off = sw128_off(i, col);
-                const float kv = __bfloat162float(*reinterpret_cast<__nv_bfloat16 *>(reinterpret_cast<uint8_t *>(Kt) + off));
-                const float qv = __bfloat162float(*reinterpret_cast<__nv_bfloat16 *>(reinterpret_cast<uint8_t *>(Qt) + off));
-                *reinterpret_cast<__nv_bfloat16 *>(reinterpret_cast<uint8_t *>(Kt) + off) = __float2bfloat16_rn(kv * fr);
-                *reinterpret_cast<__nv_bfloat16 *>(reinterpret_cast<uint8_t *>(Qt) + off) = __float2bfloat16_rn(qv * fr);
-                *reinterpret_cast<__nv_bfloat16 *>(Km + off) = __float2bfloat16_rn(kv * fm);
-                *reinterpret_cast<__nv_bfloat16 *>(Ke + off) = __float2bfloat16_rn(kv * (F * fm));
+                const float kv = ld_shared_bf16(Kt + off);
+                const float qv = ld_shared_bf16(Qt + off);
+                st_shared_b16(Kt + off, bits(kv * fr));
+                st_shared_b16(Qt + off, bits(qv * fr));
+                st_shared_b16(Km + off, bits(kv * fm));
+                st_shared_b16(Ke + off, bits(kv * (F * fm)));
             }
             load_chgates(c + 1);
             fence_proxy_async_smem();

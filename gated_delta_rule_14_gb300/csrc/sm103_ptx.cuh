@@ -206,6 +206,15 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
+// One bf16 element of shared memory, widened to fp32 / narrowed from its bits.
+__device__ __forceinline__ float ld_shared_bf16(uint32_t addr) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+    return __uint_as_float(static_cast<uint32_t>(v) << 16);
+}
+__device__ __forceinline__ void st_shared_b16(uint32_t addr, unsigned short bits) {
+    asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(bits) : "memory");
+}
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
