@@ -318,7 +318,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     // ===================================================================== operand group
     // Per-channel gates (per-channel gate only): thread = (key channel ch, token half th) holds
-    // the 32 gates of its half of the next chunk, clamped to e^-80 like the log-gates.
+    // the 32 gates of its half of the next chunk. The loads are issued a chunk ahead and left
+    // untouched until their first use (`chgate`), so the thread does not wait for them; tokens
+    // past the end load the last token's gate and read as 1, and gates are clamped to e^-80
+    // like the log-gates.
     const int gch = gtid & (kD - 1), gth = gtid >> 7;
     float ga[kCh ? 32 : 1];
     auto load_chgates = [&](int c) {
@@ -326,12 +329,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (grp == 1 && c < nchunks) {
 #pragma unroll
                 for (int u = 0; u < 32; ++u) {
-                    const int t = t_begin + c * kC + 32 * gth + u;
-                    ga[u] = t < t_end ? fmaxf(p.alpha[((static_cast<size_t>(b) * p.T + t) * p.H + h) * kD + gch], 1.8e-35f)
-                                    : 1.f;
+                    const int t = min(t_begin + c * kC + 32 * gth + u, t_end - 1);
+                    ga[u] = p.alpha[((static_cast<size_t>(b) * p.T + t) * p.H + h) * kD + gch];
                 }
             }
         }
+    };
+    auto chgate = [&](int c, int u) {   // gate u of this thread's half of chunk c
+        return t_begin + c * kC + 32 * gth + u < t_end ? fmaxf(ga[u], 1.8e-35f) : 1.f;
     };
 
     // (a) gates, norms, beta and the decay tables; issue [K;Q] K^T.
@@ -345,7 +350,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         float zprod = 1.f;
         if constexpr (kCh) {
 #pragma unroll
-            for (int u = 0; u < 32; ++u) zprod *= ga[u];
+            for (int u = 0; u < 32; ++u) zprod *= chgate(c, u);
             ChanVec &chv = sm.ch[c & 1];
             if (gth == 0) chv.eGr[gch] = zprod;   // e^{G_r}
             else chv.F[gch] = zprod;              // e^{G_end - G_r}
@@ -405,13 +410,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const int i = 32 * gth + uu;
                 float fr, fm;
                 if (gth) {
-                    run *= ga[uu];
+                    run *= chgate(c, uu);
                     fr = run;
                     fm = __fdividef(1.f, run);
                 } else {
                     fm = run;
                     fr = __fdividef(1.f, run);
-                    run *= ga[uu];
+                    run *= chgate(c, uu);
                 }
                 const uint32_t off = sw128_off(i, col);
                 const float kv = ld_shared_bf16(Kt + off);
