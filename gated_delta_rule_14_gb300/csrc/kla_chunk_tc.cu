@@ -327,11 +327,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     auto load_chgates = [&](int c) {
         if constexpr (kCh) {
             if (grp == 1 && c < nchunks) {
+                const int t0 = t_begin + c * kC + 32 * gth;
+                const int last = min(31, t_end - 1 - t0);   // tokens past the end read token t_end - 1
+                const float *g0 = p.alpha + ((static_cast<size_t>(b) * p.T + t0) * p.H + h) * kD + gch;
+                const size_t st = static_cast<size_t>(p.H) * kD;
 #pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    const int t = min(t_begin + c * kC + 32 * gth + u, t_end - 1);
-                    ga[u] = p.alpha[((static_cast<size_t>(b) * p.T + t) * p.H + h) * kD + gch];
-                }
+                for (int u = 0; u < 32; ++u) ga[u] = g0[static_cast<size_t>(min(u, last)) * st];
             }
         }
     };
