@@ -665,8 +665,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     tk[4 * u4 + u] = tv[4 * u4 + u] * g4[u];
                 }
             }
+            // every read of R ended before the solve's last barrier: T_K/T_V may overwrite it now
             const uint32_t bk = sbase + OFF_R, bv = sbase + OFF_R + 8192;
-            gsync();   // every R read done before T_K/T_V overwrite it
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const uint32_t off = sw128_off(n, 32 * kq + 16 * hh);
