@@ -66,3 +66,33 @@ def test_decode_equals_one_token_prefill():
     assert oracle.rel_l2(s_d_g, s_ref) <= 1e-5
     assert oracle.rel_l2(s_p_g, s_ref) <= 1e-2
     assert oracle.rel_l2(o_d_g, o_ref) <= 1e-2 and oracle.rel_l2(o_p_g, o_ref) <= 1e-2
+
+
+def test_decode_unaligned_vectors_take_the_per_tile_kernel():
+    """Vectors aligned only to their element size (allowed by kla_decode_step) cannot be copied
+    in 16-byte units: those calls run the one-CTA-per-tile kernel; the result must be the same
+    as the pipelined kernel's (same arithmetic in the same order) and match the oracle."""
+    import gated_delta_rule_14_gb300 as kla
+    dd = synth.make_decode(seed=8, B=4, H=2, steps=3)
+    heads = [(b, h) for b in range(4) for h in range(2)]
+    o_ref, s_ref = decode_oracle(dd, heads)
+    outs = {}
+    for shift in (0, 1):   # element offset of q, k, v inside a larger buffer
+        S = to_dev(dd.S).clone()
+        q, k, v, a, e = (to_dev(x) for x in (dd.q, dd.k, dd.v, dd.alpha, dd.eta))
+        o = []
+        for i in range(3):
+            vec = []
+            for x in (q[i], k[i], v[i]):
+                buf = torch.empty(x.numel() + 8, dtype=x.dtype, device=DEV)
+                y = buf[shift:shift + x.numel()].view(x.shape)
+                y.copy_(x)
+                vec.append(y)
+            o.append(kla.decode_step(vec[0], vec[1], vec[2], a[i], e[i], S, dd.wl.eps))
+        kla.device_status(DEV)
+        outs[shift] = (torch.stack(o).float().cpu().numpy(), S.cpu().numpy())
+    assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
+    o, S = outs[1]
+    o_g = np.stack([o[:, b, h] for b, h in heads])
+    s_g = np.stack([S[b, h] for b, h in heads])
+    assert oracle.rel_l2(o_g, o_ref) <= 1e-2 and oracle.rel_l2(s_g, s_ref) <= 1e-5
