@@ -26,8 +26,8 @@ import torch
 from . import _native
 from ._native import KlaError  # noqa: F401
 
-__all__ = ["chunk_fwd", "chunk_bwd", "decode_step", "workspace_size", "bwd_workspace_size", "device_status",
-           "KlaError"]
+__all__ = ["chunk_fwd", "chunk_fwd_host", "chunk_bwd", "decode_step", "workspace_size", "bwd_workspace_size",
+           "device_status", "KlaError"]
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -133,6 +133,63 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, alpha: torch.Te
         _stream_ptr(q.device))
     _native.check(st, "kla_chunk_fwd_ex")
     return out, S_T
+
+
+def chunk_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, alpha: torch.Tensor, eta: torch.Tensor,
+                   eps: float = 1e-6, S0: Optional[torch.Tensor] = None, *, chunk: int = 64,
+                   parts: Optional[int] = None, out: Optional[torch.Tensor] = None, S_T: Optional[torch.Tensor] = None,
+                   final_state: bool = True, device=None, buffers: Optional[dict] = None, beta_mode: str = "kla",
+                   q_scale: float = 1.0) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Chunkwise prefill of HOST tensors (pin them for overlap): the batch runs in ``parts`` parts
+    whose host->device copies, prefills and device->host copies overlap (kla_chunk_fwd_host).
+
+    Same shapes as ``chunk_fwd``; ``out`` / ``S_T`` are host tensors (pinned ones are allocated
+    when None). ``buffers`` (from ``host_buffers``) holds the device tensors, reused across calls.
+    Returns (o, S_T) on the host; they are complete once the current stream of ``device`` has
+    been synchronised.
+    """
+    bcode = _beta_code(beta_mode)
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    for n, t in (("q", q), ("k", k), ("v", v), ("alpha", alpha), ("eta", eta)):
+        if t.device.type != "cpu" or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous host tensor")
+    dcode = _dtype_code(q)
+    B, T, H, d_k = q.shape
+    d_v = v.shape[-1]
+    gate = _native.KLA_GATE_CHANNEL if alpha.dim() == 4 else _native.KLA_GATE_SCALAR
+    if buffers is None:
+        buffers = host_buffers(q, v, alpha, device=dev, with_S0=S0 is not None, with_S_T=final_state or S_T is not None)
+    if out is None:
+        out = torch.empty((B, T, H, d_v), dtype=q.dtype, pin_memory=True)
+    if S_T is None and final_state:
+        S_T = torch.empty((B, H, d_k, d_v), dtype=torch.float32, pin_memory=True)
+    parts = parts or min(B, 8)
+    st = _native.lib().kla_chunk_fwd_host(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(eta), _ptr(S0), _ptr(out), _ptr(S_T),
+        _ptr(buffers["q"]), _ptr(buffers["k"]), _ptr(buffers["v"]), _ptr(buffers["alpha"]), _ptr(buffers["eta"]),
+        _ptr(buffers.get("S0") if S0 is not None else None), _ptr(buffers["o"]),
+        _ptr(buffers.get("S_T") if S_T is not None else None), float(eps),
+        B, T, H, d_k, d_v, int(chunk), dcode, gate, bcode, float(q_scale), int(parts), _stream_ptr(dev))
+    _native.check(st, "kla_chunk_fwd_host")
+    return out, S_T
+
+
+def host_buffers(q: torch.Tensor, v: torch.Tensor, alpha: torch.Tensor, *, device=None, with_S0: bool = False,
+                 with_S_T: bool = True) -> dict:
+    """Device tensors for ``chunk_fwd_host`` calls on host tensors shaped like q, v and alpha."""
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    B, T, H, d_k = q.shape
+    d_v = v.shape[-1]
+    b = {"q": torch.empty(q.shape, dtype=q.dtype, device=dev), "k": torch.empty(q.shape, dtype=q.dtype, device=dev),
+         "v": torch.empty(v.shape, dtype=v.dtype, device=dev),
+         "alpha": torch.empty(alpha.shape, dtype=torch.float32, device=dev),
+         "eta": torch.empty((B, T, H), dtype=torch.float32, device=dev),
+         "o": torch.empty((B, T, H, d_v), dtype=q.dtype, device=dev)}
+    if with_S0:
+        b["S0"] = torch.empty((B, H, d_k, d_v), dtype=torch.float32, device=dev)
+    if with_S_T:
+        b["S_T"] = torch.empty((B, H, d_k, d_v), dtype=torch.float32, device=dev)
+    return b
 
 
 def bwd_workspace_size(B: int, T: int, H: int, d_k: int, d_v: int) -> int:

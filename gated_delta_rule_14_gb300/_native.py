@@ -55,6 +55,9 @@ def _declare(lib):
     lib.kla_decode_step_ex.argtypes = [vp, vp, vp, fp, fp, ctypes.c_float, fp, vp, i, i, i, i, i, i, i,
                                        ctypes.c_float, vp]
     lib.kla_decode_step_ex.restype = ctypes.c_int
+    lib.kla_chunk_fwd_host.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, vp, vp, vp, fp, fp, fp, vp, fp, ctypes.c_float,
+                                       i, i, i, i, i, i, i, i, i, ctypes.c_float, i, vp]
+    lib.kla_chunk_fwd_host.restype = ctypes.c_int
     lib.kla_chunk_bwd.argtypes = [vp, vp, vp, fp, fp, ctypes.c_float, fp, vp, fp, fp, fp, fp, fp, fp, fp,
                                   i, i, i, i, i, i, i, i, ctypes.c_float, vp, sz, vp]
     lib.kla_chunk_bwd.restype = ctypes.c_int

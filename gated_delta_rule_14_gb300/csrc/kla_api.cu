@@ -94,10 +94,14 @@ size_t kla_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v, int c
     return kla::chunk_tc_supports(a) ? kla::chunk_tc_workspace_bytes(B, T, H) : 0;
 }
 
-kla_status kla_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *alpha, const float *eta,
-                            float eps, const float *S0, void *o, float *S_T, int B, int T, int H, int d_k, int d_v,
-                            int chunk, kla_dtype dtype, kla_gate gate, kla_beta_mode beta_mode, float q_scale,
-                            void *workspace, size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+namespace {
+
+kla_status chunk_fwd_impl(const void *q, const void *k, const void *v, const float *alpha, const float *eta,
+                          float eps, const float *S0, void *o, float *S_T, int B, int T, int H, int d_k, int d_v,
+                          int chunk, kla_dtype dtype, kla_gate gate, kla_beta_mode beta_mode, float q_scale,
+                          void *workspace, size_t workspace_bytes, void *stream, int no_segments) {
     if (T < 0) return KLA_ERR_INVALID_ARG;
     if (!valid_mode(beta_mode, q_scale)) return KLA_ERR_INVALID_ARG;
     kla_status st = check_common(q, k, v, alpha, eta, o, B, H, d_k, d_v, dtype, gate, 16,
@@ -105,7 +109,7 @@ kla_status kla_chunk_fwd_ex(const void *q, const void *k, const void *v, const f
     if (st != KLA_OK) return st;
     if (!supported_chunk(chunk)) return KLA_ERR_UNSUPPORTED;
     if ((S0 && !aligned16(S0)) || (S_T && !aligned16(S_T))) return KLA_ERR_INVALID_ARG;
-    const size_t need = kla_chunk_fwd_workspace_size(B, T, H, d_k, d_v, chunk, dtype, gate);
+    const size_t need = no_segments ? 0 : kla_chunk_fwd_workspace_size(B, T, H, d_k, d_v, chunk, dtype, gate);
     if (workspace_bytes < need || (need > 0 && !workspace)) return KLA_ERR_INVALID_ARG;
     if (!(eps == eps)) return KLA_ERR_INVALID_ARG;   // NaN stabiliser
 
@@ -136,11 +140,32 @@ kla_status kla_chunk_fwd_ex(const void *q, const void *k, const void *v, const f
                      workspace, workspace_bytes, nullptr, cs};
     a.beta_raw = beta_mode == KLA_BETA_RAW;
     a.q_scale = q_scale;
+    a.no_segments = no_segments;
     if (err_word(&a.err) != cudaSuccess) return KLA_ERR_CUDA;
     cudaError_t e = kla::short_seq_supports(a) ? kla::launch_short_seq(a)
                     : kla::chunk_tc_supports(a) ? kla::launch_chunk_tc(a)
                                                 : kla::launch_chunk_simt(a);
     return e == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
+}
+
+}  // namespace
+
+kla_status kla::chunk_fwd_nosplit(const void *q, const void *k, const void *v, const float *alpha, const float *eta,
+                                  float eps, const float *S0, void *o, float *S_T, int B, int T, int H, int d_k,
+                                  int d_v, int chunk, kla_dtype dtype, kla_gate gate, kla_beta_mode beta_mode,
+                                  float q_scale, void *stream) {
+    return chunk_fwd_impl(q, k, v, alpha, eta, eps, S0, o, S_T, B, T, H, d_k, d_v, chunk, dtype, gate, beta_mode,
+                          q_scale, nullptr, 0, stream, 1);
+}
+
+extern "C" {
+
+kla_status kla_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *alpha, const float *eta,
+                            float eps, const float *S0, void *o, float *S_T, int B, int T, int H, int d_k, int d_v,
+                            int chunk, kla_dtype dtype, kla_gate gate, kla_beta_mode beta_mode, float q_scale,
+                            void *workspace, size_t workspace_bytes, void *stream) {
+    return chunk_fwd_impl(q, k, v, alpha, eta, eps, S0, o, S_T, B, T, H, d_k, d_v, chunk, dtype, gate, beta_mode,
+                          q_scale, workspace, workspace_bytes, stream, 0);
 }
 
 kla_status kla_chunk_fwd(const void *q, const void *k, const void *v, const float *alpha, const float *eta,

@@ -1003,7 +1003,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a) {
                                          static_cast<int>(SMEM_BYTES));
     if (e != cudaSuccess) return e;
     const int chains = a.B * a.H;
-    const SegPlan pl = make_plan(a.B, a.T, a.H);
+    const SegPlan pl = a.no_segments ? SegPlan{1, ((a.T + kC - 1) / kC) * kC} : make_plan(a.B, a.T, a.H);
     TcParams p{a.alpha, a.eta, a.eps, a.S0, a.S_T, a.B, a.T, a.H, pl.seg_len, 0, 1, pl.nseg,
                kS0Chain, kSTLast, 0, 0, a.err, a.beta_raw, a.q_scale};
     if (pl.nseg <= 1) {

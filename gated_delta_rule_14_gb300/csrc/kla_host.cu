@@ -1,0 +1,140 @@
+// kla_host.cu -- prefill from and to host memory with the copies overlapped with the kernels.
+//
+// kla_chunk_fwd_host splits the batch into parts along B (contiguous in every tensor) and runs,
+// for part i: the host-to-device copies of its inputs on an upload stream, the prefill on one of
+// several compute streams once those copies have landed, and the device-to-host copies of its
+// outputs on a download stream once the prefill is done (two streams per direction, parts
+// alternating, so two copies of a direction can be in flight). Copies of part i+1 overlap the
+// prefill of part i, and the two directions of the link overlap each other; prefills of
+// different parts may run at the same time on different SMs (each part runs whole sequences,
+// without the sequence-parallel segments, which would only add work next to other parts).
+//
+// Streams and events are created once per device on the first call and kept for the life of
+// the process. Calls are ordered after earlier work on the caller's stream and the caller's
+// stream waits for the last copy, so the call behaves as if it ran on that stream; calls on one
+// device are serialised by a host mutex while they enqueue their work.
+#include <algorithm>
+#include <mutex>
+
+#include "kla_internal.cuh"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kComputeStreams = 8;
+constexpr int kCopyStreams = 2;    // per direction: parts alternate between them
+constexpr int kMaxParts = 64;
+
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t h2d[kCopyStreams] = {}, d2h[kCopyStreams] = {}, comp[kComputeStreams] = {};
+    cudaEvent_t start = nullptr, in_done[kMaxParts] = {}, out_ready[kMaxParts] = {};
+    cudaEvent_t end[kCopyStreams] = {}, comp_done[kComputeStreams] = {};
+};
+HostPipe g_pipe[kMaxDevices];
+std::mutex g_pipe_mutex[kMaxDevices];
+
+cudaError_t init_pipe(HostPipe &p) {
+    if (p.ready) return cudaSuccess;
+    cudaError_t e = cudaSuccess;
+    const unsigned sf = cudaStreamNonBlocking, ef = cudaEventDisableTiming;
+    for (int c = 0; c < kCopyStreams; ++c) {
+        if ((e = cudaStreamCreateWithFlags(&p.h2d[c], sf)) != cudaSuccess) return e;
+        if ((e = cudaStreamCreateWithFlags(&p.d2h[c], sf)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&p.end[c], cudaEventDisableTiming)) != cudaSuccess) return e;
+    }
+    for (auto &s : p.comp)
+        if ((e = cudaStreamCreateWithFlags(&s, sf)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&p.start, ef)) != cudaSuccess) return e;
+    for (int i = 0; i < kMaxParts; ++i) {
+        if ((e = cudaEventCreateWithFlags(&p.in_done[i], ef)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&p.out_ready[i], ef)) != cudaSuccess) return e;
+    }
+    for (auto &ev : p.comp_done)
+        if ((e = cudaEventCreateWithFlags(&ev, ef)) != cudaSuccess) return e;
+    p.ready = true;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" kla_status kla_chunk_fwd_host(const void *q_h, const void *k_h, const void *v_h, const float *alpha_h,
+                                         const float *eta_h, const float *S0_h, void *o_h, float *S_T_h, void *q_d,
+                                         void *k_d, void *v_d, float *alpha_d, float *eta_d, float *S0_d, void *o_d,
+                                         float *S_T_d, float eps, int B, int T, int H, int d_k, int d_v, int chunk,
+                                         kla_dtype dtype, kla_gate gate, kla_beta_mode beta_mode, float q_scale,
+                                         int parts, void *stream) {
+    if (B < 1 || T < 1 || H < 1 || parts < 1 || parts > std::min(B, kMaxParts)) return KLA_ERR_INVALID_ARG;
+    if (!q_h || !k_h || !v_h || !alpha_h || !eta_h || !o_h || !q_d || !k_d || !v_d || !alpha_d || !eta_d || !o_d)
+        return KLA_ERR_INVALID_ARG;
+    if ((S0_h != nullptr) != (S0_d != nullptr) || (S_T_h != nullptr) != (S_T_d != nullptr)) return KLA_ERR_INVALID_ARG;
+    if (dtype != KLA_DTYPE_F32 && dtype != KLA_DTYPE_BF16) return KLA_ERR_INVALID_ARG;
+    if (gate != KLA_GATE_SCALAR && gate != KLA_GATE_CHANNEL) return KLA_ERR_INVALID_ARG;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KLA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_pipe_mutex[dev]);
+    HostPipe &P = g_pipe[dev];
+    if (init_pipe(P) != cudaSuccess) return KLA_ERR_CUDA;
+
+    const size_t esz = dtype == KLA_DTYPE_BF16 ? 2 : 4;
+    const size_t tok_per_b = static_cast<size_t>(T) * H;           // (t, h) rows of one sequence
+    const size_t qk_b = tok_per_b * d_k * esz, v_b = tok_per_b * d_v * esz;
+    const size_t a_b = tok_per_b * (gate == KLA_GATE_CHANNEL ? d_k : 1) * 4, e_b = tok_per_b * 4;
+    const size_t s_b = static_cast<size_t>(H) * d_k * d_v * 4;
+    const int bp = (B + parts - 1) / parts;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    auto H2D = cudaMemcpyHostToDevice;
+    auto D2H = cudaMemcpyDeviceToHost;
+    auto at = [](const void *p, size_t off) { return static_cast<const char *>(p) + off; };
+    auto atw = [](void *p, size_t off) { return static_cast<char *>(p) + off; };
+
+    bool ok = cudaEventRecord(P.start, cs) == cudaSuccess;
+    for (int c = 0; ok && c < kCopyStreams; ++c)
+        ok = cudaStreamWaitEvent(P.h2d[c], P.start, 0) == cudaSuccess &&
+             cudaStreamWaitEvent(P.d2h[c], P.start, 0) == cudaSuccess;
+    for (int c = 0; ok && c < kComputeStreams; ++c) ok = cudaStreamWaitEvent(P.comp[c], P.start, 0) == cudaSuccess;
+    kla_status st = KLA_OK;
+    for (int i = 0; ok && i < parts; ++i) {
+        const int b0 = i * bp, nb = std::min(bp, B - b0);
+        if (nb <= 0) break;
+        cudaStream_t up = P.h2d[i % kCopyStreams], down = P.d2h[i % kCopyStreams];
+        // inputs of part i
+        ok = cudaMemcpyAsync(atw(q_d, b0 * qk_b), at(q_h, b0 * qk_b), nb * qk_b, H2D, up) == cudaSuccess &&
+             cudaMemcpyAsync(atw(k_d, b0 * qk_b), at(k_h, b0 * qk_b), nb * qk_b, H2D, up) == cudaSuccess &&
+             cudaMemcpyAsync(atw(v_d, b0 * v_b), at(v_h, b0 * v_b), nb * v_b, H2D, up) == cudaSuccess &&
+             cudaMemcpyAsync(atw(alpha_d, b0 * a_b), at(alpha_h, b0 * a_b), nb * a_b, H2D, up) == cudaSuccess &&
+             cudaMemcpyAsync(atw(eta_d, b0 * e_b), at(eta_h, b0 * e_b), nb * e_b, H2D, up) == cudaSuccess &&
+             (!S0_h || cudaMemcpyAsync(atw(S0_d, b0 * s_b), at(S0_h, b0 * s_b), nb * s_b, H2D, up) == cudaSuccess) &&
+             cudaEventRecord(P.in_done[i], up) == cudaSuccess;
+        if (!ok) break;
+        // the prefill of part i
+        cudaStream_t comp = P.comp[i % kComputeStreams];
+        ok = cudaStreamWaitEvent(comp, P.in_done[i], 0) == cudaSuccess;
+        if (!ok) break;
+        st = kla::chunk_fwd_nosplit(at(q_d, b0 * qk_b), at(k_d, b0 * qk_b), at(v_d, b0 * v_b),
+                              reinterpret_cast<const float *>(at(alpha_d, b0 * a_b)),
+                              reinterpret_cast<const float *>(at(eta_d, b0 * e_b)), eps,
+                              S0_d ? reinterpret_cast<const float *>(at(S0_d, b0 * s_b)) : nullptr,
+                              atw(o_d, b0 * v_b), S_T_d ? reinterpret_cast<float *>(atw(S_T_d, b0 * s_b)) : nullptr,
+                              nb, T, H, d_k, d_v, chunk, dtype, gate, beta_mode, q_scale, comp);
+        if (st != KLA_OK) break;
+        ok = cudaEventRecord(P.out_ready[i], comp) == cudaSuccess &&
+             cudaStreamWaitEvent(down, P.out_ready[i], 0) == cudaSuccess;
+        if (!ok) break;
+        // outputs of part i
+        ok = cudaMemcpyAsync(atw(o_h, b0 * v_b), at(o_d, b0 * v_b), nb * v_b, D2H, down) == cudaSuccess &&
+             (!S_T_h ||
+              cudaMemcpyAsync(atw(S_T_h, b0 * s_b), at(S_T_d, b0 * s_b), nb * s_b, D2H, down) == cudaSuccess);
+    }
+    // the caller's stream continues after the last output copy (and after every compute stream,
+    // so that an error part-way leaves no work of this call behind it)
+    bool joined = true;
+    for (int c = 0; joined && c < kCopyStreams; ++c)
+        joined = cudaEventRecord(P.end[c], P.d2h[c]) == cudaSuccess && cudaStreamWaitEvent(cs, P.end[c], 0) == cudaSuccess;
+    for (int c = 0; joined && c < kComputeStreams; ++c)
+        joined = cudaEventRecord(P.comp_done[c], P.comp[c]) == cudaSuccess &&
+                 cudaStreamWaitEvent(cs, P.comp_done[c], 0) == cudaSuccess;
+    if (st != KLA_OK) return st;
+    return ok && joined ? KLA_OK : KLA_ERR_CUDA;
+}

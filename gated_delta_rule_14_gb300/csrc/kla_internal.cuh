@@ -32,6 +32,7 @@ struct ChunkArgs {
     cudaStream_t stream;
     int beta_raw;          // 1: beta = eta (KLA_BETA_RAW)
     float q_scale;         // o = S^T (q_scale q)
+    int no_segments;       // 1: never split long sequences into parallel segments
 };
 
 struct DecodeArgs {
@@ -65,6 +66,13 @@ struct BwdArgs {
     size_t workspace_bytes;
     cudaStream_t stream;
 };
+
+// kla_chunk_fwd_ex without the sequence-parallel segments (no workspace): for callers that run
+// several prefills side by side, where splitting each one would only add work.
+kla_status chunk_fwd_nosplit(const void *q, const void *k, const void *v, const float *alpha, const float *eta,
+                             float eps, const float *S0, void *o, float *S_T, int B, int T, int H, int d_k, int d_v,
+                             int chunk, kla_dtype dtype, kla_gate gate, kla_beta_mode beta_mode, float q_scale,
+                             void *stream);
 
 // fp32 CUDA-core chunk path: any supported size, fp32 or bf16 storage.
 cudaError_t launch_chunk_simt(const ChunkArgs &a);

@@ -155,6 +155,35 @@ kla_status kla_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
                                  kla_dtype dtype, kla_gate gate, void *stream);
 
 /*
+ * kla_chunk_fwd_ex from and to HOST memory, with the copies overlapped with the kernels: the
+ * batch is split into `parts` parts along B; part i's inputs go host -> device on one copy
+ * stream, its prefill runs on one of several compute streams once they have landed, and its
+ * outputs go device -> host on a second copy stream, so part i+1's copies overlap part i's
+ * prefill and both directions of the link are busy at once. The pages have no counterpart: it
+ * is the host-buffer form of kla_chunk_fwd_ex for callers whose tensors live in host memory.
+ *   q_h .. S_T_h  host tensors in the layouts of kla_chunk_fwd; pinned (page-locked) memory is
+ *                 needed for the copies to overlap anything (pageable memory still works, with
+ *                 synchronous copies); S0_h and S_T_h may be NULL (zeros / not wanted)
+ *   q_d .. S_T_d  device buffers of the same sizes, owned by the caller (S0_d / S_T_d NULL
+ *                 exactly when S0_h / S_T_h are); their contents after the call are unspecified
+ *                 except o_d and S_T_d, which hold the results
+ *   parts         1 .. min(B, 64)
+ * Each part runs whole sequences (no sequence-parallel segments, so no workspace). The call is
+ * asynchronous and ordered on `stream`: it starts after earlier work on `stream`, and work
+ * enqueued on `stream` afterwards starts after its last copy. The library keeps two copy
+ * streams, eight compute streams and a few events per device for the life of the process;
+ * calls on one device are serialised by a host mutex while they enqueue. Argument errors as
+ * for kla_chunk_fwd; T must be >= 1.
+ */
+kla_status kla_chunk_fwd_host(const void *q_h, const void *k_h, const void *v_h, const float *alpha_h,
+                              const float *eta_h, const float *S0_h, void *o_h, float *S_T_h,
+                              void *q_d, void *k_d, void *v_d, float *alpha_d, float *eta_d, float *S0_d,
+                              void *o_d, float *S_T_d, float eps,
+                              int B, int T, int H, int d_k, int d_v, int chunk,
+                              kla_dtype dtype, kla_gate gate, kla_beta_mode beta_mode, float q_scale,
+                              int parts, void *stream);
+
+/*
  * One fused single-token step for B sequences (GeekNews page above, section
  * "Kernel Triton recurrente fusionado para decodificacion": forget, predict,
  * residual, outer-product write, read; the KLA step of the KLA page).

@@ -1,0 +1,60 @@
+"""Prefill of host tensors (kla_chunk_fwd_host): the batch split into parts whose copies and
+kernels overlap must give exactly what kla_chunk_fwd gives on device copies of the same inputs
+(each part runs whole sequences through the same kernels), for any part count, with or without
+an initial and a final state."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import DEV, oracle_chains, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def host(a):
+    a = np.ascontiguousarray(a)
+    t = torch.from_numpy(a)
+    if a.dtype == np.uint16:
+        t = t.view(torch.int16).view(torch.bfloat16)
+    return t.pin_memory()
+
+
+@pytest.mark.parametrize("base,over,parts", [
+    ("gdn4k", dict(B=4, T=300, H=2, s0_sigma=0.05), 1),
+    ("gdn4k", dict(B=4, T=300, H=2, s0_sigma=0.05), 3),
+    ("kda8k", dict(B=5, T=130, H=2), 5),
+    ("gdn4k", dict(B=3, T=77, H=2, d_k=64, d_v=32, chunk=32, dtype="f32", s0_sigma=0.1), 2),
+    ("decode", dict(B=6, T=4, H=2, chunk=64, s0_sigma=0.02), 4),
+])
+def test_host_prefill_matches_device_prefill(base, over, parts):
+    import gated_delta_rule_14_gb300 as kla
+    inp = synth.make_prefill(base, seed=over["B"] * 10 + parts, **over)
+    args = [inp.q, inp.k, inp.v, inp.alpha, inp.eta]
+    o_d, s_d = kla.chunk_fwd(*(to_dev(x) for x in args), inp.wl.eps, to_dev(inp.S0), chunk=inp.wl.chunk)
+    S0 = None if inp.S0 is None else host(inp.S0)
+    o_h, s_h = kla.chunk_fwd_host(*(host(x) for x in args), inp.wl.eps, S0, chunk=inp.wl.chunk, parts=parts,
+                                  device=DEV)
+    torch.cuda.synchronize(DEV)
+    kla.device_status(DEV)
+    assert torch.equal(o_h, o_d.cpu()) and torch.equal(s_h, s_d.cpu())
+    o_ref, s_ref = oracle_chains(inp)
+    chains = [(b, h) for b in range(inp.wl.B) for h in range(inp.wl.H)]
+    o_g = np.stack([o_h.float().numpy()[b, :, h] for b, h in chains])
+    s_g = np.stack([s_h.numpy()[b, h] for b, h in chains])
+    tol = 1e-5 if inp.wl.dtype == "f32" else 1e-2
+    assert oracle.rel_l2(o_g, o_ref) <= tol and oracle.rel_l2(s_g, s_ref) <= tol
+
+
+def test_host_prefill_without_final_state_and_bad_parts():
+    import gated_delta_rule_14_gb300 as kla
+    inp = synth.make_prefill("gdn4k", seed=2, B=2, T=100, H=2)
+    args = [host(x) for x in (inp.q, inp.k, inp.v, inp.alpha, inp.eta)]
+    o_h, s_h = kla.chunk_fwd_host(*args, inp.wl.eps, final_state=False, parts=2, device=DEV)
+    torch.cuda.synchronize(DEV)
+    assert s_h is None
+    o_d, _ = kla.chunk_fwd(*(to_dev(x) for x in (inp.q, inp.k, inp.v, inp.alpha, inp.eta)), inp.wl.eps)
+    assert torch.equal(o_h, o_d.cpu())
+    with pytest.raises(kla.KlaError):
+        kla.chunk_fwd_host(*args, inp.wl.eps, parts=3, device=DEV)   # more parts than sequences
