@@ -144,3 +144,23 @@ def test_bwd_workspace_size(lib):
     # state every 8 tokens plus every residual, fp32
     assert lib.kla_chunk_bwd_workspace_size(2, 20, 3, 16, 32) == (2 * 3 * 3 * 16 * 32 + 2 * 20 * 3 * 32) * 4
     assert lib.kla_chunk_bwd_workspace_size(2, 0, 3, 16, 32) == 0
+
+
+def test_host_prefill_rejects_on_host(lib):
+    f = lib.kla_chunk_fwd_host
+    H_ = 0x10000   # fake host and device addresses, never touched: every case fails validation first
+
+    def call(**kw):
+        a = dict(q=H_, k=H_, v=H_, al=H_, et=H_, s0h=None, oh=H_, sth=None, qd=A, kd=A, vd=A, ald=A, etd=A, s0d=None,
+                 od=A, std=None, B=2, T=8, H=1, parts=2)
+        a.update(kw)
+        return f(a["q"], a["k"], a["v"], a["al"], a["et"], a["s0h"], a["oh"], a["sth"], a["qd"], a["kd"], a["vd"],
+                 a["ald"], a["etd"], a["s0d"], a["od"], a["std"], 1e-6, a["B"], a["T"], a["H"], 16, 16, 16, 0, 0, 0,
+                 1.0, a["parts"], None)
+    assert call(parts=3) == 1          # more parts than sequences
+    assert call(parts=0) == 1
+    assert call(q=None) == 1
+    assert call(od=None) == 1
+    assert call(s0h=H_) == 1           # host S0 without a device buffer for it
+    assert call(std=A) == 1            # device S_T without a host one
+    assert call(T=0) == 1
