@@ -63,6 +63,9 @@ DECODE_BYTES_PER_HEAD_STEP = 8 * 128 * 128 + 4 * 2 * 128 + 8
 TC_SOURCES = ("gated_delta_rule_14_gb300/csrc/kla_chunk_tc.cu", "gated_delta_rule_14_gb300/csrc/sm103_ptx.cuh",
               "gated_delta_rule_14_gb300/csrc/kla_internal.cuh")
 TC_TRAFFIC_GDN4K = {"52fa364b4aaa08ff": 520.920832e6}
+# sm__pipe_tensor_cycles_active (fraction of elapsed cycles) of the same kernel and capture:
+# the algorithmic TFLOP/s divided by it is the rate of the MMA phases themselves.
+TC_PIPE_ACTIVE_GDN4K = {"52fa364b4aaa08ff": 0.14987}
 
 
 def tc_fingerprint() -> str:
@@ -516,9 +519,11 @@ def main():
     value = tokens_all / (ms_max * 1e-3)
     kern_ms = res["ms"]
     roof = roofline(res["alg_bytes"], kern_ms, pk, traffic=TC_TRAFFIC_GDN4K.get(tc_fingerprint()))
-    tensor = {"achieved_tflops": round(res["alg_flop"] / (kern_ms * 1e-3) / 1e12, 2),
-              "peak_tflops": pk["bf16_tflops"],
-              "frac": round(res["alg_flop"] / (kern_ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4)}
+    tflops = res["alg_flop"] / (kern_ms * 1e-3) / 1e12
+    active = TC_PIPE_ACTIVE_GDN4K.get(tc_fingerprint())
+    tensor = {"achieved_tflops": round(tflops, 2), "peak_tflops": pk["bf16_tflops"],
+              "frac": round(tflops / pk["bf16_tflops"], 4), "pipe_active": active,
+              "frac_while_active": round(tflops / active / pk["bf16_tflops"], 4) if active else None}
 
     e2e = e2e_prefill(res, max(3, args.steps // 2), 3, dev, stream)
     e2e_val = reduce_sum(e2e["tokens_per_s"], world, dev) if world > 1 else e2e["tokens_per_s"]
