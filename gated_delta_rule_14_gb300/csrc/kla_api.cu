@@ -90,7 +90,7 @@ size_t kla_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v, int c
     if (B < 1 || H < 1 || T < 1) return 0;
     kla::ChunkArgs a{};
     a.B = B; a.T = T; a.H = H; a.d_k = d_k; a.d_v = d_v; a.chunk = chunk; a.dtype = dtype; a.gate = gate;
-    if (kla::short_seq_supports(a)) return 0;
+    if (kla::recurrent_preferred(a)) return 0;
     return kla::chunk_tc_supports(a) ? kla::chunk_tc_workspace_bytes(B, T, H) : 0;
 }
 
@@ -142,9 +142,7 @@ kla_status chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
     a.q_scale = q_scale;
     a.no_segments = no_segments;
     if (err_word(&a.err) != cudaSuccess) return KLA_ERR_CUDA;
-    cudaError_t e = kla::short_seq_supports(a) ? kla::launch_short_seq(a)
-                    : kla::chunk_tc_supports(a) ? kla::launch_chunk_tc(a)
-                                                : kla::launch_chunk_simt(a);
+    cudaError_t e = kla::recurrent_preferred(a) ? kla::launch_recurrent(a) : kla::launch_chunk_tc(a);
     return e == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
 }
 

@@ -74,8 +74,6 @@ kla_status chunk_fwd_nosplit(const void *q, const void *k, const void *v, const 
                              int chunk, kla_dtype dtype, kla_gate gate, kla_beta_mode beta_mode, float q_scale,
                              void *stream);
 
-// fp32 CUDA-core chunk path: any supported size, fp32 or bf16 storage.
-cudaError_t launch_chunk_simt(const ChunkArgs &a);
 // tcgen05 tensor-core chunk path: bf16, d_k = d_v = 128, chunk = 64.
 bool chunk_tc_supports(const ChunkArgs &a);
 cudaError_t launch_chunk_tc(const ChunkArgs &a);
@@ -90,11 +88,12 @@ size_t bwd_workspace_bytes(int B, int T, int H, int d_k, int d_v);
 cudaError_t launch_bwd(const BwdArgs &a);
 // fused single-token decode step.
 cudaError_t launch_decode(const DecodeArgs &a);
-// Short sequences (multi-token decode, speculative verification): the state tile stays in
-// registers while the tokens are walked one by one; any supported size and dtype.
+// Token-by-token recurrence with the state tile in registers: short sequences (multi-token
+// decode, speculative verification, T <= kShortSeqMaxT) and every shape the tensor-core path
+// does not take; any supported size and dtype, fp32 arithmetic.
 constexpr int kShortSeqMaxT = 16;
-bool short_seq_supports(const ChunkArgs &a);
-cudaError_t launch_short_seq(const ChunkArgs &a);
+bool recurrent_preferred(const ChunkArgs &a);
+cudaError_t launch_recurrent(const ChunkArgs &a);
 
 // ------------------------------------------------------------------ device helpers
 template <typename T> __device__ __forceinline__ float to_f32(T x);

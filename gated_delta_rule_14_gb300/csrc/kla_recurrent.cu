@@ -1,16 +1,18 @@
-// kla_short.cu -- short sequences (multi-token decode, speculative verification): T <= 16.
+// kla_recurrent.cu -- the token-by-token recurrence with the state in registers: short sequences
+// (multi-token decode, speculative verification) and every shape the tensor-core chunk path
+// does not take (fp32 inputs, heads other than 128, chunk other than 64).
 //
-// For a handful of new tokens the chunk algebra does not pay: the state tile is read once into
-// registers, the tokens are walked in order with the fused single-token step (GeekNews,
-// "Revisando las variantes de atencion lineal de la familia DeltaNet", section "Kernel Triton
-// recurrente fusionado para decodificacion"; step size from the KLA page, section "La Regola
-// di Aggiornamento KLA"), and the tile is written once. Per token,
+// The state tile is read once into registers, the tokens are walked in order with the fused
+// single-token step (GeekNews, "Revisando las variantes de atencion lineal de la familia
+// DeltaNet", section "Kernel Triton recurrente fusionado para decodificacion"; step size from the
+// KLA page, section "La Regola di Aggiornamento KLA"), and the tile is written once. Per token,
 //   S~ = alpha (.) S;  e = v - S~^T k;  beta = eta / (||k||^2 + eps);  S = S~ + beta k e^T;
 //   o = S~^T q + beta e (k . q)   (= S^T q, the read after the write).
 // Grid: one CTA of 128 threads per (32-column value tile, head, sequence); every thread keeps
-// up to 8 float4 of the d_k x 32 tile. All tokens' q, k, v, gates and step sizes are staged in
-// shared memory once, together with the state loads, so the token loop waits on no global
-// load. All arithmetic is fp32.
+// up to 8 float4 of the d_k x 32 tile. The q, k, v, gates and step sizes of 16 tokens at a time
+// are staged in shared memory (the first block together with the state loads), so the token
+// loop waits on no global load and has one block barrier per 16 tokens. All arithmetic is fp32,
+// in the recurrence's own order: it is also the exact (fp32) path.
 #include <algorithm>
 
 #include "kla_internal.cuh"
@@ -20,7 +22,7 @@ namespace {
 
 constexpr int kThreads = 128;
 
-struct ShortParams {
+struct RecParams {
     const void *q, *k, *v;
     const float *alpha, *eta;
     float eps;
@@ -92,7 +94,7 @@ __device__ __forceinline__ float reduce_scatter8(const float (&x)[8], int lane) 
 }
 
 template <typename TIn, bool kChannel, int CGW, int kRows>
-__global__ void __launch_bounds__(kThreads) short_seq_kernel(const ShortParams p) {
+__global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecParams p) {
     constexpr int kWarps = kThreads / 32;
     constexpr int BV = kWarps * CGW * 4;          // columns per CTA
     constexpr int U = BV / 4;                     // 16-byte units per tile row
@@ -124,43 +126,46 @@ __global__ void __launch_bounds__(kThreads) short_seq_kernel(const ShortParams p
         }
     }
 
-    // 2. every token's vectors into shared memory
+    // 2. the vectors of tokens [tb, tb + n) into shared memory (slots 0 .. n-1), then
+    // 3. ||k||^2, k.q and beta per token (one warp per token)
     auto tok = [&](int t) { return (static_cast<size_t>(b) * T + t) * p.H + h; };
     const TIn *gk = static_cast<const TIn *>(p.k), *gq = static_cast<const TIn *>(p.q);
-    for (int idx = tid; idx < T * DK; idx += kThreads) {
-        const int t = idx / DK, c = idx - t * DK;
-        const size_t g = tok(t) * DK + c;
-        sk[t][c] = to_f32(gk[g]);
-        sq[t][c] = to_f32(gq[g]);
-        if (kChannel) sa[t][c] = p.alpha[g];
-    }
     const TIn *gv = static_cast<const TIn *>(p.v);
-    for (int idx = tid; idx < T * BV; idx += kThreads) {
-        const int t = idx / BV, c = idx - t * BV;
-        sv[t][c] = to_f32(gv[tok(t) * p.DV + vt0 + c]);
-    }
-    if (tid < T) {
-        if (!kChannel) sas[tid] = p.alpha[tok(tid)];
-        sbeta[tid] = p.eta[tok(tid)];   // eta for now; replaced by beta below
-    }
-    __syncthreads();
-    // 3. ||k||^2, k.q and beta per token (one warp per token)
-    for (int t = warp; t < T; t += kWarps) {
-        float kk = 0.f, kq = 0.f;
-        for (int c = lane; c < DK; c += 32) {
-            kk = fmaf(sk[t][c], sk[t][c], kk);
-            kq = fmaf(sk[t][c], sq[t][c], kq);
+    auto stage = [&](int tb, int n) {
+        for (int idx = tid; idx < n * DK; idx += kThreads) {
+            const int t = idx / DK, c = idx - t * DK;
+            const size_t g = tok(tb + t) * DK + c;
+            sk[t][c] = to_f32(gk[g]);
+            sq[t][c] = to_f32(gq[g]);
+            if (kChannel) sa[t][c] = p.alpha[g];
         }
+        for (int idx = tid; idx < n * BV; idx += kThreads) {
+            const int t = idx / BV, c = idx - t * BV;
+            sv[t][c] = to_f32(gv[tok(tb + t) * p.DV + vt0 + c]);
+        }
+        if (tid < n) {
+            if (!kChannel) sas[tid] = p.alpha[tok(tb + tid)];
+            sbeta[tid] = p.eta[tok(tb + tid)];   // eta for now; replaced by beta below
+        }
+        __syncthreads();
+        for (int t = warp; t < n; t += kWarps) {
+            float kk = 0.f, kq = 0.f;
+            for (int c = lane; c < DK; c += 32) {
+                kk = fmaf(sk[t][c], sk[t][c], kk);
+                kq = fmaf(sk[t][c], sq[t][c], kq);
+            }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            kk += __shfl_xor_sync(0xffffffffu, kk, off);
-            kq += __shfl_xor_sync(0xffffffffu, kq, off);
+            for (int off = 16; off > 0; off >>= 1) {
+                kk += __shfl_xor_sync(0xffffffffu, kk, off);
+                kq += __shfl_xor_sync(0xffffffffu, kq, off);
+            }
+            if (lane == 0) {
+                sbeta[t] = kla_beta(sbeta[t], kk, p.eps, p.beta_raw);
+                skq[t] = kq;
+            }
         }
-        if (lane == 0) {
-            sbeta[t] = kla_beta(sbeta[t], kk, p.eps, p.beta_raw);
-            skq[t] = kq;
-        }
-    }
+    };
+    stage(0, min(T, kShortSeqMaxT));
     cp_async_wait_all();
     __syncthreads();
 
@@ -175,56 +180,64 @@ __global__ void __launch_bounds__(kThreads) short_seq_kernel(const ShortParams p
     }
     const int rr = live ? r0 : 0;   // lanes past d_k read row 0 and discard it
 
-    // 5. the tokens, in order; no block barrier from here on
-    for (int t = 0; t < T; ++t) {
-        const float beta = sbeta[t], kdotq = skq[t];
-        const float as = kChannel ? 1.f : sas[t];
-        float kr[kRows], qr[kRows], ar[kRows], kg[kRows];
-        rows_from_smem<kRows>(&sk[t][rr], kr);
-        rows_from_smem<kRows>(&sq[t][rr], qr);
-#pragma unroll
-        for (int r = 0; r < kRows; ++r) kg[r] = kr[r];
-        if constexpr (kChannel) {
-            rows_from_smem<kRows>(&sa[t][rr], ar);
-#pragma unroll
-            for (int r = 0; r < kRows; ++r) { kg[r] *= ar[r]; qr[r] *= ar[r]; }   // rows of alpha (.) k, q
+    // 5. the tokens, in order, kShortSeqMaxT at a time (one block barrier per block, none per token)
+    for (int tb = 0; tb < T; tb += kShortSeqMaxT) {
+        const int n = min(kShortSeqMaxT, T - tb);
+        if (tb > 0) {
+            __syncthreads();   // every lane is done with the previous block's vectors
+            stage(tb, n);
+            __syncthreads();
         }
-        // partial S~^T k and S~^T q over this lane's rows (for a scalar gate alpha is applied
-        // after the reduction); packed fp32 FMAs over column pairs
-        float2 pk0 = make_float2(0.f, 0.f), pk1 = pk0, pq0 = pk0, pq1 = pk0;
-        if (live) {
+        for (int t = 0; t < n; ++t) {
+            const float beta = sbeta[t], kdotq = skq[t];
+            const float as = kChannel ? 1.f : sas[t];
+            float kr[kRows], qr[kRows], ar[kRows], kg[kRows];
+            rows_from_smem<kRows>(&sk[t][rr], kr);
+            rows_from_smem<kRows>(&sq[t][rr], qr);
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) kg[r] = kr[r];
+            if constexpr (kChannel) {
+                rows_from_smem<kRows>(&sa[t][rr], ar);
+#pragma unroll
+                for (int r = 0; r < kRows; ++r) { kg[r] *= ar[r]; qr[r] *= ar[r]; }   // rows of alpha (.) k, q
+            }
+            // partial S~^T k and S~^T q over this lane's rows (for a scalar gate alpha is applied
+            // after the reduction); packed fp32 FMAs over column pairs
+            float2 pk0 = make_float2(0.f, 0.f), pk1 = pk0, pq0 = pk0, pq1 = pk0;
+            if (live) {
+#pragma unroll
+                for (int r = 0; r < kRows; ++r) {
+                    const float2 kk2 = make_float2(kg[r], kg[r]), qq2 = make_float2(qr[r], qr[r]);
+                    pk0 = __ffma2_rn(kk2, s[r][0], pk0); pk1 = __ffma2_rn(kk2, s[r][1], pk1);
+                    pq0 = __ffma2_rn(qq2, s[r][0], pq0); pq1 = __ffma2_rn(qq2, s[r][1], pq1);
+                }
+            }
+            const float part[8] = {pk0.x, pk0.y, pk1.x, pk1.y, pq0.x, pq0.y, pq1.x, pq1.y};
+            const float red = reduce_scatter8<CGW>(part, lane) * as;   // full sum number (lane >> 2) & 7
+            // every lane needs the four prediction sums of its column group
+            const int src = lane & 3;
+            float pred[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) pred[j] = __shfl_sync(0xffffffffu, red, (j << 2) | src);
+            const float4 vt = *reinterpret_cast<const float4 *>(&sv[t][ucol * 4]);
+            const float e[4] = {vt.x - pred[0], vt.y - pred[1], vt.z - pred[2], vt.w - pred[3]};
+            const int m = (lane >> 2) & 7;
+            if (m >= 4 && (lane & (3 & ~(CGW - 1))) == 0) {   // o = s (S~^T q + beta e (k . q))
+                const int j = m - 4;
+                const float ej = j == 0 ? e[0] : j == 1 ? e[1] : j == 2 ? e[2] : e[3];
+                static_cast<TIn *>(p.o)[tok(tb + t) * p.DV + vt0 + ucol * 4 + j] =
+                    from_f32<TIn>(p.q_scale * fmaf(beta * kdotq, ej, red));
+            }
+            // S = S~ + beta k e^T (lanes past d_k update rows they never store)
+            const float2 e01 = make_float2(e[0], e[1]), e23 = make_float2(e[2], e[3]);
 #pragma unroll
             for (int r = 0; r < kRows; ++r) {
-                const float2 kk2 = make_float2(kg[r], kg[r]), qq2 = make_float2(qr[r], qr[r]);
-                pk0 = __ffma2_rn(kk2, s[r][0], pk0); pk1 = __ffma2_rn(kk2, s[r][1], pk1);
-                pq0 = __ffma2_rn(qq2, s[r][0], pq0); pq1 = __ffma2_rn(qq2, s[r][1], pq1);
+                const float a = kChannel ? ar[r] : as;
+                const float bk = beta * kr[r];
+                const float2 a2 = make_float2(a, a), bk2 = make_float2(bk, bk);
+                s[r][0] = __ffma2_rn(a2, s[r][0], __fmul2_rn(bk2, e01));
+                s[r][1] = __ffma2_rn(a2, s[r][1], __fmul2_rn(bk2, e23));
             }
-        }
-        const float part[8] = {pk0.x, pk0.y, pk1.x, pk1.y, pq0.x, pq0.y, pq1.x, pq1.y};
-        const float red = reduce_scatter8<CGW>(part, lane) * as;   // full sum number (lane >> 2) & 7
-        // every lane needs the four prediction sums of its column group
-        const int src = lane & 3;
-        float pred[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) pred[j] = __shfl_sync(0xffffffffu, red, (j << 2) | src);
-        const float4 vt = *reinterpret_cast<const float4 *>(&sv[t][ucol * 4]);
-        const float e[4] = {vt.x - pred[0], vt.y - pred[1], vt.z - pred[2], vt.w - pred[3]};
-        const int m = (lane >> 2) & 7;
-        if (m >= 4 && (lane & (3 & ~(CGW - 1))) == 0) {   // o = s (S~^T q + beta e (k . q))
-            const int j = m - 4;
-            const float ej = j == 0 ? e[0] : j == 1 ? e[1] : j == 2 ? e[2] : e[3];
-            static_cast<TIn *>(p.o)[tok(t) * p.DV + vt0 + ucol * 4 + j] =
-                from_f32<TIn>(p.q_scale * fmaf(beta * kdotq, ej, red));
-        }
-        // S = S~ + beta k e^T (lanes past d_k update rows they never store)
-        const float2 e01 = make_float2(e[0], e[1]), e23 = make_float2(e[2], e[3]);
-#pragma unroll
-        for (int r = 0; r < kRows; ++r) {
-            const float a = kChannel ? ar[r] : as;
-            const float bk = beta * kr[r];
-            const float2 a2 = make_float2(a, a), bk2 = make_float2(bk, bk);
-            s[r][0] = __ffma2_rn(a2, s[r][0], __fmul2_rn(bk2, e01));
-            s[r][1] = __ffma2_rn(a2, s[r][1], __fmul2_rn(bk2, e23));
         }
     }
 
@@ -248,13 +261,13 @@ __global__ void __launch_bounds__(kThreads) short_seq_kernel(const ShortParams p
 }
 
 template <typename TIn, bool kChannel, int CGW>
-cudaError_t launch_rows(const ChunkArgs &a, const ShortParams &p, dim3 grid) {
+cudaError_t launch_rows(const ChunkArgs &a, const RecParams &p, dim3 grid) {
     const int rows = std::max(1, a.d_k / (32 / CGW));
     switch (rows) {
-        case 1: short_seq_kernel<TIn, kChannel, CGW, 1><<<grid, kThreads, 0, a.stream>>>(p); break;
-        case 2: short_seq_kernel<TIn, kChannel, CGW, 2><<<grid, kThreads, 0, a.stream>>>(p); break;
-        case 4: short_seq_kernel<TIn, kChannel, CGW, 4><<<grid, kThreads, 0, a.stream>>>(p); break;
-        default: short_seq_kernel<TIn, kChannel, CGW, 8><<<grid, kThreads, 0, a.stream>>>(p); break;
+        case 1: recurrent_kernel<TIn, kChannel, CGW, 1><<<grid, kThreads, 0, a.stream>>>(p); break;
+        case 2: recurrent_kernel<TIn, kChannel, CGW, 2><<<grid, kThreads, 0, a.stream>>>(p); break;
+        case 4: recurrent_kernel<TIn, kChannel, CGW, 4><<<grid, kThreads, 0, a.stream>>>(p); break;
+        default: recurrent_kernel<TIn, kChannel, CGW, 8><<<grid, kThreads, 0, a.stream>>>(p); break;
     }
     return cudaGetLastError();
 }
@@ -262,7 +275,7 @@ cudaError_t launch_rows(const ChunkArgs &a, const ShortParams &p, dim3 grid) {
 template <typename TIn, bool kChannel>
 cudaError_t launch_t(const ChunkArgs &a) {
     const int BV = std::min(a.d_v, 32);   // d_v is 16, 32, 64 or 128
-    ShortParams p{a.q, a.k, a.v, a.alpha, a.eta, a.eps, a.S0, a.o, a.S_T, a.B, a.T, a.H, a.d_k, a.d_v, a.beta_raw,
+    RecParams p{a.q, a.k, a.v, a.alpha, a.eta, a.eps, a.S0, a.o, a.S_T, a.B, a.T, a.H, a.d_k, a.d_v, a.beta_raw,
                   a.q_scale};
     dim3 grid(a.d_v / BV, a.H, a.B);
     return BV == 32 ? launch_rows<TIn, kChannel, 2>(a, p, grid) : launch_rows<TIn, kChannel, 1>(a, p, grid);
@@ -270,9 +283,11 @@ cudaError_t launch_t(const ChunkArgs &a) {
 
 }  // namespace
 
-bool short_seq_supports(const ChunkArgs &a) { return a.T >= 1 && a.T <= kShortSeqMaxT; }
+bool recurrent_preferred(const ChunkArgs &a) {
+    return a.T >= 1 && (a.T <= kShortSeqMaxT || !chunk_tc_supports(a));
+}
 
-cudaError_t launch_short_seq(const ChunkArgs &a) {
+cudaError_t launch_recurrent(const ChunkArgs &a) {
     const bool ch = a.gate == KLA_GATE_CHANNEL;
     if (a.dtype == KLA_DTYPE_BF16)
         return ch ? launch_t<__nv_bfloat16, true>(a) : launch_t<__nv_bfloat16, false>(a);
