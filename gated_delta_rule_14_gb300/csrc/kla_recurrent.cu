@@ -57,6 +57,8 @@ __device__ __forceinline__ void rows_from_smem(const float *src, float (&dst)[kR
     }
 }
 
+__device__ __forceinline__ void prefetch_l2(const void *ptr) { asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr)); }
+
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
     const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem) : "memory");
@@ -165,7 +167,24 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecParams p) 
             }
         }
     };
+    // the next block's k, q (and per-channel gates) and v, pulled into L2 while this block runs
+    auto prefetch_block = [&](int tb, int n) {
+        const int lines_k = (DK * static_cast<int>(sizeof(TIn)) + 127) / 128;
+        const int lines_a = kChannel ? (DK * 4 + 127) / 128 : 0;
+        const int per = 2 * lines_k + lines_a + 1;
+        for (int idx = tid; idx < n * per; idx += kThreads) {
+            const int t = idx / per, l = idx - t * per;
+            const size_t tk = tok(tb + t);
+            const char *ptr;
+            if (l < lines_k) ptr = reinterpret_cast<const char *>(gk + tk * DK) + 128 * l;
+            else if (l < 2 * lines_k) ptr = reinterpret_cast<const char *>(gq + tk * DK) + 128 * (l - lines_k);
+            else if (l < 2 * lines_k + lines_a) ptr = reinterpret_cast<const char *>(p.alpha + tk * DK) + 128 * (l - 2 * lines_k);
+            else ptr = reinterpret_cast<const char *>(gv + tk * p.DV + vt0);
+            prefetch_l2(ptr);
+        }
+    };
     stage(0, min(T, kShortSeqMaxT));
+    if (T > kShortSeqMaxT) prefetch_block(kShortSeqMaxT, min(kShortSeqMaxT, T - kShortSeqMaxT));
     cp_async_wait_all();
     __syncthreads();
 
@@ -187,6 +206,7 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecParams p) 
             __syncthreads();   // every lane is done with the previous block's vectors
             stage(tb, n);
             __syncthreads();
+            if (tb + kShortSeqMaxT < T) prefetch_block(tb + kShortSeqMaxT, min(kShortSeqMaxT, T - tb - kShortSeqMaxT));
         }
         for (int t = 0; t < n; ++t) {
             const float beta = sbeta[t], kdotq = skq[t];
