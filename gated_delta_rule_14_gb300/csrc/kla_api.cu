@@ -4,6 +4,11 @@
 
 #include "kla_internal.cuh"
 
+namespace kla {
+// one bounded wait on a barrier phase that nothing completes (kla_selftest.cu)
+cudaError_t launch_selftest_wait(unsigned *err, unsigned limit, cudaStream_t stream);
+}  // namespace kla
+
 namespace {
 
 // One error word per device; bounded device waits and range checks OR bits into it.
@@ -254,6 +259,15 @@ kla_status kla_chunk_bwd(const void *q, const void *k, const void *v, const floa
     kla::BwdArgs a{q, k, v, dO, alpha, eta, eps, S0, dS_T, dq, dk, dv, dalpha, deta, dS0, B, T, H, d_k, d_v,
                    dtype, gate, beta_mode == KLA_BETA_RAW, q_scale, workspace, workspace_bytes, cs};
     return kla::launch_bwd(a) == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
+}
+
+kla_status kla_selftest_wait_timeout(unsigned limit_polls, void *stream) {
+    if (limit_polls < 1 || limit_polls > 100000) return KLA_ERR_INVALID_ARG;
+    unsigned *err = nullptr;
+    if (err_word(&err) != cudaSuccess) return KLA_ERR_CUDA;
+    return kla::launch_selftest_wait(err, limit_polls, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? KLA_OK
+               : KLA_ERR_CUDA;
 }
 
 kla_status kla_device_status(void *stream) {

@@ -250,6 +250,17 @@ size_t kla_chunk_bwd_workspace_size(int B, int T, int H, int d_k, int d_v);
  */
 kla_status kla_device_status(void *stream);
 
+/*
+ * Self-test of the failure path (no counterpart on the pages): launches one thread that waits,
+ * with the bounded wait every kernel of the library uses, on a barrier phase that nothing
+ * completes. After `limit_polls` polls of at most 20 us each (1 .. 100000, i.e. at most 2 s) the
+ * wait gives up and records a time-out, exactly as a stuck wait inside a real kernel would; no
+ * fault, trap or hang is involved and the context stays usable. The next kla_device_status()
+ * on the stream returns KLA_ERR_TIMEOUT (and clears the flag). KLA_ERR_INVALID_ARG for a limit
+ * out of range.
+ */
+kla_status kla_selftest_wait_timeout(unsigned limit_polls, void *stream);
+
 /* Static, human-readable name of a status code. */
 const char *kla_status_string(kla_status status);
 

@@ -30,7 +30,8 @@ def test_header_declares_entry_points():
     names = declared_functions()
     for required in ("kla_chunk_fwd", "kla_decode_step", "kla_chunk_fwd_workspace_size", "kla_status_string",
                      "kla_device_status", "kla_abi_version", "kla_chunk_fwd_ex", "kla_decode_step_ex",
-                     "kla_chunk_bwd", "kla_chunk_bwd_workspace_size"):
+                     "kla_chunk_bwd", "kla_chunk_bwd_workspace_size", "kla_chunk_fwd_host",
+                     "kla_selftest_wait_timeout"):
         assert required in names, names
 
 
@@ -164,3 +165,9 @@ def test_host_prefill_rejects_on_host(lib):
     assert call(s0h=H_) == 1           # host S0 without a device buffer for it
     assert call(std=A) == 1            # device S_T without a host one
     assert call(T=0) == 1
+
+
+def test_selftest_rejects_limits_on_host(lib):
+    lib.kla_selftest_wait_timeout.argtypes = [ctypes.c_uint, ctypes.c_void_p]
+    assert lib.kla_selftest_wait_timeout(0, None) == 1
+    assert lib.kla_selftest_wait_timeout(100001, None) == 1
