@@ -154,9 +154,25 @@ def chunk_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, alpha: tor
         if t.device.type != "cpu" or not t.is_contiguous():
             raise ValueError(f"{n} must be a contiguous host tensor")
     dcode = _dtype_code(q)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or v.shape[:3] != q.shape[:3]:
+        raise ValueError("q, k must be [B, T, H, d_k] and v [B, T, H, d_v]")
     B, T, H, d_k = q.shape
     d_v = v.shape[-1]
-    gate = _native.KLA_GATE_CHANNEL if alpha.dim() == 4 else _native.KLA_GATE_SCALAR
+    if alpha.dtype != torch.float32 or eta.dtype != torch.float32:
+        raise TypeError("alpha and eta must be float32")
+    if tuple(alpha.shape) == (B, T, H):
+        gate = _native.KLA_GATE_SCALAR
+    elif tuple(alpha.shape) == (B, T, H, d_k):
+        gate = _native.KLA_GATE_CHANNEL
+    else:
+        raise ValueError(f"alpha must be [B,T,H] or [B,T,H,d_k], got {tuple(alpha.shape)}")
+    if tuple(eta.shape) != (B, T, H):
+        raise ValueError("eta must be [B, T, H]")
+    if S0 is not None and (S0.device.type != "cpu" or S0.dtype != torch.float32 or
+                           tuple(S0.shape) != (B, H, d_k, d_v) or not S0.is_contiguous()):
+        raise ValueError("S0 must be a contiguous float32 host tensor [B, H, d_k, d_v]")
     if buffers is None:
         buffers = host_buffers(q, v, alpha, device=dev, with_S0=S0 is not None, with_S_T=final_state or S_T is not None)
     if out is None:
