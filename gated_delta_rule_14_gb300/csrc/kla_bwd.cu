@@ -454,13 +454,21 @@ cudaError_t launch_t(const BwdArgs &a) {
 
 }  // namespace
 
+// The chunkwise tensor-core backward (kla_bwd_chunk.cu): bf16, scalar gate, d_k = d_v = 128.
+bool bwd_chunk_supports(const BwdArgs &a);
+size_t bwd_chunk_workspace_bytes(int B, int T, int H);
+cudaError_t launch_bwd_chunk(const BwdArgs &a);
+
 size_t bwd_workspace_bytes(int B, int T, int H, int d_k, int d_v) {
     if (B < 1 || H < 1 || T < 1) return 0;
     const size_t nblk = (static_cast<size_t>(T) + kBlk - 1) / kBlk;
-    return (static_cast<size_t>(B) * H * nblk * d_k * d_v + static_cast<size_t>(B) * T * H * d_v) * sizeof(float);
+    const size_t seq =
+        (static_cast<size_t>(B) * H * nblk * d_k * d_v + static_cast<size_t>(B) * T * H * d_v) * sizeof(float);
+    return d_k == 128 && d_v == 128 ? std::max(seq, bwd_chunk_workspace_bytes(B, T, H)) : seq;
 }
 
 cudaError_t launch_bwd(const BwdArgs &a) {
+    if (bwd_chunk_supports(a)) return launch_bwd_chunk(a);
     const bool ch = a.gate == KLA_GATE_CHANNEL;
     if (a.dtype == KLA_DTYPE_BF16)
         return ch ? launch_t<__nv_bfloat16, true>(a) : launch_t<__nv_bfloat16, false>(a);

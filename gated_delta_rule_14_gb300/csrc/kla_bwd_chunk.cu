@@ -1,0 +1,986 @@
+// kla_bwd_chunk.cu -- chunkwise backward pass on the tensor cores: bf16 q/k/v/dO, scalar gate,
+// d_k = d_v = 128, chunk C = 64, fp32 gradients.
+//
+// The pages give no backward algebra (GeekNews, "Revisando las variantes de atencion lineal de la
+// familia DeltaNet", section "KDA por chunks", names training as the use of the chunk mode). This
+// differentiates the chunk form of the forward (same page and section; KLA page, section
+// "Implementazione": beta enters only through the chunk solver). Per chunk, with S the state
+// entering it, G the in-chunk inclusive log-decay prefix, gamma = e^G, Gamma = e^{G_end},
+// e_end = e^{G_end - G}, ratio_ij = e^{G_i - G_j}, beta = eta / (||k||^2 + eps) (raw mode: eta):
+//   forward:  R = strict_lower(beta_i ratio_ij k_i.k_j), T = (I + R)^{-1},
+//             W = T diag(beta gamma) K,  U = T diag(beta) V,  E = U - W S,
+//             O = s (diag(gamma) Q S + A E),  A = lower(ratio_ij q_i.k_j),
+//             S' = Gamma S + (diag(e_end) K)^T E.
+//   reverse, with dS' = dL/dS' arriving from the next chunk and dO = dL/dO:
+//             dE  = diag(e_end) K dS' + s A^T dO
+//             dS  = Gamma dS' + s (diag(gamma) Q)^T dO - W^T dE           (to the previous chunk)
+//             dW  = -dE S^T,  dXK = T^T dW,  dXV = T^T dE
+//             dT  = dW K^T diag(beta gamma) + dE V^T diag(beta),  dR = -strict_lower(T^T dT T^T)
+//             dA  = s lower(dO E^T);  dAr = dA . ratio,  dRr = dR . ratio
+//             dq  = s diag(gamma) dO S^T + dAr K
+//             dk  = diag(e_end) E dS'^T + diag(beta gamma) dXK + dAr^T Q + diag(beta) dRr K
+//                   + (diag(beta) dRr)^T K  - 2 beta dbeta / (||k||^2 + eps) k     (KLA only)
+//             dv  = diag(beta) dXV
+//             dbeta_i = gamma_i k_i.dXK_i + v_i.dXV_i + sum_j dRr_ij k_i.k_j;   deta = dbeta / den
+//             dG_i    = gamma_i q_i.dQg_i + beta_i gamma_i k_i.dXK_i + rowsum_i(M) - colsum_i(M)
+//                       + rowsum_i(N) - colsum_i(N) - e_end_i k_i.dKt_i
+//                       (+ sum_j e_end_j k_j.dKt_j + Gamma <S, dS'> for the chunk's last row)
+//             with dQg = s dO S^T, dKt = E dS'^T, M = dAr . (q_i.k_j), N = beta_i dRr . (k_i.k_j);
+//             d log alpha_t = sum over the chunk's rows i >= t of dG_i,  dalpha = that / alpha.
+//
+// Four kernels (one pass over the workspace each way):
+//   bwd_prep_kernel  (chunk-parallel)  gates, [K;Q]K^T, R and A, T by blocked substitution (fp32),
+//                                      W and U; stores G, beta, den, W, U, A and T per chunk;
+//   chunk_scan_kernel<false>           the state carry S_c -> S_{c+1} per chain (fp32 registers),
+//                                      storing S_c and E_c per chunk;
+//   chunk_scan_kernel<true>            the reverse carry dS_{c+1} -> dS_c per chain, storing dS_{c+1}
+//                                      and dE_c per chunk, and dS0;
+//   bwd_grad_kernel  (chunk-parallel)  every gradient of the chunk's tokens from S_c, dS_{c+1},
+//                                      E_c, dE_c, T and the inputs.
+// Every product is a warp-level bf16 mma.sync (m16n8k16, fp32 accumulate) on 64- or 128-wide
+// tiles staged in shared memory with rows padded by 16 bytes, so that every ldmatrix phase hits
+// 8 distinct bank quads. Operands are bf16 (inputs as stored; derived tiles rounded once); the
+// carried states, the solve and every sum of a gradient are fp32.
+#include <algorithm>
+
+#include "kla_internal.cuh"
+
+namespace kla {
+namespace {
+
+constexpr int kC = 64;                  // chunk
+constexpr int kD = 128;                 // d_k = d_v
+constexpr int kP = kD + 8;              // pitch (bf16 elements) of a tile with 128 columns
+constexpr int kPs = kC + 8;             // pitch of a tile with 64 columns
+constexpr int kTileTok = kC * kP * 2;   // 64 x 128 bf16 tile: 17408 bytes
+constexpr int kTileSt = kD * kP * 2;    // 128 x 128: 34816
+constexpr int kTileSq = kC * kPs * 2;   // 64 x 64: 9216
+constexpr float kMinLogGate = -80.0f;
+
+typedef __nv_bfloat16 bf16;
+
+// ---- per-chunk workspace records (structure of arrays over n = chain * nc + chunk)
+constexpr size_t kCgFloats = 3 * kC;    // G, beta, den = ||k||^2 + eps
+struct Ws {
+    float *cg;        // [N][3][64]
+    bf16 *W;          // [N][64][128]
+    bf16 *UdE;        // [N][64][128]: U (prep -> forward carry), then dE (reverse carry -> gradients)
+    bf16 *A;          // [N][64][64]  lower(ratio . QK^T), unscaled by s
+    bf16 *Tm;         // [N][64][64]  T = (I + R)^{-1}
+    bf16 *S;          // [N][128][128] state entering the chunk
+    bf16 *E;          // [N][64][128]
+    bf16 *dS;         // [N][128][128] dL/d(state leaving the chunk)
+};
+size_t ws_bytes_per_chunk() {
+    return kCgFloats * 4 + 2 * (3 * kC * kD + 2 * kC * kC + 2 * kD * kD);
+}
+Ws carve(void *base, size_t N) {
+    char *p = static_cast<char *>(base);
+    Ws w;
+    w.cg = reinterpret_cast<float *>(p);             p += N * kCgFloats * 4;
+    w.W = reinterpret_cast<bf16 *>(p);               p += N * kC * kD * 2;
+    w.UdE = reinterpret_cast<bf16 *>(p);             p += N * kC * kD * 2;
+    w.E = reinterpret_cast<bf16 *>(p);               p += N * kC * kD * 2;
+    w.A = reinterpret_cast<bf16 *>(p);               p += N * kC * kC * 2;
+    w.Tm = reinterpret_cast<bf16 *>(p);              p += N * kC * kC * 2;
+    w.S = reinterpret_cast<bf16 *>(p);               p += N * kD * kD * 2;
+    w.dS = reinterpret_cast<bf16 *>(p);
+    return w;
+}
+
+// ---------------------------------------------------------------- warp-level MMA helpers
+__device__ __forceinline__ uint32_t sptr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm4t(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+                 "{%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Operand fragments of a 16 x 16 (A: rows x k) or 16 x 16 (B: k x two n8 tiles) block of a
+// bf16 tile at shared address `t` with row pitch `pitch` elements. The suffix names how the
+// tile stores the operand: _rk = [row][k] for A or [n][k] for B (no transpose); _kr = [k][row]
+// for A or [k][n] for B (ldmatrix.trans).
+__device__ __forceinline__ void frag_a_rk(uint32_t t, int pitch, int r0, int k0, int lane, uint32_t (&a)[4]) {
+    const int m = lane >> 3;
+    ldsm4(t + 2 * ((r0 + (lane & 7) + (m & 1) * 8) * pitch + k0 + (m >> 1) * 8), a);
+}
+__device__ __forceinline__ void frag_a_kr(uint32_t t, int pitch, int r0, int k0, int lane, uint32_t (&a)[4]) {
+    const int m = lane >> 3;
+    ldsm4t(t + 2 * ((k0 + (lane & 7) + (m >> 1) * 8) * pitch + r0 + (m & 1) * 8), a);
+}
+// b[0], b[1]: n-tile n0; b[2], b[3]: n-tile n0 + 8
+__device__ __forceinline__ void frag_b_rk(uint32_t t, int pitch, int n0, int k0, int lane, uint32_t (&b)[4]) {
+    const int m = lane >> 3;
+    ldsm4(t + 2 * ((n0 + (lane & 7) + (m >> 1) * 8) * pitch + k0 + (m & 1) * 8), b);
+}
+__device__ __forceinline__ void frag_b_kr(uint32_t t, int pitch, int n0, int k0, int lane, uint32_t (&b)[4]) {
+    const int m = lane >> 3;
+    ldsm4t(t + 2 * ((k0 + (lane & 7) + (m & 1) * 8) * pitch + n0 + (m >> 1) * 8), b);
+}
+template <int NT>   // NT n8 tiles (even)
+__device__ __forceinline__ void zero(float (&acc)[NT][4]) {
+#pragma unroll
+    for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+}
+// acc[16 x (8 NT)] += A[r0.., k0..k0+16*KS) * B[.., n0..]: one warp, A and B layouts as template flags.
+template <int NT, int KS, bool kAT, bool kBT>
+__device__ __forceinline__ void gemm(float (&acc)[NT][4], uint32_t ta, int pa, int r0, int ka, uint32_t tb, int pb,
+                                     int n0, int kb, int lane) {
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+        uint32_t a[4];
+        if (kAT) frag_a_kr(ta, pa, r0, ka + 16 * ks, lane, a);
+        else frag_a_rk(ta, pa, r0, ka + 16 * ks, lane, a);
+#pragma unroll
+        for (int j = 0; j < NT / 2; ++j) {
+            uint32_t b[4];
+            if (kBT) frag_b_kr(tb, pb, n0 + 16 * j, kb + 16 * ks, lane, b);
+            else frag_b_rk(tb, pb, n0 + 16 * j, kb + 16 * ks, lane, b);
+            mma(acc[2 * j], a, b[0], b[1]);
+            mma(acc[2 * j + 1], a, b[2], b[3]);
+        }
+    }
+}
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ float2 unpack2(uint32_t u) {
+    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162 *>(&u);
+    return __bfloat1622float2(h);
+}
+__device__ __forceinline__ void st_pair(bf16 *tile, int pitch, int r, int c, float lo, float hi) {
+    *reinterpret_cast<uint32_t *>(tile + r * pitch + c) = pack2(lo, hi);
+}
+__device__ __forceinline__ float2 ld_pair(const bf16 *tile, int pitch, int r, int c) {
+    return unpack2(*reinterpret_cast<const uint32_t *>(tile + r * pitch + c));
+}
+__device__ __forceinline__ void cp16(void *dst, const void *src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sptr(dst)), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// 64 token rows x 128 columns of a [B,T,H,128] bf16 tensor into a padded tile (rows >= L zero).
+__device__ __forceinline__ void load_tok(bf16 *tile, const bf16 *src, size_t row_stride, int L, int tid,
+                                         int nthreads) {
+    for (int i = tid; i < kC * 16; i += nthreads) {
+        const int r = i >> 4, c = (i & 15) * 8;
+        const bool ok = r < L;
+        cp16(tile + r * kP + c, src + (ok ? r : 0) * row_stride + c, ok);
+    }
+}
+// `rows` dense rows of `cols` bf16 (cols = 64 or 128) from the workspace into a padded tile.
+template <int kCols>
+__device__ __forceinline__ void load_dense(bf16 *tile, const bf16 *src, int rows, int tid, int nthreads) {
+    constexpr int kPitch = kCols + 8, kChunks = kCols / 8;
+    for (int i = tid; i < rows * kChunks; i += nthreads) {
+        const int r = i / kChunks, c = (i % kChunks) * 8;
+        cp16(tile + r * kPitch + c, src + r * kCols + c, true);
+    }
+}
+template <int kCols>
+__device__ __forceinline__ void store_dense(bf16 *dst, const bf16 *tile, int rows, int tid, int nthreads) {
+    constexpr int kPitch = kCols + 8, kChunks = kCols / 8;
+    for (int i = tid; i < rows * kChunks; i += nthreads) {
+        const int r = i / kChunks, c = (i % kChunks) * 8;
+        *reinterpret_cast<uint4 *>(dst + r * kCols + c) = *reinterpret_cast<const uint4 *>(tile + r * kPitch + c);
+    }
+}
+
+// ============================================================== kernel 1: per-chunk operands
+struct PrepParams {
+    const bf16 *q, *k, *v;
+    const float *alpha, *eta;
+    float eps;
+    int beta_raw;
+    int B, T, H, nc;
+    Ws ws;
+};
+constexpr int kPrepThreads = 256;
+// shared memory of the prep kernel
+constexpr int PR_K = 0, PR_Q = PR_K + kTileTok, PR_V = PR_Q + kTileTok;
+constexpr int PR_R = PR_V + kTileTok;                 // fp32 [64][65]: R, overwritten by T block by block
+constexpr int PR_TK = PR_R + kC * 65 * 4;             // bf16 T diag(beta gamma)
+constexpr int PR_TV = PR_TK + kTileSq;                // bf16 T diag(beta)
+constexpr int PR_A = PR_TV + kTileSq;                 // bf16 A (then T) staging
+constexpr int PR_X = PR_A + kTileSq;                  // fp32 [32][33] merge scratch
+constexpr int PR_VEC = PR_X + 32 * 33 * 4;            // g, G, beta, n2 (fp32 [4][64])
+constexpr int PR_BYTES = PR_VEC + 4 * kC * 4;
+
+__global__ void __launch_bounds__(kPrepThreads, 2) bwd_prep_kernel(PrepParams p) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    bf16 *sK = reinterpret_cast<bf16 *>(smem + PR_K), *sQ = reinterpret_cast<bf16 *>(smem + PR_Q),
+         *sV = reinterpret_cast<bf16 *>(smem + PR_V);
+    float(*sR)[65] = reinterpret_cast<float(*)[65]>(smem + PR_R);
+    bf16 *sTK = reinterpret_cast<bf16 *>(smem + PR_TK), *sTV = reinterpret_cast<bf16 *>(smem + PR_TV),
+         *sA = reinterpret_cast<bf16 *>(smem + PR_A);
+    float(*sX)[33] = reinterpret_cast<float(*)[33]>(smem + PR_X);
+    float *sg = reinterpret_cast<float *>(smem + PR_VEC), *sG = sg + kC, *sb = sG + kC, *sn = sb + kC;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int c = blockIdx.x, bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
+    const int t0 = c * kC, L = min(kC, p.T - t0);
+    const size_t n = static_cast<size_t>(bh) * p.nc + c;
+    const size_t rs = static_cast<size_t>(p.H) * kD;                      // token row stride
+    const size_t base = (static_cast<size_t>(b) * p.T + t0) * p.H + h;    // (b, t0, h)
+
+    load_tok(sK, p.k + base * kD, rs, L, tid, kPrepThreads);
+    load_tok(sQ, p.q + base * kD, rs, L, tid, kPrepThreads);
+    load_tok(sV, p.v + base * kD, rs, L, tid, kPrepThreads);
+    cp_commit();
+    float eta = 0.f;
+    if (tid < kC) {
+        const bool ok = tid < L;
+        sg[tid] = ok ? fmaxf(logf(p.alpha[base + static_cast<size_t>(tid) * p.H]), kMinLogGate) : 0.f;
+        eta = ok ? p.eta[base + static_cast<size_t>(tid) * p.H] : 0.f;
+    }
+    cp_wait<0>();
+    __syncthreads();
+
+    // ||k_t||^2: warp w takes tokens 8w .. 8w + 7
+    for (int i = 0; i < 8; ++i) {
+        const int t = warp * 8 + i;
+        const float2 x0 = ld_pair(sK, kP, t, 4 * lane), x1 = ld_pair(sK, kP, t, 4 * lane + 2);
+        float s2 = x0.x * x0.x + x0.y * x0.y + x1.x * x1.x + x1.y * x1.y;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+        if (lane == 0) sn[t] = s2;
+    }
+    // inclusive prefix of the log-gates: warp 0, two tokens per lane
+    if (warp == 0) {
+        const float x0 = sg[2 * lane], x1 = sg[2 * lane + 1];
+        float s = x0 + x1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        sG[2 * lane + 1] = s;
+        sG[2 * lane] = s - x1;
+    }
+    __syncthreads();
+    float *cg = p.ws.cg + n * kCgFloats;
+    if (tid < kC) {
+        const float den = sn[tid] + p.eps;
+        const float beta = tid < L ? kla_beta(eta, sn[tid], p.eps, p.beta_raw) : 0.f;
+        sb[tid] = beta;
+        cg[tid] = sG[tid];
+        cg[kC + tid] = beta;
+        cg[2 * kC + tid] = den;
+    }
+    __syncthreads();
+
+    // [K; Q] K^T: warp w owns rows 16 (w & 3) of K K^T (w < 4) or of Q K^T (w >= 4), all 64 columns
+    {
+        float acc[8][4];
+        zero(acc);
+        const int r0 = 16 * (warp & 3);
+        gemm<8, 8, false, false>(acc, sptr(warp < 4 ? sK : sQ), kP, r0, 0, sptr(sK), kP, 0, 0, lane);
+        const int g = lane >> 2, q4 = lane & 3;
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int i = r0 + g + 8 * hh;
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int j = 8 * nt + 2 * q4 + e;
+                    const float ratio = __expf(sG[i] - sG[j]);
+                    const float x = acc[nt][2 * hh + e];
+                    if (warp < 4) sR[i][j] = j < i ? sb[i] * ratio * x : 0.f;
+                    else acc[nt][2 * hh + e] = j <= i ? ratio * x : 0.f;
+                }
+                if (warp >= 4) st_pair(sA, kPs, i, 8 * nt + 2 * q4, acc[nt][2 * hh], acc[nt][2 * hh + 1]);
+            }
+    }
+    __syncthreads();
+    store_dense<kC>(p.ws.A + n * kC * kC, sA, kC, tid, kPrepThreads);
+
+    // T = (I + R)^{-1}, in place over R. (1) the four 16 x 16 diagonal blocks by substitution:
+    // warp 0 lanes 0-15 / 16-31 take blocks 0 / 1, warp 1 blocks 2 / 3; lane = column.
+    if (warp < 2) {
+        const int blk = 2 * warp + (lane >> 4), j = lane & 15, o = 16 * blk;
+        float t[16];
+#pragma unroll
+        for (int m = 0; m < 16; ++m) t[m] = m == j ? 1.f : 0.f;
+#pragma unroll
+        for (int i = 1; i < 16; ++i) {
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int m = 0; m < i; ++m) {
+                if (m & 1) a1 = fmaf(sR[o + i][o + m], t[m], a1);
+                else a0 = fmaf(sR[o + i][o + m], t[m], a0);
+            }
+            if (i > j) t[i] = -(a0 + a1);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int m = 0; m < 16; ++m) sR[o + m][o + j] = t[m];
+    }
+    __syncthreads();
+    // (2) merges: [T11 0; R21 T22]^{-1} has lower block -T22 R21 T11. Size 16 (two merges side by
+    // side), then size 32.
+    for (int hs = 16; hs <= 32; hs *= 2) {
+        const int nm = kC / (2 * hs);            // merges at this size
+        const int per = nm * hs * hs;            // outputs of one product over all merges
+        for (int e = tid; e < per; e += kPrepThreads) {     // X = R21 T11
+            const int mi = e / (hs * hs), r = (e / hs) % hs, cc = e % hs, o = 2 * hs * mi;
+            float s = 0.f;
+            for (int m = cc; m < hs; ++m) s = fmaf(sR[o + hs + r][o + m], sR[o + m][o + cc], s);
+            sX[mi * hs + r][cc] = s;    // hs = 16: rows 0-15 / 16-31 for the two merges
+        }
+        __syncthreads();
+        for (int e = tid; e < per; e += kPrepThreads) {     // T21 = -T22 X
+            const int mi = e / (hs * hs), r = (e / hs) % hs, cc = e % hs, o = 2 * hs * mi;
+            float s = 0.f;
+            for (int m = 0; m <= r; ++m) s = fmaf(sR[o + hs + r][o + hs + m], sX[mi * hs + m][cc], s);
+            sR[o + hs + r][o + cc] = -s;
+        }
+        __syncthreads();
+    }
+    // T diag(beta gamma), T diag(beta) and T as bf16 (the upper triangle is zero)
+    for (int e = tid; e < kC * kC / 2; e += kPrepThreads) {
+        const int i = e / (kC / 2), j = 2 * (e % (kC / 2));
+        const float t0v = j <= i ? sR[i][j] : 0.f, t1v = j + 1 <= i ? sR[i][j + 1] : 0.f;
+        const float b0 = sb[j], b1 = sb[j + 1];
+        st_pair(sTK, kPs, i, j, t0v * b0 * __expf(sG[j]), t1v * b1 * __expf(sG[j + 1]));
+        st_pair(sTV, kPs, i, j, t0v * b0, t1v * b1);
+        st_pair(sA, kPs, i, j, t0v, t1v);
+    }
+    __syncthreads();
+    store_dense<kC>(p.ws.Tm + n * kC * kC, sA, kC, tid, kPrepThreads);
+    // W = T diag(beta gamma) K (warps 0-3) and U = T diag(beta) V (warps 4-7): 16 rows x 128 each
+    float acc[16][4];
+    zero(acc);
+    const int r0 = 16 * (warp & 3);
+    gemm<16, 4, false, true>(acc, sptr(warp < 4 ? sTK : sTV), kPs, r0, 0, sptr(warp < 4 ? sK : sV), kP, 0, 0,
+                             lane);
+    __syncthreads();     // every read of K, Q, V is done: stage W in Q's tile and U in K's
+    {
+        bf16 *st = warp < 4 ? sQ : sK;
+        const int g = lane >> 2, q4 = lane & 3;
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+            st_pair(st, kP, r0 + g, 8 * nt + 2 * q4, acc[nt][0], acc[nt][1]);
+            st_pair(st, kP, r0 + g + 8, 8 * nt + 2 * q4, acc[nt][2], acc[nt][3]);
+        }
+    }
+    __syncthreads();
+    store_dense<kD>(p.ws.W + n * kC * kD, sQ, kC, tid, kPrepThreads);
+    store_dense<kD>(p.ws.UdE + n * kC * kD, sK, kC, tid, kPrepThreads);
+}
+
+// acc[MT m16 tiles][NT n8 tiles] += A * B for MT row tiles at r0, r0 + 16, ... (B fragments shared).
+template <int MT, int NT, int KS, bool kAT, bool kBT>
+__device__ __forceinline__ void gemm_m(float (&acc)[MT][NT][4], uint32_t ta, int pa, int r0, int ka, uint32_t tb,
+                                       int pb, int n0, int kb, int lane) {
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+        uint32_t a[MT][4];
+#pragma unroll
+        for (int mi = 0; mi < MT; ++mi) {
+            if (kAT) frag_a_kr(ta, pa, r0 + 16 * mi, ka + 16 * ks, lane, a[mi]);
+            else frag_a_rk(ta, pa, r0 + 16 * mi, ka + 16 * ks, lane, a[mi]);
+        }
+#pragma unroll
+        for (int j = 0; j < NT / 2; ++j) {
+            uint32_t b[4];
+            if (kBT) frag_b_kr(tb, pb, n0 + 16 * j, kb + 16 * ks, lane, b);
+            else frag_b_rk(tb, pb, n0 + 16 * j, kb + 16 * ks, lane, b);
+#pragma unroll
+            for (int mi = 0; mi < MT; ++mi) {
+                mma(acc[mi][2 * j], a[mi], b[0], b[1]);
+                mma(acc[mi][2 * j + 1], a[mi], b[2], b[3]);
+            }
+        }
+    }
+}
+
+// ============================================================== kernel 2: the carry across chunks
+// Forward (kRev = false), X = S entering chunk c, c ascending:
+//     E = U - W X;  X <- Gamma X + K^T diag(e_end) E            stores X (bf16) and E per chunk
+// Reverse (kRev = true), X = dS' = dL/d(state leaving chunk c), c descending:
+//     dE = diag(e_end) K X + s A^T dO;  X <- Gamma X + (s diag(gamma) Q)^T dO - W^T dE
+//                                                               stores X (bf16) and dE per chunk
+// One CTA of 16 warps per chain; X (128 x 128 fp32) lives in registers, warp w holding rows
+// 32 (w & 3) and columns 32 (w >> 2) of it; the chunk's tiles for step c +- 1 are fetched by
+// cp.async while step c runs.
+struct ScanParams {
+    const bf16 *q, *k, *dO;
+    const float *X0;      // S0 (forward) or dL/dS_T (reverse): [B,H,128,128] fp32, NULL = zeros
+    float *X_end;         // reverse: dL/dS0 (NULL = not wanted)
+    float q_scale;
+    int B, T, H, nc;
+    Ws ws;
+};
+constexpr int kScanThreads = 512;
+constexpr int SC_K = 0, SC_W = SC_K + kTileTok, SC_UQ = SC_W + kTileTok;   // U (forward) or Q (reverse)
+constexpr int SC_DO = SC_UQ + kTileTok, SC_A = SC_DO + kTileTok, SC_CG = SC_A + kTileSq;
+constexpr int SC_STAGE = SC_CG + static_cast<int>(kCgFloats) * 4;
+constexpr int SC_X = 2 * SC_STAGE, SC_M = SC_X + kTileSt;
+constexpr int SC_BYTES = SC_M + kTileTok;
+static_assert(SC_STAGE % 16 == 0 && SC_BYTES <= 232448, "scan shared memory");
+
+template <bool kRev>
+__global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(ScanParams p) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    bf16 *sX = reinterpret_cast<bf16 *>(smem + SC_X), *sM = reinterpret_cast<bf16 *>(smem + SC_M);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, q4 = lane & 3;
+    const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
+    const size_t rs = static_cast<size_t>(p.H) * kD;
+
+    auto stage = [&](int buf, int off) { return reinterpret_cast<bf16 *>(smem + buf * SC_STAGE + off); };
+    auto issue = [&](int c, int buf) {
+        const int t0 = c * kC, L = min(kC, p.T - t0);
+        const size_t base = ((static_cast<size_t>(b) * p.T + t0) * p.H + h) * kD;
+        const size_t n = static_cast<size_t>(bh) * p.nc + c;
+        load_tok(stage(buf, SC_K), p.k + base, rs, L, tid, kScanThreads);
+        load_dense<kD>(stage(buf, SC_W), p.ws.W + n * kC * kD, kC, tid, kScanThreads);
+        if (kRev) {
+            load_tok(stage(buf, SC_UQ), p.q + base, rs, L, tid, kScanThreads);
+            load_tok(stage(buf, SC_DO), p.dO + base, rs, L, tid, kScanThreads);
+            load_dense<kC>(stage(buf, SC_A), p.ws.A + n * kC * kC, kC, tid, kScanThreads);
+        } else {
+            load_dense<kD>(stage(buf, SC_UQ), p.ws.UdE + n * kC * kD, kC, tid, kScanThreads);
+        }
+        if (tid < static_cast<int>(kCgFloats) / 4)
+            cp16(smem + buf * SC_STAGE + SC_CG + 16 * tid, p.ws.cg + n * kCgFloats + 4 * tid, true);
+    };
+
+    // X in registers: rows xr0 + 16 mi + g (+8), columns xc0 + 8 ni + 2 q4 (+1)
+    const int xr0 = 32 * (warp & 3), xc0 = 32 * (warp >> 2);
+    float X[2][4][4];
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+        for (int ni = 0; ni < 4; ++ni)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float2 x = make_float2(0.f, 0.f);
+                if (p.X0)
+                    x = *reinterpret_cast<const float2 *>(p.X0 + (static_cast<size_t>(bh) * kD + xr0 + 16 * mi + g + 8 * hh) * kD +
+                                                          xc0 + 8 * ni + 2 * q4);
+                X[mi][ni][2 * hh] = x.x;
+                X[mi][ni][2 * hh + 1] = x.y;
+            }
+    auto put_x = [&]() {
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+            for (int ni = 0; ni < 4; ++ni)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh)
+                    st_pair(sX, kP, xr0 + 16 * mi + g + 8 * hh, xc0 + 8 * ni + 2 * q4, X[mi][ni][2 * hh],
+                            X[mi][ni][2 * hh + 1]);
+    };
+    put_x();
+    issue(kRev ? p.nc - 1 : 0, 0);
+    cp_commit();
+
+    const int m0 = 16 * (warp & 3), n0 = 32 * (warp >> 2);   // this warp's block of the 64 x 128 step
+    for (int it = 0; it < p.nc; ++it) {
+        const int c = kRev ? p.nc - 1 - it : it, buf = it & 1;
+        const size_t n = static_cast<size_t>(bh) * p.nc + c;
+        cp_wait<0>();
+        __syncthreads();   // chunk c's tiles and X (bf16) are visible; every read of buf ^ 1 is done
+        if (it + 1 < p.nc) issue(kRev ? c - 1 : c + 1, buf ^ 1);
+        cp_commit();
+        const float *cg = reinterpret_cast<const float *>(smem + buf * SC_STAGE + SC_CG);
+        const float Gend = cg[kC - 1], Gam = __expf(Gend);
+        if (kRev) {   // Q <- s diag(gamma) Q, in place (read only by the second product)
+            bf16 *sQ = stage(buf, SC_UQ);
+            for (int i = tid; i < kC * 16; i += kScanThreads) {
+                const int r = i >> 4, cc = (i & 15) * 8;
+                const float f = p.q_scale * __expf(cg[r]);
+                uint4 u = *reinterpret_cast<uint4 *>(sQ + r * kP + cc);
+                uint32_t *w = reinterpret_cast<uint32_t *>(&u);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 x = unpack2(w[e]);
+                    w[e] = pack2(f * x.x, f * x.y);
+                }
+                *reinterpret_cast<uint4 *>(sQ + r * kP + cc) = u;
+            }
+        }
+        store_dense<kD>((kRev ? p.ws.dS : p.ws.S) + n * kD * kD, sX, kD, tid, kScanThreads);
+
+        // the 64 x 128 step: E (forward) or dE (reverse)
+        float acc[1][4][4];
+        zero(acc[0]);
+        gemm_m<1, 4, 8, false, true>(acc, sptr(stage(buf, kRev ? SC_K : SC_W)), kP, m0, 0, sptr(sX), kP, n0, 0, lane);
+        float acc2[1][4][4];
+        if (kRev) {
+            zero(acc2[0]);
+            gemm_m<1, 4, 4, true, true>(acc2, sptr(stage(buf, SC_A)), kPs, m0, 0, sptr(stage(buf, SC_DO)), kP, n0, 0,
+                                        lane);
+        }
+        bf16 *Mout = (kRev ? p.ws.UdE : p.ws.E) + n * kC * kD;
+        const bf16 *sU = stage(buf, SC_UQ);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int r = m0 + g + 8 * hh;
+            const float ee = __expf(Gend - cg[r]);
+#pragma unroll
+            for (int ni = 0; ni < 4; ++ni) {
+                const int col = n0 + 8 * ni + 2 * q4;
+                float m0v, m1v;
+                if (kRev) {
+                    m0v = fmaf(ee, acc[0][ni][2 * hh], p.q_scale * acc2[0][ni][2 * hh]);
+                    m1v = fmaf(ee, acc[0][ni][2 * hh + 1], p.q_scale * acc2[0][ni][2 * hh + 1]);
+                } else {
+                    const float2 u = ld_pair(sU, kP, r, col);
+                    m0v = u.x - acc[0][ni][2 * hh];
+                    m1v = u.y - acc[0][ni][2 * hh + 1];
+                }
+                *reinterpret_cast<uint32_t *>(Mout + r * kD + col) = pack2(m0v, m1v);
+                if (kRev) st_pair(sM, kP, r, col, -m0v, -m1v);
+                else st_pair(sM, kP, r, col, ee * m0v, ee * m1v);
+            }
+        }
+        __syncthreads();   // sM and the scaled Q are visible
+
+        // X <- Gamma X + ...
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+            for (int ni = 0; ni < 4; ++ni)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) X[mi][ni][e] *= Gam;
+        if (kRev) {
+            gemm_m<2, 4, 4, true, true>(X, sptr(stage(buf, SC_UQ)), kP, xr0, 0, sptr(stage(buf, SC_DO)), kP, xc0, 0,
+                                        lane);
+            gemm_m<2, 4, 4, true, true>(X, sptr(stage(buf, SC_W)), kP, xr0, 0, sptr(sM), kP, xc0, 0, lane);
+        } else {
+            gemm_m<2, 4, 4, true, true>(X, sptr(stage(buf, SC_K)), kP, xr0, 0, sptr(sM), kP, xc0, 0, lane);
+        }
+        put_x();   // read by the next step after its barrier (every read of sX in this step is done)
+    }
+    if (kRev && p.X_end) {
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+            for (int ni = 0; ni < 4; ++ni)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh)
+                    *reinterpret_cast<float2 *>(p.X_end + (static_cast<size_t>(bh) * kD + xr0 + 16 * mi + g + 8 * hh) * kD +
+                                                xc0 + 8 * ni + 2 * q4) =
+                        make_float2(X[mi][ni][2 * hh], X[mi][ni][2 * hh + 1]);
+    }
+}
+
+// ============================================================== kernel 3: gradients of a chunk
+struct GradParams {
+    const bf16 *q, *k, *v, *dO;
+    const float *alpha;
+    float q_scale;
+    int beta_raw;
+    float *dq, *dk, *dv, *dalpha, *deta;
+    int B, T, H, nc;
+    Ws ws;
+};
+constexpr int kGradThreads = 512;
+enum { RQ_KT = 0, RQ_Q, RQ_B1, RQ_B2, RQ_B3, RQ_MA, kRowQty };   // per-row partial sums
+enum { CQ_MA = 0, CQ_MR, kColQty };                             // per-column partial sums
+constexpr int GR_Q = 0, GR_K = GR_Q + kTileTok, GR_V = GR_K + kTileTok, GR_DO = GR_V + kTileTok;
+constexpr int GR_E = GR_DO + kTileTok, GR_DE = GR_E + kTileTok;
+constexpr int GR_S = GR_DE + kTileTok, GR_DS = GR_S + kTileSt;     // S_c, dS_{c+1}; later reused:
+constexpr int GR_DW = GR_S, GR_DT = GR_DW + kTileTok, GR_Y = GR_DT + kTileSq, GR_DAR = GR_Y + kTileSq;
+constexpr int GR_DRR = GR_DAR + kTileSq, GR_BDRR = GR_DRR + kTileSq;
+static_assert(GR_BDRR + kTileSq <= GR_DS + kTileSt, "reused area");
+constexpr int GR_T = GR_DS + kTileSt, GR_CG = GR_T + kTileSq;
+constexpr int GR_RROW = GR_CG + static_cast<int>(kCgFloats) * 4;   // fp32 [kRowQty][4][64]
+constexpr int GR_RCOL = GR_RROW + kRowQty * 4 * kC * 4;            // fp32 [kColQty][4][64]
+constexpr int GR_SC = GR_RCOL + kColQty * 4 * kC * 4;              // fp32 [16] block partials of <S, dS'>
+constexpr int GR_KC = GR_SC + 16 * 4;                              // fp32 [64] coefficient of k in dk
+constexpr int GR_XS = GR_KC + kC * 4;                              // fp32 [4] scratch of warps 0-1
+constexpr int GR_BYTES = GR_XS + 16;
+static_assert(GR_BYTES <= 232448, "gradient kernel shared memory");
+
+__global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_kernel(GradParams p) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    auto tile = [&](int off) { return reinterpret_cast<bf16 *>(smem + off); };
+    bf16 *sQ = tile(GR_Q), *sK = tile(GR_K), *sV = tile(GR_V), *sDO = tile(GR_DO), *sE = tile(GR_E),
+         *sDE = tile(GR_DE), *sS = tile(GR_S), *sDS = tile(GR_DS), *sT = tile(GR_T);
+    const float *cg = reinterpret_cast<const float *>(smem + GR_CG);
+    float(*rrow)[4][kC] = reinterpret_cast<float(*)[4][kC]>(smem + GR_RROW);
+    float(*rcol)[4][kC] = reinterpret_cast<float(*)[4][kC]>(smem + GR_RCOL);
+    float *rsc = reinterpret_cast<float *>(smem + GR_SC), *kcoef = reinterpret_cast<float *>(smem + GR_KC),
+          *xs = reinterpret_cast<float *>(smem + GR_XS);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, q4 = lane & 3;
+    const int c = blockIdx.x, bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
+    const int t0 = c * kC, L = min(kC, p.T - t0);
+    const size_t n = static_cast<size_t>(bh) * p.nc + c;
+    const size_t rs = static_cast<size_t>(p.H) * kD;
+    const size_t tok0 = (static_cast<size_t>(b) * p.T + t0) * p.H + h;   // (b, t0, h)
+
+    load_tok(sQ, p.q + tok0 * kD, rs, L, tid, kGradThreads);
+    load_tok(sK, p.k + tok0 * kD, rs, L, tid, kGradThreads);
+    load_tok(sV, p.v + tok0 * kD, rs, L, tid, kGradThreads);
+    load_tok(sDO, p.dO + tok0 * kD, rs, L, tid, kGradThreads);
+    load_dense<kD>(sE, p.ws.E + n * kC * kD, kC, tid, kGradThreads);
+    load_dense<kD>(sDE, p.ws.UdE + n * kC * kD, kC, tid, kGradThreads);
+    load_dense<kD>(sS, p.ws.S + n * kD * kD, kD, tid, kGradThreads);
+    load_dense<kD>(sDS, p.ws.dS + n * kD * kD, kD, tid, kGradThreads);
+    load_dense<kC>(sT, p.ws.Tm + n * kC * kC, kC, tid, kGradThreads);
+    if (tid < static_cast<int>(kCgFloats) / 4)
+        cp16(smem + GR_CG + 16 * tid, p.ws.cg + n * kCgFloats + 4 * tid, true);
+    cp_commit();
+    cp_wait<0>();
+    __syncthreads();
+
+    const int wr = warp & 3, wc = warp >> 2, m0 = 16 * wr, n0 = 32 * wc, n0s = 16 * wc;
+    const float s = p.q_scale, Gend = cg[kC - 1];
+    int rr[2];
+    float gam[2], eend[2], bet[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        rr[hh] = m0 + g + 8 * hh;
+        gam[hh] = __expf(cg[rr[hh]]);
+        eend[hh] = __expf(Gend - cg[rr[hh]]);
+        bet[hh] = cg[kC + rr[hh]];
+    }
+    float rowp[kRowQty][2] = {};
+    float colp[kColQty][2][2] = {};
+    // sum over this thread's columns of X[r][col] * acc (X a bf16 tile with 128 columns)
+    auto rowdot = [&](const bf16 *X, const float (&a)[4][4], int hh) {
+        float sum = 0.f;
+#pragma unroll
+        for (int ni = 0; ni < 4; ++ni) {
+            const float2 x = ld_pair(X, kP, rr[hh], n0 + 8 * ni + 2 * q4);
+            sum = fmaf(x.x, a[ni][2 * hh], fmaf(x.y, a[ni][2 * hh + 1], sum));
+        }
+        return sum;
+    };
+
+    // <S, dS'>
+    {
+        float sum = 0.f;
+        for (int i = tid; i < kD * 16; i += kGradThreads) {
+            const int r = i >> 4, cc = (i & 15) * 8;
+            const uint4 a = *reinterpret_cast<const uint4 *>(sS + r * kP + cc);
+            const uint4 d = *reinterpret_cast<const uint4 *>(sDS + r * kP + cc);
+            const uint32_t *aw = reinterpret_cast<const uint32_t *>(&a), *dw = reinterpret_cast<const uint32_t *>(&d);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 x = unpack2(aw[e]), y = unpack2(dw[e]);
+                sum = fmaf(x.x, y.x, fmaf(x.y, y.y, sum));
+            }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (lane == 0) rsc[warp] = sum;
+    }
+
+    float dQ[1][4][4], dK[1][4][4], acc[1][4][4];
+    // dKt = E dS'^T -> dk += e_end dKt
+    zero(acc[0]);
+    gemm_m<1, 4, 8, false, false>(acc, sptr(sE), kP, m0, 0, sptr(sDS), kP, n0, 0, lane);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        rowp[RQ_KT][hh] = rowdot(sK, acc[0], hh);
+#pragma unroll
+        for (int ni = 0; ni < 4; ++ni) {
+            dK[0][ni][2 * hh] = eend[hh] * acc[0][ni][2 * hh];
+            dK[0][ni][2 * hh + 1] = eend[hh] * acc[0][ni][2 * hh + 1];
+        }
+    }
+    // dQg = s dO S^T -> dq = gamma dQg
+    zero(acc[0]);
+    gemm_m<1, 4, 8, false, false>(acc, sptr(sDO), kP, m0, 0, sptr(sS), kP, n0, 0, lane);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        rowp[RQ_Q][hh] = s * rowdot(sQ, acc[0], hh);
+#pragma unroll
+        for (int ni = 0; ni < 4; ++ni) {
+            dQ[0][ni][2 * hh] = s * gam[hh] * acc[0][ni][2 * hh];
+            dQ[0][ni][2 * hh + 1] = s * gam[hh] * acc[0][ni][2 * hh + 1];
+        }
+    }
+    // dW = -dE S^T (staged as bf16 once S and dS' are no longer read)
+    zero(acc[0]);
+    gemm_m<1, 4, 8, false, false>(acc, sptr(sDE), kP, m0, 0, sptr(sS), kP, n0, 0, lane);
+    __syncthreads();
+    bf16 *sDW = tile(GR_DW), *sDT = tile(GR_DT), *sY = tile(GR_Y), *sDAR = tile(GR_DAR), *sDRR = tile(GR_DRR),
+         *sBDRR = tile(GR_BDRR);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+        for (int ni = 0; ni < 4; ++ni)
+            st_pair(sDW, kP, rr[hh], n0 + 8 * ni + 2 * q4, -acc[0][ni][2 * hh], -acc[0][ni][2 * hh + 1]);
+    __syncthreads();
+
+    // dXK = T^T dW -> dk += beta gamma dXK
+    zero(acc[0]);
+    gemm_m<1, 4, 4, true, true>(acc, sptr(sT), kPs, m0, 0, sptr(sDW), kP, n0, 0, lane);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        rowp[RQ_B1][hh] = rowdot(sK, acc[0], hh);
+        const float f = bet[hh] * gam[hh];
+#pragma unroll
+        for (int ni = 0; ni < 4; ++ni) {
+            dK[0][ni][2 * hh] = fmaf(f, acc[0][ni][2 * hh], dK[0][ni][2 * hh]);
+            dK[0][ni][2 * hh + 1] = fmaf(f, acc[0][ni][2 * hh + 1], dK[0][ni][2 * hh + 1]);
+        }
+    }
+    // dXV = T^T dE -> dv = beta dXV
+    zero(acc[0]);
+    gemm_m<1, 4, 4, true, true>(acc, sptr(sT), kPs, m0, 0, sptr(sDE), kP, n0, 0, lane);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        rowp[RQ_B2][hh] = rowdot(sV, acc[0], hh);
+        if (rr[hh] < L) {
+            float *dst = p.dv + (tok0 + static_cast<size_t>(rr[hh]) * p.H) * kD;
+#pragma unroll
+            for (int ni = 0; ni < 4; ++ni)
+                *reinterpret_cast<float2 *>(dst + n0 + 8 * ni + 2 * q4) =
+                    make_float2(bet[hh] * acc[0][ni][2 * hh], bet[hh] * acc[0][ni][2 * hh + 1]);
+        }
+    }
+    // dT = dW K^T diag(beta gamma) + dE V^T diag(beta)
+    {
+        float a1[1][2][4], a2[1][2][4];
+        zero(a1[0]);
+        zero(a2[0]);
+        gemm_m<1, 2, 8, false, false>(a1, sptr(sDW), kP, m0, 0, sptr(sK), kP, n0s, 0, lane);
+        gemm_m<1, 2, 8, false, false>(a2, sptr(sDE), kP, m0, 0, sptr(sV), kP, n0s, 0, lane);
+#pragma unroll
+        for (int ni = 0; ni < 2; ++ni) {
+            const int j = n0s + 8 * ni + 2 * q4;
+            const float bj0 = cg[kC + j], bj1 = cg[kC + j + 1];
+            const float fj0 = bj0 * __expf(cg[j]), fj1 = bj1 * __expf(cg[j + 1]);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+                st_pair(sDT, kPs, rr[hh], j, fmaf(fj0, a1[0][ni][2 * hh], bj0 * a2[0][ni][2 * hh]),
+                        fmaf(fj1, a1[0][ni][2 * hh + 1], bj1 * a2[0][ni][2 * hh + 1]));
+        }
+    }
+    // dA = s lower(dO E^T), dAr = dA . ratio; M = dAr . QK^T
+    {
+        float qk[1][2][4], da[1][2][4];
+        zero(qk[0]);
+        zero(da[0]);
+        gemm_m<1, 2, 8, false, false>(qk, sptr(sQ), kP, m0, 0, sptr(sK), kP, n0s, 0, lane);
+        gemm_m<1, 2, 8, false, false>(da, sptr(sDO), kP, m0, 0, sptr(sE), kP, n0s, 0, lane);
+#pragma unroll
+        for (int ni = 0; ni < 2; ++ni)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int i = rr[hh];
+                float v2[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int j = n0s + 8 * ni + 2 * q4 + e;
+                    const float x = j <= i ? s * da[0][ni][2 * hh + e] * __expf(cg[i] - cg[j]) : 0.f;
+                    v2[e] = x;
+                    const float m = x * qk[0][ni][2 * hh + e];
+                    rowp[RQ_MA][hh] += m;
+                    colp[CQ_MA][ni][e] += m;
+                }
+                st_pair(sDAR, kPs, i, n0s + 8 * ni + 2 * q4, v2[0], v2[1]);
+            }
+    }
+    __syncthreads();   // dT and dAr are visible
+
+    // Y = T^T dT
+    {
+        float y[1][2][4];
+        zero(y[0]);
+        gemm_m<1, 2, 4, true, true>(y, sptr(sT), kPs, m0, 0, sptr(sDT), kPs, n0s, 0, lane);
+#pragma unroll
+        for (int ni = 0; ni < 2; ++ni)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+                st_pair(sY, kPs, rr[hh], n0s + 8 * ni + 2 * q4, y[0][ni][2 * hh], y[0][ni][2 * hh + 1]);
+    }
+    // dq += dAr K;  dk += dAr^T Q
+    gemm_m<1, 4, 4, false, true>(dQ, sptr(sDAR), kPs, m0, 0, sptr(sK), kP, n0, 0, lane);
+    gemm_m<1, 4, 4, true, true>(dK, sptr(sDAR), kPs, m0, 0, sptr(sQ), kP, n0, 0, lane);
+    __syncthreads();   // Y is visible
+
+    // dR = -strict_lower(Y T^T), dRr = dR . ratio; N = beta_i dRr . KK^T
+    {
+        float kk[1][2][4], dr[1][2][4];
+        zero(kk[0]);
+        zero(dr[0]);
+        gemm_m<1, 2, 8, false, false>(kk, sptr(sK), kP, m0, 0, sptr(sK), kP, n0s, 0, lane);
+        gemm_m<1, 2, 4, false, false>(dr, sptr(sY), kPs, m0, 0, sptr(sT), kPs, n0s, 0, lane);
+#pragma unroll
+        for (int ni = 0; ni < 2; ++ni)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int i = rr[hh];
+                float v2[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int j = n0s + 8 * ni + 2 * q4 + e;
+                    const float x = j < i ? -dr[0][ni][2 * hh + e] * __expf(cg[i] - cg[j]) : 0.f;
+                    v2[e] = x;
+                    const float m = x * kk[0][ni][2 * hh + e];
+                    rowp[RQ_B3][hh] += m;
+                    colp[CQ_MR][ni][e] += bet[hh] * m;
+                }
+                st_pair(sDRR, kPs, i, n0s + 8 * ni + 2 * q4, v2[0], v2[1]);
+                st_pair(sBDRR, kPs, i, n0s + 8 * ni + 2 * q4, bet[hh] * v2[0], bet[hh] * v2[1]);
+            }
+    }
+    // row partials: over the 4 lanes of a row, then one slot per column block of warps
+#pragma unroll
+    for (int qi = 0; qi < kRowQty; ++qi)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            float x = rowp[qi][hh];
+            x += __shfl_xor_sync(0xffffffffu, x, 1);
+            x += __shfl_xor_sync(0xffffffffu, x, 2);
+            if (q4 == 0) rrow[qi][wc][rr[hh]] = x;
+        }
+    // column partials: over the 8 row groups of the warp, then one slot per row block of warps
+#pragma unroll
+    for (int qi = 0; qi < kColQty; ++qi)
+#pragma unroll
+        for (int ni = 0; ni < 2; ++ni)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float x = colp[qi][ni][e];
+                x += __shfl_xor_sync(0xffffffffu, x, 4);
+                x += __shfl_xor_sync(0xffffffffu, x, 8);
+                x += __shfl_xor_sync(0xffffffffu, x, 16);
+                if (g == 0) rcol[qi][wr][n0s + 8 * ni + 2 * q4 + e] = x;
+            }
+    __syncthreads();   // dRr, beta dRr and the partial sums are visible
+
+    // dk += beta dRr K + (beta dRr)^T K
+    zero(acc[0]);
+    gemm_m<1, 4, 4, false, true>(acc, sptr(sDRR), kPs, m0, 0, sptr(sK), kP, n0, 0, lane);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+        for (int ni = 0; ni < 4; ++ni) {
+            dK[0][ni][2 * hh] = fmaf(bet[hh], acc[0][ni][2 * hh], dK[0][ni][2 * hh]);
+            dK[0][ni][2 * hh + 1] = fmaf(bet[hh], acc[0][ni][2 * hh + 1], dK[0][ni][2 * hh + 1]);
+        }
+    gemm_m<1, 4, 4, true, true>(dK, sptr(sBDRR), kPs, m0, 0, sptr(sK), kP, n0, 0, lane);
+
+    // per token: dbeta, deta, the k coefficient, dG and its reverse prefix (warps 0-1, token = tid)
+    if (tid < kC) {
+        const int t = tid;
+        float red[kRowQty];
+#pragma unroll
+        for (int qi = 0; qi < kRowQty; ++qi) red[qi] = rrow[qi][0][t] + rrow[qi][1][t] + rrow[qi][2][t] + rrow[qi][3][t];
+        const float cma = rcol[CQ_MA][0][t] + rcol[CQ_MA][1][t] + rcol[CQ_MA][2][t] + rcol[CQ_MA][3][t];
+        const float cmr = rcol[CQ_MR][0][t] + rcol[CQ_MR][1][t] + rcol[CQ_MR][2][t] + rcol[CQ_MR][3][t];
+        const float gt = __expf(cg[t]), et = __expf(Gend - cg[t]), bt = cg[kC + t], den = cg[2 * kC + t];
+        const float dbeta = fmaf(gt, red[RQ_B1], red[RQ_B2] + red[RQ_B3]);
+        float deta = dbeta, kc = 0.f;
+        if (!p.beta_raw) {
+            const bool flows = den != 0.f;
+            deta = flows ? dbeta / den : 0.f;
+            kc = flows ? -2.f * bt * dbeta / den : 0.f;
+        }
+        kcoef[t] = kc;
+        const float kt = et * red[RQ_KT];
+        float dG = gt * red[RQ_Q] + bt * gt * red[RQ_B1] + red[RQ_MA] - cma + bt * red[RQ_B3] - cmr - kt;
+        // the chunk's last row also carries the end decay's terms: sum_j e_end_j k_j.dKt_j + Gamma <S, dS'>
+        float ktot = kt;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) ktot += __shfl_xor_sync(0xffffffffu, ktot, o);
+        if (lane == 0) xs[warp] = ktot;
+        asm volatile("bar.sync 1, 64;" ::: "memory");   // warps 0-1 only
+        if (t == kC - 1) {
+            float sds = 0.f;
+#pragma unroll
+            for (int w = 0; w < 16; ++w) sds += rsc[w];
+            dG += xs[0] + xs[1] + __expf(Gend) * sds;
+        }
+        // reverse inclusive prefix over the 64 tokens: suffix sums within each warp, then warp 0
+        // adds warp 1's total
+        float x = dG;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_down_sync(0xffffffffu, x, o);
+            if (lane + o < 32) x += y;
+        }
+        if (t == 32) xs[2] = x;
+        asm volatile("bar.sync 1, 64;" ::: "memory");
+        if (t < 32) x += xs[2];
+        if (t < L) {
+            const size_t o = tok0 + static_cast<size_t>(t) * p.H;
+            p.deta[o] = deta;
+            p.dalpha[o] = x / p.alpha[o];
+        }
+    }
+    __syncthreads();   // kcoef is visible
+
+    // dk += kcoef k; write dq and dk
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        if (rr[hh] >= L) continue;
+        const float kc = kcoef[rr[hh]];
+        float *dqr = p.dq + (tok0 + static_cast<size_t>(rr[hh]) * p.H) * kD;
+        float *dkr = p.dk + (tok0 + static_cast<size_t>(rr[hh]) * p.H) * kD;
+#pragma unroll
+        for (int ni = 0; ni < 4; ++ni) {
+            const int col = n0 + 8 * ni + 2 * q4;
+            const float2 kx = ld_pair(sK, kP, rr[hh], col);
+            *reinterpret_cast<float2 *>(dqr + col) = make_float2(dQ[0][ni][2 * hh], dQ[0][ni][2 * hh + 1]);
+            *reinterpret_cast<float2 *>(dkr + col) =
+                make_float2(fmaf(kc, kx.x, dK[0][ni][2 * hh]), fmaf(kc, kx.y, dK[0][ni][2 * hh + 1]));
+        }
+    }
+}
+
+}  // namespace
+
+size_t bwd_chunk_workspace_bytes(int B, int T, int H) {
+    if (B < 1 || T < 1 || H < 1) return 0;
+    const size_t nc = (static_cast<size_t>(T) + kC - 1) / kC;
+    return static_cast<size_t>(B) * H * nc * ws_bytes_per_chunk();
+}
+
+// Sequences of at most kShortSeqMaxT tokens take the token-by-token fp32 backward: there a
+// gradient can hinge on a handful of dot products taken after a bf16 rounding, with nothing to
+// average the rounding over, and the sequential walk is short.
+bool bwd_chunk_supports(const BwdArgs &a) {
+    auto al16 = [](const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; };
+    return a.dtype == KLA_DTYPE_BF16 && a.gate == KLA_GATE_SCALAR && a.d_k == kD && a.d_v == kD && a.T > kShortSeqMaxT &&
+           static_cast<long long>(a.B) * a.H <= 65535 && al16(a.q) && al16(a.k) && al16(a.v) && al16(a.dO) &&
+           al16(a.workspace) && a.workspace_bytes >= bwd_chunk_workspace_bytes(a.B, a.T, a.H);
+}
+
+cudaError_t launch_bwd_chunk(const BwdArgs &a) {
+    const int nc = (a.T + kC - 1) / kC, chains = a.B * a.H;
+    const Ws ws = carve(a.workspace, static_cast<size_t>(chains) * nc);
+    const bf16 *q = static_cast<const bf16 *>(a.q), *k = static_cast<const bf16 *>(a.k),
+               *v = static_cast<const bf16 *>(a.v), *dO = static_cast<const bf16 *>(a.dO);
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(bwd_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PR_BYTES)) ||
+        (e = cudaFuncSetAttribute(chunk_scan_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SC_BYTES)) ||
+        (e = cudaFuncSetAttribute(chunk_scan_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SC_BYTES)) ||
+        (e = cudaFuncSetAttribute(bwd_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, GR_BYTES)))
+        return e;
+    PrepParams pp{q, k, v, a.alpha, a.eta, a.eps, a.beta_raw, a.B, a.T, a.H, nc, ws};
+    bwd_prep_kernel<<<dim3(nc, chains), kPrepThreads, PR_BYTES, a.stream>>>(pp);
+    ScanParams sf{q, k, dO, a.S0, nullptr, a.q_scale, a.B, a.T, a.H, nc, ws};
+    chunk_scan_kernel<false><<<chains, kScanThreads, SC_BYTES, a.stream>>>(sf);
+    ScanParams sr{q, k, dO, a.dS_T, a.dS0, a.q_scale, a.B, a.T, a.H, nc, ws};
+    chunk_scan_kernel<true><<<chains, kScanThreads, SC_BYTES, a.stream>>>(sr);
+    GradParams gp{q, k, v, dO, a.alpha, a.q_scale, a.beta_raw, a.dq, a.dk, a.dv, a.dalpha, a.deta, a.B, a.T, a.H, nc, ws};
+    bwd_grad_kernel<<<dim3(nc, chains), kGradThreads, GR_BYTES, a.stream>>>(gp);
+    return cudaGetLastError();
+}
+
+}  // namespace kla
