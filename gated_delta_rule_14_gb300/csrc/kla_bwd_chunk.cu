@@ -106,6 +106,32 @@ __device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4], uint3
                  : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+__device__ __forceinline__ uint32_t tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+                 "{%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// One 16 x 8 tile of A B in fp32 shared memory (tf32 operands, fp32 accumulate): A rows
+// [ar, ar+16) x columns [ac, ac+8*KS) of a matrix with pitch pa; B rows [br, br+8*KS) x columns
+// [bc, bc+8) with pitch pb.
+template <int KS>
+__device__ __forceinline__ void tile_tf32(float (&acc)[4], const float *A, int pa, int ar, int ac, const float *Bm,
+                                          int pb, int br, int bc, int lane) {
+    const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+        const float *a0 = A + (ar + g) * pa + ac + 8 * ks + q;
+        const uint32_t a[4] = {tf32(a0[0]), tf32(a0[8 * pa]), tf32(a0[4]), tf32(a0[8 * pa + 4])};
+        const float *b0 = Bm + (br + 8 * ks + q) * pb + bc + g;
+        mma_tf32(acc, a, tf32(b0[0]), tf32(b0[4 * pb]));
+    }
+}
 // Operand fragments of a 16 x 16 (A: rows x k) or 16 x 16 (B: k x two n8 tiles) block of a
 // bf16 tile at shared address `t` with row pitch `pitch` elements. The suffix names how the
 // tile stores the operand: _rk = [row][k] for A or [n][k] for B (no transpose); _kr = [k][row]
@@ -169,6 +195,9 @@ __device__ __forceinline__ void cp16(void *dst, const void *src, bool valid) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sptr(dst)), "l"(src), "r"(valid ? 16 : 0)
                  : "memory");
 }
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {   // 16-byte aligned, multiple of 16
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
@@ -212,29 +241,31 @@ struct PrepParams {
 constexpr int kPrepThreads = 256;
 // shared memory of the prep kernel
 constexpr int PR_K = 0, PR_Q = PR_K + kTileTok, PR_V = PR_Q + kTileTok;
-constexpr int PR_R = PR_V + kTileTok;                 // fp32 [64][65]: R, overwritten by T block by block
-constexpr int PR_TK = PR_R + kC * 65 * 4;             // bf16 T diag(beta gamma)
+constexpr int kPR = 68;                               // pitch of the fp32 64 x 64 tile (4 mod 32: no conflicts)
+constexpr int PR_R = PR_V + kTileTok;                 // fp32 [64][68]: R, overwritten by T block by block
+constexpr int PR_TK = PR_R + kC * kPR * 4;            // bf16 T diag(beta gamma)
 constexpr int PR_TV = PR_TK + kTileSq;                // bf16 T diag(beta)
 constexpr int PR_A = PR_TV + kTileSq;                 // bf16 A (then T) staging
-constexpr int PR_X = PR_A + kTileSq;                  // fp32 [32][33] merge scratch
-constexpr int PR_VEC = PR_X + 32 * 33 * 4;            // g, G, beta, n2 (fp32 [4][64])
-constexpr int PR_BYTES = PR_VEC + 4 * kC * 4;
+constexpr int kPX = 36;
+constexpr int PR_X = PR_A + kTileSq;                  // fp32 [32][36] merge scratch
+constexpr int PR_VEC = PR_X + 32 * kPX * 4;           // g, G, beta, n2, beta e^G (fp32 [5][64])
+constexpr int PR_BYTES = PR_VEC + 5 * kC * 4;
 
 __global__ void __launch_bounds__(kPrepThreads, 2) bwd_prep_kernel(PrepParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
     bf16 *sK = reinterpret_cast<bf16 *>(smem + PR_K), *sQ = reinterpret_cast<bf16 *>(smem + PR_Q),
          *sV = reinterpret_cast<bf16 *>(smem + PR_V);
-    float(*sR)[65] = reinterpret_cast<float(*)[65]>(smem + PR_R);
+    float(*sR)[kPR] = reinterpret_cast<float(*)[kPR]>(smem + PR_R);
     bf16 *sTK = reinterpret_cast<bf16 *>(smem + PR_TK), *sTV = reinterpret_cast<bf16 *>(smem + PR_TV),
          *sA = reinterpret_cast<bf16 *>(smem + PR_A);
-    float(*sX)[33] = reinterpret_cast<float(*)[33]>(smem + PR_X);
-    float *sg = reinterpret_cast<float *>(smem + PR_VEC), *sG = sg + kC, *sb = sG + kC, *sn = sb + kC;
+    float *sX = reinterpret_cast<float *>(smem + PR_X);
+    float *sg = reinterpret_cast<float *>(smem + PR_VEC), *sG = sg + kC, *sb = sG + kC, *sn = sb + kC, *sgb = sn + kC;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const size_t rs = static_cast<size_t>(p.H) * kD;                      // token row stride
     const int c = blockIdx.x, bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
     const int t0 = c * kC, L = min(kC, p.T - t0);
     const size_t n = static_cast<size_t>(bh) * p.nc + c;
-    const size_t rs = static_cast<size_t>(p.H) * kD;                      // token row stride
     const size_t base = (static_cast<size_t>(b) * p.T + t0) * p.H + h;    // (b, t0, h)
 
     load_tok(sK, p.k + base * kD, rs, L, tid, kPrepThreads);
@@ -249,7 +280,6 @@ __global__ void __launch_bounds__(kPrepThreads, 2) bwd_prep_kernel(PrepParams p)
     }
     cp_wait<0>();
     __syncthreads();
-
     // ||k_t||^2: warp w takes tokens 8w .. 8w + 7
     for (int i = 0; i < 8; ++i) {
         const int t = warp * 8 + i;
@@ -277,6 +307,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) bwd_prep_kernel(PrepParams p)
         const float den = sn[tid] + p.eps;
         const float beta = tid < L ? kla_beta(eta, sn[tid], p.eps, p.beta_raw) : 0.f;
         sb[tid] = beta;
+        sgb[tid] = beta * __expf(sG[tid]);
         cg[tid] = sG[tid];
         cg[kC + tid] = beta;
         cg[2 * kC + tid] = den;
@@ -331,33 +362,52 @@ __global__ void __launch_bounds__(kPrepThreads, 2) bwd_prep_kernel(PrepParams p)
         for (int m = 0; m < 16; ++m) sR[o + m][o + j] = t[m];
     }
     __syncthreads();
-    // (2) merges: [T11 0; R21 T22]^{-1} has lower block -T22 R21 T11. Size 16 (two merges side by
-    // side), then size 32.
-    for (int hs = 16; hs <= 32; hs *= 2) {
-        const int nm = kC / (2 * hs);            // merges at this size
-        const int per = nm * hs * hs;            // outputs of one product over all merges
-        for (int e = tid; e < per; e += kPrepThreads) {     // X = R21 T11
-            const int mi = e / (hs * hs), r = (e / hs) % hs, cc = e % hs, o = 2 * hs * mi;
-            float s = 0.f;
-            for (int m = cc; m < hs; ++m) s = fmaf(sR[o + hs + r][o + m], sR[o + m][o + cc], s);
-            sX[mi * hs + r][cc] = s;    // hs = 16: rows 0-15 / 16-31 for the two merges
-        }
-        __syncthreads();
-        for (int e = tid; e < per; e += kPrepThreads) {     // T21 = -T22 X
-            const int mi = e / (hs * hs), r = (e / hs) % hs, cc = e % hs, o = 2 * hs * mi;
-            float s = 0.f;
-            for (int m = 0; m <= r; ++m) s = fmaf(sR[o + hs + r][o + hs + m], sX[mi * hs + m][cc], s);
-            sR[o + hs + r][o + cc] = -s;
-        }
-        __syncthreads();
+    // (2) merges: [T11 0; R21 T22]^{-1} has lower block -T22 R21 T11, on tf32 warp MMAs.
+    // Size 16: two merges side by side (blocks at 0 and 32), warp w < 4 takes merge w >> 1 and
+    // output columns 8 (w & 1); size 32: warp w takes output rows 16 (w >> 2), columns 8 (w & 3).
+    const float *R0 = &sR[0][0];
+    float *R0w = &sR[0][0];
+    const int g = lane >> 2, q4 = lane & 3;
+    auto put_tile = [&](float *M, int pitch, int r, int cc, const float (&acc)[4], float sign) {
+        M[(r + g) * pitch + cc + 2 * q4] = sign * acc[0];
+        M[(r + g) * pitch + cc + 2 * q4 + 1] = sign * acc[1];
+        M[(r + g + 8) * pitch + cc + 2 * q4] = sign * acc[2];
+        M[(r + g + 8) * pitch + cc + 2 * q4 + 1] = sign * acc[3];
+    };
+    if (warp < 4) {   // X = R21 T11
+        const int o = 32 * (warp >> 1), nc8 = 8 * (warp & 1);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        tile_tf32<2>(acc, R0, kPR, o + 16, o, R0, kPR, o, o + nc8, lane);
+        put_tile(sX, kPX, 16 * (warp >> 1), nc8, acc, 1.f);
     }
+    __syncthreads();
+    if (warp < 4) {   // T21 = -T22 X
+        const int o = 32 * (warp >> 1), nc8 = 8 * (warp & 1);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        tile_tf32<2>(acc, R0, kPR, o + 16, o + 16, sX, kPX, 16 * (warp >> 1), nc8, lane);
+        put_tile(R0w, kPR, o + 16, o + nc8, acc, -1.f);
+    }
+    __syncthreads();
+    {   // X = R21 T11 at size 32
+        const int mr = 16 * (warp >> 2), nc8 = 8 * (warp & 3);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        tile_tf32<4>(acc, R0, kPR, 32 + mr, 0, R0, kPR, 0, nc8, lane);
+        put_tile(sX, kPX, mr, nc8, acc, 1.f);
+    }
+    __syncthreads();
+    {   // T21 = -T22 X
+        const int mr = 16 * (warp >> 2), nc8 = 8 * (warp & 3);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        tile_tf32<4>(acc, R0, kPR, 32 + mr, 32, sX, kPX, 0, nc8, lane);
+        put_tile(R0w, kPR, 32 + mr, nc8, acc, -1.f);
+    }
+    __syncthreads();
     // T diag(beta gamma), T diag(beta) and T as bf16 (the upper triangle is zero)
     for (int e = tid; e < kC * kC / 2; e += kPrepThreads) {
         const int i = e / (kC / 2), j = 2 * (e % (kC / 2));
         const float t0v = j <= i ? sR[i][j] : 0.f, t1v = j + 1 <= i ? sR[i][j + 1] : 0.f;
-        const float b0 = sb[j], b1 = sb[j + 1];
-        st_pair(sTK, kPs, i, j, t0v * b0 * __expf(sG[j]), t1v * b1 * __expf(sG[j + 1]));
-        st_pair(sTV, kPs, i, j, t0v * b0, t1v * b1);
+        st_pair(sTK, kPs, i, j, t0v * sgb[j], t1v * sgb[j + 1]);
+        st_pair(sTV, kPs, i, j, t0v * sb[j], t1v * sb[j + 1]);
         st_pair(sA, kPs, i, j, t0v, t1v);
     }
     __syncthreads();
@@ -583,6 +633,13 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(ScanParams 
 }
 
 // ============================================================== kernel 3: gradients of a chunk
+// One CTA of 16 warps per chunk, in two sides that each own one 64 x 128 accumulator in
+// registers (32 x 32 per warp):
+//   K side (warps 0-7): dk <- e_end dKt + beta gamma dXK + dAr^T Q + beta dRr K + (beta dRr)^T K;
+//                       the 64 x 64 products QK^T, dA, KK^T, Y = T^T dT and dR (16 x 32 per warp);
+//   Q side (warps 8-15): dq <- s gamma dO S^T + dAr K;  dW = -dE S^T, dv = beta T^T dE, dT.
+// Phases (block barriers between them): 1 dKt, QK^T, dA | <S,dS'>, dQg, dW;  2 dXK, dAr^T Q, KK^T |
+// dXV, dT, dAr K;  3 Y, dR and the dRr terms (K side);  then the per-token sums.
 struct GradParams {
     const bf16 *q, *k, *v, *dO;
     const float *alpha;
@@ -597,24 +654,30 @@ enum { RQ_KT = 0, RQ_Q, RQ_B1, RQ_B2, RQ_B3, RQ_MA, kRowQty };   // per-row part
 enum { CQ_MA = 0, CQ_MR, kColQty };                             // per-column partial sums
 constexpr int GR_Q = 0, GR_K = GR_Q + kTileTok, GR_V = GR_K + kTileTok, GR_DO = GR_V + kTileTok;
 constexpr int GR_E = GR_DO + kTileTok, GR_DE = GR_E + kTileTok;
-constexpr int GR_S = GR_DE + kTileTok, GR_DS = GR_S + kTileSt;     // S_c, dS_{c+1}; later reused:
-constexpr int GR_DW = GR_S, GR_DT = GR_DW + kTileTok, GR_Y = GR_DT + kTileSq, GR_DAR = GR_Y + kTileSq;
-constexpr int GR_DRR = GR_DAR + kTileSq, GR_BDRR = GR_DRR + kTileSq;
-static_assert(GR_BDRR + kTileSq <= GR_DS + kTileSt, "reused area");
-constexpr int GR_T = GR_DS + kTileSt, GR_CG = GR_T + kTileSq;
+constexpr int GR_S = GR_DE + kTileTok, GR_DS = GR_S + kTileSt;     // S_c, dS_{c+1}
+constexpr int GR_DW = GR_S;                                         // dW over S once S is read
+constexpr int GR_T = GR_DS + kTileSt, GR_DAR = GR_T + kTileSq, GR_DT = GR_DAR + kTileSq;
+constexpr int GR_Y = GR_DS, GR_DRR = GR_Y + kTileSq, GR_BDRR = GR_DRR + kTileSq;   // over dS' in phase 3
+constexpr int GR_CG = GR_DT + kTileSq;
 constexpr int GR_RROW = GR_CG + static_cast<int>(kCgFloats) * 4;   // fp32 [kRowQty][4][64]
 constexpr int GR_RCOL = GR_RROW + kRowQty * 4 * kC * 4;            // fp32 [kColQty][4][64]
-constexpr int GR_SC = GR_RCOL + kColQty * 4 * kC * 4;              // fp32 [16] block partials of <S, dS'>
-constexpr int GR_KC = GR_SC + 16 * 4;                              // fp32 [64] coefficient of k in dk
-constexpr int GR_XS = GR_KC + kC * 4;                              // fp32 [4] scratch of warps 0-1
+constexpr int GR_SC = GR_RCOL + kColQty * 4 * kC * 4;              // fp32 [8] partials of <S, dS'>
+constexpr int GR_KC = GR_SC + 8 * 4;                               // fp32 [64] coefficient of k in dk
+constexpr int GR_XS = GR_KC + kC * 4;                              // fp32 [4] scratch of the token pass
 constexpr int GR_BYTES = GR_XS + 16;
 static_assert(GR_BYTES <= 232448, "gradient kernel shared memory");
+constexpr uint32_t kBarToken = 1, kBarK = 2, kBarQ = 3;           // named barriers (0 = __syncthreads)
+
+__device__ __forceinline__ void bar_named(uint32_t id, uint32_t n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
 
 __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_kernel(GradParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
     auto tile = [&](int off) { return reinterpret_cast<bf16 *>(smem + off); };
     bf16 *sQ = tile(GR_Q), *sK = tile(GR_K), *sV = tile(GR_V), *sDO = tile(GR_DO), *sE = tile(GR_E),
-         *sDE = tile(GR_DE), *sS = tile(GR_S), *sDS = tile(GR_DS), *sT = tile(GR_T);
+         *sDE = tile(GR_DE), *sS = tile(GR_S), *sDS = tile(GR_DS), *sT = tile(GR_T), *sDW = tile(GR_DW),
+         *sDAR = tile(GR_DAR), *sDT = tile(GR_DT), *sY = tile(GR_Y), *sDRR = tile(GR_DRR), *sBDRR = tile(GR_BDRR);
     const float *cg = reinterpret_cast<const float *>(smem + GR_CG);
     float(*rrow)[4][kC] = reinterpret_cast<float(*)[4][kC]>(smem + GR_RROW);
     float(*rcol)[4][kC] = reinterpret_cast<float(*)[4][kC]>(smem + GR_RCOL);
@@ -643,248 +706,288 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_kernel(GradParams p)
     cp_wait<0>();
     __syncthreads();
 
-    const int wr = warp & 3, wc = warp >> 2, m0 = 16 * wr, n0 = 32 * wc, n0s = 16 * wc;
+    const bool kside = warp < 8;
+    const int sw = warp & 7;
+    const int r1 = 32 * (sw & 1), c1 = 32 * (sw >> 1), cb1 = sw >> 1;   // 64 x 128 products: 32 x 32 per warp
+    const int r2 = 16 * (sw & 3), c2 = 32 * (sw >> 2), cb2 = sw >> 2;   // 64 x 64 products: 16 x 32 per warp
     const float s = p.q_scale, Gend = cg[kC - 1];
-    int rr[2];
-    float gam[2], eend[2], bet[2];
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-        rr[hh] = m0 + g + 8 * hh;
-        gam[hh] = __expf(cg[rr[hh]]);
-        eend[hh] = __expf(Gend - cg[rr[hh]]);
-        bet[hh] = cg[kC + rr[hh]];
-    }
-    float rowp[kRowQty][2] = {};
-    float colp[kColQty][2][2] = {};
-    // sum over this thread's columns of X[r][col] * acc (X a bf16 tile with 128 columns)
-    auto rowdot = [&](const bf16 *X, const float (&a)[4][4], int hh) {
+    auto row1 = [&](int mi, int hh) { return r1 + 16 * mi + g + 8 * hh; };
+    auto row2 = [&](int hh) { return r2 + g + 8 * hh; };
+    // sum over this thread's columns of X[row][col] * a for a 64 x 128 accumulator and a bf16 tile X
+    auto rowdot1 = [&](const bf16 *X, const float (&a)[2][4][4], int mi, int hh) {
         float sum = 0.f;
 #pragma unroll
         for (int ni = 0; ni < 4; ++ni) {
-            const float2 x = ld_pair(X, kP, rr[hh], n0 + 8 * ni + 2 * q4);
-            sum = fmaf(x.x, a[ni][2 * hh], fmaf(x.y, a[ni][2 * hh + 1], sum));
+            const float2 x = ld_pair(X, kP, row1(mi, hh), c1 + 8 * ni + 2 * q4);
+            sum = fmaf(x.x, a[mi][ni][2 * hh], fmaf(x.y, a[mi][ni][2 * hh + 1], sum));
         }
         return sum;
     };
-
-    // <S, dS'>
-    {
-        float sum = 0.f;
-        for (int i = tid; i < kD * 16; i += kGradThreads) {
-            const int r = i >> 4, cc = (i & 15) * 8;
-            const uint4 a = *reinterpret_cast<const uint4 *>(sS + r * kP + cc);
-            const uint4 d = *reinterpret_cast<const uint4 *>(sDS + r * kP + cc);
-            const uint32_t *aw = reinterpret_cast<const uint32_t *>(&a), *dw = reinterpret_cast<const uint32_t *>(&d);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 x = unpack2(aw[e]), y = unpack2(dw[e]);
-                sum = fmaf(x.x, y.x, fmaf(x.y, y.y, sum));
-            }
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        if (lane == 0) rsc[warp] = sum;
-    }
-
-    float dQ[1][4][4], dK[1][4][4], acc[1][4][4];
-    // dKt = E dS'^T -> dk += e_end dKt
-    zero(acc[0]);
-    gemm_m<1, 4, 8, false, false>(acc, sptr(sE), kP, m0, 0, sptr(sDS), kP, n0, 0, lane);
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-        rowp[RQ_KT][hh] = rowdot(sK, acc[0], hh);
-#pragma unroll
-        for (int ni = 0; ni < 4; ++ni) {
-            dK[0][ni][2 * hh] = eend[hh] * acc[0][ni][2 * hh];
-            dK[0][ni][2 * hh + 1] = eend[hh] * acc[0][ni][2 * hh + 1];
-        }
-    }
-    // dQg = s dO S^T -> dq = gamma dQg
-    zero(acc[0]);
-    gemm_m<1, 4, 8, false, false>(acc, sptr(sDO), kP, m0, 0, sptr(sS), kP, n0, 0, lane);
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-        rowp[RQ_Q][hh] = s * rowdot(sQ, acc[0], hh);
-#pragma unroll
-        for (int ni = 0; ni < 4; ++ni) {
-            dQ[0][ni][2 * hh] = s * gam[hh] * acc[0][ni][2 * hh];
-            dQ[0][ni][2 * hh + 1] = s * gam[hh] * acc[0][ni][2 * hh + 1];
-        }
-    }
-    // dW = -dE S^T (staged as bf16 once S and dS' are no longer read)
-    zero(acc[0]);
-    gemm_m<1, 4, 8, false, false>(acc, sptr(sDE), kP, m0, 0, sptr(sS), kP, n0, 0, lane);
-    __syncthreads();
-    bf16 *sDW = tile(GR_DW), *sDT = tile(GR_DT), *sY = tile(GR_Y), *sDAR = tile(GR_DAR), *sDRR = tile(GR_DRR),
-         *sBDRR = tile(GR_BDRR);
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh)
+    // row partials over the 4 lanes of a row, into slot `cb` of quantity `qi`
+    auto put_row = [&](int qi, int cb, int row, float x) {
+        x += __shfl_xor_sync(0xffffffffu, x, 1);
+        x += __shfl_xor_sync(0xffffffffu, x, 2);
+        if (q4 == 0) rrow[qi][cb][row] = x;
+    };
+    // column partials of a 64 x 64 product over the 16 rows of the warp, into row block sw & 3
+    auto put_col = [&](int qi, const float (&x)[4][2]) {
 #pragma unroll
         for (int ni = 0; ni < 4; ++ni)
-            st_pair(sDW, kP, rr[hh], n0 + 8 * ni + 2 * q4, -acc[0][ni][2 * hh], -acc[0][ni][2 * hh + 1]);
-    __syncthreads();
-
-    // dXK = T^T dW -> dk += beta gamma dXK
-    zero(acc[0]);
-    gemm_m<1, 4, 4, true, true>(acc, sptr(sT), kPs, m0, 0, sptr(sDW), kP, n0, 0, lane);
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-        rowp[RQ_B1][hh] = rowdot(sK, acc[0], hh);
-        const float f = bet[hh] * gam[hh];
-#pragma unroll
-        for (int ni = 0; ni < 4; ++ni) {
-            dK[0][ni][2 * hh] = fmaf(f, acc[0][ni][2 * hh], dK[0][ni][2 * hh]);
-            dK[0][ni][2 * hh + 1] = fmaf(f, acc[0][ni][2 * hh + 1], dK[0][ni][2 * hh + 1]);
-        }
-    }
-    // dXV = T^T dE -> dv = beta dXV
-    zero(acc[0]);
-    gemm_m<1, 4, 4, true, true>(acc, sptr(sT), kPs, m0, 0, sptr(sDE), kP, n0, 0, lane);
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-        rowp[RQ_B2][hh] = rowdot(sV, acc[0], hh);
-        if (rr[hh] < L) {
-            float *dst = p.dv + (tok0 + static_cast<size_t>(rr[hh]) * p.H) * kD;
-#pragma unroll
-            for (int ni = 0; ni < 4; ++ni)
-                *reinterpret_cast<float2 *>(dst + n0 + 8 * ni + 2 * q4) =
-                    make_float2(bet[hh] * acc[0][ni][2 * hh], bet[hh] * acc[0][ni][2 * hh + 1]);
-        }
-    }
-    // dT = dW K^T diag(beta gamma) + dE V^T diag(beta)
-    {
-        float a1[1][2][4], a2[1][2][4];
-        zero(a1[0]);
-        zero(a2[0]);
-        gemm_m<1, 2, 8, false, false>(a1, sptr(sDW), kP, m0, 0, sptr(sK), kP, n0s, 0, lane);
-        gemm_m<1, 2, 8, false, false>(a2, sptr(sDE), kP, m0, 0, sptr(sV), kP, n0s, 0, lane);
-#pragma unroll
-        for (int ni = 0; ni < 2; ++ni) {
-            const int j = n0s + 8 * ni + 2 * q4;
-            const float bj0 = cg[kC + j], bj1 = cg[kC + j + 1];
-            const float fj0 = bj0 * __expf(cg[j]), fj1 = bj1 * __expf(cg[j + 1]);
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
-                st_pair(sDT, kPs, rr[hh], j, fmaf(fj0, a1[0][ni][2 * hh], bj0 * a2[0][ni][2 * hh]),
-                        fmaf(fj1, a1[0][ni][2 * hh + 1], bj1 * a2[0][ni][2 * hh + 1]));
-        }
-    }
-    // dA = s lower(dO E^T), dAr = dA . ratio; M = dAr . QK^T
-    {
-        float qk[1][2][4], da[1][2][4];
-        zero(qk[0]);
-        zero(da[0]);
-        gemm_m<1, 2, 8, false, false>(qk, sptr(sQ), kP, m0, 0, sptr(sK), kP, n0s, 0, lane);
-        gemm_m<1, 2, 8, false, false>(da, sptr(sDO), kP, m0, 0, sptr(sE), kP, n0s, 0, lane);
-#pragma unroll
-        for (int ni = 0; ni < 2; ++ni)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int i = rr[hh];
-                float v2[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int j = n0s + 8 * ni + 2 * q4 + e;
-                    const float x = j <= i ? s * da[0][ni][2 * hh + e] * __expf(cg[i] - cg[j]) : 0.f;
-                    v2[e] = x;
-                    const float m = x * qk[0][ni][2 * hh + e];
-                    rowp[RQ_MA][hh] += m;
-                    colp[CQ_MA][ni][e] += m;
-                }
-                st_pair(sDAR, kPs, i, n0s + 8 * ni + 2 * q4, v2[0], v2[1]);
-            }
-    }
-    __syncthreads();   // dT and dAr are visible
-
-    // Y = T^T dT
-    {
-        float y[1][2][4];
-        zero(y[0]);
-        gemm_m<1, 2, 4, true, true>(y, sptr(sT), kPs, m0, 0, sptr(sDT), kPs, n0s, 0, lane);
-#pragma unroll
-        for (int ni = 0; ni < 2; ++ni)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
-                st_pair(sY, kPs, rr[hh], n0s + 8 * ni + 2 * q4, y[0][ni][2 * hh], y[0][ni][2 * hh + 1]);
-    }
-    // dq += dAr K;  dk += dAr^T Q
-    gemm_m<1, 4, 4, false, true>(dQ, sptr(sDAR), kPs, m0, 0, sptr(sK), kP, n0, 0, lane);
-    gemm_m<1, 4, 4, true, true>(dK, sptr(sDAR), kPs, m0, 0, sptr(sQ), kP, n0, 0, lane);
-    __syncthreads();   // Y is visible
-
-    // dR = -strict_lower(Y T^T), dRr = dR . ratio; N = beta_i dRr . KK^T
-    {
-        float kk[1][2][4], dr[1][2][4];
-        zero(kk[0]);
-        zero(dr[0]);
-        gemm_m<1, 2, 8, false, false>(kk, sptr(sK), kP, m0, 0, sptr(sK), kP, n0s, 0, lane);
-        gemm_m<1, 2, 4, false, false>(dr, sptr(sY), kPs, m0, 0, sptr(sT), kPs, n0s, 0, lane);
-#pragma unroll
-        for (int ni = 0; ni < 2; ++ni)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int i = rr[hh];
-                float v2[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int j = n0s + 8 * ni + 2 * q4 + e;
-                    const float x = j < i ? -dr[0][ni][2 * hh + e] * __expf(cg[i] - cg[j]) : 0.f;
-                    v2[e] = x;
-                    const float m = x * kk[0][ni][2 * hh + e];
-                    rowp[RQ_B3][hh] += m;
-                    colp[CQ_MR][ni][e] += bet[hh] * m;
-                }
-                st_pair(sDRR, kPs, i, n0s + 8 * ni + 2 * q4, v2[0], v2[1]);
-                st_pair(sBDRR, kPs, i, n0s + 8 * ni + 2 * q4, bet[hh] * v2[0], bet[hh] * v2[1]);
-            }
-    }
-    // row partials: over the 4 lanes of a row, then one slot per column block of warps
-#pragma unroll
-    for (int qi = 0; qi < kRowQty; ++qi)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            float x = rowp[qi][hh];
-            x += __shfl_xor_sync(0xffffffffu, x, 1);
-            x += __shfl_xor_sync(0xffffffffu, x, 2);
-            if (q4 == 0) rrow[qi][wc][rr[hh]] = x;
-        }
-    // column partials: over the 8 row groups of the warp, then one slot per row block of warps
-#pragma unroll
-    for (int qi = 0; qi < kColQty; ++qi)
-#pragma unroll
-        for (int ni = 0; ni < 2; ++ni)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                float x = colp[qi][ni][e];
-                x += __shfl_xor_sync(0xffffffffu, x, 4);
-                x += __shfl_xor_sync(0xffffffffu, x, 8);
-                x += __shfl_xor_sync(0xffffffffu, x, 16);
-                if (g == 0) rcol[qi][wr][n0s + 8 * ni + 2 * q4 + e] = x;
+                float y = x[ni][e];
+                y += __shfl_xor_sync(0xffffffffu, y, 4);
+                y += __shfl_xor_sync(0xffffffffu, y, 8);
+                y += __shfl_xor_sync(0xffffffffu, y, 16);
+                if (g == 0) rcol[qi][sw & 3][c2 + 8 * ni + 2 * q4 + e] = y;
             }
-    __syncthreads();   // dRr, beta dRr and the partial sums are visible
+    };
+    auto ratio = [&](int i, int j) { return __expf(cg[i] - cg[j]); };
 
-    // dk += beta dRr K + (beta dRr)^T K
-    zero(acc[0]);
-    gemm_m<1, 4, 4, false, true>(acc, sptr(sDRR), kPs, m0, 0, sptr(sK), kP, n0, 0, lane);
+    float acc[2][4][4];   // the side's 64 x 128 accumulator (dk or dq)
+    float tmp[2][4][4];
+    float kk[1][4][4];    // K side: K K^T, kept from phase 2 to phase 3
+    if (kside) {
+        // ---- phase 1 (K side): dKt = E dS'^T -> dk = e_end dKt;  QK^T;  dA = s lower(dO E^T)
+        zero(acc[0]);
+        zero(acc[1]);
+        gemm_m<2, 4, 8, false, false>(acc, sptr(sE), kP, r1, 0, sptr(sDS), kP, c1, 0, lane);
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh)
+        for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
-        for (int ni = 0; ni < 4; ++ni) {
-            dK[0][ni][2 * hh] = fmaf(bet[hh], acc[0][ni][2 * hh], dK[0][ni][2 * hh]);
-            dK[0][ni][2 * hh + 1] = fmaf(bet[hh], acc[0][ni][2 * hh + 1], dK[0][ni][2 * hh + 1]);
+            for (int hh = 0; hh < 2; ++hh) {
+                const int r = row1(mi, hh);
+                put_row(RQ_KT, cb1, r, rowdot1(sK, acc, mi, hh));
+                const float ee = __expf(Gend - cg[r]);
+#pragma unroll
+                for (int ni = 0; ni < 4; ++ni) {
+                    acc[mi][ni][2 * hh] *= ee;
+                    acc[mi][ni][2 * hh + 1] *= ee;
+                }
+            }
+        float qk[1][4][4], da[1][4][4];
+        zero(qk[0]);
+        zero(da[0]);
+        gemm_m<1, 4, 8, false, false>(qk, sptr(sQ), kP, r2, 0, sptr(sK), kP, c2, 0, lane);
+        gemm_m<1, 4, 8, false, false>(da, sptr(sDO), kP, r2, 0, sptr(sE), kP, c2, 0, lane);
+        float colm[4][2] = {};
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int i = row2(hh);
+            float rowm = 0.f;
+#pragma unroll
+            for (int ni = 0; ni < 4; ++ni) {
+                float v2[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int j = c2 + 8 * ni + 2 * q4 + e;
+                    const float x = j <= i ? s * da[0][ni][2 * hh + e] * ratio(i, j) : 0.f;
+                    v2[e] = x;
+                    const float m = x * qk[0][ni][2 * hh + e];
+                    rowm += m;
+                    colm[ni][e] += m;
+                }
+                st_pair(sDAR, kPs, i, c2 + 8 * ni + 2 * q4, v2[0], v2[1]);
+            }
+            put_row(RQ_MA, cb2, i, rowm);
         }
-    gemm_m<1, 4, 4, true, true>(dK, sptr(sBDRR), kPs, m0, 0, sptr(sK), kP, n0, 0, lane);
-
-    // per token: dbeta, deta, the k coefficient, dG and its reverse prefix (warps 0-1, token = tid)
-    if (tid < kC) {
-        const int t = tid;
-        float red[kRowQty];
+        put_col(CQ_MA, colm);
+    } else {
+        // ---- phase 1 (Q side): <S, dS'>;  dQg = s dO S^T -> dq = gamma dQg;  dW = -dE S^T
+        {
+            float sum = 0.f;
+            for (int i = tid - 256; i < kD * 16; i += 256) {
+                const int r = i >> 4, cc = (i & 15) * 8;
+                const uint4 x = *reinterpret_cast<const uint4 *>(sS + r * kP + cc);
+                const uint4 y = *reinterpret_cast<const uint4 *>(sDS + r * kP + cc);
+                const uint32_t *xw = reinterpret_cast<const uint32_t *>(&x), *yw = reinterpret_cast<const uint32_t *>(&y);
 #pragma unroll
-        for (int qi = 0; qi < kRowQty; ++qi) red[qi] = rrow[qi][0][t] + rrow[qi][1][t] + rrow[qi][2][t] + rrow[qi][3][t];
+                for (int e = 0; e < 4; ++e) {
+                    const float2 u = unpack2(xw[e]), w = unpack2(yw[e]);
+                    sum = fmaf(u.x, w.x, fmaf(u.y, w.y, sum));
+                }
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            if (lane == 0) rsc[sw] = sum;
+        }
+        zero(acc[0]);
+        zero(acc[1]);
+        gemm_m<2, 4, 8, false, false>(acc, sptr(sDO), kP, r1, 0, sptr(sS), kP, c1, 0, lane);
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int r = row1(mi, hh);
+                put_row(RQ_Q, cb1, r, s * rowdot1(sQ, acc, mi, hh));
+                const float f = s * __expf(cg[r]);
+#pragma unroll
+                for (int ni = 0; ni < 4; ++ni) {
+                    acc[mi][ni][2 * hh] *= f;
+                    acc[mi][ni][2 * hh + 1] *= f;
+                }
+            }
+        zero(tmp[0]);
+        zero(tmp[1]);
+        gemm_m<2, 4, 8, false, false>(tmp, sptr(sDE), kP, r1, 0, sptr(sS), kP, c1, 0, lane);
+        bar_named(kBarQ, 256);   // every read of S is done (only this side reads it): dW goes over it
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                for (int ni = 0; ni < 4; ++ni)
+                    st_pair(sDW, kP, row1(mi, hh), c1 + 8 * ni + 2 * q4, -tmp[mi][ni][2 * hh], -tmp[mi][ni][2 * hh + 1]);
+    }
+    __syncthreads();   // dW and dAr are visible; dS' is no longer read
+
+    if (kside) {
+        // ---- phase 2 (K side): dXK = T^T dW -> dk += beta gamma dXK;  dk += dAr^T Q;  KK^T
+        zero(tmp[0]);
+        zero(tmp[1]);
+        gemm_m<2, 4, 4, true, true>(tmp, sptr(sT), kPs, r1, 0, sptr(sDW), kP, c1, 0, lane);
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int r = row1(mi, hh);
+                put_row(RQ_B1, cb1, r, rowdot1(sK, tmp, mi, hh));
+                const float f = cg[kC + r] * __expf(cg[r]);
+#pragma unroll
+                for (int ni = 0; ni < 4; ++ni) {
+                    acc[mi][ni][2 * hh] = fmaf(f, tmp[mi][ni][2 * hh], acc[mi][ni][2 * hh]);
+                    acc[mi][ni][2 * hh + 1] = fmaf(f, tmp[mi][ni][2 * hh + 1], acc[mi][ni][2 * hh + 1]);
+                }
+            }
+        gemm_m<2, 4, 4, true, true>(acc, sptr(sDAR), kPs, r1, 0, sptr(sQ), kP, c1, 0, lane);
+        zero(kk[0]);
+        gemm_m<1, 4, 8, false, false>(kk, sptr(sK), kP, r2, 0, sptr(sK), kP, c2, 0, lane);
+    } else {
+        // ---- phase 2 (Q side): dXV = T^T dE -> dv;  dT;  dq += dAr K -> dq out
+        zero(tmp[0]);
+        zero(tmp[1]);
+        gemm_m<2, 4, 4, true, true>(tmp, sptr(sT), kPs, r1, 0, sptr(sDE), kP, c1, 0, lane);
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int r = row1(mi, hh);
+                put_row(RQ_B2, cb1, r, rowdot1(sV, tmp, mi, hh));
+                if (r < L) {
+                    const float bt = cg[kC + r];
+                    float *dst = p.dv + (tok0 + static_cast<size_t>(r) * p.H) * kD;
+#pragma unroll
+                    for (int ni = 0; ni < 4; ++ni)
+                        *reinterpret_cast<float2 *>(dst + c1 + 8 * ni + 2 * q4) =
+                            make_float2(bt * tmp[mi][ni][2 * hh], bt * tmp[mi][ni][2 * hh + 1]);
+                }
+            }
+        {   // dT = dW K^T diag(beta gamma) + dE V^T diag(beta)
+            float a1[1][4][4], a2[1][4][4];
+            zero(a1[0]);
+            zero(a2[0]);
+            gemm_m<1, 4, 8, false, false>(a1, sptr(sDW), kP, r2, 0, sptr(sK), kP, c2, 0, lane);
+            gemm_m<1, 4, 8, false, false>(a2, sptr(sDE), kP, r2, 0, sptr(sV), kP, c2, 0, lane);
+#pragma unroll
+            for (int ni = 0; ni < 4; ++ni) {
+                const int j = c2 + 8 * ni + 2 * q4;
+                const float bj0 = cg[kC + j], bj1 = cg[kC + j + 1];
+                const float fj0 = bj0 * __expf(cg[j]), fj1 = bj1 * __expf(cg[j + 1]);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh)
+                    st_pair(sDT, kPs, row2(hh), j, fmaf(fj0, a1[0][ni][2 * hh], bj0 * a2[0][ni][2 * hh]),
+                            fmaf(fj1, a1[0][ni][2 * hh + 1], bj1 * a2[0][ni][2 * hh + 1]));
+            }
+        }
+        gemm_m<2, 4, 4, false, true>(acc, sptr(sDAR), kPs, r1, 0, sptr(sK), kP, c1, 0, lane);
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int r = row1(mi, hh);
+                if (r >= L) continue;
+                float *dst = p.dq + (tok0 + static_cast<size_t>(r) * p.H) * kD;
+#pragma unroll
+                for (int ni = 0; ni < 4; ++ni)
+                    *reinterpret_cast<float2 *>(dst + c1 + 8 * ni + 2 * q4) =
+                        make_float2(acc[mi][ni][2 * hh], acc[mi][ni][2 * hh + 1]);
+            }
+    }
+    __syncthreads();   // dT is visible
+
+    if (kside) {
+        // ---- phase 3 (K side): Y = T^T dT;  dR = -strict_lower(Y T^T), dRr = dR . ratio;
+        //      dk += beta dRr K + (beta dRr)^T K
+        {
+            float y[1][4][4];
+            zero(y[0]);
+            gemm_m<1, 4, 4, true, true>(y, sptr(sT), kPs, r2, 0, sptr(sDT), kPs, c2, 0, lane);
+#pragma unroll
+            for (int ni = 0; ni < 4; ++ni)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh)
+                    st_pair(sY, kPs, row2(hh), c2 + 8 * ni + 2 * q4, y[0][ni][2 * hh], y[0][ni][2 * hh + 1]);
+        }
+        bar_named(kBarK, 256);
+        {
+            float dr[1][4][4];
+            zero(dr[0]);
+            gemm_m<1, 4, 4, false, false>(dr, sptr(sY), kPs, r2, 0, sptr(sT), kPs, c2, 0, lane);
+            float coln[4][2] = {};
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int i = row2(hh);
+                const float bi = cg[kC + i];
+                float rown = 0.f;
+#pragma unroll
+                for (int ni = 0; ni < 4; ++ni) {
+                    float v2[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int j = c2 + 8 * ni + 2 * q4 + e;
+                        const float x = j < i ? -dr[0][ni][2 * hh + e] * ratio(i, j) : 0.f;
+                        v2[e] = x;
+                        const float m = x * kk[0][ni][2 * hh + e];
+                        rown += m;
+                        coln[ni][e] += bi * m;
+                    }
+                    st_pair(sDRR, kPs, i, c2 + 8 * ni + 2 * q4, v2[0], v2[1]);
+                    st_pair(sBDRR, kPs, i, c2 + 8 * ni + 2 * q4, bi * v2[0], bi * v2[1]);
+                }
+                put_row(RQ_B3, cb2, i, rown);
+            }
+            put_col(CQ_MR, coln);
+        }
+        bar_named(kBarK, 256);
+        zero(tmp[0]);
+        zero(tmp[1]);
+        gemm_m<2, 4, 4, false, true>(tmp, sptr(sDRR), kPs, r1, 0, sptr(sK), kP, c1, 0, lane);
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const float bt = cg[kC + row1(mi, hh)];
+#pragma unroll
+                for (int ni = 0; ni < 4; ++ni) {
+                    acc[mi][ni][2 * hh] = fmaf(bt, tmp[mi][ni][2 * hh], acc[mi][ni][2 * hh]);
+                    acc[mi][ni][2 * hh + 1] = fmaf(bt, tmp[mi][ni][2 * hh + 1], acc[mi][ni][2 * hh + 1]);
+                }
+            }
+        gemm_m<2, 4, 4, true, true>(acc, sptr(sBDRR), kPs, r1, 0, sptr(sK), kP, c1, 0, lane);
+    }
+    __syncthreads();   // every partial sum is in shared memory
+
+    // per token (warps 8-9, token = tid - 256): dbeta, deta, the k coefficient, dG and its reverse prefix
+    if (tid >= 256 && tid < 256 + kC) {
+        const int t = tid - 256;
+        auto rsum4 = [&](int qi) { return rrow[qi][0][t] + rrow[qi][1][t] + rrow[qi][2][t] + rrow[qi][3][t]; };
+        auto rsum2 = [&](int qi) { return rrow[qi][0][t] + rrow[qi][1][t]; };
+        const float kt_raw = rsum4(RQ_KT), qd = rsum4(RQ_Q), b1 = rsum4(RQ_B1), b2 = rsum4(RQ_B2);
+        const float b3 = rsum2(RQ_B3), ma = rsum2(RQ_MA);
         const float cma = rcol[CQ_MA][0][t] + rcol[CQ_MA][1][t] + rcol[CQ_MA][2][t] + rcol[CQ_MA][3][t];
         const float cmr = rcol[CQ_MR][0][t] + rcol[CQ_MR][1][t] + rcol[CQ_MR][2][t] + rcol[CQ_MR][3][t];
         const float gt = __expf(cg[t]), et = __expf(Gend - cg[t]), bt = cg[kC + t], den = cg[2 * kC + t];
-        const float dbeta = fmaf(gt, red[RQ_B1], red[RQ_B2] + red[RQ_B3]);
+        const float dbeta = fmaf(gt, b1, b2 + b3);
         float deta = dbeta, kc = 0.f;
         if (!p.beta_raw) {
             const bool flows = den != 0.f;
@@ -892,22 +995,22 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_kernel(GradParams p)
             kc = flows ? -2.f * bt * dbeta / den : 0.f;
         }
         kcoef[t] = kc;
-        const float kt = et * red[RQ_KT];
-        float dG = gt * red[RQ_Q] + bt * gt * red[RQ_B1] + red[RQ_MA] - cma + bt * red[RQ_B3] - cmr - kt;
+        const float kt = et * kt_raw;
+        float dG = gt * qd + bt * gt * b1 + ma - cma + bt * b3 - cmr - kt;
         // the chunk's last row also carries the end decay's terms: sum_j e_end_j k_j.dKt_j + Gamma <S, dS'>
         float ktot = kt;
 #pragma unroll
         for (int o = 16; o; o >>= 1) ktot += __shfl_xor_sync(0xffffffffu, ktot, o);
-        if (lane == 0) xs[warp] = ktot;
-        asm volatile("bar.sync 1, 64;" ::: "memory");   // warps 0-1 only
+        if (lane == 0) xs[warp - 8] = ktot;
+        bar_named(kBarToken, 64);
         if (t == kC - 1) {
             float sds = 0.f;
 #pragma unroll
-            for (int w = 0; w < 16; ++w) sds += rsc[w];
+            for (int w = 0; w < 8; ++w) sds += rsc[w];
             dG += xs[0] + xs[1] + __expf(Gend) * sds;
         }
-        // reverse inclusive prefix over the 64 tokens: suffix sums within each warp, then warp 0
-        // adds warp 1's total
+        // reverse inclusive prefix over the 64 tokens: suffix sums within each warp, then the
+        // first warp adds the second warp's total
         float x = dG;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -915,7 +1018,7 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_kernel(GradParams p)
             if (lane + o < 32) x += y;
         }
         if (t == 32) xs[2] = x;
-        asm volatile("bar.sync 1, 64;" ::: "memory");
+        bar_named(kBarToken, 64);
         if (t < 32) x += xs[2];
         if (t < L) {
             const size_t o = tok0 + static_cast<size_t>(t) * p.H;
@@ -925,21 +1028,23 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_kernel(GradParams p)
     }
     __syncthreads();   // kcoef is visible
 
-    // dk += kcoef k; write dq and dk
+    if (kside) {   // dk += kcoef k; write dk
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-        if (rr[hh] >= L) continue;
-        const float kc = kcoef[rr[hh]];
-        float *dqr = p.dq + (tok0 + static_cast<size_t>(rr[hh]) * p.H) * kD;
-        float *dkr = p.dk + (tok0 + static_cast<size_t>(rr[hh]) * p.H) * kD;
+        for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
-        for (int ni = 0; ni < 4; ++ni) {
-            const int col = n0 + 8 * ni + 2 * q4;
-            const float2 kx = ld_pair(sK, kP, rr[hh], col);
-            *reinterpret_cast<float2 *>(dqr + col) = make_float2(dQ[0][ni][2 * hh], dQ[0][ni][2 * hh + 1]);
-            *reinterpret_cast<float2 *>(dkr + col) =
-                make_float2(fmaf(kc, kx.x, dK[0][ni][2 * hh]), fmaf(kc, kx.y, dK[0][ni][2 * hh + 1]));
-        }
+            for (int hh = 0; hh < 2; ++hh) {
+                const int r = row1(mi, hh);
+                if (r >= L) continue;
+                const float kc = kcoef[r];
+                float *dst = p.dk + (tok0 + static_cast<size_t>(r) * p.H) * kD;
+#pragma unroll
+                for (int ni = 0; ni < 4; ++ni) {
+                    const int col = c1 + 8 * ni + 2 * q4;
+                    const float2 kx = ld_pair(sK, kP, r, col);
+                    *reinterpret_cast<float2 *>(dst + col) =
+                        make_float2(fmaf(kc, kx.x, acc[mi][ni][2 * hh]), fmaf(kc, kx.y, acc[mi][ni][2 * hh + 1]));
+                }
+            }
     }
 }
 
