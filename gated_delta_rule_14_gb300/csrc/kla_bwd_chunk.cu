@@ -248,8 +248,8 @@ constexpr int PR_TV = PR_TK + kTileSq;                // bf16 T diag(beta)
 constexpr int PR_A = PR_TV + kTileSq;                 // bf16 A (then T) staging
 constexpr int kPX = 36;
 constexpr int PR_X = PR_A + kTileSq;                  // fp32 [32][36] merge scratch
-constexpr int PR_VEC = PR_X + 32 * kPX * 4;           // g, G, beta, n2, beta e^G (fp32 [5][64])
-constexpr int PR_BYTES = PR_VEC + 5 * kC * 4;
+constexpr int PR_VEC = PR_X + 32 * kPX * 4;           // eta, G, beta, beta e^G (fp32 [4][64])
+constexpr int PR_BYTES = PR_VEC + 4 * kC * 4;
 
 __global__ void __launch_bounds__(kPrepThreads, 2) bwd_prep_kernel(PrepParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) bwd_prep_kernel(PrepParams p)
     bf16 *sTK = reinterpret_cast<bf16 *>(smem + PR_TK), *sTV = reinterpret_cast<bf16 *>(smem + PR_TV),
          *sA = reinterpret_cast<bf16 *>(smem + PR_A);
     float *sX = reinterpret_cast<float *>(smem + PR_X);
-    float *sg = reinterpret_cast<float *>(smem + PR_VEC), *sG = sg + kC, *sb = sG + kC, *sn = sb + kC, *sgb = sn + kC;
+    float *seta = reinterpret_cast<float *>(smem + PR_VEC), *sG = seta + kC, *sb = sG + kC, *sgb = sb + kC;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const size_t rs = static_cast<size_t>(p.H) * kD;                      // token row stride
@@ -272,47 +272,29 @@ __global__ void __launch_bounds__(kPrepThreads, 2) bwd_prep_kernel(PrepParams p)
     load_tok(sQ, p.q + base * kD, rs, L, tid, kPrepThreads);
     load_tok(sV, p.v + base * kD, rs, L, tid, kPrepThreads);
     cp_commit();
-    float eta = 0.f;
-    if (tid < kC) {
-        const bool ok = tid < L;
-        sg[tid] = ok ? fmaxf(logf(p.alpha[base + static_cast<size_t>(tid) * p.H]), kMinLogGate) : 0.f;
-        eta = ok ? p.eta[base + static_cast<size_t>(tid) * p.H] : 0.f;
+    // gates while the tiles land (warp 0, tokens 2 lane and 2 lane + 1): g = log alpha, inclusive
+    // prefix G, eta
+    if (warp == 0) {
+        float x[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int t = 2 * lane + e;
+            const bool ok = t < L;
+            x[e] = ok ? fmaxf(logf(p.alpha[base + static_cast<size_t>(t) * p.H]), kMinLogGate) : 0.f;
+            seta[t] = ok ? p.eta[base + static_cast<size_t>(t) * p.H] : 0.f;
+        }
+        float sc = x[0] + x[1];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, sc, o);
+            if (lane >= o) sc += y;
+        }
+        sG[2 * lane + 1] = sc;
+        sG[2 * lane] = sc - x[1];
     }
     cp_wait<0>();
     __syncthreads();
-    // ||k_t||^2: warp w takes tokens 8w .. 8w + 7
-    for (int i = 0; i < 8; ++i) {
-        const int t = warp * 8 + i;
-        const float2 x0 = ld_pair(sK, kP, t, 4 * lane), x1 = ld_pair(sK, kP, t, 4 * lane + 2);
-        float s2 = x0.x * x0.x + x0.y * x0.y + x1.x * x1.x + x1.y * x1.y;
-#pragma unroll
-        for (int o = 16; o; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
-        if (lane == 0) sn[t] = s2;
-    }
-    // inclusive prefix of the log-gates: warp 0, two tokens per lane
-    if (warp == 0) {
-        const float x0 = sg[2 * lane], x1 = sg[2 * lane + 1];
-        float s = x0 + x1;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, s, o);
-            if (lane >= o) s += y;
-        }
-        sG[2 * lane + 1] = s;
-        sG[2 * lane] = s - x1;
-    }
-    __syncthreads();
     float *cg = p.ws.cg + n * kCgFloats;
-    if (tid < kC) {
-        const float den = sn[tid] + p.eps;
-        const float beta = tid < L ? kla_beta(eta, sn[tid], p.eps, p.beta_raw) : 0.f;
-        sb[tid] = beta;
-        sgb[tid] = beta * __expf(sG[tid]);
-        cg[tid] = sG[tid];
-        cg[kC + tid] = beta;
-        cg[2 * kC + tid] = den;
-    }
-    __syncthreads();
 
     // [K; Q] K^T: warp w owns rows 16 (w & 3) of K K^T (w < 4) or of Q K^T (w >= 4), all 64 columns
     {
@@ -321,6 +303,31 @@ __global__ void __launch_bounds__(kPrepThreads, 2) bwd_prep_kernel(PrepParams p)
         const int r0 = 16 * (warp & 3);
         gemm<8, 8, false, false>(acc, sptr(warp < 4 ? sK : sQ), kP, r0, 0, sptr(sK), kP, 0, 0, lane);
         const int g = lane >> 2, q4 = lane & 3;
+        float rb[2] = {0.f, 0.f};   // beta of this thread's two rows (K K^T warps)
+        if (warp < 4) {
+            // ||k_i||^2 is the diagonal of K K^T: the thread holding (i, i) publishes it with the
+            // row's G, beta and ||k||^2 + eps
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int i = r0 + g + 8 * hh;
+                        if (8 * nt + 2 * q4 + e == i) {
+                            const float n2 = acc[nt][2 * hh + e];
+                            const float beta = i < L ? kla_beta(seta[i], n2, p.eps, p.beta_raw) : 0.f;
+                            sb[i] = beta;
+                            sgb[i] = beta * __expf(sG[i]);
+                            cg[i] = sG[i];
+                            cg[kC + i] = beta;
+                            cg[2 * kC + i] = n2 + p.eps;
+                        }
+                    }
+            __syncwarp();
+            rb[0] = sb[r0 + g];
+            rb[1] = sb[r0 + g + 8];
+        }
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
@@ -331,7 +338,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) bwd_prep_kernel(PrepParams p)
                     const int j = 8 * nt + 2 * q4 + e;
                     const float ratio = __expf(sG[i] - sG[j]);
                     const float x = acc[nt][2 * hh + e];
-                    if (warp < 4) sR[i][j] = j < i ? sb[i] * ratio * x : 0.f;
+                    if (warp < 4) sR[i][j] = j < i ? rb[hh] * ratio * x : 0.f;
                     else acc[nt][2 * hh + e] = j <= i ? ratio * x : 0.f;
                 }
                 if (warp >= 4) st_pair(sA, kPs, i, 8 * nt + 2 * q4, acc[nt][2 * hh], acc[nt][2 * hh + 1]);
@@ -635,11 +642,12 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(ScanParams 
 // ============================================================== kernel 3: gradients of a chunk
 // One CTA of 16 warps per chunk, in two sides that each own one 64 x 128 accumulator in
 // registers (32 x 32 per warp):
-//   K side (warps 0-7): dk <- e_end dKt + beta gamma dXK + dAr^T Q + beta dRr K + (beta dRr)^T K;
+//   K side (warps 0-7): dk <- e_end dKt + beta gamma dXK + dAr^T Q + (beta dRr)^T K + beta dRr K;
 //                       the 64 x 64 products QK^T, dA, KK^T, Y = T^T dT and dR (16 x 32 per warp);
-//   Q side (warps 8-15): dq <- s gamma dO S^T + dAr K;  dW = -dE S^T, dv = beta T^T dE, dT.
+//   Q side (warps 8-15): dq <- s gamma dO S^T + dAr K;  dW = -dE S^T, dv = beta T^T dE, dT, and
+//                       beta dRr K, handed to the K side through shared memory.
 // Phases (block barriers between them): 1 dKt, QK^T, dA | <S,dS'>, dQg, dW;  2 dXK, dAr^T Q, KK^T |
-// dXV, dT, dAr K;  3 Y, dR and the dRr terms (K side);  then the per-token sums.
+// dXV, dT;  3 Y, dR | dAr K;  4 (beta dRr)^T K | beta dRr K;  then the per-token sums.
 struct GradParams {
     const bf16 *q, *k, *v, *dO;
     const float *alpha;
@@ -659,6 +667,9 @@ constexpr int GR_DW = GR_S;                                         // dW over S
 constexpr int GR_T = GR_DS + kTileSt, GR_DAR = GR_T + kTileSq, GR_DT = GR_DAR + kTileSq;
 constexpr int GR_Y = GR_DS, GR_DRR = GR_Y + kTileSq, GR_BDRR = GR_DRR + kTileSq;   // over dS' in phase 3
 constexpr int GR_CG = GR_DT + kTileSq;
+constexpr int kPX1 = kD + 8;                                        // fp32 hand-over tile over V and dO (phase 3)
+constexpr int GR_XCH = GR_V;
+static_assert(GR_XCH + kC * kPX1 * 4 <= GR_DO + kTileTok, "hand-over tile");
 constexpr int GR_RROW = GR_CG + static_cast<int>(kCgFloats) * 4;   // fp32 [kRowQty][4][64]
 constexpr int GR_RCOL = GR_RROW + kRowQty * 4 * kC * 4;            // fp32 [kColQty][4][64]
 constexpr int GR_SC = GR_RCOL + kColQty * 4 * kC * 4;              // fp32 [8] partials of <S, dS'>
@@ -899,25 +910,12 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_kernel(GradParams p)
                             fmaf(fj1, a1[0][ni][2 * hh + 1], bj1 * a2[0][ni][2 * hh + 1]));
             }
         }
-        gemm_m<2, 4, 4, false, true>(acc, sptr(sDAR), kPs, r1, 0, sptr(sK), kP, c1, 0, lane);
-#pragma unroll
-        for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int r = row1(mi, hh);
-                if (r >= L) continue;
-                float *dst = p.dq + (tok0 + static_cast<size_t>(r) * p.H) * kD;
-#pragma unroll
-                for (int ni = 0; ni < 4; ++ni)
-                    *reinterpret_cast<float2 *>(dst + c1 + 8 * ni + 2 * q4) =
-                        make_float2(acc[mi][ni][2 * hh], acc[mi][ni][2 * hh + 1]);
-            }
     }
     __syncthreads();   // dT is visible
 
+    float *xch = reinterpret_cast<float *>(smem + GR_XCH);   // fp32 [64][kPX1]: Q side -> K side
     if (kside) {
-        // ---- phase 3 (K side): Y = T^T dT;  dR = -strict_lower(Y T^T), dRr = dR . ratio;
-        //      dk += beta dRr K + (beta dRr)^T K
+        // ---- phase 3 (K side): Y = T^T dT;  dR = -strict_lower(Y T^T), dRr = dR . ratio
         {
             float y[1][4][4];
             zero(y[0]);
@@ -958,7 +956,27 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_kernel(GradParams p)
             }
             put_col(CQ_MR, coln);
         }
-        bar_named(kBarK, 256);
+    } else {
+        // ---- phase 3 (Q side): dq += dAr K -> dq out
+        gemm_m<2, 4, 4, false, true>(acc, sptr(sDAR), kPs, r1, 0, sptr(sK), kP, c1, 0, lane);
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int r = row1(mi, hh);
+                if (r >= L) continue;
+                float *dst = p.dq + (tok0 + static_cast<size_t>(r) * p.H) * kD;
+#pragma unroll
+                for (int ni = 0; ni < 4; ++ni)
+                    *reinterpret_cast<float2 *>(dst + c1 + 8 * ni + 2 * q4) =
+                        make_float2(acc[mi][ni][2 * hh], acc[mi][ni][2 * hh + 1]);
+            }
+    }
+    __syncthreads();   // dRr and beta dRr are visible
+    if (kside) {
+        gemm_m<2, 4, 4, true, true>(acc, sptr(sBDRR), kPs, r1, 0, sptr(sK), kP, c1, 0, lane);   // dk += (beta dRr)^T K
+    } else {
+        // beta dRr K for the K side, handed over in fp32 at the same fragment positions
         zero(tmp[0]);
         zero(tmp[1]);
         gemm_m<2, 4, 4, false, true>(tmp, sptr(sDRR), kPs, r1, 0, sptr(sK), kP, c1, 0, lane);
@@ -966,16 +984,27 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_kernel(GradParams p)
         for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-                const float bt = cg[kC + row1(mi, hh)];
+                const int r = row1(mi, hh);
+                const float bt = cg[kC + r];
+#pragma unroll
+                for (int ni = 0; ni < 4; ++ni)
+                    *reinterpret_cast<float2 *>(xch + r * kPX1 + c1 + 8 * ni + 2 * q4) =
+                        make_float2(bt * tmp[mi][ni][2 * hh], bt * tmp[mi][ni][2 * hh + 1]);
+            }
+    }
+    __syncthreads();   // the hand-over and every partial sum are in shared memory
+    if (kside) {
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
                 for (int ni = 0; ni < 4; ++ni) {
-                    acc[mi][ni][2 * hh] = fmaf(bt, tmp[mi][ni][2 * hh], acc[mi][ni][2 * hh]);
-                    acc[mi][ni][2 * hh + 1] = fmaf(bt, tmp[mi][ni][2 * hh + 1], acc[mi][ni][2 * hh + 1]);
+                    const float2 x = *reinterpret_cast<const float2 *>(xch + row1(mi, hh) * kPX1 + c1 + 8 * ni + 2 * q4);
+                    acc[mi][ni][2 * hh] += x.x;
+                    acc[mi][ni][2 * hh + 1] += x.y;
                 }
-            }
-        gemm_m<2, 4, 4, true, true>(acc, sptr(sBDRR), kPs, r1, 0, sptr(sK), kP, c1, 0, lane);
     }
-    __syncthreads();   // every partial sum is in shared memory
 
     // per token (warps 8-9, token = tid - 256): dbeta, deta, the k coefficient, dG and its reverse prefix
     if (tid >= 256 && tid < 256 + kC) {
