@@ -344,12 +344,15 @@ def bench_verify(ntok, calls, seed, dev, flush, stream, pk):
 BWD_BYTES_PER_TOKEN_HEAD = 4 * 2 * 128 + 8 + 3 * 4 * 128 + 8   # q, k, v, dO in; dq, dk, dv, dalpha, deta out
 
 
-def bench_bwd(name, steps, seed, dev, flush, stream, pk):
+BWD_KERNELS_PER_CALL = 4   # chunkwise path: prep, forward carry, reverse carry, gradients
+
+
+def bench_bwd(name, steps, seed, dev, flush, stream, pk, **override):
     """Backward pass of the named prefill workload (dL/do random bf16, dL/dS_T = 0)."""
     import torch
 
     import gated_delta_rule_14_gb300 as kla
-    inp, d = prefill_inputs(name, seed, dev)
+    inp, d = prefill_inputs(name, seed, dev, **override)
     wl = inp.wl
     g = torch.Generator(device=dev)
     g.manual_seed(seed)
@@ -364,7 +367,10 @@ def bench_bwd(name, steps, seed, dev, flush, stream, pk):
     alg = wl.B * wl.T * wl.H * BWD_BYTES_PER_TOKEN_HEAD
     return {"value": wl.B * wl.T / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
             "workspace_bytes": ws.numel(), "roofline": roofline(alg, ms, pk),
-            "note": "token-sequential fp32 backward, one CTA per (sequence, head): latency-bound"}
+            "note": "chunkwise backward on warp-level bf16 MMAs: chunk-parallel prep (T = (I+R)^-1, W, U, A), "
+                    "forward and reverse chunk-state carries (one CTA per chain), chunk-parallel gradients; "
+                    "~4.2 GB of DRAM traffic per call (ncu, per-chunk S_c, dS_c, E_c, dE_c, W, U, A, T records) "
+                    "against the algorithmic bytes"}
 
 
 def e2e_prefill(res, steps, warmup, dev, stream, parts=8):
@@ -476,6 +482,9 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=1024)
     ap.add_argument("--verify-calls", type=int, default=256)
     ap.add_argument("--no-bwd", action="store_true")
+    ap.add_argument("--bwd-only", action="store_true",
+                    help="time only the backward pass of gdn4k (a small case for profiling with --bwd-batch)")
+    ap.add_argument("--bwd-batch", type=int, default=8)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -503,6 +512,12 @@ def main():
         # of its inputs in L2 and without the flush's dirty lines left to write back
         flush_buf.zero_()
         torch.sum(flush_rd, dim=0, out=flush_sink)
+
+    if args.bwd_only:
+        r = bench_bwd("gdn4k", args.steps, seed=rank, dev=dev, flush=flush, stream=stream, pk=pk, B=args.bwd_batch)
+        if rank == 0:
+            print(json.dumps({"bwd_gdn4k": r, "batch": args.bwd_batch}), flush=True)
+        return
 
     clocks = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
     clocks.start()
@@ -562,7 +577,7 @@ def main():
             t0 = time.time()
             extras["bwd_gdn4k"] = bench_bwd("gdn4k", 3, seed=rank, dev=dev, flush=flush, stream=stream, pk=pk)
             clocks.mark(t0, time.time())
-            launches += 3
+            launches += 3 * BWD_KERNELS_PER_CALL
             torch.cuda.empty_cache()
     clk = clocks.stop()
 
