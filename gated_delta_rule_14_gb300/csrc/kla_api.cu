@@ -7,6 +7,10 @@
 namespace kla {
 // one bounded wait on a barrier phase that nothing completes (kla_selftest.cu)
 cudaError_t launch_selftest_wait(unsigned *err, unsigned limit, cudaStream_t stream);
+// several tokens per call on the pipelined decode tile walk (kla_decode.cu): T <= kShortSeqMaxT,
+// d_k = 128, d_v a multiple of 32, 16-byte aligned q, k, v, states and per-channel gates
+bool tokens_pipe_supports(const ChunkArgs &a);
+cudaError_t launch_tokens_pipe(const ChunkArgs &a);
 }  // namespace kla
 
 namespace {
@@ -147,7 +151,9 @@ kla_status chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
     a.q_scale = q_scale;
     a.no_segments = no_segments;
     if (err_word(&a.err) != cudaSuccess) return KLA_ERR_CUDA;
-    cudaError_t e = kla::recurrent_preferred(a) ? kla::launch_recurrent(a) : kla::launch_chunk_tc(a);
+    cudaError_t e = !kla::recurrent_preferred(a)      ? kla::launch_chunk_tc(a)
+                    : kla::tokens_pipe_supports(a) ? kla::launch_tokens_pipe(a)
+                                                   : kla::launch_recurrent(a);
     return e == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
 }
 

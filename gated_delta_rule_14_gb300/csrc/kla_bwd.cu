@@ -47,8 +47,9 @@ struct BwdParams {
     float q_scale;
 };
 
-__device__ __forceinline__ void prefetch_l2(const void *ptr) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+__device__ __forceinline__ void prefetch_l2(const void *ptr) {   // the 128-byte line holding ptr
+    const uintptr_t line = reinterpret_cast<uintptr_t>(ptr) & ~static_cast<uintptr_t>(127);
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(line));
 }
 
 // Reduce 4 partial column sums over the 16 row-group lanes (lane bits 1-4) and hand every lane

@@ -344,7 +344,308 @@ cudaError_t launch_t(const DecodeArgs &a) {
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------- several tokens per call
+// Multi-token decode and speculative verification (T <= kShortSeqMaxT tokens per sequence in
+// one call, kla_chunk_fwd): the persistent tile walk of decode_pipe_kernel with a token loop
+// inside each tile. A tile (32 value columns of one head) of the state is copied in once, the
+// T steps run on it in registers, in the single-token step's arithmetic and order (one block
+// barrier per token, partial sums double-buffered by token parity), and it is written once as
+// S_T; the tiles of the next head stream in meanwhile. The per-token ||k||^2 and k . q are
+// formed up front, one warp per token. The step is issue-bound once the state streams, so the
+// scalar gate scales the two reduced sums rather than every row, and d_k is fixed at 128.
+struct TokParams {
+    const void *q, *k, *v;
+    const float *alpha, *eta;
+    float eps;
+    const float *S0;      // NULL: zeros
+    float *S_T;           // NULL: not written; may alias S0 (each tile is read before it is written)
+    void *o;
+    int B, T, H, DK, DV;
+    int beta_raw;
+    float q_scale;
+    int stage_bytes, off_kq, off_v, off_a, off_e;   // dynamic shared-memory stage layout
+};
+
+// d_k = 128, two warps per tile: thread (rg, cg) holds key rows 16 rg .. 16 rg + 15
+// (consecutive, so k_u and q_u of its rows arrive as 16-byte loads) and value columns
+// 4 cg .. 4 cg + 3 of the tile; the cross-warp sum of a token's partials is over two warps.
+constexpr int kTokThreads = 64;
+template <typename TIn, bool kChannel>
+__global__ void __launch_bounds__(kTokThreads, 8) tokens_pipe_kernel(const TokParams p, int ntiles) {
+    constexpr int NCG = 8, BV = 32, DK = 128, RPT = 16;   // RPT rows per thread
+    constexpr int kThreads = kTokThreads;
+    static_assert(kThreads / NCG * RPT == DK, "rows per thread");
+    extern __shared__ __align__(16) unsigned char dsm[];
+    __shared__ __align__(16) float sred[2][kThreads / 32][2 * NCG * 4];
+    __shared__ float sbeta[kShortSeqMaxT], skqd[kShortSeqMaxT];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cg = tid % NCG, i0 = (tid / NCG) * RPT;
+    const int DV = p.DV, T = p.T, ctiles = DV / BV;
+    auto stage = [&](int slot, int off) { return dsm + slot * p.stage_bytes + off; };
+    auto tile_bh = [&](int t, int &v0) {
+        v0 = (t % ctiles) * BV;
+        return static_cast<size_t>(t / ctiles);   // = b * H + h
+    };
+    auto row_of = [&](size_t bh, int u) {          // [B, T, H] row of token u of chain bh
+        const int b = static_cast<int>(bh) / p.H, h = static_cast<int>(bh) - b * p.H;
+        return (static_cast<size_t>(b) * T + u) * p.H + h;
+    };
+    // RPT consecutive values of a TIn row in shared memory, as fp32
+    auto loadrow = [](const TIn *src, float (&x)[RPT]) {
+#pragma unroll
+        for (int h = 0; h < RPT / 8; ++h) {
+            if constexpr (sizeof(TIn) == 2) {
+                const uint4 w = *reinterpret_cast<const uint4 *>(src + 8 * h);
+                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    x[8 * h + 2 * j] = __uint_as_float(ww[j] << 16);
+                    x[8 * h + 2 * j + 1] = __uint_as_float(ww[j] & 0xffff0000u);
+                }
+            } else {
+                const float4 a = *reinterpret_cast<const float4 *>(src + 8 * h);
+                const float4 b = *reinterpret_cast<const float4 *>(src + 8 * h + 4);
+                x[8 * h] = a.x; x[8 * h + 1] = a.y; x[8 * h + 2] = a.z; x[8 * h + 3] = a.w;
+                x[8 * h + 4] = b.x; x[8 * h + 5] = b.y; x[8 * h + 6] = b.z; x[8 * h + 7] = b.w;
+            }
+        }
+    };
+    auto prefetch = [&](int t, int slot) {
+        int v0;
+        const size_t bh = tile_bh(t, v0);
+        float *sS = reinterpret_cast<float *>(stage(slot, 0));
+        if (p.S0) {
+            const float *Sg = p.S0 + bh * DK * DV + v0;
+            for (int c = tid; c < DK * (BV / 4); c += kThreads) {
+                const int row = c >> 3, ch = c & 7;
+                cp_async16(&sS[row * BV + ch * 4], Sg + static_cast<size_t>(row) * DV + ch * 4);
+            }
+        } else {
+            for (int c = tid; c < DK * (BV / 4); c += kThreads)
+                *reinterpret_cast<float4 *>(&sS[c * 4]) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        constexpr int per16 = 16 / sizeof(TIn);
+        constexpr int nch = DK / per16;                // 16-byte chunks of one k or q row
+        const size_t row0 = row_of(bh, 0);
+        TIn *skq = reinterpret_cast<TIn *>(stage(slot, p.off_kq));
+        for (int c = tid; c < T * 2 * nch; c += kThreads) {
+            const int u = c / (2 * nch), rem = c - u * 2 * nch, which = rem / nch, ch = rem - which * nch;
+            const TIn *src = static_cast<const TIn *>(which ? p.q : p.k) + (row0 + static_cast<size_t>(u) * p.H) * DK + ch * per16;
+            cp_async16(skq + (2 * u + which) * DK + ch * per16, src);
+        }
+        TIn *sv = reinterpret_cast<TIn *>(stage(slot, p.off_v));
+        constexpr int nvc = BV / per16;                // 16-byte chunks of a token's 32 values
+        for (int c = tid; c < T * nvc; c += kThreads) {
+            const int u = c / nvc, ch = c - u * nvc;
+            cp_async16(sv + u * BV + ch * per16,
+                       static_cast<const TIn *>(p.v) + (row0 + static_cast<size_t>(u) * p.H) * DV + v0 + ch * per16);
+        }
+        float *sa = reinterpret_cast<float *>(stage(slot, p.off_a));
+        if (kChannel) {
+            for (int c = tid; c < T * (DK / 4); c += kThreads) {
+                const int u = c / (DK / 4), ch = c - u * (DK / 4);
+                cp_async16(sa + u * DK + ch * 4, p.alpha + (row0 + static_cast<size_t>(u) * p.H) * DK + ch * 4);
+            }
+        } else if (tid < T) {
+            cp_async4(sa + tid, p.alpha + row0 + static_cast<size_t>(tid) * p.H);
+        }
+        float *se = reinterpret_cast<float *>(stage(slot, p.off_e));
+        if (tid >= 32 && tid < 32 + T) cp_async4(se + (tid - 32), p.eta + row0 + static_cast<size_t>(tid - 32) * p.H);
+    };
+
+    int it = 0;
+    if (blockIdx.x < ntiles) prefetch(blockIdx.x, 0);
+    cp_async_commit();
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+        const int slot = it & 1;
+        if (t + static_cast<int>(gridDim.x) < ntiles) prefetch(t + gridDim.x, slot ^ 1);
+        cp_async_commit();
+        cp_async_wait_1();   // this thread's copies of tile t have landed
+        __syncthreads();     // and everyone else's (and the zero fill of a NULL S0)
+        int v0;
+        const size_t bh = tile_bh(t, v0);
+        const float *sS = reinterpret_cast<const float *>(stage(slot, 0));
+        const TIn *skq = reinterpret_cast<const TIn *>(stage(slot, p.off_kq));
+        const TIn *sv = reinterpret_cast<const TIn *>(stage(slot, p.off_v));
+        const float *sa = reinterpret_cast<const float *>(stage(slot, p.off_a));
+        const float *se = reinterpret_cast<const float *>(stage(slot, p.off_e));
+
+        for (int u = warp; u < T; u += kThreads / 32) {   // beta_u and k_u . q_u, one warp per token
+            float kk = 0.f, kq = 0.f;
+#pragma unroll
+            for (int j = 0; j < DK / 32; ++j) {
+                const float kt = to_f32(skq[2 * u * DK + lane + 32 * j]), qt = to_f32(skq[(2 * u + 1) * DK + lane + 32 * j]);
+                kk = fmaf(kt, kt, kk);
+                kq = fmaf(kt, qt, kq);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                kk += __shfl_xor_sync(0xffffffffu, kk, off);
+                kq += __shfl_xor_sync(0xffffffffu, kq, off);
+            }
+            if (lane == 0) {
+                sbeta[u] = kla_beta(se[u], kk, p.eps, p.beta_raw);
+                skqd[u] = kq;
+            }
+        }
+        float2 s[RPT][2];   // this thread's rows, columns (4 cg, 4 cg + 1) and (4 cg + 2, 4 cg + 3)
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            const float4 x = *reinterpret_cast<const float4 *>(&sS[(i0 + r) * BV + cg * 4]);
+            s[r][0] = make_float2(x.x, x.y);
+            s[r][1] = make_float2(x.z, x.w);
+        }
+        __syncthreads();   // beta and k . q of every token are visible
+
+        const size_t row0 = row_of(bh, 0);
+        int par = 0;
+        for (int u = 0; u < T; ++u, par ^= 1) {
+            float kv[RPT], qv[RPT], av[RPT];
+            loadrow(skq + 2 * u * DK + i0, kv);
+            loadrow(skq + (2 * u + 1) * DK + i0, qv);
+            if (kChannel) {
+#pragma unroll
+                for (int j = 0; j < RPT / 4; ++j) {
+                    const float4 x = *reinterpret_cast<const float4 *>(sa + u * DK + i0 + 4 * j);
+                    av[4 * j] = x.x; av[4 * j + 1] = x.y; av[4 * j + 2] = x.z; av[4 * j + 3] = x.w;
+                }
+            }
+            // scalar gate: S~^T k = alpha (S^T k), applied after the reduction; paired fp32 FMAs
+            float2 pk0 = make_float2(0.f, 0.f), pk1 = pk0, pq0 = pk0, pq1 = pk0;
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) {
+                const float ak = kChannel ? av[r] * kv[r] : kv[r], aq = kChannel ? av[r] * qv[r] : qv[r];
+                const float2 kk2 = make_float2(ak, ak), qq2 = make_float2(aq, aq);
+                pk0 = __ffma2_rn(kk2, s[r][0], pk0); pk1 = __ffma2_rn(kk2, s[r][1], pk1);
+                pq0 = __ffma2_rn(qq2, s[r][0], pq0); pq1 = __ffma2_rn(qq2, s[r][1], pq1);
+            }
+            float4 pk = make_float4(pk0.x, pk0.y, pk1.x, pk1.y), pq = make_float4(pq0.x, pq0.y, pq1.x, pq1.y);
+#pragma unroll
+            for (int off = NCG; off < 32; off <<= 1) {
+                pk.x += __shfl_xor_sync(0xffffffffu, pk.x, off); pk.y += __shfl_xor_sync(0xffffffffu, pk.y, off);
+                pk.z += __shfl_xor_sync(0xffffffffu, pk.z, off); pk.w += __shfl_xor_sync(0xffffffffu, pk.w, off);
+                pq.x += __shfl_xor_sync(0xffffffffu, pq.x, off); pq.y += __shfl_xor_sync(0xffffffffu, pq.y, off);
+                pq.z += __shfl_xor_sync(0xffffffffu, pq.z, off); pq.w += __shfl_xor_sync(0xffffffffu, pq.w, off);
+            }
+            if (lane < NCG) {
+                *reinterpret_cast<float4 *>(&sred[par][warp][lane * 4]) = pk;
+                *reinterpret_cast<float4 *>(&sred[par][warp][NCG * 4 + lane * 4]) = pq;
+            }
+            __syncthreads();   // the partial sums of token u (the other parity is token u +- 1's)
+            float4 pred = make_float4(0.f, 0.f, 0.f, 0.f), rd = pred;
+#pragma unroll
+            for (int w = 0; w < kThreads / 32; ++w) {
+                const float4 x = *reinterpret_cast<const float4 *>(&sred[par][w][cg * 4]);
+                const float4 y = *reinterpret_cast<const float4 *>(&sred[par][w][NCG * 4 + cg * 4]);
+                pred.x += x.x; pred.y += x.y; pred.z += x.z; pred.w += x.w;
+                rd.x += y.x; rd.y += y.y; rd.z += y.z; rd.w += y.w;
+            }
+            const float a_scalar = kChannel ? 1.f : sa[u];
+            if (!kChannel) {
+                pred.x *= a_scalar; pred.y *= a_scalar; pred.z *= a_scalar; pred.w *= a_scalar;
+                rd.x *= a_scalar; rd.y *= a_scalar; rd.z *= a_scalar; rd.w *= a_scalar;
+            }
+            const TIn *vv = sv + u * BV + cg * 4;
+            float4 e;
+            e.x = to_f32(vv[0]) - pred.x; e.y = to_f32(vv[1]) - pred.y;
+            e.z = to_f32(vv[2]) - pred.z; e.w = to_f32(vv[3]) - pred.w;
+            const float beta = sbeta[u];
+            if (i0 == 0) {   // o = s (S~^T q + beta e (k . q))
+                TIn *o = static_cast<TIn *>(p.o) + (row0 + static_cast<size_t>(u) * p.H) * DV + v0 + cg * 4;
+                const float bkq = beta * skqd[u], sc = p.q_scale;
+                o[0] = from_f32<TIn>(sc * fmaf(bkq, e.x, rd.x));
+                o[1] = from_f32<TIn>(sc * fmaf(bkq, e.y, rd.y));
+                o[2] = from_f32<TIn>(sc * fmaf(bkq, e.z, rd.z));
+                o[3] = from_f32<TIn>(sc * fmaf(bkq, e.w, rd.w));
+            }
+            const float2 be01 = make_float2(beta * e.x, beta * e.y), be23 = make_float2(beta * e.z, beta * e.w);
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) {   // S = S~ + k (beta e)^T
+                const float a = kChannel ? av[r] : a_scalar;
+                const float2 a2 = make_float2(a, a), k2 = make_float2(kv[r], kv[r]);
+                s[r][0] = __ffma2_rn(a2, s[r][0], __fmul2_rn(k2, be01));
+                s[r][1] = __ffma2_rn(a2, s[r][1], __fmul2_rn(k2, be23));
+            }
+        }
+        if (p.S_T) {
+            float *Sbh = p.S_T + bh * DK * DV;
+#pragma unroll
+            for (int r = 0; r < RPT; ++r)
+                *reinterpret_cast<float4 *>(Sbh + static_cast<size_t>(i0 + r) * DV + v0 + cg * 4) =
+                    make_float4(s[r][0].x, s[r][0].y, s[r][1].x, s[r][1].y);
+        }
+        __syncthreads();   // the slot, beta and k . q are rewritten for the next tile
+    }
+}
+
+TokParams tok_params(const ChunkArgs &a) {
+    const int esz = a.dtype == KLA_DTYPE_BF16 ? 2 : 4;
+    auto up16 = [](int x) { return (x + 15) & ~15; };
+    TokParams p{a.q, a.k, a.v, a.alpha, a.eta, a.eps, a.S0, a.S_T, a.o, a.B, a.T, a.H, a.d_k, a.d_v,
+                a.beta_raw, a.q_scale, 0, 0, 0, 0, 0};
+    p.off_kq = a.d_k * 32 * 4;
+    p.off_v = up16(p.off_kq + a.T * 2 * a.d_k * esz);
+    p.off_a = up16(p.off_v + a.T * 32 * esz);
+    p.off_e = up16(p.off_a + a.T * (a.gate == KLA_GATE_CHANNEL ? a.d_k : 1) * 4);
+    p.stage_bytes = up16(p.off_e + a.T * 4);
+    return p;
+}
+
+template <typename TIn, bool kChannel>
+cudaError_t launch_tokens_t(const ChunkArgs &a) {
+    // Looked up once per device (and token count): the shared-memory limit (set for the largest
+    // stage, T = kShortSeqMaxT and d_k = 128), the SM count and the resident CTAs per SM, so a
+    // launch costs no more host time than the single-token step's.
+    static bool attr_set[64] = {};
+    static int sms_of[64] = {};
+    static int per_sm[64][kShortSeqMaxT + 1] = {};
+    const TokParams p = tok_params(a);
+    const int smem = 2 * p.stage_bytes;
+    auto kern = tokens_pipe_kernel<TIn, kChannel>;
+    constexpr int kThreads = kTokThreads;
+    int dev = 0;
+    cudaError_t e;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        ChunkArgs big = a;
+        big.T = kShortSeqMaxT;
+        big.d_k = 128;
+        const int max_smem = 2 * tok_params(big).stage_bytes;
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem)) != cudaSuccess)
+            return e;
+        attr_set[dev] = true;
+    }
+    if (sms_of[dev] == 0 &&
+        (e = cudaDeviceGetAttribute(&sms_of[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
+    int &n = per_sm[dev][a.T];
+    if (n == 0) {
+        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, smem)) != cudaSuccess) return e;
+        n = std::max(1, n);
+    }
+    const int ntiles = (a.d_v / 32) * a.H * a.B;
+    const int grid = std::min(ntiles, n * sms_of[dev]);
+    kern<<<grid, kThreads, smem, a.stream>>>(p, ntiles);
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+bool tokens_pipe_supports(const ChunkArgs &a) {
+    auto al = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; };
+    return a.T >= 1 && a.T <= kShortSeqMaxT && a.d_v % 32 == 0 && a.d_k == 128 &&
+           al(a.q) && al(a.k) && al(a.v) && (!a.S0 || al(a.S0)) && (!a.S_T || al(a.S_T)) &&
+           (a.gate == KLA_GATE_SCALAR || al(a.alpha));
+}
+
+cudaError_t launch_tokens_pipe(const ChunkArgs &a) {
+    const bool ch = a.gate == KLA_GATE_CHANNEL;
+    if (a.dtype == KLA_DTYPE_BF16)
+        return ch ? launch_tokens_t<__nv_bfloat16, true>(a) : launch_tokens_t<__nv_bfloat16, false>(a);
+    return ch ? launch_tokens_t<float, true>(a) : launch_tokens_t<float, false>(a);
+}
 
 cudaError_t launch_decode(const DecodeArgs &a) {
     const bool ch = a.gate == KLA_GATE_CHANNEL;

@@ -145,3 +145,39 @@ def test_full_config_sampled(name, nchains):
     chains = sample_chains(inp.wl.B, inp.wl.H, nchains, seed=5)
     ref = run_oracle(inp, dO, dST, chains)
     compare(pick(got, chains), ref, tol(inp.wl))
+
+
+def test_chunked_backward_is_deterministic():
+    """The chunkwise path sums in a fixed order (no atomics): two calls agree bit for bit."""
+    inp = synth.make_prefill("gdn4k", seed=11, B=2, T=150, H=2, s0_sigma=0.05)
+    dO, dST = _grad_inputs(inp, seed=12, with_dst=True)
+    a = run_gpu(inp, dO, dST)
+    b = run_gpu(inp, dO, dST)
+    for n in NAMES:
+        assert np.array_equal(a[n], b[n]), n
+
+
+def test_unaligned_inputs_take_the_token_path():
+    """q, k, v, dO views that start 2 bytes past a 16-byte boundary are valid bf16 arguments; the
+    chunkwise path needs 16-byte rows, so they run the token-by-token fp32 backward and meet its
+    1e-4 bar."""
+    import torch
+
+    import gated_delta_rule_14_gb300 as kla
+    inp = synth.make_prefill("gdn4k", seed=13, B=1, T=70, H=2, s0_sigma=0.05)
+    dO, dST = _grad_inputs(inp, seed=14, with_dst=True)
+
+    def shifted(a):
+        t = to_dev(a)
+        buf = torch.empty(t.numel() + 8, dtype=t.dtype, device=DEV)
+        view = buf[1:1 + t.numel()].view(t.shape)
+        view.copy_(t)
+        assert view.data_ptr() % 16 == 2
+        return view
+    g = kla.chunk_bwd(shifted(inp.q), shifted(inp.k), shifted(inp.v), to_dev(inp.alpha), to_dev(inp.eta), shifted(dO),
+                      inp.wl.eps, to_dev(inp.S0), to_dev(dST))
+    kla.device_status(DEV)
+    got = {n: g[n].cpu().numpy().astype(np.float64) for n in NAMES}
+    ref = run_oracle(inp, dO, dST)
+    chains = [(b, h) for b in range(inp.wl.B) for h in range(inp.wl.H)]
+    compare(pick(got, chains), ref, TOL["bf16"])
