@@ -15,8 +15,8 @@ Extras in the same JSON line: long131k prefill (B=1 H=16 T=131072), kda8k prefil
 (per-key-channel gate, B=4 H=16 T=8192), decode (batch 64, H16, 1024 single-token
 steps, L2 flushed before every step), decode_graph (the same steps as one CUDA graph, L2 not
 flushed), verify4 (the decode batch advanced 4 tokens per
-call, as in speculative verification) and bwd_gdn4k (the backward pass of the headline
-workload), each with its own roofline.
+call, as in speculative verification), bwd_gdn4k and bwd_long131k (the backward passes of
+the headline and the long-context workloads), each with its own roofline.
 
 --impl reference times the fp64 CPU oracle on the host cores on a bounded sample of the
 same workload (whole sequences of some (b, h) chains) and reports the same metric.
@@ -345,6 +345,8 @@ BWD_BYTES_PER_TOKEN_HEAD = 4 * 2 * 128 + 8 + 3 * 4 * 128 + 8   # q, k, v, dO in;
 
 
 BWD_KERNELS_PER_CALL = 4   # chunkwise path: prep, forward carry, reverse carry, gradients
+# long131k: prep, 2 x (value runs, transitions, combine, reruns), gradients
+BWD_LONG_KERNELS_PER_CALL = 10
 
 
 def bench_bwd(name, steps, seed, dev, flush, stream, pk, **override):
@@ -357,7 +359,8 @@ def bench_bwd(name, steps, seed, dev, flush, stream, pk, **override):
     g = torch.Generator(device=dev)
     g.manual_seed(seed)
     dO = torch.randn((wl.B, wl.T, wl.H, wl.d_v), device=dev, generator=g).to(torch.bfloat16)
-    ws = torch.empty(kla.bwd_workspace_size(wl.B, wl.T, wl.H, wl.d_k, wl.d_v), dtype=torch.uint8, device=dev)
+    ws = torch.empty(kla.bwd_workspace_size(wl.B, wl.T, wl.H, wl.d_k, wl.d_v, torch.bfloat16), dtype=torch.uint8,
+                     device=dev)
 
     def step():
         kla.chunk_bwd(d["q"], d["k"], d["v"], d["alpha"], d["eta"], dO, wl.eps, workspace=ws, want_dS0=False)
@@ -578,6 +581,13 @@ def main():
             extras["bwd_gdn4k"] = bench_bwd("gdn4k", 3, seed=rank, dev=dev, flush=flush, stream=stream, pk=pk)
             clocks.mark(t0, time.time())
             launches += 3 * BWD_KERNELS_PER_CALL
+            torch.cuda.empty_cache()
+            t0 = time.time()
+            extras["bwd_long131k"] = bench_bwd("long131k", 3, seed=rank, dev=dev, flush=flush, stream=stream, pk=pk)
+            extras["bwd_long131k"]["note"] = ("chunkwise backward with the chunk-state carries split into "
+                                              "segments run in parallel (16 chains of 2048 chunks)")
+            clocks.mark(t0, time.time())
+            launches += 3 * BWD_LONG_KERNELS_PER_CALL
             torch.cuda.empty_cache()
     clk = clocks.stop()
 

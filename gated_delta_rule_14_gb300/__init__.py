@@ -208,9 +208,16 @@ def host_buffers(q: torch.Tensor, v: torch.Tensor, alpha: torch.Tensor, *, devic
     return b
 
 
-def bwd_workspace_size(B: int, T: int, H: int, d_k: int, d_v: int) -> int:
-    """Device scratch bytes ``chunk_bwd`` needs for these sizes."""
-    return int(_native.lib().kla_chunk_bwd_workspace_size(B, T, H, d_k, d_v))
+def bwd_workspace_size(B: int, T: int, H: int, d_k: int, d_v: int, dtype: Optional[torch.dtype] = None,
+                       per_channel_gate: bool = False) -> int:
+    """Device scratch bytes ``chunk_bwd`` needs for these sizes: enough for either backward path,
+    or, given the input dtype (and the gate), the need of the path that 16-byte aligned inputs
+    take."""
+    if dtype is None:
+        return int(_native.lib().kla_chunk_bwd_workspace_size(B, T, H, d_k, d_v))
+    dcode = _native.KLA_DTYPE_BF16 if dtype == torch.bfloat16 else _native.KLA_DTYPE_F32
+    gcode = _native.KLA_GATE_CHANNEL if per_channel_gate else _native.KLA_GATE_SCALAR
+    return int(_native.lib().kla_chunk_bwd_workspace_size_ex(B, T, H, d_k, d_v, dcode, gcode))
 
 
 def chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, alpha: torch.Tensor, eta: torch.Tensor,
@@ -253,7 +260,9 @@ def chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, alpha: torch.Te
          "dv": torch.empty((B, T, H, d_v), **f32), "dalpha": torch.empty(alpha.shape, **f32),
          "deta": torch.empty((B, T, H), **f32),
          "dS0": torch.empty((B, H, d_k, d_v), **f32) if want_dS0 else None}
-    need = bwd_workspace_size(B, T, H, d_k, d_v)
+    aligned = all(t.data_ptr() % 16 == 0 for t in (q, k, v, dO))
+    need = (bwd_workspace_size(B, T, H, d_k, d_v, q.dtype, gate == _native.KLA_GATE_CHANNEL) if aligned
+            else bwd_workspace_size(B, T, H, d_k, d_v))
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()

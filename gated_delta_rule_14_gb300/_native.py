@@ -63,6 +63,8 @@ def _declare(lib):
     lib.kla_chunk_bwd.restype = ctypes.c_int
     lib.kla_chunk_bwd_workspace_size.argtypes = [i, i, i, i, i]
     lib.kla_chunk_bwd_workspace_size.restype = sz
+    lib.kla_chunk_bwd_workspace_size_ex.argtypes = [i, i, i, i, i, i, i]
+    lib.kla_chunk_bwd_workspace_size_ex.restype = sz
     lib.kla_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
     lib.kla_selftest_wait_timeout.restype = ctypes.c_int
     lib.kla_device_status.argtypes = [vp]

@@ -11,6 +11,11 @@ cudaError_t launch_selftest_wait(unsigned *err, unsigned limit, cudaStream_t str
 // d_k = 128, d_v a multiple of 32, 16-byte aligned q, k, v, states and per-channel gates
 bool tokens_pipe_supports(const ChunkArgs &a);
 cudaError_t launch_tokens_pipe(const ChunkArgs &a);
+// backward paths: the chunkwise one (kla_bwd_chunk.cu) runs when it supports the call, with a
+// workspace of its own size; the token-sequential one (kla_bwd.cu) otherwise
+bool bwd_chunk_supports(const BwdArgs &a);
+size_t bwd_chunk_workspace_bytes(int B, int T, int H);
+size_t bwd_seq_workspace_bytes(int B, int T, int H, int d_k, int d_v);
 }  // namespace kla
 
 namespace {
@@ -81,7 +86,7 @@ bool overlaps(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi; }
 
 extern "C" {
 
-int kla_abi_version(void) { return 101; }
+int kla_abi_version(void) { return 102; }
 
 const char *kla_status_string(kla_status s) {
     switch (s) {
@@ -220,6 +225,12 @@ size_t kla_chunk_bwd_workspace_size(int B, int T, int H, int d_k, int d_v) {
     return kla::bwd_workspace_bytes(B, T, H, d_k, d_v);
 }
 
+size_t kla_chunk_bwd_workspace_size_ex(int B, int T, int H, int d_k, int d_v, kla_dtype dtype, kla_gate gate) {
+    const bool chunked = dtype == KLA_DTYPE_BF16 && gate == KLA_GATE_SCALAR && d_k == 128 && d_v == 128 &&
+                         T > kla::kShortSeqMaxT && B >= 1 && H >= 1;
+    return chunked ? kla::bwd_chunk_workspace_bytes(B, T, H) : kla::bwd_seq_workspace_bytes(B, T, H, d_k, d_v);
+}
+
 kla_status kla_chunk_bwd(const void *q, const void *k, const void *v, const float *alpha, const float *eta,
                          float eps, const float *S0, const void *dO, const float *dS_T, float *dq, float *dk,
                          float *dv, float *dalpha, float *deta, float *dS0, int B, int T, int H, int d_k, int d_v,
@@ -235,7 +246,12 @@ kla_status kla_chunk_bwd(const void *q, const void *k, const void *v, const floa
         return KLA_ERR_INVALID_ARG;
     if ((S0 && !aligned16(S0)) || (dS_T && !aligned16(dS_T)) || (dS0 && !aligned16(dS0))) return KLA_ERR_INVALID_ARG;
     if (!(eps == eps)) return KLA_ERR_INVALID_ARG;
-    const size_t need = kla::bwd_workspace_bytes(B, T, H, d_k, d_v);
+    kla::BwdArgs a{q, k, v, dO, alpha, eta, eps, S0, dS_T, dq, dk, dv, dalpha, deta, dS0, B, T, H, d_k, d_v,
+                   dtype, gate, beta_mode == KLA_BETA_RAW, q_scale, workspace, workspace_bytes,
+                   static_cast<cudaStream_t>(stream)};
+    // the chunkwise path needs its own (smaller) workspace; any other call the token-sequential one's
+    const size_t need = T > 0 && kla::bwd_chunk_supports(a) ? kla::bwd_chunk_workspace_bytes(B, T, H)
+                                                            : kla::bwd_seq_workspace_bytes(B, T, H, d_k, d_v);
     if (workspace_bytes < need || (need > 0 && (!workspace || !aligned16(workspace)))) return KLA_ERR_INVALID_ARG;
 
     const size_t esz = dtype == KLA_DTYPE_BF16 ? 2 : 4;
@@ -262,8 +278,6 @@ kla_status kla_chunk_bwd(const void *q, const void *k, const void *v, const floa
                              : cudaMemsetAsync(dS0, 0, sbytes, cs);
         return e == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
     }
-    kla::BwdArgs a{q, k, v, dO, alpha, eta, eps, S0, dS_T, dq, dk, dv, dalpha, deta, dS0, B, T, H, d_k, d_v,
-                   dtype, gate, beta_mode == KLA_BETA_RAW, q_scale, workspace, workspace_bytes, cs};
     return kla::launch_bwd(a) == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
 }
 

@@ -460,12 +460,15 @@ bool bwd_chunk_supports(const BwdArgs &a);
 size_t bwd_chunk_workspace_bytes(int B, int T, int H);
 cudaError_t launch_bwd_chunk(const BwdArgs &a);
 
-size_t bwd_workspace_bytes(int B, int T, int H, int d_k, int d_v) {
+size_t bwd_seq_workspace_bytes(int B, int T, int H, int d_k, int d_v) {
     if (B < 1 || H < 1 || T < 1) return 0;
     const size_t nblk = (static_cast<size_t>(T) + kBlk - 1) / kBlk;
-    const size_t seq =
-        (static_cast<size_t>(B) * H * nblk * d_k * d_v + static_cast<size_t>(B) * T * H * d_v) * sizeof(float);
-    return d_k == 128 && d_v == 128 ? std::max(seq, bwd_chunk_workspace_bytes(B, T, H)) : seq;
+    return (static_cast<size_t>(B) * H * nblk * d_k * d_v + static_cast<size_t>(B) * T * H * d_v) * sizeof(float);
+}
+
+size_t bwd_workspace_bytes(int B, int T, int H, int d_k, int d_v) {   // either path
+    const size_t seq = bwd_seq_workspace_bytes(B, T, H, d_k, d_v);
+    return d_k == 128 && d_v == 128 && T > kShortSeqMaxT ? std::max(seq, bwd_chunk_workspace_bytes(B, T, H)) : seq;
 }
 
 cudaError_t launch_bwd(const BwdArgs &a) {

@@ -70,6 +70,7 @@ struct Ws {
     bf16 *S;          // [N][128][128] state entering the chunk
     bf16 *E;          // [N][64][128]
     bf16 *dS;         // [N][128][128] dL/d(state leaving the chunk)
+    float *seg;       // long chains split into segments: Z | M | start states, each [chains][nseg][128][128]
 };
 size_t ws_bytes_per_chunk() {
     return kCgFloats * 4 + 2 * (3 * kC * kD + 2 * kC * kC + 2 * kD * kD);
@@ -84,8 +85,41 @@ Ws carve(void *base, size_t N) {
     w.A = reinterpret_cast<bf16 *>(p);               p += N * kC * kC * 2;
     w.Tm = reinterpret_cast<bf16 *>(p);              p += N * kC * kC * 2;
     w.S = reinterpret_cast<bf16 *>(p);               p += N * kD * kD * 2;
-    w.dS = reinterpret_cast<bf16 *>(p);
+    w.dS = reinterpret_cast<bf16 *>(p);              p += N * kD * kD * 2;
+    w.seg = reinterpret_cast<float *>(p);
     return w;
+}
+
+// Segments for the two carries of a long chain (the forward prefill's sequence-parallel scan,
+// applied to them): both carries are affine in their state, X_end = M X_start + Z over a
+// segment. Cost model in chunk-steps, one CTA per SM: pass 1 runs the value runs of segments
+// 0..n-2 and the transitions of 1..n-2, pass 3 reruns 1..n-1; split only when it saves a fifth.
+struct CarryPlan {
+    int nseg, seg_len;   // seg_len in chunks
+};
+CarryPlan carry_plan(int chains, int nc) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess || sms <= 0)
+        return {1, nc};
+    auto waves = [&](long ctas) { return (ctas + sms - 1) / sms; };
+    double best = 0.8 * static_cast<double>(waves(chains)) * nc;
+    int best_n = 1;
+    for (int n = 2; n <= 64; ++n) {
+        const int L = (nc + n - 1) / n;
+        if (L < 8) break;
+        const int nn = (nc + L - 1) / L;
+        if (nn < 2) continue;
+        const double cost = static_cast<double>(waves(static_cast<long>(chains) * (2 * nn - 3)) +
+                                                waves(static_cast<long>(chains) * (nn - 1))) * L;
+        if (cost < best) {
+            best = cost;
+            best_n = n;
+        }
+    }
+    if (best_n <= 1) return {1, nc};
+    const int L = (nc + best_n - 1) / best_n;
+    return {(nc + L - 1) / L, L};
 }
 
 // ---------------------------------------------------------------- warp-level MMA helpers
@@ -482,6 +516,21 @@ struct ScanParams {
     float q_scale;
     int B, T, H, nc;
     Ws ws;
+    // Segments (a long chain split for a sequence-parallel scan; one segment = the whole chain
+    // otherwise). Segment r in processing order covers chunks [s L, min((s + 1) L, nc)) with
+    // s = r (forward) or s = nseg - 1 - r (reverse). A launch runs segments seg_begin ..
+    // seg_begin + seg_count - 1 of every chain, one CTA each.
+    int seg_len, seg_begin, seg_count, nseg;
+    int x0_mode;          // kX0Chain, kX0Identity or kX0Given
+    int drive;            // 0: drop U (forward) or the dO terms (reverse): the linear part only
+    int records;          // per-chunk records (S_c, E_c or dS_{c+1}, dE_c): 0 none, 1 all, 2 segment r = 0 only
+    float *Xseg;          // NULL, or [chains][nseg][128][128]: X at the end of each segment
+    const float *Xst;     // kX0Given: [chains][nseg][128][128] start states
+};
+enum : int {
+    kX0Chain = 0,      // X0 for the chain's first segment (r = 0), zeros for the others
+    kX0Identity = 1,   // the identity (the segment's transition)
+    kX0Given = 2,      // Xst[chain][r]
 };
 constexpr int kScanThreads = 512;
 constexpr int SC_K = 0, SC_W = SC_K + kTileTok, SC_UQ = SC_W + kTileTok;   // U (forward) or Q (reverse)
@@ -497,8 +546,14 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(ScanParams 
     bf16 *sX = reinterpret_cast<bf16 *>(smem + SC_X), *sM = reinterpret_cast<bf16 *>(smem + SC_M);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, q4 = lane & 3;
-    const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
+    const int bh = blockIdx.x / p.seg_count, r = p.seg_begin + blockIdx.x % p.seg_count;
+    const int b = bh / p.H, h = bh % p.H;
     const size_t rs = static_cast<size_t>(p.H) * kD;
+    const int sidx = kRev ? p.nseg - 1 - r : r;   // segment index in time
+    const int c_lo = sidx * p.seg_len, c_hi = min((sidx + 1) * p.seg_len, p.nc) - 1;
+    const int steps = c_hi - c_lo + 1;
+    if (steps <= 0) return;
+    const bool rec = p.records == 1 || (p.records == 2 && r == 0);
 
     auto stage = [&](int buf, int off) { return reinterpret_cast<bf16 *>(smem + buf * SC_STAGE + off); };
     auto issue = [&](int c, int buf) {
@@ -507,12 +562,14 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(ScanParams 
         const size_t n = static_cast<size_t>(bh) * p.nc + c;
         load_tok(stage(buf, SC_K), p.k + base, rs, L, tid, kScanThreads);
         load_dense<kD>(stage(buf, SC_W), p.ws.W + n * kC * kD, kC, tid, kScanThreads);
-        if (kRev) {
-            load_tok(stage(buf, SC_UQ), p.q + base, rs, L, tid, kScanThreads);
-            load_tok(stage(buf, SC_DO), p.dO + base, rs, L, tid, kScanThreads);
-            load_dense<kC>(stage(buf, SC_A), p.ws.A + n * kC * kC, kC, tid, kScanThreads);
-        } else {
-            load_dense<kD>(stage(buf, SC_UQ), p.ws.UdE + n * kC * kD, kC, tid, kScanThreads);
+        if (p.drive) {
+            if (kRev) {
+                load_tok(stage(buf, SC_UQ), p.q + base, rs, L, tid, kScanThreads);
+                load_tok(stage(buf, SC_DO), p.dO + base, rs, L, tid, kScanThreads);
+                load_dense<kC>(stage(buf, SC_A), p.ws.A + n * kC * kC, kC, tid, kScanThreads);
+            } else {
+                load_dense<kD>(stage(buf, SC_UQ), p.ws.UdE + n * kC * kD, kC, tid, kScanThreads);
+            }
         }
         if (tid < static_cast<int>(kCgFloats) / 4)
             cp16(smem + buf * SC_STAGE + SC_CG + 16 * tid, p.ws.cg + n * kCgFloats + 4 * tid, true);
@@ -527,10 +584,15 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(ScanParams 
         for (int ni = 0; ni < 4; ++ni)
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
+                const int row = xr0 + 16 * mi + g + 8 * hh, col = xc0 + 8 * ni + 2 * q4;
                 float2 x = make_float2(0.f, 0.f);
-                if (p.X0)
-                    x = *reinterpret_cast<const float2 *>(p.X0 + (static_cast<size_t>(bh) * kD + xr0 + 16 * mi + g + 8 * hh) * kD +
-                                                          xc0 + 8 * ni + 2 * q4);
+                if (p.x0_mode == kX0Identity) {
+                    x = make_float2(row == col ? 1.f : 0.f, row == col + 1 ? 1.f : 0.f);
+                } else if (p.x0_mode == kX0Given) {
+                    x = *reinterpret_cast<const float2 *>(p.Xst + ((static_cast<size_t>(bh) * p.nseg + r) * kD + row) * kD + col);
+                } else if (p.X0 && r == 0) {
+                    x = *reinterpret_cast<const float2 *>(p.X0 + (static_cast<size_t>(bh) * kD + row) * kD + col);
+                }
                 X[mi][ni][2 * hh] = x.x;
                 X[mi][ni][2 * hh + 1] = x.y;
             }
@@ -545,35 +607,35 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(ScanParams 
                             X[mi][ni][2 * hh + 1]);
     };
     put_x();
-    issue(kRev ? p.nc - 1 : 0, 0);
+    issue(kRev ? c_hi : c_lo, 0);
     cp_commit();
 
     const int m0 = 16 * (warp & 3), n0 = 32 * (warp >> 2);   // this warp's block of the 64 x 128 step
-    for (int it = 0; it < p.nc; ++it) {
-        const int c = kRev ? p.nc - 1 - it : it, buf = it & 1;
+    for (int it = 0; it < steps; ++it) {
+        const int c = kRev ? c_hi - it : c_lo + it, buf = it & 1;
         const size_t n = static_cast<size_t>(bh) * p.nc + c;
         cp_wait<0>();
         __syncthreads();   // chunk c's tiles and X (bf16) are visible; every read of buf ^ 1 is done
-        if (it + 1 < p.nc) issue(kRev ? c - 1 : c + 1, buf ^ 1);
+        if (it + 1 < steps) issue(kRev ? c - 1 : c + 1, buf ^ 1);
         cp_commit();
         const float *cg = reinterpret_cast<const float *>(smem + buf * SC_STAGE + SC_CG);
         const float Gend = cg[kC - 1], Gam = __expf(Gend);
-        if (kRev) {   // Q <- s diag(gamma) Q, in place (read only by the second product)
+        if (kRev && p.drive) {   // Q <- s diag(gamma) Q, in place (read only by the second product)
             bf16 *sQ = stage(buf, SC_UQ);
             for (int i = tid; i < kC * 16; i += kScanThreads) {
-                const int r = i >> 4, cc = (i & 15) * 8;
-                const float f = p.q_scale * __expf(cg[r]);
-                uint4 u = *reinterpret_cast<uint4 *>(sQ + r * kP + cc);
+                const int tr = i >> 4, cc = (i & 15) * 8;
+                const float f = p.q_scale * __expf(cg[tr]);
+                uint4 u = *reinterpret_cast<uint4 *>(sQ + tr * kP + cc);
                 uint32_t *w = reinterpret_cast<uint32_t *>(&u);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float2 x = unpack2(w[e]);
                     w[e] = pack2(f * x.x, f * x.y);
                 }
-                *reinterpret_cast<uint4 *>(sQ + r * kP + cc) = u;
+                *reinterpret_cast<uint4 *>(sQ + tr * kP + cc) = u;
             }
         }
-        store_dense<kD>((kRev ? p.ws.dS : p.ws.S) + n * kD * kD, sX, kD, tid, kScanThreads);
+        if (rec) store_dense<kD>((kRev ? p.ws.dS : p.ws.S) + n * kD * kD, sX, kD, tid, kScanThreads);
 
         // the 64 x 128 step: E (forward) or dE (reverse)
         float acc[1][4][4];
@@ -582,15 +644,16 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(ScanParams 
         float acc2[1][4][4];
         if (kRev) {
             zero(acc2[0]);
-            gemm_m<1, 4, 4, true, true>(acc2, sptr(stage(buf, SC_A)), kPs, m0, 0, sptr(stage(buf, SC_DO)), kP, n0, 0,
-                                        lane);
+            if (p.drive)
+                gemm_m<1, 4, 4, true, true>(acc2, sptr(stage(buf, SC_A)), kPs, m0, 0, sptr(stage(buf, SC_DO)), kP, n0,
+                                            0, lane);
         }
         bf16 *Mout = (kRev ? p.ws.UdE : p.ws.E) + n * kC * kD;
         const bf16 *sU = stage(buf, SC_UQ);
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-            const int r = m0 + g + 8 * hh;
-            const float ee = __expf(Gend - cg[r]);
+            const int rw = m0 + g + 8 * hh;
+            const float ee = __expf(Gend - cg[rw]);
 #pragma unroll
             for (int ni = 0; ni < 4; ++ni) {
                 const int col = n0 + 8 * ni + 2 * q4;
@@ -599,13 +662,13 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(ScanParams 
                     m0v = fmaf(ee, acc[0][ni][2 * hh], p.q_scale * acc2[0][ni][2 * hh]);
                     m1v = fmaf(ee, acc[0][ni][2 * hh + 1], p.q_scale * acc2[0][ni][2 * hh + 1]);
                 } else {
-                    const float2 u = ld_pair(sU, kP, r, col);
+                    const float2 u = p.drive ? ld_pair(sU, kP, rw, col) : make_float2(0.f, 0.f);
                     m0v = u.x - acc[0][ni][2 * hh];
                     m1v = u.y - acc[0][ni][2 * hh + 1];
                 }
-                *reinterpret_cast<uint32_t *>(Mout + r * kD + col) = pack2(m0v, m1v);
-                if (kRev) st_pair(sM, kP, r, col, -m0v, -m1v);
-                else st_pair(sM, kP, r, col, ee * m0v, ee * m1v);
+                if (rec) *reinterpret_cast<uint32_t *>(Mout + rw * kD + col) = pack2(m0v, m1v);
+                if (kRev) st_pair(sM, kP, rw, col, -m0v, -m1v);
+                else st_pair(sM, kP, rw, col, ee * m0v, ee * m1v);
             }
         }
         __syncthreads();   // sM and the scaled Q are visible
@@ -618,25 +681,28 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(ScanParams 
 #pragma unroll
                 for (int e = 0; e < 4; ++e) X[mi][ni][e] *= Gam;
         if (kRev) {
-            gemm_m<2, 4, 4, true, true>(X, sptr(stage(buf, SC_UQ)), kP, xr0, 0, sptr(stage(buf, SC_DO)), kP, xc0, 0,
-                                        lane);
+            if (p.drive)
+                gemm_m<2, 4, 4, true, true>(X, sptr(stage(buf, SC_UQ)), kP, xr0, 0, sptr(stage(buf, SC_DO)), kP, xc0,
+                                            0, lane);
             gemm_m<2, 4, 4, true, true>(X, sptr(stage(buf, SC_W)), kP, xr0, 0, sptr(sM), kP, xc0, 0, lane);
         } else {
             gemm_m<2, 4, 4, true, true>(X, sptr(stage(buf, SC_K)), kP, xr0, 0, sptr(sM), kP, xc0, 0, lane);
         }
         put_x();   // read by the next step after its barrier (every read of sX in this step is done)
     }
-    if (kRev && p.X_end) {
+    // the end state of the segment; in reverse, the segment holding chunk 0 ends in dL/dS0
+    auto put_end = [&](float *dst) {
 #pragma unroll
         for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
             for (int ni = 0; ni < 4; ++ni)
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh)
-                    *reinterpret_cast<float2 *>(p.X_end + (static_cast<size_t>(bh) * kD + xr0 + 16 * mi + g + 8 * hh) * kD +
-                                                xc0 + 8 * ni + 2 * q4) =
+                    *reinterpret_cast<float2 *>(dst + (xr0 + 16 * mi + g + 8 * hh) * kD + xc0 + 8 * ni + 2 * q4) =
                         make_float2(X[mi][ni][2 * hh], X[mi][ni][2 * hh + 1]);
-    }
+    };
+    if (p.Xseg) put_end(p.Xseg + (static_cast<size_t>(bh) * p.nseg + r) * kD * kD);
+    if (kRev && p.X_end && c_lo == 0) put_end(p.X_end + static_cast<size_t>(bh) * kD * kD);
 }
 
 // ============================================================== kernel 3: gradients of a chunk
@@ -1081,8 +1147,10 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_kernel(GradParams p)
 
 size_t bwd_chunk_workspace_bytes(int B, int T, int H) {
     if (B < 1 || T < 1 || H < 1) return 0;
-    const size_t nc = (static_cast<size_t>(T) + kC - 1) / kC;
-    return static_cast<size_t>(B) * H * nc * ws_bytes_per_chunk();
+    const size_t nc = (static_cast<size_t>(T) + kC - 1) / kC, chains = static_cast<size_t>(B) * H;
+    const CarryPlan pl = carry_plan(B * H, static_cast<int>(nc));
+    const size_t seg = pl.nseg > 1 ? 3 * chains * pl.nseg * kD * kD * sizeof(float) : 0;
+    return chains * nc * ws_bytes_per_chunk() + seg;
 }
 
 // Sequences of at most kShortSeqMaxT tokens take the token-by-token fp32 backward: there a
@@ -1108,10 +1176,50 @@ cudaError_t launch_bwd_chunk(const BwdArgs &a) {
         return e;
     PrepParams pp{q, k, v, a.alpha, a.eta, a.eps, a.beta_raw, a.B, a.T, a.H, nc, ws};
     bwd_prep_kernel<<<dim3(nc, chains), kPrepThreads, PR_BYTES, a.stream>>>(pp);
-    ScanParams sf{q, k, dO, a.S0, nullptr, a.q_scale, a.B, a.T, a.H, nc, ws};
-    chunk_scan_kernel<false><<<chains, kScanThreads, SC_BYTES, a.stream>>>(sf);
-    ScanParams sr{q, k, dO, a.dS_T, a.dS0, a.q_scale, a.B, a.T, a.H, nc, ws};
-    chunk_scan_kernel<true><<<chains, kScanThreads, SC_BYTES, a.stream>>>(sr);
+    const CarryPlan pl = carry_plan(chains, nc);
+    const size_t part = static_cast<size_t>(chains) * pl.nseg * kD * kD;
+    for (int rev = 0; rev < 2; ++rev) {
+        auto kern = rev ? chunk_scan_kernel<true> : chunk_scan_kernel<false>;
+        ScanParams sp{q, k, dO, rev ? a.dS_T : a.S0, rev ? a.dS0 : nullptr, a.q_scale, a.B, a.T, a.H, nc, ws,
+                      pl.seg_len, 0, 1, pl.nseg, kX0Chain, 1, 1, nullptr, nullptr};
+        if (pl.nseg <= 1) {
+            kern<<<chains, kScanThreads, SC_BYTES, a.stream>>>(sp);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            continue;
+        }
+        float *Z = ws.seg, *M = Z + part, *Sst = M + part;
+        // pass 1a: segments 0..n-2 (in processing order) from the chain's start (segment 0, the
+        // true run: records kept) or from zero; their end states Z
+        ScanParams p1 = sp;
+        p1.seg_count = pl.nseg - 1;
+        p1.records = 2;
+        p1.Xseg = Z;
+        p1.X_end = nullptr;
+        kern<<<chains * p1.seg_count, kScanThreads, SC_BYTES, a.stream>>>(p1);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        // pass 1b: transitions M of segments 1..n-2 (from the identity, linear part only)
+        if (pl.nseg > 2) {
+            ScanParams p2 = sp;
+            p2.seg_begin = 1;
+            p2.seg_count = pl.nseg - 2;
+            p2.x0_mode = kX0Identity;
+            p2.drive = 0;
+            p2.records = 0;
+            p2.Xseg = M;
+            p2.X_end = nullptr;
+            kern<<<chains * p2.seg_count, kScanThreads, SC_BYTES, a.stream>>>(p2);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        }
+        // pass 2: true start states of segments 1..n-1; pass 3: rerun them with records
+        if ((e = launch_seg_combine(Z, M, Sst, chains, pl.nseg, a.stream)) != cudaSuccess) return e;
+        ScanParams p3 = sp;
+        p3.seg_begin = 1;
+        p3.seg_count = pl.nseg - 1;
+        p3.x0_mode = kX0Given;
+        p3.Xst = Sst;
+        kern<<<chains * p3.seg_count, kScanThreads, SC_BYTES, a.stream>>>(p3);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     GradParams gp{q, k, v, dO, a.alpha, a.q_scale, a.beta_raw, a.dq, a.dk, a.dv, a.dalpha, a.deta, a.B, a.T, a.H, nc, ws};
     bwd_grad_kernel<<<dim3(nc, chains), kGradThreads, GR_BYTES, a.stream>>>(gp);
     return cudaGetLastError();

@@ -211,9 +211,9 @@ kla_status kla_decode_step_ex(const void *q, const void *k, const void *v,
 /*
  * Backward pass of kla_chunk_fwd_ex (training): the gradients of a scalar loss L with respect to
  * every input, given dO = dL/do and dS_T = dL/dS_T. The pages give no backward algebra; this is
- * the chain rule through forget, predict, residual, step size, write and read in reverse token
- * order (the fp64 oracle of the tests is checked against finite differences of the forward).
- * All arithmetic is fp32; every gradient is written in fp32.
+ * the chain rule through the forward (the fp64 oracle of the tests, the chain rule through
+ * forget, predict, residual, step size, write and read in reverse token order, is checked
+ * against finite differences of the forward). Every gradient is written in fp32.
  *
  *   q, k, v, alpha, eta, eps, S0, dtype, gate, beta_mode, q_scale: as for kla_chunk_fwd_ex (the
  *            same values the forward ran with); q, k, v need only their element alignment here
@@ -224,12 +224,18 @@ kla_status kla_decode_step_ex(const void *q, const void *k, const void *v,
  *   dalpha   fp32, shaped like alpha               written (dL/dalpha, not dL/dlog alpha)
  *   deta     fp32 [B, T, H]                        written
  *   dS0      fp32 [B, H, d_k, d_v] or NULL         written when given (dL/dS0)
- *   workspace, workspace_bytes: device scratch of at least kla_chunk_bwd_workspace_size(...) bytes,
- *            16-byte aligned: the state every 8 tokens and every residual of the forward,
- *            (ceil(T / 8) d_k d_v + T d_v) floats per (sequence, head)
+ *   workspace, workspace_bytes: 16-byte aligned device scratch of at least
+ *            kla_chunk_bwd_workspace_size(...) bytes (enough for either path), or of
+ *            kla_chunk_bwd_workspace_size_ex(...) bytes when q, k, v and dO are 16-byte aligned
  * Outputs must not overlap each other or any input. T = 0 writes dS0 = dS_T (or zeros) only.
- * Supported sizes: d_k, d_v in {16, 32, 64, 128}. One CTA per (sequence, head) walks its tokens
- * forward, then backward: the time grows with T, not with B * H.
+ * Supported sizes: d_k, d_v in {16, 32, 64, 128}. Two paths:
+ *   - bf16, scalar gate, d_k = d_v = 128, T > 16, 16-byte aligned q, k, v, dO: chunkwise (64-token
+ *     chunks) on the tensor cores, bf16 operands with fp32 accumulation and fp32 carried states
+ *     (relative L2 error ~3e-3 against fp64); the chunk-state carries of long sequences with few
+ *     (sequence, head) chains run as a sequence-parallel scan; alpha must be > 0 (dalpha is formed
+ *     from dL/dlog alpha);
+ *   - every other call: token by token in fp32, one CTA per (sequence, head), so the time grows
+ *     with T and not with B * H.
  */
 kla_status kla_chunk_bwd(const void *q, const void *k, const void *v,
                          const float *alpha, const float *eta, float eps, const float *S0,
@@ -239,8 +245,16 @@ kla_status kla_chunk_bwd(const void *q, const void *k, const void *v,
                          kla_dtype dtype, kla_gate gate, kla_beta_mode beta_mode, float q_scale,
                          void *workspace, size_t workspace_bytes, void *stream);
 
-/* Bytes of device scratch kla_chunk_bwd needs for these sizes (0 when T = 0). */
+/* Bytes of device scratch kla_chunk_bwd needs for these sizes on either path (0 when T = 0). */
 size_t kla_chunk_bwd_workspace_size(int B, int T, int H, int d_k, int d_v);
+
+/*
+ * Bytes of device scratch kla_chunk_bwd needs for these sizes, dtype and gate when q, k, v and dO
+ * are 16-byte aligned: the chunkwise path's records (~129 KB per 64-token chunk of every chain)
+ * when it applies, else the token-sequential path's. Like kla_chunk_fwd_workspace_size, it may
+ * query the current device's SM count (the segment plan of long sequences).
+ */
+size_t kla_chunk_bwd_workspace_size_ex(int B, int T, int H, int d_k, int d_v, kla_dtype dtype, kla_gate gate);
 
 /*
  * Synchronises `stream`, then reads and clears the device-side error flags that

@@ -30,7 +30,8 @@ def test_header_declares_entry_points():
     names = declared_functions()
     for required in ("kla_chunk_fwd", "kla_decode_step", "kla_chunk_fwd_workspace_size", "kla_status_string",
                      "kla_device_status", "kla_abi_version", "kla_chunk_fwd_ex", "kla_decode_step_ex",
-                     "kla_chunk_bwd", "kla_chunk_bwd_workspace_size", "kla_chunk_fwd_host",
+                     "kla_chunk_bwd", "kla_chunk_bwd_workspace_size", "kla_chunk_bwd_workspace_size_ex",
+                     "kla_chunk_fwd_host",
                      "kla_selftest_wait_timeout"):
         assert required in names, names
 
@@ -44,7 +45,7 @@ def test_status_strings_and_version(lib):
     for code, token in [(0, "KLA_OK"), (1, "INVALID_ARG"), (2, "UNSUPPORTED"), (3, "CUDA"), (4, "TIMEOUT")]:
         assert token in lib.kla_status_string(code).decode()
     assert "UNKNOWN" in lib.kla_status_string(99).decode()
-    assert lib.kla_abi_version() == 101
+    assert lib.kla_abi_version() == 102
 
 
 # Fake, never dereferenced device addresses: every case below must be rejected on the host.
@@ -143,8 +144,20 @@ def test_bwd_rejects_on_host(lib, kw, code):
 
 def test_bwd_workspace_size(lib):
     # state every 8 tokens plus every residual, fp32
-    assert lib.kla_chunk_bwd_workspace_size(2, 20, 3, 16, 32) == (2 * 3 * 3 * 16 * 32 + 2 * 20 * 3 * 32) * 4
+    seq = (2 * 3 * 3 * 16 * 32 + 2 * 20 * 3 * 32) * 4
+    assert lib.kla_chunk_bwd_workspace_size(2, 20, 3, 16, 32) == seq
     assert lib.kla_chunk_bwd_workspace_size(2, 0, 3, 16, 32) == 0
+    lib.kla_chunk_bwd_workspace_size_ex.restype = ctypes.c_size_t
+    ex = lib.kla_chunk_bwd_workspace_size_ex
+    assert ex(2, 20, 3, 16, 32, 1, 0) == seq                       # not the chunkwise shape
+    # bf16, scalar gate, d = 128: per 64-token chunk of every chain, G / beta / norm (fp32) and
+    # W, U (then dE), E, A, T, S_c, dS_{c+1} (bf16); no segments without a device to plan on
+    per_chunk = 3 * 64 * 4 + 2 * (3 * 64 * 128 + 2 * 64 * 64 + 2 * 128 * 128)
+    assert ex(2, 200, 3, 128, 128, 1, 0) == 2 * 3 * 4 * per_chunk
+    assert ex(2, 200, 3, 128, 128, 0, 0) == (2 * 3 * 25 * 128 * 128 + 2 * 200 * 3 * 128) * 4  # fp32: token path
+    assert ex(2, 16, 3, 128, 128, 1, 0) == (2 * 3 * 2 * 128 * 128 + 2 * 16 * 3 * 128) * 4   # T <= 16: token path
+    assert ex(2, 200, 3, 128, 128, 1, 1) == (2 * 3 * 25 * 128 * 128 + 2 * 200 * 3 * 128) * 4  # per-channel gate
+    assert lib.kla_chunk_bwd_workspace_size(2, 200, 3, 128, 128) >= ex(2, 200, 3, 128, 128, 1, 0)
 
 
 def test_host_prefill_rejects_on_host(lib):

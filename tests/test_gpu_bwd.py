@@ -181,3 +181,18 @@ def test_unaligned_inputs_take_the_token_path():
     ref = run_oracle(inp, dO, dST)
     chains = [(b, h) for b in range(inp.wl.B) for h in range(inp.wl.H)]
     compare(pick(got, chains), ref, TOL["bf16"])
+
+
+@pytest.mark.parametrize("T,mode", [(4059, {}), (2048 + 31, dict(beta_mode="raw", q_scale=0.5))])
+def test_long_chain_segmented_carries(T, mode):
+    """Few chains and many chunks: the chunkwise backward splits both carries into segments run in
+    parallel (value runs, transitions from the identity, start states combined, reruns; with two
+    chains and 64 chunks the cost model picks 8 segments), with S0, dL/dS_T and a ragged tail."""
+    over = dict(B=1, T=T, H=2, s0_sigma=0.05)
+    if mode:
+        over["key_norm"] = "l2"
+    inp = synth.make_prefill("gdn4k", seed=T, **over)
+    dO, dST = _grad_inputs(inp, seed=T + 1, with_dst=True)
+    got = run_gpu(inp, dO, dST, **mode)
+    ref = run_oracle(inp, dO, dST, **mode)
+    compare(pick(got, [(0, 0), (0, 1)]), ref, TOL_CHUNK)
