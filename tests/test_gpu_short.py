@@ -28,6 +28,8 @@ CASES = [
     ("bf16", 128, 128, 15, "channel", 0.05),
     ("bf16", 128, 128, 16, "scalar", 0.05),
     ("bf16", 64, 64, 7, "channel", 0.1),
+    ("bf16", 128, 128, 1, "channel", 0.05),
+    ("f32", 128, 64, 1, "scalar", 0.0),
 ]
 
 
