@@ -363,7 +363,8 @@ struct TokParams {
     int B, T, H, DK, DV;
     int beta_raw;
     float q_scale;
-    int stage_bytes, off_kq, off_v, off_a, off_e;   // dynamic shared-memory stage layout
+    int s_bytes;                                    // the state tile (one buffer)
+    int stage_bytes, off_kq, off_v, off_a, off_e;   // the tokens' stage layout (two buffers)
 };
 
 // d_k = 128, two warps per tile: thread (rg, cg) holds key rows 16 rg .. 16 rg + 15
@@ -382,7 +383,6 @@ __global__ void __launch_bounds__(kTokThreads, 8) tokens_pipe_kernel(const TokPa
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cg = tid % NCG, i0 = (tid / NCG) * RPT;
     const int DV = p.DV, T = p.T, ctiles = DV / BV;
-    auto stage = [&](int slot, int off) { return dsm + slot * p.stage_bytes + off; };
     auto tile_bh = [&](int t, int &v0) {
         v0 = (t % ctiles) * BV;
         return static_cast<size_t>(t / ctiles);   // = b * H + h
@@ -411,10 +411,11 @@ __global__ void __launch_bounds__(kTokThreads, 8) tokens_pipe_kernel(const TokPa
             }
         }
     };
-    auto prefetch = [&](int t, int slot) {
+    float *sS = reinterpret_cast<float *>(dsm);   // one state tile (refilled for the next tile early)
+    auto stage = [&](int slot, int off) { return dsm + p.s_bytes + slot * p.stage_bytes + off; };
+    auto prefetch_state = [&](int t) {
         int v0;
         const size_t bh = tile_bh(t, v0);
-        float *sS = reinterpret_cast<float *>(stage(slot, 0));
         if (p.S0) {
             const float *Sg = p.S0 + bh * DK * DV + v0;
             for (int c = tid; c < DK * (BV / 4); c += kThreads) {
@@ -425,6 +426,10 @@ __global__ void __launch_bounds__(kTokThreads, 8) tokens_pipe_kernel(const TokPa
             for (int c = tid; c < DK * (BV / 4); c += kThreads)
                 *reinterpret_cast<float4 *>(&sS[c * 4]) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
+    };
+    auto prefetch_tokens = [&](int t, int slot) {
+        int v0;
+        const size_t bh = tile_bh(t, v0);
         constexpr int per16 = 16 / sizeof(TIn);
         constexpr int nch = DK / per16;                // 16-byte chunks of one k or q row
         const size_t row0 = row_of(bh, 0);
@@ -455,17 +460,17 @@ __global__ void __launch_bounds__(kTokThreads, 8) tokens_pipe_kernel(const TokPa
     };
 
     int it = 0;
-    if (blockIdx.x < ntiles) prefetch(blockIdx.x, 0);
+    if (blockIdx.x < ntiles) {
+        prefetch_state(blockIdx.x);
+        prefetch_tokens(blockIdx.x, 0);
+    }
     cp_async_commit();
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
         const int slot = it & 1;
-        if (t + static_cast<int>(gridDim.x) < ntiles) prefetch(t + gridDim.x, slot ^ 1);
-        cp_async_commit();
-        cp_async_wait_1();   // this thread's copies of tile t have landed
-        __syncthreads();     // and everyone else's (and the zero fill of a NULL S0)
+        asm volatile("cp.async.wait_group 0;" ::: "memory");   // tile t's state and tokens have landed
+        __syncthreads();     // everyone's copies (and the zero fill of a NULL S0) are visible
         int v0;
         const size_t bh = tile_bh(t, v0);
-        const float *sS = reinterpret_cast<const float *>(stage(slot, 0));
         const TIn *skq = reinterpret_cast<const TIn *>(stage(slot, p.off_kq));
         const TIn *sv = reinterpret_cast<const TIn *>(stage(slot, p.off_v));
         const float *sa = reinterpret_cast<const float *>(stage(slot, p.off_a));
@@ -496,7 +501,12 @@ __global__ void __launch_bounds__(kTokThreads, 8) tokens_pipe_kernel(const TokPa
             s[r][0] = make_float2(x.x, x.y);
             s[r][1] = make_float2(x.z, x.w);
         }
-        __syncthreads();   // beta and k . q of every token are visible
+        __syncthreads();   // beta and k . q of every token are visible; the state buffer is free
+        if (t + static_cast<int>(gridDim.x) < ntiles) {   // the next tile streams in during this one's tokens
+            prefetch_state(t + gridDim.x);
+            prefetch_tokens(t + gridDim.x, slot ^ 1);
+        }
+        cp_async_commit();
 
         const size_t row0 = row_of(bh, 0);
         int par = 0;
@@ -575,7 +585,8 @@ __global__ void __launch_bounds__(kTokThreads, 8) tokens_pipe_kernel(const TokPa
                 *reinterpret_cast<float4 *>(Sbh + static_cast<size_t>(i0 + r) * DV + v0 + cg * 4) =
                     make_float4(s[r][0].x, s[r][0].y, s[r][1].x, s[r][1].y);
         }
-        __syncthreads();   // the slot, beta and k . q are rewritten for the next tile
+        // the next tile's first barrier orders this tile's reads of the token slot, beta and
+        // k . q before they are rewritten
     }
 }
 
@@ -583,9 +594,10 @@ TokParams tok_params(const ChunkArgs &a) {
     const int esz = a.dtype == KLA_DTYPE_BF16 ? 2 : 4;
     auto up16 = [](int x) { return (x + 15) & ~15; };
     TokParams p{a.q, a.k, a.v, a.alpha, a.eta, a.eps, a.S0, a.S_T, a.o, a.B, a.T, a.H, a.d_k, a.d_v,
-                a.beta_raw, a.q_scale, 0, 0, 0, 0, 0};
-    p.off_kq = a.d_k * 32 * 4;
-    p.off_v = up16(p.off_kq + a.T * 2 * a.d_k * esz);
+                a.beta_raw, a.q_scale, 0, 0, 0, 0, 0, 0};
+    p.s_bytes = a.d_k * 32 * 4;
+    p.off_kq = 0;
+    p.off_v = up16(a.T * 2 * a.d_k * esz);
     p.off_a = up16(p.off_v + a.T * 32 * esz);
     p.off_e = up16(p.off_a + a.T * (a.gate == KLA_GATE_CHANNEL ? a.d_k : 1) * 4);
     p.stage_bytes = up16(p.off_e + a.T * 4);
@@ -601,7 +613,7 @@ cudaError_t launch_tokens_t(const ChunkArgs &a) {
     static int sms_of[64] = {};
     static int per_sm[64][kShortSeqMaxT + 1] = {};
     const TokParams p = tok_params(a);
-    const int smem = 2 * p.stage_bytes;
+    const int smem = p.s_bytes + 2 * p.stage_bytes;
     auto kern = tokens_pipe_kernel<TIn, kChannel>;
     constexpr int kThreads = kTokThreads;
     int dev = 0;
@@ -612,7 +624,8 @@ cudaError_t launch_tokens_t(const ChunkArgs &a) {
         ChunkArgs big = a;
         big.T = kShortSeqMaxT;
         big.d_k = 128;
-        const int max_smem = 2 * tok_params(big).stage_bytes;
+        const TokParams pb = tok_params(big);
+        const int max_smem = pb.s_bytes + 2 * pb.stage_bytes;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem)) != cudaSuccess)
             return e;
         attr_set[dev] = true;
