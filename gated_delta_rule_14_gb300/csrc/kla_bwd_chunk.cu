@@ -1176,6 +1176,7 @@ cudaError_t launch_bwd_chunk(const BwdArgs &a) {
         return e;
     PrepParams pp{q, k, v, a.alpha, a.eta, a.eps, a.beta_raw, a.B, a.T, a.H, nc, ws};
     bwd_prep_kernel<<<dim3(nc, chains), kPrepThreads, PR_BYTES, a.stream>>>(pp);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const CarryPlan pl = carry_plan(chains, nc);
     const size_t part = static_cast<size_t>(chains) * pl.nseg * kD * kD;
     for (int rev = 0; rev < 2; ++rev) {
