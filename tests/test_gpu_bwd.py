@@ -183,7 +183,8 @@ def test_unaligned_inputs_take_the_token_path():
     compare(pick(got, chains), ref, TOL["bf16"])
 
 
-@pytest.mark.parametrize("T,mode", [(4059, {}), (2048 + 31, dict(beta_mode="raw", q_scale=0.5))])
+@pytest.mark.parametrize("T,mode", [(4059, {}), (2048 + 31, dict(beta_mode="raw", q_scale=0.5)),
+                                    (16384 - 5, {})])   # 256 chunks on two chains: 32 segments of 8
 def test_long_chain_segmented_carries(T, mode):
     """Few chains and many chunks: the chunkwise backward splits both carries into segments run in
     parallel (value runs, transitions from the identity, start states combined, reruns; with two
