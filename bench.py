@@ -372,7 +372,7 @@ def bench_bwd(name, steps, seed, dev, flush, stream, pk, **override):
             "workspace_bytes": ws.numel(), "roofline": roofline(alg, ms, pk),
             "note": "chunkwise backward on warp-level bf16 MMAs: chunk-parallel prep (T = (I+R)^-1, W, U, A), "
                     "forward and reverse chunk-state carries (one CTA per chain), chunk-parallel gradients; "
-                    "~4.2 GB of DRAM traffic per call (ncu, per-chunk S_c, dS_c, E_c, dE_c, W, U, A, T records) "
+                    "~4.5 GB of DRAM traffic per call (ncu at B = 4, per-chunk S_c, dS_c, E_c, dE_c, W, U, A, T records) "
                     "against the algorithmic bytes"}
 
 
