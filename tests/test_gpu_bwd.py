@@ -197,3 +197,22 @@ def test_long_chain_segmented_carries(T, mode):
     got = run_gpu(inp, dO, dST, **mode)
     ref = run_oracle(inp, dO, dST, **mode)
     compare(pick(got, [(0, 0), (0, 1)]), ref, TOL_CHUNK)
+
+
+@pytest.mark.parametrize("mode", [{}, dict(beta_mode="raw")])
+def test_chunked_backward_zero_keys_and_unit_gates(mode):
+    """Degenerate tokens inside chunks: keys that are exactly zero with eps = 0 (beta = 0 by
+    definition, no gradient flows through the step size) and gates of exactly 1 (no decay)."""
+    import dataclasses
+    # the raw step (beta = eta) needs unit keys: beta norm(k)^2 > 2 makes the recurrence diverge
+    norm = dict(key_norm="l2") if mode else {}
+    inp = synth.make_prefill("gdn4k", seed=77, B=1, T=150, H=2, s0_sigma=0.05, eps=0.0, **norm)
+    k = inp.k.copy()
+    k[:, [0, 5, 63, 64, 100, 149]] = 0                      # bf16 zero bits
+    alpha = inp.alpha.copy()
+    alpha[:, 10:40] = 1.0
+    inp = dataclasses.replace(inp, k=k, alpha=alpha)
+    dO, dST = _grad_inputs(inp, seed=78, with_dst=True)
+    got = run_gpu(inp, dO, dST, **mode)
+    ref = run_oracle(inp, dO, dST, **mode)
+    compare(pick(got, [(0, 0), (0, 1)]), ref, TOL_CHUNK)
