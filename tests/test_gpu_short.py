@@ -1,6 +1,8 @@
 """Short sequences (T <= 16: multi-token decode, speculative verification) against the fp64
-oracle. kla_chunk_fwd runs these on a kernel that keeps each state tile in registers and walks
-the tokens one by one, so the result must equal T single-token decode steps as well."""
+oracle. kla_chunk_fwd runs these either on a kernel that keeps each state tile in registers and
+walks the tokens one by one (whose result must equal T single-token decode steps as well), or,
+for bf16 with a scalar gate, d_k = d_v = 128 and T >= 5, on the chunk form of the recurrence
+with the call's tokens as one chunk (warp-level tensor cores, one CTA per head)."""
 import ctypes
 import dataclasses
 
@@ -81,19 +83,22 @@ def test_equals_repeated_decode_steps():
     assert oracle.rel_l2(ST.cpu().numpy(), S.cpu().numpy()) <= 1e-6
 
 
-def test_speculative_verify_then_accept_prefix():
-    """Verification pattern: run k draft tokens from the committed state without touching it,
+@pytest.mark.parametrize("T,j", [(4, 2), (8, 5), (16, 9)])
+def test_speculative_verify_then_accept_prefix(T, j):
+    """Verification pattern: run T draft tokens from the committed state without touching it,
     accept a prefix of j tokens, then advance the committed state by those j tokens in place.
-    Outputs of the prefix and the advanced state must match the oracle on the prefix alone."""
+    Outputs of the prefix and the advanced state must match the oracle on the prefix alone. Each
+    pair runs on one kernel (the token loop below 5 tokens, the chunk form with the same token
+    padding from 5), where later tokens add exact zeros to the prefix, so the accepted outputs
+    equal the draft's bit for bit."""
     import gated_delta_rule_14_gb300 as kla
-    inp = synth.make_prefill("decode", seed=33, B=8, T=5, H=4, chunk=64, s0_sigma=0.02)
+    inp = synth.make_prefill("decode", seed=33, B=8, T=T, H=4, chunk=64, s0_sigma=0.02)
     q, k, v, a, e = (to_dev(x) for x in (inp.q, inp.k, inp.v, inp.alpha, inp.eta))
     S = to_dev(inp.S0).clone()
     S_before = S.clone()
     o_draft, _ = kla.chunk_fwd(q, k, v, a, e, inp.wl.eps, S)       # S_T into a new buffer
     kla.device_status(DEV)
     assert (S == S_before).all().item()
-    j = 3
     o_acc, S_out = kla.chunk_fwd(q[:, :j].contiguous(), k[:, :j].contiguous(), v[:, :j].contiguous(),
                                  a[:, :j].contiguous(), e[:, :j].contiguous(), inp.wl.eps, S, S_T=S)
     kla.device_status(DEV)
@@ -130,3 +135,54 @@ def test_serving_batch_sampled():
     inp = synth.make_prefill("decode", seed=2, T=4, chunk=64)
     o, S = run_prefill(inp)
     check(inp, o, S, sample_chains(inp.wl.B, inp.wl.H, 16, seed=3))
+
+
+# The chunk-form kernel: both token paddings (T <= 8 packs K and Q into one 16-row tile, 9..16
+# uses two), ragged T inside each, and a head count that does not divide the persistent grid.
+@pytest.mark.parametrize("T", [5, 7, 8, 9, 13, 16])
+def test_chunk_form_tokens(T):
+    inp = synth.make_prefill("decode", seed=500 + T, B=5, T=T, H=3, chunk=64, s0_sigma=0.05)
+    o, S = run_prefill(inp)
+    check(inp, o, S)
+
+
+def test_chunk_form_zero_state_and_no_final_state():
+    import torch
+
+    import gated_delta_rule_14_gb300 as kla
+    inp = synth.make_prefill("decode", seed=9, B=2, T=11, H=3, chunk=64, s0_sigma=0.0)
+    inp = dataclasses.replace(inp, S0=None)
+    o, S = run_prefill(inp)
+    check(inp, o, S)
+    o2 = torch.empty((2, 11, 3, 128), dtype=torch.bfloat16, device=DEV)
+    lib = kla._native.lib()
+    args = [to_dev(x) for x in (inp.q, inp.k, inp.v, inp.alpha, inp.eta)]
+    st = lib.kla_chunk_fwd(*(x.data_ptr() for x in args), ctypes.c_float(inp.wl.eps), None, o2.data_ptr(),
+                           None, 2, 11, 3, 128, 128, 64, 1, 0, None, 0,
+                           torch.cuda.current_stream(DEV).cuda_stream)
+    assert st == 0
+    kla.device_status(DEV)
+    assert np.array_equal(o2.float().cpu().numpy(), o.astype(np.float32))
+
+
+@pytest.mark.parametrize("T", [6, 12])
+def test_chunk_form_degenerate_tokens(T):
+    """Keys that are exactly zero with eps = 0 (beta = 0: the step writes nothing), gates of
+    exactly 1 (no decay) and of exactly 0 (the state before the token is forgotten)."""
+    inp = synth.make_prefill("decode", seed=40 + T, B=2, T=T, H=2, chunk=64, s0_sigma=0.05, eps=0.0)
+    k, alpha = inp.k.copy(), inp.alpha.copy()
+    k[0, [0, T - 1], 0] = 0
+    k[1, 2, 1] = 0
+    alpha[0, 1:4, 1] = 1.0
+    alpha[1, 3, 0] = 0.0
+    inp = dataclasses.replace(inp, k=k, alpha=alpha)
+    o, S = run_prefill(inp)
+    check(inp, o, S)
+
+
+def test_chunk_form_serving_batch_sampled():
+    # verification of 8 draft tokens at the decode batch: 64 sequences x 16 heads
+    inp = synth.make_prefill("decode", seed=5, T=8, chunk=64)
+    o, S = run_prefill(inp)
+    check(inp, o, S, sample_chains(inp.wl.B, inp.wl.H, 16, seed=4))
+
