@@ -14,8 +14,8 @@ the kernels are launched on.
 Extras in the same JSON line: long131k prefill (B=1 H=16 T=131072), kda8k prefill
 (per-key-channel gate, B=4 H=16 T=8192), decode (batch 64, H16, 1024 single-token
 steps, L2 flushed before every step), decode_graph (the same steps as one CUDA graph, L2 not
-flushed), verify4 (the decode batch advanced 4 tokens per
-call, as in speculative verification), bwd_gdn4k and bwd_long131k (the backward passes of
+flushed), verify4 / verify8 / verify16 (the decode batch advanced 4, 8 or 16 tokens per
+call, as in speculative verification: the token loop at 4, the chunk form at 8 and 16), bwd_gdn4k and bwd_long131k (the backward passes of
 the headline and the long-context workloads), each with its own roofline.
 
 --impl reference times the fp64 CPU oracle on the host cores on a bounded sample of the
@@ -336,8 +336,10 @@ def bench_verify(ntok, calls, seed, dev, flush, stream, pk):
     kla.device_status(dev)
     heads = wl.B * wl.H
     alg_bytes = heads * (8 * wl.d_k * wl.d_v + ntok * (PREFILL_BYTES_PER_TOKEN_HEAD))
+    kernel = ("chunk form (tokens_tc_kernel: one CTA per head, warp-level tensor cores)" if ntok >= 5 else
+              "token loop (tokens_pipe_kernel: 128 x 32 state tiles in registers)")
     return {"value": wl.B * ntok / (ms * 1e-3), "unit": "tokens/s", "ms_per_call": ms, "calls": calls,
-            "tokens_per_call": ntok, "batch": wl.B, "roofline": roofline(alg_bytes, ms, pk),
+            "tokens_per_call": ntok, "batch": wl.B, "kernel": kernel, "roofline": roofline(alg_bytes, ms, pk),
             "l2": "flushed before every call (256 MiB write, then 256 MiB read)"}
 
 
@@ -576,6 +578,12 @@ def main():
         extras["verify4"] = bench_verify(4, args.verify_calls, seed=rank, dev=dev, flush=flush, stream=stream, pk=pk)
         clocks.mark(t0, time.time())
         launches += args.verify_calls
+        for ntok in (8, 16):
+            t0 = time.time()
+            extras[f"verify{ntok}"] = bench_verify(ntok, args.verify_calls, seed=rank, dev=dev, flush=flush,
+                                                   stream=stream, pk=pk)
+            clocks.mark(t0, time.time())
+            launches += args.verify_calls
         if not args.no_bwd:
             t0 = time.time()
             extras["bwd_gdn4k"] = bench_bwd("gdn4k", 3, seed=rank, dev=dev, flush=flush, stream=stream, pk=pk)
