@@ -6,8 +6,11 @@
 // outputs on a download stream once the prefill is done (two streams per direction, parts
 // alternating, so two copies of a direction can be in flight). Copies of part i+1 overlap the
 // prefill of part i, and the two directions of the link overlap each other; prefills of
-// different parts may run at the same time on different SMs (each part runs whole sequences,
-// without the sequence-parallel segments, which would only add work next to other parts).
+// different parts may run at the same time on different SMs. Parts run whole sequences (the
+// sequence-parallel segments would only add work next to other parts), except the last one:
+// nothing runs beside it but the remaining copies, and its prefill plus its download are the
+// call's tail, so it takes the segments when they shorten it, with the fixed scratch array of
+// kla_chunk_fwd_noalloc (the last parts of consecutive calls are ordered on it by an event).
 //
 // Streams and events are created once per device on the first call and kept for the life of
 // the process. Calls are ordered after earlier work on the caller's stream and the caller's
@@ -30,6 +33,7 @@ struct HostPipe {
     cudaStream_t h2d[kCopyStreams] = {}, d2h[kCopyStreams] = {}, comp[kComputeStreams] = {};
     cudaEvent_t start = nullptr, in_done[kMaxParts] = {}, out_ready[kMaxParts] = {};
     cudaEvent_t end[kCopyStreams] = {}, comp_done[kComputeStreams] = {};
+    cudaEvent_t scratch_free = nullptr;   // the last part's use of the shared scratch has ended
 };
 HostPipe g_pipe[kMaxDevices];
 std::mutex g_pipe_mutex[kMaxDevices];
@@ -46,6 +50,7 @@ cudaError_t init_pipe(HostPipe &p) {
     for (auto &s : p.comp)
         if ((e = cudaStreamCreateWithFlags(&s, sf)) != cudaSuccess) return e;
     if ((e = cudaEventCreateWithFlags(&p.start, ef)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&p.scratch_free, ef)) != cudaSuccess) return e;
     for (int i = 0; i < kMaxParts; ++i) {
         if ((e = cudaEventCreateWithFlags(&p.in_done[i], ef)) != cudaSuccess) return e;
         if ((e = cudaEventCreateWithFlags(&p.out_ready[i], ef)) != cudaSuccess) return e;
@@ -112,13 +117,28 @@ extern "C" kla_status kla_chunk_fwd_host(const void *q_h, const void *k_h, const
         cudaStream_t comp = P.comp[i % kComputeStreams];
         ok = cudaStreamWaitEvent(comp, P.in_done[i], 0) == cudaSuccess;
         if (!ok) break;
-        st = kla::chunk_fwd_nosplit(at(q_d, b0 * qk_b), at(k_d, b0 * qk_b), at(v_d, b0 * v_b),
-                              reinterpret_cast<const float *>(at(alpha_d, b0 * a_b)),
-                              reinterpret_cast<const float *>(at(eta_d, b0 * e_b)), eps,
-                              S0_d ? reinterpret_cast<const float *>(at(S0_d, b0 * s_b)) : nullptr,
-                              atw(o_d, b0 * v_b), S_T_d ? reinterpret_cast<float *>(atw(S_T_d, b0 * s_b)) : nullptr,
-                              nb, T, H, d_k, d_v, chunk, dtype, gate, beta_mode, q_scale, comp);
-        if (st != KLA_OK) break;
+        const void *qp = at(q_d, b0 * qk_b), *kp = at(k_d, b0 * qk_b), *vp = at(v_d, b0 * v_b);
+        const float *ap = reinterpret_cast<const float *>(at(alpha_d, b0 * a_b));
+        const float *ep = reinterpret_cast<const float *>(at(eta_d, b0 * e_b));
+        const float *s0p = S0_d ? reinterpret_cast<const float *>(at(S0_d, b0 * s_b)) : nullptr;
+        float *stp = S_T_d ? reinterpret_cast<float *>(atw(S_T_d, b0 * s_b)) : nullptr;
+        const size_t need = b0 + nb >= B ? kla_chunk_fwd_workspace_size(nb, T, H, d_k, d_v, chunk, dtype, gate) : 0;
+        if (need > 0 && need <= static_cast<size_t>(KLA_NOALLOC_SCRATCH_BYTES)) {   // the last part, segmented
+            void *scratch = nullptr;
+            if (kla::noalloc_scratch(&scratch) != cudaSuccess || cudaStreamWaitEvent(comp, P.scratch_free, 0) != cudaSuccess) {
+                st = KLA_ERR_CUDA;
+                break;
+            }
+            st = kla_chunk_fwd_ex(qp, kp, vp, ap, ep, eps, s0p, atw(o_d, b0 * v_b), stp, nb, T, H, d_k, d_v, chunk, dtype,
+                                  gate, beta_mode, q_scale, scratch, KLA_NOALLOC_SCRATCH_BYTES, comp);
+            if (st != KLA_OK) break;
+            ok = cudaEventRecord(P.scratch_free, comp) == cudaSuccess;
+            if (!ok) break;
+        } else {
+            st = kla::chunk_fwd_nosplit(qp, kp, vp, ap, ep, eps, s0p, atw(o_d, b0 * v_b), stp, nb, T, H, d_k, d_v, chunk,
+                                        dtype, gate, beta_mode, q_scale, comp);
+            if (st != KLA_OK) break;
+        }
         ok = cudaEventRecord(P.out_ready[i], comp) == cudaSuccess &&
              cudaStreamWaitEvent(down, P.out_ready[i], 0) == cudaSuccess;
         if (!ok) break;

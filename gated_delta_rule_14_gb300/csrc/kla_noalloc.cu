@@ -12,7 +12,8 @@
 // segmented prefill writes every scratch element it later reads within the same call (segment
 // value runs, transition runs, then the combine pass), so nothing has to be cleared between
 // calls. Calls whose kernels may overlap on the GPU (different streams, no ordering between
-// them) race on the array: callers must order them.
+// them) race on the array: callers must order them. kla_chunk_fwd_host borrows the array for
+// the last part of its batch (ordered among host calls by an event of its own).
 #include <mutex>
 
 #include "kla_internal.cuh"
@@ -25,10 +26,12 @@ constexpr int kMaxDevices = 64;
 void *g_scratch_ptr[kMaxDevices] = {};
 std::mutex g_scratch_mutex;
 
+}  // namespace
+
 // Device address of the scratch array on the current device. In host code the array's name
 // is only a host-side stand-in, so the address must come from the runtime; it is looked up
 // on the first call per device (with that device current) and cached.
-cudaError_t scratch_address(void **out) {
+cudaError_t kla::noalloc_scratch(void **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -44,8 +47,6 @@ cudaError_t scratch_address(void **out) {
     return cudaSuccess;
 }
 
-}  // namespace
-
 extern "C" kla_status kla_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *alpha,
                                             const float *eta, float eps, const float *S0, void *o, float *S_T,
                                             int B, int T, int H, int d_k, int d_v, int chunk, kla_dtype dtype,
@@ -53,7 +54,7 @@ extern "C" kla_status kla_chunk_fwd_noalloc(const void *q, const void *k, const 
     const size_t need = kla_chunk_fwd_workspace_size(B, T, H, d_k, d_v, chunk, dtype, gate);
     if (need > static_cast<size_t>(KLA_NOALLOC_SCRATCH_BYTES)) return KLA_ERR_UNSUPPORTED;
     void *scratch = nullptr;
-    if (need > 0 && scratch_address(&scratch) != cudaSuccess) return KLA_ERR_CUDA;
+    if (need > 0 && kla::noalloc_scratch(&scratch) != cudaSuccess) return KLA_ERR_CUDA;
     return kla_chunk_fwd(q, k, v, alpha, eta, eps, S0, o, S_T, B, T, H, d_k, d_v, chunk, dtype, gate, scratch,
                          need > 0 ? static_cast<size_t>(KLA_NOALLOC_SCRATCH_BYTES) : 0, stream);
 }

@@ -168,7 +168,11 @@ kla_status kla_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
  *                 exactly when S0_h / S_T_h are); their contents after the call are unspecified
  *                 except o_d and S_T_d, which hold the results
  *   parts         1 .. min(B, 64)
- * Each part runs whole sequences (no sequence-parallel segments, so no workspace). The call is
+ * Parts run whole sequences, except the last part when the sequence-parallel segments of
+ * kla_chunk_fwd shorten it (long sequences, few chains per part): it then takes its scratch
+ * from the fixed array of kla_chunk_fwd_noalloc (no allocation). The last parts of host calls
+ * are ordered on that array by an event of the library's; a kla_chunk_fwd_noalloc call whose
+ * kernels may run at the same time as a host call must be ordered against it by the caller. The call is
  * asynchronous and ordered on `stream`: it starts after earlier work on `stream`, and work
  * enqueued on `stream` afterwards starts after its last copy. The library keeps two copy
  * streams, eight compute streams and a few events per device for the life of the process;

@@ -1,7 +1,8 @@
 """Prefill of host tensors (kla_chunk_fwd_host): the batch split into parts whose copies and
 kernels overlap must give exactly what kla_chunk_fwd gives on device copies of the same inputs
 (each part runs whole sequences through the same kernels), for any part count, with or without
-an initial and a final state."""
+an initial and a final state. The last part of a batch of long sequences runs the
+sequence-parallel segments instead; it is checked against the oracle."""
 import numpy as np
 import pytest
 import torch
@@ -58,3 +59,33 @@ def test_host_prefill_without_final_state_and_bad_parts():
     assert torch.equal(o_h, o_d.cpu())
     with pytest.raises(kla.KlaError):
         kla.chunk_fwd_host(*args, inp.wl.eps, parts=3, device=DEV)   # more parts than sequences
+
+
+def test_host_prefill_segments_the_last_part():
+    """Parts of one sequence of 4096 tokens (16 chains of 64 chunks): the last part, the call's
+    tail, runs the sequence-parallel segments on the library's fixed scratch. A second call (one
+    part, so its prefill runs on another of the library's compute streams) is issued from another
+    stream while the first may still run: the two share the scratch, ordered by the library's
+    event. Both match the oracle on sampled chains; repeating the first call reproduces it bit
+    for bit."""
+    import gated_delta_rule_14_gb300 as kla
+    lib = kla._native.lib()
+    torch.cuda.set_device(DEV)
+    assert lib.kla_chunk_fwd_workspace_size(1, 4096, 16, 128, 128, 64, 1, 0) > 0   # segments pay off here
+    inp = synth.make_prefill("gdn4k", seed=41, B=2, T=4096, H=16, s0_sigma=0.05)
+    args = [host(x) for x in (inp.q, inp.k, inp.v, inp.alpha, inp.eta)]
+    S0 = host(inp.S0)
+    o1, s1 = kla.chunk_fwd_host(*args, inp.wl.eps, S0, parts=2, device=DEV)
+    side = torch.cuda.Stream(DEV)
+    with torch.cuda.stream(side):
+        o2, s2 = kla.chunk_fwd_host(*args, inp.wl.eps, S0, parts=1, device=DEV)
+    o3, s3 = kla.chunk_fwd_host(*args, inp.wl.eps, S0, parts=2, device=DEV)
+    torch.cuda.synchronize(DEV)
+    kla.device_status(DEV)
+    assert torch.equal(o1, o3) and torch.equal(s1, s3)
+    chains = [(0, 0), (0, 9), (0, 15), (1, 0), (1, 6), (1, 15)]
+    o_ref, s_ref = oracle_chains(inp, chains)
+    for o, st in ((o1, s1), (o2, s2)):
+        o_g = np.stack([o.float().numpy()[b, :, h] for b, h in chains])
+        s_g = np.stack([st.numpy()[b, h] for b, h in chains])
+        assert oracle.rel_l2(o_g, o_ref) <= 1e-2 and oracle.rel_l2(s_g, s_ref) <= 1e-2
