@@ -101,6 +101,13 @@ typedef enum kla_beta_mode {
  * e^-80 (the gates averaged over 32 tokens above about 0.082). A chunk outside that range
  * raises a device flag that kla_device_status() reports as KLA_ERR_INVALID_ARG (its results
  * are then not valid); chunk = 16 or 32 runs the fp32 path, which has no such limit.
+ *
+ * Calls of 1 to 16 tokens (multi-token decode, speculative verification) ignore `chunk`: bf16
+ * with a scalar gate and d_k = d_v = 128 runs the call's tokens as one chunk on warp-level
+ * tensor cores from 5 tokens (the state rounded to bf16 as an operand, as on the chunkwise
+ * path); other calls walk the tokens in order on fp32 state tiles. A call's first j outputs are
+ * bit-identical to those of a call with only its first j tokens when both token counts fall in
+ * the same one of the ranges 1-4, 5-8 and 9-16 (bf16, scalar gate, d = 128; always otherwise).
  */
 kla_status kla_chunk_fwd(const void *q, const void *k, const void *v,
                          const float *alpha, const float *eta, float eps,
