@@ -21,6 +21,12 @@
 
 #include "kla_internal.cuh"
 
+namespace kla {
+// Device address of the fixed KLA_NOALLOC_SCRATCH_BYTES scratch array on the current device
+// (kla_noalloc.cu).
+cudaError_t noalloc_scratch(void **out);
+}  // namespace kla
+
 namespace {
 
 constexpr int kMaxDevices = 64;

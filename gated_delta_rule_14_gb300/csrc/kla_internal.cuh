@@ -69,8 +69,6 @@ struct BwdArgs {
 
 // kla_chunk_fwd_ex without the sequence-parallel segments (no workspace): for callers that run
 // several prefills side by side, where splitting each one would only add work.
-// Device address of the fixed KLA_NOALLOC_SCRATCH_BYTES scratch array on the current device.
-cudaError_t noalloc_scratch(void **out);
 kla_status chunk_fwd_nosplit(const void *q, const void *k, const void *v, const float *alpha, const float *eta,
                              float eps, const float *S0, void *o, float *S_T, int B, int T, int H, int d_k, int d_v,
                              int chunk, kla_dtype dtype, kla_gate gate, kla_beta_mode beta_mode, float q_scale,

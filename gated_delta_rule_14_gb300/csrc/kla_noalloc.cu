@@ -28,6 +28,10 @@ std::mutex g_scratch_mutex;
 
 }  // namespace
 
+namespace kla {
+cudaError_t noalloc_scratch(void **out);
+}  // namespace kla
+
 // Device address of the scratch array on the current device. In host code the array's name
 // is only a host-side stand-in, so the address must come from the runtime; it is looked up
 // on the first call per device (with that device current) and cached.
