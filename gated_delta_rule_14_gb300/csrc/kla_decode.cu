@@ -599,6 +599,7 @@ __global__ void __launch_bounds__(kTokThreads, 8) tokens_pipe_kernel(const TokPa
 // columns, contractions on warp-level tensor cores:
 //   [K; Q] S            -> K S, Q S     bf16 MMAs, the state rounded to bf16 as an operand
 //   Y = diag(beta) (V - diag(e^G) K S),  E = T Y,  T = (I + R)^{-1}      tf32 MMAs
+//     (the page's order: provisional errors of all tokens, then the unit-lower solve)
 //   O = s (diag(e^G) Q S + A E)                                          tf32 MMAs
 //   S' = e^{G_end} S + K^T diag(e^{G_end - G}) E   bf16 MMAs into the fp32 state accumulators
 // with G the in-call prefix of log alpha, R_im = beta_i e^{G_i - G_m} k_i . k_m (m < i) and
