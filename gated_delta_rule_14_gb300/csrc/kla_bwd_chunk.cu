@@ -42,6 +42,7 @@
 // 8 distinct bank quads. Operands are bf16 (inputs as stored; derived tiles rounded once); the
 // carried states, the solve and every sum of a gradient are fp32.
 #include <algorithm>
+#include <mutex>
 
 #include "kla_internal.cuh"
 #include "warp_mma.cuh"
@@ -1094,6 +1095,21 @@ bool bwd_chunk_supports(const BwdArgs &a) {
            al16(a.workspace) && a.workspace_bytes >= bwd_chunk_workspace_bytes(a.B, a.T, a.H);
 }
 
+// When the CTAs of pass 1a and pass 1b of a segmented carry fit on the SMs together (the plan
+// counts them as one wave), pass 1b runs on a second stream of the library's, between a fork and
+// a join recorded on the caller's stream; with two waves both stay in order on the caller's
+// stream. One stream and two events per device; the mutex keeps a call's fork and join records
+// from interleaving with another thread's.
+namespace {
+struct CarryAux {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+constexpr int kMaxCarryDevices = 64;
+CarryAux g_carry_aux[kMaxCarryDevices];
+std::mutex g_carry_aux_mutex[kMaxCarryDevices];
+}  // namespace
+
 cudaError_t launch_bwd_chunk(const BwdArgs &a) {
     const int nc = (a.T + kC - 1) / kC, chains = a.B * a.H;
     const Ws ws = carve(a.workspace, static_cast<size_t>(chains) * nc);
@@ -1127,20 +1143,48 @@ cudaError_t launch_bwd_chunk(const BwdArgs &a) {
         p1.records = 2;
         p1.Xseg = Z;
         p1.X_end = nullptr;
-        kern<<<chains * p1.seg_count, kScanThreads, SC_BYTES, a.stream>>>(p1);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        // pass 1b: transitions M of segments 1..n-2 (from the identity, linear part only)
-        if (pl.nseg > 2) {
-            ScanParams p2 = sp;
-            p2.seg_begin = 1;
-            p2.seg_count = pl.nseg - 2;
-            p2.x0_mode = kX0Identity;
-            p2.drive = 0;
-            p2.records = 0;
-            p2.Xseg = M;
-            p2.X_end = nullptr;
-            kern<<<chains * p2.seg_count, kScanThreads, SC_BYTES, a.stream>>>(p2);
+        // pass 1b: transitions M of segments 1..n-2 (from the identity, linear part only); it
+        // writes only M and reads only the prep's records, so it may run beside pass 1a
+        ScanParams p2 = sp;
+        p2.seg_begin = 1;
+        p2.seg_count = pl.nseg - 2;
+        p2.x0_mode = kX0Identity;
+        p2.drive = 0;
+        p2.records = 0;
+        p2.Xseg = M;
+        p2.X_end = nullptr;
+        int dev = 0, sms = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return e;
+        const bool one_wave = static_cast<long>(chains) * (p1.seg_count + p2.seg_count) <= sms;
+        if (pl.nseg <= 2 || !one_wave) {
+            kern<<<chains * p1.seg_count, kScanThreads, SC_BYTES, a.stream>>>(p1);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            if (pl.nseg > 2) {
+                kern<<<chains * p2.seg_count, kScanThreads, SC_BYTES, a.stream>>>(p2);
+                if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            }
+        } else {
+            if (dev < 0 || dev >= kMaxCarryDevices) return cudaErrorInvalidDevice;
+            std::lock_guard<std::mutex> lock(g_carry_aux_mutex[dev]);
+            CarryAux &ax = g_carry_aux[dev];
+            if (!ax.s) {
+                if ((e = cudaStreamCreateWithFlags(&ax.s, cudaStreamNonBlocking)) != cudaSuccess ||
+                    (e = cudaEventCreateWithFlags(&ax.fork, cudaEventDisableTiming)) != cudaSuccess ||
+                    (e = cudaEventCreateWithFlags(&ax.join, cudaEventDisableTiming)) != cudaSuccess)
+                    return e;
+            }
+            if ((e = cudaEventRecord(ax.fork, a.stream)) != cudaSuccess ||
+                (e = cudaStreamWaitEvent(ax.s, ax.fork, 0)) != cudaSuccess)
+                return e;
+            kern<<<chains * p1.seg_count, kScanThreads, SC_BYTES, a.stream>>>(p1);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            kern<<<chains * p2.seg_count, kScanThreads, SC_BYTES, ax.s>>>(p2);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            if ((e = cudaEventRecord(ax.join, ax.s)) != cudaSuccess ||
+                (e = cudaStreamWaitEvent(a.stream, ax.join, 0)) != cudaSuccess)
+                return e;
         }
         // pass 2: true start states of segments 1..n-1; pass 3: rerun them with records
         if ((e = launch_seg_combine(Z, M, Sst, chains, pl.nseg, a.stream)) != cudaSuccess) return e;
