@@ -110,12 +110,11 @@ size_t kla_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v, int c
 
 }  // extern "C"
 
-namespace {
-
-kla_status chunk_fwd_impl(const void *q, const void *k, const void *v, const float *alpha, const float *eta,
-                          float eps, const float *S0, void *o, float *S_T, int B, int T, int H, int d_k, int d_v,
-                          int chunk, kla_dtype dtype, kla_gate gate, kla_beta_mode beta_mode, float q_scale,
-                          void *workspace, size_t workspace_bytes, void *stream, int no_segments) {
+// Every argument check of the chunk forward except the workspace's.
+kla_status kla::check_chunk_fwd(const void *q, const void *k, const void *v, const float *alpha, const float *eta,
+                                float eps, const float *S0, const void *o, const float *S_T, int B, int T, int H,
+                                int d_k, int d_v, int chunk, kla_dtype dtype, kla_gate gate,
+                                kla_beta_mode beta_mode, float q_scale) {
     if (T < 0) return KLA_ERR_INVALID_ARG;
     if (!valid_mode(beta_mode, q_scale)) return KLA_ERR_INVALID_ARG;
     kla_status st = check_common(q, k, v, alpha, eta, o, B, H, d_k, d_v, dtype, gate, 16,
@@ -123,8 +122,6 @@ kla_status chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
     if (st != KLA_OK) return st;
     if (!supported_chunk(chunk)) return KLA_ERR_UNSUPPORTED;
     if ((S0 && !aligned16(S0)) || (S_T && !aligned16(S_T))) return KLA_ERR_INVALID_ARG;
-    const size_t need = no_segments ? 0 : kla_chunk_fwd_workspace_size(B, T, H, d_k, d_v, chunk, dtype, gate);
-    if (workspace_bytes < need || (need > 0 && !workspace)) return KLA_ERR_INVALID_ARG;
     if (!(eps == eps)) return KLA_ERR_INVALID_ARG;   // NaN stabiliser
 
     // The final state may alias S0 exactly but must not overlap anything else.
@@ -141,6 +138,21 @@ kla_status chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
             if (x.hi > x.lo && overlaps(s, x)) return KLA_ERR_INVALID_ARG;
         if (S0 && S0 != S_T && overlaps(s, span(S0, sbytes))) return KLA_ERR_INVALID_ARG;
     }
+    return KLA_OK;
+}
+
+namespace {
+
+kla_status chunk_fwd_impl(const void *q, const void *k, const void *v, const float *alpha, const float *eta,
+                          float eps, const float *S0, void *o, float *S_T, int B, int T, int H, int d_k, int d_v,
+                          int chunk, kla_dtype dtype, kla_gate gate, kla_beta_mode beta_mode, float q_scale,
+                          void *workspace, size_t workspace_bytes, void *stream, int no_segments) {
+    kla_status st = kla::check_chunk_fwd(q, k, v, alpha, eta, eps, S0, o, S_T, B, T, H, d_k, d_v, chunk, dtype,
+                                         gate, beta_mode, q_scale);
+    if (st != KLA_OK) return st;
+    const size_t need = no_segments ? 0 : kla_chunk_fwd_workspace_size(B, T, H, d_k, d_v, chunk, dtype, gate);
+    if (workspace_bytes < need || (need > 0 && !workspace)) return KLA_ERR_INVALID_ARG;
+    const size_t sbytes = static_cast<size_t>(B) * H * d_k * d_v * 4;
 
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (T == 0) {   // no tokens: the final state is the initial state

@@ -137,9 +137,10 @@ extern "C" kla_status kla_chunk_fwd_host(const void *q_h, const void *k_h, const
             }
             st = kla_chunk_fwd_ex(qp, kp, vp, ap, ep, eps, s0p, atw(o_d, b0 * v_b), stp, nb, T, H, d_k, d_v, chunk, dtype,
                                   gate, beta_mode, q_scale, scratch, KLA_NOALLOC_SCRATCH_BYTES, comp);
-            if (st != KLA_OK) break;
+            // recorded even when the prefill failed part-way: kernels it did enqueue may still use
+            // the array, and the next user of the array must wait for them
             ok = cudaEventRecord(P.scratch_free, comp) == cudaSuccess;
-            if (!ok) break;
+            if (st != KLA_OK || !ok) break;
         } else {
             st = kla::chunk_fwd_nosplit(qp, kp, vp, ap, ep, eps, s0p, atw(o_d, b0 * v_b), stp, nb, T, H, d_k, d_v, chunk,
                                         dtype, gate, beta_mode, q_scale, comp);

@@ -74,6 +74,12 @@ kla_status chunk_fwd_nosplit(const void *q, const void *k, const void *v, const 
                              int chunk, kla_dtype dtype, kla_gate gate, kla_beta_mode beta_mode, float q_scale,
                              void *stream);
 
+// Every argument check of kla_chunk_fwd_ex except the workspace's (its errors, in its order).
+kla_status check_chunk_fwd(const void *q, const void *k, const void *v, const float *alpha, const float *eta,
+                           float eps, const float *S0, const void *o, const float *S_T, int B, int T, int H, int d_k,
+                           int d_v, int chunk, kla_dtype dtype, kla_gate gate, kla_beta_mode beta_mode,
+                           float q_scale);
+
 // tcgen05 tensor-core chunk path: bf16, d_k = d_v = 128, chunk = 64.
 bool chunk_tc_supports(const ChunkArgs &a);
 cudaError_t launch_chunk_tc(const ChunkArgs &a);

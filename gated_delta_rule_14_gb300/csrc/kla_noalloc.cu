@@ -55,6 +55,10 @@ extern "C" kla_status kla_chunk_fwd_noalloc(const void *q, const void *k, const 
                                             const float *eta, float eps, const float *S0, void *o, float *S_T,
                                             int B, int T, int H, int d_k, int d_v, int chunk, kla_dtype dtype,
                                             kla_gate gate, void *stream) {
+    // the errors of kla_chunk_fwd come first; only a valid call is refused for its size
+    const kla_status st = kla::check_chunk_fwd(q, k, v, alpha, eta, eps, S0, o, S_T, B, T, H, d_k, d_v, chunk, dtype,
+                                               gate, KLA_BETA_KACZMARZ, 1.0f);
+    if (st != KLA_OK) return st;
     const size_t need = kla_chunk_fwd_workspace_size(B, T, H, d_k, d_v, chunk, dtype, gate);
     if (need > static_cast<size_t>(KLA_NOALLOC_SCRATCH_BYTES)) return KLA_ERR_UNSUPPORTED;
     void *scratch = nullptr;

@@ -36,6 +36,10 @@
  *    return KLA_ERR_INVALID_ARG or KLA_ERR_UNSUPPORTED; nothing is written then.
  *  - Device-side waits are bounded; a wait that gives up records a flag that
  *    kla_device_status() reports as KLA_ERR_TIMEOUT.
+ *  - The library keeps a few per-device objects for the life of the process (streams and
+ *    events of its own, the device addresses of its error word and scratch array, looked up
+ *    on first use). cudaDeviceReset() destroys them: do not call into the library on a
+ *    device after resetting it.
  *  - Supported sizes: d_k, d_v in {16, 32, 64, 128}; chunk in {16, 32, 64}.
  *    bf16 inputs with d_k = d_v = 128 and chunk = 64 run on the tensor-core
  *    (tcgen05) path; every other supported case runs on the fp32 CUDA-core path.
@@ -145,8 +149,9 @@ size_t kla_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v, int c
  * long sequence with few (sequence, head) chains is split into segments) comes instead from a
  * fixed array of KLA_NOALLOC_SCRATCH_BYTES inside the library's device image; every GPU that
  * loads the library holds that array until the process exits.
- *  - Sizes whose scratch (kla_chunk_fwd_workspace_size) exceeds KLA_NOALLOC_SCRATCH_BYTES are
- *    rejected with KLA_ERR_UNSUPPORTED before anything is launched.
+ *  - The arguments are checked first, exactly as kla_chunk_fwd checks them (same errors); a
+ *    valid call whose scratch (kla_chunk_fwd_workspace_size) exceeds KLA_NOALLOC_SCRATCH_BYTES
+ *    is then rejected with KLA_ERR_UNSUPPORTED, before anything is launched.
  *  - The first call on a device that needs scratch looks up the array's device address with
  *    that device current (a host-side runtime query, no allocation); make that first call
  *    before any stream capture.

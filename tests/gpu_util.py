@@ -48,6 +48,19 @@ def oracle_chains(inp, chains=None, **mode):
     return o[:, :, 0], S[:, 0]
 
 
+def oracle_whole(inp, **mode):
+    """fp64 oracle over the whole input (every chain, all host cores): o [B,T,H,dv], S_T [B,H,dk,dv]."""
+    return oracle.recurrent(inp.as_f64("q"), inp.as_f64("k"), inp.as_f64("v"), inp.as_f64("alpha"),
+                            inp.as_f64("eta"), inp.wl.eps, inp.as_f64("S0"), nthreads=os.cpu_count() or 1, **mode)
+
+
+def worst_chain(o, o_ref):
+    """Largest per-(sequence, head) relative L2 error of o [B,T,H,dv]: a diagnostic beside the
+    whole-tensor figure."""
+    B, H = o.shape[0], o.shape[2]
+    return max(oracle.rel_l2(o[b, :, h], o_ref[b, :, h]) for b in range(B) for h in range(H))
+
+
 def gather_chains(o, S, chains):
     return (np.stack([o[b, :, h] for b, h in chains]), np.stack([S[b, h] for b, h in chains]))
 

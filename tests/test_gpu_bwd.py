@@ -9,12 +9,14 @@ Two paths, two bars:
     forward's tensor-core path; they are held to the bf16 bar of the forward, 1e-2;
   * every other shape runs the token-by-token fp32 backward: 1e-5 for fp32 inputs, 1e-4 for bf16
     inputs (longer sums of larger terms)."""
+import os
+
 import numpy as np
 import pytest
 
 import oracle
 import synth
-from gpu_util import DEV, sample_chains, to_dev
+from gpu_util import DEV, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -134,17 +136,28 @@ def test_backward_without_ds0_and_empty_sequence():
     assert torch.equal(g["dS0"], dst)
 
 
-@pytest.mark.parametrize("name,nchains", [("gdn4k", 2), ("kda8k", 1)])
-def test_full_config_sampled(name, nchains):
-    """The bench configuration (all chains on the GPU), checked on sampled chains."""
+def run_oracle_whole(inp, dO, dST, **mode):
+    """Oracle gradients of the whole input in one call, chains split over the host cores. The
+    oracle keeps every state of the chains it is working on ((T + 1) d_k d_v doubles each), so the
+    thread count is capped to hold that under ~8 GB."""
+    wl = inp.wl
+    per_chain = (wl.T + 1) * wl.d_k * wl.d_v * 8
+    threads = max(1, min(os.cpu_count() or 1, int(8e9 // per_chain)))
+    g = oracle.load().backward(_as64(inp.q), _as64(inp.k), _as64(inp.v), _as64(inp.alpha), _as64(inp.eta), wl.eps,
+                               None if inp.S0 is None else inp.S0.astype(np.float64), _as64(dO),
+                               None if dST is None else dST.astype(np.float64), nthreads=threads, **mode)
+    return {n: g[n] for n in NAMES}
+
+
+@pytest.mark.parametrize("name", ["gdn4k", "kda8k"])
+def test_full_config_whole_tensor(name):
+    """The backward of the prefill workloads at full size (gdn4k on the chunkwise path, kda8k on
+    the token-sequential one), every gradient compared over the whole tensor."""
     inp = synth.make_prefill(name, seed=1)
-    if name == "kda8k":
-        inp = synth.make_prefill(name, seed=1, T=2048)   # keeps the oracle's stored states small
     dO, dST = _grad_inputs(inp, seed=2, with_dst=True)
     got = run_gpu(inp, dO, dST)
-    chains = sample_chains(inp.wl.B, inp.wl.H, nchains, seed=5)
-    ref = run_oracle(inp, dO, dST, chains)
-    compare(pick(got, chains), ref, tol(inp.wl))
+    ref = run_oracle_whole(inp, dO, dST)
+    compare(got, ref, tol(inp.wl))
 
 
 def test_chunked_backward_is_deterministic():

@@ -6,7 +6,7 @@ import torch
 
 import oracle
 import synth
-from gpu_util import DEV, decode_oracle, sample_chains, to_dev
+from gpu_util import DEV, decode_oracle, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -35,15 +35,18 @@ def test_decode_small(dtype, d, gate):
     assert oracle.rel_l2(o_g, o_ref) <= tol and oracle.rel_l2(s_g, s_ref) <= tol
 
 
-def test_decode_full_config_sampled():
+def test_decode_full_config_whole_tensor():
+    """The decode workload at full size (64 sequences x 16 heads, 1024 steps) against the oracle
+    over every head: relative L2 over all outputs of all steps and over the whole final state."""
     dd = synth.make_decode(seed=0)
     o, S = run_decode(dd)
     assert np.isfinite(o).all() and np.isfinite(S).all()
-    heads = sample_chains(dd.wl.B, dd.wl.H, 16, seed=2)
+    heads = [(b, h) for b in range(dd.wl.B) for h in range(dd.wl.H)]
     o_ref, s_ref = decode_oracle(dd, heads)
     o_g = np.stack([o[:, b, h] for b, h in heads])
     s_g = np.stack([S[b, h] for b, h in heads])
-    assert oracle.rel_l2(o_g, o_ref) <= 1e-2 and oracle.rel_l2(s_g, s_ref) <= 1e-2
+    eo, es = oracle.rel_l2(o_g, o_ref), oracle.rel_l2(s_g, s_ref)
+    assert eo <= 1e-2 and es <= 1e-2, f"rel-L2 o={eo:.3e} S={es:.3e}"
 
 
 def test_decode_equals_one_token_prefill():
