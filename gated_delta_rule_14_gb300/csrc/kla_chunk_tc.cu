@@ -30,12 +30,17 @@
 //    state update, the output tile and its TMA store;
 //  * operand group (warps 8-15): meanwhile builds the state-independent operands of chunk
 //    c+1: gates, norms, [K;Q] K^T, R and A, T = (I + R)^{-1}, W^T and U^T.
-// The 64 x 64 unit-lower inverse T is computed in fp32: 16 x 16 diagonal blocks by
-// substitution, then two levels of block merging (16 -> 32 -> 64) on warp-level tf32 MMAs.
-// The groups hand over through mbarriers that alternate strictly (no wait can alias a phase
-// two steps back): `ready` (operands of chunk c are complete), `freed` (the state group has
-// consumed the single-buffered W^T tile and U^T of chunk c), `done[c&1]` (chunk c is fully
-// retired: its A tile, gate vectors and q/k/v stage may be reused).
+// The 64 x 64 unit-lower inverse T is computed in fp32, in place over R: 16 x 16 diagonal
+// blocks by substitution, then two levels of block merging (16 -> 32 -> 64) on warp-level tf32
+// MMAs. The groups hand over through mbarriers that alternate strictly (no wait can alias a
+// phase two steps back): `ready` (operands of chunk c are complete), `freed` (the state group
+// has consumed the single-buffered W^T tile and U^T of chunk c), `done[c&1]` (the gate vectors
+// of chunk c+2 are written). The q/k stage of chunk c is refilled with chunk c+2 as soon as
+// the products reading its Q and K tiles have completed; its landing (`full`) also orders the
+// reuse of chunk c's A tile. The v tile is single-buffered: it takes chunk c+1 as soon as the
+// U^T product of chunk c has read it. Per-channel gate: K_end alternates between two buffers,
+// so the operand group's scaled tiles of chunk c+1 do not wait for E^T K_end of chunk c.
+// Every tcgen05.mma is issued by one elected lane inside a warp-uniform branch.
 #include <cuda.h>
 
 #include <algorithm>
@@ -55,6 +60,7 @@ constexpr int kD = 128;         // d_k = d_v
 constexpr int kGroup = 256;     // threads per warp group
 constexpr int kThreads = 2 * kGroup;
 constexpr uint32_t kBarState = 1, kBarOperand = 2;   // named barriers of the two groups
+constexpr uint32_t kBarPair0 = 3;                     // 3..6: warp pairs of the operand group (solve)
 constexpr float kMinLogGate = -80.0f;
 constexpr float kSafeDecay = -80.0f;   // chunk decay above which e^{-G_j} is representable
 constexpr uint32_t kWaitLimit = 100000;   // x 20 us: a stuck wait gives up after ~2 s
@@ -62,17 +68,19 @@ constexpr uint32_t kWaitLimit = 100000;   // x 20 us: a stuck wait gives up afte
 // ---- shared memory map (offsets from a 1024-byte aligned base)
 constexpr uint32_t OFF_QK = 0;                        // 2 stages x 32 KB: [blk0: K rows | Q rows][blk1 ...]
 constexpr uint32_t QK_STAGE = 32768;
-constexpr uint32_t OFF_V = OFF_QK + 2 * QK_STAGE;     // 2 stages x 16 KB: [blk0: 64 rows][blk1: 64 rows]
-constexpr uint32_t V_STAGE = 16384;
-constexpr uint32_t OFF_AQK = OFF_V + 2 * V_STAGE;     // 2 x 8 KB: A (query rows) bf16, K-major
-constexpr uint32_t OFF_WT = OFF_AQK + 2 * 8192;       // 16 KB: T fp32 during the solve, then W^T bf16
+constexpr uint32_t OFF_V = OFF_QK + 2 * QK_STAGE;     // 16 KB: v tile [blk0: 64 rows][blk1: 64 rows], refilled
+                                                      // as soon as the U^T product has read it
+constexpr uint32_t OFF_KE1 = OFF_V + 16384;           // 16 KB: per-channel gate: K_end of odd chunks
+constexpr uint32_t OFF_AQK = OFF_KE1 + 16384;         // 2 x 8 KB: A (query rows) bf16, K-major
+constexpr uint32_t OFF_WT = OFF_AQK + 2 * 8192;       // 16 KB: T_K | T_V bf16 for the W^T/U^T MMAs, then W^T bf16
 constexpr uint32_t OFF_ST = OFF_WT + 16384;           // 32 KB: S^T bf16, K-major, 2 blocks of 128 rows
 constexpr uint32_t OFF_ET = OFF_ST + 32768;           // 16 KB: E^T bf16
 constexpr uint32_t OFF_ETS = OFF_ET + 16384;          // 16 KB: E^T diag(e^{G_end-G}) bf16, then O staging
-constexpr uint32_t OFF_R = OFF_ETS + 16384;           // 16 KB: R fp32, then T_K | T_V bf16 tiles
+                                                      // (per-channel gate: K_end of even chunks)
+constexpr uint32_t OFF_R = OFF_ETS + 16384;           // 16 KB: R fp32, overwritten in place by T = (I + R)^{-1}
 constexpr uint32_t OFF_XS = OFF_R + 16384;            // 7 KB: solve scratch
 constexpr uint32_t OFF_SMALL = OFF_XS + 7168;         // per-chunk vectors + barriers
-constexpr uint32_t SMALL_BYTES = 8192;
+constexpr uint32_t SMALL_BYTES = 10240;
 constexpr uint32_t SMEM_BYTES = OFF_SMALL + SMALL_BYTES + 1024;   // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
@@ -85,9 +93,8 @@ constexpr uint32_t TM_1B = 256;   // (Q S)^T           64
 constexpr uint32_t TM_3 = 320;    // (A E)^T           64
 constexpr uint32_t TM_2 = 384;    // (K_end^T E)^T     128
 
-constexpr uint32_t kTileBytes = 4 * 8192 + 2 * 8192;   // q, k, v chunk tiles per stage
 
-struct ChunkVec {          // per-chunk vectors (double-buffered by chunk parity)
+struct ChunkVec {          // per-chunk vectors (three buffers, by chunk index mod 3)
     float G[kC];           // inclusive prefix of log-gates
     float beta[kC];
     float eG[kC];          // e^{G_i}
@@ -106,15 +113,16 @@ struct ChanVec {
     float eGr[kD];         // e^{G_r}: scales the state operand
     float gam[kD];         // e^{G_end}: decay of the state over the chunk
     float F[kD];           // e^{G_end - G_r}
-    float pad[kD];
 };
 struct Small {
-    ChunkVec v[2];
-    ChanVec ch[2];
-    uint64_t full[2];              // q/k/v stage landed (TMA)
+    ChunkVec v[3];                 // chunk c uses buffer c % 3: the vectors of chunk c+2 can be
+    ChanVec ch[3];                 // written while chunks c and c+1 are still in use
+    uint64_t full[2];              // q/k stage landed (TMA), by chunk parity
+    uint64_t fullv;                // v tile landed (TMA), once per chunk
+    uint64_t m2k[2];               // per-channel gate: E^T K_end of chunk c done (its K_end buffer c & 1 is free)
     uint64_t mA, mW, m1, m2, mO;   // tcgen05.commit of the five MMA groups
     uint64_t ready, freed;         // operand group -> state group, state group -> operand group
-    uint64_t done[2];              // chunk retired, by parity
+    uint64_t done[2];              // gate vectors of chunk c+2 written, by the parity of c
     uint32_t tmem_base;
     volatile int abort;
 };
@@ -176,7 +184,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t sbase = smem_u32(smem);
     Small &sm = *reinterpret_cast<Small *>(smem + OFF_SMALL);
     float *Rm = reinterpret_cast<float *>(smem + OFF_R);    // R, swizzled fp32 [64][64]
-    float *Tm = reinterpret_cast<float *>(smem + OFF_WT);   // T, swizzled fp32 [64][64]
+    float *Tm = Rm;                                         // T replaces R block by block
     float *Xs = reinterpret_cast<float *>(smem + OFF_XS);   // solve scratch
     __shared__ int abort_snap[2];
 
@@ -198,6 +206,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t bar_1 = smem_u32(&sm.m1), bar_2 = smem_u32(&sm.m2), bar_o = smem_u32(&sm.mO);
     const uint32_t bar_ready = smem_u32(&sm.ready), bar_freed = smem_u32(&sm.freed);
     const uint32_t bar_done0 = smem_u32(&sm.done[0]);
+    const uint32_t bar_fullv = smem_u32(&sm.fullv), bar_m2k0 = smem_u32(&sm.m2k[0]);
 
     if (tid == 0) {
         mbar_init(bar_full0, 1);
@@ -211,6 +220,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_init(bar_freed, 1);
         mbar_init(bar_done0, 1);
         mbar_init(bar_done0 + 8, 1);
+        mbar_init(bar_fullv, 1);
+        mbar_init(bar_m2k0, 1);
+        mbar_init(bar_m2k0 + 8, 1);
         sm.abort = 0;
         abort_snap[0] = abort_snap[1] = 0;
         fence_mbar_init();
@@ -235,22 +247,26 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t id_2 = idesc_bf16(128, 128, 0, 1);     // N=128, MN-major B
 
     auto qk_of = [&](int c) { return sbase + OFF_QK + (c & 1) * QK_STAGE; };
-    auto v_of = [&](int c) { return sbase + OFF_V + (c & 1) * V_STAGE; };
+    auto v_of = [&](int) { return sbase + OFF_V; };
+    auto ke_of = [&](int c) { return sbase + ((c & 1) ? OFF_KE1 : OFF_ETS); };   // per-channel gate: K_end
     auto aqk_of = [&](int c) { return sbase + OFF_AQK + (c & 1) * 8192; };
 
-    auto issue_loads = [&](int c) {   // one thread
+    auto issue_loads = [&](int c) {   // q and k tiles of chunk c; one thread
         const uint32_t bar = bar_full0 + 8 * (c & 1);
-        const uint32_t qk = qk_of(c), vv = v_of(c);
-        mbar_arrive_expect_tx(bar, p.zero_v ? 4 * 8192 : kTileBytes);
+        const uint32_t qk = qk_of(c);
+        mbar_arrive_expect_tx(bar, 4 * 8192);
         const int t0 = t_begin + c * kC;
         tma_load_4d(qk + 0, &tm_k, bar, 0, h, t0, b);
         tma_load_4d(qk + 8192, &tm_q, bar, 0, h, t0, b);
         tma_load_4d(qk + 16384, &tm_k, bar, 64, h, t0, b);
         tma_load_4d(qk + 24576, &tm_q, bar, 64, h, t0, b);
-        if (!p.zero_v) {
-            tma_load_4d(vv + 0, &tm_v, bar, 0, h, t0, b);
-            tma_load_4d(vv + 8192, &tm_v, bar, 64, h, t0, b);
-        }
+    };
+    auto issue_v = [&](int c) {   // v tile of chunk c; one thread
+        const uint32_t vv = v_of(c);
+        mbar_arrive_expect_tx(bar_fullv, 2 * 8192);
+        const int t0 = t_begin + c * kC;
+        tma_load_4d(vv + 0, &tm_v, bar_fullv, 0, h, t0, b);
+        tma_load_4d(vv + 8192, &tm_v, bar_fullv, 64, h, t0, b);
     };
     auto wait = [&](uint32_t bar, uint32_t parity) {
         if (!mbar_wait_bounded(bar, parity, kWaitLimit)) sm.abort = 1;
@@ -267,6 +283,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (tid == 0) {
         issue_loads(0);
         if (nchunks > 1) issue_loads(1);
+        if (!p.zero_v) issue_v(0);
     }
 
     // Per-token gate vectors (G, e^{G}, e^{-G}, e^{G_end - G}, eta) of a chunk are computed by
@@ -287,7 +304,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     };
     auto gate_vec = [&](int c) {   // warp 0 only
         if (c >= nchunks) return;
-        ChunkVec &cv = sm.v[c & 1];
+        ChunkVec &cv = sm.v[c % 3];
         const float g0 = fmaxf(__logf(a_nx[0]), kMinLogGate), g1 = fmaxf(__logf(a_nx[1]), kMinLogGate);
         float s = g0 + g1;
 #pragma unroll
@@ -319,56 +336,81 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __syncthreads();
 
     // ===================================================================== operand group
-    // Per-channel gates (per-channel gate only): thread = (key channel ch, token half th) holds
-    // the 32 gates of its half of the next chunk. The loads are issued a chunk ahead and left
-    // untouched until their first use (`chgate`), so the thread does not wait for them; tokens
-    // past the end load the last token's gate and read as 1, and gates are clamped to e^-80
-    // like the log-gates.
-    const int gch = gtid & (kD - 1), gth = gtid >> 7;
-    float ga[kCh ? 32 : 1];
+    // Per-channel gates (per-channel gate only): thread = (8-channel group cg, token half th,
+    // 4-token sub-range sb of the half): lanes sb = lane % 8 of one warp share (cg, th), so the
+    // running products of the gates across a half are shuffle scans over those 8 lanes. A thread
+    // holds its 4 x 8 gates of the next chunk; the loads are issued a chunk ahead and left
+    // untouched until their first use (`chgate`), so the thread does not wait for them. Tokens
+    // past the end load the last token's gate and read as 1, and gates are clamped to e^-80 like
+    // the log-gates.
+    const int csb = lane & 7, cgth = gw * 4 + (lane >> 3);
+    const int ccg = cgth & 15, cth = cgth >> 4;
+    float ga[kCh ? 4 : 1][kCh ? 8 : 1];
     auto load_chgates = [&](int c) {
         if constexpr (kCh) {
             if (grp == 1 && c < nchunks) {
-                const int t0 = t_begin + c * kC + 32 * gth;
-                const int last = min(31, t_end - 1 - t0);   // tokens past the end read token t_end - 1
-                const float *g0 = p.alpha + ((static_cast<size_t>(b) * p.T + t0) * p.H + h) * kD + gch;
-                const size_t st = static_cast<size_t>(p.H) * kD;
 #pragma unroll
-                for (int u = 0; u < 32; ++u) ga[u] = g0[static_cast<size_t>(min(u, last)) * st];
+                for (int u = 0; u < 4; ++u) {
+                    const int t = min(t_begin + c * kC + 32 * cth + 4 * csb + u, t_end - 1);
+                    const float *g0 = p.alpha + ((static_cast<size_t>(b) * p.T + t) * p.H + h) * kD + 8 * ccg;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) ga[u][j] = g0[j];
+                }
             }
         }
     };
-    auto chgate = [&](int c, int u) {   // gate u of this thread's half of chunk c
-        return t_begin + c * kC + 32 * gth + u < t_end ? fmaxf(ga[u], 1.8e-35f) : 1.f;
+    auto chgate = [&](int c, int u, int j) {   // gate of token u of this thread's sub-range, channel j of its group
+        return t_begin + c * kC + 32 * cth + 4 * csb + u < t_end ? fmaxf(ga[u][j], 1.8e-35f) : 1.f;
     };
 
     // (a) gates, norms, beta and the decay tables; issue [K;Q] K^T.
     auto op_front = [&](int c) {
-        ChunkVec &cv = sm.v[c & 1];
+        ChunkVec &cv = sm.v[c % 3];
         const uint32_t qk = qk_of(c);
-        if (c >= 2) wait(bar_done0 + 8 * (c & 1), ((c - 2) >> 1) & 1);   // chunk c-2 retired
-        // T_K/T_V (R area) and TM_W/TM_U of chunk c-1 are read by its W^T/U^T MMAs
-        if (c >= 1) wait(bar_W, (c - 1) & 1);
-        // per-channel: products of the gates over each half of the chunk
-        float zprod = 1.f;
+        if (c >= 2) wait(bar_done0 + 8 * (c & 1), ((c - 2) >> 1) & 1);   // gate vectors of chunk c
+        // per-channel: products of the gates over each half of the chunk; `ex` is the product over
+        // the sub-ranges between this thread's and the reference token (before it in half 1, after
+        // it in half 0), `tot` over the whole half
+        float ex[kCh ? 8 : 1], tot[kCh ? 8 : 1];
         if constexpr (kCh) {
+            bool low = false;
 #pragma unroll
-            for (int u = 0; u < 32; ++u) zprod *= chgate(c, u);
-            ChanVec &chv = sm.ch[c & 1];
-            if (gth == 0) chv.eGr[gch] = zprod;   // e^{G_r}
-            else chv.F[gch] = zprod;              // e^{G_end - G_r}
-            if (zprod < 1.8e-35f) atomicOr(p.err, kErrGateRange);
+            for (int j = 0; j < 8; ++j) {
+                float l = 1.f;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) l *= chgate(c, u, j);
+                float sc = l;   // inclusive scan towards the reference token
+#pragma unroll
+                for (int off = 1; off < 8; off <<= 1) {
+                    const float y = cth ? __shfl_up_sync(0xffffffffu, sc, off, 8)
+                                        : __shfl_down_sync(0xffffffffu, sc, off, 8);
+                    if (cth ? csb >= off : csb + off < 8) sc *= y;
+                }
+                const float nb = cth ? __shfl_up_sync(0xffffffffu, sc, 1, 8) : __shfl_down_sync(0xffffffffu, sc, 1, 8);
+                ex[j] = (cth ? csb == 0 : csb == 7) ? 1.f : nb;
+                tot[j] = __shfl_sync(0xffffffffu, sc, cth ? 7 : 0, 8);
+                low |= tot[j] < 1.8e-35f;
+            }
+            ChanVec &chv = sm.ch[c % 3];
+            if (csb == 0) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) (cth ? chv.F : chv.eGr)[8 * ccg + j] = tot[j];   // e^{G_end-G_r} | e^{G_r}
+                if (low) atomicOr(p.err, kErrGateRange);
+            }
         }
         wait(bar_full0 + 8 * (c & 1), (c >> 1) & 1);
-        if (!kCh && gtid == 0) {   // scalar gate: [K;Q] K^T needs only the tiles; issue it first
+        if (!kCh && gw == 0) {   // scalar gate: [K;Q] K^T needs only the tiles; issue it first
             tc_fence_after();
-            const uint64_t dq = sw128_desc(qk, 16, 1024);
+            if (elect_one()) {
+                const uint64_t dq = sw128_desc(qk, 16, 1024);
 #pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
-                mma_bf16(tbase + TM_A, desc_add(dq, off), desc_add(dq, off), id_qk, s);
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
+                    mma_bf16(tbase + TM_A, desc_add(dq, off), desc_add(dq, off), id_qk, s);
+                }
+                mma_commit(bar_A);
             }
-            mma_commit(bar_A);
+            __syncwarp();
         }
         // ||k_i||^2: 4 threads per key row, 32 channels each
         float n2 = 0.f;
@@ -396,38 +438,59 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // Scaled tiles with reference token r: K_r = K e^{G-G_r}, Q_r = Q e^{G-G_r} (in place),
             // K_m = K e^{G_r-G} (B of [K_r;Q_r] K_m^T, over the R area) and K_end = K e^{G_end-G}
             // (B of E^T K_end, over the E^T_s area, free once E^T K_end of chunk c-1 has run).
-            ChanVec &chv = sm.ch[c & 1];
-            const float F = chv.F[gch];
-            if (gth == 0) chv.gam[gch] = zprod * F;
-            if (c >= 1) wait(bar_2, (c - 1) & 1);
-            const uint32_t col = (gch & 63) * 2, blk = gch >> 6;
-            const uint32_t Kt = qk + blk * 16384, Qt = Kt + 8192;
-            const uint32_t Km = sbase + OFF_R + blk * 8192, Ke = sbase + OFF_ETS + blk * 8192;
-            auto bits = [](float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); };
-            float run = 1.f;
+            ChanVec &chv = sm.ch[c % 3];
+            float Fv[8];
 #pragma unroll
-            for (int u = 0; u < 32; ++u) {
-                // th 1: tokens 32..63 ascending, run = e^{G_i - G_r};  th 0: tokens 31..0, run = e^{G_r - G_i}
-                // (the factors scale bf16 operands: the fast reciprocal's 2 ulp are far below bf16's)
-                const int uu = gth ? u : 31 - u;
-                const int i = 32 * gth + uu;
-                float fr, fm;
-                if (gth) {
-                    run *= chgate(c, uu);
-                    fr = run;
-                    fm = __fdividef(1.f, run);
-                } else {
-                    fm = run;
-                    fr = __fdividef(1.f, run);
-                    run *= chgate(c, uu);
+            for (int j = 0; j < 8; ++j) Fv[j] = chv.F[8 * ccg + j];
+            if (cth == 0 && csb == 0) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) chv.gam[8 * ccg + j] = tot[j] * Fv[j];   // e^{G_end}
+            }
+            // K_end of this chunk goes to buffer c & 1: E^T K_end of chunk c-2 must have read it
+            if (c >= 2) wait(bar_m2k0 + 8 * (c & 1), ((c - 2) >> 1) & 1);
+            const uint32_t blk = ccg >> 3, colb = (ccg & 7) * 16;
+            const uint32_t Kt = qk + blk * 16384, Qt = Kt + 8192;
+            const uint32_t Km = sbase + OFF_R + blk * 8192, Ke = ke_of(c) + blk * 8192;
+            float run[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) run[j] = ex[j];
+#pragma unroll
+            for (int step = 0; step < 4; ++step) {
+                // half 1: tokens ascending from the reference, run = e^{G_i - G_r}; half 0: tokens
+                // descending towards the chunk start, run = e^{G_r - G_i} (the factors scale bf16
+                // operands: the fast reciprocal's 2 ulp are far below bf16's)
+                const int u = cth ? step : 3 - step;
+                const int i = 32 * cth + 4 * csb + u;
+                float fr[8], fm[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (cth) {
+                        run[j] *= chgate(c, u, j);
+                        fr[j] = run[j];
+                        fm[j] = __fdividef(1.f, run[j]);
+                    } else {
+                        fm[j] = run[j];
+                        fr[j] = __fdividef(1.f, run[j]);
+                        run[j] *= chgate(c, u, j);
+                    }
                 }
-                const uint32_t off = sw128_off(i, col);
-                const float kv = ld_shared_bf16(Kt + off);
-                const float qv = ld_shared_bf16(Qt + off);
-                st_shared_b16(Kt + off, bits(kv * fr));
-                st_shared_b16(Qt + off, bits(qv * fr));
-                st_shared_b16(Km + off, bits(kv * fm));
-                st_shared_b16(Ke + off, bits(kv * (F * fm)));
+                const uint32_t off = sw128_off(i, colb);
+                const uint4 kx = ld_shared_v4(Kt + off), qx = ld_shared_v4(Qt + off);
+                const uint32_t kw[4] = {kx.x, kx.y, kx.z, kx.w}, qw[4] = {qx.x, qx.y, qx.z, qx.w};
+                uint32_t o1[4], o2[4], o3[4], o4[4];
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const float k0 = bf16lo(kw[w]), k1 = bf16hi(kw[w]), q0 = bf16lo(qw[w]), q1 = bf16hi(qw[w]);
+                    const int j0 = 2 * w, j1 = 2 * w + 1;
+                    o1[w] = pack_bf16(k0 * fr[j0], k1 * fr[j1]);
+                    o2[w] = pack_bf16(q0 * fr[j0], q1 * fr[j1]);
+                    o3[w] = pack_bf16(k0 * fm[j0], k1 * fm[j1]);
+                    o4[w] = pack_bf16(k0 * (Fv[j0] * fm[j0]), k1 * (Fv[j1] * fm[j1]));
+                }
+                st_shared_v4(Kt + off, o1[0], o1[1], o1[2], o1[3]);
+                st_shared_v4(Qt + off, o2[0], o2[1], o2[2], o2[3]);
+                st_shared_v4(Km + off, o3[0], o3[1], o3[2], o3[3]);
+                st_shared_v4(Ke + off, o4[0], o4[1], o4[2], o4[3]);
             }
             load_chgates(c + 1);
             fence_proxy_async_smem();
@@ -435,16 +498,19 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             kb_stride = 8192;
             kb_base = sbase + OFF_R;
         }
-        if (kCh && gtid == 0) {
+        if (kCh && gw == 0) {
             tc_fence_after();
-            const uint64_t dq = sw128_desc(qk, 16, 1024), dkb = sw128_desc(kb_base, 16, 1024);
+            if (elect_one()) {
+                const uint64_t dq = sw128_desc(qk, 16, 1024), dkb = sw128_desc(kb_base, 16, 1024);
 #pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
-                const uint32_t boff = (s >> 2) * kb_stride + (s & 3) * 32;
-                mma_bf16(tbase + TM_A, desc_add(dq, off), desc_add(dkb, boff), id_qk, s);
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
+                    const uint32_t boff = (s >> 2) * kb_stride + (s & 3) * 32;
+                    mma_bf16(tbase + TM_A, desc_add(dq, off), desc_add(dkb, boff), id_qk, s);
+                }
+                mma_commit(bar_A);
             }
-            mma_commit(bar_A);
+            __syncwarp();
         }
     };
 
@@ -453,12 +519,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     auto issue_wu = [&](int c) {   // one thread
         tc_fence_after();
         const uint32_t qk = qk_of(c), vv = v_of(c);
-        const uint32_t tw = sbase + OFF_R + (kCh ? 8192 : 0);
+        const uint32_t tw = sbase + OFF_WT + (kCh ? 8192 : 0);
         const uint64_t dk = sw128_desc(qk, 16384, 1024), dtw = sw128_desc(tw, 16, 1024);
 #pragma unroll
         for (int s = 0; s < 4; ++s) mma_bf16(tbase + TM_W, desc_add(dk, s * 2048), desc_add(dtw, s * 32), id_w, s);
         if (!p.zero_v) {
-            const uint64_t dv = sw128_desc(vv, 8192, 1024), dtv = sw128_desc(sbase + OFF_R + 8192, 16, 1024);
+            if (!mbar_wait_bounded(bar_fullv, c & 1, kWaitLimit)) sm.abort = 1;   // v tile of chunk c
+            const uint64_t dv = sw128_desc(vv, 8192, 1024), dtv = sw128_desc(sbase + OFF_WT + 8192, 16, 1024);
 #pragma unroll
             for (int s = 0; s < 4; ++s) mma_bf16(tbase + TM_U, desc_add(dv, s * 2048), desc_add(dtv, s * 32), id_w, s);
         }
@@ -466,7 +533,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     };
     // (b) R and A from [KK^T; QK^T]; T = (I + R)^{-1}; T_K, T_V; issue W^T, U^T.
     auto op_mid = [&](int c) {
-        ChunkVec &cv = sm.v[c & 1];
+        ChunkVec &cv = sm.v[c % 3];
         gsync();   // beta of this chunk visible
         wait(bar_A, c & 1);
         tc_fence_after();
@@ -525,9 +592,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        // The W^T tile area (T lives there during the solve) and U^T are single-buffered: wait
-        // until the state group has consumed those of chunk c-1.
-        if (c >= 1) wait(bar_freed, (c - 1) & 1);
         gsync();
         // ---- diagonal 16x16 blocks (one per warp pair): right-looking substitution in steps of
         // 4 rows. Lane = (row group r4 = lane / 8, column l = 8 (warp & 1) + lane % 8); the lanes of
@@ -563,6 +627,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     }
                 }
             }
+            // both warps of the pair have read this block of R: replace it by the block of T
+            named_sync(kBarPair0 + (gw >> 1), 64);
 #pragma unroll
             for (int u = 0; u < 4; ++u) Tm[fidx(o + 4 * r4 + u, o + l)] = acc[u];
         }
@@ -599,6 +665,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 mma_tf32_16x8x8(e, a, bb);
             }
             const int cc = c0 + 8 * nt + 2 * t4;
+            named_sync(kBarPair0 + pp, 64);   // both warps of the pair have read R_{r0,c0}
             Tm[fidx(r0 + g8, cc)] = -e[0];
             Tm[fidx(r0 + g8, cc + 1)] = -e[1];
             Tm[fidx(r0 + g8 + 8, cc)] = -e[2];
@@ -667,8 +734,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     tk[4 * u4 + u] = tv[4 * u4 + u] * g4[u];
                 }
             }
-            // every read of R ended before the solve's last barrier: T_K/T_V may overwrite it now
-            const uint32_t bk = sbase + OFF_R, bv = sbase + OFF_R + 8192;
+            // T_K/T_V go to the W^T tile area: wait until the state group has consumed W^T and U^T
+            // of chunk c-1 (and so the W^T/U^T MMAs of chunk c-1 have read their T_K/T_V)
+            if (c >= 1) wait(bar_freed, (c - 1) & 1);
+            const uint32_t bk = sbase + OFF_WT, bv = sbase + OFF_WT + 8192;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const uint32_t off = sw128_off(n, 32 * kq + 16 * hh);
@@ -678,9 +747,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         fence_proxy_async_smem();
         gsync();
-        if (gtid == 0) {
-            issue_wu(c);
-            mbar_arrive(bar_ready);   // A, gate vectors and tiles of chunk c written; W^T/U^T in flight
+        if (gw == 0) {
+            tc_fence_after();
+            if (elect_one()) {
+                issue_wu(c);
+                mbar_arrive(bar_ready);   // A, gate vectors and tiles of chunk c written; W^T/U^T in flight
+            }
+            __syncwarp();
         }
     };
 
@@ -707,18 +780,22 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // W^T of chunk c -> bf16 MN-major B operand (rows k, 64 tokens per row), over the T area
         wait(bar_W, c & 1);
         tc_fence_after();
-#pragma unroll
-        for (int pc = 0; pc < 2; ++pc) {
-            uint32_t v[16];
-            tmem_ld16(tlane + TM_W + 32 * half + 16 * pc, v);
+        // U^T of chunk c is computed: the v tile takes chunk c+1
+        if (warp == 0) {
+            if (!p.zero_v && c + 1 < nchunks && elect_one()) issue_v(c + 1);
+            __syncwarp();
+        }
+        {
+            uint32_t v[32];
+            tmem_ld32(tlane + TM_W + 32 * half, v);
             tmem_ld_wait();
 #pragma unroll
-            for (int ch = 0; ch < 2; ++ch)
-                st_bf16x8u(sbase + OFF_WT + sw128_off(row, half * 64 + pc * 32 + ch * 16), v + 8 * ch);
+            for (int ch = 0; ch < 4; ++ch)
+                st_bf16x8u(sbase + OFF_WT + sw128_off(row, half * 64 + ch * 16), v + 8 * ch);
         }
         const uint32_t base = sbase + OFF_ST + half * 16384;
         if constexpr (kCh) {   // state operand S^T diag(e^{G_r}) (per key channel)
-            const float *eGr = sm.ch[c & 1].eGr + 64 * half;
+            const float *eGr = sm.ch[c % 3].eGr + 64 * half;
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) {
                 const float4 a = *reinterpret_cast<const float4 *>(eGr + 8 * ch);
@@ -735,22 +812,26 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         fence_proxy_async_smem();
         if (gtid == 0) tma_store_wait_read_all();   // the previous output staging is free again
         gsync();
-        if (gtid == 0) {
+        if (gw == 0) {
             tc_fence_after();
-            const uint64_t dst = sw128_desc(sbase + OFF_ST, 16, 1024), dwt = sw128_desc(sbase + OFF_WT, 16384, 1024);
+            if (elect_one()) {
+                const uint64_t dst = sw128_desc(sbase + OFF_ST, 16, 1024),
+                               dwt = sw128_desc(sbase + OFF_WT, 16384, 1024);
 #pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint32_t aoff = (s >> 2) * 16384 + (s & 3) * 32;
-                mma_bf16(tbase + TM_1A, desc_add(dst, aoff), desc_add(dwt, s * 2048), id_1a, s);
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t aoff = (s >> 2) * 16384 + (s & 3) * 32;
+                    mma_bf16(tbase + TM_1A, desc_add(dst, aoff), desc_add(dwt, s * 2048), id_1a, s);
+                }
+                mma_commit(bar_1);
             }
-            mma_commit(bar_1);
+            __syncwarp();
         }
     };
 
     // (e) E^T = U^T - (W S)^T and E^T diag(e^{G_end-G}); release W^T and U^T; issue E^T_s K
     // and E^T A^T.
     auto st_issue2 = [&](int c) {
-        const ChunkVec &cv = sm.v[c & 1];
+        const ChunkVec &cv = sm.v[c % 3];
         wait(bar_1, c & 1);
         tc_fence_after();
 #pragma unroll
@@ -775,56 +856,83 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         fence_proxy_async_smem();
         tc_fence_before();
         gsync();
-        if (gtid == 0) {
-            mbar_arrive(bar_freed);   // W^T read by the finished S^T W^T, U^T loaded by every thread
+        // warp 0 issues the product the state update waits for, warp 1 the output products, so
+        // neither issue sequence waits behind the other
+        if (gw == 0) {
             tc_fence_after();
-            const uint32_t qk = qk_of(c);
-            // scalar gate: (E^T diag(e^{G_end-G})) K; per-channel gate: E^T K_end (K_end over the
-            // E^T_s area, 64-row blocks)
-            const uint32_t a2 = sbase + (kCh ? OFF_ET : OFF_ETS);
-            const uint32_t b2 = kCh ? sbase + OFF_ETS : qk, lbo2 = kCh ? 8192 : 16384;
-            const uint64_t da2 = sw128_desc(a2, 16, 1024), db2 = sw128_desc(b2, lbo2, 1024);
+            if (elect_one()) {
+                mbar_arrive(bar_freed);   // W^T read by the finished S^T W^T, U^T loaded by every thread
+                // scalar gate: (E^T diag(e^{G_end-G})) K; per-channel gate: E^T K_end (K_end over the
+                // E^T_s area, 64-row blocks)
+                const uint32_t a2 = sbase + (kCh ? OFF_ET : OFF_ETS);
+                const uint32_t b2 = kCh ? ke_of(c) : qk_of(c), lbo2 = kCh ? 8192 : 16384;
+                const uint64_t da2 = sw128_desc(a2, 16, 1024), db2 = sw128_desc(b2, lbo2, 1024);
 #pragma unroll
-            for (int s = 0; s < 4; ++s) mma_bf16(tbase + TM_2, desc_add(da2, s * 32), desc_add(db2, s * 2048), id_2, s);
-            mma_commit(bar_2);   // the state update waits only for this one
-            if (write_out) {     // the output products: S^T Q^T and E^T A^T
-                const uint64_t dst = sw128_desc(sbase + OFF_ST, 16, 1024), dqq = sw128_desc(qk + 8192, 16, 1024);
-#pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
-                    mma_bf16(tbase + TM_1B, desc_add(dst, off), desc_add(dqq, off), id_qk, s);
-                }
-                const uint64_t det = sw128_desc(sbase + OFF_ET, 16, 1024), daq = sw128_desc(aqk_of(c), 16, 1024);
-#pragma unroll
-                for (int s = 0; s < 4; ++s) mma_bf16(tbase + TM_3, desc_add(det, s * 32), desc_add(daq, s * 32), id_qk, s);
+                for (int s = 0; s < 4; ++s)
+                    mma_bf16(tbase + TM_2, desc_add(da2, s * 32), desc_add(db2, s * 2048), id_2, s);
+                mma_commit(bar_2);
+                if (kCh) mma_commit(bar_m2k0 + 8 * (c & 1));   // the K_end buffer of chunk c is free
             }
-            mma_commit(bar_o);
+            __syncwarp();
+        } else if (gw == 1) {
+            tc_fence_after();
+            if (elect_one()) {
+                if (write_out) {     // the output products: S^T Q^T and E^T A^T
+                    const uint64_t dst = sw128_desc(sbase + OFF_ST, 16, 1024),
+                                   dqq = sw128_desc(qk_of(c) + 8192, 16, 1024);
+#pragma unroll
+                    for (int s = 0; s < 8; ++s) {
+                        const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
+                        mma_bf16(tbase + TM_1B, desc_add(dst, off), desc_add(dqq, off), id_qk, s);
+                    }
+                    const uint64_t det = sw128_desc(sbase + OFF_ET, 16, 1024), daq = sw128_desc(aqk_of(c), 16, 1024);
+#pragma unroll
+                    for (int s = 0; s < 4; ++s)
+                        mma_bf16(tbase + TM_3, desc_add(det, s * 32), desc_add(daq, s * 32), id_qk, s);
+                }
+                mma_commit(bar_o);
+            }
+            __syncwarp();
         }
     };
 
     // (f) S^T <- e^{G_end} S^T + (K_end^T E)^T; O^T = e^{G} (Q S)^T + (A E)^T -> TMA store;
     // retire chunk c and prefetch chunk c+2 into its stage.
     auto st_finish = [&](int c) {
-        const ChunkVec &cv = sm.v[c & 1];
+        const ChunkVec &cv = sm.v[c % 3];
+        if (warp == 0) {   // gate vectors of chunk c+2 into the buffer of chunk c-1 (retired)
+            gate_vec(c + 2);
+            __threadfence_block();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_done0 + 8 * (c & 1));
+        }
         wait(bar_2, c & 1);
         tc_fence_after();
         {
             const float gam = cv.eG[kC - 1];
-            const float *gch = sm.ch[c & 1].gam + 64 * half;
+            const float *gch = sm.ch[c % 3].gam + 64 * half;
+            // 32 columns per wait; 16 with the per-channel gate, whose decay vector needs the registers
+            constexpr int kW = kCh ? 16 : 32;
 #pragma unroll
-            for (int hh = 0; hh < 4; ++hh) {
-                uint32_t v[16];
-                tmem_ld16(tlane + TM_2 + 64 * half + 16 * hh, v);
+            for (int hh = 0; hh < 64 / kW; ++hh) {
+                uint32_t v[kW];
+                if constexpr (kW == 32) tmem_ld32(tlane + TM_2 + 64 * half + 32 * hh, v);
+                else tmem_ld16(tlane + TM_2 + 64 * half + 16 * hh, v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int kk = 0; kk < 16; ++kk) {
-                    const float gk = kCh ? gch[16 * hh + kk] : gam;
-                    s_reg[16 * hh + kk] = fmaf(gk, s_reg[16 * hh + kk], __uint_as_float(v[kk]));
+                for (int kk = 0; kk < kW; ++kk) {
+                    const float gk = kCh ? gch[kW * hh + kk] : gam;
+                    s_reg[kW * hh + kk] = fmaf(gk, s_reg[kW * hh + kk], __uint_as_float(v[kk]));
                 }
             }
         }
         wait(bar_o, c & 1);
         tc_fence_after();
+        // Q and K of chunk c have been read by the finished products: refill the stage with chunk c+2
+        if (warp == 0) {
+            if (c + 2 < nchunks && elect_one()) issue_loads(c + 2);
+            __syncwarp();
+        }
         if (write_out) {
             // Pair value channels (m, m^1) so each lane stores two channels as one bf16x2:
             // within each group of 16 tokens, even lanes keep tokens 0-7, odd lanes 8-15.
@@ -864,13 +972,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tma_store_4d(&tm_o, stg0 + 8192, 64, h, t0, b);
                 tma_store_commit();
             }
-            if (c + 2 < nchunks) issue_loads(c + 2);
-        }
-        if (warp == 0) {   // gate vectors of chunk c+2 into the buffer chunk c just released
-            gate_vec(c + 2);
-            __threadfence_block();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_done0 + 8 * (c & 1));
         }
     };
 
