@@ -105,7 +105,7 @@ size_t kla_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v, int c
     kla::ChunkArgs a{};
     a.B = B; a.T = T; a.H = H; a.d_k = d_k; a.d_v = d_v; a.chunk = chunk; a.dtype = dtype; a.gate = gate;
     if (kla::recurrent_preferred(a)) return 0;
-    return kla::chunk_tc_supports(a) ? kla::chunk_tc_workspace_bytes(B, T, H) : 0;
+    return kla::chunk_tc_supports(a) ? kla::chunk_tc_workspace_bytes(B, T, H, gate) : 0;
 }
 
 }  // extern "C"
@@ -179,9 +179,9 @@ kla_status chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
 kla_status kla::chunk_fwd_nosplit(const void *q, const void *k, const void *v, const float *alpha, const float *eta,
                                   float eps, const float *S0, void *o, float *S_T, int B, int T, int H, int d_k,
                                   int d_v, int chunk, kla_dtype dtype, kla_gate gate, kla_beta_mode beta_mode,
-                                  float q_scale, void *stream) {
+                                  float q_scale, void *workspace, size_t workspace_bytes, void *stream) {
     return chunk_fwd_impl(q, k, v, alpha, eta, eps, S0, o, S_T, B, T, H, d_k, d_v, chunk, dtype, gate, beta_mode,
-                          q_scale, nullptr, 0, stream, 1);
+                          q_scale, workspace, workspace_bytes, stream, 1);
 }
 
 extern "C" {

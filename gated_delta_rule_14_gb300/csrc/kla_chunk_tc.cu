@@ -151,6 +151,7 @@ struct TcParams {
     unsigned *err;
     int beta_raw;  // 1: beta = eta
     float q_scale; // o = S^T (q_scale q)
+    const unsigned *rescue;   // per-channel gate: [B*H] marks of chains rerun exactly (skipped here), or NULL
 };
 
 __device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x << 16); }
@@ -177,6 +178,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                 const TcParams p) {
+    // a chain marked for the exact rerun is skipped entirely (its S0 stays as it is)
+    if (p.rescue && p.rescue[blockIdx.x / p.seg_count] != 0u) return;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base, derived from the shared array itself so that every access below
     // stays a shared-memory access (no generic addressing)
@@ -371,9 +374,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // per-channel: products of the gates over each half of the chunk; `ex` is the product over
         // the sub-ranges between this thread's and the reference token (before it in half 1, after
         // it in half 0), `tot` over the whole half
-        float ex[kCh ? 8 : 1], tot[kCh ? 8 : 1];
+        float ex[kCh ? 8 : 1];
         if constexpr (kCh) {
             bool low = false;
+            float tot[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 float l = 1.f;
@@ -395,7 +399,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (csb == 0) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) (cth ? chv.F : chv.eGr)[8 * ccg + j] = tot[j];   // e^{G_end-G_r} | e^{G_r}
-                if (low) atomicOr(p.err, kErrGateRange);
+                if (low) atomicOr(p.err, kErrGateRange);   // no flag array: the range error is reported
             }
         }
         wait(bar_full0 + 8 * (c & 1), (c >> 1) & 1);
@@ -444,7 +448,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int j = 0; j < 8; ++j) Fv[j] = chv.F[8 * ccg + j];
             if (cth == 0 && csb == 0) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) chv.gam[8 * ccg + j] = tot[j] * Fv[j];   // e^{G_end}
+                for (int j = 0; j < 8; ++j) chv.gam[8 * ccg + j] = chv.eGr[8 * ccg + j] * Fv[j];   // e^{G_end}
             }
             // K_end of this chunk goes to buffer c & 1: E^T K_end of chunk c-2 must have read it
             if (c >= 2) wait(bar_m2k0 + 8 * (c & 1), ((c - 2) >> 1) & 1);
@@ -1012,6 +1016,26 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
 }
 
+// Per-channel gate: marks the (sequence, head) chains with a chunk whose gates, for some key
+// channel, multiply to less than e^-78 over tokens 0-31 or 32-63 of the chunk (a margin inside
+// the e^-80 limit of the factorised in-chunk products, with the same per-token clamp and tokens
+// past the end counted as 1). One CTA of 128 threads (one per key channel) per (chunk, head,
+// sequence); coalesced reads of 128 consecutive gates per token.
+__global__ void __launch_bounds__(kD) gate_range_kernel(const float *alpha, int T, int H, unsigned *marks) {
+    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z, k = threadIdx.x;
+    const float kLow = 1.3e-34f;   // ~ e^-78
+    bool low = false;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        float prod = 1.f;
+        const int t0 = c * kC + 32 * half, t1 = min(T, t0 + 32);
+        for (int t = t0; t < t1; ++t)
+            prod *= fmaxf(alpha[((static_cast<size_t>(b) * T + t) * H + h) * kD + k], 1.8e-35f);
+        low |= prod < kLow;
+    }
+    if (__syncthreads_or(low) && k == 0) marks[static_cast<size_t>(b) * H + h] = 1u;
+}
+
 // ---------------------------------------------------------------------------- host side
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
@@ -1098,12 +1122,27 @@ SegPlan make_plan(int B, int T, int H) {
     return {(nchunks + L - 1) / L, L * kC};
 }
 
-}  // namespace
-
-size_t chunk_tc_workspace_bytes(int B, int T, int H) {
+// Segment states (Z, M and the start states, each [chains][nseg][d][d] fp32) when the sequence is
+// split; then, with the per-channel gate, one flag per chain (256-byte aligned).
+size_t seg_workspace_bytes(int B, int T, int H) {
     const SegPlan pl = make_plan(B, T, H);
     if (pl.nseg <= 1) return 0;
-    return 3ull * B * H * pl.nseg * kD * kD * sizeof(float);   // Z, M and the start states
+    return 3ull * B * H * pl.nseg * kD * kD * sizeof(float);
+}
+size_t rescue_flag_bytes(int B, int H) { return (static_cast<size_t>(B) * H * sizeof(unsigned) + 255) & ~size_t(255); }
+
+// Per-channel gate: rerun, on the exact fp32 recurrence, the chains gate_range_kernel marked (the
+// tensor-core kernel skipped them); every other CTA of the launch returns at once.
+cudaError_t launch_rescue(const ChunkArgs &a, const unsigned *flags) {
+    ChunkArgs r = a;
+    r.only = flags;
+    return launch_recurrent(r);
+}
+
+}  // namespace
+
+size_t chunk_tc_workspace_bytes(int B, int T, int H, kla_gate gate) {
+    return seg_workspace_bytes(B, T, H) + (gate == KLA_GATE_CHANNEL ? rescue_flag_bytes(B, H) : 0);
 }
 
 bool chunk_tc_supports(const ChunkArgs &a) {
@@ -1121,15 +1160,28 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a) {
     if (e != cudaSuccess) return e;
     const int chains = a.B * a.H;
     const SegPlan pl = a.no_segments ? SegPlan{1, ((a.T + kC - 1) / kC) * kC} : make_plan(a.B, a.T, a.H);
+    const size_t seg_bytes = pl.nseg <= 1 ? 0 : seg_workspace_bytes(a.B, a.T, a.H);
+    // Per-channel gate with a workspace: chains whose gates leave the range of the factorised
+    // products are marked first (marks after the segment states), skipped by the tensor-core
+    // launches and rerun exactly after them. Without a workspace they are only reported.
+    unsigned *flags = nullptr;
+    if (a.gate == KLA_GATE_CHANNEL && a.workspace && a.workspace_bytes >= seg_bytes + rescue_flag_bytes(a.B, a.H)) {
+        flags = reinterpret_cast<unsigned *>(static_cast<char *>(a.workspace) + seg_bytes);
+        if ((e = cudaMemsetAsync(flags, 0, static_cast<size_t>(chains) * sizeof(unsigned), a.stream)) != cudaSuccess)
+            return e;
+        gate_range_kernel<<<dim3((a.T + kC - 1) / kC, a.H, a.B), kD, 0, a.stream>>>(a.alpha, a.T, a.H, flags);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     TcParams p{a.alpha, a.eta, a.eps, a.S0, a.S_T, a.B, a.T, a.H, pl.seg_len, 0, 1, pl.nseg,
-               kS0Chain, kSTLast, 0, 0, a.err, a.beta_raw, a.q_scale};
+               kS0Chain, kSTLast, 0, 0, a.err, a.beta_raw, a.q_scale, flags};
     if (pl.nseg <= 1) {
         kern<<<chains, kThreads, SMEM_BYTES, a.stream>>>(mq, mk, mv, mo, p);
-        return cudaGetLastError();
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        return flags ? launch_rescue(a, flags) : cudaSuccess;
     }
     // Sequence-parallel scan over segments (workspace: Z | M | start states, each
     // [chains][nseg][d][d] fp32).
-    if (!a.workspace || a.workspace_bytes < chunk_tc_workspace_bytes(a.B, a.T, a.H)) return cudaErrorInvalidValue;
+    if (!a.workspace || a.workspace_bytes < seg_bytes) return cudaErrorInvalidValue;
     const size_t part = static_cast<size_t>(chains) * pl.nseg * kD * kD;
     float *Z = static_cast<float *>(a.workspace), *M = Z + part, *Sst = M + part;
     // pass 1a: segments 0..n-2 from the true start (segment 0) or zero; segment 0 writes its outputs
@@ -1191,7 +1243,8 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a) {
     p3.S0 = Sst;
     p3.s0_mode = kS0Segment;
     kern<<<chains * p3.seg_count, kThreads, SMEM_BYTES, a.stream>>>(mq, mk, mv, mo, p3);
-    return cudaGetLastError();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return flags ? launch_rescue(a, flags) : cudaSuccess;
 }
 
 }  // namespace kla

@@ -11,6 +11,8 @@
 // nothing runs beside it but the remaining copies, and its prefill plus its download are the
 // call's tail, so it takes the segments when they shorten it, with the fixed scratch array of
 // kla_chunk_fwd_noalloc (the last parts of consecutive calls are ordered on it by an event).
+// With the per-channel gate, the other parts' rerun marks live in the array's last MiB, one
+// slot per compute stream.
 //
 // Streams and events are created once per device on the first call and kept for the life of
 // the process. Calls are ordered after earlier work on the caller's stream and the caller's
@@ -33,6 +35,11 @@ constexpr int kMaxDevices = 64;
 constexpr int kComputeStreams = 8;
 constexpr int kCopyStreams = 2;    // per direction: parts alternate between them
 constexpr int kMaxParts = 64;
+// The last MiB of the fixed scratch array holds, per compute stream, the flags with which the
+// per-channel-gate prefill of a part marks chains for its exact rerun (parts sharing a slot
+// share a stream, so they run one after the other); the last part's segments use the rest.
+constexpr size_t kFlagTail = size_t(1) << 20;
+constexpr size_t kFlagSlot = kFlagTail / kComputeStreams;
 
 struct HostPipe {
     bool ready = false;
@@ -106,6 +113,8 @@ extern "C" kla_status kla_chunk_fwd_host(const void *q_h, const void *k_h, const
              cudaStreamWaitEvent(P.d2h[c], P.start, 0) == cudaSuccess;
     for (int c = 0; ok && c < kComputeStreams; ++c) ok = cudaStreamWaitEvent(P.comp[c], P.start, 0) == cudaSuccess;
     kla_status st = KLA_OK;
+    void *scratch = nullptr;   // device address of the fixed scratch array
+    if (ok && kla::noalloc_scratch(&scratch) != cudaSuccess) ok = false;
     for (int i = 0; ok && i < parts; ++i) {
         const int b0 = i * bp, nb = std::min(bp, B - b0);
         if (nb <= 0) break;
@@ -129,21 +138,24 @@ extern "C" kla_status kla_chunk_fwd_host(const void *q_h, const void *k_h, const
         const float *s0p = S0_d ? reinterpret_cast<const float *>(at(S0_d, b0 * s_b)) : nullptr;
         float *stp = S_T_d ? reinterpret_cast<float *>(atw(S_T_d, b0 * s_b)) : nullptr;
         const size_t need = b0 + nb >= B ? kla_chunk_fwd_workspace_size(nb, T, H, d_k, d_v, chunk, dtype, gate) : 0;
-        if (need > 0 && need <= static_cast<size_t>(KLA_NOALLOC_SCRATCH_BYTES)) {   // the last part, segmented
-            void *scratch = nullptr;
-            if (kla::noalloc_scratch(&scratch) != cudaSuccess || cudaStreamWaitEvent(comp, P.scratch_free, 0) != cudaSuccess) {
+        const size_t seg_room = static_cast<size_t>(KLA_NOALLOC_SCRATCH_BYTES) - kFlagTail;
+        if (need > 0 && need <= seg_room) {   // the last part, segmented or with the per-channel flags
+            if (cudaStreamWaitEvent(comp, P.scratch_free, 0) != cudaSuccess) {
                 st = KLA_ERR_CUDA;
                 break;
             }
             st = kla_chunk_fwd_ex(qp, kp, vp, ap, ep, eps, s0p, atw(o_d, b0 * v_b), stp, nb, T, H, d_k, d_v, chunk, dtype,
-                                  gate, beta_mode, q_scale, scratch, KLA_NOALLOC_SCRATCH_BYTES, comp);
+                                  gate, beta_mode, q_scale, scratch, seg_room, comp);
             // recorded even when the prefill failed part-way: kernels it did enqueue may still use
             // the array, and the next user of the array must wait for them
             ok = cudaEventRecord(P.scratch_free, comp) == cudaSuccess;
             if (st != KLA_OK || !ok) break;
         } else {
+            void *slot = gate == KLA_GATE_CHANNEL
+                             ? static_cast<char *>(scratch) + seg_room + (i % kComputeStreams) * kFlagSlot
+                             : nullptr;
             st = kla::chunk_fwd_nosplit(qp, kp, vp, ap, ep, eps, s0p, atw(o_d, b0 * v_b), stp, nb, T, H, d_k, d_v, chunk,
-                                        dtype, gate, beta_mode, q_scale, comp);
+                                        dtype, gate, beta_mode, q_scale, slot, slot ? kFlagSlot : 0, comp);
             if (st != KLA_OK) break;
         }
         ok = cudaEventRecord(P.out_ready[i], comp) == cudaSuccess &&

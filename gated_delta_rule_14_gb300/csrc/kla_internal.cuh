@@ -33,6 +33,7 @@ struct ChunkArgs {
     int beta_raw;          // 1: beta = eta (KLA_BETA_RAW)
     float q_scale;         // o = S^T (q_scale q)
     int no_segments;       // 1: never split long sequences into parallel segments
+    const unsigned *only;  // recurrent path: when set, only chains (b, h) with only[b * H + h] != 0 run
 };
 
 struct DecodeArgs {
@@ -67,12 +68,14 @@ struct BwdArgs {
     cudaStream_t stream;
 };
 
-// kla_chunk_fwd_ex without the sequence-parallel segments (no workspace): for callers that run
-// several prefills side by side, where splitting each one would only add work.
+// kla_chunk_fwd_ex without the sequence-parallel segments: for callers that run several
+// prefills side by side, where splitting each one would only add work. The workspace is optional
+// (NULL, 0): with the per-channel gate and at least 4 * B * H bytes, chains outside the range of
+// the factorised in-chunk products are rerun exactly, otherwise they are only reported.
 kla_status chunk_fwd_nosplit(const void *q, const void *k, const void *v, const float *alpha, const float *eta,
                              float eps, const float *S0, void *o, float *S_T, int B, int T, int H, int d_k, int d_v,
                              int chunk, kla_dtype dtype, kla_gate gate, kla_beta_mode beta_mode, float q_scale,
-                             void *stream);
+                             void *workspace, size_t workspace_bytes, void *stream);
 
 // Every argument check of kla_chunk_fwd_ex except the workspace's (its errors, in its order).
 kla_status check_chunk_fwd(const void *q, const void *k, const void *v, const float *alpha, const float *eta,
@@ -83,9 +86,10 @@ kla_status check_chunk_fwd(const void *q, const void *k, const void *v, const fl
 // tcgen05 tensor-core chunk path: bf16, d_k = d_v = 128, chunk = 64.
 bool chunk_tc_supports(const ChunkArgs &a);
 cudaError_t launch_chunk_tc(const ChunkArgs &a);
-// Device scratch the tensor-core path needs for these sizes (non-zero when it splits long
-// sequences into segments that run in parallel).
-size_t chunk_tc_workspace_bytes(int B, int T, int H);
+// Device scratch the tensor-core path needs for these sizes: the segments' states when it splits
+// long sequences into segments that run in parallel, and with the per-channel gate one flag per
+// (sequence, head) chain whose gates leave the range of the factorised in-chunk products.
+size_t chunk_tc_workspace_bytes(int B, int T, int H, kla_gate gate);
 // Start states of the segments of every chain: S_start[s+1] = M_s S_start[s] + Z_s.
 cudaError_t launch_seg_combine(const float *Z, const float *M, float *Sst, int chains, int nseg,
                                cudaStream_t stream);

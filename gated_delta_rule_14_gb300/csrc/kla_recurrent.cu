@@ -32,6 +32,7 @@ struct RecParams {
     int B, T, H, DK, DV;
     int beta_raw;
     float q_scale;
+    const unsigned *only;   // when set, chains with only[b * H + h] == 0 return at once
 };
 
 // Lane layout. A warp owns CGW float4 column groups (CGW * 4 value columns) over ALL d_k rows,
@@ -110,6 +111,7 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecParams p) 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cg = lane % CGW, rg = lane / CGW;
     const int h = blockIdx.y, b = blockIdx.z;
+    if (p.only && p.only[static_cast<size_t>(b) * p.H + h] == 0) return;
     const int vt0 = blockIdx.x * BV;              // first column of the CTA's tile
     const int ucol = warp * CGW + cg;             // this lane's 16-byte unit within a tile row
     const size_t bh = static_cast<size_t>(b) * p.H + h;
@@ -296,7 +298,7 @@ template <typename TIn, bool kChannel>
 cudaError_t launch_t(const ChunkArgs &a) {
     const int BV = std::min(a.d_v, 32);   // d_v is 16, 32, 64 or 128
     RecParams p{a.q, a.k, a.v, a.alpha, a.eta, a.eps, a.S0, a.o, a.S_T, a.B, a.T, a.H, a.d_k, a.d_v, a.beta_raw,
-                  a.q_scale};
+                  a.q_scale, a.only};
     dim3 grid(a.d_v / BV, a.H, a.B);
     return BV == 32 ? launch_rows<TIn, kChannel, 2>(a, p, grid) : launch_rows<TIn, kChannel, 1>(a, p, grid);
 }

@@ -97,14 +97,17 @@ typedef enum kla_beta_mode {
  *            chunk is masked.
  *   chunk    tokens per chunk
  *   workspace, workspace_bytes: device scratch of at least
- *            kla_chunk_fwd_workspace_size(...) bytes (may be NULL when that size is 0)
+ *            kla_chunk_fwd_workspace_size(...) bytes (may be NULL when that size is 0); its
+ *            contents need no initialisation and are unspecified after the call
  *
  * Per-key-channel gates on the tensor-core path: the in-chunk products are factorised
  * around the 32nd token of each chunk, which is exact as long as, for every key channel, the
  * product of the gates over tokens 0-31 and over tokens 32-63 of a chunk each stays above
- * e^-80 (the gates averaged over 32 tokens above about 0.082). A chunk outside that range
- * raises a device flag that kla_device_status() reports as KLA_ERR_INVALID_ARG (its results
- * are then not valid); chunk = 16 or 32 runs the fp32 path, which has no such limit.
+ * e^-80 (the gates averaged over 32 tokens above about 0.082). The call first marks, in the
+ * workspace, every (sequence, head) chain with a chunk near or outside that range (one pass over
+ * alpha); the tensor-core kernel skips the marked chains and the same call reruns them on the
+ * fp32 token-by-token path, so every alpha in (0, 1] gives valid results and KLA_OK. The marks
+ * cost 4 bytes per chain of workspace. chunk = 16 or 32 runs the fp32 path throughout.
  *
  * Calls of 1 to 16 tokens (multi-token decode, speculative verification) ignore `chunk`: bf16
  * with a scalar gate and d_k = d_v = 128 runs the call's tokens as one chunk on warp-level
@@ -135,8 +138,10 @@ kla_status kla_chunk_fwd_ex(const void *q, const void *k, const void *v,
                             kla_dtype dtype, kla_gate gate, kla_beta_mode beta_mode, float q_scale,
                             void *workspace, size_t workspace_bytes, void *stream);
 
-/* Bytes of device scratch kla_chunk_fwd / kla_chunk_fwd_ex need for these sizes (0 if none);
- * the step-size mode and the query scale do not change it. */
+/* Bytes of device scratch kla_chunk_fwd / kla_chunk_fwd_ex need for these sizes (0 if none):
+ * the segments' states when a long sequence with few (sequence, head) chains is split into
+ * segments, and with the per-channel gate on the tensor-core path the chains' rerun marks (4
+ * bytes per chain). The step-size mode and the query scale do not change it. */
 size_t kla_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v, int chunk,
                                     kla_dtype dtype, kla_gate gate);
 
@@ -145,10 +150,11 @@ size_t kla_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v, int c
  * (for example a runtime whose memory manager owns all device memory, or code that must not
  * allocate while work is in flight on its stream). The pages have no counterpart: it is a
  * deployment variant of kla_chunk_fwd with the same arguments, results and errors, minus the
- * workspace. The scratch that kla_chunk_fwd would take from the caller (non-zero only when a
- * long sequence with few (sequence, head) chains is split into segments) comes instead from a
- * fixed array of KLA_NOALLOC_SCRATCH_BYTES inside the library's device image; every GPU that
- * loads the library holds that array until the process exits.
+ * workspace. The scratch that kla_chunk_fwd would take from the caller (the segments' states
+ * when a long sequence with few (sequence, head) chains is split into segments, and the rerun
+ * marks of the per-channel gate) comes instead from a fixed array of KLA_NOALLOC_SCRATCH_BYTES
+ * inside the library's device image; every GPU that loads the library holds that array until
+ * the process exits.
  *  - The arguments are checked first, exactly as kla_chunk_fwd checks them (same errors); a
  *    valid call whose scratch (kla_chunk_fwd_workspace_size) exceeds KLA_NOALLOC_SCRATCH_BYTES
  *    is then rejected with KLA_ERR_UNSUPPORTED, before anything is launched.
@@ -182,9 +188,12 @@ kla_status kla_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
  *   parts         1 .. min(B, 64)
  * Parts run whole sequences, except the last part when the sequence-parallel segments of
  * kla_chunk_fwd shorten it (long sequences, few chains per part): it then takes its scratch
- * from the fixed array of kla_chunk_fwd_noalloc (no allocation). The last parts of host calls
- * are ordered on that array by an event of the library's; a kla_chunk_fwd_noalloc call whose
- * kernels may run at the same time as a host call must be ordered against it by the caller. The call is
+ * from the fixed array of kla_chunk_fwd_noalloc (no allocation). With the per-channel gate,
+ * every part's rerun marks (see kla_chunk_fwd) live in that array too: up to 32768 chains per
+ * part; a part with more chains reports out-of-range gates through kla_device_status instead of
+ * rerunning them. The last parts of host calls are ordered on that array by an event of the
+ * library's; a kla_chunk_fwd_noalloc call whose kernels may run at the same time as a host call
+ * must be ordered against it by the caller. The call is
  * asynchronous and ordered on `stream`: it starts after earlier work on `stream`, and work
  * enqueued on `stream` afterwards starts after its last copy. The library keeps two copy
  * streams, eight compute streams and a few events per device for the life of the process;

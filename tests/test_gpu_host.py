@@ -89,3 +89,25 @@ def test_host_prefill_segments_the_last_part():
         o_g = np.stack([o.float().numpy()[b, :, h] for b, h in chains])
         s_g = np.stack([st.numpy()[b, h] for b, h in chains])
         assert oracle.rel_l2(o_g, o_ref) <= 1e-2 and oracle.rel_l2(s_g, s_ref) <= 1e-2
+
+
+@pytest.mark.parametrize("parts", [1, 3])
+def test_host_prefill_reruns_out_of_range_channel_gates(parts):
+    """Per-channel gates outside the factorised range in a part other than the last and in the
+    last part: both are rerun exactly inside the host call, as kla_chunk_fwd does."""
+    import gated_delta_rule_14_gb300 as kla
+    inp = synth.make_prefill("kda8k", seed=40 + parts, B=3, T=130, H=2)
+    inp.alpha[0, 10:45, 1, 7] = 1e-3     # part 0 (of 3)
+    inp.alpha[2, 64:100, 0, 90] = 1e-3   # the last part
+    args = [inp.q, inp.k, inp.v, inp.alpha, inp.eta]
+    o_d, s_d = kla.chunk_fwd(*(to_dev(x) for x in args), inp.wl.eps, None, chunk=inp.wl.chunk)
+    o_h, s_h = kla.chunk_fwd_host(*(host(x) for x in args), inp.wl.eps, None, chunk=inp.wl.chunk, parts=parts,
+                                  device=DEV)
+    torch.cuda.synchronize(DEV)
+    kla.device_status(DEV)   # raises if anything was only reported
+    assert torch.equal(o_h, o_d.cpu()) and torch.equal(s_h, s_d.cpu())
+    o_ref, s_ref = oracle_chains(inp)
+    chains = [(b, h) for b in range(inp.wl.B) for h in range(inp.wl.H)]
+    o_g = np.stack([o_h.float().numpy()[b, :, h] for b, h in chains])
+    s_g = np.stack([s_h.numpy()[b, h] for b, h in chains])
+    assert oracle.rel_l2(o_g, o_ref) <= 1e-2 and oracle.rel_l2(s_g, s_ref) <= 1e-2

@@ -144,22 +144,61 @@ def test_zero_keys_eps_zero_unit_gates(gate):
     check(inp, o, S)
 
 
-def test_channel_gate_out_of_range_is_reported():
-    """Per-channel gates whose product over half a chunk falls below e^-80 are outside the exact
-    range of the tensor-core path: the call reports it through kla_device_status."""
-    import gated_delta_rule_14_gb300 as kla
-    inp = synth.make_prefill("kda8k", seed=3, B=1, T=64, H=1)
-    inp.alpha[0, :32, 0, 5] = 1e-3       # 32 tokens at 1e-3: product 1e-96
-    with pytest.raises(kla.KlaError) as ei:
-        run_prefill(inp)
-    assert ei.value.status == 1
-    # the same gates run exactly on the fp32 path (chunk 32)
-    o, S = run_prefill(inp, chunk=32)
+def _starve(alpha, b, h, t0, n, ch, value=1e-3):
+    """Per-channel gates of `value` for n tokens from t0 in key channel ch of chain (b, h): their
+    product over half a chunk falls far below e^-80."""
+    alpha[b, t0:t0 + n, h, ch] = value
+
+
+def test_channel_gate_out_of_range_is_rerun_exactly():
+    """Per-channel gates whose product over half a chunk falls below e^-80 leave the range of the
+    tensor-core path's factorised products: the call marks those chains and reruns them on the
+    fp32 token-by-token path in the same call, so the results are valid and no error is
+    reported. The rerun chains' final states match the oracle to the fp32 bar, which the
+    tensor-core path (bf16 operands) would not meet."""
+    inp = synth.make_prefill("kda8k", seed=3, B=2, T=150, H=2, s0_sigma=0.05)
+    _starve(inp.alpha, 0, 1, 0, 32, 5)               # first half of chunk 0
+    _starve(inp.alpha, 1, 0, 70, 40, 100, 1e-30)     # across the halves of chunk 1, down to 1e-30
+    o, S = run_prefill(inp)                          # device_status raises on any reported error
     check(inp, o, S)
-    # and the device flag was cleared by the first status read
-    inp2 = synth.make_prefill("kda8k", seed=4, B=1, T=64, H=1)
-    o, S = run_prefill(inp2)
-    check(inp2, o, S)
+    o_ref, s_ref = oracle_chains(inp, [(0, 1), (1, 0)])
+    o_g, s_g = gather_chains(o, S, [(0, 1), (1, 0)])
+    assert oracle.rel_l2(s_g, s_ref) <= 1e-5, "marked chains were not rerun on the fp32 path"
+    # the same gates on the fp32 path throughout (chunk 32)
+    o32, S32 = run_prefill(inp, chunk=32)
+    check(inp, o32, S32)
+    # unmarked chains keep the tensor-core results: a call without the starved chains agrees
+    clean = synth.make_prefill("kda8k", seed=3, B=2, T=150, H=2, s0_sigma=0.05)
+    o_c, S_c = run_prefill(clean)
+    for b, h in [(0, 0), (1, 1)]:
+        assert np.array_equal(o[b, :, h], o_c[b, :, h]) and np.array_equal(S[b, h], S_c[b, h])
+
+
+def test_channel_gate_out_of_range_in_place_state():
+    """S_T = S0 (in-place continuation) with a marked chain: the tensor-core kernel must leave that
+    chain's state alone, because its exact rerun starts from S0."""
+    import gated_delta_rule_14_gb300 as kla
+    inp = synth.make_prefill("kda8k", seed=8, B=1, T=200, H=2, s0_sigma=0.05)
+    _starve(inp.alpha, 0, 0, 100, 30, 17)
+    S = to_dev(inp.S0).clone()
+    o, S_out = kla.chunk_fwd(to_dev(inp.q), to_dev(inp.k), to_dev(inp.v), to_dev(inp.alpha), to_dev(inp.eta),
+                             inp.wl.eps, S, S_T=S)
+    kla.device_status(DEV)
+    assert S_out.data_ptr() == S.data_ptr()
+    check(inp, o.float().cpu().numpy().astype(np.float64), S.cpu().numpy().astype(np.float64))
+
+
+def test_channel_gate_out_of_range_with_segments():
+    """A long per-channel sequence split into segments (value runs, transitions, reruns), with
+    starved gates in a middle segment and in the last one."""
+    import gated_delta_rule_14_gb300 as kla
+    T = 64 * 100 + 5
+    inp = synth.make_prefill("kda8k", seed=21, B=1, T=T, H=1, s0_sigma=0.05)
+    assert kla.workspace_size(1, T, 1, 128, 128, 64, per_channel_gate=True) > 4
+    _starve(inp.alpha, 0, 0, 64 * 40 + 2, 33, 64)
+    _starve(inp.alpha, 0, 0, T - 50, 40, 3)
+    o, S = run_prefill(inp)
+    check(inp, o, S)
 
 
 @pytest.mark.parametrize("gate,T,H,s0", [("scalar", 64 * 200 + 17, 2, 0.05), ("scalar", 64 * 40, 1, 0.0),

@@ -67,10 +67,15 @@ def _call_reference_entry(inp, S0):
     ("long131k", dict(B=1, T=64 * 200 + 17, H=2, s0_sigma=0.05)),   # split into segments: uses the scratch
     ("kda8k", dict(B=1, T=64 * 120, H=1)),                          # per-channel gate, segments
     ("gdn4k", dict(B=2, T=300, H=3)),                                # no segments: no scratch
+    ("kda8k", dict(B=2, T=200, H=2, starve=True)),                   # per-channel rerun marks in the scratch
 ])
 def test_matches_kla_chunk_fwd_bit_for_bit(name, over):
     import gated_delta_rule_14_gb300 as kla
+    over = dict(over)
+    starve = over.pop("starve", False)
     inp = synth.make_prefill(name, seed=11, **over)
+    if starve:   # gates out of the tensor-core path's range in one chain: it is rerun exactly
+        inp.alpha[1, 70:110, 0, 9] = 1e-3
     wl = inp.wl
     need = kla.workspace_size(wl.B, wl.T, wl.H, wl.d_k, wl.d_v, wl.chunk, per_channel_gate=(wl.gate == "channel"))
     assert need <= SCRATCH_BYTES
