@@ -62,10 +62,10 @@ DECODE_BYTES_PER_HEAD_STEP = 8 * 128 * 128 + 4 * 2 * 128 + 8
 # reports null.
 TC_SOURCES = ("gated_delta_rule_14_gb300/csrc/kla_chunk_tc.cu", "gated_delta_rule_14_gb300/csrc/sm103_ptx.cuh",
               "gated_delta_rule_14_gb300/csrc/kla_internal.cuh")
-TC_TRAFFIC_GDN4K = {"b5dcb6b7ca595b8d": 521.226496e6}
+TC_TRAFFIC_GDN4K = {"e9fa9b8b231d85d0": 520.831488e6}
 # sm__pipe_tensor_cycles_active (fraction of elapsed cycles) of the same kernel and capture:
 # the algorithmic TFLOP/s divided by it is the rate of the MMA phases themselves.
-TC_PIPE_ACTIVE_GDN4K = {"b5dcb6b7ca595b8d": 0.14990}
+TC_PIPE_ACTIVE_GDN4K = {"e9fa9b8b231d85d0": 0.13132}
 
 
 def tc_fingerprint() -> str:
@@ -490,6 +490,8 @@ def main():
     ap.add_argument("--bwd-only", action="store_true",
                     help="time only the backward pass of gdn4k (a small case for profiling with --bwd-batch)")
     ap.add_argument("--bwd-batch", type=int, default=8)
+    ap.add_argument("--prefill-only", choices=["gdn4k", "kda8k", "long131k"], default=None,
+                    help="time only the prefill of this workload (a command for profiling one kernel)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -517,6 +519,14 @@ def main():
         # of its inputs in L2 and without the flush's dirty lines left to write back
         flush_buf.zero_()
         torch.sum(flush_rd, dim=0, out=flush_sink)
+
+    if args.prefill_only:
+        r = bench_prefill(args.prefill_only, args.steps, args.warmup, seed=rank, dev=dev, flush=flush, stream=stream,
+                          pk=pk)
+        if rank == 0:
+            print(json.dumps({"prefill": args.prefill_only, "ms_per_step": r["ms"],
+                              "roofline": roofline(r["alg_bytes"], r["ms"], pk)}), flush=True)
+        return
 
     if args.bwd_only:
         r = bench_bwd("gdn4k", args.steps, seed=rank, dev=dev, flush=flush, stream=stream, pk=pk, B=args.bwd_batch)
