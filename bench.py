@@ -318,13 +318,17 @@ def bench_decode_graph(steps_tok, seed, dev, pk, replays=3):
             "note": "one CUDA graph of all steps; effective GB/s above the HBM peak means L2 hits"}
 
 
-def bench_verify(ntok, calls, seed, dev, flush, stream, pk):
+def bench_verify(ntok, calls, seed, dev, flush, stream, pk, channel=False):
     """Multi-token decode (speculative verification): every call advances the decode batch's
-    states in place by `ntok` tokens; L2 flushed before every call."""
+    states in place by `ntok` tokens; L2 flushed before every call. channel=True: the same batch
+    (64 sequences x 16 heads) with the per-key-channel gates of the kda8k workload."""
     import torch
 
     import gated_delta_rule_14_gb300 as kla
-    inp, d = prefill_inputs("decode", seed, dev, T=ntok, chunk=64, s0_sigma=0.02)
+    if channel:
+        inp, d = prefill_inputs("kda8k", seed, dev, B=64, T=ntok, H=16, s0_sigma=0.02)
+    else:
+        inp, d = prefill_inputs("decode", seed, dev, T=ntok, chunk=64, s0_sigma=0.02)
     wl = inp.wl
     S = to_dev(inp.S0, dev)
     o = torch.empty((wl.B, wl.T, wl.H, wl.d_v), dtype=torch.bfloat16, device=dev)
@@ -335,9 +339,14 @@ def bench_verify(ntok, calls, seed, dev, flush, stream, pk):
     ms = statistics.fmean(time_steps(step, calls, 3, flush, stream))
     kla.device_status(dev)
     heads = wl.B * wl.H
-    alg_bytes = heads * (8 * wl.d_k * wl.d_v + ntok * (PREFILL_BYTES_PER_TOKEN_HEAD))
-    kernel = ("chunk form (tokens_tc_kernel: one CTA per head, warp-level tensor cores)" if ntok >= 5 else
-              "token loop (tokens_pipe_kernel: 128 x 32 state tiles in registers)")
+    per = PREFILL_BYTES_PER_TOKEN_HEAD_KDA if channel else PREFILL_BYTES_PER_TOKEN_HEAD
+    alg_bytes = heads * (8 * wl.d_k * wl.d_v + ntok * per)
+    if ntok < 5:
+        kernel = "token loop (tokens_pipe_kernel: 128 x 32 state tiles in registers)"
+    elif channel:
+        kernel = "chunk form, per-channel gate (tokens_ch_kernel: one CTA per head, exact in-call products)"
+    else:
+        kernel = "chunk form (tokens_tc_kernel: one CTA per head, warp-level tensor cores)"
     return {"value": wl.B * ntok / (ms * 1e-3), "unit": "tokens/s", "ms_per_call": ms, "calls": calls,
             "tokens_per_call": ntok, "batch": wl.B, "kernel": kernel, "roofline": roofline(alg_bytes, ms, pk),
             "l2": "flushed before every call (256 MiB write, then 256 MiB read)"}
@@ -593,6 +602,11 @@ def main():
                                                    stream=stream, pk=pk)
             clocks.mark(t0, time.time())
             launches += args.verify_calls
+        t0 = time.time()
+        extras["verify16_kda"] = bench_verify(16, args.verify_calls, seed=rank, dev=dev, flush=flush, stream=stream,
+                                              pk=pk, channel=True)
+        clocks.mark(t0, time.time())
+        launches += args.verify_calls
         if not args.no_bwd:
             t0 = time.time()
             extras["bwd_gdn4k"] = bench_bwd("gdn4k", 3, seed=rank, dev=dev, flush=flush, stream=stream, pk=pk)

@@ -1058,7 +1058,7 @@ bool tokens_pipe_supports(const ChunkArgs &a) {
 cudaError_t launch_tokens_pipe(const ChunkArgs &a) {
     const bool ch = a.gate == KLA_GATE_CHANNEL;
     if (a.dtype == KLA_DTYPE_BF16)
-        return ch ? launch_tokens_t<__nv_bfloat16, true>(a)
+        return ch ? (tokens_ch_supports(a) ? launch_tokens_ch(a) : launch_tokens_t<__nv_bfloat16, true>(a))
                   : tokens_tc_preferred(a) ? launch_tokens_tc(a) : launch_tokens_t<__nv_bfloat16, false>(a);
     return ch ? launch_tokens_t<float, true>(a) : launch_tokens_t<float, false>(a);
 }

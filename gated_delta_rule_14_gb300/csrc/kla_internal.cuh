@@ -102,6 +102,10 @@ cudaError_t launch_decode(const DecodeArgs &a);
 // decode, speculative verification, T <= kShortSeqMaxT) and every shape the tensor-core path
 // does not take; any supported size and dtype, fp32 arithmetic.
 constexpr int kShortSeqMaxT = 16;
+// The chunk form of 9-16 tokens with the per-channel gate (bf16, d_k = d_v = 128, 16-byte
+// aligned q, k, v, o, alpha and states): kla_tokens_ch.cu.
+bool tokens_ch_supports(const ChunkArgs &a);
+cudaError_t launch_tokens_ch(const ChunkArgs &a);
 bool recurrent_preferred(const ChunkArgs &a);
 cudaError_t launch_recurrent(const ChunkArgs &a);
 

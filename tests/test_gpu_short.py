@@ -186,3 +186,56 @@ def test_chunk_form_serving_batch_sampled():
     o, S = run_prefill(inp)
     check(inp, o, S, sample_chains(inp.wl.B, inp.wl.H, 16, seed=4))
 
+
+
+# The chunk form with the per-key-channel gate (bf16, d_k = d_v = 128, 9 to 16 tokens): in-call
+# products R and A formed exactly per channel, the decays inside scaled K, Q and K_end tiles.
+# T = 8 runs the token loop beside it.
+@pytest.mark.parametrize("T", [8, 9, 10, 13, 16])
+def test_channel_chunk_form_tokens(T):
+    inp = synth.make_prefill("kda8k", seed=700 + T, B=5, T=T, H=3, s0_sigma=0.05)
+    o, S = run_prefill(inp)
+    check(inp, o, S)
+
+
+def test_channel_chunk_form_extreme_gates():
+    """Per-channel gates of 1e-30 (the in-call decay far beyond e^-80 in some channels), exactly 0
+    and exactly 1, and keys that are exactly zero with eps = 0: the in-call products take
+    e^{G_i - G_m} <= 1 directly, so every gate in [0, 1] is exact."""
+    inp = synth.make_prefill("kda8k", seed=71, B=2, T=14, H=2, s0_sigma=0.05, eps=0.0)
+    k, alpha = inp.k.copy(), inp.alpha.copy()
+    alpha[0, 2:12, 0, 5:40] = 1e-30
+    alpha[1, 4, 1, :] = 0.0
+    alpha[1, 6:10, 0, :] = 1.0
+    k[0, [0, 13], 1] = 0
+    k[1, 7, 0] = 0
+    inp = dataclasses.replace(inp, k=k, alpha=alpha)
+    o, S = run_prefill(inp)
+    check(inp, o, S)
+
+
+def test_channel_chunk_form_verify_then_accept_prefix():
+    """Verification with the per-channel gate: the first j outputs of a 14-token draft equal a
+    j-token call's bit for bit (both padded to 16 tokens; later tokens add exact zeros), and the
+    state advanced in place by the accepted prefix matches the oracle."""
+    import gated_delta_rule_14_gb300 as kla
+    T, j = 14, 10
+    inp = synth.make_prefill("kda8k", seed=72, B=6, T=T, H=4, s0_sigma=0.02)
+    q, k, v, a, e = (to_dev(x) for x in (inp.q, inp.k, inp.v, inp.alpha, inp.eta))
+    S = to_dev(inp.S0).clone()
+    o_draft, _ = kla.chunk_fwd(q, k, v, a, e, inp.wl.eps, S)
+    o_acc, _ = kla.chunk_fwd(q[:, :j].contiguous(), k[:, :j].contiguous(), v[:, :j].contiguous(),
+                             a[:, :j].contiguous(), e[:, :j].contiguous(), inp.wl.eps, S, S_T=S)
+    kla.device_status(DEV)
+    assert (o_acc == o_draft[:, :j]).all().item()
+    pre = synth.PrefillInputs(dataclasses.replace(inp.wl, T=j), inp.q[:, :j], inp.k[:, :j], inp.v[:, :j],
+                              inp.alpha[:, :j], inp.eta[:, :j], inp.S0)
+    check(pre, o_acc.float().cpu().numpy().astype(np.float64), S.cpu().numpy().astype(np.float64))
+
+
+def test_channel_chunk_form_serving_batch_whole():
+    """16 draft tokens with the per-channel gate at the decode batch (64 sequences x 16 heads),
+    every head against the oracle."""
+    inp = synth.make_prefill("kda8k", seed=73, B=64, T=16, H=16, s0_sigma=0.02)
+    o, S = run_prefill(inp)
+    check(inp, o, S)
