@@ -62,10 +62,11 @@ DECODE_BYTES_PER_HEAD_STEP = 8 * 128 * 128 + 4 * 2 * 128 + 8
 # reports null.
 TC_SOURCES = ("gated_delta_rule_14_gb300/csrc/kla_chunk_tc.cu", "gated_delta_rule_14_gb300/csrc/sm103_ptx.cuh",
               "gated_delta_rule_14_gb300/csrc/kla_internal.cuh")
-TC_TRAFFIC_GDN4K = {"e9fa9b8b231d85d0": 520.831488e6}
+# (98a19049...: the same kernel code as e9fa9b8b...; the header gained two host declarations only.)
+TC_TRAFFIC_GDN4K = {"e9fa9b8b231d85d0": 520.831488e6, "98a1904944c627c7": 520.831488e6}
 # sm__pipe_tensor_cycles_active (fraction of elapsed cycles) of the same kernel and capture:
 # the algorithmic TFLOP/s divided by it is the rate of the MMA phases themselves.
-TC_PIPE_ACTIVE_GDN4K = {"e9fa9b8b231d85d0": 0.13132}
+TC_PIPE_ACTIVE_GDN4K = {"e9fa9b8b231d85d0": 0.13132, "98a1904944c627c7": 0.13132}
 
 
 def tc_fingerprint() -> str:
@@ -353,6 +354,7 @@ def bench_verify(ntok, calls, seed, dev, flush, stream, pk, channel=False):
 
 
 BWD_BYTES_PER_TOKEN_HEAD = 4 * 2 * 128 + 8 + 3 * 4 * 128 + 8   # q, k, v, dO in; dq, dk, dv, dalpha, deta out
+BWD_BYTES_PER_TOKEN_HEAD_KDA = BWD_BYTES_PER_TOKEN_HEAD + 2 * 4 * 127   # alpha and dalpha per key channel
 
 
 BWD_KERNELS_PER_CALL = 4   # chunkwise path: prep, forward carry, reverse carry, gradients
@@ -370,15 +372,15 @@ def bench_bwd(name, steps, seed, dev, flush, stream, pk, **override):
     g = torch.Generator(device=dev)
     g.manual_seed(seed)
     dO = torch.randn((wl.B, wl.T, wl.H, wl.d_v), device=dev, generator=g).to(torch.bfloat16)
-    ws = torch.empty(kla.bwd_workspace_size(wl.B, wl.T, wl.H, wl.d_k, wl.d_v, torch.bfloat16), dtype=torch.uint8,
-                     device=dev)
+    ws = torch.empty(kla.bwd_workspace_size(wl.B, wl.T, wl.H, wl.d_k, wl.d_v, torch.bfloat16,
+                                            per_channel_gate=wl.gate == "channel"), dtype=torch.uint8, device=dev)
 
     def step():
         kla.chunk_bwd(d["q"], d["k"], d["v"], d["alpha"], d["eta"], dO, wl.eps, workspace=ws, want_dS0=False)
 
     ms = statistics.fmean(time_steps(step, steps, 1, flush, stream))
     kla.device_status(dev)
-    alg = wl.B * wl.T * wl.H * BWD_BYTES_PER_TOKEN_HEAD
+    alg = wl.B * wl.T * wl.H * (BWD_BYTES_PER_TOKEN_HEAD_KDA if wl.gate == "channel" else BWD_BYTES_PER_TOKEN_HEAD)
     return {"value": wl.B * wl.T / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
             "workspace_bytes": ws.numel(), "roofline": roofline(alg, ms, pk),
             "note": "chunkwise backward on warp-level bf16 MMAs: chunk-parallel prep (T = (I+R)^-1, W, U, A), "
@@ -619,6 +621,13 @@ def main():
                                               "segments run in parallel (16 chains of 2048 chunks)")
             clocks.mark(t0, time.time())
             launches += 3 * BWD_LONG_KERNELS_PER_CALL
+            torch.cuda.empty_cache()
+            t0 = time.time()
+            extras["bwd_kda8k"] = bench_bwd("kda8k", 2, seed=rank, dev=dev, flush=flush, stream=stream, pk=pk)
+            extras["bwd_kda8k"]["note"] = ("per-channel gate: the token-sequential fp32 backward (one CTA per "
+                                           "chain, 8192 tokens in order); no chunkwise per-channel backward yet")
+            clocks.mark(t0, time.time())
+            launches += 2
             torch.cuda.empty_cache()
     clk = clocks.stop()
 
