@@ -358,6 +358,8 @@ BWD_BYTES_PER_TOKEN_HEAD_KDA = BWD_BYTES_PER_TOKEN_HEAD + 2 * 4 * 127   # alpha 
 
 
 BWD_KERNELS_PER_CALL = 4   # chunkwise path: prep, forward carry, reverse carry, gradients
+# per-channel gate: range check, prep, two carries, gradients, the rerun launch (its CTAs return)
+BWD_KDA_KERNELS_PER_CALL = 6
 # long131k: prep, 2 x (value runs, transitions, combine, reruns), gradients
 BWD_LONG_KERNELS_PER_CALL = 10
 
@@ -499,7 +501,8 @@ def main():
     ap.add_argument("--verify-calls", type=int, default=256)
     ap.add_argument("--no-bwd", action="store_true")
     ap.add_argument("--bwd-only", action="store_true",
-                    help="time only the backward pass of gdn4k (a small case for profiling with --bwd-batch)")
+                    help="time only the backward pass of --bwd-workload (a small case for profiling with --bwd-batch)")
+    ap.add_argument("--bwd-workload", choices=["gdn4k", "kda8k"], default="gdn4k")
     ap.add_argument("--bwd-batch", type=int, default=8)
     ap.add_argument("--prefill-only", choices=["gdn4k", "kda8k", "long131k"], default=None,
                     help="time only the prefill of this workload (a command for profiling one kernel)")
@@ -540,9 +543,10 @@ def main():
         return
 
     if args.bwd_only:
-        r = bench_bwd("gdn4k", args.steps, seed=rank, dev=dev, flush=flush, stream=stream, pk=pk, B=args.bwd_batch)
+        r = bench_bwd(args.bwd_workload, args.steps, seed=rank, dev=dev, flush=flush, stream=stream, pk=pk,
+                      B=args.bwd_batch)
         if rank == 0:
-            print(json.dumps({"bwd_gdn4k": r, "batch": args.bwd_batch}), flush=True)
+            print(json.dumps({f"bwd_{args.bwd_workload}": r, "batch": args.bwd_batch}), flush=True)
         return
 
     clocks = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
@@ -623,11 +627,14 @@ def main():
             launches += 3 * BWD_LONG_KERNELS_PER_CALL
             torch.cuda.empty_cache()
             t0 = time.time()
-            extras["bwd_kda8k"] = bench_bwd("kda8k", 2, seed=rank, dev=dev, flush=flush, stream=stream, pk=pk)
-            extras["bwd_kda8k"]["note"] = ("per-channel gate: the token-sequential fp32 backward (one CTA per "
-                                           "chain, 8192 tokens in order); no chunkwise per-channel backward yet")
+            extras["bwd_kda8k"] = bench_bwd("kda8k", 3, seed=rank, dev=dev, flush=flush, stream=stream, pk=pk)
+            extras["bwd_kda8k"]["note"] = ("per-channel gate, chunkwise: gate range check, prep with the per-channel "
+                                           "factor tiles (K e^{G-G_r}, K e^{G_r-G}, Q e^{G-G_r}), forward and reverse "
+                                           "chunk-state carries, chunk-parallel gradients with dk, dq and the "
+                                           "log-decay gradient per channel in registers; chains outside the "
+                                           "factorised range rerun on the token-sequential path (none here)")
             clocks.mark(t0, time.time())
-            launches += 2
+            launches += 3 * BWD_KDA_KERNELS_PER_CALL
             torch.cuda.empty_cache()
     clk = clocks.stop()
 

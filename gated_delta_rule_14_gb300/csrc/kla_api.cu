@@ -14,8 +14,7 @@ cudaError_t launch_tokens_pipe(const ChunkArgs &a);
 // backward paths: the chunkwise one (kla_bwd_chunk.cu) runs when it supports the call, with a
 // workspace of its own size; the token-sequential one (kla_bwd.cu) otherwise
 bool bwd_chunk_supports(const BwdArgs &a);
-size_t bwd_chunk_workspace_bytes(int B, int T, int H);
-size_t bwd_seq_workspace_bytes(int B, int T, int H, int d_k, int d_v);
+size_t bwd_chunk_workspace_bytes(int B, int T, int H, kla_gate gate);
 }  // namespace kla
 
 namespace {
@@ -238,9 +237,9 @@ size_t kla_chunk_bwd_workspace_size(int B, int T, int H, int d_k, int d_v) {
 }
 
 size_t kla_chunk_bwd_workspace_size_ex(int B, int T, int H, int d_k, int d_v, kla_dtype dtype, kla_gate gate) {
-    const bool chunked = dtype == KLA_DTYPE_BF16 && gate == KLA_GATE_SCALAR && d_k == 128 && d_v == 128 &&
-                         T > kla::kShortSeqMaxT && B >= 1 && H >= 1;
-    return chunked ? kla::bwd_chunk_workspace_bytes(B, T, H) : kla::bwd_seq_workspace_bytes(B, T, H, d_k, d_v);
+    const bool chunked = dtype == KLA_DTYPE_BF16 && (gate == KLA_GATE_SCALAR || gate == KLA_GATE_CHANNEL) &&
+                         d_k == 128 && d_v == 128 && T > kla::kShortSeqMaxT && B >= 1 && H >= 1;
+    return chunked ? kla::bwd_chunk_workspace_bytes(B, T, H, gate) : kla::bwd_seq_workspace_bytes(B, T, H, d_k, d_v);
 }
 
 kla_status kla_chunk_bwd(const void *q, const void *k, const void *v, const float *alpha, const float *eta,
@@ -262,7 +261,7 @@ kla_status kla_chunk_bwd(const void *q, const void *k, const void *v, const floa
                    dtype, gate, beta_mode == KLA_BETA_RAW, q_scale, workspace, workspace_bytes,
                    static_cast<cudaStream_t>(stream)};
     // the chunkwise path needs its own (smaller) workspace; any other call the token-sequential one's
-    const size_t need = T > 0 && kla::bwd_chunk_supports(a) ? kla::bwd_chunk_workspace_bytes(B, T, H)
+    const size_t need = T > 0 && kla::bwd_chunk_supports(a) ? kla::bwd_chunk_workspace_bytes(B, T, H, gate)
                                                             : kla::bwd_seq_workspace_bytes(B, T, H, d_k, d_v);
     if (workspace_bytes < need || (need > 0 && (!workspace || !aligned16(workspace)))) return KLA_ERR_INVALID_ARG;
 

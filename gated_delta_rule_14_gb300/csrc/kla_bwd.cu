@@ -45,6 +45,7 @@ struct BwdParams {
     int B, T, H, DK, DV, nblk;
     int beta_raw;
     float q_scale;
+    const unsigned *only;   // NULL, or [B*H]: only chains with a nonzero mark run (the others return at once)
 };
 
 __device__ __forceinline__ void prefetch_l2(const void *ptr) {   // the 128-byte line holding ptr
@@ -100,6 +101,7 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const BwdParams p) {
     const int cg = lane & 1, rg = lane >> 1;
     const int h = blockIdx.x, b = blockIdx.y;
     const size_t bh = static_cast<size_t>(b) * p.H + h;
+    if (p.only && p.only[bh] == 0u) return;
     const int col = warp * 8 + cg * 4;                // this lane's first value column
     const int r0 = rg * kRows;
     const bool live = r0 < DK;
@@ -434,12 +436,12 @@ size_t bwd_smem_bytes(int DK, int DV, int rows) {
 }
 
 template <typename TIn, bool kChannel>
-cudaError_t launch_t(const BwdArgs &a) {
+cudaError_t launch_t(const BwdArgs &a, const unsigned *only) {
     const int nblk = (a.T + kBlk - 1) / kBlk;
     float *ck = static_cast<float *>(a.workspace);
     float *ew = ck + static_cast<size_t>(a.B) * a.H * nblk * a.d_k * a.d_v;
     BwdParams p{a.q, a.k, a.v, a.dO, a.alpha, a.eta, a.eps, a.S0, a.dS_T, a.dq, a.dk, a.dv, a.dalpha, a.deta,
-                a.dS0, ck, ew, a.B, a.T, a.H, a.d_k, a.d_v, nblk, a.beta_raw, a.q_scale};
+                a.dS0, ck, ew, a.B, a.T, a.H, a.d_k, a.d_v, nblk, a.beta_raw, a.q_scale, only};
     const int rows = std::max(1, a.d_k / 16);
     const size_t smem = bwd_smem_bytes(a.d_k, a.d_v, rows);
     auto kern = rows == 1 ? bwd_kernel<TIn, kChannel, 1>
@@ -455,9 +457,9 @@ cudaError_t launch_t(const BwdArgs &a) {
 
 }  // namespace
 
-// The chunkwise tensor-core backward (kla_bwd_chunk.cu): bf16, scalar gate, d_k = d_v = 128.
+// The chunkwise tensor-core backward (kla_bwd_chunk.cu, kla_bwd_chunk_ch.cu): bf16, d_k = d_v = 128.
 bool bwd_chunk_supports(const BwdArgs &a);
-size_t bwd_chunk_workspace_bytes(int B, int T, int H);
+size_t bwd_chunk_workspace_bytes(int B, int T, int H, kla_gate gate);
 cudaError_t launch_bwd_chunk(const BwdArgs &a);
 
 size_t bwd_seq_workspace_bytes(int B, int T, int H, int d_k, int d_v) {
@@ -466,17 +468,23 @@ size_t bwd_seq_workspace_bytes(int B, int T, int H, int d_k, int d_v) {
     return (static_cast<size_t>(B) * H * nblk * d_k * d_v + static_cast<size_t>(B) * T * H * d_v) * sizeof(float);
 }
 
-size_t bwd_workspace_bytes(int B, int T, int H, int d_k, int d_v) {   // either path
+size_t bwd_workspace_bytes(int B, int T, int H, int d_k, int d_v) {   // either path, either gate
     const size_t seq = bwd_seq_workspace_bytes(B, T, H, d_k, d_v);
-    return d_k == 128 && d_v == 128 && T > kShortSeqMaxT ? std::max(seq, bwd_chunk_workspace_bytes(B, T, H)) : seq;
+    if (!(d_k == 128 && d_v == 128 && T > kShortSeqMaxT)) return seq;
+    return std::max({seq, bwd_chunk_workspace_bytes(B, T, H, KLA_GATE_SCALAR),
+                     bwd_chunk_workspace_bytes(B, T, H, KLA_GATE_CHANNEL)});
+}
+
+cudaError_t launch_bwd_seq(const BwdArgs &a, const unsigned *only) {
+    const bool ch = a.gate == KLA_GATE_CHANNEL;
+    if (a.dtype == KLA_DTYPE_BF16)
+        return ch ? launch_t<__nv_bfloat16, true>(a, only) : launch_t<__nv_bfloat16, false>(a, only);
+    return ch ? launch_t<float, true>(a, only) : launch_t<float, false>(a, only);
 }
 
 cudaError_t launch_bwd(const BwdArgs &a) {
     if (bwd_chunk_supports(a)) return launch_bwd_chunk(a);
-    const bool ch = a.gate == KLA_GATE_CHANNEL;
-    if (a.dtype == KLA_DTYPE_BF16)
-        return ch ? launch_t<__nv_bfloat16, true>(a) : launch_t<__nv_bfloat16, false>(a);
-    return ch ? launch_t<float, true>(a) : launch_t<float, false>(a);
+    return launch_bwd_seq(a, nullptr);
 }
 
 }  // namespace kla

@@ -44,53 +44,12 @@
 #include <algorithm>
 #include <mutex>
 
-#include "kla_internal.cuh"
-#include "warp_mma.cuh"
+#include "kla_bwd_chunk.cuh"
 
 namespace kla {
 namespace {
 
-constexpr int kC = 64;                  // chunk
-constexpr int kD = 128;                 // d_k = d_v
-constexpr int kP = kD + 8;              // pitch (bf16 elements) of a tile with 128 columns
-constexpr int kPs = kC + 8;             // pitch of a tile with 64 columns
-constexpr int kTileTok = kC * kP * 2;   // 64 x 128 bf16 tile: 17408 bytes
-constexpr int kTileSt = kD * kP * 2;    // 128 x 128: 34816
-constexpr int kTileSq = kC * kPs * 2;   // 64 x 64: 9216
-constexpr float kMinLogGate = -80.0f;
-
-typedef __nv_bfloat16 bf16;
-
-// ---- per-chunk workspace records (structure of arrays over n = chain * nc + chunk)
-constexpr size_t kCgFloats = 3 * kC;    // G, beta, den = ||k||^2 + eps
-struct Ws {
-    float *cg;        // [N][3][64]
-    bf16 *W;          // [N][64][128]
-    bf16 *UdE;        // [N][64][128]: U (prep -> forward carry), then dE (reverse carry -> gradients)
-    bf16 *A;          // [N][64][64]  lower(ratio . QK^T), unscaled by s
-    bf16 *Tm;         // [N][64][64]  T = (I + R)^{-1}
-    bf16 *S;          // [N][128][128] state entering the chunk
-    bf16 *E;          // [N][64][128]
-    bf16 *dS;         // [N][128][128] dL/d(state leaving the chunk)
-    float *seg;       // long chains split into segments: Z | M | start states, each [chains][nseg][128][128]
-};
-size_t ws_bytes_per_chunk() {
-    return kCgFloats * 4 + 2 * (3 * kC * kD + 2 * kC * kC + 2 * kD * kD);
-}
-Ws carve(void *base, size_t N) {
-    char *p = static_cast<char *>(base);
-    Ws w;
-    w.cg = reinterpret_cast<float *>(p);             p += N * kCgFloats * 4;
-    w.W = reinterpret_cast<bf16 *>(p);               p += N * kC * kD * 2;
-    w.UdE = reinterpret_cast<bf16 *>(p);             p += N * kC * kD * 2;
-    w.E = reinterpret_cast<bf16 *>(p);               p += N * kC * kD * 2;
-    w.A = reinterpret_cast<bf16 *>(p);               p += N * kC * kC * 2;
-    w.Tm = reinterpret_cast<bf16 *>(p);              p += N * kC * kC * 2;
-    w.S = reinterpret_cast<bf16 *>(p);               p += N * kD * kD * 2;
-    w.dS = reinterpret_cast<bf16 *>(p);              p += N * kD * kD * 2;
-    w.seg = reinterpret_cast<float *>(p);
-    return w;
-}
+using namespace bwdc;
 
 // Segments for the two carries of a long chain (the forward prefill's sequence-parallel scan,
 // applied to them): both carries are affine in their state, X_end = M X_start + Z over a
@@ -124,77 +83,6 @@ CarryPlan carry_plan(int chains, int nc) {
     return {(nc + L - 1) / L, L};
 }
 
-// ---------------------------------------------------------------- warp-level MMA helpers
-using namespace wmma16;
-
-template <int NT>   // NT n8 tiles (even)
-__device__ __forceinline__ void zero(float (&acc)[NT][4]) {
-#pragma unroll
-    for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-}
-// acc[16 x (8 NT)] += A[r0.., k0..k0+16*KS) * B[.., n0..]: one warp, A and B layouts as template flags.
-template <int NT, int KS, bool kAT, bool kBT>
-__device__ __forceinline__ void gemm(float (&acc)[NT][4], uint32_t ta, int pa, int r0, int ka, uint32_t tb, int pb,
-                                     int n0, int kb, int lane) {
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-        uint32_t a[4];
-        if (kAT) frag_a_kr(ta, pa, r0, ka + 16 * ks, lane, a);
-        else frag_a_rk(ta, pa, r0, ka + 16 * ks, lane, a);
-#pragma unroll
-        for (int j = 0; j < NT / 2; ++j) {
-            uint32_t b[4];
-            if (kBT) frag_b_kr(tb, pb, n0 + 16 * j, kb + 16 * ks, lane, b);
-            else frag_b_rk(tb, pb, n0 + 16 * j, kb + 16 * ks, lane, b);
-            mma(acc[2 * j], a, b[0], b[1]);
-            mma(acc[2 * j + 1], a, b[2], b[3]);
-        }
-    }
-}
-__device__ __forceinline__ void st_pair(bf16 *tile, int pitch, int r, int c, float lo, float hi) {
-    *reinterpret_cast<uint32_t *>(tile + r * pitch + c) = pack2(lo, hi);
-}
-__device__ __forceinline__ float2 ld_pair(const bf16 *tile, int pitch, int r, int c) {
-    return unpack2(*reinterpret_cast<const uint32_t *>(tile + r * pitch + c));
-}
-__device__ __forceinline__ void cp16(void *dst, const void *src, bool valid) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sptr(dst)), "l"(src), "r"(valid ? 16 : 0)
-                 : "memory");
-}
-__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {   // 16-byte aligned, multiple of 16
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-// 64 token rows x 128 columns of a [B,T,H,128] bf16 tensor into a padded tile (rows >= L zero).
-__device__ __forceinline__ void load_tok(bf16 *tile, const bf16 *src, size_t row_stride, int L, int tid,
-                                         int nthreads) {
-    for (int i = tid; i < kC * 16; i += nthreads) {
-        const int r = i >> 4, c = (i & 15) * 8;
-        const bool ok = r < L;
-        cp16(tile + r * kP + c, src + (ok ? r : 0) * row_stride + c, ok);
-    }
-}
-// `rows` dense rows of `cols` bf16 (cols = 64 or 128) from the workspace into a padded tile.
-template <int kCols>
-__device__ __forceinline__ void load_dense(bf16 *tile, const bf16 *src, int rows, int tid, int nthreads) {
-    constexpr int kPitch = kCols + 8, kChunks = kCols / 8;
-    for (int i = tid; i < rows * kChunks; i += nthreads) {
-        const int r = i / kChunks, c = (i % kChunks) * 8;
-        cp16(tile + r * kPitch + c, src + r * kCols + c, true);
-    }
-}
-template <int kCols>
-__device__ __forceinline__ void store_dense(bf16 *dst, const bf16 *tile, int rows, int tid, int nthreads) {
-    constexpr int kPitch = kCols + 8, kChunks = kCols / 8;
-    for (int i = tid; i < rows * kChunks; i += nthreads) {
-        const int r = i / kChunks, c = (i % kChunks) * 8;
-        *reinterpret_cast<uint4 *>(dst + r * kCols + c) = *reinterpret_cast<const uint4 *>(tile + r * kPitch + c);
-    }
-}
-
 // ============================================================== kernel 1: per-chunk operands
 struct PrepParams {
     const bf16 *q, *k, *v;
@@ -207,12 +95,10 @@ struct PrepParams {
 constexpr int kPrepThreads = 256;
 // shared memory of the prep kernel
 constexpr int PR_K = 0, PR_Q = PR_K + kTileTok, PR_V = PR_Q + kTileTok;
-constexpr int kPR = 68;                               // pitch of the fp32 64 x 64 tile (4 mod 32: no conflicts)
 constexpr int PR_R = PR_V + kTileTok;                 // fp32 [64][68]: R, overwritten by T block by block
 constexpr int PR_TK = PR_R + kC * kPR * 4;            // bf16 T diag(beta gamma)
 constexpr int PR_TV = PR_TK + kTileSq;                // bf16 T diag(beta)
 constexpr int PR_A = PR_TV + kTileSq;                 // bf16 A (then T) staging
-constexpr int kPX = 36;
 constexpr int PR_X = PR_A + kTileSq;                  // fp32 [32][36] merge scratch
 constexpr int PR_VEC = PR_X + 32 * kPX * 4;           // eta, G, beta, beta e^G (fp32 [4][64])
 constexpr int PR_BYTES = PR_VEC + 4 * kC * 4;
@@ -313,68 +199,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) bwd_prep_kernel(PrepParams p)
     __syncthreads();
     store_dense<kC>(p.ws.A + n * kC * kC, sA, kC, tid, kPrepThreads);
 
-    // T = (I + R)^{-1}, in place over R. (1) the four 16 x 16 diagonal blocks by substitution:
-    // warp 0 lanes 0-15 / 16-31 take blocks 0 / 1, warp 1 blocks 2 / 3; lane = column.
-    if (warp < 2) {
-        const int blk = 2 * warp + (lane >> 4), j = lane & 15, o = 16 * blk;
-        float t[16];
-#pragma unroll
-        for (int m = 0; m < 16; ++m) t[m] = m == j ? 1.f : 0.f;
-#pragma unroll
-        for (int i = 1; i < 16; ++i) {
-            float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-            for (int m = 0; m < i; ++m) {
-                if (m & 1) a1 = fmaf(sR[o + i][o + m], t[m], a1);
-                else a0 = fmaf(sR[o + i][o + m], t[m], a0);
-            }
-            if (i > j) t[i] = -(a0 + a1);
-        }
-        __syncwarp();
-#pragma unroll
-        for (int m = 0; m < 16; ++m) sR[o + m][o + j] = t[m];
-    }
-    __syncthreads();
-    // (2) merges: [T11 0; R21 T22]^{-1} has lower block -T22 R21 T11, on tf32 warp MMAs.
-    // Size 16: two merges side by side (blocks at 0 and 32), warp w < 4 takes merge w >> 1 and
-    // output columns 8 (w & 1); size 32: warp w takes output rows 16 (w >> 2), columns 8 (w & 3).
-    const float *R0 = &sR[0][0];
-    float *R0w = &sR[0][0];
-    const int g = lane >> 2, q4 = lane & 3;
-    auto put_tile = [&](float *M, int pitch, int r, int cc, const float (&acc)[4], float sign) {
-        M[(r + g) * pitch + cc + 2 * q4] = sign * acc[0];
-        M[(r + g) * pitch + cc + 2 * q4 + 1] = sign * acc[1];
-        M[(r + g + 8) * pitch + cc + 2 * q4] = sign * acc[2];
-        M[(r + g + 8) * pitch + cc + 2 * q4 + 1] = sign * acc[3];
-    };
-    if (warp < 4) {   // X = R21 T11
-        const int o = 32 * (warp >> 1), nc8 = 8 * (warp & 1);
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        tile_tf32<2>(acc, R0, kPR, o + 16, o, R0, kPR, o, o + nc8, lane);
-        put_tile(sX, kPX, 16 * (warp >> 1), nc8, acc, 1.f);
-    }
-    __syncthreads();
-    if (warp < 4) {   // T21 = -T22 X
-        const int o = 32 * (warp >> 1), nc8 = 8 * (warp & 1);
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        tile_tf32<2>(acc, R0, kPR, o + 16, o + 16, sX, kPX, 16 * (warp >> 1), nc8, lane);
-        put_tile(R0w, kPR, o + 16, o + nc8, acc, -1.f);
-    }
-    __syncthreads();
-    {   // X = R21 T11 at size 32
-        const int mr = 16 * (warp >> 2), nc8 = 8 * (warp & 3);
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        tile_tf32<4>(acc, R0, kPR, 32 + mr, 0, R0, kPR, 0, nc8, lane);
-        put_tile(sX, kPX, mr, nc8, acc, 1.f);
-    }
-    __syncthreads();
-    {   // T21 = -T22 X
-        const int mr = 16 * (warp >> 2), nc8 = 8 * (warp & 3);
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        tile_tf32<4>(acc, R0, kPR, 32 + mr, 32, sX, kPX, 0, nc8, lane);
-        put_tile(R0w, kPR, 32 + mr, nc8, acc, -1.f);
-    }
-    __syncthreads();
+    unit_lower_inverse64(sR, sX, warp, lane);
     // T diag(beta gamma), T diag(beta) and T as bf16 (the upper triangle is zero)
     for (int e = tid; e < kC * kC / 2; e += kPrepThreads) {
         const int i = e / (kC / 2), j = 2 * (e % (kC / 2));
@@ -406,35 +231,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2) bwd_prep_kernel(PrepParams p)
     store_dense<kD>(p.ws.UdE + n * kC * kD, sK, kC, tid, kPrepThreads);
 }
 
-// acc[MT m16 tiles][NT n8 tiles] += A * B for MT row tiles at r0, r0 + 16, ... (B fragments shared).
-template <int MT, int NT, int KS, bool kAT, bool kBT>
-__device__ __forceinline__ void gemm_m(float (&acc)[MT][NT][4], uint32_t ta, int pa, int r0, int ka, uint32_t tb,
-                                       int pb, int n0, int kb, int lane) {
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-        uint32_t a[MT][4];
-#pragma unroll
-        for (int mi = 0; mi < MT; ++mi) {
-            if (kAT) frag_a_kr(ta, pa, r0 + 16 * mi, ka + 16 * ks, lane, a[mi]);
-            else frag_a_rk(ta, pa, r0 + 16 * mi, ka + 16 * ks, lane, a[mi]);
-        }
-#pragma unroll
-        for (int j = 0; j < NT / 2; ++j) {
-            uint32_t b[4];
-            if (kBT) frag_b_kr(tb, pb, n0 + 16 * j, kb + 16 * ks, lane, b);
-            else frag_b_rk(tb, pb, n0 + 16 * j, kb + 16 * ks, lane, b);
-#pragma unroll
-            for (int mi = 0; mi < MT; ++mi) {
-                mma(acc[mi][2 * j], a[mi], b[0], b[1]);
-                mma(acc[mi][2 * j + 1], a[mi], b[2], b[3]);
-            }
-        }
-    }
-}
-
 // ============================================================== kernel 2: the carry across chunks
 // Forward (kRev = false), X = S entering chunk c, c ascending:
 //     E = U - W X;  X <- Gamma X + K^T diag(e_end) E            stores X (bf16) and E per chunk
+// (kCh: the per-key-channel gate, with K e^{G_end - G} and s Q e^{G} read from the prep's records
+// and Gamma = diag(e^{G_end}) applied to the rows of X.)
 // Reverse (kRev = true), X = dS' = dL/d(state leaving chunk c), c descending:
 //     dE = diag(e_end) K X + s A^T dO;  X <- Gamma X + (s diag(gamma) Q)^T dO - W^T dE
 //                                                               stores X (bf16) and dE per chunk
@@ -458,6 +259,7 @@ struct ScanParams {
     int records;          // per-chunk records (S_c, E_c or dS_{c+1}, dE_c): 0 none, 1 all, 2 segment r = 0 only
     float *Xseg;          // NULL, or [chains][nseg][128][128]: X at the end of each segment
     const float *Xst;     // kX0Given: [chains][nseg][128][128] start states
+    const unsigned *skip; // NULL, or [B*H]: chains left to the token-sequential path (their CTAs return)
 };
 enum : int {
     kX0Chain = 0,      // X0 for the chain's first segment (r = 0), zeros for the others
@@ -472,7 +274,7 @@ constexpr int SC_X = 2 * SC_STAGE, SC_M = SC_X + kTileSt;
 constexpr int SC_BYTES = SC_M + kTileTok;
 static_assert(SC_STAGE % 16 == 0 && SC_BYTES <= 232448, "scan shared memory");
 
-template <bool kRev>
+template <bool kRev, bool kCh>
 __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(ScanParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
     bf16 *sX = reinterpret_cast<bf16 *>(smem + SC_X), *sM = reinterpret_cast<bf16 *>(smem + SC_M);
@@ -480,6 +282,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(ScanParams 
     const int g = lane >> 2, q4 = lane & 3;
     const int bh = blockIdx.x / p.seg_count, r = p.seg_begin + blockIdx.x % p.seg_count;
     const int b = bh / p.H, h = bh % p.H;
+    if (p.skip && p.skip[bh]) return;
     const size_t rs = static_cast<size_t>(p.H) * kD;
     const int sidx = kRev ? p.nseg - 1 - r : r;   // segment index in time
     const int c_lo = sidx * p.seg_len, c_hi = min((sidx + 1) * p.seg_len, p.nc) - 1;
@@ -492,19 +295,24 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(ScanParams 
         const int t0 = c * kC, L = min(kC, p.T - t0);
         const size_t base = ((static_cast<size_t>(b) * p.T + t0) * p.H + h) * kD;
         const size_t n = static_cast<size_t>(bh) * p.nc + c;
-        load_tok(stage(buf, SC_K), p.k + base, rs, L, tid, kScanThreads);
+        if (kCh) load_dense<kD>(stage(buf, SC_K), p.ws.Ke + n * kC * kD, kC, tid, kScanThreads);
+        else load_tok(stage(buf, SC_K), p.k + base, rs, L, tid, kScanThreads);
         load_dense<kD>(stage(buf, SC_W), p.ws.W + n * kC * kD, kC, tid, kScanThreads);
         if (p.drive) {
             if (kRev) {
-                load_tok(stage(buf, SC_UQ), p.q + base, rs, L, tid, kScanThreads);
+                if (kCh) load_dense<kD>(stage(buf, SC_UQ), p.ws.Qg + n * kC * kD, kC, tid, kScanThreads);
+                else load_tok(stage(buf, SC_UQ), p.q + base, rs, L, tid, kScanThreads);
                 load_tok(stage(buf, SC_DO), p.dO + base, rs, L, tid, kScanThreads);
                 load_dense<kC>(stage(buf, SC_A), p.ws.A + n * kC * kC, kC, tid, kScanThreads);
             } else {
                 load_dense<kD>(stage(buf, SC_UQ), p.ws.UdE + n * kC * kD, kC, tid, kScanThreads);
             }
         }
-        if (tid < static_cast<int>(kCgFloats) / 4)
+        if (kCh) {   // e^{G_end} per key channel
+            if (tid < kD / 4) cp16(smem + buf * SC_STAGE + SC_CG + 16 * tid, p.ws.gend + n * kD + 4 * tid, true);
+        } else if (tid < static_cast<int>(kCgFloats) / 4) {
             cp16(smem + buf * SC_STAGE + SC_CG + 16 * tid, p.ws.cg + n * kCgFloats + 4 * tid, true);
+        }
     };
 
     // X in registers: rows xr0 + 16 mi + g (+8), columns xc0 + 8 ni + 2 q4 (+1)
@@ -551,8 +359,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(ScanParams 
         if (it + 1 < steps) issue(kRev ? c - 1 : c + 1, buf ^ 1);
         cp_commit();
         const float *cg = reinterpret_cast<const float *>(smem + buf * SC_STAGE + SC_CG);
-        const float Gend = cg[kC - 1], Gam = __expf(Gend);
-        if (kRev && p.drive) {   // Q <- s diag(gamma) Q, in place (read only by the second product)
+        const float Gend = kCh ? 0.f : cg[kC - 1], Gam = kCh ? 1.f : __expf(Gend);
+        if (!kCh && kRev && p.drive) {   // Q <- s diag(gamma) Q, in place (read only by the second product)
             bf16 *sQ = stage(buf, SC_UQ);
             for (int i = tid; i < kC * 16; i += kScanThreads) {
                 const int tr = i >> 4, cc = (i & 15) * 8;
@@ -585,7 +393,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(ScanParams 
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             const int rw = m0 + g + 8 * hh;
-            const float ee = __expf(Gend - cg[rw]);
+            const float ee = kCh ? 1.f : __expf(Gend - cg[rw]);   // per-channel gate: in the Ke record
 #pragma unroll
             for (int ni = 0; ni < 4; ++ni) {
                 const int col = n0 + 8 * ni + 2 * q4;
@@ -605,13 +413,13 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(ScanParams 
         }
         __syncthreads();   // sM and the scaled Q are visible
 
-        // X <- Gamma X + ...
+        // X <- Gamma X + ...  (per-channel gate: row i of X decays by e^{G_end, i})
 #pragma unroll
         for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
             for (int ni = 0; ni < 4; ++ni)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) X[mi][ni][e] *= Gam;
+                for (int e = 0; e < 4; ++e) X[mi][ni][e] *= kCh ? cg[xr0 + 16 * mi + g + 8 * (e >> 1)] : Gam;
         if (kRev) {
             if (p.drive)
                 gemm_m<2, 4, 4, true, true>(X, sptr(stage(buf, SC_UQ)), kP, xr0, 0, sptr(stage(buf, SC_DO)), kP, xc0,
@@ -676,10 +484,6 @@ constexpr int GR_XS = GR_KC + kC * 4;                              // fp32 [4] s
 constexpr int GR_BYTES = GR_XS + 16;
 static_assert(GR_BYTES <= 232448, "gradient kernel shared memory");
 constexpr uint32_t kBarToken = 1, kBarK = 2, kBarQ = 3;           // named barriers (0 = __syncthreads)
-
-__device__ __forceinline__ void bar_named(uint32_t id, uint32_t n) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
 
 __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_kernel(GradParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
@@ -1077,12 +881,24 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_kernel(GradParams p)
 
 }  // namespace
 
-size_t bwd_chunk_workspace_bytes(int B, int T, int H) {
-    if (B < 1 || T < 1 || H < 1) return 0;
+namespace {
+// Per-channel gate: one mark per chain (256-byte aligned) in front of the rest of the workspace.
+size_t mark_bytes(int B, int H) { return (static_cast<size_t>(B) * H * sizeof(unsigned) + 255) & ~size_t(255); }
+size_t record_bytes(int B, int T, int H, bool ch) {
     const size_t nc = (static_cast<size_t>(T) + kC - 1) / kC, chains = static_cast<size_t>(B) * H;
     const CarryPlan pl = carry_plan(B * H, static_cast<int>(nc));
     const size_t seg = pl.nseg > 1 ? 3 * chains * pl.nseg * kD * kD * sizeof(float) : 0;
-    return chains * nc * ws_bytes_per_chunk() + seg;
+    return chains * nc * ws_bytes_per_chunk(ch) + seg;
+}
+}  // namespace
+
+// Scalar gate: the per-chunk records (and segment states). Per-channel gate: the marks, then room
+// for either the records or the token-sequential path's checkpoints, which rerun the marked chains
+// after the chunkwise kernels are done with the records.
+size_t bwd_chunk_workspace_bytes(int B, int T, int H, kla_gate gate) {
+    if (B < 1 || T < 1 || H < 1) return 0;
+    if (gate != KLA_GATE_CHANNEL) return record_bytes(B, T, H, false);
+    return mark_bytes(B, H) + std::max(record_bytes(B, T, H, true), bwd_seq_workspace_bytes(B, T, H, kD, kD));
 }
 
 // Sequences of at most kShortSeqMaxT tokens take the token-by-token fp32 backward: there a
@@ -1090,9 +906,11 @@ size_t bwd_chunk_workspace_bytes(int B, int T, int H) {
 // average the rounding over, and the sequential walk is short.
 bool bwd_chunk_supports(const BwdArgs &a) {
     auto al16 = [](const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; };
-    return a.dtype == KLA_DTYPE_BF16 && a.gate == KLA_GATE_SCALAR && a.d_k == kD && a.d_v == kD && a.T > kShortSeqMaxT &&
-           static_cast<long long>(a.B) * a.H <= 65535 && al16(a.q) && al16(a.k) && al16(a.v) && al16(a.dO) &&
-           al16(a.workspace) && a.workspace_bytes >= bwd_chunk_workspace_bytes(a.B, a.T, a.H);
+    const bool ch = a.gate == KLA_GATE_CHANNEL;
+    return a.dtype == KLA_DTYPE_BF16 && (a.gate == KLA_GATE_SCALAR || ch) && a.d_k == kD && a.d_v == kD &&
+           a.T > kShortSeqMaxT && static_cast<long long>(a.B) * a.H <= 65535 && al16(a.q) && al16(a.k) &&
+           al16(a.v) && al16(a.dO) && al16(a.workspace) &&
+           a.workspace_bytes >= bwd_chunk_workspace_bytes(a.B, a.T, a.H, a.gate);
 }
 
 // When the CTAs of pass 1a and pass 1b of a segmented carry fit on the SMs together (the plan
@@ -1112,24 +930,39 @@ std::mutex g_carry_aux_mutex[kMaxCarryDevices];
 
 cudaError_t launch_bwd_chunk(const BwdArgs &a) {
     const int nc = (a.T + kC - 1) / kC, chains = a.B * a.H;
-    const Ws ws = carve(a.workspace, static_cast<size_t>(chains) * nc);
+    const bool ch = a.gate == KLA_GATE_CHANNEL;
+    // per-channel gate: marks of the chains out of the factorised range, then the records
+    unsigned *marks = ch ? static_cast<unsigned *>(a.workspace) : nullptr;
+    void *rec = ch ? static_cast<char *>(a.workspace) + mark_bytes(a.B, a.H) : a.workspace;
+    const Ws ws = carve(rec, static_cast<size_t>(chains) * nc, ch);
     const bf16 *q = static_cast<const bf16 *>(a.q), *k = static_cast<const bf16 *>(a.k),
                *v = static_cast<const bf16 *>(a.v), *dO = static_cast<const bf16 *>(a.dO);
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(bwd_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PR_BYTES)) ||
-        (e = cudaFuncSetAttribute(chunk_scan_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SC_BYTES)) ||
-        (e = cudaFuncSetAttribute(chunk_scan_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SC_BYTES)) ||
-        (e = cudaFuncSetAttribute(bwd_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, GR_BYTES)))
+    auto scan_f = ch ? chunk_scan_kernel<false, true> : chunk_scan_kernel<false, false>;
+    auto scan_r = ch ? chunk_scan_kernel<true, true> : chunk_scan_kernel<true, false>;
+    if ((e = cudaFuncSetAttribute(scan_f, cudaFuncAttributeMaxDynamicSharedMemorySize, SC_BYTES)) ||
+        (e = cudaFuncSetAttribute(scan_r, cudaFuncAttributeMaxDynamicSharedMemorySize, SC_BYTES)))
         return e;
-    PrepParams pp{q, k, v, a.alpha, a.eta, a.eps, a.beta_raw, a.B, a.T, a.H, nc, ws};
-    bwd_prep_kernel<<<dim3(nc, chains), kPrepThreads, PR_BYTES, a.stream>>>(pp);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const ChBwd cp{q, k, v, dO, a.alpha, a.eta, a.eps, a.q_scale, a.beta_raw, a.B, a.T, a.H, nc, ws, marks,
+                   a.dq, a.dk, a.dv, a.dalpha, a.deta};
+    if (ch) {
+        if ((e = launch_gate_range(a.alpha, a.B, a.T, a.H, marks, a.stream)) != cudaSuccess ||
+            (e = launch_bwd_prep_ch(cp, a.stream)) != cudaSuccess)
+            return e;
+    } else {
+        if ((e = cudaFuncSetAttribute(bwd_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PR_BYTES)) ||
+            (e = cudaFuncSetAttribute(bwd_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, GR_BYTES)))
+            return e;
+        PrepParams pp{q, k, v, a.alpha, a.eta, a.eps, a.beta_raw, a.B, a.T, a.H, nc, ws};
+        bwd_prep_kernel<<<dim3(nc, chains), kPrepThreads, PR_BYTES, a.stream>>>(pp);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     const CarryPlan pl = carry_plan(chains, nc);
     const size_t part = static_cast<size_t>(chains) * pl.nseg * kD * kD;
     for (int rev = 0; rev < 2; ++rev) {
-        auto kern = rev ? chunk_scan_kernel<true> : chunk_scan_kernel<false>;
+        auto kern = rev ? scan_r : scan_f;
         ScanParams sp{q, k, dO, rev ? a.dS_T : a.S0, rev ? a.dS0 : nullptr, a.q_scale, a.B, a.T, a.H, nc, ws,
-                      pl.seg_len, 0, 1, pl.nseg, kX0Chain, 1, 1, nullptr, nullptr};
+                      pl.seg_len, 0, 1, pl.nseg, kX0Chain, 1, 1, nullptr, nullptr, marks};
         if (pl.nseg <= 1) {
             kern<<<chains, kScanThreads, SC_BYTES, a.stream>>>(sp);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -1195,6 +1028,15 @@ cudaError_t launch_bwd_chunk(const BwdArgs &a) {
         p3.Xst = Sst;
         kern<<<chains * p3.seg_count, kScanThreads, SC_BYTES, a.stream>>>(p3);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (ch) {
+        // the chunkwise gradients, then the marked chains again on the exact token-sequential path,
+        // its checkpoints over the records (every kernel that reads them has run by then)
+        if ((e = launch_bwd_grad_ch(cp, a.stream)) != cudaSuccess) return e;
+        BwdArgs r = a;
+        r.workspace = rec;
+        r.workspace_bytes = a.workspace_bytes - mark_bytes(a.B, a.H);
+        return launch_bwd_seq(r, marks);
     }
     GradParams gp{q, k, v, dO, a.alpha, a.q_scale, a.beta_raw, a.dq, a.dk, a.dv, a.dalpha, a.deta, a.B, a.T, a.H, nc, ws};
     bwd_grad_kernel<<<dim3(nc, chains), kGradThreads, GR_BYTES, a.stream>>>(gp);

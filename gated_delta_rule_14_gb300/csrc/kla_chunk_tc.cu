@@ -1141,6 +1141,14 @@ cudaError_t launch_rescue(const ChunkArgs &a, const unsigned *flags) {
 
 }  // namespace
 
+cudaError_t launch_gate_range(const float *alpha, int B, int T, int H, unsigned *marks, cudaStream_t stream) {
+    cudaError_t e = cudaMemsetAsync(marks, 0, static_cast<size_t>(B) * H * sizeof(unsigned), stream);
+    if (e != cudaSuccess) return e;
+    if (T < 1) return cudaSuccess;
+    gate_range_kernel<<<dim3((T + kC - 1) / kC, H, B), kD, 0, stream>>>(alpha, T, H, marks);
+    return cudaGetLastError();
+}
+
 size_t chunk_tc_workspace_bytes(int B, int T, int H, kla_gate gate) {
     return seg_workspace_bytes(B, T, H) + (gate == KLA_GATE_CHANNEL ? rescue_flag_bytes(B, H) : 0);
 }
@@ -1167,10 +1175,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a) {
     unsigned *flags = nullptr;
     if (a.gate == KLA_GATE_CHANNEL && a.workspace && a.workspace_bytes >= seg_bytes + rescue_flag_bytes(a.B, a.H)) {
         flags = reinterpret_cast<unsigned *>(static_cast<char *>(a.workspace) + seg_bytes);
-        if ((e = cudaMemsetAsync(flags, 0, static_cast<size_t>(chains) * sizeof(unsigned), a.stream)) != cudaSuccess)
-            return e;
-        gate_range_kernel<<<dim3((a.T + kC - 1) / kC, a.H, a.B), kD, 0, a.stream>>>(a.alpha, a.T, a.H, flags);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = launch_gate_range(a.alpha, a.B, a.T, a.H, flags, a.stream)) != cudaSuccess) return e;
     }
     TcParams p{a.alpha, a.eta, a.eps, a.S0, a.S_T, a.B, a.T, a.H, pl.seg_len, 0, 1, pl.nseg,
                kS0Chain, kSTLast, 0, 0, a.err, a.beta_raw, a.q_scale, flags};

@@ -90,12 +90,20 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a);
 // long sequences into segments that run in parallel, and with the per-channel gate one flag per
 // (sequence, head) chain whose gates leave the range of the factorised in-chunk products.
 size_t chunk_tc_workspace_bytes(int B, int T, int H, kla_gate gate);
+// Per-channel gate (fp32 [B, T, H, 128]): zeroes marks[B*H], then marks every (sequence, head)
+// chain with a 64-token chunk whose gates, for some key channel, multiply to less than ~e^-78 over
+// tokens 0-31 or 32-63 (the range of the in-chunk products factorised around token 31).
+cudaError_t launch_gate_range(const float *alpha, int B, int T, int H, unsigned *marks, cudaStream_t stream);
 // Start states of the segments of every chain: S_start[s+1] = M_s S_start[s] + Z_s.
 cudaError_t launch_seg_combine(const float *Z, const float *M, float *Sst, int chains, int nseg,
                                cudaStream_t stream);
 // backward pass (checkpoints every 8 tokens plus the residuals in the workspace).
 size_t bwd_workspace_bytes(int B, int T, int H, int d_k, int d_v);
 cudaError_t launch_bwd(const BwdArgs &a);
+// The token-sequential fp32 backward (kla_bwd.cu) on every chain, or only on the chains with a
+// nonzero mark in only[B*H]; its workspace is bwd_seq_workspace_bytes.
+size_t bwd_seq_workspace_bytes(int B, int T, int H, int d_k, int d_v);
+cudaError_t launch_bwd_seq(const BwdArgs &a, const unsigned *only);
 // fused single-token decode step.
 cudaError_t launch_decode(const DecodeArgs &a);
 // Token-by-token recurrence with the state tile in registers: short sequences (multi-token

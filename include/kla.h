@@ -257,11 +257,15 @@ kla_status kla_decode_step_ex(const void *q, const void *k, const void *v,
  *            kla_chunk_bwd_workspace_size_ex(...) bytes when q, k, v and dO are 16-byte aligned
  * Outputs must not overlap each other or any input. T = 0 writes dS0 = dS_T (or zeros) only.
  * Supported sizes: d_k, d_v in {16, 32, 64, 128}. Two paths:
- *   - bf16, scalar gate, d_k = d_v = 128, T > 16, 16-byte aligned q, k, v, dO: chunkwise (64-token
+ *   - bf16, d_k = d_v = 128, T > 16, 16-byte aligned q, k, v, dO, either gate: chunkwise (64-token
  *     chunks) on the tensor cores, bf16 operands with fp32 accumulation and fp32 carried states
  *     (relative L2 error ~3e-3 against fp64); the chunk-state carries of long sequences with few
  *     (sequence, head) chains run as a sequence-parallel scan; alpha must be > 0 (dalpha is formed
- *     from dL/dlog alpha);
+ *     from dL/dlog alpha). With the per-channel gate the in-chunk decays are factorised around
+ *     the 32nd token of each chunk, as in kla_chunk_fwd: the call first marks, in the workspace,
+ *     the (sequence, head) chains with a chunk near or outside that range, the chunkwise kernels
+ *     skip them and the same call runs them on the token-by-token path below, so every alpha in
+ *     (0, 1] gives valid gradients;
  *   - every other call: token by token in fp32, one CTA per (sequence, head), so the time grows
  *     with T and not with B * H.
  */
@@ -278,9 +282,12 @@ size_t kla_chunk_bwd_workspace_size(int B, int T, int H, int d_k, int d_v);
 
 /*
  * Bytes of device scratch kla_chunk_bwd needs for these sizes, dtype and gate when q, k, v and dO
- * are 16-byte aligned: the chunkwise path's records (~129 KB per 64-token chunk of every chain)
- * when it applies, else the token-sequential path's. Like kla_chunk_fwd_workspace_size, it may
- * query the current device's SM count (the segment plan of long sequences).
+ * are 16-byte aligned: with the scalar gate the chunkwise path's records (~129 KB per 64-token
+ * chunk of every chain) when it applies; with the per-channel gate on the chunkwise path, 4 bytes
+ * per chain for the range marks (256-byte aligned) and room for the larger of its records (~161 KB
+ * per chunk) and the token-sequential path's checkpoints (which rerun the marked chains); else
+ * the token-sequential path's. Like kla_chunk_fwd_workspace_size, it may query the current
+ * device's SM count (the segment plan of long sequences).
  */
 size_t kla_chunk_bwd_workspace_size_ex(int B, int T, int H, int d_k, int d_v, kla_dtype dtype, kla_gate gate);
 

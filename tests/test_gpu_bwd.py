@@ -4,9 +4,10 @@ relative L2 over the whole tensor, and the oracle receives the same stored (fp32
 inputs.
 
 Two paths, two bars:
-  * bf16 inputs with a scalar gate and d_k = d_v = 128 run the chunkwise tensor-core backward,
-    whose products take bf16 operands with fp32 accumulation and fp32 carried states, like the
-    forward's tensor-core path; they are held to the bf16 bar of the forward, 1e-2;
+  * bf16 inputs with d_k = d_v = 128 and more than 16 tokens run the chunkwise tensor-core
+    backward (scalar or per-channel gate), whose products take bf16 operands with fp32
+    accumulation and fp32 carried states, like the forward's tensor-core path; they are held to
+    the bf16 bar of the forward, 1e-2;
   * every other shape runs the token-by-token fp32 backward: 1e-5 for fp32 inputs, 1e-4 for bf16
     inputs (longer sums of larger terms)."""
 import os
@@ -25,7 +26,7 @@ TOL_CHUNK = 1e-2
 
 
 def tol(wl):
-    chunked = wl.dtype == "bf16" and wl.gate == "scalar" and wl.d_k == 128 and wl.d_v == 128 and wl.T > 16
+    chunked = wl.dtype == "bf16" and wl.d_k == 128 and wl.d_v == 128 and wl.T > 16
     return TOL_CHUNK if chunked else TOL[wl.dtype]
 NAMES = ("dq", "dk", "dv", "dalpha", "deta", "dS0")
 
@@ -101,6 +102,12 @@ CASES = [
     ("gdn4k", dict(B=2, T=257, H=1, s0_sigma=0.05, key_norm="l2"), dict(beta_mode="raw", q_scale=0.5), True),
     ("gdn4k", dict(B=1, T=200, H=2, s0_sigma=0.02), dict(q_scale=128 ** -0.5), True),
     ("long131k", dict(T=320, H=2), {}, True),
+    # chunkwise per-channel gate: shortest chunked length, ragged tails over several chunks, raw
+    # step, query scale, initial state and dL/dS_T
+    ("kda8k", dict(B=1, T=17, H=2), {}, True),
+    ("kda8k", dict(B=2, T=200, H=2, s0_sigma=0.05), {}, True),
+    ("kda8k", dict(B=1, T=257, H=2, s0_sigma=0.05, key_norm="l2"), dict(beta_mode="raw", q_scale=0.5), True),
+    ("kda8k", dict(B=1, T=128, H=3), dict(q_scale=128 ** -0.5), False),
 ]
 
 
@@ -151,8 +158,8 @@ def run_oracle_whole(inp, dO, dST, **mode):
 
 @pytest.mark.parametrize("name", ["gdn4k", "kda8k"])
 def test_full_config_whole_tensor(name):
-    """The backward of the prefill workloads at full size (gdn4k on the chunkwise path, kda8k on
-    the token-sequential one), every gradient compared over the whole tensor."""
+    """The backward of the prefill workloads at full size on the chunkwise path (scalar gate on
+    gdn4k, per-channel gate on kda8k), every gradient compared over the whole tensor."""
     inp = synth.make_prefill(name, seed=1)
     dO, dST = _grad_inputs(inp, seed=2, with_dst=True)
     got = run_gpu(inp, dO, dST)
@@ -228,4 +235,76 @@ def test_chunked_backward_zero_keys_and_unit_gates(mode):
     dO, dST = _grad_inputs(inp, seed=78, with_dst=True)
     got = run_gpu(inp, dO, dST, **mode)
     ref = run_oracle(inp, dO, dST, **mode)
+    compare(pick(got, [(0, 0), (0, 1)]), ref, TOL_CHUNK)
+
+
+@pytest.mark.parametrize("mode", [{}, dict(beta_mode="raw")])
+def test_channel_chunked_backward_zero_keys_and_unit_gates(mode):
+    """Per-channel gate, degenerate tokens inside chunks: zero keys with eps = 0 (beta = 0, no
+    gradient through the step size), gates of exactly 1 on every channel, and gates of 1 on half
+    of the channels only."""
+    import dataclasses
+    norm = dict(key_norm="l2") if mode else {}
+    inp = synth.make_prefill("kda8k", seed=79, B=1, T=150, H=2, s0_sigma=0.05, eps=0.0, **norm)
+    k = inp.k.copy()
+    k[:, [0, 5, 63, 64, 100, 149]] = 0
+    alpha = inp.alpha.copy()
+    alpha[:, 10:40] = 1.0
+    alpha[:, 70:120, :, ::2] = 1.0
+    inp = dataclasses.replace(inp, k=k, alpha=alpha)
+    dO, dST = _grad_inputs(inp, seed=80, with_dst=True)
+    got = run_gpu(inp, dO, dST, **mode)
+    ref = run_oracle(inp, dO, dST, **mode)
+    compare(pick(got, [(0, 0), (0, 1)]), ref, TOL_CHUNK)
+
+
+def test_channel_chunked_backward_strong_decay():
+    """Per-channel gates well below those of the kda8k workload (log alpha = -softplus(N(-2, 1.5)),
+    inside the factorised range): the decay-crossing terms of d alpha cancel in pairs, and the
+    kernel keeps them cancelling under bf16 rounding."""
+    import dataclasses
+    inp = synth.make_prefill("kda8k", seed=81, B=1, T=300, H=2, s0_sigma=0.05)
+    rng = np.random.default_rng(82)
+    x = rng.normal(-2.0, 1.5, inp.alpha.shape)
+    alpha = np.exp(-np.logaddexp(0.0, x)).astype(np.float32)
+    alpha = np.maximum(alpha, np.float32(0.12))   # half-chunk products stay above e^-78
+    inp = dataclasses.replace(inp, alpha=alpha)
+    dO, dST = _grad_inputs(inp, seed=83, with_dst=True)
+    got = run_gpu(inp, dO, dST)
+    ref = run_oracle(inp, dO, dST)
+    compare(pick(got, [(0, 0), (0, 1)]), ref, TOL_CHUNK)
+
+
+def test_channel_chunked_backward_is_deterministic():
+    inp = synth.make_prefill("kda8k", seed=84, B=2, T=150, H=2, s0_sigma=0.05)
+    dO, dST = _grad_inputs(inp, seed=85, with_dst=True)
+    a = run_gpu(inp, dO, dST)
+    b = run_gpu(inp, dO, dST)
+    for n in NAMES:
+        assert np.array_equal(a[n], b[n]), n
+
+
+def test_channel_gate_out_of_range_chain_takes_the_exact_path():
+    """A chain whose per-channel gates multiply below ~e^-78 over half a chunk is outside the range
+    of the factorised in-chunk products: the chunkwise kernels skip it and the token-sequential
+    fp32 backward reruns it in the same call, so it meets that path's 1e-4 bar while the other
+    chains stay chunkwise."""
+    inp = synth.make_prefill("kda8k", seed=86, B=2, T=200, H=2, s0_sigma=0.05)
+    inp.alpha[1, 70:110, 0, 9] = 1e-3
+    dO, dST = _grad_inputs(inp, seed=87, with_dst=True)
+    got = run_gpu(inp, dO, dST)
+    chains = [(0, 0), (0, 1), (1, 0), (1, 1)]
+    ref = run_oracle(inp, dO, dST, chains=chains)
+    compare(pick(got, chains), ref, TOL_CHUNK)
+    compare(pick(got, [(1, 0)]), run_oracle(inp, dO, dST, chains=[(1, 0)]), TOL["bf16"])
+
+
+@pytest.mark.parametrize("T", [4059, 16384 - 5])
+def test_channel_long_chain_segmented_carries(T):
+    """Per-channel gate with few chains and many chunks: both carries split into segments run in
+    parallel, reading the per-channel records (decayed keys, scaled queries, end decays)."""
+    inp = synth.make_prefill("kda8k", seed=T + 3, B=1, T=T, H=2, s0_sigma=0.05)
+    dO, dST = _grad_inputs(inp, seed=T + 4, with_dst=True)
+    got = run_gpu(inp, dO, dST)
+    ref = run_oracle(inp, dO, dST)
     compare(pick(got, [(0, 0), (0, 1)]), ref, TOL_CHUNK)
