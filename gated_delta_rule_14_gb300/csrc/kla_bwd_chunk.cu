@@ -388,7 +388,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(ScanParams 
                 gemm_m<1, 4, 4, true, true>(acc2, sptr(stage(buf, SC_A)), kPs, m0, 0, sptr(stage(buf, SC_DO)), kP, n0,
                                             0, lane);
         }
-        bf16 *Mout = (kRev ? p.ws.UdE : p.ws.E) + n * kC * kD;
+        bf16 *Mout = (kRev ? p.ws.dE : p.ws.E) + n * kC * kD;
         const bf16 *sU = stage(buf, SC_UQ);
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
@@ -509,7 +509,7 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_kernel(GradParams p)
     load_tok(sV, p.v + tok0 * kD, rs, L, tid, kGradThreads);
     load_tok(sDO, p.dO + tok0 * kD, rs, L, tid, kGradThreads);
     load_dense<kD>(sE, p.ws.E + n * kC * kD, kC, tid, kGradThreads);
-    load_dense<kD>(sDE, p.ws.UdE + n * kC * kD, kC, tid, kGradThreads);
+    load_dense<kD>(sDE, p.ws.dE + n * kC * kD, kC, tid, kGradThreads);
     load_dense<kD>(sS, p.ws.S + n * kD * kD, kD, tid, kGradThreads);
     load_dense<kD>(sDS, p.ws.dS + n * kD * kD, kD, tid, kGradThreads);
     load_dense<kC>(sT, p.ws.Tm + n * kC * kC, kC, tid, kGradThreads);
@@ -909,15 +909,17 @@ bool bwd_chunk_supports(const BwdArgs &a) {
     const bool ch = a.gate == KLA_GATE_CHANNEL;
     return a.dtype == KLA_DTYPE_BF16 && (a.gate == KLA_GATE_SCALAR || ch) && a.d_k == kD && a.d_v == kD &&
            a.T > kShortSeqMaxT && static_cast<long long>(a.B) * a.H <= 65535 && al16(a.q) && al16(a.k) &&
-           al16(a.v) && al16(a.dO) && al16(a.workspace) &&
+           al16(a.v) && al16(a.dO) && (!ch || al16(a.alpha)) && al16(a.workspace) &&
            a.workspace_bytes >= bwd_chunk_workspace_bytes(a.B, a.T, a.H, a.gate);
 }
 
-// When the CTAs of pass 1a and pass 1b of a segmented carry fit on the SMs together (the plan
-// counts them as one wave), pass 1b runs on a second stream of the library's, between a fork and
-// a join recorded on the caller's stream; with two waves both stay in order on the caller's
-// stream. One stream and two events per device; the mutex keeps a call's fork and join records
-// from interleaving with another thread's.
+// Two launches that fit on the SMs together run side by side: the second on a stream of the
+// library's, between a fork and a join recorded on the caller's stream. That is pass 1a and pass
+// 1b of a segmented carry (the plan counts them as one wave), and the forward and reverse carries
+// themselves when neither is segmented and their CTAs fit in one wave (the reverse recursion reads
+// neither S nor E, only the prep's records). With two waves everything stays in order on the
+// caller's stream. One stream and two events per device; the mutex keeps a call's fork and join
+// records from interleaving with another thread's.
 namespace {
 struct CarryAux {
     cudaStream_t s = nullptr;
@@ -926,6 +928,19 @@ struct CarryAux {
 constexpr int kMaxCarryDevices = 64;
 CarryAux g_carry_aux[kMaxCarryDevices];
 std::mutex g_carry_aux_mutex[kMaxCarryDevices];
+cudaError_t carry_aux(int dev, CarryAux **out) {   // the caller holds g_carry_aux_mutex[dev]
+    if (dev < 0 || dev >= kMaxCarryDevices) return cudaErrorInvalidDevice;
+    CarryAux &ax = g_carry_aux[dev];
+    cudaError_t e;
+    if (!ax.s) {
+        if ((e = cudaStreamCreateWithFlags(&ax.s, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&ax.fork, cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&ax.join, cudaEventDisableTiming)) != cudaSuccess)
+            return e;
+    }
+    *out = &ax;
+    return cudaSuccess;
+}
 }  // namespace
 
 cudaError_t launch_bwd_chunk(const BwdArgs &a) {
@@ -959,7 +974,31 @@ cudaError_t launch_bwd_chunk(const BwdArgs &a) {
     }
     const CarryPlan pl = carry_plan(chains, nc);
     const size_t part = static_cast<size_t>(chains) * pl.nseg * kD * kD;
-    for (int rev = 0; rev < 2; ++rev) {
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
+    const bool side_by_side = pl.nseg <= 1 && 2L * chains <= sms && ws.dE != ws.UdE;
+    if (side_by_side) {   // both carries in one wave
+        ScanParams sf{q, k, dO, a.S0, nullptr, a.q_scale, a.B, a.T, a.H, nc, ws,
+                      pl.seg_len, 0, 1, pl.nseg, kX0Chain, 1, 1, nullptr, nullptr, marks};
+        ScanParams sr = sf;
+        sr.X0 = a.dS_T;
+        sr.X_end = a.dS0;
+        std::lock_guard<std::mutex> lock(g_carry_aux_mutex[dev]);
+        CarryAux *ax = nullptr;
+        if ((e = carry_aux(dev, &ax)) != cudaSuccess || (e = cudaEventRecord(ax->fork, a.stream)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(ax->s, ax->fork, 0)) != cudaSuccess)
+            return e;
+        scan_r<<<chains, kScanThreads, SC_BYTES, a.stream>>>(sr);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        scan_f<<<chains, kScanThreads, SC_BYTES, ax->s>>>(sf);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = cudaEventRecord(ax->join, ax->s)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(a.stream, ax->join, 0)) != cudaSuccess)
+            return e;
+    }
+    for (int rev = 0; rev < 2 && !side_by_side; ++rev) {
         auto kern = rev ? scan_r : scan_f;
         ScanParams sp{q, k, dO, rev ? a.dS_T : a.S0, rev ? a.dS0 : nullptr, a.q_scale, a.B, a.T, a.H, nc, ws,
                       pl.seg_len, 0, 1, pl.nseg, kX0Chain, 1, 1, nullptr, nullptr, marks};
@@ -986,10 +1025,6 @@ cudaError_t launch_bwd_chunk(const BwdArgs &a) {
         p2.records = 0;
         p2.Xseg = M;
         p2.X_end = nullptr;
-        int dev = 0, sms = 0;
-        if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
-            (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-            return e;
         const bool one_wave = static_cast<long>(chains) * (p1.seg_count + p2.seg_count) <= sms;
         if (pl.nseg <= 2 || !one_wave) {
             kern<<<chains * p1.seg_count, kScanThreads, SC_BYTES, a.stream>>>(p1);
@@ -999,24 +1034,17 @@ cudaError_t launch_bwd_chunk(const BwdArgs &a) {
                 if ((e = cudaGetLastError()) != cudaSuccess) return e;
             }
         } else {
-            if (dev < 0 || dev >= kMaxCarryDevices) return cudaErrorInvalidDevice;
             std::lock_guard<std::mutex> lock(g_carry_aux_mutex[dev]);
-            CarryAux &ax = g_carry_aux[dev];
-            if (!ax.s) {
-                if ((e = cudaStreamCreateWithFlags(&ax.s, cudaStreamNonBlocking)) != cudaSuccess ||
-                    (e = cudaEventCreateWithFlags(&ax.fork, cudaEventDisableTiming)) != cudaSuccess ||
-                    (e = cudaEventCreateWithFlags(&ax.join, cudaEventDisableTiming)) != cudaSuccess)
-                    return e;
-            }
-            if ((e = cudaEventRecord(ax.fork, a.stream)) != cudaSuccess ||
-                (e = cudaStreamWaitEvent(ax.s, ax.fork, 0)) != cudaSuccess)
+            CarryAux *ax = nullptr;
+            if ((e = carry_aux(dev, &ax)) != cudaSuccess || (e = cudaEventRecord(ax->fork, a.stream)) != cudaSuccess ||
+                (e = cudaStreamWaitEvent(ax->s, ax->fork, 0)) != cudaSuccess)
                 return e;
             kern<<<chains * p1.seg_count, kScanThreads, SC_BYTES, a.stream>>>(p1);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
-            kern<<<chains * p2.seg_count, kScanThreads, SC_BYTES, ax.s>>>(p2);
+            kern<<<chains * p2.seg_count, kScanThreads, SC_BYTES, ax->s>>>(p2);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
-            if ((e = cudaEventRecord(ax.join, ax.s)) != cudaSuccess ||
-                (e = cudaStreamWaitEvent(a.stream, ax.join, 0)) != cudaSuccess)
+            if ((e = cudaEventRecord(ax->join, ax->s)) != cudaSuccess ||
+                (e = cudaStreamWaitEvent(a.stream, ax->join, 0)) != cudaSuccess)
                 return e;
         }
         // pass 2: true start states of segments 1..n-1; pass 3: rerun them with records

@@ -28,21 +28,23 @@ constexpr size_t kCgFloats = 3 * kC;    // G (scalar gate only), beta, den = ||k
 struct Ws {
     float *cg;        // [N][3][64]
     bf16 *W;          // [N][64][128]
-    bf16 *UdE;        // [N][64][128]: U (prep -> forward carry), then dE (reverse carry -> gradients)
+    bf16 *UdE;        // [N][64][128]: U (prep -> forward carry), then dE with the scalar gate
+    bf16 *dE;         // [N][64][128]: dE (reverse carry -> gradients): UdE, or its own record with
+                      // the per-channel gate (so that the two carries may run at the same time)
     bf16 *A;          // [N][64][64]  lower(ratio . QK^T), unscaled by s
     bf16 *Tm;         // [N][64][64]  T = (I + R)^{-1}
     bf16 *S;          // [N][128][128] state entering the chunk
     bf16 *E;          // [N][64][128]
     bf16 *dS;         // [N][128][128] dL/d(state leaving the chunk)
     // per-key-channel gate only (NULL otherwise): the decayed key and query tiles the two carries
-    // read in place of k and q, and the chunk's end decay per key channel
+    // read in place of k and q, and the chunk's end decay per key channel (dE above follows them)
     bf16 *Ke;         // [N][64][128] K e^{G_end - G}
     bf16 *Qg;         // [N][64][128] s Q e^{G}
     float *gend;      // [N][128]     e^{G_end}
     float *seg;       // long chains split into segments: Z | M | start states, each [chains][nseg][128][128]
 };
 inline size_t ws_bytes_per_chunk(bool ch) {
-    return kCgFloats * 4 + 2 * (3 * kC * kD + 2 * kC * kC + 2 * kD * kD) + (ch ? 2 * (2 * kC * kD) + 4 * kD : 0);
+    return kCgFloats * 4 + 2 * (3 * kC * kD + 2 * kC * kC + 2 * kD * kD) + (ch ? 2 * (3 * kC * kD) + 4 * kD : 0);
 }
 inline Ws carve(void *base, size_t N, bool ch) {
     char *p = static_cast<char *>(base);
@@ -57,7 +59,9 @@ inline Ws carve(void *base, size_t N, bool ch) {
     w.dS = reinterpret_cast<bf16 *>(p);              p += N * kD * kD * 2;
     w.Ke = w.Qg = nullptr;
     w.gend = nullptr;
+    w.dE = w.UdE;
     if (ch) {
+        w.dE = reinterpret_cast<bf16 *>(p);          p += N * kC * kD * 2;
         w.Ke = reinterpret_cast<bf16 *>(p);          p += N * kC * kD * 2;
         w.Qg = reinterpret_cast<bf16 *>(p);          p += N * kC * kD * 2;
         w.gend = reinterpret_cast<float *>(p);       p += N * kD * 4;

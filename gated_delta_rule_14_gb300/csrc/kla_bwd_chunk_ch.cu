@@ -41,19 +41,37 @@ namespace kla {
 namespace bwdc {
 namespace {
 
-// Log-gate prefix over the 32 tokens [32 hf, 32 hf + 32) of the chunk for key channel c; tokens at
-// or past L count as alpha = 1. lg receives the 32 clamped log-gates; returns their sum.
-__device__ __forceinline__ float gate_logs(const float *alpha, size_t tok0, int H, int L, int c, int hf,
-                                           float (&lg)[32]) {
-    float sum = 0.f;
+// Log-gates of key channels 2 cp and 2 cp + 1 over the 16 tokens [16 qt, 16 qt + 16) of the chunk
+// (tokens at or past L count as alpha = 1), clamped at kMinLogGate; their sums go to
+// squart[qt][2 cp], squart[qt][2 cp + 1] (fp32 [4][128]).
+__device__ __forceinline__ void gate_logs(const float *alpha, size_t tok0, int H, int L, int cp, int qt,
+                                          float (&lg)[2][16], float *squart) {
+    float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-    for (int u = 0; u < 32; ++u) {
-        const int t = 32 * hf + u;
-        const float a = t < L ? alpha[(tok0 + static_cast<size_t>(t) * H) * kD + c] : 1.f;
-        lg[u] = fmaxf(logf(a), kMinLogGate);
-        sum += lg[u];
+    for (int u = 0; u < 16; ++u) {
+        const int t = 16 * qt + u;
+        float2 a = make_float2(1.f, 1.f);
+        if (t < L) a = *reinterpret_cast<const float2 *>(alpha + (tok0 + static_cast<size_t>(t) * H) * kD + 2 * cp);
+        lg[0][u] = fmaxf(logf(a.x), kMinLogGate);
+        lg[1][u] = fmaxf(logf(a.y), kMinLogGate);
+        s0 += lg[0][u];
+        s1 += lg[1][u];
     }
-    return sum;
+    *reinterpret_cast<float2 *>(squart + qt * kD + 2 * cp) = make_float2(s0, s1);
+}
+// After every quarter sum is in squart: the inclusive prefix G at the start of quarter qt (its
+// offset), the reference G_r (tokens 0-31) and G_end, for channel c. Every kernel forms them in this
+// order of summation.
+struct GateRef {
+    float off, Gr, Gend;
+};
+__device__ __forceinline__ GateRef gate_ref(const float *squart, int c, int qt) {
+    const float s0 = squart[c], s1 = squart[kD + c], s2 = squart[2 * kD + c], s3 = squart[3 * kD + c];
+    GateRef r;
+    r.Gr = s0 + s1;
+    r.Gend = (r.Gr + s2) + s3;
+    r.off = qt == 0 ? 0.f : qt == 1 ? s0 : qt == 2 ? r.Gr : r.Gr + s2;
+    return r;
 }
 
 // ============================================================== prep: per-chunk operands
@@ -66,8 +84,8 @@ constexpr int PC_R = PC_KM + kTileTok;                // fp32 [64][kPR]: R, then
 constexpr int PC_TB = PC_R + kC * kPR * 4;            // bf16 T diag(beta)
 constexpr int PC_A = PC_TB + kTileSq;                 // bf16 A, then T, staging
 constexpr int PC_X = PC_A + kTileSq;                  // fp32 [32][kPX] merge scratch
-constexpr int PC_VEC = PC_X + 32 * kPX * 4;           // eta, beta [64]; half sums [2][128]; e^{G_r} [128]
-constexpr int PC_BYTES = PC_VEC + (2 * kC + 3 * kD) * 4;
+constexpr int PC_VEC = PC_X + 32 * kPX * 4;           // eta, beta [64]; quarter sums [4][128]; e^{G_r} [128]
+constexpr int PC_BYTES = PC_VEC + (2 * kC + 5 * kD) * 4;
 static_assert(2 * (PC_BYTES + 1024) <= 233472, "two prep CTAs per SM");
 
 __global__ void __launch_bounds__(kPrepThreads, 2) bwd_prep_ch_kernel(ChBwd p) {
@@ -77,7 +95,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) bwd_prep_ch_kernel(ChBwd p) {
     float(*sR)[kPR] = reinterpret_cast<float(*)[kPR]>(smem + PC_R);
     bf16 *sTB = reinterpret_cast<bf16 *>(smem + PC_TB), *sA = reinterpret_cast<bf16 *>(smem + PC_A);
     float *sX = reinterpret_cast<float *>(smem + PC_X);
-    float *seta = reinterpret_cast<float *>(smem + PC_VEC), *sb = seta + kC, *shalf = sb + kC, *segr = shalf + 2 * kD;
+    float *seta = reinterpret_cast<float *>(smem + PC_VEC), *sb = seta + kC, *squart = sb + kC, *segr = squart + 4 * kD;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int c = blockIdx.x, bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
@@ -91,10 +109,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2) bwd_prep_ch_kernel(ChBwd p) {
     load_tok(sQ, p.q + tok0 * kD, rs, L, tid, kPrepThreads);
     load_tok(sV, p.v + tok0 * kD, rs, L, tid, kPrepThreads);
     cp_commit();
-    // log-gates while the tiles land: thread (channel ch, half hf)
-    const int ch = tid & (kD - 1), hf = tid >> 7;
-    float lg[32];
-    shalf[hf * kD + ch] = gate_logs(p.alpha, tok0, p.H, L, ch, hf, lg);
+    // log-gates while the tiles land: thread (channel pair cp, quarter qt of the chunk)
+    const int cp = tid & 63, qt = tid >> 6;
+    float lg[2][16];
+    gate_logs(p.alpha, tok0, p.H, L, cp, qt, lg, squart);
     if (tid < kC) seta[tid] = tid < L ? p.eta[tok0 + static_cast<size_t>(tid) * p.H] : 0.f;
     cp_wait<0>();
     __syncthreads();
@@ -116,26 +134,31 @@ __global__ void __launch_bounds__(kPrepThreads, 2) bwd_prep_ch_kernel(ChBwd p) {
             cg[2 * kC + i] = n2 + p.eps;
         }
     }
-    __syncthreads();   // every read of the raw K is done; the half sums are visible
+    __syncthreads();   // every read of the raw K is done; the quarter sums are visible
 
     // factor tiles, in place: K_r, Q_r (over K, Q) and K_m; the records K_e, s Q_g and e^{G_end}
     {
-        const float Gr = shalf[ch], Gend = Gr + shalf[kD + ch];
-        float G = hf ? Gr : 0.f;
-        bf16 *ke = p.ws.Ke + n * kC * kD, *qg = p.ws.Qg + n * kC * kD;
-        if (hf == 0) segr[ch] = __expf(Gr);
-        else p.ws.gend[n * kD + ch] = __expf(Gend);
+        const GateRef g0 = gate_ref(squart, 2 * cp, qt), g1 = gate_ref(squart, 2 * cp + 1, qt);
+        float G0 = g0.off, G1 = g1.off;
+        uint32_t *ke = reinterpret_cast<uint32_t *>(p.ws.Ke + n * kC * kD) + cp;
+        uint32_t *qg = reinterpret_cast<uint32_t *>(p.ws.Qg + n * kC * kD) + cp;
+        if (qt == 0) *reinterpret_cast<float2 *>(segr + 2 * cp) = make_float2(__expf(g0.Gr), __expf(g1.Gr));
+        if (qt == 3)
+            *reinterpret_cast<float2 *>(p.ws.gend + n * kD + 2 * cp) = make_float2(__expf(g0.Gend), __expf(g1.Gend));
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-            const int i = 32 * hf + u;
-            G += lg[u];
-            const float fr = __expf(G - Gr), fm = __expf(Gr - G), eg = __expf(G), ee = __expf(Gend - G);
-            const float kv = __bfloat162float(sK[i * kP + ch]), qv = __bfloat162float(sQ[i * kP + ch]);
-            sK[i * kP + ch] = __float2bfloat16_rn(kv * fr);
-            sQ[i * kP + ch] = __float2bfloat16_rn(qv * fr);
-            sKM[i * kP + ch] = __float2bfloat16_rn(kv * fm);
-            ke[i * kD + ch] = __float2bfloat16_rn(kv * ee);
-            qg[i * kD + ch] = __float2bfloat16_rn(p.q_scale * qv * eg);
+        for (int u = 0; u < 16; ++u) {
+            const int i = 16 * qt + u;
+            G0 += lg[0][u];
+            G1 += lg[1][u];
+            const float fr0 = __expf(G0 - g0.Gr), fm0 = __expf(g0.Gr - G0), eg0 = __expf(G0), ee0 = __expf(g0.Gend - G0);
+            const float fr1 = __expf(G1 - g1.Gr), fm1 = __expf(g1.Gr - G1), eg1 = __expf(G1), ee1 = __expf(g1.Gend - G1);
+            uint32_t *pk = reinterpret_cast<uint32_t *>(sK + i * kP) + cp, *pq = reinterpret_cast<uint32_t *>(sQ + i * kP) + cp;
+            const float2 kv = unpack2(*pk), qv = unpack2(*pq);
+            *pk = pack2(kv.x * fr0, kv.y * fr1);
+            *pq = pack2(qv.x * fr0, qv.y * fr1);
+            reinterpret_cast<uint32_t *>(sKM + i * kP)[cp] = pack2(kv.x * fm0, kv.y * fm1);
+            ke[i * (kD / 2)] = pack2(kv.x * ee0, kv.y * ee1);
+            qg[i * (kD / 2)] = pack2(p.q_scale * qv.x * eg0, p.q_scale * qv.y * eg1);
         }
     }
     __syncthreads();
@@ -225,17 +248,17 @@ __device__ __forceinline__ void gemm_k2(float (&acc)[MT][NT][4], uint32_t ta, in
 }
 
 // ============================================================== gradients of a chunk
-// One CTA of 8 warps per chunk. Warp w owns the 32 x 32 block (rows 32 (w & 1), columns
-// 32 (w >> 1)) of every 64 x 128 quantity and keeps dk, dq and dG for it in registers, so every
-// elementwise step is local; 64 x 64 products give a warp 16 x 32 (rows 16 (w & 3), columns
-// 32 (w >> 2)). Phases (block barriers between them):
+// One CTA of 16 warps per chunk. Warp w owns the 16 x 32 block (rows 16 (w & 3), columns
+// 32 (w >> 2)) of every 64 x 128 quantity and keeps dk, dq and dG for it in registers, so every
+// elementwise step is local; 64 x 64 products give a warp 16 x 16 (rows
+// 16 (w & 3), columns 16 (w >> 2)). Phases (block barriers between them):
 //   1  <S, dS'> per channel; dKe = E dS'^T; dQg = s dO S^T; dW = -dE S^T; dA = s lower(dO E^T)
 //   1b dW and dA stored; the bf16 factor tiles K_g, K_r, K_m, Q_r built over S, dS' and E
-//   2  dXK = T^T dW; dXV = T^T dE -> dv; dT
-//   3  Y = T^T dT; P = K_r K_m^T, dR and dP = beta dR; dQr = dA K_m -> dq
+//   2  dQr = dA K_m -> dq; dXK = T^T dW; dXV = T^T dE -> dv; dT
+//   3  Y = T^T dT; P = K_r K_m^T, dR and dP = beta dR
 //   4  dKr = dP K_m; dKm = dP^T K_r + dA^T Q_r; then per token dbeta, deta, the k coefficient,
 //      dk, and the reverse prefix of dG per channel -> dalpha.
-constexpr int kGradThreads = 256;
+constexpr int kGradThreads = 512;
 constexpr int kPG = kD + 8;                                   // pitch (floats) of the fp32 64 x 128 tiles
 constexpr int GC_S = 0;                                       // S; then dW | K_g; then dG (fp32)
 constexpr int GC_DS = GC_S + kTileSt;                         // dS'; then K_r | K_m
@@ -251,11 +274,11 @@ constexpr int GC_CG = GC_G + kC * kPG * 4;                    // cg record: (G),
 constexpr int GC_GR = GC_CG + static_cast<int>(kCgFloats) * 4;   // fp32 [128] G_r
 constexpr int GC_GE = GC_GR + kD * 4;                         // fp32 [128] G_end
 constexpr int GC_DGAM = GC_GE + kD * 4;                       // fp32 [128] <S, dS'> per channel
-constexpr int GC_COLK = GC_DGAM + kD * 4;                     // fp32 [2][128] column sums of dKe K_e
-constexpr int GC_RROW = GC_COLK + 2 * kD * 4;                 // fp32 [3][4][64] row partials
+constexpr int GC_COLK = GC_DGAM + kD * 4;                     // fp32 [4][128] column sums of dKe K_e
+constexpr int GC_RROW = GC_COLK + 4 * kD * 4;                 // fp32 [3][4][64] row partials
 constexpr int GC_KC = GC_RROW + 3 * 4 * kC * 4;               // fp32 [64] k coefficient
-constexpr int GC_HALF = GC_KC + kC * 4;                       // fp32 [2][128] half sums of the gates / of dG
-constexpr int GC_BYTES = GC_HALF + 2 * kD * 4;
+constexpr int GC_QS = GC_KC + kC * 4;                         // fp32 [4][128] partial sums of the gates / of dG
+constexpr int GC_BYTES = GC_QS + 4 * kD * 4;
 static_assert(kC * kPG * 4 == kTileSt, "dG tile over S");
 static_assert(GC_BYTES <= 232448, "gradient kernel shared memory");
 enum { RB_XK = 0, RB_XV, RB_R };   // row partials: K_g . dXK, V . dXV, dR . P
@@ -271,7 +294,7 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_ch_kernel(ChBwd p) {
     const float *cg = reinterpret_cast<const float *>(smem + GC_CG);
     float *sGr = reinterpret_cast<float *>(smem + GC_GR), *sGe = reinterpret_cast<float *>(smem + GC_GE),
           *sDGam = reinterpret_cast<float *>(smem + GC_DGAM), *sColK = reinterpret_cast<float *>(smem + GC_COLK),
-          *kcoef = reinterpret_cast<float *>(smem + GC_KC), *shalf = reinterpret_cast<float *>(smem + GC_HALF);
+          *kcoef = reinterpret_cast<float *>(smem + GC_KC), *squart = reinterpret_cast<float *>(smem + GC_QS);
     float(*rrow)[4][kC] = reinterpret_cast<float(*)[4][kC]>(smem + GC_RROW);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, q4 = lane & 3;
@@ -288,52 +311,59 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_ch_kernel(ChBwd p) {
     load_tok(sV, p.v + tok0 * kD, rs, L, tid, kGradThreads);
     load_tok(sDO, p.dO + tok0 * kD, rs, L, tid, kGradThreads);
     load_dense<kD>(sE, p.ws.E + n * kC * kD, kC, tid, kGradThreads);
-    load_dense<kD>(sDE, p.ws.UdE + n * kC * kD, kC, tid, kGradThreads);
+    load_dense<kD>(sDE, p.ws.dE + n * kC * kD, kC, tid, kGradThreads);
     load_dense<kD>(sS, p.ws.S + n * kD * kD, kD, tid, kGradThreads);
     load_dense<kD>(sDS, p.ws.dS + n * kD * kD, kD, tid, kGradThreads);
     load_dense<kC>(sT, p.ws.Tm + n * kC * kC, kC, tid, kGradThreads);
     if (tid < static_cast<int>(kCgFloats) / 4)
         cp16(smem + GC_CG + 16 * tid, p.ws.cg + n * kCgFloats + 4 * tid, true);
     cp_commit();
-    // G per (token, channel) while the tiles land, in the prep kernel's order of summation
+    // G per (token, channel) while the tiles land, in the prep kernel's order of summation:
+    // threads 0-255 as (channel pair, quarter of the chunk)
     {
-        const int ch = tid & (kD - 1), hf = tid >> 7;
-        float lg[32];
-        shalf[hf * kD + ch] = gate_logs(p.alpha, tok0, p.H, L, ch, hf, lg);
+        const int cp = tid & 63, qt = (tid >> 6) & 3;
+        float lg[2][16];
+        if (tid < 4 * 64) gate_logs(p.alpha, tok0, p.H, L, cp, qt, lg, squart);
         __syncthreads();
-        const float Gr = shalf[ch];
-        float G = hf ? Gr : 0.f;
+        if (tid < 4 * 64) {
+            const GateRef g0 = gate_ref(squart, 2 * cp, qt), g1 = gate_ref(squart, 2 * cp + 1, qt);
+            float G0 = g0.off, G1 = g1.off;
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-            G += lg[u];
-            sG[(32 * hf + u) * kPG + ch] = G;
+            for (int u = 0; u < 16; ++u) {
+                G0 += lg[0][u];
+                G1 += lg[1][u];
+                *reinterpret_cast<float2 *>(sG + (16 * qt + u) * kPG + 2 * cp) = make_float2(G0, G1);
+            }
+            if (qt == 0) {
+                *reinterpret_cast<float2 *>(sGr + 2 * cp) = make_float2(g0.Gr, g1.Gr);
+                *reinterpret_cast<float2 *>(sGe + 2 * cp) = make_float2(g0.Gend, g1.Gend);
+            }
         }
-        if (hf == 0) sGr[ch] = Gr;
-        else sGe[ch] = G;
     }
     cp_wait<0>();
     __syncthreads();
 
-    const int r1 = 32 * (warp & 1), c1 = 32 * (warp >> 1), cb1 = warp >> 1;   // 64 x 128: 32 x 32 per warp
-    const int r2 = 16 * (warp & 3), c2 = 32 * (warp >> 2), cb2 = warp >> 2;   // 64 x 64: 16 x 32 per warp
-    auto row1 = [&](int mi, int hh) { return r1 + 16 * mi + g + 8 * hh; };
+    const int r1 = 16 * (warp & 3), c1 = 32 * (warp >> 2), cb = warp >> 2;   // 64 x 128: 16 x 32 per warp
+    const int c2 = 16 * (warp >> 2);                                         // 64 x 64: 16 x 16 per warp
+    auto row1 = [&](int hh) { return r1 + g + 8 * hh; };
     auto col1 = [&](int ni) { return c1 + 8 * ni + 2 * q4; };
-    auto row2 = [&](int hh) { return r2 + g + 8 * hh; };
+    auto col2 = [&](int ni) { return c2 + 8 * ni + 2 * q4; };
     auto gpair = [&](int r, int col) { return *reinterpret_cast<const float2 *>(sG + r * kPG + col); };
-    auto put_row = [&](int qi, int cb, int row, float x) {   // sum over the 4 lanes of a row
+    auto put_row = [&](int qi, int row, float x) {   // sum over the 4 lanes of a row, into column block cb
         x += __shfl_xor_sync(0xffffffffu, x, 1);
         x += __shfl_xor_sync(0xffffffffu, x, 2);
         if (q4 == 0) rrow[qi][cb][row] = x;
     };
+    auto dq_row = [&](int r) { return p.dq + (tok0 + static_cast<size_t>(r) * p.H) * kD; };
 
-    float dk[2][4][4], dg[2][4][4], tmp[2][4][4];
-    float da[1][4][4];
+    float dk[1][4][4], dq[1][4][4], dg[1][4][4], tmp[1][4][4];
+    float da[1][2][4];
     // ---- phase 1
-    {   // <S, dS'> per key channel (row of S): two threads per row
-        const int r = tid >> 1, h0 = (tid & 1) * 64;
+    {   // <S, dS'> per key channel (row of S): four threads per row
+        const int r = tid >> 2, h0 = (tid & 3) * 32;
         float sum = 0.f;
 #pragma unroll
-        for (int cc = 0; cc < 64; cc += 8) {
+        for (int cc = 0; cc < 32; cc += 8) {
             const uint4 x = *reinterpret_cast<const uint4 *>(sS + r * kP + h0 + cc);
             const uint4 y = *reinterpret_cast<const uint4 *>(sDS + r * kP + h0 + cc);
             const uint32_t *xw = reinterpret_cast<const uint32_t *>(&x), *yw = reinterpret_cast<const uint32_t *>(&y);
@@ -344,12 +374,12 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_ch_kernel(ChBwd p) {
             }
         }
         sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-        if ((tid & 1) == 0) sDGam[r] = sum;
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        if ((tid & 3) == 0) sDGam[r] = sum;
     }
     // dKe = E dS'^T: dk = dKe e^{G_end - G}, dG = -dKe K_e, column sums of dKe K_e for the last row
     zero(dk[0]);
-    zero(dk[1]);
-    gemm_k2<2, 4, 8, false, false>(dk, sptr(sE), kP, r1, 0, sptr(sDS), kP, c1, 0, lane);
+    gemm_k2<1, 4, 8, false, false>(dk, sptr(sE), kP, r1, 0, sptr(sDS), kP, c1, 0, lane);
     {
         float colk[4][2] = {};
 #pragma unroll
@@ -357,21 +387,18 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_ch_kernel(ChBwd p) {
             const int col = col1(ni);
             const float ge0 = sGe[col], ge1 = sGe[col + 1];
 #pragma unroll
-            for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int r = row1(mi, hh);
-                    const float2 G2 = gpair(r, col), k2 = ld_pair(sK, kP, r, col);
-                    const float e0 = __expf(ge0 - G2.x), e1 = __expf(ge1 - G2.y);
-                    const float x0 = dk[mi][ni][2 * hh] * e0, x1 = dk[mi][ni][2 * hh + 1] * e1;   // dk terms
-                    const float m0 = x0 * k2.x, m1 = x1 * k2.y;                                  // dKe . K_e
-                    dg[mi][ni][2 * hh] = -m0;
-                    dg[mi][ni][2 * hh + 1] = -m1;
-                    colk[ni][0] += m0;
-                    colk[ni][1] += m1;
-                    dk[mi][ni][2 * hh] = x0;
-                    dk[mi][ni][2 * hh + 1] = x1;
-                }
+            for (int hh = 0; hh < 2; ++hh) {
+                const int r = row1(hh);
+                const float2 G2 = gpair(r, col), k2 = ld_pair(sK, kP, r, col);
+                const float x0 = dk[0][ni][2 * hh] * __expf(ge0 - G2.x), x1 = dk[0][ni][2 * hh + 1] * __expf(ge1 - G2.y);
+                const float m0 = x0 * k2.x, m1 = x1 * k2.y;   // dKe . K_e
+                dg[0][ni][2 * hh] = -m0;
+                dg[0][ni][2 * hh + 1] = -m1;
+                colk[ni][0] += m0;
+                colk[ni][1] += m1;
+                dk[0][ni][2 * hh] = x0;
+                dk[0][ni][2 * hh + 1] = x1;
+            }
         }
 #pragma unroll
         for (int ni = 0; ni < 4; ++ni)
@@ -381,54 +408,47 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_ch_kernel(ChBwd p) {
                 y += __shfl_xor_sync(0xffffffffu, y, 4);
                 y += __shfl_xor_sync(0xffffffffu, y, 8);
                 y += __shfl_xor_sync(0xffffffffu, y, 16);
-                if (g == 0) sColK[(warp & 1) * kD + col1(ni) + e] = y;
+                if (g == 0) sColK[(warp & 3) * kD + col1(ni) + e] = y;
             }
     }
-    // dQg = s dO S^T: dq = dQg e^{G} (written out now; the same thread adds the dQr term in phase 3),
-    // dG += dQg Q_g
-    zero(tmp[0]);
-    zero(tmp[1]);
-    gemm_k2<2, 4, 8, false, false>(tmp, sptr(sDO), kP, r1, 0, sptr(sS), kP, c1, 0, lane);
+    // dQg = s dO S^T: dq = dQg e^{G}, dG += dQg Q_g
+    zero(dq[0]);
+    gemm_k2<1, 4, 8, false, false>(dq, sptr(sDO), kP, r1, 0, sptr(sS), kP, c1, 0, lane);
 #pragma unroll
-    for (int mi = 0; mi < 2; ++mi)
+    for (int hh = 0; hh < 2; ++hh) {
+        const int r = row1(hh);
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int r = row1(mi, hh);
-            float *dst = p.dq + (tok0 + static_cast<size_t>(r) * p.H) * kD;
-#pragma unroll
-            for (int ni = 0; ni < 4; ++ni) {
-                const int col = col1(ni);
-                const float2 G2 = gpair(r, col), q2 = ld_pair(sQ, kP, r, col);
-                const float e0 = s * __expf(G2.x), e1 = s * __expf(G2.y);
-                const float x0 = tmp[mi][ni][2 * hh] * e0, x1 = tmp[mi][ni][2 * hh + 1] * e1;
-                dg[mi][ni][2 * hh] = fmaf(x0, q2.x, dg[mi][ni][2 * hh]);
-                dg[mi][ni][2 * hh + 1] = fmaf(x1, q2.y, dg[mi][ni][2 * hh + 1]);
-                if (r < L) *reinterpret_cast<float2 *>(dst + col) = make_float2(x0, x1);
-            }
+        for (int ni = 0; ni < 4; ++ni) {
+            const int col = col1(ni);
+            const float2 G2 = gpair(r, col), q2 = ld_pair(sQ, kP, r, col);
+            const float x0 = dq[0][ni][2 * hh] * s * __expf(G2.x), x1 = dq[0][ni][2 * hh + 1] * s * __expf(G2.y);
+            dg[0][ni][2 * hh] = fmaf(x0, q2.x, dg[0][ni][2 * hh]);
+            dg[0][ni][2 * hh + 1] = fmaf(x1, q2.y, dg[0][ni][2 * hh + 1]);
+            dq[0][ni][2 * hh] = x0;
+            dq[0][ni][2 * hh + 1] = x1;
         }
+    }
     // dW = -dE S^T (stored after the barrier, over S)
     zero(tmp[0]);
-    zero(tmp[1]);
-    gemm_k2<2, 4, 8, false, false>(tmp, sptr(sDE), kP, r1, 0, sptr(sS), kP, c1, 0, lane);
+    gemm_k2<1, 4, 8, false, false>(tmp, sptr(sDE), kP, r1, 0, sptr(sS), kP, c1, 0, lane);
     // dA = s lower(dO E^T) (stored after the barrier, over dO)
-    zero(da[0]);
-    gemm_k2<1, 4, 8, false, false>(da, sptr(sDO), kP, r2, 0, sptr(sE), kP, c2, 0, lane);
+    da[0][0][0] = da[0][0][1] = da[0][0][2] = da[0][0][3] = 0.f;
+    da[0][1][0] = da[0][1][1] = da[0][1][2] = da[0][1][3] = 0.f;
+    gemm_k2<1, 2, 8, false, false>(da, sptr(sDO), kP, r1, 0, sptr(sE), kP, c2, 0, lane);
     __syncthreads();   // every read of S, dS', E and dO is done
 
     // ---- phase 1b: dW, dA; the factor tiles
 #pragma unroll
-    for (int mi = 0; mi < 2; ++mi)
+    for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-            for (int ni = 0; ni < 4; ++ni)
-                st_pair(sDW, kP, row1(mi, hh), col1(ni), -tmp[mi][ni][2 * hh], -tmp[mi][ni][2 * hh + 1]);
+        for (int ni = 0; ni < 4; ++ni)
+            st_pair(sDW, kP, row1(hh), col1(ni), -tmp[0][ni][2 * hh], -tmp[0][ni][2 * hh + 1]);
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
-        const int i = row2(hh);
+        const int i = row1(hh);
 #pragma unroll
-        for (int ni = 0; ni < 4; ++ni) {
-            const int j = c2 + 8 * ni + 2 * q4;
+        for (int ni = 0; ni < 2; ++ni) {
+            const int j = col2(ni);
             st_pair(sDA, kPs, i, j, j <= i ? s * da[0][ni][2 * hh] : 0.f, j + 1 <= i ? s * da[0][ni][2 * hh + 1] : 0.f);
         }
     }
@@ -459,184 +479,171 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_ch_kernel(ChBwd p) {
     }
     __syncthreads();
 
-    // ---- phase 2: dXK = T^T dW -> dk, dG, dbeta part;  dXV = T^T dE -> dv, dbeta part;  dT;  P
+    // ---- phase 2: dQr -> dq;  dXK = T^T dW -> dk, dG, dbeta part;  dXV = T^T dE -> dv, dbeta part;  dT
+    // dQr = dA K_m: dq += dQr e^{G - G_r}, dG += dQr Q_r (the bf16 Q_r of dA^T Q_r); dq is complete
     zero(tmp[0]);
-    zero(tmp[1]);
-    gemm_k2<2, 4, 4, true, true>(tmp, sptr(sT), kPs, r1, 0, sptr(sDW), kP, c1, 0, lane);
+    gemm_m<1, 4, 4, false, true>(tmp, sptr(sDA), kPs, r1, 0, sptr(sKM), kP, c1, 0, lane);
 #pragma unroll
-    for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int r = row1(mi, hh);
-            const float bt = cg[kC + r];
-            float rsum = 0.f;
-#pragma unroll
-            for (int ni = 0; ni < 4; ++ni) {
-                const int col = col1(ni);
-                const float2 G2 = gpair(r, col), k2 = ld_pair(sK, kP, r, col);
-                const float eg0 = __expf(G2.x), eg1 = __expf(G2.y);
-                const float kg0 = k2.x * eg0, kg1 = k2.y * eg1;   // K_g
-                const float x0 = tmp[mi][ni][2 * hh], x1 = tmp[mi][ni][2 * hh + 1];
-                rsum = fmaf(x0, kg0, fmaf(x1, kg1, rsum));
-                dg[mi][ni][2 * hh] = fmaf(bt * x0, kg0, dg[mi][ni][2 * hh]);
-                dg[mi][ni][2 * hh + 1] = fmaf(bt * x1, kg1, dg[mi][ni][2 * hh + 1]);
-                dk[mi][ni][2 * hh] = fmaf(bt * eg0, x0, dk[mi][ni][2 * hh]);
-                dk[mi][ni][2 * hh + 1] = fmaf(bt * eg1, x1, dk[mi][ni][2 * hh + 1]);
-            }
-            put_row(RB_XK, cb1, r, rsum);
-        }
-    zero(tmp[0]);
-    zero(tmp[1]);
-    gemm_k2<2, 4, 4, true, true>(tmp, sptr(sT), kPs, r1, 0, sptr(sDE), kP, c1, 0, lane);
-#pragma unroll
-    for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int r = row1(mi, hh);
-            const float bt = cg[kC + r];
-            float rsum = 0.f;
-            float *dst = p.dv + (tok0 + static_cast<size_t>(r) * p.H) * kD;
-#pragma unroll
-            for (int ni = 0; ni < 4; ++ni) {
-                const int col = col1(ni);
-                const float2 v2 = ld_pair(sV, kP, r, col);
-                rsum = fmaf(tmp[mi][ni][2 * hh], v2.x, fmaf(tmp[mi][ni][2 * hh + 1], v2.y, rsum));
-                if (r < L)
-                    *reinterpret_cast<float2 *>(dst + col) =
-                        make_float2(bt * tmp[mi][ni][2 * hh], bt * tmp[mi][ni][2 * hh + 1]);
-            }
-            put_row(RB_XV, cb1, r, rsum);
-        }
-    {   // dT = (dW K_g^T + dE V^T) diag(beta)  (over Q)
-        float a1[1][4][4];
-        zero(a1[0]);
-        gemm_k2<1, 4, 8, false, false>(a1, sptr(sDW), kP, r2, 0, sptr(sKG), kP, c2, 0, lane);
-        gemm_k2<1, 4, 8, false, false>(a1, sptr(sDE), kP, r2, 0, sptr(sV), kP, c2, 0, lane);
+    for (int hh = 0; hh < 2; ++hh) {
+        const int r = row1(hh);
+        float *dst = dq_row(r);
 #pragma unroll
         for (int ni = 0; ni < 4; ++ni) {
-            const int j = c2 + 8 * ni + 2 * q4;
+            const int col = col1(ni);
+            const float2 G2 = gpair(r, col), qr = ld_pair(sQR, kP, r, col);
+            const float x0 = tmp[0][ni][2 * hh], x1 = tmp[0][ni][2 * hh + 1];
+            dg[0][ni][2 * hh] = fmaf(x0, qr.x, dg[0][ni][2 * hh]);
+            dg[0][ni][2 * hh + 1] = fmaf(x1, qr.y, dg[0][ni][2 * hh + 1]);
+            if (r < L)
+                *reinterpret_cast<float2 *>(dst + col) =
+                    make_float2(fmaf(x0, __expf(G2.x - sGr[col]), dq[0][ni][2 * hh]),
+                                fmaf(x1, __expf(G2.y - sGr[col + 1]), dq[0][ni][2 * hh + 1]));
+        }
+    }
+    zero(tmp[0]);
+    gemm_k2<1, 4, 4, true, true>(tmp, sptr(sT), kPs, r1, 0, sptr(sDW), kP, c1, 0, lane);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        const int r = row1(hh);
+        const float bt = cg[kC + r];
+        float rsum = 0.f;
+#pragma unroll
+        for (int ni = 0; ni < 4; ++ni) {
+            const int col = col1(ni);
+            const float2 G2 = gpair(r, col), k2 = ld_pair(sK, kP, r, col);
+            const float eg0 = __expf(G2.x), eg1 = __expf(G2.y);
+            const float kg0 = k2.x * eg0, kg1 = k2.y * eg1;   // K_g
+            const float x0 = tmp[0][ni][2 * hh], x1 = tmp[0][ni][2 * hh + 1];
+            rsum = fmaf(x0, kg0, fmaf(x1, kg1, rsum));
+            dg[0][ni][2 * hh] = fmaf(bt * x0, kg0, dg[0][ni][2 * hh]);
+            dg[0][ni][2 * hh + 1] = fmaf(bt * x1, kg1, dg[0][ni][2 * hh + 1]);
+            dk[0][ni][2 * hh] = fmaf(bt * eg0, x0, dk[0][ni][2 * hh]);
+            dk[0][ni][2 * hh + 1] = fmaf(bt * eg1, x1, dk[0][ni][2 * hh + 1]);
+        }
+        put_row(RB_XK, r, rsum);
+    }
+    zero(tmp[0]);
+    gemm_k2<1, 4, 4, true, true>(tmp, sptr(sT), kPs, r1, 0, sptr(sDE), kP, c1, 0, lane);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        const int r = row1(hh);
+        const float bt = cg[kC + r];
+        float rsum = 0.f;
+        float *dst = p.dv + (tok0 + static_cast<size_t>(r) * p.H) * kD;
+#pragma unroll
+        for (int ni = 0; ni < 4; ++ni) {
+            const int col = col1(ni);
+            const float2 v2 = ld_pair(sV, kP, r, col);
+            rsum = fmaf(tmp[0][ni][2 * hh], v2.x, fmaf(tmp[0][ni][2 * hh + 1], v2.y, rsum));
+            if (r < L)
+                *reinterpret_cast<float2 *>(dst + col) = make_float2(bt * tmp[0][ni][2 * hh], bt * tmp[0][ni][2 * hh + 1]);
+        }
+        put_row(RB_XV, r, rsum);
+    }
+    {   // dT = (dW K_g^T + dE V^T) diag(beta)  (over Q)
+        float a1[1][2][4] = {};
+        gemm_k2<1, 2, 8, false, false>(a1, sptr(sDW), kP, r1, 0, sptr(sKG), kP, c2, 0, lane);
+        gemm_k2<1, 2, 8, false, false>(a1, sptr(sDE), kP, r1, 0, sptr(sV), kP, c2, 0, lane);
+#pragma unroll
+        for (int ni = 0; ni < 2; ++ni) {
+            const int j = col2(ni);
             const float bj0 = cg[kC + j], bj1 = cg[kC + j + 1];
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh)
-                st_pair(sDT, kPs, row2(hh), j, bj0 * a1[0][ni][2 * hh], bj1 * a1[0][ni][2 * hh + 1]);
+                st_pair(sDT, kPs, row1(hh), j, bj0 * a1[0][ni][2 * hh], bj1 * a1[0][ni][2 * hh + 1]);
         }
     }
     __syncthreads();   // dT is visible; V and dE are no longer read
 
-    // ---- phase 3: Y = T^T dT (over V);  dR = -strict_lower(Y T^T), dP = beta dR (over dE);  dQr -> dq
+    // ---- phase 3: Y = T^T dT (over V);  P, dR = -strict_lower(Y T^T), dP = beta dR (over dE);  dQr -> dq
     {
-        float y[1][4][4];
-        zero(y[0]);
-        gemm_k2<1, 4, 4, true, true>(y, sptr(sT), kPs, r2, 0, sptr(sDT), kPs, c2, 0, lane);
+        float y[1][2][4] = {};
+        gemm_k2<1, 2, 4, true, true>(y, sptr(sT), kPs, r1, 0, sptr(sDT), kPs, c2, 0, lane);
 #pragma unroll
-        for (int ni = 0; ni < 4; ++ni)
+        for (int ni = 0; ni < 2; ++ni)
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh)
-                st_pair(sY, kPs, row2(hh), c2 + 8 * ni + 2 * q4, y[0][ni][2 * hh], y[0][ni][2 * hh + 1]);
+                st_pair(sY, kPs, row1(hh), col2(ni), y[0][ni][2 * hh], y[0][ni][2 * hh + 1]);
     }
     __syncthreads();
     {
-        float pk[1][4][4];   // P = K_r K_m^T for the dR . P sums
-        zero(pk[0]);
-        gemm_k2<1, 4, 8, false, false>(pk, sptr(sKR), kP, r2, 0, sptr(sKM), kP, c2, 0, lane);
-        float dr[1][4][4];
-        zero(dr[0]);
-        gemm_k2<1, 4, 4, false, false>(dr, sptr(sY), kPs, r2, 0, sptr(sT), kPs, c2, 0, lane);
+        float pk[1][2][4] = {};   // P = K_r K_m^T for the dR . P sums
+        gemm_k2<1, 2, 8, false, false>(pk, sptr(sKR), kP, r1, 0, sptr(sKM), kP, c2, 0, lane);
+        float dr[1][2][4] = {};
+        gemm_k2<1, 2, 4, false, false>(dr, sptr(sY), kPs, r1, 0, sptr(sT), kPs, c2, 0, lane);
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-            const int i = row2(hh);
+            const int i = row1(hh);
             const float bi = cg[kC + i];
             float rsum = 0.f;
 #pragma unroll
-            for (int ni = 0; ni < 4; ++ni) {
-                const int j = c2 + 8 * ni + 2 * q4;
+            for (int ni = 0; ni < 2; ++ni) {
+                const int j = col2(ni);
                 const float x0 = j < i ? -dr[0][ni][2 * hh] : 0.f, x1 = j + 1 < i ? -dr[0][ni][2 * hh + 1] : 0.f;
                 rsum = fmaf(x0, pk[0][ni][2 * hh], fmaf(x1, pk[0][ni][2 * hh + 1], rsum));
                 st_pair(sDP, kPs, i, j, bi * x0, bi * x1);
             }
-            put_row(RB_R, cb2, i, rsum);
+            put_row(RB_R, i, rsum);
         }
     }
-    // dQr = dA K_m: dq += dQr e^{G - G_r}, dG += dQr Q_r (the bf16 Q_r of dA^T Q_r); dq is complete
-    zero(tmp[0]);
-    zero(tmp[1]);
-    gemm_k2<2, 4, 4, false, true>(tmp, sptr(sDA), kPs, r1, 0, sptr(sKM), kP, c1, 0, lane);
-#pragma unroll
-    for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int r = row1(mi, hh);
-            float *dst = p.dq + (tok0 + static_cast<size_t>(r) * p.H) * kD;
-#pragma unroll
-            for (int ni = 0; ni < 4; ++ni) {
-                const int col = col1(ni);
-                const float2 G2 = gpair(r, col), qr = ld_pair(sQR, kP, r, col);
-                const float x0 = tmp[mi][ni][2 * hh], x1 = tmp[mi][ni][2 * hh + 1];
-                dg[mi][ni][2 * hh] = fmaf(x0, qr.x, dg[mi][ni][2 * hh]);
-                dg[mi][ni][2 * hh + 1] = fmaf(x1, qr.y, dg[mi][ni][2 * hh + 1]);
-                if (r < L) {
-                    const float2 d = *reinterpret_cast<const float2 *>(dst + col);
-                    *reinterpret_cast<float2 *>(dst + col) = make_float2(fmaf(x0, __expf(G2.x - sGr[col]), d.x),
-                                                                         fmaf(x1, __expf(G2.y - sGr[col + 1]), d.y));
-                }
-            }
-        }
     __syncthreads();   // dP is visible
 
     // ---- phase 4: dKr = dP K_m -> dk, dG;  dKm = dP^T K_r + dA^T Q_r -> dk, dG
+    // alpha of the chunk's tokens for the last step, rows 0-31 over dT and rows 32-63 over Y (both read
+    // last in phase 3)
+    {
+        float *sAl0 = reinterpret_cast<float *>(sDT), *sAl1 = reinterpret_cast<float *>(sY);
+        for (int e = tid; e < kC * kD / 4; e += kGradThreads) {
+            const int t = e >> 5, cc = (e & 31) * 4;
+            if (t < L) cp16((t < 32 ? sAl0 + t * kD : sAl1 + (t - 32) * kD) + cc,
+                            p.alpha + (tok0 + static_cast<size_t>(t) * p.H) * kD + cc, true);
+        }
+        cp_commit();
+    }
     zero(tmp[0]);
-    zero(tmp[1]);
-    gemm_k2<2, 4, 4, false, true>(tmp, sptr(sDP), kPs, r1, 0, sptr(sKM), kP, c1, 0, lane);
+    gemm_k2<1, 4, 4, false, true>(tmp, sptr(sDP), kPs, r1, 0, sptr(sKM), kP, c1, 0, lane);
 #pragma unroll
-    for (int mi = 0; mi < 2; ++mi)
+    for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-            for (int ni = 0; ni < 4; ++ni) {
-                const int r = row1(mi, hh), col = col1(ni);
-                const float2 G2 = gpair(r, col), kr = ld_pair(sKR, kP, r, col);
-                const float x0 = tmp[mi][ni][2 * hh], x1 = tmp[mi][ni][2 * hh + 1];
-                dg[mi][ni][2 * hh] = fmaf(x0, kr.x, dg[mi][ni][2 * hh]);
-                dg[mi][ni][2 * hh + 1] = fmaf(x1, kr.y, dg[mi][ni][2 * hh + 1]);
-                dk[mi][ni][2 * hh] = fmaf(x0, __expf(G2.x - sGr[col]), dk[mi][ni][2 * hh]);
-                dk[mi][ni][2 * hh + 1] = fmaf(x1, __expf(G2.y - sGr[col + 1]), dk[mi][ni][2 * hh + 1]);
-            }
+        for (int ni = 0; ni < 4; ++ni) {
+            const int r = row1(hh), col = col1(ni);
+            const float2 G2 = gpair(r, col), kr = ld_pair(sKR, kP, r, col);
+            const float x0 = tmp[0][ni][2 * hh], x1 = tmp[0][ni][2 * hh + 1];
+            dg[0][ni][2 * hh] = fmaf(x0, kr.x, dg[0][ni][2 * hh]);
+            dg[0][ni][2 * hh + 1] = fmaf(x1, kr.y, dg[0][ni][2 * hh + 1]);
+            dk[0][ni][2 * hh] = fmaf(x0, __expf(G2.x - sGr[col]), dk[0][ni][2 * hh]);
+            dk[0][ni][2 * hh + 1] = fmaf(x1, __expf(G2.y - sGr[col + 1]), dk[0][ni][2 * hh + 1]);
+        }
     zero(tmp[0]);
-    zero(tmp[1]);
-    gemm_k2<2, 4, 4, true, true>(tmp, sptr(sDP), kPs, r1, 0, sptr(sKR), kP, c1, 0, lane);
-    gemm_k2<2, 4, 4, true, true>(tmp, sptr(sDA), kPs, r1, 0, sptr(sQR), kP, c1, 0, lane);
+    gemm_k2<1, 4, 4, true, true>(tmp, sptr(sDP), kPs, r1, 0, sptr(sKR), kP, c1, 0, lane);
+    gemm_k2<1, 4, 4, true, true>(tmp, sptr(sDA), kPs, r1, 0, sptr(sQR), kP, c1, 0, lane);
 #pragma unroll
-    for (int mi = 0; mi < 2; ++mi)
+    for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-            for (int ni = 0; ni < 4; ++ni) {
-                const int r = row1(mi, hh), col = col1(ni);
-                const float2 G2 = gpair(r, col), km = ld_pair(sKM, kP, r, col);
-                const float x0 = tmp[mi][ni][2 * hh], x1 = tmp[mi][ni][2 * hh + 1];
-                dg[mi][ni][2 * hh] = fmaf(-x0, km.x, dg[mi][ni][2 * hh]);
-                dg[mi][ni][2 * hh + 1] = fmaf(-x1, km.y, dg[mi][ni][2 * hh + 1]);
-                dk[mi][ni][2 * hh] = fmaf(x0, __expf(sGr[col] - G2.x), dk[mi][ni][2 * hh]);
-                dk[mi][ni][2 * hh + 1] = fmaf(x1, __expf(sGr[col + 1] - G2.y), dk[mi][ni][2 * hh + 1]);
-            }
+        for (int ni = 0; ni < 4; ++ni) {
+            const int r = row1(hh), col = col1(ni);
+            const float2 G2 = gpair(r, col), km = ld_pair(sKM, kP, r, col);
+            const float x0 = tmp[0][ni][2 * hh], x1 = tmp[0][ni][2 * hh + 1];
+            dg[0][ni][2 * hh] = fmaf(-x0, km.x, dg[0][ni][2 * hh]);
+            dg[0][ni][2 * hh + 1] = fmaf(-x1, km.y, dg[0][ni][2 * hh + 1]);
+            dk[0][ni][2 * hh] = fmaf(x0, __expf(sGr[col] - G2.x), dk[0][ni][2 * hh]);
+            dk[0][ni][2 * hh + 1] = fmaf(x1, __expf(sGr[col + 1] - G2.y), dk[0][ni][2 * hh + 1]);
+        }
     // dG to shared memory (over dW | K_g, read last in phase 2)
 #pragma unroll
-    for (int mi = 0; mi < 2; ++mi)
+    for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-            for (int ni = 0; ni < 4; ++ni)
-                *reinterpret_cast<float2 *>(sDG + row1(mi, hh) * kPG + col1(ni)) =
-                    make_float2(dg[mi][ni][2 * hh], dg[mi][ni][2 * hh + 1]);
+        for (int ni = 0; ni < 4; ++ni)
+            *reinterpret_cast<float2 *>(sDG + row1(hh) * kPG + col1(ni)) =
+                make_float2(dg[0][ni][2 * hh], dg[0][ni][2 * hh + 1]);
     __syncthreads();   // dG and every row partial are in shared memory
 
+    cp_wait<0>();
     // per token (threads 0-63): dbeta, deta, the k coefficient
     if (tid < kC) {
         const int t = tid;
-        const float xk = rrow[RB_XK][0][t] + rrow[RB_XK][1][t] + rrow[RB_XK][2][t] + rrow[RB_XK][3][t];
-        const float xv = rrow[RB_XV][0][t] + rrow[RB_XV][1][t] + rrow[RB_XV][2][t] + rrow[RB_XV][3][t];
-        const float xr = rrow[RB_R][0][t] + rrow[RB_R][1][t];
-        const float dbeta = xk + xv + xr, bt = cg[kC + t], den = cg[2 * kC + t];
+        auto rsum4 = [&](int qi) { return rrow[qi][0][t] + rrow[qi][1][t] + rrow[qi][2][t] + rrow[qi][3][t]; };
+        const float dbeta = rsum4(RB_XK) + rsum4(RB_XV) + rsum4(RB_R), bt = cg[kC + t], den = cg[2 * kC + t];
         float deta = dbeta, kc = 0.f;
         if (!p.beta_raw) {
             const bool flows = den != 0.f;
@@ -646,41 +653,42 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_ch_kernel(ChBwd p) {
         kcoef[t] = kc;
         if (t < L) p.deta[tok0 + static_cast<size_t>(t) * p.H] = deta;
     }
-    // reverse prefix of dG per channel, in two halves of 32 tokens: the half sums first
-    const int ch = tid & (kD - 1), hf = tid >> 7;
+    // reverse prefix of dG per channel, in quarters of 16 tokens: the quarter sums first
+    const int ch = tid & (kD - 1), qt = tid >> 7;
     {
         float sum = 0.f;
-#pragma unroll 8
-        for (int u = 0; u < 32; ++u) sum += sDG[(32 * hf + u) * kPG + ch];
-        shalf[hf * kD + ch] = sum;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) sum += sDG[(16 * qt + u) * kPG + ch];
+        squart[qt * kD + ch] = sum;
     }
-    __syncthreads();   // kcoef and the half sums are visible
+    __syncthreads();   // kcoef, the quarter sums and alpha are visible
 
 #pragma unroll
-    for (int mi = 0; mi < 2; ++mi)
+    for (int hh = 0; hh < 2; ++hh) {
+        const int r = row1(hh);
+        if (r >= L) continue;
+        const float kc = kcoef[r];
+        float *dst = p.dk + (tok0 + static_cast<size_t>(r) * p.H) * kD;
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int r = row1(mi, hh);
-            if (r >= L) continue;
-            const float kc = kcoef[r];
-            float *dst = p.dk + (tok0 + static_cast<size_t>(r) * p.H) * kD;
-#pragma unroll
-            for (int ni = 0; ni < 4; ++ni) {
-                const int col = col1(ni);
-                const float2 kx = ld_pair(sK, kP, r, col);
-                *reinterpret_cast<float2 *>(dst + col) =
-                    make_float2(fmaf(kc, kx.x, dk[mi][ni][2 * hh]), fmaf(kc, kx.y, dk[mi][ni][2 * hh + 1]));
-            }
+        for (int ni = 0; ni < 4; ++ni) {
+            const int col = col1(ni);
+            const float2 kx = ld_pair(sK, kP, r, col);
+            *reinterpret_cast<float2 *>(dst + col) =
+                make_float2(fmaf(kc, kx.x, dk[0][ni][2 * hh]), fmaf(kc, kx.y, dk[0][ni][2 * hh + 1]));
         }
+    }
     {   // the end decay's terms join the last row: sum_i dKe K_e + Gamma <S, dS'>
-        float run = sColK[ch] + sColK[kD + ch] + __expf(sGe[ch]) * sDGam[ch];
-        if (hf == 0) run += shalf[kD + ch];
-        for (int u = 31; u >= 0; --u) {
-            const int t = 32 * hf + u;
+        float run = sColK[ch] + sColK[kD + ch] + sColK[2 * kD + ch] + sColK[3 * kD + ch] +
+                    __expf(sGe[ch]) * sDGam[ch];
+        for (int q = 3; q > qt; --q) run += squart[q * kD + ch];
+#pragma unroll 4
+        for (int u = 15; u >= 0; --u) {
+            const int t = 16 * qt + u;
             run += sDG[t * kPG + ch];
             if (t < L) {
-                const size_t o = (tok0 + static_cast<size_t>(t) * p.H) * kD + ch;
-                p.dalpha[o] = run / p.alpha[o];
+                const float a = t < 32 ? reinterpret_cast<const float *>(sDT)[t * kD + ch]
+                                       : reinterpret_cast<const float *>(sY)[(t - 32) * kD + ch];
+                p.dalpha[(tok0 + static_cast<size_t>(t) * p.H) * kD + ch] = run / a;
             }
         }
     }

@@ -157,10 +157,10 @@ def test_bwd_workspace_size(lib):
     assert ex(2, 200, 3, 128, 128, 0, 0) == (2 * 3 * 25 * 128 * 128 + 2 * 200 * 3 * 128) * 4  # fp32: token path
     assert ex(2, 16, 3, 128, 128, 1, 0) == (2 * 3 * 2 * 128 * 128 + 2 * 16 * 3 * 128) * 4   # T <= 16: token path
     # bf16, per-channel gate, d = 128: one mark per chain (256-byte aligned), then room for the larger
-    # of the chunkwise records (those above plus K e^{G_end - G}, s Q e^{G} and e^{G_end}) and the
-    # token path's checkpoints, which rerun the chains outside the factorised range
+    # of the chunkwise records (those above plus dE of its own, K e^{G_end - G}, s Q e^{G} and
+    # e^{G_end}) and the token path's checkpoints, which rerun the chains outside the factorised range
     seq_ws = (2 * 3 * 25 * 128 * 128 + 2 * 200 * 3 * 128) * 4
-    rec_ch = 2 * 3 * 4 * (per_chunk + 2 * 2 * 64 * 128 + 4 * 128)
+    rec_ch = 2 * 3 * 4 * (per_chunk + 3 * 2 * 64 * 128 + 4 * 128)
     assert ex(2, 200, 3, 128, 128, 1, 1) == 256 + max(rec_ch, seq_ws)
     assert ex(2, 200, 3, 128, 128, 0, 1) == seq_ws                  # fp32 per-channel: token path
     assert lib.kla_chunk_bwd_workspace_size(2, 200, 3, 128, 128) >= ex(2, 200, 3, 128, 128, 1, 0)
