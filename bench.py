@@ -62,11 +62,10 @@ DECODE_BYTES_PER_HEAD_STEP = 8 * 128 * 128 + 4 * 2 * 128 + 8
 # reports null.
 TC_SOURCES = ("gated_delta_rule_14_gb300/csrc/kla_chunk_tc.cu", "gated_delta_rule_14_gb300/csrc/sm103_ptx.cuh",
               "gated_delta_rule_14_gb300/csrc/kla_internal.cuh")
-# (98a19049...: the same kernel code as e9fa9b8b...; the header gained two host declarations only.)
-TC_TRAFFIC_GDN4K = {"e9fa9b8b231d85d0": 520.831488e6, "98a1904944c627c7": 520.831488e6}
+TC_TRAFFIC_GDN4K = {"90a46a61cd1e6f13": 520.460032e6}
 # sm__pipe_tensor_cycles_active (fraction of elapsed cycles) of the same kernel and capture:
 # the algorithmic TFLOP/s divided by it is the rate of the MMA phases themselves.
-TC_PIPE_ACTIVE_GDN4K = {"e9fa9b8b231d85d0": 0.13132, "98a1904944c627c7": 0.13132}
+TC_PIPE_ACTIVE_GDN4K = {"90a46a61cd1e6f13": 0.13155}
 
 
 def tc_fingerprint() -> str:
@@ -506,6 +505,8 @@ def main():
     ap.add_argument("--bwd-batch", type=int, default=8)
     ap.add_argument("--prefill-only", choices=["gdn4k", "kda8k", "long131k"], default=None,
                     help="time only the prefill of this workload (a command for profiling one kernel)")
+    ap.add_argument("--verify-only", choices=["4", "8", "16", "16kda"], default=None,
+                    help="time only this multi-token call on the decode batch (--verify-calls calls)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -540,6 +541,13 @@ def main():
         if rank == 0:
             print(json.dumps({"prefill": args.prefill_only, "ms_per_step": r["ms"],
                               "roofline": roofline(r["alg_bytes"], r["ms"], pk)}), flush=True)
+        return
+
+    if args.verify_only:
+        ntok, ch = int(args.verify_only.replace("kda", "")), args.verify_only.endswith("kda")
+        r = bench_verify(ntok, args.verify_calls, seed=rank, dev=dev, flush=flush, stream=stream, pk=pk, channel=ch)
+        if rank == 0:
+            print(json.dumps({f"verify{args.verify_only}": r}), flush=True)
         return
 
     if args.bwd_only:
