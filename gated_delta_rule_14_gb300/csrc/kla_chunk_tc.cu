@@ -362,8 +362,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
         }
     };
-    auto chgate = [&](int c, int u, int j) {   // gate of token u of this thread's sub-range, channel j of its group
-        return t_begin + c * kC + 32 * cth + 4 * csb + u < t_end ? fmaxf(ga[u][j], 1.8e-35f) : 1.f;
+    // gate of token u of this thread's sub-range, channel j of its group; inb[u]: token u is inside the
+    // sequence (formed once per chunk)
+    auto chgate = [&](const bool (&inb)[4], int u, int j) { return inb[u] ? fmaxf(ga[u][j], 1.8e-35f) : 1.f; };
+    auto in_bounds = [&](int c, bool (&inb)[4]) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) inb[u] = t_begin + c * kC + 32 * cth + 4 * csb + u < t_end;
     };
 
     // (a) gates, norms, beta and the decay tables; issue [K;Q] K^T.
@@ -375,14 +379,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // the sub-ranges between this thread's and the reference token (before it in half 1, after
         // it in half 0), `tot` over the whole half
         float ex[kCh ? 8 : 1];
+        bool inb[4];
         if constexpr (kCh) {
+            in_bounds(c, inb);
             bool low = false;
             float tot[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 float l = 1.f;
 #pragma unroll
-                for (int u = 0; u < 4; ++u) l *= chgate(c, u, j);
+                for (int u = 0; u < 4; ++u) l *= chgate(inb, u, j);
                 float sc = l;   // inclusive scan towards the reference token
 #pragma unroll
                 for (int off = 1; off < 8; off <<= 1) {
@@ -469,13 +475,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     if (cth) {
-                        run[j] *= chgate(c, u, j);
+                        run[j] *= chgate(inb, u, j);
                         fr[j] = run[j];
                         fm[j] = __fdividef(1.f, run[j]);
                     } else {
                         fm[j] = run[j];
                         fr[j] = __fdividef(1.f, run[j]);
-                        run[j] *= chgate(c, u, j);
+                        run[j] *= chgate(inb, u, j);
                     }
                 }
                 const uint32_t off = sw128_off(i, colb);
@@ -483,13 +489,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const uint32_t kw[4] = {kx.x, kx.y, kx.z, kx.w}, qw[4] = {qx.x, qx.y, qx.z, qx.w};
                 uint32_t o1[4], o2[4], o3[4], o4[4];
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const float k0 = bf16lo(kw[w]), k1 = bf16hi(kw[w]), q0 = bf16lo(qw[w]), q1 = bf16hi(qw[w]);
-                    const int j0 = 2 * w, j1 = 2 * w + 1;
-                    o1[w] = pack_bf16(k0 * fr[j0], k1 * fr[j1]);
-                    o2[w] = pack_bf16(q0 * fr[j0], q1 * fr[j1]);
-                    o3[w] = pack_bf16(k0 * fm[j0], k1 * fm[j1]);
-                    o4[w] = pack_bf16(k0 * (Fv[j0] * fm[j0]), k1 * (Fv[j1] * fm[j1]));
+                for (int w = 0; w < 4; ++w) {   // channel pairs, on packed fp32 multiplies
+                    const float2 k2 = make_float2(bf16lo(kw[w]), bf16hi(kw[w]));
+                    const float2 q2 = make_float2(bf16lo(qw[w]), bf16hi(qw[w]));
+                    const float2 fr2 = make_float2(fr[2 * w], fr[2 * w + 1]), fm2 = make_float2(fm[2 * w], fm[2 * w + 1]);
+                    const float2 a = __fmul2_rn(k2, fr2), bq = __fmul2_rn(q2, fr2), m = __fmul2_rn(k2, fm2),
+                                 e = __fmul2_rn(m, make_float2(Fv[2 * w], Fv[2 * w + 1]));   // K_m e^{G_end-G_r}
+                    o1[w] = pack_bf16(a.x, a.y);
+                    o2[w] = pack_bf16(bq.x, bq.y);
+                    o3[w] = pack_bf16(m.x, m.y);
+                    o4[w] = pack_bf16(e.x, e.y);
                 }
                 st_shared_v4(Kt + off, o1[0], o1[1], o1[2], o1[3]);
                 st_shared_v4(Qt + off, o2[0], o2[1], o2[2], o2[3]);
