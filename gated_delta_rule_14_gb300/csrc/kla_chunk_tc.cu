@@ -384,20 +384,26 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             in_bounds(c, inb);
             bool low = false;
             float tot[8];
+            // the scan runs towards the reference token: from lane csb - off (half 1) or csb + off
+            // (half 0) of the 8-lane group, one indexed shuffle a step
+            const int dir = cth ? -1 : 1;
+            const int src1 = (csb + dir) & 7, src2 = (csb + 2 * dir) & 7, src4 = (csb + 4 * dir) & 7;
+            const bool in1 = cth ? csb >= 1 : csb + 1 < 8, in2 = cth ? csb >= 2 : csb + 2 < 8,
+                       in4 = cth ? csb >= 4 : csb + 4 < 8;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 float l = 1.f;
 #pragma unroll
                 for (int u = 0; u < 4; ++u) l *= chgate(inb, u, j);
                 float sc = l;   // inclusive scan towards the reference token
-#pragma unroll
-                for (int off = 1; off < 8; off <<= 1) {
-                    const float y = cth ? __shfl_up_sync(0xffffffffu, sc, off, 8)
-                                        : __shfl_down_sync(0xffffffffu, sc, off, 8);
-                    if (cth ? csb >= off : csb + off < 8) sc *= y;
-                }
-                const float nb = cth ? __shfl_up_sync(0xffffffffu, sc, 1, 8) : __shfl_down_sync(0xffffffffu, sc, 1, 8);
-                ex[j] = (cth ? csb == 0 : csb == 7) ? 1.f : nb;
+                float y = __shfl_sync(0xffffffffu, sc, src1, 8);
+                if (in1) sc *= y;
+                y = __shfl_sync(0xffffffffu, sc, src2, 8);
+                if (in2) sc *= y;
+                y = __shfl_sync(0xffffffffu, sc, src4, 8);
+                if (in4) sc *= y;
+                const float nb = __shfl_sync(0xffffffffu, sc, src1, 8);
+                ex[j] = in1 ? nb : 1.f;
                 tot[j] = __shfl_sync(0xffffffffu, sc, cth ? 7 : 0, 8);
                 low |= tot[j] < 1.8e-35f;
             }
