@@ -225,3 +225,23 @@ def test_long_sequence_segments_state_in_place():
     o_ref, s_ref = oracle_chains(inp)
     assert oracle.rel_l2(S.cpu().numpy()[0], s_ref) <= 1e-2
     assert oracle.rel_l2(o.float().cpu().numpy()[:, :, 0], o_ref) <= 1e-2
+
+
+def test_channel_gate_alpha_not_16_byte_aligned():
+    """The ABI needs only 4-byte alignment of alpha: a view of the per-channel gates starting 4 bytes
+    past a 16-byte boundary gives the aligned call's results bit for bit and meets the oracle's bar."""
+    import torch
+
+    import gated_delta_rule_14_gb300 as kla
+    inp = synth.make_prefill("kda8k", seed=41, B=2, T=200, H=2, s0_sigma=0.05)
+    a = to_dev(inp.alpha)
+    buf = torch.empty(a.numel() + 4, dtype=torch.float32, device=DEV)
+    a_off = buf[1:1 + a.numel()].view(a.shape)
+    a_off.copy_(a)
+    assert a.data_ptr() % 16 == 0 and a_off.data_ptr() % 16 == 4
+    args = (to_dev(inp.q), to_dev(inp.k), to_dev(inp.v))
+    o1, s1 = kla.chunk_fwd(*args, a, to_dev(inp.eta), inp.wl.eps, to_dev(inp.S0))
+    o2, s2 = kla.chunk_fwd(*args, a_off, to_dev(inp.eta), inp.wl.eps, to_dev(inp.S0))
+    kla.device_status(DEV)
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+    check(inp, o2.float().cpu().numpy().astype(np.float64), s2.cpu().numpy().astype(np.float64))
