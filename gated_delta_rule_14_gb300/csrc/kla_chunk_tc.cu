@@ -352,12 +352,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     auto load_chgates = [&](int c) {
         if constexpr (kCh) {
             if (grp == 1 && c < nchunks) {
+                // the 4 tokens are consecutive rows: one base address and a row stride (tokens past
+                // the end reread the last row)
+                const int t = t_begin + c * kC + 32 * cth + 4 * csb, tl = min(t, t_end - 1);
+                const float *g0 = p.alpha + ((static_cast<size_t>(b) * p.T + tl) * p.H + h) * kD + 8 * ccg;
+                const size_t rs = static_cast<size_t>(p.H) * kD;
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const int t = min(t_begin + c * kC + 32 * cth + 4 * csb + u, t_end - 1);
-                    const float *g0 = p.alpha + ((static_cast<size_t>(b) * p.T + t) * p.H + h) * kD + 8 * ccg;
+                    const float *gu = g0 + (t + u < t_end ? u : t_end - 1 - tl) * rs;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) ga[u][j] = g0[j];
+                    for (int j = 0; j < 8; ++j) ga[u][j] = gu[j];
                 }
             }
         }
