@@ -299,12 +299,16 @@ def test_channel_gate_out_of_range_chain_takes_the_exact_path():
     compare(pick(got, [(1, 0)]), run_oracle(inp, dO, dST, chains=[(1, 0)]), TOL["bf16"])
 
 
-@pytest.mark.parametrize("T", [4059, 16384 - 5])
-def test_channel_long_chain_segmented_carries(T):
+@pytest.mark.parametrize("T,mode", [(4059, {}), (2048 + 31, dict(beta_mode="raw", q_scale=0.5)), (16384 - 5, {})])
+def test_channel_long_chain_segmented_carries(T, mode):
     """Per-channel gate with few chains and many chunks: both carries split into segments run in
-    parallel, reading the per-channel records (decayed keys, scaled queries, end decays)."""
-    inp = synth.make_prefill("kda8k", seed=T + 3, B=1, T=T, H=2, s0_sigma=0.05)
+    parallel, reading the per-channel records (decayed keys, scaled queries, end decays); also
+    with the raw step (unit keys) and a query scale."""
+    over = dict(B=1, T=T, H=2, s0_sigma=0.05)
+    if mode:
+        over["key_norm"] = "l2"
+    inp = synth.make_prefill("kda8k", seed=T + 3, **over)
     dO, dST = _grad_inputs(inp, seed=T + 4, with_dst=True)
-    got = run_gpu(inp, dO, dST)
-    ref = run_oracle(inp, dO, dST)
+    got = run_gpu(inp, dO, dST, **mode)
+    ref = run_oracle(inp, dO, dST, **mode)
     compare(pick(got, [(0, 0), (0, 1)]), ref, TOL_CHUNK)
