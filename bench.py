@@ -393,8 +393,9 @@ def bench_bwd(name, steps, seed, dev, flush, stream, pk, **override):
 def e2e_prefill(res, steps, warmup, dev, stream, parts=8):
     """Same workload through the public host-buffer API (kla_chunk_fwd_host) with pinned host
     tensors: per step the H2D copies of q, k, v, alpha, eta, the prefill and the D2H copies of o
-    and S_T, all inside the timed region; the batch runs in `parts` parts so copies of one part
-    overlap the prefill of another."""
+    and S_T, all inside the timed region; the work runs in `parts` parts (slices of whole chunks of
+    every sequence for this bf16 / scalar-gate / d = 128 workload) so copies of one part overlap
+    the prefill of another."""
     import torch
 
     import gated_delta_rule_14_gb300 as kla
@@ -406,7 +407,6 @@ def e2e_prefill(res, steps, warmup, dev, stream, parts=8):
     ST_h = torch.empty(res["ST"].shape, dtype=res["ST"].dtype, pin_memory=True)
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = o_h.numel() * o_h.element_size() + ST_h.numel() * ST_h.element_size()
-    parts = min(parts, wl.B)
 
     def step():
         kla.chunk_fwd_host(host["q"], host["k"], host["v"], host["alpha"], host["eta"], wl.eps, chunk=wl.chunk,

@@ -140,8 +140,10 @@ def chunk_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, alpha: tor
                    parts: Optional[int] = None, out: Optional[torch.Tensor] = None, S_T: Optional[torch.Tensor] = None,
                    final_state: bool = True, device=None, buffers: Optional[dict] = None, beta_mode: str = "kla",
                    q_scale: float = 1.0) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
-    """Chunkwise prefill of HOST tensors (pin them for overlap): the batch runs in ``parts`` parts
-    whose host->device copies, prefills and device->host copies overlap (kla_chunk_fwd_host).
+    """Chunkwise prefill of HOST tensors (pin them for overlap): the work runs in ``parts`` parts
+    whose host->device copies, prefills and device->host copies overlap (kla_chunk_fwd_host):
+    time slices of whole chunks for bf16 with the scalar gate and d = 128 (up to 64 parts, at most
+    one per chunk), ranges of whole sequences otherwise (up to min(B, 64) parts).
 
     Same shapes as ``chunk_fwd``; ``out`` / ``S_T`` are host tensors (pinned ones are allocated
     when None). ``buffers`` (from ``host_buffers``) holds the device tensors, reused across calls.

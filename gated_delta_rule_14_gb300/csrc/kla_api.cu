@@ -183,6 +183,20 @@ kla_status kla::chunk_fwd_nosplit(const void *q, const void *k, const void *v, c
                           q_scale, workspace, workspace_bytes, stream, 1);
 }
 
+kla_status kla::chunk_fwd_slice(const void *q, const void *k, const void *v, const float *alpha, const float *eta,
+                                float eps, const float *S0, void *o, float *S_T, int B, int T, int T_stride, int H,
+                                kla_beta_mode beta_mode, float q_scale, void *stream) {
+    if (T < 1 || T_stride < T) return KLA_ERR_INVALID_ARG;
+    kla::ChunkArgs a{q, k, v, alpha, eta, eps, S0, o, S_T, B, T, H, 128, 128, 64, KLA_DTYPE_BF16, KLA_GATE_SCALAR,
+                     nullptr, 0, nullptr, static_cast<cudaStream_t>(stream)};
+    a.beta_raw = beta_mode == KLA_BETA_RAW;
+    a.q_scale = q_scale;
+    a.no_segments = 1;
+    a.T_stride = T_stride;
+    if (err_word(&a.err) != cudaSuccess) return KLA_ERR_CUDA;
+    return kla::launch_chunk_tc(a) == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
+}
+
 extern "C" {
 
 kla_status kla_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *alpha, const float *eta,

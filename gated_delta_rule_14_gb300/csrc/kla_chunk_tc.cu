@@ -152,6 +152,7 @@ struct TcParams {
     int beta_raw;  // 1: beta = eta
     float q_scale; // o = S^T (q_scale q)
     const unsigned *rescue;   // per-channel gate: [B*H] marks of chains rerun exactly (skipped here), or NULL
+    int Ts;                   // tokens between sequences in alpha and eta (T, or more for a slice)
 };
 
 __device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x << 16); }
@@ -299,7 +300,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int u = 0; u < 2; ++u) {
                 const int t = t_begin + c * kC + 2 * lane + u;
                 const bool ok = t < t_end;
-                const size_t tok = (static_cast<size_t>(b) * p.T + t) * p.H + h;
+                const size_t tok = (static_cast<size_t>(b) * p.Ts + t) * p.H + h;
                 a_nx[u] = (ok && !kCh) ? p.alpha[tok] : 1.f;
                 e_nx[u] = ok ? p.eta[tok] : 0.f;
             }
@@ -355,7 +356,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 // the 4 tokens are consecutive rows: one base address and a row stride (tokens past
                 // the end reread the last row)
                 const int t = t_begin + c * kC + 32 * cth + 4 * csb, tl = min(t, t_end - 1);
-                const float *g0 = p.alpha + ((static_cast<size_t>(b) * p.T + tl) * p.H + h) * kD + 8 * ccg;
+                const float *g0 = p.alpha + ((static_cast<size_t>(b) * p.Ts + tl) * p.H + h) * kD + 8 * ccg;
                 const size_t rs = static_cast<size_t>(p.H) * kD;
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
@@ -1073,14 +1074,15 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [B, T, H, 128] bf16 tensor; box = 64 channels x 64 tokens of one (b, h).
-bool make_map(CUtensorMap *m, const void *base, int B, int T, int H, bool swizzle) {
+// [B, T, H, 128] bf16 tensor (sequences Ts >= T tokens apart: a T-token slice of longer ones);
+// box = 64 channels x 64 tokens of one (b, h).
+bool make_map(CUtensorMap *m, const void *base, int B, int T, int H, bool swizzle, int Ts) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T),
                                 static_cast<cuuint64_t>(B)};
     const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(H) * kD * 2,
-                                   static_cast<cuuint64_t>(T) * H * kD * 2};
+                                   static_cast<cuuint64_t>(Ts) * H * kD * 2};
     const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kC), 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
@@ -1178,8 +1180,12 @@ bool chunk_tc_supports(const ChunkArgs &a) {
 
 cudaError_t launch_chunk_tc(const ChunkArgs &a) {
     CUtensorMap mq, mk, mv, mo;
-    if (!make_map(&mq, a.q, a.B, a.T, a.H, true) || !make_map(&mk, a.k, a.B, a.T, a.H, true) ||
-        !make_map(&mv, a.v, a.B, a.T, a.H, true) || !make_map(&mo, a.o, a.B, a.T, a.H, false))
+    const int Ts = a.T_stride > 0 ? a.T_stride : a.T;
+    // a slice of longer sequences: scalar gate, one segment (the range check, the rerun and the
+    // segment plan index whole sequences)
+    if (Ts != a.T && (Ts < a.T || a.gate != KLA_GATE_SCALAR || !a.no_segments)) return cudaErrorInvalidValue;
+    if (!make_map(&mq, a.q, a.B, a.T, a.H, true, Ts) || !make_map(&mk, a.k, a.B, a.T, a.H, true, Ts) ||
+        !make_map(&mv, a.v, a.B, a.T, a.H, true, Ts) || !make_map(&mo, a.o, a.B, a.T, a.H, false, Ts))
         return cudaErrorInvalidValue;
     auto kern = a.gate == KLA_GATE_CHANNEL ? chunk_tc_kernel<true> : chunk_tc_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1197,7 +1203,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a) {
         if ((e = launch_gate_range(a.alpha, a.B, a.T, a.H, flags, a.stream)) != cudaSuccess) return e;
     }
     TcParams p{a.alpha, a.eta, a.eps, a.S0, a.S_T, a.B, a.T, a.H, pl.seg_len, 0, 1, pl.nseg,
-               kS0Chain, kSTLast, 0, 0, a.err, a.beta_raw, a.q_scale, flags};
+               kS0Chain, kSTLast, 0, 0, a.err, a.beta_raw, a.q_scale, flags, Ts};
     if (pl.nseg <= 1) {
         kern<<<chains, kThreads, SMEM_BYTES, a.stream>>>(mq, mk, mv, mo, p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;

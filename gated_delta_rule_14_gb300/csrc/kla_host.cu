@@ -1,18 +1,26 @@
 // kla_host.cu -- prefill from and to host memory with the copies overlapped with the kernels.
 //
-// kla_chunk_fwd_host splits the batch into parts along B (contiguous in every tensor) and runs,
-// for part i: the host-to-device copies of its inputs on an upload stream, the prefill on one of
+// kla_chunk_fwd_host splits the work into parts and runs, for part i: the host-to-device copies of its inputs on an upload stream, the prefill on one of
 // several compute streams once those copies have landed, and the device-to-host copies of its
 // outputs on a download stream once the prefill is done (two streams per direction, parts
 // alternating, so two copies of a direction can be in flight). Copies of part i+1 overlap the
-// prefill of part i, and the two directions of the link overlap each other; prefills of
-// different parts may run at the same time on different SMs. Parts run whole sequences (the
-// sequence-parallel segments would only add work next to other parts), except the last one:
+// prefill of part i, and the two directions of the link overlap each other.
+//
+// Time parts (bf16, scalar gate, d_k = d_v = 128, chunk 64, at least one chunk per part): part i
+// is a slice of 64-token chunks of every sequence (small slices first and last, large ones in
+// between), copied with strided (2-D) copies; the slices
+// run in order on one compute stream with the state carried in place between them (in S_T_d, or
+// in the fixed scratch array of kla_chunk_fwd_noalloc when no final state is wanted), each on
+// all (sequence, head) chains at once. The first upload and the last prefill and download, which
+// nothing overlaps, are then a part's share of the copies and a few chunk steps.
+//
+// Batch parts (every other call): part i is a range of whole sequences (contiguous in every
+// tensor); prefills of different parts may run at the same time on different SMs. The
+// sequence-parallel segments would only add work next to other parts, except in the last part:
 // nothing runs beside it but the remaining copies, and its prefill plus its download are the
-// call's tail, so it takes the segments when they shorten it, with the fixed scratch array of
-// kla_chunk_fwd_noalloc (the last parts of consecutive calls are ordered on it by an event).
-// With the per-channel gate, the other parts' rerun marks live in the array's last MiB, one
-// slot per compute stream.
+// call's tail, so it takes the segments when they shorten it, with the fixed scratch array (the
+// last parts of consecutive calls are ordered on it by an event). With the per-channel gate, the
+// other parts' rerun marks live in the array's last MiB, one slot per compute stream.
 //
 // Streams and events are created once per device on the first call and kept for the life of
 // the process. Calls are ordered after earlier work on the caller's stream and the caller's
@@ -82,7 +90,12 @@ extern "C" kla_status kla_chunk_fwd_host(const void *q_h, const void *k_h, const
                                          float *S_T_d, float eps, int B, int T, int H, int d_k, int d_v, int chunk,
                                          kla_dtype dtype, kla_gate gate, kla_beta_mode beta_mode, float q_scale,
                                          int parts, void *stream) {
-    if (B < 1 || T < 1 || H < 1 || parts < 1 || parts > std::min(B, kMaxParts)) return KLA_ERR_INVALID_ARG;
+    const bool time_parts = dtype == KLA_DTYPE_BF16 && gate == KLA_GATE_SCALAR && d_k == 128 && d_v == 128 &&
+                            chunk == 64 && T > 16 && parts >= 1 && parts <= T / 64 &&
+                            (S_T_d || static_cast<size_t>(B) * H * d_k * d_v * 4 <=
+                                          static_cast<size_t>(KLA_NOALLOC_SCRATCH_BYTES) - kFlagTail);
+    if (B < 1 || T < 1 || H < 1 || parts < 1 || parts > (time_parts ? kMaxParts : std::min(B, kMaxParts)))
+        return KLA_ERR_INVALID_ARG;
     if (!q_h || !k_h || !v_h || !alpha_h || !eta_h || !o_h || !q_d || !k_d || !v_d || !alpha_d || !eta_d || !o_d)
         return KLA_ERR_INVALID_ARG;
     if ((S0_h != nullptr) != (S0_d != nullptr) || (S_T_h != nullptr) != (S_T_d != nullptr)) return KLA_ERR_INVALID_ARG;
@@ -115,7 +128,60 @@ extern "C" kla_status kla_chunk_fwd_host(const void *q_h, const void *k_h, const
     kla_status st = KLA_OK;
     void *scratch = nullptr;   // device address of the fixed scratch array
     if (ok && kla::noalloc_scratch(&scratch) != cudaSuccess) ok = false;
-    for (int i = 0; ok && i < parts; ++i) {
+    if (time_parts && ok) {
+        st = kla::check_chunk_fwd(q_d, k_d, v_d, alpha_d, eta_d, eps, S0_d, o_d, S_T_d, B, T, H, d_k, d_v, chunk, dtype,
+                                  gate, beta_mode, q_scale);
+        // Slice sizes follow a triangle (weights 1, 2, .., 2, 1): the first upload and the last
+        // prefill and download, which nothing overlaps, are a small slice each while the copies of
+        // the large middle slices overlap the link's other direction and the prefills. Slice i
+        // covers chunks [cb[i], cb[i + 1]), at least one each.
+        const int nchunks = (T + 63) / 64;
+        int cb[kMaxParts + 1];
+        {
+            long wsum = 0;
+            for (int i = 0; i < parts; ++i) wsum += std::min(i + 1, parts - i);
+            long acc = 0;
+            cb[0] = 0;
+            for (int i = 0; i < parts; ++i) {
+                acc += std::min(i + 1, parts - i);
+                const int want = static_cast<int>((acc * nchunks + wsum / 2) / wsum);
+                cb[i + 1] = std::min(std::max(want, cb[i] + 1), nchunks - (parts - 1 - i));
+            }
+        }
+        float *state = S_T_d ? S_T_d : static_cast<float *>(scratch);
+        cudaStream_t comp = P.comp[0];
+        if (st == KLA_OK && !S_T_d && cudaStreamWaitEvent(comp, P.scratch_free, 0) != cudaSuccess) st = KLA_ERR_CUDA;
+        const size_t qrow = static_cast<size_t>(H) * d_k * esz, vrow = static_cast<size_t>(H) * d_v * esz,
+                     arow = static_cast<size_t>(H) * 4;   // bytes per token of every sequence
+        cudaStream_t down = P.d2h[0];
+        for (int i = 0; st == KLA_OK && ok && i < parts; ++i) {
+            const int t0 = 64 * cb[i], nt = std::min(T, 64 * cb[i + 1]) - t0;
+            cudaStream_t up = P.h2d[i % kCopyStreams];
+            down = P.d2h[i % kCopyStreams];
+            auto in2d = [&](void *dst, const void *src, size_t row) {   // tokens [t0, t0 + nt) of every sequence
+                return cudaMemcpy2DAsync(atw(dst, t0 * row), T * row, at(src, t0 * row), T * row, nt * row, B, H2D,
+                                         up) == cudaSuccess;
+            };
+            ok = in2d(q_d, q_h, qrow) && in2d(k_d, k_h, qrow) && in2d(v_d, v_h, vrow) && in2d(alpha_d, alpha_h, arow) &&
+                 in2d(eta_d, eta_h, arow) &&
+                 (i > 0 || !S0_h || cudaMemcpyAsync(S0_d, S0_h, B * s_b, H2D, up) == cudaSuccess) &&
+                 cudaEventRecord(P.in_done[i], up) == cudaSuccess && cudaStreamWaitEvent(comp, P.in_done[i], 0) == cudaSuccess;
+            if (!ok) break;
+            st = kla::chunk_fwd_slice(at(q_d, t0 * qrow), at(k_d, t0 * qrow), at(v_d, t0 * vrow),
+                                      reinterpret_cast<const float *>(at(alpha_d, t0 * arow)),
+                                      reinterpret_cast<const float *>(at(eta_d, t0 * arow)), eps, i == 0 ? S0_d : state,
+                                      atw(o_d, t0 * vrow), state, B, nt, T, H, beta_mode, q_scale, comp);
+            if (st != KLA_OK) break;
+            ok = cudaEventRecord(P.out_ready[i], comp) == cudaSuccess &&
+                 cudaStreamWaitEvent(down, P.out_ready[i], 0) == cudaSuccess &&
+                 cudaMemcpy2DAsync(atw(o_h, t0 * vrow), T * vrow, at(o_d, t0 * vrow), T * vrow, nt * vrow, B, D2H,
+                                   down) == cudaSuccess;
+        }
+        if (st == KLA_OK && ok && S_T_h) ok = cudaMemcpyAsync(S_T_h, S_T_d, B * s_b, D2H, down) == cudaSuccess;
+        // recorded even after a failure part-way: the next user of the array waits for what was enqueued
+        if (!S_T_d && cudaEventRecord(P.scratch_free, comp) != cudaSuccess) ok = false;
+    }
+    for (int i = 0; !time_parts && ok && i < parts; ++i) {
         const int b0 = i * bp, nb = std::min(bp, B - b0);
         if (nb <= 0) break;
         cudaStream_t up = P.h2d[i % kCopyStreams], down = P.d2h[i % kCopyStreams];

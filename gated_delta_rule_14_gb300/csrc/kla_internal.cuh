@@ -34,6 +34,8 @@ struct ChunkArgs {
     float q_scale;         // o = S^T (q_scale q)
     int no_segments;       // 1: never split long sequences into parallel segments
     const unsigned *only;  // recurrent path: when set, only chains (b, h) with only[b * H + h] != 0 run
+    int T_stride;          // tensor-core path, scalar gate: tokens between sequences in q/k/v/o/alpha/eta
+                           // (0: T); a T-token slice of longer sequences when larger than T
 };
 
 struct DecodeArgs {
@@ -76,6 +78,14 @@ kla_status chunk_fwd_nosplit(const void *q, const void *k, const void *v, const 
                              float eps, const float *S0, void *o, float *S_T, int B, int T, int H, int d_k, int d_v,
                              int chunk, kla_dtype dtype, kla_gate gate, kla_beta_mode beta_mode, float q_scale,
                              void *workspace, size_t workspace_bytes, void *stream);
+
+// The tensor-core prefill of tokens [t0, t0 + T) of every sequence (bf16, scalar gate, d_k = d_v = 128,
+// chunk 64, no segments): q, k, v, o, alpha and eta point at token t0 of sequence 0 and successive
+// sequences are T_stride tokens apart. The caller has validated the whole tensors; t0 is a
+// multiple of 64, so the state carried from the previous slice enters at a chunk boundary.
+kla_status chunk_fwd_slice(const void *q, const void *k, const void *v, const float *alpha, const float *eta,
+                           float eps, const float *S0, void *o, float *S_T, int B, int T, int T_stride, int H,
+                           kla_beta_mode beta_mode, float q_scale, void *stream);
 
 // Every argument check of kla_chunk_fwd_ex except the workspace's (its errors, in its order).
 kla_status check_chunk_fwd(const void *q, const void *k, const void *v, const float *alpha, const float *eta,

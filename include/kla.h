@@ -177,10 +177,10 @@ kla_status kla_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
 
 /*
  * kla_chunk_fwd_ex from and to HOST memory, with the copies overlapped with the kernels: the
- * batch is split into `parts` parts along B; part i's inputs go host -> device on one copy
- * stream, its prefill runs on one of several compute streams once they have landed, and its
- * outputs go device -> host on a second copy stream, so part i+1's copies overlap part i's
- * prefill and both directions of the link are busy at once. The pages have no counterpart: it
+ * work is split into `parts` parts; part i's inputs go host -> device on one copy stream, its
+ * prefill runs on a compute stream once they have landed, and its outputs go device -> host on a
+ * second copy stream, so part i+1's copies overlap part i's prefill and both directions of the
+ * link are busy at once. The pages have no counterpart: it
  * is the host-buffer form of kla_chunk_fwd_ex for callers whose tensors live in host memory.
  *   q_h .. S_T_h  host tensors in the layouts of kla_chunk_fwd; pinned (page-locked) memory is
  *                 needed for the copies to overlap anything (pageable memory still works, with
@@ -188,8 +188,14 @@ kla_status kla_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
  *   q_d .. S_T_d  device buffers of the same sizes, owned by the caller (S0_d / S_T_d NULL
  *                 exactly when S0_h / S_T_h are); their contents after the call are unspecified
  *                 except o_d and S_T_d, which hold the results
- *   parts         1 .. min(B, 64)
- * Parts run whole sequences, except the last part when the sequence-parallel segments of
+ *   parts         time parts: 1 .. min(64, T / 64); batch parts: 1 .. min(B, 64)
+ * Time parts (bf16, scalar gate, d_k = d_v = 128, chunk 64, and parts <= T / 64; without a final
+ * state also B * H * 64 KB <= 23 MiB): part i is the same slice of whole 64-token chunks of every
+ * sequence (the last slice takes the remainder), copied with strided copies; the slices run in
+ * order on one compute stream with the state carried between them in fp32, in S_T_d or, when no
+ * final state is wanted, in the fixed array of kla_chunk_fwd_noalloc (ordered by the same event as
+ * below); the results equal kla_chunk_fwd's bit for bit. Every other call takes batch parts.
+ * Batch parts run whole sequences, except the last part when the sequence-parallel segments of
  * kla_chunk_fwd shorten it (long sequences, few chains per part): it then takes its scratch
  * from the fixed array of kla_chunk_fwd_noalloc (no allocation). With the per-channel gate,
  * every part's rerun marks (see kla_chunk_fwd) live in that array too: up to 32768 chains per

@@ -1,8 +1,10 @@
-"""Prefill of host tensors (kla_chunk_fwd_host): the batch split into parts whose copies and
-kernels overlap must give exactly what kla_chunk_fwd gives on device copies of the same inputs
-(each part runs whole sequences through the same kernels), for any part count, with or without
-an initial and a final state. The last part of a batch of long sequences runs the
-sequence-parallel segments instead; it is checked against the oracle."""
+"""Prefill of host tensors (kla_chunk_fwd_host): the work split into parts whose copies and
+kernels overlap must give exactly what kla_chunk_fwd gives on device copies of the same inputs,
+for any part count, with or without an initial and a final state. bf16 calls with the scalar gate
+and d = 128 split along time (slices of whole chunks, the state carried in fp32 between them);
+the others split the batch (whole sequences through the same kernels). The last part of a batch
+of long sequences runs the sequence-parallel segments instead; it is checked against the
+oracle."""
 import numpy as np
 import pytest
 import torch
@@ -62,17 +64,17 @@ def test_host_prefill_without_final_state_and_bad_parts():
 
 
 def test_host_prefill_segments_the_last_part():
-    """Parts of one sequence of 4096 tokens (16 chains of 64 chunks): the last part, the call's
-    tail, runs the sequence-parallel segments on the library's fixed scratch. A second call (one
-    part, so its prefill runs on another of the library's compute streams) is issued from another
-    stream while the first may still run: the two share the scratch, ordered by the library's
-    event. Both match the oracle on sampled chains; repeating the first call reproduces it bit
-    for bit."""
+    """Batch parts of one sequence of 4096 tokens (16 chains of 64 chunks, per-channel gate): the
+    last part, the call's tail, runs the sequence-parallel segments on the library's fixed
+    scratch. A second call (one part, so its prefill runs on another of the library's compute
+    streams) is issued from another stream while the first may still run: the two share the
+    scratch, ordered by the library's event. Both match the oracle on sampled chains; repeating
+    the first call reproduces it bit for bit."""
     import gated_delta_rule_14_gb300 as kla
     lib = kla._native.lib()
     torch.cuda.set_device(DEV)
-    assert lib.kla_chunk_fwd_workspace_size(1, 4096, 16, 128, 128, 64, 1, 0) > 0   # segments pay off here
-    inp = synth.make_prefill("gdn4k", seed=41, B=2, T=4096, H=16, s0_sigma=0.05)
+    assert lib.kla_chunk_fwd_workspace_size(1, 4096, 16, 128, 128, 64, 1, 1) > 4 * 16   # segments pay off here
+    inp = synth.make_prefill("kda8k", seed=41, B=2, T=4096, H=16, s0_sigma=0.05)
     args = [host(x) for x in (inp.q, inp.k, inp.v, inp.alpha, inp.eta)]
     S0 = host(inp.S0)
     o1, s1 = kla.chunk_fwd_host(*args, inp.wl.eps, S0, parts=2, device=DEV)
@@ -111,3 +113,23 @@ def test_host_prefill_reruns_out_of_range_channel_gates(parts):
     o_g = np.stack([o_h.float().numpy()[b, :, h] for b, h in chains])
     s_g = np.stack([s_h.numpy()[b, h] for b, h in chains])
     assert oracle.rel_l2(o_g, o_ref) <= 1e-2 and oracle.rel_l2(s_g, s_ref) <= 1e-2
+
+
+@pytest.mark.parametrize("parts,final", [(5, True), (16, False), (1, False)])
+def test_host_prefill_time_parts(parts, final):
+    """Time parts (bf16, scalar gate, d = 128): slices of whole chunks of every sequence, the last
+    one ragged; the state carried between slices in S_T, or, without a final state, in the
+    library's fixed scratch (two calls back to back share it). Equal bit for bit to kla_chunk_fwd
+    on device copies, whose kernel keeps the state in fp32 as the slices do."""
+    import gated_delta_rule_14_gb300 as kla
+    inp = synth.make_prefill("gdn4k", seed=60 + parts, B=3, T=1100, H=2, s0_sigma=0.05)
+    dev_args = [to_dev(x) for x in (inp.q, inp.k, inp.v, inp.alpha, inp.eta)]
+    o_d, s_d = kla.chunk_fwd(*dev_args, inp.wl.eps, to_dev(inp.S0))
+    args = [host(x) for x in (inp.q, inp.k, inp.v, inp.alpha, inp.eta)]
+    outs = [kla.chunk_fwd_host(*args, inp.wl.eps, host(inp.S0), parts=parts, final_state=final, device=DEV)
+            for _ in range(2)]
+    torch.cuda.synchronize(DEV)
+    kla.device_status(DEV)
+    for o_h, s_h in outs:
+        assert torch.equal(o_h, o_d.cpu())
+        assert (s_h is None) if not final else torch.equal(s_h, s_d.cpu())
