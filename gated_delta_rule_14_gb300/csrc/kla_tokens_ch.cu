@@ -171,23 +171,41 @@ __global__ void __launch_bounds__(tch::kThreads, 2) tokens_ch_kernel(const TokCh
                 const float2 qi23 = unpack2(*reinterpret_cast<const uint32_t *>(sq + i * tch::kPb + c0 + 2));
                 const float4 Gi = *reinterpret_cast<const float4 *>(sG + i * DK + c0);
                 const float bi = sbeta[i];
-                for (int m = 0; m <= i; ++m) {
-                    const float2 km01 = unpack2(*reinterpret_cast<const uint32_t *>(sk + m * tch::kPb + c0));
-                    const float2 km23 = unpack2(*reinterpret_cast<const uint32_t *>(sk + m * tch::kPb + c0 + 2));
-                    const float4 Gm = *reinterpret_cast<const float4 *>(sG + m * DK + c0);
-                    const float d0 = __expf(Gi.x - Gm.x), d1 = __expf(Gi.y - Gm.y), d2 = __expf(Gi.z - Gm.z),
-                                d3 = __expf(Gi.w - Gm.w);
-                    const float w0 = km01.x * d0, w1 = km01.y * d1, w2 = km23.x * d2, w3 = km23.y * d3;
-                    float r = ki01.x * w0 + ki01.y * w1 + ki23.x * w2 + ki23.y * w3;
-                    float a = qi01.x * w0 + qi01.y * w1 + qi23.x * w2 + qi23.y * w3;
+                constexpr int kGrp = 2;
+                // columns m <= i in groups of kGrp: the 2 kGrp reductions of a group run level by level
+                // together, so a group costs one chain of five shuffle latencies (columns past i are
+                // rows of zeros' worth of work and are not stored)
+                for (int m0 = 0; m0 <= i; m0 += kGrp) {
+                    float r[kGrp], a[kGrp];
+#pragma unroll
+                    for (int u = 0; u < kGrp; ++u) {
+                        const int m = min(m0 + u, 15);
+                        const float2 km01 = unpack2(*reinterpret_cast<const uint32_t *>(sk + m * tch::kPb + c0));
+                        const float2 km23 = unpack2(*reinterpret_cast<const uint32_t *>(sk + m * tch::kPb + c0 + 2));
+                        const float4 Gm = *reinterpret_cast<const float4 *>(sG + m * DK + c0);
+                        const float d0 = __expf(Gi.x - Gm.x), d1 = __expf(Gi.y - Gm.y), d2 = __expf(Gi.z - Gm.z),
+                                    d3 = __expf(Gi.w - Gm.w);
+                        const float w0 = km01.x * d0, w1 = km01.y * d1, w2 = km23.x * d2, w3 = km23.y * d3;
+                        r[u] = ki01.x * w0 + ki01.y * w1 + ki23.x * w2 + ki23.y * w3;
+                        a[u] = qi01.x * w0 + qi01.y * w1 + qi23.x * w2 + qi23.y * w3;
+                    }
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) {
-                        r += __shfl_xor_sync(full, r, o);
-                        a += __shfl_xor_sync(full, a, o);
+#pragma unroll
+                        for (int u = 0; u < kGrp; ++u) {
+                            r[u] += __shfl_xor_sync(full, r[u], o);
+                            a[u] += __shfl_xor_sync(full, a[u], o);
+                        }
                     }
                     if (lane == 0) {
-                        sR[i * MP + m] = m < i ? bi * r : 0.f;
-                        sAm[i * MP + m] = a;
+#pragma unroll
+                        for (int u = 0; u < kGrp; ++u) {
+                            const int m = m0 + u;
+                            if (m <= i) {
+                                sR[i * MP + m] = m < i ? bi * r[u] : 0.f;
+                                sAm[i * MP + m] = a[u];
+                            }
+                        }
                     }
                 }
                 if (lane < 16 - (i + 1)) {   // the upper triangle is zero
