@@ -11,9 +11,11 @@
 //   O    = s ((Q . e^G) S + A E)
 //   S'   = diag(e^{G_end}) S + (K . e^{G_end - G})^T E
 // where (X . e^G) scales element [t][k] of X by e^{G_t[k]} and diag(e^{G_end}) scales the state's
-// key rows. R and A are formed exactly on the CUDA cores: e^{G_i[k] - G_m[k]} <= 1 for m <= i, so
-// no factor can overflow whatever the gates (a factorisation around a reference token, as on
-// the 64-token chunk path, would bound the gates' range). The contractions with the state run
+// key rows. No factor may overflow whatever the gates: the two 8 x 8 diagonal blocks of R and A
+// are formed exactly on the CUDA cores (e^{G_i[k] - G_m[k]} <= 1 for m <= i), and the block of
+// rows 8-15 and columns 0-7 is factorised around token 8, where both factors e^{G_i - G_8} and
+// e^{G_8 - G_m} are at most 1 (a single reference token for the whole call, as on the 64-token
+// chunk path, would bound the gates' range). The contractions with the state and that block run
 // on warp-level bf16 tensor cores with fp32 accumulation, the small T x T ones in tf32.
 //
 // One CTA of 256 threads per head at a time (persistent over heads; two CTAs per SM, so one
@@ -158,13 +160,65 @@ __global__ void __launch_bounds__(tch::kThreads, 2) tokens_ch_kernel(const TokCh
         }
         __syncthreads();   // (B) G, e^{G_end} and beta visible
 
-        // (2) R and A exactly: warp w takes rows w and 15 - w (17 pairs), lane = 4 key channels;
-        // K . e^{G_end - G} from the raw keys meanwhile
+        // (2) R and A. Block (rows 8-15, columns 0-7) factorises around token 8 with both factors at
+        // most 1 (m < 8 <= i: e^{G_i - G_8} and e^{G_8 - G_m}, so nothing overflows and an underflow
+        // only loses a term below e^-87): one warp MMA over [K_hi; Q_hi] e^{G - G_8} and
+        // K_lo e^{G_8 - G}, in bf16 like the contractions with the state. The two 8 x 8 diagonal
+        // blocks are formed exactly per channel: warp w takes rows w and 15 - w (9 entries), lane =
+        // 4 key channels. K . e^{G_end - G} from the raw keys meanwhile.
+        bf16 *sHi = sEc;                                 // [K_hi; Q_hi] e^{G - G_8}: 16 rows
+        bf16 *sLo = reinterpret_cast<bf16 *>(sE);        // K_lo e^{G_8 - G}: rows 0-7 (8-15 zero)
         {
+            const int t = tid >> 4, cc = 8 * (tid & 15);   // row t of [K_hi; Q_hi], 8 channels
+            const int i = 8 + (t & 7);
+            const uint4 x = *reinterpret_cast<const uint4 *>((t < 8 ? sk : sq) + i * tch::kPb + cc);
+            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+            uint32_t o4[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 f = unpack2(w[u]);
+                const int k0 = cc + 2 * u;
+                o4[u] = pack2(f.x * __expf(sG[i * DK + k0] - sG[8 * DK + k0]),
+                              f.y * __expf(sG[i * DK + k0 + 1] - sG[8 * DK + k0 + 1]));
+            }
+            *reinterpret_cast<uint4 *>(sHi + t * tch::kPb + cc) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+            if (t < 8) {
+                const uint4 y = *reinterpret_cast<const uint4 *>(sk + t * tch::kPb + cc);
+                const uint32_t wy[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float2 f = unpack2(wy[u]);
+                    const int k0 = cc + 2 * u;
+                    o4[u] = pack2(f.x * __expf(sG[8 * DK + k0] - sG[t * DK + k0]),
+                                  f.y * __expf(sG[8 * DK + k0 + 1] - sG[t * DK + k0 + 1]));
+                }
+                *reinterpret_cast<uint4 *>(sLo + t * tch::kPb + cc) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+            } else {
+                *reinterpret_cast<uint4 *>(sLo + t * tch::kPb + cc) = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        __syncthreads();
+        {
+            if (warp == 7) {   // the off-diagonal block on the tensor cores
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < DK / 16; ++ks) {
+                    uint32_t a[4], bb[4];
+                    frag_a_rk(sptr(sHi), tch::kPb, 0, 16 * ks, lane, a);
+                    frag_b_rk(sptr(sLo), tch::kPb, 0, 16 * ks, lane, bb);
+                    mma(acc, a, bb[0], bb[1]);
+                }
+                const int i = 8 + g, m = 2 * q4;
+                const float bi = sbeta[i];
+                sR[i * MP + m] = bi * acc[0];
+                sR[i * MP + m + 1] = bi * acc[1];
+                sAm[i * MP + m] = acc[2];
+                sAm[i * MP + m + 1] = acc[3];
+            }
             const int c0 = 4 * lane;
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
-                const int i = rr ? 15 - warp : warp;
+                const int i = rr ? 15 - warp : warp, mlo = i < 8 ? 0 : 8;
                 const float2 ki01 = unpack2(*reinterpret_cast<const uint32_t *>(sk + i * tch::kPb + c0));
                 const float2 ki23 = unpack2(*reinterpret_cast<const uint32_t *>(sk + i * tch::kPb + c0 + 2));
                 const float2 qi01 = unpack2(*reinterpret_cast<const uint32_t *>(sq + i * tch::kPb + c0));
@@ -172,10 +226,9 @@ __global__ void __launch_bounds__(tch::kThreads, 2) tokens_ch_kernel(const TokCh
                 const float4 Gi = *reinterpret_cast<const float4 *>(sG + i * DK + c0);
                 const float bi = sbeta[i];
                 constexpr int kGrp = 2;
-                // columns m <= i in groups of kGrp: the 2 kGrp reductions of a group run level by level
-                // together, so a group costs one chain of five shuffle latencies (columns past i are
-                // rows of zeros' worth of work and are not stored)
-                for (int m0 = 0; m0 <= i; m0 += kGrp) {
+                // columns mlo <= m <= i in groups of kGrp: the 2 kGrp reductions of a group run level
+                // by level together, so a group costs one chain of five shuffle latencies
+                for (int m0 = mlo; m0 <= i; m0 += kGrp) {
                     float r[kGrp], a[kGrp];
 #pragma unroll
                     for (int u = 0; u < kGrp; ++u) {
