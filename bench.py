@@ -344,7 +344,7 @@ def bench_verify(ntok, calls, seed, dev, flush, stream, pk, channel=False):
     if ntok < 5:
         kernel = "token loop (tokens_pipe_kernel: 128 x 32 state tiles in registers)"
     elif channel:
-        kernel = "chunk form, per-channel gate (tokens_ch_kernel: one CTA per head, exact in-call products)"
+        kernel = "chunk form, per-channel gate (tokens_ch_kernel: one CTA per head, in-call decay factors <= 1)"
     else:
         kernel = "chunk form (tokens_tc_kernel: one CTA per head, warp-level tensor cores)"
     return {"value": wl.B * ntok / (ms * 1e-3), "unit": "tokens/s", "ms_per_call": ms, "calls": calls,

@@ -112,8 +112,8 @@ typedef enum kla_beta_mode {
  * Calls of 1 to 16 tokens (multi-token decode, speculative verification) ignore `chunk`: bf16
  * with d_k = d_v = 128 runs the call's tokens as one chunk on warp-level tensor cores from 5
  * tokens with the scalar gate and from 9 with the per-channel gate (when alpha is 16-byte
- * aligned; the in-call products are then formed exactly per channel, so any gate in (0, 1] is
- * exact), the state rounded to bf16 as an operand as on the chunkwise path; other calls walk the
+ * aligned; no in-call decay factor exceeds 1, so any gate in (0, 1] gives valid results), the
+ * state rounded to bf16 as an operand as on the chunkwise path; other calls walk the
  * tokens in order on fp32 state tiles. A call's first j outputs are bit-identical to those of a
  * call with only its first j tokens when both token counts fall in the same one of the ranges
  * 1-4, 5-8 and 9-16 (bf16, scalar gate, d = 128), 1-8 and 9-16 (bf16, per-channel gate,
