@@ -62,10 +62,10 @@ DECODE_BYTES_PER_HEAD_STEP = 8 * 128 * 128 + 4 * 2 * 128 + 8
 # reports null.
 TC_SOURCES = ("gated_delta_rule_14_gb300/csrc/kla_chunk_tc.cu", "gated_delta_rule_14_gb300/csrc/sm103_ptx.cuh",
               "gated_delta_rule_14_gb300/csrc/kla_internal.cuh")
-TC_TRAFFIC_GDN4K = {"c7a7056964089d9e": 520.32128e6}
+TC_TRAFFIC_GDN4K = {"064b64879e7b4310": 520.263936e6}
 # sm__pipe_tensor_cycles_active (fraction of elapsed cycles) of the same kernel and capture:
 # the algorithmic TFLOP/s divided by it is the rate of the MMA phases themselves.
-TC_PIPE_ACTIVE_GDN4K = {"c7a7056964089d9e": 0.1313}
+TC_PIPE_ACTIVE_GDN4K = {"064b64879e7b4310": 0.1311}
 
 
 def tc_fingerprint() -> str:
