@@ -83,6 +83,11 @@ bool overlaps(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi; }
 
 }  // namespace
 
+// The error word for launchers below the entry points (the backward's carries).
+namespace kla {
+cudaError_t device_error_word(unsigned **out) { return err_word(out); }
+}  // namespace kla
+
 extern "C" {
 
 int kla_abi_version(void) { return 102; }

@@ -31,16 +31,16 @@
 // Four kernels (one pass over the workspace each way):
 //   bwd_prep_kernel  (chunk-parallel)  gates, [K;Q]K^T, R and A, T by blocked substitution (fp32),
 //                                      W and U; stores G, beta, den, W, U, A and T per chunk;
-//   chunk_scan_kernel<false>           the state carry S_c -> S_{c+1} per chain (fp32 registers),
-//                                      storing S_c and E_c per chunk;
-//   chunk_scan_kernel<true>            the reverse carry dS_{c+1} -> dS_c per chain, storing dS_{c+1}
-//                                      and dE_c per chunk, and dS0;
+//   carry_tc_kernel<false>             the state carry S_c -> S_{c+1} per chain (fp32 registers,
+//                                      tcgen05 products), storing S_c and E_c per chunk;
+//   carry_tc_kernel<true>              the reverse carry dS_{c+1} -> dS_c per chain, storing dS_{c+1}
+//                                      and dE_c per chunk, and dS0 (both in kla_bwd_carry_tc.cu);
 //   bwd_grad_kernel  (chunk-parallel)  every gradient of the chunk's tokens from S_c, dS_{c+1},
 //                                      E_c, dE_c, T and the inputs.
-// Every product is a warp-level bf16 mma.sync (m16n8k16, fp32 accumulate) on 64- or 128-wide
-// tiles staged in shared memory with rows padded by 16 bytes, so that every ldmatrix phase hits
-// 8 distinct bank quads. Operands are bf16 (inputs as stored; derived tiles rounded once); the
-// carried states, the solve and every sum of a gradient are fp32.
+// In the prep and gradient kernels every product is a warp-level bf16 mma.sync (m16n8k16, fp32
+// accumulate) on 64- or 128-wide tiles staged in shared memory with rows padded by 16 bytes, so
+// that every ldmatrix phase hits 8 distinct bank quads. Operands are bf16 (inputs as stored;
+// derived tiles rounded once); the carried states, the solve and every sum of a gradient are fp32.
 #include <algorithm>
 #include <mutex>
 
@@ -232,218 +232,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2) bwd_prep_kernel(PrepParams p)
 }
 
 // ============================================================== kernel 2: the carry across chunks
-// Forward (kRev = false), X = S entering chunk c, c ascending:
-//     E = U - W X;  X <- Gamma X + K^T diag(e_end) E            stores X (bf16) and E per chunk
-// (kCh: the per-key-channel gate, with K e^{G_end - G} and s Q e^{G} read from the prep's records
-// and Gamma = diag(e^{G_end}) applied to the rows of X.)
-// Reverse (kRev = true), X = dS' = dL/d(state leaving chunk c), c descending:
-//     dE = diag(e_end) K X + s A^T dO;  X <- Gamma X + (s diag(gamma) Q)^T dO - W^T dE
-//                                                               stores X (bf16) and dE per chunk
-// One CTA of 16 warps per chain; X (128 x 128 fp32) lives in registers, warp w holding rows
-// 32 (w & 3) and columns 32 (w >> 2) of it; the chunk's tiles for step c +- 1 are fetched by
-// cp.async while step c runs.
-struct ScanParams {
-    const bf16 *q, *k, *dO;
-    const float *X0;      // S0 (forward) or dL/dS_T (reverse): [B,H,128,128] fp32, NULL = zeros
-    float *X_end;         // reverse: dL/dS0 (NULL = not wanted)
-    float q_scale;
-    int B, T, H, nc;
-    Ws ws;
-    // Segments (a long chain split for a sequence-parallel scan; one segment = the whole chain
-    // otherwise). Segment r in processing order covers chunks [s L, min((s + 1) L, nc)) with
-    // s = r (forward) or s = nseg - 1 - r (reverse). A launch runs segments seg_begin ..
-    // seg_begin + seg_count - 1 of every chain, one CTA each.
-    int seg_len, seg_begin, seg_count, nseg;
-    int x0_mode;          // kX0Chain, kX0Identity or kX0Given
-    int drive;            // 0: drop U (forward) or the dO terms (reverse): the linear part only
-    int records;          // per-chunk records (S_c, E_c or dS_{c+1}, dE_c): 0 none, 1 all, 2 segment r = 0 only
-    float *Xseg;          // NULL, or [chains][nseg][128][128]: X at the end of each segment
-    const float *Xst;     // kX0Given: [chains][nseg][128][128] start states
-    const unsigned *skip; // NULL, or [B*H]: chains left to the token-sequential path (their CTAs return)
-};
-enum : int {
-    kX0Chain = 0,      // X0 for the chain's first segment (r = 0), zeros for the others
-    kX0Identity = 1,   // the identity (the segment's transition)
-    kX0Given = 2,      // Xst[chain][r]
-};
-constexpr int kScanThreads = 512;
-constexpr int SC_K = 0, SC_W = SC_K + kTileTok, SC_UQ = SC_W + kTileTok;   // U (forward) or Q (reverse)
-constexpr int SC_DO = SC_UQ + kTileTok, SC_A = SC_DO + kTileTok, SC_CG = SC_A + kTileSq;
-constexpr int SC_STAGE = SC_CG + static_cast<int>(kCgFloats) * 4;
-constexpr int SC_X = 2 * SC_STAGE, SC_M = SC_X + kTileSt;
-constexpr int SC_BYTES = SC_M + kTileTok;
-static_assert(SC_STAGE % 16 == 0 && SC_BYTES <= 232448, "scan shared memory");
-
-template <bool kRev, bool kCh>
-__global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(ScanParams p) {
-    extern __shared__ __align__(16) unsigned char smem[];
-    bf16 *sX = reinterpret_cast<bf16 *>(smem + SC_X), *sM = reinterpret_cast<bf16 *>(smem + SC_M);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g = lane >> 2, q4 = lane & 3;
-    const int bh = blockIdx.x / p.seg_count, r = p.seg_begin + blockIdx.x % p.seg_count;
-    const int b = bh / p.H, h = bh % p.H;
-    if (p.skip && p.skip[bh]) return;
-    const size_t rs = static_cast<size_t>(p.H) * kD;
-    const int sidx = kRev ? p.nseg - 1 - r : r;   // segment index in time
-    const int c_lo = sidx * p.seg_len, c_hi = min((sidx + 1) * p.seg_len, p.nc) - 1;
-    const int steps = c_hi - c_lo + 1;
-    if (steps <= 0) return;
-    const bool rec = p.records == 1 || (p.records == 2 && r == 0);
-
-    auto stage = [&](int buf, int off) { return reinterpret_cast<bf16 *>(smem + buf * SC_STAGE + off); };
-    auto issue = [&](int c, int buf) {
-        const int t0 = c * kC, L = min(kC, p.T - t0);
-        const size_t base = ((static_cast<size_t>(b) * p.T + t0) * p.H + h) * kD;
-        const size_t n = static_cast<size_t>(bh) * p.nc + c;
-        if (kCh) load_dense<kD>(stage(buf, SC_K), p.ws.Ke + n * kC * kD, kC, tid, kScanThreads);
-        else load_tok(stage(buf, SC_K), p.k + base, rs, L, tid, kScanThreads);
-        load_dense<kD>(stage(buf, SC_W), p.ws.W + n * kC * kD, kC, tid, kScanThreads);
-        if (p.drive) {
-            if (kRev) {
-                if (kCh) load_dense<kD>(stage(buf, SC_UQ), p.ws.Qg + n * kC * kD, kC, tid, kScanThreads);
-                else load_tok(stage(buf, SC_UQ), p.q + base, rs, L, tid, kScanThreads);
-                load_tok(stage(buf, SC_DO), p.dO + base, rs, L, tid, kScanThreads);
-                load_dense<kC>(stage(buf, SC_A), p.ws.A + n * kC * kC, kC, tid, kScanThreads);
-            } else {
-                load_dense<kD>(stage(buf, SC_UQ), p.ws.UdE + n * kC * kD, kC, tid, kScanThreads);
-            }
-        }
-        if (kCh) {   // e^{G_end} per key channel
-            if (tid < kD / 4) cp16(smem + buf * SC_STAGE + SC_CG + 16 * tid, p.ws.gend + n * kD + 4 * tid, true);
-        } else if (tid < static_cast<int>(kCgFloats) / 4) {
-            cp16(smem + buf * SC_STAGE + SC_CG + 16 * tid, p.ws.cg + n * kCgFloats + 4 * tid, true);
-        }
-    };
-
-    // X in registers: rows xr0 + 16 mi + g (+8), columns xc0 + 8 ni + 2 q4 (+1)
-    const int xr0 = 32 * (warp & 3), xc0 = 32 * (warp >> 2);
-    float X[2][4][4];
-#pragma unroll
-    for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-        for (int ni = 0; ni < 4; ++ni)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int row = xr0 + 16 * mi + g + 8 * hh, col = xc0 + 8 * ni + 2 * q4;
-                float2 x = make_float2(0.f, 0.f);
-                if (p.x0_mode == kX0Identity) {
-                    x = make_float2(row == col ? 1.f : 0.f, row == col + 1 ? 1.f : 0.f);
-                } else if (p.x0_mode == kX0Given) {
-                    x = *reinterpret_cast<const float2 *>(p.Xst + ((static_cast<size_t>(bh) * p.nseg + r) * kD + row) * kD + col);
-                } else if (p.X0 && r == 0) {
-                    x = *reinterpret_cast<const float2 *>(p.X0 + (static_cast<size_t>(bh) * kD + row) * kD + col);
-                }
-                X[mi][ni][2 * hh] = x.x;
-                X[mi][ni][2 * hh + 1] = x.y;
-            }
-    auto put_x = [&]() {
-#pragma unroll
-        for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-            for (int ni = 0; ni < 4; ++ni)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
-                    st_pair(sX, kP, xr0 + 16 * mi + g + 8 * hh, xc0 + 8 * ni + 2 * q4, X[mi][ni][2 * hh],
-                            X[mi][ni][2 * hh + 1]);
-    };
-    put_x();
-    issue(kRev ? c_hi : c_lo, 0);
-    cp_commit();
-
-    const int m0 = 16 * (warp & 3), n0 = 32 * (warp >> 2);   // this warp's block of the 64 x 128 step
-    for (int it = 0; it < steps; ++it) {
-        const int c = kRev ? c_hi - it : c_lo + it, buf = it & 1;
-        const size_t n = static_cast<size_t>(bh) * p.nc + c;
-        cp_wait<0>();
-        __syncthreads();   // chunk c's tiles and X (bf16) are visible; every read of buf ^ 1 is done
-        if (it + 1 < steps) issue(kRev ? c - 1 : c + 1, buf ^ 1);
-        cp_commit();
-        const float *cg = reinterpret_cast<const float *>(smem + buf * SC_STAGE + SC_CG);
-        const float Gend = kCh ? 0.f : cg[kC - 1], Gam = kCh ? 1.f : __expf(Gend);
-        if (!kCh && kRev && p.drive) {   // Q <- s diag(gamma) Q, in place (read only by the second product)
-            bf16 *sQ = stage(buf, SC_UQ);
-            for (int i = tid; i < kC * 16; i += kScanThreads) {
-                const int tr = i >> 4, cc = (i & 15) * 8;
-                const float f = p.q_scale * __expf(cg[tr]);
-                uint4 u = *reinterpret_cast<uint4 *>(sQ + tr * kP + cc);
-                uint32_t *w = reinterpret_cast<uint32_t *>(&u);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 x = unpack2(w[e]);
-                    w[e] = pack2(f * x.x, f * x.y);
-                }
-                *reinterpret_cast<uint4 *>(sQ + tr * kP + cc) = u;
-            }
-        }
-        if (rec) store_dense<kD>((kRev ? p.ws.dS : p.ws.S) + n * kD * kD, sX, kD, tid, kScanThreads);
-
-        // the 64 x 128 step: E (forward) or dE (reverse)
-        float acc[1][4][4];
-        zero(acc[0]);
-        gemm_m<1, 4, 8, false, true>(acc, sptr(stage(buf, kRev ? SC_K : SC_W)), kP, m0, 0, sptr(sX), kP, n0, 0, lane);
-        float acc2[1][4][4];
-        if (kRev) {
-            zero(acc2[0]);
-            if (p.drive)
-                gemm_m<1, 4, 4, true, true>(acc2, sptr(stage(buf, SC_A)), kPs, m0, 0, sptr(stage(buf, SC_DO)), kP, n0,
-                                            0, lane);
-        }
-        bf16 *Mout = (kRev ? p.ws.dE : p.ws.E) + n * kC * kD;
-        const bf16 *sU = stage(buf, SC_UQ);
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int rw = m0 + g + 8 * hh;
-            const float ee = kCh ? 1.f : __expf(Gend - cg[rw]);   // per-channel gate: in the Ke record
-#pragma unroll
-            for (int ni = 0; ni < 4; ++ni) {
-                const int col = n0 + 8 * ni + 2 * q4;
-                float m0v, m1v;
-                if (kRev) {
-                    m0v = fmaf(ee, acc[0][ni][2 * hh], p.q_scale * acc2[0][ni][2 * hh]);
-                    m1v = fmaf(ee, acc[0][ni][2 * hh + 1], p.q_scale * acc2[0][ni][2 * hh + 1]);
-                } else {
-                    const float2 u = p.drive ? ld_pair(sU, kP, rw, col) : make_float2(0.f, 0.f);
-                    m0v = u.x - acc[0][ni][2 * hh];
-                    m1v = u.y - acc[0][ni][2 * hh + 1];
-                }
-                if (rec) *reinterpret_cast<uint32_t *>(Mout + rw * kD + col) = pack2(m0v, m1v);
-                if (kRev) st_pair(sM, kP, rw, col, -m0v, -m1v);
-                else st_pair(sM, kP, rw, col, ee * m0v, ee * m1v);
-            }
-        }
-        __syncthreads();   // sM and the scaled Q are visible
-
-        // X <- Gamma X + ...  (per-channel gate: row i of X decays by e^{G_end, i})
-#pragma unroll
-        for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-            for (int ni = 0; ni < 4; ++ni)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) X[mi][ni][e] *= kCh ? cg[xr0 + 16 * mi + g + 8 * (e >> 1)] : Gam;
-        if (kRev) {
-            if (p.drive)
-                gemm_m<2, 4, 4, true, true>(X, sptr(stage(buf, SC_UQ)), kP, xr0, 0, sptr(stage(buf, SC_DO)), kP, xc0,
-                                            0, lane);
-            gemm_m<2, 4, 4, true, true>(X, sptr(stage(buf, SC_W)), kP, xr0, 0, sptr(sM), kP, xc0, 0, lane);
-        } else {
-            gemm_m<2, 4, 4, true, true>(X, sptr(stage(buf, SC_K)), kP, xr0, 0, sptr(sM), kP, xc0, 0, lane);
-        }
-        put_x();   // read by the next step after its barrier (every read of sX in this step is done)
-    }
-    // the end state of the segment; in reverse, the segment holding chunk 0 ends in dL/dS0
-    auto put_end = [&](float *dst) {
-#pragma unroll
-        for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-            for (int ni = 0; ni < 4; ++ni)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
-                    *reinterpret_cast<float2 *>(dst + (xr0 + 16 * mi + g + 8 * hh) * kD + xc0 + 8 * ni + 2 * q4) =
-                        make_float2(X[mi][ni][2 * hh], X[mi][ni][2 * hh + 1]);
-    };
-    if (p.Xseg) put_end(p.Xseg + (static_cast<size_t>(bh) * p.nseg + r) * kD * kD);
-    if (kRev && p.X_end && c_lo == 0) put_end(p.X_end + static_cast<size_t>(bh) * kD * kD);
-}
+// The forward carry (X = S entering chunk c, c ascending: E = U - W X, X <- Gamma X +
+// K^T diag(e_end) E, storing X and E per chunk) and the reverse carry (X = dL/d(state leaving
+// chunk c), c descending: dE = diag(e_end) K X + s A^T dO, X <- Gamma X + (s diag(gamma) Q)^T dO
+// - W^T dE, storing X and dE per chunk) run on the tensor cores: launch_carry_tc in
+// kla_bwd_carry_tc.cu.
 
 // ============================================================== kernel 3: gradients of a chunk
 // One CTA of 16 warps per chunk, in two sides that each own one 64 x 128 accumulator in
@@ -953,11 +746,8 @@ cudaError_t launch_bwd_chunk(const BwdArgs &a) {
     const bf16 *q = static_cast<const bf16 *>(a.q), *k = static_cast<const bf16 *>(a.k),
                *v = static_cast<const bf16 *>(a.v), *dO = static_cast<const bf16 *>(a.dO);
     cudaError_t e;
-    auto scan_f = ch ? chunk_scan_kernel<false, true> : chunk_scan_kernel<false, false>;
-    auto scan_r = ch ? chunk_scan_kernel<true, true> : chunk_scan_kernel<true, false>;
-    if ((e = cudaFuncSetAttribute(scan_f, cudaFuncAttributeMaxDynamicSharedMemorySize, SC_BYTES)) ||
-        (e = cudaFuncSetAttribute(scan_r, cudaFuncAttributeMaxDynamicSharedMemorySize, SC_BYTES)))
-        return e;
+    unsigned *err = nullptr;
+    if ((e = device_error_word(&err)) != cudaSuccess) return e;
     const ChBwd cp{q, k, v, dO, a.alpha, a.eta, a.eps, a.q_scale, a.beta_raw, a.B, a.T, a.H, nc, ws, marks,
                    a.dq, a.dk, a.dv, a.dalpha, a.deta};
     if (ch) {
@@ -981,7 +771,7 @@ cudaError_t launch_bwd_chunk(const BwdArgs &a) {
     const bool side_by_side = pl.nseg <= 1 && 2L * chains <= sms && ws.dE != ws.UdE;
     if (side_by_side) {   // both carries in one wave
         ScanParams sf{q, k, dO, a.S0, nullptr, a.q_scale, a.B, a.T, a.H, nc, ws,
-                      pl.seg_len, 0, 1, pl.nseg, kX0Chain, 1, 1, nullptr, nullptr, marks};
+                      pl.seg_len, 0, 1, pl.nseg, kX0Chain, 1, 1, nullptr, nullptr, marks, err};
         ScanParams sr = sf;
         sr.X0 = a.dS_T;
         sr.X_end = a.dS0;
@@ -990,21 +780,21 @@ cudaError_t launch_bwd_chunk(const BwdArgs &a) {
         if ((e = carry_aux(dev, &ax)) != cudaSuccess || (e = cudaEventRecord(ax->fork, a.stream)) != cudaSuccess ||
             (e = cudaStreamWaitEvent(ax->s, ax->fork, 0)) != cudaSuccess)
             return e;
-        scan_r<<<chains, kScanThreads, SC_BYTES, a.stream>>>(sr);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        scan_f<<<chains, kScanThreads, SC_BYTES, ax->s>>>(sf);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = launch_carry_tc(sr, true, ch, chains, a.stream)) != cudaSuccess ||
+            (e = launch_carry_tc(sf, false, ch, chains, ax->s)) != cudaSuccess)
+            return e;
         if ((e = cudaEventRecord(ax->join, ax->s)) != cudaSuccess ||
             (e = cudaStreamWaitEvent(a.stream, ax->join, 0)) != cudaSuccess)
             return e;
     }
     for (int rev = 0; rev < 2 && !side_by_side; ++rev) {
-        auto kern = rev ? scan_r : scan_f;
+        auto kern = [&](const ScanParams &sp, int grid, cudaStream_t st) {
+            return launch_carry_tc(sp, rev != 0, ch, grid, st);
+        };
         ScanParams sp{q, k, dO, rev ? a.dS_T : a.S0, rev ? a.dS0 : nullptr, a.q_scale, a.B, a.T, a.H, nc, ws,
-                      pl.seg_len, 0, 1, pl.nseg, kX0Chain, 1, 1, nullptr, nullptr, marks};
+                      pl.seg_len, 0, 1, pl.nseg, kX0Chain, 1, 1, nullptr, nullptr, marks, err};
         if (pl.nseg <= 1) {
-            kern<<<chains, kScanThreads, SC_BYTES, a.stream>>>(sp);
-            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            if ((e = kern(sp, chains, a.stream)) != cudaSuccess) return e;
             continue;
         }
         float *Z = ws.seg, *M = Z + part, *Sst = M + part;
@@ -1027,22 +817,17 @@ cudaError_t launch_bwd_chunk(const BwdArgs &a) {
         p2.X_end = nullptr;
         const bool one_wave = static_cast<long>(chains) * (p1.seg_count + p2.seg_count) <= sms;
         if (pl.nseg <= 2 || !one_wave) {
-            kern<<<chains * p1.seg_count, kScanThreads, SC_BYTES, a.stream>>>(p1);
-            if ((e = cudaGetLastError()) != cudaSuccess) return e;
-            if (pl.nseg > 2) {
-                kern<<<chains * p2.seg_count, kScanThreads, SC_BYTES, a.stream>>>(p2);
-                if ((e = cudaGetLastError()) != cudaSuccess) return e;
-            }
+            if ((e = kern(p1, chains * p1.seg_count, a.stream)) != cudaSuccess) return e;
+            if (pl.nseg > 2 && (e = kern(p2, chains * p2.seg_count, a.stream)) != cudaSuccess) return e;
         } else {
             std::lock_guard<std::mutex> lock(g_carry_aux_mutex[dev]);
             CarryAux *ax = nullptr;
             if ((e = carry_aux(dev, &ax)) != cudaSuccess || (e = cudaEventRecord(ax->fork, a.stream)) != cudaSuccess ||
                 (e = cudaStreamWaitEvent(ax->s, ax->fork, 0)) != cudaSuccess)
                 return e;
-            kern<<<chains * p1.seg_count, kScanThreads, SC_BYTES, a.stream>>>(p1);
-            if ((e = cudaGetLastError()) != cudaSuccess) return e;
-            kern<<<chains * p2.seg_count, kScanThreads, SC_BYTES, ax->s>>>(p2);
-            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            if ((e = kern(p1, chains * p1.seg_count, a.stream)) != cudaSuccess ||
+                (e = kern(p2, chains * p2.seg_count, ax->s)) != cudaSuccess)
+                return e;
             if ((e = cudaEventRecord(ax->join, ax->s)) != cudaSuccess ||
                 (e = cudaStreamWaitEvent(a.stream, ax->join, 0)) != cudaSuccess)
                 return e;
@@ -1054,8 +839,7 @@ cudaError_t launch_bwd_chunk(const BwdArgs &a) {
         p3.seg_count = pl.nseg - 1;
         p3.x0_mode = kX0Given;
         p3.Xst = Sst;
-        kern<<<chains * p3.seg_count, kScanThreads, SC_BYTES, a.stream>>>(p3);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = kern(p3, chains * p3.seg_count, a.stream)) != cudaSuccess) return e;
     }
     if (ch) {
         // the chunkwise gradients, then the marked chains again on the exact token-sequential path,

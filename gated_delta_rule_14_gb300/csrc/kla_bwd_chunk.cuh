@@ -1,7 +1,8 @@
-// kla_bwd_chunk.cuh -- pieces shared by the chunkwise backward kernels (kla_bwd_chunk.cu: the
-// scalar gate and both chunk-state carries; kla_bwd_chunk_ch.cu: prep and gradients of the
-// per-key-channel gate): the per-chunk workspace records, padded shared-memory tiles, warp-level
-// bf16 MMAs on them, cp.async staging and the 64 x 64 unit-lower inverse.
+// kla_bwd_chunk.cuh -- pieces shared by the chunkwise backward kernels (kla_bwd_chunk.cu: prep and
+// gradients of the scalar gate and the launch sequence; kla_bwd_chunk_ch.cu: prep and gradients of
+// the per-key-channel gate; kla_bwd_carry_tc.cu: both chunk-state carries, on the tensor cores):
+// the per-chunk workspace records, the carries' parameters, padded shared-memory tiles,
+// warp-level bf16 MMAs on them, cp.async staging and the 64 x 64 unit-lower inverse.
 #pragma once
 
 #include "kla_internal.cuh"
@@ -251,6 +252,39 @@ struct ChBwd {
     const unsigned *skip;   // [B*H] chains left to the token-sequential path (their CTAs return at once)
     float *dq, *dk, *dv, *dalpha, *deta;
 };
+// ---- the chunk-state carries (one CTA per chain segment, chunks in order)
+struct ScanParams {
+    const bf16 *q, *k, *dO;
+    const float *X0;      // S0 (forward) or dL/dS_T (reverse): [B,H,128,128] fp32, NULL = zeros
+    float *X_end;         // reverse: dL/dS0 (NULL = not wanted)
+    float q_scale;
+    int B, T, H, nc;
+    Ws ws;
+    // Segments (a long chain split for a sequence-parallel scan; one segment = the whole chain
+    // otherwise). Segment r in processing order covers chunks [s L, min((s + 1) L, nc)) with
+    // s = r (forward) or s = nseg - 1 - r (reverse). A launch runs segments seg_begin ..
+    // seg_begin + seg_count - 1 of every chain, one CTA each.
+    int seg_len, seg_begin, seg_count, nseg;
+    int x0_mode;          // kX0Chain, kX0Identity or kX0Given
+    int drive;            // 0: drop U (forward) or the dO terms (reverse): the linear part only
+    int records;          // per-chunk records (S_c, E_c or dS_{c+1}, dE_c): 0 none, 1 all, 2 segment r = 0 only
+    float *Xseg;          // NULL, or [chains][nseg][128][128]: X at the end of each segment
+    const float *Xst;     // kX0Given: [chains][nseg][128][128] start states
+    const unsigned *skip; // NULL, or [B*H]: chains left to the token-sequential path (their CTAs return)
+    unsigned *err;        // device error word (a bounded wait that gives up sets kErrTimeout)
+};
+enum : int {
+    kX0Chain = 0,      // X0 for the chain's first segment (r = 0), zeros for the others
+    kX0Identity = 1,   // the identity (the segment's transition)
+    kX0Given = 2,      // Xst[chain][r]
+};
+}  // namespace bwdc
+// Device address of the library's error word on the current device.
+cudaError_t device_error_word(unsigned **out);
+namespace bwdc {
+// Runs `grid` CTAs of the forward (rev = false) or reverse carry on the tensor cores.
+cudaError_t launch_carry_tc(const ScanParams &p, bool rev, bool ch, int grid, cudaStream_t stream);
+
 cudaError_t launch_bwd_prep_ch(const ChBwd &p, cudaStream_t stream);
 cudaError_t launch_bwd_grad_ch(const ChBwd &p, cudaStream_t stream);
 
