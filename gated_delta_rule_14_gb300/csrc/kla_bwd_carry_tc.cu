@@ -48,7 +48,6 @@ constexpr uint32_t kSmemBytes = OFF_BAR + 64 + 1024;   // + room to align the ba
 static_assert(ST_G + 4 * kD <= kStage && kSmemBytes <= 232448, "carry shared memory");
 // TMEM columns: D1 | D1b | D2 | D2b
 constexpr uint32_t TM_D1 = 0, TM_D1B = 64, TM_D2 = 128, TM_D2B = 256;
-constexpr uint32_t kWaitLimit = 100000;   // x 20 us: a stuck wait gives up after ~2 s
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint32_t bar, int x, int y) {
     asm volatile(
@@ -69,6 +68,16 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
                  : "memory");
 }
 __device__ __forceinline__ unsigned short bf16_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
+__device__ __forceinline__ float bf16_val(unsigned short bits) { return __uint_as_float(static_cast<uint32_t>(bits) << 16); }
+// Waits for phase `parity` of `bar` by polling (the waits of a step are short; this form also keeps
+// the forward per-channel carry within its registers). Gives up after 2^31 clock cycles (about a
+// second).
+__device__ __forceinline__ bool wait_poll(uint32_t bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > (1ll << 31)) return false;
+    return true;
+}
 
 template <bool kRev, bool kCh>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -127,12 +136,14 @@ carry_tc_kernel(const __grid_constant__ CUtensorMap mK, const __grid_constant__ 
         else if (p.X0 && r == 0) x = p.X0[(static_cast<size_t>(bh) * kD + k) * kD + v];
         X[j] = x;
     }
-    // bf16 X^T tile (MN-major A operand and the state record): element (k, v)
-    const uint32_t xcol = sbase + OFF_X + (v >> 6) * kTile, ecol = sbase + OFF_E + (v >> 6) * kHalf;
+    // bf16 X^T tile (MN-major A operand and the state record): element (k, v) of this thread's
+    // 64-channel column block; the E^T / dE^T tile likewise, element (t, v)
+    unsigned short *xcol = reinterpret_cast<unsigned short *>(smem + OFF_X + (v >> 6) * kTile);
+    unsigned short *ecol = reinterpret_cast<unsigned short *>(smem + OFF_E + (v >> 6) * kHalf);
     const uint32_t vb = (v & 63) * 2;
     auto put_x = [&]() {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) st_shared_b16(xcol + sw128_off(32 * q + j, vb), bf16_bits(X[j]));
+        for (int j = 0; j < 32; ++j) xcol[sw128_off(32 * q + j, vb) >> 1] = bf16_bits(X[j]);
         fence_proxy_async_smem();
     };
     put_x();
@@ -186,17 +197,17 @@ carry_tc_kernel(const __grid_constant__ CUtensorMap mK, const __grid_constant__ 
             if (it + 1 < steps && elect_one()) issue(kRev ? c - 1 : c + 1, s ^ 1);
             __syncwarp();
         }
-        ok = mbar_wait_bounded(bar_full + 8 * s, (it >> 1) & 1, kWaitLimit);
+        ok = wait_poll(bar_full + 8 * s, (it >> 1) & 1);
         if (!ok) *abort_flag = 1;
-        // the state record (S_c, or dS_{c+1} in reverse; thread 0 owns every record store and
-        // waits for them) and the first products
+        // the state record (S_c, or dS_{c+1} in reverse; thread 32 owns every record store and
+        // waits for them) and the first products (warp 0)
+        if (tid == 32 && ok && rec) {
+            tma_store_2d(&mXr, sbase + OFF_X, 0, n * kD);
+            tma_store_2d(&mXr, sbase + OFF_X + kTile, 64, n * kD);
+            tma_store_commit();
+        }
         if (warp == 0) {
             const bool wok = __all_sync(0xffffffffu, ok);
-            if (wok && rec && lane == 0) {
-                tma_store_2d(&mXr, sbase + OFF_X, 0, n * kD);
-                tma_store_2d(&mXr, sbase + OFF_X + kTile, 64, n * kD);
-                tma_store_commit();
-            }
             if (wok && elect_one()) {
                 tc_fence_after();
                 const uint64_t dx = sw128_desc(sbase + OFF_X, kTile, 1024);
@@ -218,7 +229,8 @@ carry_tc_kernel(const __grid_constant__ CUtensorMap mK, const __grid_constant__ 
         // scalar gate: the decayed copy the second products read (K_e forward, s e^G Q reverse);
         // both tiles share one swizzled layout, so 16-byte granules copy in place
         if (!kCh && (!kRev || drive)) {
-            const uint32_t src = st + (kRev ? ST_UQ : ST_K), dst = sbase + OFF_KS;
+            const uint8_t *src = smem + s * kStage + (kRev ? ST_UQ : ST_K);
+            uint8_t *dst = smem + OFF_KS;
             const float Gend = gv[kC - 1];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
@@ -226,17 +238,17 @@ carry_tc_kernel(const __grid_constant__ CUtensorMap mK, const __grid_constant__ 
                 const int t = (i >> 3) & (kC - 1);
                 const uint32_t off = (i >> 9) * kHalf + t * 128 + (i & 7) * 16;
                 const float f = kRev ? p.q_scale * __expf(gv[t]) : __expf(Gend - gv[t]);
-                const uint4 x = ld_shared_v4(src + off);
+                const uint4 x = *reinterpret_cast<const uint4 *>(src + off);
                 const uint32_t w[4] = {x.x, x.y, x.z, x.w};
                 uint32_t o[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     o[e] = pack_bf16(f * __uint_as_float(w[e] << 16), f * __uint_as_float(w[e] & 0xffff0000u));
-                st_shared_v4(dst + off, o[0], o[1], o[2], o[3]);
+                *reinterpret_cast<uint4 *>(dst + off) = make_uint4(o[0], o[1], o[2], o[3]);
             }
             fence_proxy_async_smem();
         }
-        if (!mbar_wait_bounded(bar_mma, mma_par, kWaitLimit)) *abort_flag = 1;
+        if (!wait_poll(bar_mma, mma_par)) *abort_flag = 1;
         mma_par ^= 1;
         tc_fence_after();
         // E^T (forward) or dE^T (reverse) for tokens [16 q, 16 q + 16) of this lane's value channel
@@ -246,6 +258,8 @@ carry_tc_kernel(const __grid_constant__ CUtensorMap mK, const __grid_constant__ 
             if (kRev && drive) tmem_ld16(tl + TM_D1B + 16 * q, d2);
             tmem_ld_wait();
             const float Gend = kCh ? 0.f : gv[kC - 1];
+            const unsigned short *ucol =
+                reinterpret_cast<const unsigned short *>(smem + s * kStage + ST_UQ + (v >> 6) * kHalf);
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
                 const int t = 16 * q + jj;
@@ -255,24 +269,24 @@ carry_tc_kernel(const __grid_constant__ CUtensorMap mK, const __grid_constant__ 
                     e = ee * __uint_as_float(d[jj]);
                     if (drive) e = fmaf(p.q_scale, __uint_as_float(d2[jj]), e);
                 } else {
-                    const float u = drive ? ld_shared_bf16(st + ST_UQ + (v >> 6) * kHalf + sw128_off(t, vb)) : 0.f;
+                    const float u = drive ? bf16_val(ucol[sw128_off(t, vb) >> 1]) : 0.f;
                     e = u - __uint_as_float(d[jj]);
                 }
-                st_shared_b16(ecol + sw128_off(t, vb), bf16_bits(e));
+                ecol[sw128_off(t, vb) >> 1] = bf16_bits(e);
             }
             fence_proxy_async_smem();
         }
         tc_fence_before();
-        if (tid == 0) tma_store_wait_read_all();   // the state record has left the X^T tile
+        if (tid == 32) tma_store_wait_read_all();   // the state record has left the X^T tile
         __syncthreads();
         if (*abort_flag) break;
         tc_fence_after();
+        if (tid == 32 && rec) {
+            tma_store_2d(&mEr, sbase + OFF_E, 0, n * kC);
+            tma_store_2d(&mEr, sbase + OFF_E + kHalf, 64, n * kC);
+            tma_store_commit();
+        }
         if (warp == 0) {
-            if (rec && lane == 0) {
-                tma_store_2d(&mEr, sbase + OFF_E, 0, n * kC);
-                tma_store_2d(&mEr, sbase + OFF_E + kHalf, 64, n * kC);
-                tma_store_commit();
-            }
             if (elect_one()) {
                 const uint64_t de = sw128_desc(sbase + OFF_E, kHalf, 1024);
                 if (kRev) {
@@ -297,7 +311,7 @@ carry_tc_kernel(const __grid_constant__ CUtensorMap mK, const __grid_constant__ 
             }
             __syncwarp();
         }
-        if (!mbar_wait_bounded(bar_mma, mma_par, kWaitLimit)) *abort_flag = 1;
+        if (!wait_poll(bar_mma, mma_par)) *abort_flag = 1;
         mma_par ^= 1;
         tc_fence_after();
         // X'^T = Gamma X^T + D2 (- D2b): the decay, then the products in two passes of 16 key channels
@@ -315,24 +329,31 @@ carry_tc_kernel(const __grid_constant__ CUtensorMap mK, const __grid_constant__ 
 #pragma unroll
             for (int j = 0; j < 32; ++j) X[j] *= Gam;
         }
+        // every load in flight before one wait (two rounds for the forward per-channel carry,
+        // whose registers are fullest)
+        constexpr int kRounds = (!kRev && kCh) ? 2 : 1, kCols = 32 / kRounds;
 #pragma unroll
-        for (int pc = 0; pc < 2; ++pc) {
-            uint32_t a[16], bb[16];
+        for (int pc = 0; pc < kRounds; ++pc) {
+            uint32_t a[kCols], bb[kRev ? kCols : 1];
             const bool has_a = !kRev || drive;
-            if (has_a) tmem_ld16(tl + TM_D2 + 32 * q + 16 * pc, a);
-            if (kRev) tmem_ld16(tl + TM_D2B + 32 * q + 16 * pc, bb);
+            if (has_a) {
+                if constexpr (kCols == 32) tmem_ld32(tl + TM_D2 + 32 * q, a);
+                else tmem_ld16(tl + TM_D2 + 32 * q + 16 * pc, a);
+            }
+            if constexpr (kRev) tmem_ld32(tl + TM_D2B + 32 * q, bb);
             tmem_ld_wait();
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-                float x = X[16 * pc + jj];
+            for (int jj = 0; jj < kCols; ++jj) {
+                const int j = kCols * pc + jj;
+                float x = X[j];
                 if (has_a) x += __uint_as_float(a[jj]);
-                if (kRev) x -= __uint_as_float(bb[jj]);
-                X[16 * pc + jj] = x;
+                if constexpr (kRev) x -= __uint_as_float(bb[jj]);
+                X[j] = x;
             }
         }
         put_x();
         tc_fence_before();
-        if (tid == 0) tma_store_wait_read_all();   // the E / dE record has left its tile
+        if (tid == 32) tma_store_wait_read_all();   // the E / dE record has left its tile
         __syncthreads();
     }
     const bool aborted = *abort_flag != 0;
@@ -345,10 +366,8 @@ carry_tc_kernel(const __grid_constant__ CUtensorMap mK, const __grid_constant__ 
         if (p.Xseg) put_end(p.Xseg + (static_cast<size_t>(bh) * p.nseg + r) * kD * kD);
         if (kRev && p.X_end && c_lo == 0) put_end(p.X_end + static_cast<size_t>(bh) * kD * kD);
     }
-    if (tid == 0) {
-        tma_store_wait_all();
-        if (aborted && p.err) atomicOr(p.err, kErrTimeout);
-    }
+    if (tid == 32) tma_store_wait_all();
+    if (tid == 0 && aborted && p.err) atomicOr(p.err, kErrTimeout);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
