@@ -384,8 +384,9 @@ def bench_bwd(name, steps, seed, dev, flush, stream, pk, **override):
     alg = wl.B * wl.T * wl.H * (BWD_BYTES_PER_TOKEN_HEAD_KDA if wl.gate == "channel" else BWD_BYTES_PER_TOKEN_HEAD)
     return {"value": wl.B * wl.T / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
             "workspace_bytes": ws.numel(), "roofline": roofline(alg, ms, pk),
-            "note": "chunkwise backward on warp-level bf16 MMAs: chunk-parallel prep (T = (I+R)^-1, W, U, A), "
-                    "forward and reverse chunk-state carries (one CTA per chain), chunk-parallel gradients; "
+            "note": "chunkwise backward: chunk-parallel prep (T = (I+R)^-1, W, U, A) and gradients on warp-level "
+                    "bf16 MMAs, the forward and reverse chunk-state carries on tcgen05 (one CTA per chain, "
+                    "TMA-staged tiles, TMA record stores); "
                     "~4.5 GB of DRAM traffic per call (ncu at B = 4, per-chunk S_c, dS_c, E_c, dE_c, W, U, A, T records) "
                     "against the algorithmic bytes"}
 
@@ -638,7 +639,7 @@ def main():
             extras["bwd_kda8k"] = bench_bwd("kda8k", 3, seed=rank, dev=dev, flush=flush, stream=stream, pk=pk)
             extras["bwd_kda8k"]["note"] = ("per-channel gate, chunkwise: gate range check, prep with the per-channel "
                                            "factor tiles (K e^{G-G_r}, K e^{G_r-G}, Q e^{G-G_r}), forward and reverse "
-                                           "chunk-state carries, chunk-parallel gradients with dk, dq and the "
+                                           "chunk-state carries on tcgen05 side by side, chunk-parallel gradients with dk, dq and the "
                                            "log-decay gradient per channel in registers; chains outside the "
                                            "factorised range rerun on the token-sequential path (none here)")
             clocks.mark(t0, time.time())
