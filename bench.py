@@ -508,6 +508,8 @@ def main():
                     help="time only the prefill of this workload (a command for profiling one kernel)")
     ap.add_argument("--verify-only", choices=["4", "8", "16", "16kda"], default=None,
                     help="time only this multi-token call on the decode batch (--verify-calls calls)")
+    ap.add_argument("--e2e-parts", type=int, default=8,
+                    help="time slices of the host-buffer prefill (the e2e number)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -578,7 +580,7 @@ def main():
     tensor = {"achieved_tflops": round(tflops, 2), "peak_tflops": pk["bf16_tflops"],
               "frac": round(tflops / pk["bf16_tflops"], 4), "pipe_active": active}
 
-    e2e = e2e_prefill(res, max(3, args.steps // 2), 3, dev, stream)
+    e2e = e2e_prefill(res, max(3, args.steps // 2), 3, dev, stream, parts=args.e2e_parts)
     e2e_val = reduce_sum(e2e["tokens_per_s"], world, dev) if world > 1 else e2e["tokens_per_s"]
     launches = args.steps * 1   # one kernel per prefill step
 
