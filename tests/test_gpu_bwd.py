@@ -121,6 +121,20 @@ def test_backward_against_oracle(base, over, mode, with_dst):
     compare(pick(got, chains), ref, tol(inp.wl))
 
 
+@pytest.mark.parametrize("base", ["gdn4k", "kda8k"])
+def test_more_chains_than_sms(base):
+    """More chains than a GB300 has SMs (192 against 152): the tensor-core carries, one CTA per
+    chain holding all of its SM's tensor memory, run in two waves (and the per-channel gate's two
+    carries one after the other, as they no longer fit side by side). Every gradient of every
+    chain against the oracle."""
+    inp = synth.make_prefill(base, seed=43, B=3, T=130, H=64, s0_sigma=0.05)
+    dO, dST = _grad_inputs(inp, seed=44, with_dst=True)
+    got = run_gpu(inp, dO, dST)
+    ref = run_oracle(inp, dO, dST)
+    chains = [(b, h) for b in range(inp.wl.B) for h in range(inp.wl.H)]
+    compare(pick(got, chains), ref, tol(inp.wl))
+
+
 def test_backward_without_ds0_and_empty_sequence():
     import torch
 

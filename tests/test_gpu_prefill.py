@@ -126,6 +126,16 @@ def test_full_config_whole_tensor(name):
     assert eo <= tol and es <= tol, f"rel-L2 o={eo:.3e} S={es:.3e} (worst chain {worst_chain(o, o_ref):.3e})"
 
 
+@pytest.mark.parametrize("base", ["gdn4k", "kda8k"])
+def test_more_chains_than_sms(base):
+    """More (sequence, head) chains than a GB300 has SMs (192 against 152): the tensor-core
+    prefill's CTAs, one per chain and each holding all of its SM's tensor memory, run in two
+    waves, the second allocating what the first released. Every chain against the oracle."""
+    inp = synth.make_prefill(base, seed=41, B=3, T=130, H=64, s0_sigma=0.05)
+    o, S = run_prefill(inp)
+    check(inp, o, S)
+
+
 @pytest.mark.parametrize("gate", ["scalar", "channel"])
 def test_zero_keys_eps_zero_unit_gates(gate):
     """Degenerate tokens on the tensor-core prefill: keys that are exactly zero with eps = 0 (the
