@@ -376,7 +376,10 @@ carry_tc_kernel(const __grid_constant__ CUtensorMap mK, const __grid_constant__ 
     }
 }
 
+}  // namespace
+
 // ---------------------------------------------------------------------------- host side
+namespace {
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -395,7 +398,8 @@ EncodeTiledFn encoder() {
     return fn;
 }
 
-// A [rows][cols] bf16 record, boxes of box_rows x 64 columns, 128-byte swizzle.
+}  // namespace
+
 bool map_record(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
     EncodeTiledFn fn = encoder();
     if (!fn) return false;
@@ -407,7 +411,6 @@ bool map_record(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, 
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-// A [B, T, H, 128] bf16 input, boxes of 64 tokens x 64 channels of one (b, h); tokens past T read 0.
 bool map_tokens(CUtensorMap *m, const void *base, int B, int T, int H) {
     EncodeTiledFn fn = encoder();
     if (!fn) return false;
@@ -422,6 +425,7 @@ bool map_tokens(CUtensorMap *m, const void *base, int B, int T, int H) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+namespace {
 template <bool kRev, bool kCh>
 cudaError_t launch_t(const ScanParams &p, int grid, cudaStream_t stream) {
     const uint64_t N = static_cast<uint64_t>(p.B) * p.H * p.nc;

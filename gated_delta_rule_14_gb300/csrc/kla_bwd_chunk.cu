@@ -29,17 +29,18 @@
 //             d log alpha_t = sum over the chunk's rows i >= t of dG_i,  dalpha = that / alpha.
 //
 // Four kernels (one pass over the workspace each way):
-//   bwd_prep_kernel  (chunk-parallel)  gates, [K;Q]K^T, R and A, T by blocked substitution (fp32),
-//                                      W and U; stores G, beta, den, W, U, A and T per chunk;
+//   prep_tc_kernel   (chunk-parallel)  gates, [K;Q]K^T, R and A, T by blocked substitution (fp32),
+//                                      W and U; stores G, beta, den, W, U, A and T per chunk
+//                                      (tcgen05, kla_bwd_prep_tc.cu);
 //   carry_tc_kernel<false>             the state carry S_c -> S_{c+1} per chain (fp32 registers,
 //                                      tcgen05 products), storing S_c and E_c per chunk;
 //   carry_tc_kernel<true>              the reverse carry dS_{c+1} -> dS_c per chain, storing dS_{c+1}
 //                                      and dE_c per chunk, and dS0 (both in kla_bwd_carry_tc.cu);
 //   bwd_grad_kernel  (chunk-parallel)  every gradient of the chunk's tokens from S_c, dS_{c+1},
 //                                      E_c, dE_c, T and the inputs.
-// In the prep and gradient kernels every product is a warp-level bf16 mma.sync (m16n8k16, fp32
-// accumulate) on 64- or 128-wide tiles staged in shared memory with rows padded by 16 bytes, so
-// that every ldmatrix phase hits 8 distinct bank quads. Operands are bf16 (inputs as stored;
+// In the gradient kernel every product is a warp-level bf16 mma.sync (m16n8k16, fp32 accumulate)
+// on 64- or 128-wide tiles staged in shared memory with rows padded by 16 bytes, so that every
+// ldmatrix phase hits 8 distinct bank quads. Operands are bf16 (inputs as stored;
 // derived tiles rounded once); the carried states, the solve and every sum of a gradient are fp32.
 #include <algorithm>
 #include <mutex>
@@ -84,152 +85,9 @@ CarryPlan carry_plan(int chains, int nc) {
 }
 
 // ============================================================== kernel 1: per-chunk operands
-struct PrepParams {
-    const bf16 *q, *k, *v;
-    const float *alpha, *eta;
-    float eps;
-    int beta_raw;
-    int B, T, H, nc;
-    Ws ws;
-};
-constexpr int kPrepThreads = 256;
-// shared memory of the prep kernel
-constexpr int PR_K = 0, PR_Q = PR_K + kTileTok, PR_V = PR_Q + kTileTok;
-constexpr int PR_R = PR_V + kTileTok;                 // fp32 [64][68]: R, overwritten by T block by block
-constexpr int PR_TK = PR_R + kC * kPR * 4;            // bf16 T diag(beta gamma)
-constexpr int PR_TV = PR_TK + kTileSq;                // bf16 T diag(beta)
-constexpr int PR_A = PR_TV + kTileSq;                 // bf16 A (then T) staging
-constexpr int PR_X = PR_A + kTileSq;                  // fp32 [32][36] merge scratch
-constexpr int PR_VEC = PR_X + 32 * kPX * 4;           // eta, G, beta, beta e^G (fp32 [4][64])
-constexpr int PR_BYTES = PR_VEC + 4 * kC * 4;
-
-__global__ void __launch_bounds__(kPrepThreads, 2) bwd_prep_kernel(PrepParams p) {
-    extern __shared__ __align__(16) unsigned char smem[];
-    bf16 *sK = reinterpret_cast<bf16 *>(smem + PR_K), *sQ = reinterpret_cast<bf16 *>(smem + PR_Q),
-         *sV = reinterpret_cast<bf16 *>(smem + PR_V);
-    float(*sR)[kPR] = reinterpret_cast<float(*)[kPR]>(smem + PR_R);
-    bf16 *sTK = reinterpret_cast<bf16 *>(smem + PR_TK), *sTV = reinterpret_cast<bf16 *>(smem + PR_TV),
-         *sA = reinterpret_cast<bf16 *>(smem + PR_A);
-    float *sX = reinterpret_cast<float *>(smem + PR_X);
-    float *seta = reinterpret_cast<float *>(smem + PR_VEC), *sG = seta + kC, *sb = sG + kC, *sgb = sb + kC;
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const size_t rs = static_cast<size_t>(p.H) * kD;                      // token row stride
-    const int c = blockIdx.x, bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
-    const int t0 = c * kC, L = min(kC, p.T - t0);
-    const size_t n = static_cast<size_t>(bh) * p.nc + c;
-    const size_t base = (static_cast<size_t>(b) * p.T + t0) * p.H + h;    // (b, t0, h)
-
-    load_tok(sK, p.k + base * kD, rs, L, tid, kPrepThreads);
-    load_tok(sQ, p.q + base * kD, rs, L, tid, kPrepThreads);
-    load_tok(sV, p.v + base * kD, rs, L, tid, kPrepThreads);
-    cp_commit();
-    // gates while the tiles land (warp 0, tokens 2 lane and 2 lane + 1): g = log alpha, inclusive
-    // prefix G, eta
-    if (warp == 0) {
-        float x[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int t = 2 * lane + e;
-            const bool ok = t < L;
-            x[e] = ok ? fmaxf(logf(p.alpha[base + static_cast<size_t>(t) * p.H]), kMinLogGate) : 0.f;
-            seta[t] = ok ? p.eta[base + static_cast<size_t>(t) * p.H] : 0.f;
-        }
-        float sc = x[0] + x[1];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, sc, o);
-            if (lane >= o) sc += y;
-        }
-        sG[2 * lane + 1] = sc;
-        sG[2 * lane] = sc - x[1];
-    }
-    cp_wait<0>();
-    __syncthreads();
-    float *cg = p.ws.cg + n * kCgFloats;
-
-    // [K; Q] K^T: warp w owns rows 16 (w & 3) of K K^T (w < 4) or of Q K^T (w >= 4), all 64 columns
-    {
-        float acc[8][4];
-        zero(acc);
-        const int r0 = 16 * (warp & 3);
-        gemm<8, 8, false, false>(acc, sptr(warp < 4 ? sK : sQ), kP, r0, 0, sptr(sK), kP, 0, 0, lane);
-        const int g = lane >> 2, q4 = lane & 3;
-        float rb[2] = {0.f, 0.f};   // beta of this thread's two rows (K K^T warps)
-        if (warp < 4) {
-            // ||k_i||^2 is the diagonal of K K^T: the thread holding (i, i) publishes it with the
-            // row's G, beta and ||k||^2 + eps
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int i = r0 + g + 8 * hh;
-                        if (8 * nt + 2 * q4 + e == i) {
-                            const float n2 = acc[nt][2 * hh + e];
-                            const float beta = i < L ? kla_beta(seta[i], n2, p.eps, p.beta_raw) : 0.f;
-                            sb[i] = beta;
-                            sgb[i] = beta * __expf(sG[i]);
-                            cg[i] = sG[i];
-                            cg[kC + i] = beta;
-                            cg[2 * kC + i] = n2 + p.eps;
-                        }
-                    }
-            __syncwarp();
-            rb[0] = sb[r0 + g];
-            rb[1] = sb[r0 + g + 8];
-        }
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int i = r0 + g + 8 * hh;
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int j = 8 * nt + 2 * q4 + e;
-                    const float ratio = __expf(sG[i] - sG[j]);
-                    const float x = acc[nt][2 * hh + e];
-                    if (warp < 4) sR[i][j] = j < i ? rb[hh] * ratio * x : 0.f;
-                    else acc[nt][2 * hh + e] = j <= i ? ratio * x : 0.f;
-                }
-                if (warp >= 4) st_pair(sA, kPs, i, 8 * nt + 2 * q4, acc[nt][2 * hh], acc[nt][2 * hh + 1]);
-            }
-    }
-    __syncthreads();
-    store_dense<kC>(p.ws.A + n * kC * kC, sA, kC, tid, kPrepThreads);
-
-    unit_lower_inverse64(sR, sX, warp, lane);
-    // T diag(beta gamma), T diag(beta) and T as bf16 (the upper triangle is zero)
-    for (int e = tid; e < kC * kC / 2; e += kPrepThreads) {
-        const int i = e / (kC / 2), j = 2 * (e % (kC / 2));
-        const float t0v = j <= i ? sR[i][j] : 0.f, t1v = j + 1 <= i ? sR[i][j + 1] : 0.f;
-        st_pair(sTK, kPs, i, j, t0v * sgb[j], t1v * sgb[j + 1]);
-        st_pair(sTV, kPs, i, j, t0v * sb[j], t1v * sb[j + 1]);
-        st_pair(sA, kPs, i, j, t0v, t1v);
-    }
-    __syncthreads();
-    store_dense<kC>(p.ws.Tm + n * kC * kC, sA, kC, tid, kPrepThreads);
-    // W = T diag(beta gamma) K (warps 0-3) and U = T diag(beta) V (warps 4-7): 16 rows x 128 each
-    float acc[16][4];
-    zero(acc);
-    const int r0 = 16 * (warp & 3);
-    gemm<16, 4, false, true>(acc, sptr(warp < 4 ? sTK : sTV), kPs, r0, 0, sptr(warp < 4 ? sK : sV), kP, 0, 0,
-                             lane);
-    __syncthreads();     // every read of K, Q, V is done: stage W in Q's tile and U in K's
-    {
-        bf16 *st = warp < 4 ? sQ : sK;
-        const int g = lane >> 2, q4 = lane & 3;
-#pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-            st_pair(st, kP, r0 + g, 8 * nt + 2 * q4, acc[nt][0], acc[nt][1]);
-            st_pair(st, kP, r0 + g + 8, 8 * nt + 2 * q4, acc[nt][2], acc[nt][3]);
-        }
-    }
-    __syncthreads();
-    store_dense<kD>(p.ws.W + n * kC * kD, sQ, kC, tid, kPrepThreads);
-    store_dense<kD>(p.ws.UdE + n * kC * kD, sK, kC, tid, kPrepThreads);
-}
+// Gates and their prefix, ||k||^2 from the diagonal of K K^T, [K;Q] K^T, R and A, T by blocked
+// substitution (fp32), W and U, storing G, beta, den, W, U, A and T per chunk: on the tensor
+// cores, launch_prep_tc in kla_bwd_prep_tc.cu.
 
 // ============================================================== kernel 2: the carry across chunks
 // The forward carry (X = S entering chunk c, c ascending: E = U - W X, X <- Gamma X +
@@ -755,12 +613,9 @@ cudaError_t launch_bwd_chunk(const BwdArgs &a) {
             (e = launch_bwd_prep_ch(cp, a.stream)) != cudaSuccess)
             return e;
     } else {
-        if ((e = cudaFuncSetAttribute(bwd_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PR_BYTES)) ||
-            (e = cudaFuncSetAttribute(bwd_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, GR_BYTES)))
+        if ((e = cudaFuncSetAttribute(bwd_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, GR_BYTES)) ||
+            (e = launch_prep_tc(q, k, v, a.alpha, a.eta, a.eps, a.beta_raw, a.B, a.T, a.H, nc, ws, err, a.stream)))
             return e;
-        PrepParams pp{q, k, v, a.alpha, a.eta, a.eps, a.beta_raw, a.B, a.T, a.H, nc, ws};
-        bwd_prep_kernel<<<dim3(nc, chains), kPrepThreads, PR_BYTES, a.stream>>>(pp);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     const CarryPlan pl = carry_plan(chains, nc);
     const size_t part = static_cast<size_t>(chains) * pl.nseg * kD * kD;

@@ -1,9 +1,12 @@
-// kla_bwd_chunk.cuh -- pieces shared by the chunkwise backward kernels (kla_bwd_chunk.cu: prep and
-// gradients of the scalar gate and the launch sequence; kla_bwd_chunk_ch.cu: prep and gradients of
-// the per-key-channel gate; kla_bwd_carry_tc.cu: both chunk-state carries, on the tensor cores):
+// kla_bwd_chunk.cuh -- pieces shared by the chunkwise backward kernels (kla_bwd_chunk.cu: gradients
+// of the scalar gate and the launch sequence; kla_bwd_prep_tc.cu: the scalar gate's prep on the
+// tensor cores; kla_bwd_chunk_ch.cu: prep and gradients of the per-key-channel gate;
+// kla_bwd_carry_tc.cu: both chunk-state carries, on the tensor cores):
 // the per-chunk workspace records, the carries' parameters, padded shared-memory tiles,
 // warp-level bf16 MMAs on them, cp.async staging and the 64 x 64 unit-lower inverse.
 #pragma once
+
+#include <cuda.h>
 
 #include "kla_internal.cuh"
 #include "warp_mma.cuh"
@@ -282,6 +285,16 @@ enum : int {
 // Device address of the library's error word on the current device.
 cudaError_t device_error_word(unsigned **out);
 namespace bwdc {
+// Tensor maps (128-byte swizzle) of the tensor-core kernels: a [rows][cols] bf16 record in boxes
+// of box_rows x 64 columns, and a [B, T, H, 128] bf16 input in boxes of 64 tokens x 64 channels
+// of one (b, h), tokens past T reading 0. False when the driver's encoder is unavailable or
+// rejects the map.
+bool map_record(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_rows);
+bool map_tokens(CUtensorMap *m, const void *base, int B, int T, int H);
+// The scalar gate's per-chunk records (cg, A, T, W, U) on the tensor cores, one CTA per chunk.
+cudaError_t launch_prep_tc(const bf16 *q, const bf16 *k, const bf16 *v, const float *alpha, const float *eta,
+                           float eps, int beta_raw, int B, int T, int H, int nc, const Ws &ws, unsigned *err,
+                           cudaStream_t stream);
 // Runs `grid` CTAs of the forward (rev = false) or reverse carry on the tensor cores.
 cudaError_t launch_carry_tc(const ScanParams &p, bool rev, bool ch, int grid, cudaStream_t stream);
 
