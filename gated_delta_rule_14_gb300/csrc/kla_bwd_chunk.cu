@@ -607,7 +607,7 @@ cudaError_t launch_bwd_chunk(const BwdArgs &a) {
     unsigned *err = nullptr;
     if ((e = device_error_word(&err)) != cudaSuccess) return e;
     const ChBwd cp{q, k, v, dO, a.alpha, a.eta, a.eps, a.q_scale, a.beta_raw, a.B, a.T, a.H, nc, ws, marks,
-                   a.dq, a.dk, a.dv, a.dalpha, a.deta};
+                   a.dq, a.dk, a.dv, a.dalpha, a.deta, err};
     if (ch) {
         if ((e = launch_gate_range(a.alpha, a.B, a.T, a.H, marks, a.stream)) != cudaSuccess ||
             (e = launch_bwd_prep_ch(cp, a.stream)) != cudaSuccess)

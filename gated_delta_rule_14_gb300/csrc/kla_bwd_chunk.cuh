@@ -254,6 +254,7 @@ struct ChBwd {
     Ws ws;
     const unsigned *skip;   // [B*H] chains left to the token-sequential path (their CTAs return at once)
     float *dq, *dk, *dv, *dalpha, *deta;
+    unsigned *err;          // device error word (a bounded wait that gives up sets kErrTimeout)
 };
 // ---- the chunk-state carries (one CTA per chain segment, chunks in order)
 struct ScanParams {

@@ -36,6 +36,7 @@
 // forward's range check (a half-chunk product of gates below ~e^-78 marks the chain) applies
 // unchanged; marked chains skip these kernels and take the token-sequential fp32 backward.
 #include "kla_bwd_chunk.cuh"
+#include "sm103_ptx.cuh"
 
 namespace kla {
 namespace bwdc {
@@ -75,53 +76,94 @@ __device__ __forceinline__ GateRef gate_ref(const float *squart, int c, int qt) 
 }
 
 // ============================================================== prep: per-chunk operands
-constexpr int kPrepThreads = 256;
-constexpr int PC_K = 0;                               // K, then K_r in place
-constexpr int PC_Q = PC_K + kTileTok;                 // Q, then Q_r in place; W staging at the end
-constexpr int PC_V = PC_Q + kTileTok;                 // V
-constexpr int PC_KM = PC_V + kTileTok;                // K_m; U staging at the end
-constexpr int PC_R = PC_KM + kTileTok;                // fp32 [64][kPR]: R, then T in place
-constexpr int PC_TB = PC_R + kC * kPR * 4;            // bf16 T diag(beta)
-constexpr int PC_A = PC_TB + kTileSq;                 // bf16 A, then T, staging
-constexpr int PC_X = PC_A + kTileSq;                  // fp32 [32][kPX] merge scratch
-constexpr int PC_VEC = PC_X + 32 * kPX * 4;           // eta, beta [64]; quarter sums [4][128]; e^{G_r} [128]
-constexpr int PC_BYTES = PC_VEC + (2 * kC + 5 * kD) * 4;
-static_assert(2 * (PC_BYTES + 1024) <= 233472, "two prep CTAs per SM");
+// One CTA of 8 warps per chunk, two per SM, on the tensor cores. The q, k, v tiles land by TMA in
+// the 128-byte-swizzled layout; threads (channel pair, quarter) rewrite K and Q in place as the
+// factor tiles K_r, Q_r and write K_m, storing the K_e, s Q_g and e^{G_end} records on the way; one
+// M = 128 product gives P = K_r K_m^T (rows 0-63) and Q_r K_m^T (rows 64-127) in TMEM, whose rows
+// become R = beta P (strictly lower, fp32) and A (lower, bf16, stored); T = (I + R)^{-1} in fp32;
+// T_V = T diag(beta) enters W_r^T = K_r^T T_V^T and U^T = V^T T_V^T (M = 128 channels), and
+// W = W_r diag(e^{G_r}) is one factor per TMEM lane on the way to the records.
+namespace pc {
+constexpr int kThreads = 256;
+constexpr uint32_t kHalf = 8192;                    // 64 rows x 128 bytes
+constexpr uint32_t OFF_QK = 0;                      // [K_r half 0 | Q_r half 0 | K_r half 1 | Q_r half 1]; W, U staging
+constexpr uint32_t OFF_TV = OFF_QK + kHalf;         // T_V over Q_r half 0 (read by the first product only)
+constexpr uint32_t OFF_V = 4 * kHalf;               // V [half][64 t][64 v]
+constexpr uint32_t OFF_KM = OFF_V + 2 * kHalf;      // K_m [half][64 t][64 k], K-major
+constexpr uint32_t OFF_R = OFF_KM + 2 * kHalf;      // fp32 [64][kPR]: R, then T
+constexpr uint32_t OFF_X = OFF_R + kC * kPR * 4;    // solve scratch fp32 [32][kPX]
+constexpr uint32_t OFF_VEC = OFF_X + 32 * kPX * 4;  // eta, beta [64]; quarter sums [4][128]; e^{G_r} [128]
+constexpr uint32_t OFF_BAR = OFF_VEC + (2 * kC + 5 * kD) * 4;
+constexpr uint32_t kBytes = OFF_BAR + 64 + 1024;
+static_assert(OFF_R % 16 == 0 && 2 * kBytes <= 232448, "two prep CTAs per SM");
+constexpr uint32_t TM_P = 0, TM_W = 0, TM_U = 64, kTmemCols = 128;   // W^T over P once read
+constexpr uint32_t kWaitLimit = 100000;                                // x 20 us: ~2 s
+}  // namespace pc
 
-__global__ void __launch_bounds__(kPrepThreads, 2) bwd_prep_ch_kernel(ChBwd p) {
-    extern __shared__ __align__(16) unsigned char smem[];
-    bf16 *sK = reinterpret_cast<bf16 *>(smem + PC_K), *sQ = reinterpret_cast<bf16 *>(smem + PC_Q),
-         *sV = reinterpret_cast<bf16 *>(smem + PC_V), *sKM = reinterpret_cast<bf16 *>(smem + PC_KM);
-    float(*sR)[kPR] = reinterpret_cast<float(*)[kPR]>(smem + PC_R);
-    bf16 *sTB = reinterpret_cast<bf16 *>(smem + PC_TB), *sA = reinterpret_cast<bf16 *>(smem + PC_A);
-    float *sX = reinterpret_cast<float *>(smem + PC_X);
-    float *seta = reinterpret_cast<float *>(smem + PC_VEC), *sb = seta + kC, *squart = sb + kC, *segr = squart + 4 * kD;
+__device__ __forceinline__ unsigned short bf16_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
+__device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tmap),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
 
+__global__ void __launch_bounds__(pc::kThreads, 2)
+bwd_prep_ch_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+                   const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mW,
+                   const __grid_constant__ CUtensorMap mU, const ChBwd p) {
+    using namespace pc;
+    using namespace ptx;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int c = blockIdx.x, bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
     if (p.skip && p.skip[bh]) return;
-    const size_t rs = static_cast<size_t>(p.H) * kD;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(smem);
+    float(*sR)[kPR] = reinterpret_cast<float(*)[kPR]>(smem + OFF_R);
+    float *sX = reinterpret_cast<float *>(smem + OFF_X);
+    float *seta = reinterpret_cast<float *>(smem + OFF_VEC), *sb = seta + kC, *squart = sb + kC, *segr = squart + 4 * kD;
+    const uint32_t bar_full = sbase + OFF_BAR, bar_mma = bar_full + 8;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + OFF_BAR + 16);
+    const int row = 32 * (warp & 3) + lane, half = warp >> 2;   // TMEM lane, column half
     const int t0 = c * kC, L = min(kC, p.T - t0);
     const size_t n = static_cast<size_t>(bh) * p.nc + c;
     const size_t tok0 = (static_cast<size_t>(b) * p.T + t0) * p.H + h;
 
-    load_tok(sK, p.k + tok0 * kD, rs, L, tid, kPrepThreads);
-    load_tok(sQ, p.q + tok0 * kD, rs, L, tid, kPrepThreads);
-    load_tok(sV, p.v + tok0 * kD, rs, L, tid, kPrepThreads);
-    cp_commit();
+    if (tid == 0) {
+        mbar_init(bar_full, 1);
+        mbar_init(bar_mma, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(bar_full, 6 * kHalf);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            tma_load_4d(sbase + OFF_QK + 2 * kHalf * hh, &mK, bar_full, 64 * hh, h, t0, b);
+            tma_load_4d(sbase + OFF_QK + 2 * kHalf * hh + kHalf, &mQ, bar_full, 64 * hh, h, t0, b);
+            tma_load_4d(sbase + OFF_V + kHalf * hh, &mV, bar_full, 64 * hh, h, t0, b);
+        }
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tslot), kTmemCols);
+        tmem_relinquish();
+    }
     // log-gates while the tiles land: thread (channel pair cp, quarter qt of the chunk)
     const int cp = tid & 63, qt = tid >> 6;
     float lg[2][16];
     gate_logs(p.alpha, tok0, p.H, L, cp, qt, lg, squart);
     if (tid < kC) seta[tid] = tid < L ? p.eta[tok0 + static_cast<size_t>(tid) * p.H] : 0.f;
-    cp_wait<0>();
+    bool ok = mbar_wait_bounded(bar_full, 0, kWaitLimit);
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tslot;
+    const uint32_t tl = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);
 
-    // ||k||^2, beta and the cg record: warp w takes tokens 8 w .. 8 w + 7, a lane 4 channels
+    // ||k||^2 from the raw K tile, beta and the cg record: warp w takes tokens 8 w .. 8 w + 7, a
+    // lane 4 channels (4 lane .. 4 lane + 3: k half lane / 16, bytes 8 (lane % 16) of the row)
     float *cg = p.ws.cg + n * kCgFloats;
     for (int u = 0; u < 8; ++u) {
         const int i = 8 * warp + u;
-        const uint2 x = *reinterpret_cast<const uint2 *>(sK + i * kP + 4 * lane);
+        const uint2 x = *reinterpret_cast<const uint2 *>(smem + OFF_QK + 2 * kHalf * (lane >> 4) +
+                                                        sw128_off(i, 8 * (lane & 15)));
         const float2 a = unpack2(x.x), bb = unpack2(x.y);
         float n2 = fmaf(a.x, a.x, fmaf(a.y, a.y, fmaf(bb.x, bb.x, bb.y * bb.y)));
 #pragma unroll
@@ -145,6 +187,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2) bwd_prep_ch_kernel(ChBwd p) {
         if (qt == 0) *reinterpret_cast<float2 *>(segr + 2 * cp) = make_float2(__expf(g0.Gr), __expf(g1.Gr));
         if (qt == 3)
             *reinterpret_cast<float2 *>(p.ws.gend + n * kD + 2 * cp) = make_float2(__expf(g0.Gend), __expf(g1.Gend));
+        const uint32_t cb = 4 * (cp & 31);   // byte column of the channel pair in its 64-channel half
+        uint8_t *kt = smem + OFF_QK + 2 * kHalf * (cp >> 5), *qtl = kt + kHalf;
+        uint8_t *km = smem + OFF_KM + kHalf * (cp >> 5);
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
             const int i = 16 * qt + u;
@@ -152,72 +197,135 @@ __global__ void __launch_bounds__(kPrepThreads, 2) bwd_prep_ch_kernel(ChBwd p) {
             G1 += lg[1][u];
             const float fr0 = __expf(G0 - g0.Gr), fm0 = __expf(g0.Gr - G0), eg0 = __expf(G0), ee0 = __expf(g0.Gend - G0);
             const float fr1 = __expf(G1 - g1.Gr), fm1 = __expf(g1.Gr - G1), eg1 = __expf(G1), ee1 = __expf(g1.Gend - G1);
-            uint32_t *pk = reinterpret_cast<uint32_t *>(sK + i * kP) + cp, *pq = reinterpret_cast<uint32_t *>(sQ + i * kP) + cp;
+            const uint32_t off = sw128_off(i, cb);
+            uint32_t *pk = reinterpret_cast<uint32_t *>(kt + off), *pq = reinterpret_cast<uint32_t *>(qtl + off);
             const float2 kv = unpack2(*pk), qv = unpack2(*pq);
             *pk = pack2(kv.x * fr0, kv.y * fr1);
             *pq = pack2(qv.x * fr0, qv.y * fr1);
-            reinterpret_cast<uint32_t *>(sKM + i * kP)[cp] = pack2(kv.x * fm0, kv.y * fm1);
+            *reinterpret_cast<uint32_t *>(km + off) = pack2(kv.x * fm0, kv.y * fm1);
             ke[i * (kD / 2)] = pack2(kv.x * ee0, kv.y * ee1);
             qg[i * (kD / 2)] = pack2(p.q_scale * qv.x * eg0, p.q_scale * qv.y * eg1);
         }
     }
+    fence_proxy_async_smem();
+    tc_fence_before();
     __syncthreads();
-
-    // [K_r; Q_r] K_m^T: warp w owns rows 16 (w & 3) of P (w < 4: R = beta P, strictly lower) or of
-    // Q_r K_m^T (w >= 4: A, lower)
-    {
-        float acc[8][4];
-        zero(acc);
-        const int r0 = 16 * (warp & 3);
-        gemm<8, 8, false, false>(acc, sptr(warp < 4 ? sK : sQ), kP, r0, 0, sptr(sKM), kP, 0, 0, lane);
-        const int g = lane >> 2, q4 = lane & 3;
+    if (warp == 0) {   // [K_r; Q_r] K_m^T
+        tc_fence_after();
+        if (__all_sync(0xffffffffu, ok) && elect_one()) {
+            const uint64_t da = sw128_desc(sbase + OFF_QK, 16, 1024), db = sw128_desc(sbase + OFF_KM, 16, 1024);
+            const uint32_t id = idesc_bf16(128, 64, 0, 0);
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int i = r0 + g + 8 * hh, j = 8 * nt + 2 * q4;
-                if (warp < 4) {
-                    const float bi = sb[i];
-                    sR[i][j] = j < i ? bi * acc[nt][2 * hh] : 0.f;
-                    sR[i][j + 1] = j + 1 < i ? bi * acc[nt][2 * hh + 1] : 0.f;
-                } else {
-                    st_pair(sA, kPs, i, j, j <= i ? acc[nt][2 * hh] : 0.f, j + 1 <= i ? acc[nt][2 * hh + 1] : 0.f);
-                }
-            }
+            for (int s = 0; s < 8; ++s)
+                mma_bf16(tbase + TM_P, desc_add(da, (s >> 2) * 2 * kHalf + (s & 3) * 32),
+                         desc_add(db, (s >> 2) * kHalf + (s & 3) * 32), id, s);
+            mma_commit(bar_mma);
+        }
+        __syncwarp();
     }
-    __syncthreads();
-    store_dense<kC>(p.ws.A + n * kC * kC, sA, kC, tid, kPrepThreads);
-
-    unit_lower_inverse64(sR, sX, warp, lane);
-    // T diag(beta) and T as bf16 (the upper triangle is zero)
-    for (int e = tid; e < kC * kC / 2; e += kPrepThreads) {
-        const int i = e / (kC / 2), j = 2 * (e % (kC / 2));
-        const float t0v = j <= i ? sR[i][j] : 0.f, t1v = j + 1 <= i ? sR[i][j + 1] : 0.f;
-        st_pair(sTB, kPs, i, j, t0v * sb[j], t1v * sb[j + 1]);
-        st_pair(sA, kPs, i, j, t0v, t1v);
-    }
-    __syncthreads();
-    store_dense<kC>(p.ws.Tm + n * kC * kC, sA, kC, tid, kPrepThreads);
-    // W = (T diag(beta) K_r) diag(e^{G_r}) (warps 0-3) and U = T diag(beta) V (warps 4-7)
-    float acc[16][4];
-    zero(acc);
-    const int r0 = 16 * (warp & 3);
-    gemm<16, 4, false, true>(acc, sptr(sTB), kPs, r0, 0, sptr(warp < 4 ? sK : sV), kP, 0, 0, lane);
-    __syncthreads();   // every read of K_r, V is done: stage W in Q_r's tile and U in K_m's
-    {
-        bf16 *st = warp < 4 ? sQ : sKM;
-        const int g = lane >> 2, q4 = lane & 3;
+    if (!mbar_wait_bounded(bar_mma, 0, kWaitLimit)) ok = false;
+    tc_fence_after();
+    {   // this thread's half-row: R = beta P (strictly lower) or A (lower, to its record)
+        uint32_t xr[32];
+        tmem_ld32(tl + TM_P + 32 * half, xr);
+        tmem_ld_wait();
+        const int i = row & (kC - 1);
+        const bool key_row = row < kC;
+        const float scale = key_row ? sb[i] : 1.f;
+        float v[32];
 #pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-            const int col = 8 * nt + 2 * q4;
-            const float f0 = warp < 4 ? segr[col] : 1.f, f1 = warp < 4 ? segr[col + 1] : 1.f;
-            st_pair(st, kP, r0 + g, col, f0 * acc[nt][0], f1 * acc[nt][1]);
-            st_pair(st, kP, r0 + g + 8, col, f0 * acc[nt][2], f1 * acc[nt][3]);
+        for (int jj = 0; jj < 32; ++jj) {
+            const int j = 32 * half + jj;
+            v[jj] = (key_row ? j < i : j <= i) ? scale * __uint_as_float(xr[jj]) : 0.f;
+        }
+        if (key_row) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                *reinterpret_cast<float4 *>(&sR[i][32 * half + 4 * q]) =
+                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        } else {
+            bf16 *dst = p.ws.A + (n * kC + i) * kC + 32 * half;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4 *>(dst + 8 * q) =
+                    make_uint4(pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
+                               pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
         }
     }
+    __syncthreads();   // R complete
+    unit_lower_inverse64(sR, sX, warp, lane);   // T over R; ends with a block barrier
+    {   // T (bf16 record) and T_V = T diag(beta) (bf16, K-major, 128-byte swizzle)
+        const int r = tid >> 2, kq = tid & 3;
+        bf16 *trec = p.ws.Tm + (n * kC + r) * kC + 16 * kq;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            float tv[8], tt[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int j = 16 * kq + 8 * hh + u;
+                tt[u] = j <= r ? sR[r][j] : 0.f;
+                tv[u] = tt[u] * sb[j];
+            }
+            *reinterpret_cast<uint4 *>(trec + 8 * hh) =
+                make_uint4(pack_bf16(tt[0], tt[1]), pack_bf16(tt[2], tt[3]), pack_bf16(tt[4], tt[5]),
+                           pack_bf16(tt[6], tt[7]));
+            st_shared_v4(sbase + OFF_TV + sw128_off(r, 32 * kq + 16 * hh), pack_bf16(tv[0], tv[1]),
+                         pack_bf16(tv[2], tv[3]), pack_bf16(tv[4], tv[5]), pack_bf16(tv[6], tv[7]));
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
     __syncthreads();
-    store_dense<kD>(p.ws.W + n * kC * kD, sQ, kC, tid, kPrepThreads);
-    store_dense<kD>(p.ws.UdE + n * kC * kD, sKM, kC, tid, kPrepThreads);
+    if (warp == 0) {   // W_r^T = K_r^T T_V^T and U^T = V^T T_V^T (M = 128 channels, N = 64, K = 64)
+        tc_fence_after();
+        if (elect_one()) {
+            const uint32_t id = idesc_bf16(128, 64, 1, 0);
+            const uint64_t dk = sw128_desc(sbase + OFF_QK, 2 * kHalf, 1024), dv = sw128_desc(sbase + OFF_V, kHalf, 1024);
+            const uint64_t dt = sw128_desc(sbase + OFF_TV, 16, 1024);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) mma_bf16(tbase + TM_W, desc_add(dk, s * 2048), desc_add(dt, s * 32), id, s);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) mma_bf16(tbase + TM_U, desc_add(dv, s * 2048), desc_add(dt, s * 32), id, s);
+            mma_commit(bar_mma);
+        }
+        __syncwarp();
+    }
+    if (!mbar_wait_bounded(bar_mma, 1, kWaitLimit)) ok = false;
+    tc_fence_after();
+    {   // rows of W^T (times e^{G_r} of the channel) and U^T -> record-layout staging tiles over the q/k area
+        const uint32_t cb = (row & 63) * 2, hb = (row >> 6) * kHalf;
+        unsigned short *wst = reinterpret_cast<unsigned short *>(smem + OFF_QK + hb);
+        unsigned short *ust = reinterpret_cast<unsigned short *>(smem + OFF_QK + 2 * kHalf + hb);
+        const float fw = segr[row];
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            uint32_t d[32];
+            tmem_ld32(tl + (m ? TM_U : TM_W) + 32 * half, d);
+            tmem_ld_wait();
+            unsigned short *st = m ? ust : wst;
+            const float f = m ? 1.f : fw;
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) st[sw128_off(32 * half + jj, cb) >> 1] = bf16_bits(f * __uint_as_float(d[jj]));
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+        const int y = static_cast<int>(n) * kC;
+        tma_store_2d(&mW, sbase + OFF_QK, 0, y);
+        tma_store_2d(&mW, sbase + OFF_QK + kHalf, 64, y);
+        tma_store_2d(&mU, sbase + OFF_QK + 2 * kHalf, 0, y);
+        tma_store_2d(&mU, sbase + OFF_QK + 3 * kHalf, 64, y);
+        tma_store_commit();
+        tma_store_wait_all();
+        if (!ok && p.err) atomicOr(p.err, kErrTimeout);
+    }
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tbase, kTmemCols);
+    }
 }
 
 // gemm_m with the k-steps unrolled by two only: with 255 registers a thread, full unrolling lets the
@@ -697,9 +805,16 @@ __global__ void __launch_bounds__(kGradThreads, 1) bwd_grad_ch_kernel(ChBwd p) {
 }  // namespace
 
 cudaError_t launch_bwd_prep_ch(const ChBwd &p, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(bwd_prep_ch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PC_BYTES);
+    const uint64_t N = static_cast<uint64_t>(p.B) * p.H * p.nc;
+    CUtensorMap mQ, mK, mV, mW, mU;
+    if (!map_tokens(&mQ, p.q, p.B, p.T, p.H) || !map_tokens(&mK, p.k, p.B, p.T, p.H) ||
+        !map_tokens(&mV, p.v, p.B, p.T, p.H) || !map_record(&mW, p.ws.W, kD, N * kC, kC) ||
+        !map_record(&mU, p.ws.UdE, kD, N * kC, kC))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(bwd_prep_ch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(pc::kBytes));
     if (e != cudaSuccess) return e;
-    bwd_prep_ch_kernel<<<dim3(p.nc, p.B * p.H), kPrepThreads, PC_BYTES, stream>>>(p);
+    bwd_prep_ch_kernel<<<dim3(p.nc, p.B * p.H), pc::kThreads, pc::kBytes, stream>>>(mQ, mK, mV, mW, mU, p);
     return cudaGetLastError();
 }
 
