@@ -384,9 +384,9 @@ def bench_bwd(name, steps, seed, dev, flush, stream, pk, **override):
     alg = wl.B * wl.T * wl.H * (BWD_BYTES_PER_TOKEN_HEAD_KDA if wl.gate == "channel" else BWD_BYTES_PER_TOKEN_HEAD)
     return {"value": wl.B * wl.T / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
             "workspace_bytes": ws.numel(), "roofline": roofline(alg, ms, pk),
-            "note": "chunkwise backward: chunk-parallel prep (T = (I+R)^-1, W, U, A) and gradients on warp-level "
-                    "bf16 MMAs, the forward and reverse chunk-state carries on tcgen05 (one CTA per chain, "
-                    "TMA-staged tiles, TMA record stores); "
+            "note": "chunkwise backward: the chunk-parallel prep (T = (I+R)^-1, W, U, A) and the forward and "
+                    "reverse chunk-state carries (one CTA per chain) on tcgen05 with TMA-staged tiles and TMA "
+                    "record stores, the chunk-parallel gradients on warp-level bf16 MMAs; "
                     "~4.5 GB of DRAM traffic per call (ncu at B = 4, per-chunk S_c, dS_c, E_c, dE_c, W, U, A, T records) "
                     "against the algorithmic bytes"}
 
