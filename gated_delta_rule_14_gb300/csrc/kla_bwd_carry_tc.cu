@@ -49,26 +49,6 @@ static_assert(ST_G + 4 * kD <= kStage && kSmemBytes <= 232448, "carry shared mem
 // TMEM columns: D1 | D1b | D2 | D2b
 constexpr uint32_t TM_D1 = 0, TM_D1B = 64, TM_D2 = 128, TM_D2B = 256;
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint32_t bar, int x, int y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], "
-        "[%2];" ::"r"(dst),
-        "l"(tmap), "r"(bar), "r"(x), "r"(y)
-        : "memory");
-}
-__device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int x, int y) {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tmap),
-                 "r"(src), "r"(x), "r"(y)
-                 : "memory");
-}
-// A contiguous run of bytes into shared memory (16-byte aligned, a multiple of 16), counted on `bar`.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-__device__ __forceinline__ unsigned short bf16_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
-__device__ __forceinline__ float bf16_val(unsigned short bits) { return __uint_as_float(static_cast<uint32_t>(bits) << 16); }
 // Waits for phase `parity` of `bar` by polling (the waits of a step are short; this form also keeps
 // the forward per-channel carry within its registers). Gives up after 2^31 clock cycles (about a
 // second).

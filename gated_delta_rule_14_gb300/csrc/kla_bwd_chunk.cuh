@@ -9,6 +9,7 @@
 #include <cuda.h>
 
 #include "kla_internal.cuh"
+#include "sm103_ptx.cuh"
 #include "warp_mma.cuh"
 
 namespace kla {
@@ -26,6 +27,30 @@ constexpr int kTileSq = kC * kPs * 2;   // 64 x 64: 9216
 constexpr float kMinLogGate = -80.0f;
 
 typedef __nv_bfloat16 bf16;
+
+// ---- bulk copies of the tensor-core kernels (addresses 16-byte aligned; box columns a multiple of 8)
+// A 2-D box of a tensor map into shared memory, counted on `bar`; a box out of shared memory in
+// the thread's bulk group; a contiguous run of bytes (a multiple of 16) into shared memory.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint32_t bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], "
+        "[%2];" ::"r"(dst),
+        "l"(tmap), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tmap),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+// A bf16 value as its 16 bits (round to nearest even) and back.
+__device__ __forceinline__ unsigned short bf16_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
+__device__ __forceinline__ float bf16_val(unsigned short bits) { return __uint_as_float(static_cast<uint32_t>(bits) << 16); }
 
 // ---- per-chunk workspace records (structure of arrays over n = chain * nc + chunk)
 constexpr size_t kCgFloats = 3 * kC;    // G (scalar gate only), beta, den = ||k||^2 + eps

@@ -100,12 +100,6 @@ constexpr uint32_t TM_P = 0, TM_W = 0, TM_U = 64, kTmemCols = 128;   // W^T over
 constexpr uint32_t kWaitLimit = 100000;                                // x 20 us: ~2 s
 }  // namespace pc
 
-__device__ __forceinline__ unsigned short bf16_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
-__device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int x, int y) {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tmap),
-                 "r"(src), "r"(x), "r"(y)
-                 : "memory");
-}
 
 __global__ void __launch_bounds__(pc::kThreads, 2)
 bwd_prep_ch_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,

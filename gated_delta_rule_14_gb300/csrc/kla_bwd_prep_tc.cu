@@ -39,12 +39,6 @@ static_assert(OFF_R % 16 == 0 && OFF_X % 16 == 0 && kSmemBytes <= 232448 / 3, "t
 constexpr uint32_t TM_A = 0, TM_W = 0, TM_U = 64, kTmemCols = 128;
 constexpr uint32_t kWaitLimit = 100000;               // x 20 us: a stuck wait gives up after ~2 s
 
-__device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int x, int y) {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tmap),
-                 "r"(src), "r"(x), "r"(y)
-                 : "memory");
-}
-__device__ __forceinline__ unsigned short bf16_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
 
 struct PrepTcParams {
     const float *alpha, *eta;
